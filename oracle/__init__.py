@@ -1,0 +1,157 @@
+"""fp64 CPU oracle for the KDA forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  The product (the CUDA library and its Python binding)
+never imports, links or executes anything under ``oracle/``; the two share no
+code.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, double precision); this
+module only compiles it with gcc and marshals numpy arrays into it.
+
+Forms
+-----
+``recurrent``: the token recurrence that defines the method
+    S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+    o_t = scale * S_t^T q_t
+    (the recurrence that ``naive_chunk_kda`` evaluates; page "手撕KDA",
+    section "1 Naive").
+``chunked``: the chunked WY/UT evaluation in the order of that listing, for
+    any chunk size.
+
+Parity status: pinned by the ``-m "not gpu"`` tests in tests/test_oracle_pins.py
+(brute-force Kronecker transition, closed forms, textbook delta rule,
+hand-computed scalar fixture, invariants).  The pages print no numeric example
+for KDA, so no pin is a printed value from the pages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile kda_oracle.c into oracle/_build/libkda_oracle.so with gcc."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.kda_oracle_run.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                P, P, P, P, P, ctypes.c_double,
+                ctypes.c_int, P, P, P, P, P, P, P, P, ctypes.c_int]
+            lib.kda_oracle_run.restype = ctypes.c_int
+            lib.kda_oracle_tri_inverse.argtypes = [ctypes.c_int, P, P]
+            lib.kda_oracle_tri_inverse.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def tri_inverse(M: np.ndarray) -> np.ndarray:
+    """(I + M)^{-1} for strictly lower-triangular M, by the oracle's forward substitution."""
+    M = np.ascontiguousarray(M, dtype=np.float64)
+    n = M.shape[0]
+    out = np.zeros((n, n), dtype=np.float64)
+    _load().kda_oracle_tri_inverse(n, _ptr(M), _ptr(out))
+    return out
+
+
+def _seq_bounds(B, T, cu_seqlens):
+    if cu_seqlens is None:
+        return [(b * T, T) for b in range(B)]
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return [(int(cu[i]), int(cu[i + 1] - cu[i])) for i in range(len(cu) - 1)]
+
+
+def forward_units(q, k, v, g, beta, scale, units, initial_state=None, cu_seqlens=None,
+                  form: str = "chunked", chunk: int = 64, nthreads: int | None = None):
+    """Run the oracle on selected (sequence, value-head) units.
+
+    q, k: [B, T, H, K]; v: [B, T, HV, V]; g: [B, T, HV, K]; beta: [B, T, HV]
+    (float32 values; bf16 inputs are passed widened, which is exact).  With
+    cu_seqlens ([N+1]) B must be 1 and sequences are packed along T.
+    initial_state: [NS, HV, K, V] or None (zeros).
+    Returns a list of (o [len, V] float64, S_final [K, V] float64), one per unit.
+    """
+    q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    seqs = _seq_bounds(B, T, cu_seqlens)
+    n = len(units)
+    tok0 = np.array([seqs[s][0] for s, _ in units], dtype=np.int64)
+    lens = np.array([seqs[s][1] for s, _ in units], dtype=np.int32)
+    hvs = np.array([h for _, h in units], dtype=np.int32)
+    o_off = np.zeros(n, dtype=np.int64)
+    if n:
+        o_off[1:] = np.cumsum(lens.astype(np.int64) * V)[:-1]
+    o_out = np.zeros(int(lens.astype(np.int64).sum()) * V, dtype=np.float64)
+    s_out = np.zeros((n, K, V), dtype=np.float64)
+    s0 = None
+    s0_off = None
+    if initial_state is not None:
+        s0 = _f32(initial_state)
+        s0_off = np.array([(s * HV + h) * K * V for s, h in units], dtype=np.int64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _load().kda_oracle_run(
+        0 if form == "recurrent" else 1, int(chunk), H, HV, K, V,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        n, _ptr(tok0), _ptr(lens), _ptr(hvs), _ptr(s0), _ptr(s0_off),
+        _ptr(o_out), _ptr(o_off), _ptr(s_out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    res = []
+    for i in range(n):
+        L = int(lens[i])
+        res.append((o_out[o_off[i]:o_off[i] + L * V].reshape(L, V), s_out[i]))
+    return res
+
+
+def forward(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
+            form: str = "chunked", chunk: int = 64, nthreads: int | None = None):
+    """Run the oracle on every unit.  Returns (o [B,T,HV,V] f64, S [NS,HV,K,V] f64)."""
+    B, T = np.shape(q)[0], np.shape(q)[1]
+    HV, V = np.shape(v)[2], np.shape(v)[3]
+    K = np.shape(q)[3]
+    seqs = _seq_bounds(B, T, cu_seqlens)
+    units = [(s, h) for s in range(len(seqs)) for h in range(HV)]
+    res = forward_units(q, k, v, g, beta, scale, units, initial_state, cu_seqlens,
+                        form, chunk, nthreads)
+    o = np.zeros((B * T, HV, V), dtype=np.float64)
+    S = np.zeros((len(seqs), HV, K, V), dtype=np.float64)
+    for (s, h), (ou, su) in zip(units, res):
+        t0, L = seqs[s]
+        o[t0:t0 + L, h, :] = ou
+        S[s, h] = su
+    return o.reshape(B, T, HV, V), S

@@ -1,0 +1,222 @@
+"""Pins for the fp64 oracle, checked against things other than the oracle itself.
+
+The pages print no numeric example for KDA (their formula sections lost their
+images), so the pins are: a brute-force evaluation over the full (K*V)-dimensional
+state space, closed forms, the textbook delta rule, a hand-computed scalar
+fixture, and invariants the method must satisfy.  Each is chosen so that a
+plausible slip in the oracle (a dropped term, a wrong sign, beta on the wrong
+side, exp2 for exp, a transposed operand, a wrong GVA map) fails at least one.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_inputs(rng, B, T, H, HV, K, V, g_scale=0.125, s0=False, n_seq=None):
+    q = rng.standard_normal((B, T, H, K))
+    k = rng.standard_normal((B, T, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, HV, V))
+    g = -np.abs(rng.standard_normal((B, T, HV, K))) * g_scale * 4
+    beta = 1 / (1 + np.exp(-rng.standard_normal((B, T, HV))))
+    S0 = rng.standard_normal((n_seq or B, HV, K, V)) * 0.5 if s0 else None
+    f = lambda a: None if a is None else a.astype(np.float32)
+    return f(q), f(k), f(v), f(g), f(beta), f(S0)
+
+
+def brute_force(q, k, v, g, beta, scale, S0=None):
+    """Evaluate the recurrence as an affine map on vec(S) (row-major, K*V entries),
+    building each token's transition with Kronecker products:
+        vec(S_t) = kron((I - b k k^T) Diag(e^g), I_V) vec(S_{t-1}) + vec(b k v^T)
+        o_t      = scale * kron(q^T, I_V) vec(S_t)."""
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    G = HV // H
+    o = np.zeros((B, T, HV, V))
+    S = np.zeros((B, HV, K, V))
+    IV = np.eye(V)
+    for b in range(B):
+        for h in range(HV):
+            s = np.zeros(K * V) if S0 is None else S0[b, h].astype(np.float64).reshape(-1)
+            for t in range(T):
+                kt = k[b, t, h // G].astype(np.float64)
+                qt = q[b, t, h // G].astype(np.float64)
+                bt = float(beta[b, t, h])
+                left = (np.eye(K) - bt * np.outer(kt, kt)) @ np.diag(np.exp(g[b, t, h].astype(np.float64)))
+                s = np.kron(left, IV) @ s + np.outer(bt * kt, v[b, t, h].astype(np.float64)).reshape(-1)
+                o[b, t, h] = scale * (np.kron(qt[None, :], IV) @ s)
+            S[b, h] = s.reshape(K, V)
+    return o, S
+
+
+@pytest.mark.parametrize("form,chunk", [("recurrent", 1), ("chunked", 1), ("chunked", 3),
+                                        ("chunked", 4), ("chunked", 64)])
+def test_brute_force_kronecker(form, chunk):
+    rng = np.random.default_rng(11)
+    B, T, H, HV, K, V = 2, 9, 1, 2, 3, 2
+    q, k, v, g, beta, S0 = rand_inputs(rng, B, T, H, HV, K, V, s0=True)
+    scale = 0.7
+    o_ref, S_ref = brute_force(q, k, v, g, beta, scale, S0)
+    o, S = oracle.forward(q, k, v, g, beta, scale, initial_state=S0, form=form, chunk=chunk)
+    assert np.abs(o - o_ref).max() <= 1e-12 * max(1.0, np.abs(o_ref).max())
+    assert np.abs(S - S_ref).max() <= 1e-12 * max(1.0, np.abs(S_ref).max())
+
+
+@pytest.mark.parametrize("T", [1, 17, 64, 130])
+def test_chunk_size_independence(T):
+    rng = np.random.default_rng(T)
+    B, H, HV, K, V = 1, 2, 2, 8, 5
+    q, k, v, g, beta, S0 = rand_inputs(rng, B, T, H, HV, K, V, s0=True)
+    o_r, S_r = oracle.forward(q, k, v, g, beta, 0.5, S0, form="recurrent")
+    for C in (1, 2, 3, 16, 64):
+        o_c, S_c = oracle.forward(q, k, v, g, beta, 0.5, S0, form="chunked", chunk=C)
+        assert np.abs(o_c - o_r).max() <= 1e-12 * np.abs(o_r).max()
+        assert np.abs(S_c - S_r).max() <= 1e-12 * np.abs(S_r).max()
+
+
+def test_tri_inverse_identity_and_neumann():
+    rng = np.random.default_rng(3)
+    for n in (1, 5, 16, 64):
+        M = np.tril(rng.standard_normal((n, n)) * 0.3, -1)
+        T = oracle.tri_inverse(M)
+        assert np.abs((np.eye(n) + M) @ T - np.eye(n)).max() <= 1e-12
+        assert np.allclose(T, np.tril(T))
+        assert np.allclose(np.diag(T), 1.0)
+    # 16 x 16: the inverse equals the finite Neumann product (M is nilpotent, M^16 = 0):
+    # (I + M)^{-1} = (I - M)(I + M^2)(I + M^4)(I + M^8)
+    M = np.tril(rng.standard_normal((16, 16)) * 0.3, -1)
+    I = np.eye(16)
+    M2 = M @ M
+    M4 = M2 @ M2
+    M8 = M4 @ M4
+    neumann = (I - M) @ (I + M2) @ (I + M4) @ (I + M8)
+    T = oracle.tri_inverse(M)
+    assert np.abs(T - neumann).max() <= 1e-12 * np.abs(neumann).max()
+
+
+@pytest.mark.parametrize("form", ["recurrent", "chunked"])
+def test_beta_zero_is_pure_decay(form):
+    rng = np.random.default_rng(5)
+    B, T, H, HV, K, V = 1, 70, 1, 1, 6, 4
+    q, k, v, g, beta, S0 = rand_inputs(rng, B, T, H, HV, K, V, s0=True)
+    beta[:] = 0
+    o, S = oracle.forward(q, k, v, g, beta, 0.3, S0, form=form, chunk=16)
+    G = np.cumsum(g[0, :, 0].astype(np.float64), axis=0)          # [T, K]
+    St = np.exp(G)[:, :, None] * S0[0, 0][None].astype(np.float64)  # [T, K, V]
+    o_ref = 0.3 * np.einsum("tk,tkv->tv", q[0, :, 0].astype(np.float64), St)
+    assert np.abs(o[0, :, 0] - o_ref).max() <= 1e-12 * np.abs(o_ref).max()
+    assert np.abs(S[0, 0] - St[-1]).max() <= 1e-12 * np.abs(St[-1]).max()
+
+
+@pytest.mark.parametrize("form", ["recurrent", "chunked"])
+def test_delta_rule_exact_retrieval(form):
+    """g = 0, beta = 1, unit-norm keys: the plain delta rule writes v_t exactly
+    under k_t, so reading with q_t = k_t returns v_t (o_t = S_t^T k_t)."""
+    rng = np.random.default_rng(6)
+    B, T, H, HV, K, V = 1, 40, 1, 1, 8, 5
+    q, k, v, g, beta, S0 = rand_inputs(rng, B, T, H, HV, K, V, s0=True)
+    # keys with exactly unit norm in binary floating point: +-1/2 on four of the
+    # eight coordinates
+    k[:] = 0
+    for t in range(T):
+        idx = rng.choice(K, size=4, replace=False)
+        k[0, t, 0, idx] = rng.choice([-0.5, 0.5], size=4)
+    g[:] = 0
+    beta[:] = 1
+    o, _ = oracle.forward(k, k, v, g, beta, 1.0, S0, form=form, chunk=7)
+    assert np.abs(o - v.astype(np.float64)).max() <= 1e-10
+
+
+def test_delta_rule_matches_textbook_update():
+    """g = 0: each step is the textbook delta-rule update S += beta k (v - S^T k)^T."""
+    rng = np.random.default_rng(7)
+    T, K, V = 25, 6, 3
+    q, k, v, g, beta, _ = rand_inputs(rng, 1, T, 1, 1, K, V)
+    g[:] = 0
+    o, S = oracle.forward(q, k, v, g, beta, 1.0, None, form="chunked", chunk=8)
+    Sr = np.zeros((K, V))
+    for t in range(T):
+        kt, vt, qt = (x[0, t, 0].astype(np.float64) for x in (k, v, q))
+        pred = Sr.T @ kt
+        Sr = Sr + float(beta[0, t, 0]) * np.outer(kt, vt - pred)
+        assert np.allclose(o[0, t, 0], Sr.T @ qt, rtol=0, atol=1e-12)
+    assert np.allclose(S[0, 0], Sr, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("form", ["recurrent", "chunked"])
+def test_scalar_golden_fixture(form):
+    rows = np.loadtxt(os.path.join(GOLDEN, "scalar_k1v1.txt"), comments="#")
+    T = rows.shape[0]
+    q = rows[:, 0].reshape(1, T, 1, 1).astype(np.float32)
+    k = rows[:, 1].reshape(1, T, 1, 1).astype(np.float32)
+    v = rows[:, 2].reshape(1, T, 1, 1).astype(np.float32)
+    g = np.log(rows[:, 3]).reshape(1, T, 1, 1).astype(np.float32)
+    beta = rows[:, 4].reshape(1, T, 1).astype(np.float32)
+    o, S = oracle.forward(q, k, v, g, beta, 1.0, None, form=form, chunk=3)
+    np.testing.assert_allclose(o[0, :, 0, 0], rows[:, 6], rtol=1e-7, atol=1e-7)
+    np.testing.assert_allclose(S[0, 0, 0, 0], rows[-1, 5], rtol=1e-7, atol=1e-7)
+
+
+@pytest.mark.parametrize("form", ["recurrent", "chunked"])
+def test_split_sequence_continuity(form):
+    rng = np.random.default_rng(8)
+    B, T, H, HV, K, V = 1, 100, 1, 2, 8, 6
+    q, k, v, g, beta, S0 = rand_inputs(rng, B, T, H, HV, K, V, s0=True)
+    o, S = oracle.forward(q, k, v, g, beta, 0.4, S0, form=form, chunk=16)
+    m = 37
+    sl = lambda a, a0, a1: a[:, a0:a1]
+    o1, S1 = oracle.forward(*(sl(a, 0, m) for a in (q, k, v, g, beta)), 0.4, S0, form=form, chunk=16)
+    o2, S2 = oracle.forward(*(sl(a, m, T) for a in (q, k, v, g, beta)), 0.4, S1.astype(np.float32),
+                            form=form, chunk=16)
+    # the carried state is rounded to fp32 when passed back in; compare loosely
+    assert np.abs(np.concatenate([o1, o2], axis=1) - o).max() <= 1e-6 * np.abs(o).max()
+    assert np.abs(S2 - S).max() <= 1e-6 * np.abs(S).max()
+
+
+def test_gva_equals_repeated_heads():
+    rng = np.random.default_rng(9)
+    B, T, H, HV, K, V = 1, 33, 2, 8, 4, 3
+    q, k, v, g, beta, S0 = rand_inputs(rng, B, T, H, HV, K, V, s0=True)
+    o, S = oracle.forward(q, k, v, g, beta, 0.5, S0, form="chunked", chunk=8)
+    G = HV // H
+    qr, kr = np.repeat(q, G, axis=2), np.repeat(k, G, axis=2)   # key head hv // G
+    o2, S2 = oracle.forward(qr, kr, v, g, beta, 0.5, S0, form="recurrent")
+    assert np.abs(o - o2).max() <= 1e-12 * np.abs(o).max()
+    assert np.abs(S - S2).max() <= 1e-12 * np.abs(S).max()
+
+
+def test_varlen_equals_separate_calls_and_empty_sequence():
+    rng = np.random.default_rng(10)
+    lens = [5, 0, 19, 1, 40]
+    T = sum(lens)
+    H, HV, K, V = 1, 2, 4, 3
+    q, k, v, g, beta, S0 = rand_inputs(rng, 1, T, H, HV, K, V, s0=True, n_seq=len(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    o, S = oracle.forward(q, k, v, g, beta, 0.5, S0, cu_seqlens=cu, form="chunked", chunk=16)
+    for i, L in enumerate(lens):
+        a0, a1 = cu[i], cu[i + 1]
+        if L == 0:
+            assert np.array_equal(S[i], S0[i].astype(np.float64))
+            continue
+        oi, Si = oracle.forward(*(x[:, a0:a1] for x in (q, k, v, g, beta)), 0.5, S0[i:i + 1],
+                                form="recurrent")
+        assert np.abs(o[:, a0:a1] - oi).max() <= 1e-12 * np.abs(oi).max()
+        assert np.abs(S[i] - Si[0]).max() <= 1e-12 * np.abs(Si).max()
+
+
+def test_zero_padded_row_is_identity():
+    """A row with k = 0 and g = 0 leaves the state unchanged (the reading used
+    for rows past the end of a partial chunk)."""
+    rng = np.random.default_rng(12)
+    T, K, V = 10, 4, 3
+    q, k, v, g, beta, S0 = rand_inputs(rng, 1, T, 1, 1, K, V, s0=True)
+    _, S = oracle.forward(q, k, v, g, beta, 0.5, S0, form="recurrent")
+    pad = lambda a, val: np.concatenate([a, np.full_like(a[:, :3], val)], axis=1)
+    _, S2 = oracle.forward(pad(q, 1.0), pad(k, 0.0), pad(v, 1.0), pad(g, 0.0), pad(beta, 0.5),
+                           0.5, S0, form="chunked", chunk=4)
+    assert np.abs(S - S2).max() <= 1e-12 * np.abs(S).max()
