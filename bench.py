@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA chunked forward on one GB300 (or N, as independent replicas).
+
+One step = one kda_chunk_fwd call over the headline workload (B=1, T=4096,
+H=HV=32, K=V=128, bf16 q/k/v/o, fp32 g/beta/state), inputs resident in HBM.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method here) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA chunked fwd tokens/s & TFLOP/s on 1 GB300 (T=4096,H=32,K=V=128); % roofline"
+WORKLOAD_INDEX = 1
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+# the kernel kda_chunk_fwd runs for the headline workload (one launch per step)
+DOMINANT_KERNEL = "recurrent_fwd_kernel"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["kimi_delta_attention_gb300/csrc/kda_chunk_tc.cu",
+                  "kimi_delta_attention_gb300/csrc/kda_recurrent.cu",
+                  "kimi_delta_attention_gb300/csrc/sm103.cuh",
+                  "kimi_delta_attention_gb300/csrc/kda_common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """Reads SM clocks and clock-event (throttle) reasons during the timed region
+    through NVML (read-only queries), falling back to nvidia-smi."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._handle = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) == 0:
+                    self._nvml, self._handle = nv, h
+                    mx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = mx.value
+        except OSError:
+            pass
+
+    def _sample(self):
+        nv, h = self._nvml, self._handle
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) != 0:
+            return
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        reasons = rs.value if fn(h, ctypes.byref(rs)) == 0 else 0
+        self.samples.append((clk.value, reasons))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(0.002)
+
+    def start(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._nvml is not None:
+            self._t.join()
+            if not self.samples:
+                self._sample()
+
+    def summary(self):
+        if self._nvml is None:
+            return self._smi_summary()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = [s for s, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle")
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml"}
+
+    def _smi_summary(self):
+        import subprocess
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                                  "clocks_event_reasons.active", "--format=csv,noheader,nounits"],
+                                 capture_output=True, text=True, timeout=20).stdout.strip()
+            sm, mx, act = [s.strip() for s in out.split(",")]
+            bits = int(act, 16)
+            reasons = sorted(n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle")
+            return {"sm_mhz": float(sm), "sm_max_mhz": float(mx), "reasons": reasons, "samples": 1,
+                    "source": "nvidia-smi after the timed region"}
+        except Exception as e:  # noqa: BLE001
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": str(e)}
+
+
+# ------------------------------------------------------------------ helpers --
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def load_traffic(kernel_name: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel_name)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(x=None, units: int | None = None):
+    """Time the fp64 oracle (chunked form, C = 64) on a bounded sample of the
+    headline workload: `units` value heads of the single sequence, one thread
+    per head.  Returns (tokens/s scaled to all heads, cores, sample text, s)."""
+    import oracle
+    from kimi_delta_attention_gb300 import workloads as W
+    if x is None:
+        x = W.workload_inputs(WORKLOAD_INDEX)
+    cores = os.cpu_count() or 1
+    if units is None:
+        units = min(cores, x.v.shape[2])
+    f = lambda t: t.float().numpy()
+    args = [f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta)]
+    sel = [(0, h) for h in range(units)]
+    t0 = time.perf_counter()
+    oracle.forward_units(*args, x.scale, sel, form="chunked", chunk=64, nthreads=units)
+    dt = time.perf_counter() - t0
+    HV = x.v.shape[2]
+    tokens_equiv = x.tokens() * units / HV
+    sample = (f"{units} of {HV} value heads x {x.tokens()} tokens of the headline workload, "
+              f"fp64 chunked oracle (C=64), {units} threads; {dt:.2f} s wall; "
+              f"tokens/s counts a token as all {HV} heads")
+    return tokens_equiv / dt, units, sample, dt
+
+
+# --------------------------------------------------------------------- arms --
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from kimi_delta_attention_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    x = W.workload_inputs(WORKLOAD_INDEX)
+    vals, times = [], []
+    cores = None
+    sample = None
+    n_steps = max(1, args.steps)
+    for i in range(max(0, args.warmup) + n_steps):
+        v, cores, sample, dt = cpu_baseline(x=x)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": n_steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w, n):
+    return {"workload": w.name, "model": None, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
+            "V": w.V, "global_batch": w.B * n, "seq_len": w.T, "chunk": 64,
+            "parallelism": f"replicas x{n} (independent problems per GPU)",
+            "l2": "flushed between timed steps (256 MiB device write outside the step events)",
+            "initial_state": "zeros (not read)", "final_state": "written"}
+
+
+def run_gpu(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import kimi_delta_attention_gb300 as kda
+    from kimi_delta_attention_gb300 import workloads as W
+    kda.build()
+    kda.load_library()
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    host = W.workload_inputs(WORKLOAD_INDEX)
+    x = host.to(dev)
+    B, T, H, K = x.q.shape
+    HV, V = x.v.shape[2], x.v.shape[3]
+    out = torch.empty_like(x.v)
+    fin = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
+    shape = kda.make_shape(x.q, x.v)
+    wsp = torch.empty(kda.kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, x.scale, out=out, final_state=fin, workspace=wsp,
+                          stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if kda.kda_read_device_status(wsp) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if ws > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = kda.kda_read_device_status(wsp)
+
+    tokens = B * T
+    value = ws * tokens / (ms * 1e-3)
+    flops = W.flops_convention(host)
+    tflops = ws * flops / (ms * 1e-3) / 1e12
+    alg_bytes = W.algorithmic_bytes(host, final_state=True) - 0  # initial state not read
+    hbm_gbs, bf16_tf, peak_src = load_peaks()
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    kernel_name = DOMINANT_KERNEL
+
+    # end to end through the public API with pinned host buffers
+    e2e = e2e_measure(kda, host, dev, stream, max(3, min(args.steps, 20)))
+
+    line = {
+        "impl": "kda_gb300", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w, ws), "tflops": tflops,
+        "roofline_time_ms": max(alg_bytes / (hbm_gbs * 1e9), flops / (bf16_tf * 1e12)) * 1e3,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": load_traffic(kernel_name),
+                     "kernel": kernel_name, "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s"},
+        "clocks": sampler.summary(), "e2e": e2e, "gpu_launches": args.steps * 1,
+        "device_status": status, "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = cpu_baseline(x=host)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_measure(kda, host, dev, stream, steps):
+    """Same metric through kda_chunk_fwd with host buffers: every step copies the
+    inputs from pinned host memory to the device, runs the forward and copies o
+    and the final state back."""
+    import torch
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv, hg, hb = (pin(t) for t in (host.q, host.k, host.v, host.g, host.beta))
+    dq, dk, dv, dg, db = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, hg, hb))
+    ho = torch.empty(host.v.shape, dtype=host.v.dtype).pin_memory()
+    B, T, H, K = host.q.shape
+    HV, V = host.v.shape[2], host.v.shape[3]
+    hs = torch.empty((B, HV, K, V), dtype=torch.float32).pin_memory()
+    do = torch.empty_like(dv)
+    ds = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+    d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
+
+    def step():
+        for d, h in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb)):
+            d.copy_(h, non_blocking=True)
+        kda.kda_chunk_fwd(dq, dk, dv, dg, db, host.scale, out=do, final_state=ds, stream=stream.cuda_stream)
+        ho.copy_(do, non_blocking=True)
+        hs.copy_(ds, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": B * T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kda_gb300", choices=["kda_gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,132 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * Operation (per sequence and value head hv, independently):
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ * q_t and k_t come from key head hv / (HV / H) (grouped value heads).  This is
+ * the recurrence that the chunked listing `naive_chunk_kda` evaluates (page
+ * "手撕KDA", section "1 Naive": argument list, shapes, GVA expansion by
+ * repeat_interleave, chunk loop).  g is a natural-log decay (<= 0 in practice),
+ * beta is used as given (no sigmoid), q and k are used as given (no L2
+ * normalisation): those pre-stages are not part of this operation.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
+ *    16-byte aligned (beta and cu_seqlens: 4-byte aligned).  The caller allocates and owns every buffer; the library
+ *    never allocates or frees device memory and never synchronises the device.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and runs asynchronously.
+ *  - Arguments are validated on the host before anything is enqueued; on any
+ *    error nothing is launched and nothing is written.
+ *  - cu_seqlens is not read on the host (that would need a device sync); each
+ *    block checks the bounds of its own sequence on the device and reports a
+ *    violation through the device status word in the workspace.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_F32 = 0,   /* fp32 q, k, v, o */
+  KDA_BF16 = 1   /* bf16 q, k, v, o */
+} kda_dtype;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,     /* bad shape, null required pointer, HV % H != 0, ... */
+  KDA_ERR_UNSUPPORTED = 2,     /* valid but not compiled: K or V outside {64, 128} */
+  KDA_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned */
+  KDA_ERR_CUDA = 4,            /* a CUDA runtime call failed (launch, attribute, ...) */
+  KDA_ERR_DEVICE_TIMEOUT = 5,  /* device status: a bounded on-chip wait gave up */
+  KDA_ERR_WORKSPACE = 6,       /* workspace missing or smaller than required */
+  KDA_ERR_DEVICE_BOUNDS = 7    /* device status: cu_seqlens out of order or out of range */
+} kda_status;
+
+typedef struct {
+  int B;          /* batch (must be 1 when cu_seqlens is given)                  */
+  int T;          /* tokens per sequence, or packed total with cu_seqlens         */
+  int H;          /* key heads (q, k)                                              */
+  int HV;         /* value heads (v, g, beta, state); HV % H == 0                 */
+  int K;          /* key dim; 64 or 128                                            */
+  int V;          /* value dim; 64 or 128                                          */
+  int num_seqs;   /* N when cu_seqlens is given, else 0                            */
+  kda_dtype io_dtype;  /* dtype of q, k, v and out; g, beta and states are fp32 */
+} kda_shape;
+
+/*
+ * Chunked forward (the hot path).  Page "手撕KDA", section "1 Naive"
+ * (naive_chunk_kda) defines the operation; the chunked evaluation (within-chunk
+ * cumsum of g, decayed keys and queries, strictly lower-triangular L, inverse of
+ * (I + L), W/U, serial state carry, intra-chunk output) follows that listing.
+ *
+ *   q, k          [B, T, H, K]   io_dtype
+ *   v             [B, T, HV, V]  io_dtype
+ *   g             [B, T, HV, K]  fp32, log-space decay
+ *   beta          [B, T, HV]     fp32
+ *   scale         > 0 and finite (the listing's default is K^-0.5; pass it)
+ *   initial_state [NS, HV, K, V] fp32 or NULL (zeros); NS = B, or num_seqs
+ *   cu_seqlens    [num_seqs + 1] int32 or NULL; cu[0] = 0, non-decreasing,
+ *                 cu[num_seqs] = T; sequences are packed along T
+ *   out           [B, T, HV, V]  io_dtype; must not alias an input
+ *   final_state   [NS, HV, K, V] fp32 or NULL (not written); may alias
+ *                 initial_state (each state slice is read before it is written)
+ *   workspace     device scratch of at least kda_chunk_fwd_workspace_size()
+ *                 bytes (holds the device status word); owned by the caller;
+ *                 calls that share a workspace must be ordered on one stream
+ * Returns KDA_OK when the work was enqueued.  T = 0 (or all sequences empty)
+ * copies initial_state (or zeros) to final_state.
+ * bf16 with K = V = 128 runs the tensor-core chunk kernel; fp32 I/O and other
+ * supported sizes run the token-recurrent CUDA-core kernel (same operation).
+ */
+KDA_API kda_status kda_chunk_fwd(const kda_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, float scale,
+                         const float* initial_state, const int32_t* cu_seqlens, void* out,
+                         float* final_state, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * Token-recurrent forward: the defining recurrence evaluated token by token on
+ * CUDA cores in fp32 (same arguments and results as kda_chunk_fwd).  Kept as
+ * the exact-precision path and as a cross-check for the chunked kernel.
+ */
+KDA_API kda_status kda_recurrent_fwd(const kda_shape* shape, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, float scale,
+                             const float* initial_state, const int32_t* cu_seqlens, void* out,
+                             float* final_state, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Bytes of device workspace the forward entry points need for `shape` (>= 256). */
+KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape* shape);
+
+/*
+ * Read the device status word a previous call left in `workspace`: enqueues a
+ * 4-byte device-to-host copy on `stream` and waits for that stream.  Returns
+ * KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_BOUNDS (diagnostics only;
+ * not for the hot loop).
+ */
+KDA_API kda_status kda_read_device_status(const void* workspace, void* stream);
+
+/* Static string for a status code. */
+KDA_API const char* kda_status_string(kda_status status);
+
+/* Chunk size used by the tensor-core kernel (tokens per chunk). */
+KDA_API int kda_chunk_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

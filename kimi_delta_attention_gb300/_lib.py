@@ -1,0 +1,157 @@
+"""ctypes binding of the C ABI in include/kda.h (argument marshalling only).
+
+Every step of the forward runs in the CUDA library libkda.so; this module only
+turns torch tensors into device pointers and sizes, allocates outputs with
+torch when the caller did not pass them, and raises on a non-OK status.  There
+is no fallback: if the library is missing the call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import builder as _build
+
+_lock = threading.Lock()
+_lib = None
+
+KDA_F32 = 0
+KDA_BF16 = 1
+
+STATUS_NAMES = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIGNMENT",
+    4: "KDA_ERR_CUDA", 5: "KDA_ERR_DEVICE_TIMEOUT", 6: "KDA_ERR_WORKSPACE", 7: "KDA_ERR_DEVICE_BOUNDS",
+}
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
+           "kda_read_device_status", "kda_status_string", "kda_chunk_size")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class KdaShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("HV", ctypes.c_int),
+                ("K", ctypes.c_int), ("V", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("io_dtype", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libkda.so (built in-tree by kimi_delta_attention_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"KDA CUDA library not built ({p}); run kimi_delta_attention_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        fwd_args = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, P, P, S, P]
+        for name in ("kda_chunk_fwd", "kda_recurrent_fwd"):
+            fn = getattr(lib, name)
+            fn.argtypes = fwd_args
+            fn.restype = I
+        lib.kda_chunk_fwd_workspace_size.argtypes = [ctypes.POINTER(KdaShape)]
+        lib.kda_chunk_fwd_workspace_size.restype = S
+        lib.kda_read_device_status.argtypes = [P, P]
+        lib.kda_read_device_status.restype = I
+        lib.kda_status_string.argtypes = [I]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_chunk_size.argtypes = []
+        lib.kda_chunk_size.restype = I
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def kda_status_string(code: int) -> str:
+    return load_library().kda_status_string(int(code)).decode()
+
+
+def _check(code: int):
+    if code != 0:
+        raise KdaError(code, kda_status_string(code))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def make_shape(q, v, cu_seqlens=None) -> KdaShape:
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    io = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}.get(q.dtype)
+    if io is None:
+        raise KdaError(1, f"unsupported io dtype {q.dtype}")
+    ns = 0 if cu_seqlens is None else int(cu_seqlens.numel()) - 1
+    return KdaShape(B, T, H, HV, K, V, ns, io)
+
+
+def kda_chunk_fwd_workspace_size(shape: KdaShape) -> int:
+    return int(load_library().kda_chunk_fwd_workspace_size(ctypes.byref(shape)))
+
+
+def kda_chunk_size() -> int:
+    return int(load_library().kda_chunk_size())
+
+
+def _forward(entry: str, q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+             out=None, final_state=None, output_final_state=True, workspace=None, stream=None):
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise KdaError(1, f"{name} must be a contiguous CUDA tensor")
+    shape = make_shape(q, v, cu_seqlens)
+    K = q.shape[3]
+    if scale is None:
+        scale = K ** -0.5
+    NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
+    HV, V = v.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((NS, HV, K, V), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    code = getattr(lib, entry)(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), ctypes.c_void_p(stream))
+    _check(code)
+    return out, final_state
+
+
+def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None, out=None,
+                  final_state=None, output_final_state=True, workspace=None, stream=None):
+    """Chunked KDA forward on the GPU.  Shapes: q, k [B,T,H,K]; v [B,T,HV,V];
+    g [B,T,HV,K] fp32; beta [B,T,HV] fp32; initial_state [NS,HV,K,V] fp32;
+    cu_seqlens [N+1] int32.  Returns (o [B,T,HV,V], final_state or None)."""
+    return _forward("kda_chunk_fwd", q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
+                    final_state, output_final_state, workspace, stream)
+
+
+def kda_recurrent_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None, out=None,
+                      final_state=None, output_final_state=True, workspace=None, stream=None):
+    """Token-recurrent KDA forward on the GPU (same arguments and results)."""
+    return _forward("kda_recurrent_fwd", q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
+                    final_state, output_final_state, workspace, stream)
+
+
+def kda_read_device_status(workspace, stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device).cuda_stream
+    return int(load_library().kda_read_device_status(_ptr(workspace), ctypes.c_void_p(stream)))

@@ -1,0 +1,153 @@
+// kda_abi.cu -- the C ABI declared in include/kda.h: host-side validation,
+// workspace sizing, status reporting and dispatch to the forward kernels.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_recurrent_fwd(const FwdParams& p, bool bf16, cudaStream_t stream);
+bool chunk_tc_supported(const FwdParams& p, bool bf16);
+cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
+}  // namespace kda
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+struct Checked {
+  kda::FwdParams p;
+  bool bf16;
+  size_t units;  // sequences * value heads
+};
+
+kda_status validate(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,
+                    const float* beta, float scale, const float* s0, const int32_t* cu, void* out,
+                    float* sfin, void* ws, size_t ws_bytes, Checked& c) {
+  if (!s) return KDA_ERR_INVALID_ARG;
+  if (s->B < 0 || s->T < 0 || s->H < 1 || s->HV < 1 || s->K < 1 || s->V < 1) return KDA_ERR_INVALID_ARG;
+  if (s->HV % s->H != 0) return KDA_ERR_INVALID_ARG;
+  if (s->io_dtype != KDA_F32 && s->io_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+  if (cu) {
+    if (s->B != 1 || s->num_seqs < 1) return KDA_ERR_INVALID_ARG;
+  } else if (s->num_seqs != 0) {
+    return KDA_ERR_INVALID_ARG;
+  }
+  if ((s->K != 64 && s->K != 128) || (s->V != 64 && s->V != 128)) return KDA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < kda::kWorkspaceBytes) return KDA_ERR_WORKSPACE;
+
+  const size_t ns = cu ? static_cast<size_t>(s->num_seqs) : static_cast<size_t>(s->B);
+  const size_t tokens = cu ? static_cast<size_t>(s->T) : static_cast<size_t>(s->B) * s->T;
+  const size_t es = s->io_dtype == KDA_BF16 ? 2 : 4;
+  const size_t n_qk = tokens * s->H * s->K * es, n_v = tokens * s->HV * s->V * es;
+  const size_t n_g = tokens * s->HV * s->K * 4, n_b = tokens * s->HV * 4;
+  const size_t n_s = ns * s->HV * s->K * s->V * 4;
+  if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  // tensors read or written in 16-byte vectors / TMA tiles need 16-byte
+  // alignment; beta and cu_seqlens are read one element at a time
+  const void* ptrs16[] = {q, k, v, g, s0, out, sfin, ws};
+  for (const void* ptr : ptrs16)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  if ((beta && !aligned(beta, 4)) || (cu && !aligned(cu, 4))) return KDA_ERR_ALIGNMENT;
+  // out must not alias an input; final_state may alias initial_state only exactly
+  const void* ins[] = {q, k, v, g, beta, s0};
+  const size_t nins[] = {n_qk, n_qk, n_v, n_g, n_b, n_s};
+  for (int i = 0; i < 6; ++i) {
+    if (overlaps(out, n_v, ins[i], nins[i])) return KDA_ERR_INVALID_ARG;
+    if (i < 5 && overlaps(sfin, n_s, ins[i], nins[i])) return KDA_ERR_INVALID_ARG;
+  }
+  if (sfin && s0 && sfin != s0 && overlaps(sfin, n_s, s0, n_s)) return KDA_ERR_INVALID_ARG;
+  if (overlaps(sfin, n_s, out, n_v) || overlaps(ws, ws_bytes, out, n_v) || overlaps(ws, ws_bytes, sfin, n_s))
+    return KDA_ERR_INVALID_ARG;
+
+  kda::FwdParams& p = c.p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = s0; p.cu = cu;
+  p.out = out; p.sfin = sfin; p.status = static_cast<uint32_t*>(ws);
+  p.scale = scale; p.T = s->T; p.H = s->H; p.HV = s->HV; p.K = s->K; p.V = s->V;
+  p.num_seqs = static_cast<int>(ns);
+  c.bf16 = s->io_dtype == KDA_BF16;
+  c.units = ns * s->HV;
+  return KDA_OK;
+}
+
+kda_status run(bool use_tc, const kda_shape* s, const void* q, const void* k, const void* v,
+               const float* g, const float* beta, float scale, const float* s0, const int32_t* cu,
+               void* out, float* sfin, void* ws, size_t ws_bytes, void* stream) {
+  Checked c;
+  const kda_status st = validate(s, q, k, v, g, beta, scale, s0, cu, out, sfin, ws, ws_bytes, c);
+  if (st != KDA_OK) return st;
+  if (c.units == 0) return KDA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
+  cudaError_t e;
+  if (use_tc && kda::chunk_tc_supported(c.p, c.bf16))
+    e = kda::launch_chunk_tc_fwd(c.p, cs);
+  else
+    e = kda::launch_recurrent_fwd(c.p, c.bf16, cs);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_chunk_fwd(const kda_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, float scale, const float* initial_state,
+                         const int32_t* cu_seqlens, void* out, float* final_state, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return run(true, shape, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, workspace,
+             workspace_bytes, stream);
+}
+
+kda_status kda_recurrent_fwd(const kda_shape* shape, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, float scale, const float* initial_state,
+                             const int32_t* cu_seqlens, void* out, float* final_state, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return run(false, shape, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, workspace,
+             workspace_bytes, stream);
+}
+
+size_t kda_chunk_fwd_workspace_size(const kda_shape* shape) {
+  (void)shape;
+  return kda::kWorkspaceBytes;
+}
+
+kda_status kda_read_device_status(const void* workspace, void* stream) {
+  if (!workspace) return KDA_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return KDA_ERR_CUDA;
+  if (word & kda::kStatusTimeout) return KDA_ERR_DEVICE_TIMEOUT;
+  if (word & kda::kStatusBounds) return KDA_ERR_DEVICE_BOUNDS;
+  return KDA_OK;
+}
+
+const char* kda_status_string(kda_status status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape (K and V must be 64 or 128)";
+    case KDA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case KDA_ERR_CUDA: return "CUDA runtime error";
+    case KDA_ERR_DEVICE_TIMEOUT: return "device: a bounded on-chip wait timed out";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_DEVICE_BOUNDS: return "device: cu_seqlens out of order or out of range";
+  }
+  return "unknown status";
+}
+
+int kda_chunk_size(void) { return 64; }
+
+}  // extern "C"

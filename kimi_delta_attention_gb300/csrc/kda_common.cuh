@@ -1,0 +1,64 @@
+// kda_common.cuh -- launch parameters and small helpers shared by the KDA
+// forward kernels (CUDA library side only).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace kda {
+
+// Device status word bits (the first 32-bit word of the workspace).
+constexpr uint32_t kStatusTimeout = 1u;   // a bounded on-chip wait gave up
+constexpr uint32_t kStatusBounds = 2u;    // cu_seqlens entry out of order / range
+
+// Workspace layout: [0, 4) status word; the rest is reserved.
+constexpr size_t kWorkspaceBytes = 256;
+
+struct FwdParams {
+  const void* q;         // [tokens, H, K]   io type
+  const void* k;         // [tokens, H, K]   io type
+  const void* v;         // [tokens, HV, V]  io type
+  const float* g;        // [tokens, HV, K]
+  const float* beta;     // [tokens, HV]
+  const float* s0;       // [NS, HV, K, V] or null
+  const int32_t* cu;     // [NS + 1] or null
+  void* out;             // [tokens, HV, V]  io type
+  float* sfin;           // [NS, HV, K, V] or null
+  uint32_t* status;      // device status word
+  float scale;
+  int T;                 // tokens per sequence (fixed length) or packed total
+  int H, HV, K, V;
+  int num_seqs;          // NS
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Token range [tok0, tok0 + len) of sequence `seq`.  With cu_seqlens each block
+// checks the two entries it uses; a violation sets kStatusBounds and yields an
+// empty range (the block then writes nothing).
+__device__ __forceinline__ bool seq_range(const FwdParams& p, int seq, long& tok0, int& len) {
+  if (p.cu == nullptr) {
+    tok0 = static_cast<long>(seq) * p.T;
+    len = p.T;
+    return true;
+  }
+  const int a = p.cu[seq], b = p.cu[seq + 1];
+  if (a < 0 || b < a || b > p.T || (seq == 0 && a != 0) || (seq == p.num_seqs - 1 && b != p.T)) {
+    atomicOr(p.status, kStatusBounds);
+    tok0 = 0;
+    len = 0;
+    return false;
+  }
+  tok0 = a;
+  len = b - a;
+  return true;
+}
+
+}  // namespace kda

@@ -1,0 +1,95 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before touching the GPU.
+
+No compute call is made: every call here fails validation, which happens on
+the host before anything is enqueued, so fake (never dereferenced) device
+addresses are safe to pass.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kimi_delta_attention_gb300 as kda
+from kimi_delta_attention_gb300 import _lib
+from kimi_delta_attention_gb300.builder import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load_library()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)))
+
+
+def test_exports_match_header(lib):
+    declared = header_symbols()
+    assert declared == sorted(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = kda.kda_status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert kda.kda_status_string(99) == "unknown status"
+
+
+def test_workspace_size_and_chunk(lib):
+    shape = _lib.KdaShape(1, 4096, 32, 32, 128, 128, 0, _lib.KDA_BF16)
+    assert kda.kda_chunk_fwd_workspace_size(shape) >= 256
+    assert kda.kda_chunk_size() in (16, 32, 64, 128)
+
+
+FAKE = 0x10000  # aligned, never dereferenced
+
+
+def call(lib, shape, q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, g=FAKE + 0x300000,
+         beta=FAKE + 0x400000, scale=0.088, s0=None, cu=None, out=FAKE + 0x500000,
+         sfin=None, ws=FAKE + 0x600000, ws_bytes=256, entry="kda_chunk_fwd"):
+    P = ctypes.c_void_p
+    return getattr(lib, entry)(ctypes.byref(shape), P(q), P(k), P(v), P(g), P(beta), ctypes.c_float(scale),
+                               P(s0), P(cu), P(out), P(sfin), P(ws), ctypes.c_size_t(ws_bytes), P(0))
+
+
+def S(B=1, T=8, H=2, HV=2, K=64, V=64, ns=0, io=_lib.KDA_F32):
+    return _lib.KdaShape(B, T, H, HV, K, V, ns, io)
+
+
+@pytest.mark.parametrize("entry", ["kda_chunk_fwd", "kda_recurrent_fwd"])
+def test_host_validation_rejects(lib, entry):
+    c = lambda *a, **kw: call(lib, *a, entry=entry, **kw)
+    assert c(S(HV=3, H=2)) == 1                       # HV % H != 0
+    assert c(S(H=0)) == 1
+    assert c(S(T=-1)) == 1
+    assert c(S(K=96)) == 2                            # unsupported head dim
+    assert c(S(V=32)) == 2
+    assert c(S(io=5)) == 1                            # bad dtype
+    assert c(S(), scale=0.0) == 1
+    assert c(S(), scale=float("nan")) == 1
+    assert c(S(), q=None) == 1                        # null required pointer
+    assert c(S(), out=None) == 1
+    assert c(S(), q=FAKE + 8) == 3                    # misaligned
+    assert c(S(), g=FAKE + 0x300000 + 4) == 3
+    assert c(S(), beta=FAKE + 0x400000 + 2) == 3
+    assert c(S(), ws=None) == 6                       # workspace missing
+    assert c(S(), ws_bytes=16) == 6                   # workspace too small
+    assert c(S(B=2, ns=1), cu=FAKE + 0x700000) == 1   # varlen needs B == 1
+    assert c(S(ns=0), cu=FAKE + 0x700000) == 1        # varlen needs num_seqs >= 1
+    assert c(S(ns=2)) == 1                            # num_seqs without cu_seqlens
+    assert c(S(), out=FAKE) == 1                      # out aliases q
+    assert c(S(), sfin=FAKE + 0x300000) == 1          # final state aliases g
+    assert c(S(), s0=FAKE + 0x800000, sfin=FAKE + 0x800000 + 16) == 1  # partial overlap
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        _lib.load_library(str(tmp_path / "nope.so"))
