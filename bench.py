@@ -31,7 +31,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 # the kernel kda_chunk_fwd runs for the headline workload (one launch per step)
-DOMINANT_KERNEL = "recurrent_fwd_kernel"
+DOMINANT_KERNEL = "kda_chunk_fused_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["kimi_delta_attention_gb300/csrc/kda_chunk_tc.cu",
                   "kimi_delta_attention_gb300/csrc/kda_recurrent.cu",

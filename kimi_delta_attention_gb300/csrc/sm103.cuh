@@ -73,6 +73,20 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier that also ORs a per-thread predicate across the `count`
+// participating threads; every thread receives the same result.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.b32 pin, %3, 0;\n\t"
+      "bar.red.or.pred pout, %1, %2, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
 
 // ------------------------------------------------------------------ TMEM ----
 // Allocate `ncols` (power of two, >= 32) columns; executed by one full warp.
