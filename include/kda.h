@@ -84,8 +84,11 @@ typedef struct {
  *   final_state   [NS, HV, K, V] fp32 or NULL (not written); may alias
  *                 initial_state (each state slice is read before it is written)
  *   workspace     device scratch of at least kda_chunk_fwd_workspace_size()
- *                 bytes (holds the device status word); owned by the caller;
- *                 calls that share a workspace must be ordered on one stream
+ *                 bytes, owned by the caller: the device status word and, for
+ *                 the tensor-core kernel, a ring of per-chunk records for each
+ *                 (sequence, value head) (8 x 73 KiB each).  Nothing in it
+ *                 needs initialising.  Calls that share a workspace must be
+ *                 ordered on one stream.
  * Returns KDA_OK when the work was enqueued.  T = 0 (or all sequences empty)
  * copies initial_state (or zeros) to final_state.
  * bf16 with K = V = 128 runs the tensor-core chunk kernel; fp32 I/O and other
@@ -99,8 +102,9 @@ KDA_API kda_status kda_chunk_fwd(const kda_shape* shape, const void* q, const vo
 
 /*
  * Token-recurrent forward: the defining recurrence evaluated token by token on
- * CUDA cores in fp32 (same arguments and results as kda_chunk_fwd).  Kept as
- * the exact-precision path and as a cross-check for the chunked kernel.
+ * CUDA cores in fp32 (same arguments and results as kda_chunk_fwd; its
+ * workspace needs only the 256-byte status word).  Kept as the
+ * exact-precision path and as a cross-check for the chunked kernel.
  */
 KDA_API kda_status kda_recurrent_fwd(const kda_shape* shape, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, float scale,
@@ -108,7 +112,9 @@ KDA_API kda_status kda_recurrent_fwd(const kda_shape* shape, const void* q, cons
                              float* final_state, void* workspace, size_t workspace_bytes,
                              void* stream);
 
-/* Bytes of device workspace the forward entry points need for `shape` (>= 256). */
+/* Bytes of device workspace kda_chunk_fwd needs for `shape` (>= 256; also
+ * enough for kda_recurrent_fwd).  Depends on the number of sequences and value
+ * heads, not on T. */
 KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape* shape);
 
 /*

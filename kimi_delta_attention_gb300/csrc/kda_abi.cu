@@ -10,6 +10,7 @@
 namespace kda {
 cudaError_t launch_recurrent_fwd(const FwdParams& p, bool bf16, cudaStream_t stream);
 bool chunk_tc_supported(const FwdParams& p, bool bf16);
+size_t chunk_tc_ring_bytes(int num_seqs, int HV);
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
 }  // namespace kda
 
@@ -23,15 +24,26 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+// Workspace bytes an entry point needs: the status word, plus the record ring
+// when the tensor-core chunk kernel will run.
+size_t workspace_needed(const kda_shape* s, bool use_tc) {
+  if (!s) return kda::kWorkspaceBytes;
+  const bool tc = use_tc && s->io_dtype == KDA_BF16 && s->K == 128 && s->V == 128 && s->HV >= 1;
+  if (!tc) return kda::kWorkspaceBytes;
+  const int ns = s->num_seqs > 0 ? s->num_seqs : s->B;
+  if (ns <= 0) return kda::kWorkspaceBytes;
+  return kda::kRingOffset + kda::chunk_tc_ring_bytes(ns, s->HV);
+}
+
 struct Checked {
   kda::FwdParams p;
   bool bf16;
   size_t units;  // sequences * value heads
 };
 
-kda_status validate(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,
-                    const float* beta, float scale, const float* s0, const int32_t* cu, void* out,
-                    float* sfin, void* ws, size_t ws_bytes, Checked& c) {
+kda_status validate(bool use_tc, const kda_shape* s, const void* q, const void* k, const void* v,
+                    const float* g, const float* beta, float scale, const float* s0, const int32_t* cu,
+                    void* out, float* sfin, void* ws, size_t ws_bytes, Checked& c) {
   if (!s) return KDA_ERR_INVALID_ARG;
   if (s->B < 0 || s->T < 0 || s->H < 1 || s->HV < 1 || s->K < 1 || s->V < 1) return KDA_ERR_INVALID_ARG;
   if (s->HV % s->H != 0) return KDA_ERR_INVALID_ARG;
@@ -43,7 +55,7 @@ kda_status validate(const kda_shape* s, const void* q, const void* k, const void
     return KDA_ERR_INVALID_ARG;
   }
   if ((s->K != 64 && s->K != 128) || (s->V != 64 && s->V != 128)) return KDA_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < kda::kWorkspaceBytes) return KDA_ERR_WORKSPACE;
+  if (!ws || ws_bytes < workspace_needed(s, use_tc)) return KDA_ERR_WORKSPACE;
 
   const size_t ns = cu ? static_cast<size_t>(s->num_seqs) : static_cast<size_t>(s->B);
   const size_t tokens = cu ? static_cast<size_t>(s->T) : static_cast<size_t>(s->B) * s->T;
@@ -73,6 +85,7 @@ kda_status validate(const kda_shape* s, const void* q, const void* k, const void
   std::memset(&p, 0, sizeof(p));
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = s0; p.cu = cu;
   p.out = out; p.sfin = sfin; p.status = static_cast<uint32_t*>(ws);
+  p.ring = ws_bytes > kda::kRingOffset ? static_cast<uint8_t*>(ws) + kda::kRingOffset : nullptr;
   p.scale = scale; p.T = s->T; p.H = s->H; p.HV = s->HV; p.K = s->K; p.V = s->V;
   p.num_seqs = static_cast<int>(ns);
   c.bf16 = s->io_dtype == KDA_BF16;
@@ -84,13 +97,13 @@ kda_status run(bool use_tc, const kda_shape* s, const void* q, const void* k, co
                const float* g, const float* beta, float scale, const float* s0, const int32_t* cu,
                void* out, float* sfin, void* ws, size_t ws_bytes, void* stream) {
   Checked c;
-  const kda_status st = validate(s, q, k, v, g, beta, scale, s0, cu, out, sfin, ws, ws_bytes, c);
+  const kda_status st = validate(use_tc, s, q, k, v, g, beta, scale, s0, cu, out, sfin, ws, ws_bytes, c);
   if (st != KDA_OK) return st;
   if (c.units == 0) return KDA_OK;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
   cudaError_t e;
-  if (use_tc && kda::chunk_tc_supported(c.p, c.bf16))
+  if (use_tc && c.p.ring && kda::chunk_tc_supported(c.p, c.bf16))
     e = kda::launch_chunk_tc_fwd(c.p, cs);
   else
     e = kda::launch_recurrent_fwd(c.p, c.bf16, cs);
@@ -117,10 +130,7 @@ kda_status kda_recurrent_fwd(const kda_shape* shape, const void* q, const void* 
              workspace_bytes, stream);
 }
 
-size_t kda_chunk_fwd_workspace_size(const kda_shape* shape) {
-  (void)shape;
-  return kda::kWorkspaceBytes;
-}
+size_t kda_chunk_fwd_workspace_size(const kda_shape* shape) { return workspace_needed(shape, true); }
 
 kda_status kda_read_device_status(const void* workspace, void* stream) {
   if (!workspace) return KDA_ERR_INVALID_ARG;

@@ -1,33 +1,43 @@
 // kda_chunk_tc.cu -- fused tensor-core chunked KDA forward for sm_103a (bf16 I/O,
-// K = V = 128, chunk C = 64).
+// K = V = 128, chunk C = 64), one thread-block cluster per (sequence, value head).
 //
 // Chunked evaluation (page "手撕KDA", section "1 Naive", naive_chunk_kda; the
 // decayed-operand factorisation follows the FlashKDA walk-through, page
 // "KDA源码剖析之FlashKDA（上）", parts 9-11):
-//   gc      = inclusive cumsum of g over the chunk rows, g_last = gc[C-1]
-//   kd      = k e^{gc},  ki = k e^{-gc},  kr = k e^{g_last - gc},  qd = scale q e^{gc}
-//   M       = strict_tril(Diag(beta) kd ki^T)           (beta scales rows)
-//   Aqk     = tril(qd ki^T)                              (diagonal kept)
-//   A       = (I + M)^{-1} Diag(beta)                    (beta scales columns)
+//   gc   = inclusive cumsum of g over the chunk rows, g_last = gc[C-1]
+//   kd   = k e^{gc},  ki = k e^{-gc},  kr = k e^{g_last - gc},  qd = scale q e^{gc}
+//   M    = strict_tril(Diag(beta) kd ki^T)        (beta scales rows)
+//   Aqk  = tril(qd ki^T)                           (diagonal kept)
+//   A    = (I + M)^{-1} Diag(beta)                 (beta scales columns)
 //   W = A kd,  U = A v
 //   per chunk, serially:  v_new = U - W S;  o = qd S + Aqk v_new;
 //                         S <- Diag(e^{g_last}) S + kr^T v_new
 //
-// One CTA per (sequence, value head, 32-column slice of V): grid (4, HV, NS).
-// Warps 0-3 ("prepare") build chunk n+1's operands while warps 4-7 ("chain")
-// run chunk n's state update; the per-chunk record (qd, W, kr^T, Aqk, U, e^{g_last})
-// is double-buffered in shared memory.  All dense contractions are tcgen05.mma
-// (bf16 operands in 128-byte-swizzled shared memory, fp32 accumulators in TMEM):
-//   prepare: L = kd ki^T, Aqk = qd ki^T (M=64,N=64,K=128); [W | U] = A [kd^T ; v^T]^T (M=64,N=160,K=64)
-//   chain:   X = W S, O = qd S (M=64,N=32,K=128); P = kr^T v_new (M=128,N=32,K=64);
-//            O += Aqk v_new (M=64,N=32,K=64)
-// The K x 32 fp32 state slice lives in the chain threads' registers (thread d
-// holds row d); its bf16 copy S^T in shared memory is the MMA operand.
-// q, k and the v slice arrive by TMA; g and beta by coalesced register loads
-// one chunk ahead.  The 64 x 64 unit-lower-triangular inverse runs on CUDA
-// cores in fp32 (16 x 16 diagonal blocks by forward substitution, then block
-// rows).  Every mbarrier wait is bounded; on a timeout the CTA records
-// kStatusTimeout, drains, frees TMEM and returns.
+// Work split.  The cluster's 4 CTAs each own a 32-column slice of V (the chain)
+// and CTA r prepares the chunks n = r (mod 4) (the producer), so the
+// V-independent preparation is done once per chunk.  A producer writes the
+// chunk's record (qd, W, kr^T, Aqk in 128-byte-swizzled tile layout, U as four
+// 32-column slices, e^{g_last}) into a per-head ring of 8 slots in the
+// workspace (L2-resident; every part is staged in shared memory and written
+// with bulk copies) and publishes it with a cluster-scope mbarrier arrive on
+// every CTA; each CTA's chain bulk-copies the record into one of two
+// shared-memory slots and acknowledges it back to the producer.  A producer
+// keeps at most two records unacknowledged.  (Distributed shared memory
+// measured ~17 B/clk per SM on GB300, too slow to carry ~60 KB per chunk; bulk
+// copies from L2 are not.)
+//
+// Warps 0-3: producer.  Warps 4-7: chain (thread d holds row d of the fp32
+// K x 32 state slice in registers; its bf16 copy in shared memory is the MMA
+// operand; one chain thread also issues the record loads).  All dense
+// contractions are tcgen05.mma with fp32 accumulators in TMEM:
+//   producer: L = kd ki^T, Aqk = qd ki^T          (M=64, N=64,  K=128)
+//             W = A kd, U = A v (B MN-major)       (M=64, N=128, K=64) x 2
+//   chain:    X = W S, O = qd S                    (M=64, N=32,  K=128)
+//             P = kr^T v_new                       (M=128,N=32,  K=64)
+//             O += Aqk v_new                       (M=64, N=32,  K=64)
+// The 64 x 64 unit-lower-triangular inverse runs on CUDA cores in fp32.
+// Every wait is bounded; on a timeout a role records kStatusTimeout, all of
+// its threads agree through bar.red.or, drain what they issued and return.
 #include <cudaTypedefs.h>
 
 #include "kda_common.cuh"
@@ -41,42 +51,58 @@ constexpr int KD = 128;       // key dim
 constexpr int VD = 128;       // value dim
 constexpr int VS = 32;        // value columns per CTA
 constexpr int NSLICE = VD / VS;
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 256; // 4 producer warps, 4 chain warps
 constexpr int MB_LD = 68;     // padded row stride (floats) of the fp32 inverse buffer
+constexpr int RING = 16;      // record slots per head in the workspace ring
+
+// ---- record layout (global ring slot and shared slot share the first part) ----
+constexpr uint32_t R_QD = 0;          // [64 x 128] bf16 SW128
+constexpr uint32_t R_WM = 16384;      // [64 x 128] bf16 SW128
+constexpr uint32_t R_KRT = 32768;     // [128 x 64] bf16 SW128 (kr transposed)
+constexpr uint32_t R_AQK = 49152;     // [64 x 64]  bf16 SW128
+constexpr uint32_t R_TILES = 57344;   // bytes of the four tiles above
+constexpr uint32_t G_U = 57344;       // global: 4 slices of U, each [64 x 32] bf16 row-major
+constexpr uint32_t G_GAM = 57344 + 4 * 4096;  // global: e^{g_last} [128] fp32
+constexpr uint32_t GSLOT = 74752;             // global slot stride (1024-multiple)
+constexpr uint32_t S_U = 57344;       // shared slot: this CTA's U slice [64 x 32] bf16
+constexpr uint32_t S_GAM = 61440;     // shared slot: e^{g_last} [128] fp32
+constexpr uint32_t SSLOT = 62464;     // shared slot stride (1024-multiple)
+constexpr uint32_t REC_TX = R_TILES + 4096 + 512;
 
 // ---- shared memory map (offsets from a 1024-aligned base) ----
-constexpr uint32_t SET_BYTES = 65536;
-constexpr uint32_t OFF_QD = 0;          // [64 x 128] bf16 SW128 (raw q lands here)
-constexpr uint32_t OFF_WM = 16384;      // [64 x 128] bf16 SW128
-constexpr uint32_t OFF_KRT = 32768;     // [128 x 64] bf16 SW128 (kr transposed)
-constexpr uint32_t OFF_AQK = 49152;     // [64 x 64]  bf16 SW128
-constexpr uint32_t OFF_U = 57344;       // [64 x 32]  fp32 row-major
-constexpr uint32_t OFF_KD = 2 * SET_BYTES;       // 131072 [64 x 128] bf16 SW128
-constexpr uint32_t OFF_KI = OFF_KD + 16384;      // 147456 [64 x 128] bf16 SW128 (raw k lands here)
-constexpr uint32_t OFF_WUB = OFF_KI + 16384;     // 163840 [160 x 64] bf16 SW128: kd^T rows, then v^T rows
-constexpr uint32_t OFF_AMAT = OFF_WUB + 20480;   // 184320 [64 x 64] bf16 SW128 (also fp32 scratch)
-constexpr uint32_t OFF_ST = OFF_AMAT + 8192;     // 192512 [32 x 128] bf16 SW128 (S^T)
-constexpr uint32_t OFF_VNT = OFF_ST + 8192;      // 200704 [32 x 64] bf16 SW128 (v_new^T)
-constexpr uint32_t OFF_VST = OFF_VNT + 4096;     // 204800 [64 x 32] bf16 (raw v slice, TMA)
-constexpr uint32_t OFF_MB = OFF_VST + 4096;      // 208896 [64 x 68] fp32 (M, then T in place)
-constexpr uint32_t OFF_GAM = OFF_MB + 64 * MB_LD * 4;  // 226304 [2][128] fp32 e^{g_last}
-constexpr uint32_t OFF_BETA = OFF_GAM + 1024;          // 227328 [64] fp32
-constexpr uint32_t OFF_BAR = OFF_BETA + 256;           // 227584 mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 128;           // 227712 tmem base, abort flag
+constexpr uint32_t OFF_SLOT = 0;                          // 2 record slots
+constexpr uint32_t OFF_PQD = 2 * SSLOT;                   // 124928 producer q -> qd [64 x 128] SW128
+constexpr uint32_t OFF_PKD = OFF_PQD + 16384;             // 141312 kd [64 x 128] SW128
+constexpr uint32_t OFF_PV = OFF_PKD + 16384;              // 157696 raw v [64 x 128] as 2 SW128 boxes
+constexpr uint32_t OFF_PB = OFF_PV + 16384;               // 174080 ki (raw k) | later M fp32 + A bf16
+constexpr uint32_t OFF_MB = OFF_PB;                       //        [64 x 68] fp32
+constexpr uint32_t OFF_AMAT = OFF_PB + 17408;             // 191488 [64 x 64] bf16 SW128; before it is
+constexpr uint32_t OFF_RS = OFF_AMAT;                     //        written: Aqk staging, then [16 x 48] fp32
+constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB staging: kr^T, later U slices
+constexpr uint32_t OFF_ST = OFF_STG + 16384;              // 216064 S  [128 x 32] bf16 MN-major SW64
+constexpr uint32_t OFF_VNT = OFF_ST + 8192;               // 224256 v_new [64 x 32] bf16 MN-major SW64
+constexpr uint32_t OFF_BETA = OFF_VNT + 4096;             // 228352 [64] fp32
+constexpr uint32_t OFF_BAR = OFF_BETA + 256;              // 228608 mbarriers
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 228864 tmem base
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
-constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;     // + alignment slack
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;        // + alignment slack
 
 // barrier slots
-constexpr int BAR_RAW = 0, BAR_PMMA = 1, BAR_READY0 = 2, BAR_FREE0 = 4, BAR_A = 6, BAR_B = 7;
+constexpr int B_FULL = 0;    // [2] record landed in shared slot s (tx)
+constexpr int B_PUB = 2;     // [4 x 2] record j of producer r published: index 2r + (j & 1) (remote arrive)
+constexpr int B_ACK = 10;    // [2] this CTA's record j loaded by all 4 CTAs: index j & 1 (4 remote arrives)
+constexpr int B_RAW = 12;    // producer raw q/k/v (tx)
+constexpr int B_PMMA = 13;   // producer MMA commits
+constexpr int B_A = 14;      // chain X/O MMA commit
+constexpr int B_B = 15;      // chain P/O MMA commit
 
 // TMEM columns
-constexpr uint32_t TM_L = 0, TM_AQ = 64, TM_WU = 0, TM_X = 256, TM_O0 = 288, TM_P = 352;
+constexpr uint32_t TM_L = 0, TM_AQ = 64, TM_W = 0, TM_U = 128, TM_X = 256, TM_O0 = 288, TM_P = 352;
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t RAW_TX_BYTES = 16384 + 16384 + 4096;  // q + k + v slice
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
+constexpr uint32_t RAW_TX_BYTES = 3 * 16384;        // q, k, v tiles
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s
 
-// named barriers
 constexpr uint32_t NB_PREP = 1, NB_CHAIN = 2;
 
 struct Maps {
@@ -84,61 +110,130 @@ struct Maps {
 };
 
 // Optional per-phase cycle counters (build with -DKDA_PROFILE): thread 0 of the
-// prepare and chain warpgroups of block (0,0,0) accumulate clock64 deltas and
+// producer and of the chain of block (0,0,0) accumulate clock64 deltas and
 // store them after the status word in the workspace (16 + 16 uint64 slots).
 #ifdef KDA_PROFILE
-#define PROF_DECL uint64_t prof_acc[16] = {0}; uint64_t prof_last = clock64(); \
+#define PROF_DECL                                 \
+  uint64_t prof_acc[16] = {0};                    \
+  uint64_t prof_last = clock64();                 \
   const bool prof_on = (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
-#define PROF(i) do { if (prof_on) { const uint64_t t_ = clock64(); prof_acc[i] += t_ - prof_last; prof_last = t_; } } while (0)
-#define PROF_STORE(base) do { if (prof_on) { uint64_t* dst_ = reinterpret_cast<uint64_t*>(p.status) + 1 + (base); \
-  for (int i_ = 0; i_ < 16; ++i_) dst_[i_] = prof_acc[i_]; } } while (0)
+#define PROF(i)                                 \
+  do {                                          \
+    if (prof_on) {                              \
+      const uint64_t t_ = clock64();            \
+      prof_acc[i] += t_ - prof_last;            \
+      prof_last = t_;                           \
+    }                                           \
+  } while (0)
+#define PROF_STORE(base)                                                            \
+  do {                                                                              \
+    if (prof_on) {                                                                  \
+      uint64_t* dst_ = reinterpret_cast<uint64_t*>(p.status) + 1 + (base);          \
+      for (int i_ = 0; i_ < 16; ++i_) dst_[i_] = prof_acc[i_];                      \
+    }                                                                               \
+  } while (0)
 #else
 #define PROF_DECL
-#define PROF(i) do { } while (0)
-#define PROF_STORE(base) do { } while (0)
+#define PROF(i) \
+  do {          \
+  } while (0)
+#define PROF_STORE(base) \
+  do {                   \
+  } while (0)
 #endif
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
-__device__ __forceinline__ uint16_t f2bf(float f) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
 }
-__device__ __forceinline__ void st_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+__device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
+__device__ __forceinline__ void st_v4_global(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  __stcg(reinterpret_cast<uint4*>(p), make_uint4(a, b, c, d));
+}
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+// Role barriers: reconverge the warp first (bar.sync / bar.red are .aligned).
+__device__ __forceinline__ void role_sync(uint32_t id) {
+  __syncwarp();
+  named_bar_sync(id, 128);
+}
+__device__ __forceinline__ bool role_any(uint32_t id, bool pred) {
+  __syncwarp();
+  return named_bar_any(id, 128, pred);
+}
+
+// One block row (16 rows starting at 16*BI) of T = (I + M)^{-1}, with the rows
+// above already final in `mb` (M below the diagonal blocks, T elsewhere):
+//   R      = M[16BI.., 0..16BI) T[0..16BI, 0..16BI)
+//   T_row  = -T_ii R
+template <int BI>
+__device__ __forceinline__ void inverse_block_row(float* mb, float* rs, int pt) {
+  constexpr int NCOL = 16 * BI;
+  constexpr int PER = 2 * BI;
+  const int r = pt >> 3;
+  const int c0 = (pt & 7) * PER;
+  const float* mrow = mb + (16 * BI + r) * MB_LD;
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) {
+    const float a = mrow[k];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = fmaf(a, mb[k * MB_LD + c0 + e], acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) rs[r * 48 + c0 + e] = acc[e];
+  role_sync(NB_PREP);
+  const float* trow = mb + (16 * BI + r) * MB_LD + 16 * BI;
+  float t[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) t[e] = 0.f;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const float a = trow[m];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) t[e] = fmaf(a, rs[m * 48 + c0 + e], t[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) mb[(16 * BI + r) * MB_LD + c0 + e] = -t[e];
+  role_sync(NB_PREP);
+}
+
+__global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
-  float* gam = reinterpret_cast<float*>(sm + OFF_GAM);
   float* beta_s = reinterpret_cast<float*>(sm + OFF_BETA);
   float* mb = reinterpret_cast<float*>(sm + OFF_MB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slice = blockIdx.x, hv = blockIdx.y, seq = blockIdx.z;
+  const int hv = blockIdx.y, seq = blockIdx.z;
+  const uint32_t rank = cluster_ctarank();  // == blockIdx.x: the V slice and producer index
   const int HV = p.HV;
   const int hk = hv / (HV / p.H);
-  const int v0 = slice * VS;
+  const int v0 = static_cast<int>(rank) * VS;
 
   long tok0;
   int len;
   seq_range(p, seq, tok0, len);
   const int NT = (len + C - 1) / C;
+  uint8_t* ring = p.ring + (static_cast<size_t>(seq) * HV + hv) * (static_cast<size_t>(RING) * GSLOT);
 
   if (tid == 0) {
-    mbar_init(&bars[BAR_RAW], 1);
-    mbar_init(&bars[BAR_PMMA], 1);
-    mbar_init(&bars[BAR_READY0], 1);
-    mbar_init(&bars[BAR_READY0 + 1], 1);
-    mbar_init(&bars[BAR_FREE0], 1);
-    mbar_init(&bars[BAR_FREE0 + 1], 1);
-    mbar_init(&bars[BAR_A], 1);
-    mbar_init(&bars[BAR_B], 1);
+    mbar_init(&bars[B_FULL], 1);
+    mbar_init(&bars[B_FULL + 1], 1);
+    for (int r = 0; r < 8; ++r) mbar_init(&bars[B_PUB + r], 1);
+    mbar_init(&bars[B_ACK], NSLICE);
+    mbar_init(&bars[B_ACK + 1], NSLICE);
+    mbar_init(&bars[B_RAW], 1);
+    mbar_init(&bars[B_PMMA], 1);
+    mbar_init(&bars[B_A], 1);
+    mbar_init(&bars[B_B], 1);
     fence_mbar_init();
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.k);
@@ -150,132 +245,135 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // every CTA's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const size_t state_off = (static_cast<size_t>(seq) * HV + hv) * KD * VD;
 
   if (warp < 4) {
-    // =========================== prepare warpgroup ===========================
-    const int pt = tid;  // key dim owned in the elementwise pass
-    const int pw = warp;
+    // ============================== producer ===============================
+    const int pt = tid;   // key dim owned in the elementwise pass
+    const int pw = warp;  // TMEM lane quadrant
     const float scale = p.scale;
-    const float* gptr = p.g;
-    uint32_t pmma_phase = 0;   // completed waits on the prepare MMA barrier
-    uint32_t pmma_issued = 0;  // commits issued to it (elected thread)
-    bool tma_pending = false;  // a raw load was issued and not yet waited for
-    int pending_chunk = 0;
-    bool failed = false;       // this thread saw a wait give up
+    uint32_t pmma_phase = 0, pmma_issued = 0;
+    bool raw_pending = false;
+    int raw_pending_j = 0;
+    bool failed = false;
     auto timeout = [&]() {
       failed = true;
       atomicOr(p.status, kStatusTimeout);
     };
     PROF_DECL
 
-    auto issue_raw = [&](int n) {  // elected thread: TMA q, k, v slice of chunk n
-      const int s = n & 1;
-      const int row0 = static_cast<int>(tok0) + n * C;
-      mbar_arrive_expect_tx(&bars[BAR_RAW], RAW_TX_BYTES);
-      tma_load_3d(sm + s * SET_BYTES + OFF_QD, &maps.q, &bars[BAR_RAW], 0, hk, row0);
-      tma_load_3d(sm + s * SET_BYTES + OFF_QD + 8192, &maps.q, &bars[BAR_RAW], 64, hk, row0);
-      tma_load_3d(sm + OFF_KI, &maps.k, &bars[BAR_RAW], 0, hk, row0);
-      tma_load_3d(sm + OFF_KI + 8192, &maps.k, &bars[BAR_RAW], 64, hk, row0);
-      tma_load_3d(sm + OFF_VST, &maps.v, &bars[BAR_RAW], v0, hv, row0);
+    auto issue_raw = [&](int m, int j) {  // elected: TMA q, k, v tiles of chunk m (own chunk j)
+      const int row0 = static_cast<int>(tok0) + m * C;
+      mbar_arrive_expect_tx(&bars[B_RAW], RAW_TX_BYTES);
+      tma_load_3d(sm + OFF_PQD, &maps.q, &bars[B_RAW], 0, hk, row0);
+      tma_load_3d(sm + OFF_PQD + 8192, &maps.q, &bars[B_RAW], 64, hk, row0);
+      tma_load_3d(sm + OFF_PB, &maps.k, &bars[B_RAW], 0, hk, row0);
+      tma_load_3d(sm + OFF_PB + 8192, &maps.k, &bars[B_RAW], 64, hk, row0);
+      tma_load_3d(sm + OFF_PV, &maps.v, &bars[B_RAW], 0, hv, row0);
+      tma_load_3d(sm + OFF_PV + 8192, &maps.v, &bars[B_RAW], 64, hv, row0);
+      raw_pending = true;
+      raw_pending_j = j;
     };
     float gpre[C];
     float bpre = 0.f;
-    auto prefetch_gb = [&](int n) {
-      const int rows = min(C, len - n * C);
-      const long base = tok0 + static_cast<long>(n) * C;
+    // g (and beta) of a chunk arrive in registers in four 16-row parts issued at
+    // different points of the previous chunk, so that few loads are in flight at once
+    auto prefetch_gb = [&](int m, int part) {
+      const int rows = min(C, len - m * C);
+      const long base = tok0 + static_cast<long>(m) * C;
 #pragma unroll
-      for (int c = 0; c < C; ++c)
-        gpre[c] = (c < rows) ? __ldg(gptr + (static_cast<size_t>(base + c) * HV + hv) * KD + pt) : 0.f;
-      if (pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
+      for (int c = 16 * part; c < 16 * part + 16; ++c)
+        gpre[c] = (c < rows) ? __ldg(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD + pt) : 0.f;
+      if (part == 0 && pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
+    };
+    bool pub_pending = false;  // record j-1 stored but not yet published
+    auto publish = [&](int jp) {  // elected thread: record jp is complete in the ring
+      fence_proxy_async_global();
+      bool ok = true;
+      if (jp >= 2) ok = mbar_wait_cluster(&bars[B_ACK + (jp & 1)], ((jp - 2) >> 1) & 1, WAIT_LIMIT_NS);
+      if (ok) {
+        const uint32_t pub = smem_u32(&bars[B_PUB + 2 * rank + (jp & 1)]);
+        for (uint32_t c = 0; c < NSLICE; ++c) mbar_arrive_cluster(mapa_shared(pub, c));
+      } else {
+        timeout();
+      }
     };
 
-    if (NT > 0) {
-      if (pt == 0) {
-        issue_raw(0);
-        tma_pending = true;
-        pending_chunk = 0;
-      }
-      prefetch_gb(0);
+    const int first = static_cast<int>(rank);
+    if (first < NT) {
+      if (pt == 0) issue_raw(first, 0);
+#pragma unroll
+      for (int part = 0; part < 4; ++part) prefetch_gb(first, part);
     }
-
-    for (int n = 0; n < NT; ++n) {
-      const int s = n & 1;
-      uint8_t* set = sm + s * SET_BYTES;
-      const int rows = min(C, len - n * C);
-      // ---- 1. raw q, k, v of chunk n ----
-      if (!mbar_wait(&bars[BAR_RAW], n & 1, WAIT_LIMIT_NS)) timeout();
-      if (named_bar_any(NB_PREP, 128, failed)) break;
-      if (pt == 0) tma_pending = false;
+    int j = 0;
+    for (int m = first; m < NT; m += NSLICE, ++j) {
+      uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
+      const int rows = min(C, len - m * C);
+      // ---- 1. raw q, k, v of chunk m ----
+      if (!mbar_wait(&bars[B_RAW], j & 1, WAIT_LIMIT_NS)) timeout();
+      if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
+      if (role_any(NB_PREP, failed)) break;
+      if (pt == 0) raw_pending = false;
       PROF(0);
 
-      // ---- 2. elementwise: cumsum, decayed operands ----
+      // ---- 2. elementwise: cumsum, decayed operands; kr^T and e^{g_last} to the record ----
       if (pt < C) beta_s[pt] = bpre;
       float glast = 0.f;
 #pragma unroll
       for (int c = 0; c < C; ++c) glast += gpre[c];
       const float gamma = __expf(glast);
-      gam[s * KD + pt] = gamma;
+      __stcg(reinterpret_cast<float*>(gs + G_GAM) + pt, gamma);
       {
         float gc = 0.f;
-        uint8_t* qd_t = set + OFF_QD;
-        uint8_t* ki_t = sm + OFF_KI;
-        uint8_t* kd_t = sm + OFF_KD;
+        uint8_t* qd_t = sm + OFF_PQD;
+        uint8_t* ki_t = sm + OFF_PB;
+        uint8_t* kd_t = sm + OFF_PKD;
+        const uint32_t col_part = (pt >> 6) * 8192u + ((pt & 7) << 1);
+        const uint32_t chunk_part = (pt >> 3) & 7u;
 #pragma unroll
         for (int c8 = 0; c8 < C / 8; ++c8) {
-          uint32_t kdT[4], krT[4];
+          uint16_t kraw[8], qraw[8];
+          uint32_t off[8];
 #pragma unroll
-          for (int cc = 0; cc < 8; cc += 2) {
-            float kdv[2], krv[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int c = c8 * 8 + cc + h;
-              gc += gpre[c];
-              const float e = __expf(gc);
-              const float ie = __expf(-gc);
-              const uint32_t off = sw128_offset(c, pt, C);
-              const bool valid = c < rows;
-              const float kv = valid ? bf2f(*reinterpret_cast<const uint16_t*>(ki_t + off)) : 0.f;
-              const float qv = valid ? bf2f(*reinterpret_cast<const uint16_t*>(qd_t + off)) : 0.f;
-              const float kdf = kv * e;
-              const float kif = kv * ie;
-              kdv[h] = kdf;
-              krv[h] = kif * gamma;
-              *reinterpret_cast<uint16_t*>(kd_t + off) = f2bf(kdf);
-              *reinterpret_cast<uint16_t*>(ki_t + off) = f2bf(kif);
-              *reinterpret_cast<uint16_t*>(qd_t + off) = f2bf(qv * e * scale);
-            }
-            kdT[cc / 2] = pack2(kdv[0], kdv[1]);
-            krT[cc / 2] = pack2(krv[0], krv[1]);
+          for (int cc = 0; cc < 8; ++cc) {
+            const int c = c8 * 8 + cc;
+            off[cc] = col_part + c * 128u + ((chunk_part ^ (c & 7)) << 4);
+            kraw[cc] = *reinterpret_cast<const uint16_t*>(ki_t + off[cc]);
+            qraw[cc] = *reinterpret_cast<const uint16_t*>(qd_t + off[cc]);
           }
-          st_v4(sm + OFF_WUB + sw128_offset(pt, c8 * 8, 160), kdT[0], kdT[1], kdT[2], kdT[3]);
-          st_v4(set + OFF_KRT + sw128_offset(pt, c8 * 8, 128), krT[0], krT[1], krT[2], krT[3]);
+          float kdv[8], kiv[8], qdv[8], krv[8];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const int c = c8 * 8 + cc;
+            gc += gpre[c];
+            const float e = __expf(gc);
+            const float ie = __expf(-gc);
+            const bool valid = c < rows;
+            const float kv = valid ? bf2f(kraw[cc]) : 0.f;
+            const float qv = valid ? bf2f(qraw[cc]) : 0.f;
+            kdv[cc] = kv * e;
+            kiv[cc] = kv * ie;
+            krv[cc] = kiv[cc] * gamma;
+            qdv[cc] = qv * e * scale;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            *reinterpret_cast<uint16_t*>(kd_t + off[cc]) = f2bf(kdv[cc]);
+            *reinterpret_cast<uint16_t*>(ki_t + off[cc]) = f2bf(kiv[cc]);
+            *reinterpret_cast<uint16_t*>(qd_t + off[cc]) = f2bf(qdv[cc]);
+          }
+          st_v4(sm + OFF_STG + sw128_offset(pt, c8 * 8, 128), pack2(krv[0], krv[1]), pack2(krv[2], krv[3]),
+                pack2(krv[4], krv[5]), pack2(krv[6], krv[7]));
         }
       }
-      {  // v slice transposed into rows 128..159 of the W/U B operand
-        const int vv = pt >> 2, cb = (pt & 3) * 16;
-        const uint16_t* vst = reinterpret_cast<const uint16_t*>(sm + OFF_VST);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            const int c = cb + h * 8 + i;
-            const float a = (c < rows) ? bf2f(vst[c * VS + vv]) : 0.f;
-            const float b = (c + 1 < rows) ? bf2f(vst[(c + 1) * VS + vv]) : 0.f;
-            w[i / 2] = pack2(a, b);
-          }
-          st_v4(sm + OFF_WUB + sw128_offset(128 + vv, cb + h * 8, 160), w[0], w[1], w[2], w[3]);
-        }
-      }
-      if (n + 1 < NT) prefetch_gb(n + 1);
       fence_proxy_async_smem();
-      named_bar_sync(NB_PREP, 128);
+      role_sync(NB_PREP);
       PROF(1);
 
-      // ---- 3. L = kd ki^T, Aqk = qd ki^T ----
+      // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd tile to the record ----
       if (pt == 0) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_f16kind(64, 64);
@@ -284,34 +382,29 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t koff = kb * 8192 + ks * 32;
-            const uint64_t bd = sdesc_sw128(smem_u32(sm + OFF_KI + koff));
-            umma_f16(tmem + TM_L, sdesc_sw128(smem_u32(sm + OFF_KD + koff)), bd, idesc, (kb | ks) != 0);
-            umma_f16(tmem + TM_AQ, sdesc_sw128(smem_u32(set + OFF_QD + koff)), bd, idesc, (kb | ks) != 0);
+            const uint64_t bd = sdesc_sw128(smem_u32(sm + OFF_PB + koff));
+            umma_f16(tmem + TM_L, sdesc_sw128(smem_u32(sm + OFF_PKD + koff)), bd, idesc, (kb | ks) != 0);
+            umma_f16(tmem + TM_AQ, sdesc_sw128(smem_u32(sm + OFF_PQD + koff)), bd, idesc, (kb | ks) != 0);
           }
-        umma_commit(&bars[BAR_PMMA]);
+        umma_commit(&bars[B_PMMA]);
         ++pmma_issued;
+        bulk_store(gs + R_QD, sm + OFF_PQD, 16384);
+        bulk_store(gs + R_KRT, sm + OFF_STG, 16384);
+        bulk_commit();
+        if (pub_pending) {  // the previous record's W/U stores (the older group) are complete
+          bulk_wait_group<1>();
+          publish(j - 1);
+          pub_pending = false;
+        }
       }
+      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 0);
       __syncwarp();
-      if (!mbar_wait(&bars[BAR_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
+      if (!mbar_wait(&bars[B_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
       ++pmma_phase;
       tc_fence_after();
       PROF(2);
 
-      // KI and VST are free again: fetch chunk n+1 (its set must be released by the chain)
-      if (pt == 0 && n + 1 < NT && !failed) {
-        bool ok = true;
-        if (n + 1 >= 2) ok = mbar_wait(&bars[BAR_FREE0 + ((n + 1) & 1)], ((n - 1) >> 1) & 1, WAIT_LIMIT_NS);
-        if (ok) {
-          issue_raw(n + 1);
-          tma_pending = true;
-          pending_chunk = n + 1;
-        } else {
-          timeout();
-        }
-      }
-      PROF(3);
-
-      // ---- 4. TMEM -> M (fp32, rows scaled by beta, strictly lower) and Aqk (bf16, lower) ----
+      // ---- 4. TMEM -> M (fp32, rows scaled by beta, strictly lower), Aqk -> record ----
       __syncwarp();
       {
         const int i = 16 * pw + (lane & 15);
@@ -325,12 +418,12 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
               float4 v4;
-              const int j = 32 * half + 4 * j4;
-              v4.x = (j + 0 < i) ? bi * r[4 * j4 + 0] : 0.f;
-              v4.y = (j + 1 < i) ? bi * r[4 * j4 + 1] : 0.f;
-              v4.z = (j + 2 < i) ? bi * r[4 * j4 + 2] : 0.f;
-              v4.w = (j + 3 < i) ? bi * r[4 * j4 + 3] : 0.f;
-              *reinterpret_cast<float4*>(mb + i * MB_LD + j) = v4;
+              const int jj = 32 * half + 4 * j4;
+              v4.x = (jj + 0 < i) ? bi * r[4 * j4 + 0] : 0.f;
+              v4.y = (jj + 1 < i) ? bi * r[4 * j4 + 1] : 0.f;
+              v4.z = (jj + 2 < i) ? bi * r[4 * j4 + 2] : 0.f;
+              v4.w = (jj + 3 < i) ? bi * r[4 * j4 + 3] : 0.f;
+              *reinterpret_cast<float4*>(mb + i * MB_LD + jj) = v4;
             }
           }
           tmem_ld32(tmem_addr(tmem, 32 * pw, TM_AQ + 32 * half), r);
@@ -341,142 +434,163 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
               uint32_t w[4];
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
-                const int j = 32 * half + 8 * j8 + 2 * t;
-                w[t] = pack2((j <= i) ? r[8 * j8 + 2 * t] : 0.f, (j + 1 <= i) ? r[8 * j8 + 2 * t + 1] : 0.f);
+                const int jj = 32 * half + 8 * j8 + 2 * t;
+                w[t] = pack2((jj <= i) ? r[8 * j8 + 2 * t] : 0.f, (jj + 1 <= i) ? r[8 * j8 + 2 * t + 1] : 0.f);
               }
-              st_v4(set + OFF_AQK + sw128_offset(i, 32 * half + 8 * j8, 64), w[0], w[1], w[2], w[3]);
+              st_v4(sm + OFF_AMAT + sw128_offset(i, 32 * half + 8 * j8, 64), w[0], w[1], w[2], w[3]);
             }
           }
         }
       }
       tc_fence_before();
-      if (named_bar_any(NB_PREP, 128, failed)) break;
-      PROF(4);
+      fence_proxy_async_smem();
+      if (role_any(NB_PREP, failed)) break;
+      if (pt == 0) {
+        bulk_store(gs + R_AQK, sm + OFF_AMAT, 8192);
+        bulk_commit();
+      }
+      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 1);
+      PROF(3);
 
-      // ---- 5. T = (I + M)^{-1}: 16x16 diagonal blocks, then block rows ----
+      // ---- 5. T = (I + M)^{-1}: 16x16 diagonal blocks by forward substitution, then block rows ----
+      if (lane < 16) {
+        const int b0 = 16 * pw, jc = lane;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = (i == jc) ? 1.f : 0.f;
+#pragma unroll
+        for (int mm = 0; mm < 16; ++mm) {
+          const float xm = acc[mm];  // final: column jc of T, row mm
+#pragma unroll
+          for (int i = mm + 1; i < 16; ++i) acc[i] = fmaf(-mb[(b0 + i) * MB_LD + b0 + mm], xm, acc[i]);
+        }
+        __syncwarp(0x0000FFFFu);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
+      }
+      if (pt == 0) bulk_wait_read();  // the Aqk staging (reused as scratch next) has been read
+      role_sync(NB_PREP);
+      PROF(4);
       {
-        if (lane < 16) {
-          const int b0 = 16 * pw, j = lane;
-          float x[16];
+        float* rs = reinterpret_cast<float*>(sm + OFF_RS);
+        inverse_block_row<1>(mb, rs, pt);
+        inverse_block_row<2>(mb, rs, pt);
+        inverse_block_row<3>(mb, rs, pt);
+      }
+      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 2);
+      PROF(5);
+      {  // A = T Diag(beta) -> bf16 SW128
+        const int i = pt >> 1, jb = (pt & 1) * 32;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float acc = (i == j) ? 1.f : 0.f;
+        for (int j8 = 0; j8 < 4; ++j8) {
+          uint32_t w[4];
 #pragma unroll
-            for (int m = 0; m < i; ++m) acc = fmaf(-mb[(b0 + i) * MB_LD + b0 + m], x[m], acc);
-            x[i] = acc;
+          for (int t = 0; t < 4; ++t) {
+            const int jj = jb + 8 * j8 + 2 * t;
+            const float a = (jj <= i) ? mb[i * MB_LD + jj] * beta_s[jj] : 0.f;
+            const float b = (jj + 1 <= i) ? mb[i * MB_LD + jj + 1] * beta_s[jj + 1] : 0.f;
+            w[t] = pack2(a, b);
           }
-          __syncwarp(0x0000FFFFu);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) mb[(b0 + i) * MB_LD + b0 + j] = x[i];
-        }
-        named_bar_sync(NB_PREP, 128);
-        PROF(5);
-        float* rs = reinterpret_cast<float*>(sm + OFF_AMAT);  // [16][48] fp32 scratch
-        const int r = pt >> 3;
-        for (int bi = 1; bi < 4; ++bi) {
-          const int ncol = 16 * bi;          // columns of the block row left of the diagonal
-          const int per = 2 * bi;            // elements per thread
-          const int c0 = (pt & 7) * per;
-          const float* mrow = mb + (16 * bi + r) * MB_LD;
-          for (int e = 0; e < per; ++e) {    // R = M_i[:, :16i] T[:16i, :16i]
-            const int c = c0 + e;
-            float acc = 0.f;
-            for (int k = c; k < ncol; ++k) acc = fmaf(mrow[k], mb[k * MB_LD + c], acc);
-            rs[r * 48 + c] = acc;
-          }
-          named_bar_sync(NB_PREP, 128);
-          const float* trow = mb + (16 * bi + r) * MB_LD + 16 * bi;  // T_ii row r
-          for (int e = 0; e < per; ++e) {    // T_i[:, :16i] = -T_ii R
-            const int c = c0 + e;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m) acc = fmaf(trow[m], rs[m * 48 + c], acc);
-            mb[(16 * bi + r) * MB_LD + c] = -acc;
-          }
-          named_bar_sync(NB_PREP, 128);
-        }
-        PROF(6);
-        // A = T Diag(beta) -> bf16 SW128
-        {
-          const int i = pt >> 1, jb = (pt & 1) * 32;
-#pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int j = jb + 8 * j8 + 2 * t;
-              const float a = (j <= i) ? mb[i * MB_LD + j] * beta_s[j] : 0.f;
-              const float b = (j + 1 <= i) ? mb[i * MB_LD + j + 1] * beta_s[j + 1] : 0.f;
-              w[t] = pack2(a, b);
-            }
-            st_v4(sm + OFF_AMAT + sw128_offset(i, jb + 8 * j8, 64), w[0], w[1], w[2], w[3]);
-          }
+          st_v4(sm + OFF_AMAT + sw128_offset(i, jb + 8 * j8, 64), w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(NB_PREP, 128);
-      PROF(7);
+      role_sync(NB_PREP);
+      PROF(6);
 
-      // ---- 6. [W | U] = A [kd^T ; v^T]^T ----
+      // ---- 6. W = A kd, U = A v (kd and v as MN-major B operands) ----
       if (pt == 0) {
         tc_fence_after();
-        constexpr uint32_t idesc = idesc_f16kind(64, 160);
+        constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_f16(tmem + TM_WU, sdesc_sw128(smem_u32(sm + OFF_AMAT + ks * 32)),
-                   sdesc_sw128(smem_u32(sm + OFF_WUB + ks * 32)), idesc, ks != 0);
-        umma_commit(&bars[BAR_PMMA]);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = sdesc_sw128(smem_u32(sm + OFF_AMAT + ks * 32));
+          umma_f16(tmem + TM_W, ad, sdesc(smem_u32(sm + OFF_PKD + ks * 2048), 8192, 1024, 2), idesc, ks != 0);
+          umma_f16(tmem + TM_U, ad, sdesc(smem_u32(sm + OFF_PV + ks * 2048), 8192, 1024, 2), idesc, ks != 0);
+        }
+        umma_commit(&bars[B_PMMA]);
         ++pmma_issued;
       }
       __syncwarp();
-      if (!mbar_wait(&bars[BAR_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
+      if (!mbar_wait(&bars[B_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
       ++pmma_phase;
       tc_fence_after();
-      PROF(8);
+      // raw buffers are free again: fetch the next own chunk
+      if (pt == 0 && m + NSLICE < NT && !failed) {
+        bulk_wait_read();  // the qd tile store has read its source
+        issue_raw(m + NSLICE, j + 1);
+      }
+      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 3);
+      PROF(7);
 
-      // ---- 7. W -> bf16 SW128, U -> fp32 ----
+      // ---- 7. W -> record (bf16 SW128), U -> record (4 slices of [64 x 32] bf16) ----
       __syncwarp();
       {
         const int i = 16 * pw + (lane & 15);
         float r[32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_WU + 32 * q4), r);
+          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_W + 32 * q4), r);
           tmem_ld_wait();
           if (lane < 16) {
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8)
-              st_v4(set + OFF_WM + sw128_offset(i, 32 * q4 + 8 * j8, 64), pack2(r[8 * j8], r[8 * j8 + 1]),
+              st_v4(sm + OFF_PKD + sw128_offset(i, 32 * q4 + 8 * j8, 64), pack2(r[8 * j8], r[8 * j8 + 1]),
                     pack2(r[8 * j8 + 2], r[8 * j8 + 3]), pack2(r[8 * j8 + 4], r[8 * j8 + 5]),
                     pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
           }
         }
-        tmem_ld32(tmem_addr(tmem, 32 * pw, TM_WU + 128), r);
-        tmem_ld_wait();
-        if (lane < 16) {
-          float4* urow = reinterpret_cast<float4*>(set + OFF_U + i * (VS * 4));
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) urow[j4] = make_float4(r[4 * j4], r[4 * j4 + 1], r[4 * j4 + 2], r[4 * j4 + 3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_U + 32 * q4), r);
+          tmem_ld_wait();
+          if (lane < 16) {
+            uint8_t* urow = sm + OFF_STG + q4 * 4096 + i * (VS * 2);
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8)
+              st_v4(urow + 16 * j8, pack2(r[8 * j8], r[8 * j8 + 1]), pack2(r[8 * j8 + 2], r[8 * j8 + 3]),
+                    pack2(r[8 * j8 + 4], r[8 * j8 + 5]), pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
+          }
         }
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      if (named_bar_any(NB_PREP, 128, failed)) break;
-      if (pt == 0) mbar_arrive(&bars[BAR_READY0 + s]);
+      fence_proxy_async_global();  // e^{g_last} went out with plain stores
+      if (role_any(NB_PREP, failed)) break;
+      PROF(8);
+
+      // ---- 8. W/U to the ring; the record is published after the next chunk's
+      //         elementwise pass (or at the end), once these stores have landed ----
+      if (pt == 0) {
+        bulk_store(gs + R_WM, sm + OFF_PKD, 16384);
+        bulk_store(gs + G_U, sm + OFF_STG, 16384);
+        bulk_commit();
+        pub_pending = true;
+      }
       PROF(9);
     }
-    // drain after an abort: copies and MMAs still in flight must finish before
-    // the CTA frees TMEM and exits
+    if (pt == 0 && pub_pending && !failed) {
+      bulk_wait_all();
+      publish(j - 1);
+      pub_pending = false;
+    }
+    // drain after an abort: copies and MMAs this role issued must finish first
     if (pt == 0) {
-      if (tma_pending && !mbar_wait(&bars[BAR_RAW], pending_chunk & 1, WAIT_LIMIT_NS))
+      if (raw_pending && !mbar_wait(&bars[B_RAW], raw_pending_j & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+      if (pmma_issued > pmma_phase && !mbar_wait(&bars[B_PMMA], (pmma_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
-      if (pmma_issued > pmma_phase && !mbar_wait(&bars[BAR_PMMA], (pmma_issued - 1) & 1, WAIT_LIMIT_NS))
-        atomicOr(p.status, kStatusTimeout);
+      bulk_wait_all();
+      // records this CTA published must be loaded everywhere before it exits
+      for (int jj = (j >= 2 ? j - 2 : 0); !failed && jj < j; ++jj)
+        if (!mbar_wait_cluster(&bars[B_ACK + (jj & 1)], (jj >> 1) & 1, WAIT_LIMIT_NS))
+          atomicOr(p.status, kStatusTimeout);
       PROF_STORE(0);
     }
+    __syncwarp();
   } else {
-    // ============================= chain warpgroup =============================
-    const int qt = tid - 128;   // state row d
-    const int qw = warp - 4;    // TMEM lane quadrant
+    // ================================ chain ================================
+    const int qt = tid - 128;  // state row d
+    const int qw = warp - 4;   // TMEM lane quadrant
     const int d = qt;
     float st[VS];
     if (p.s0) {
@@ -484,83 +598,147 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 #pragma unroll
       for (int j4 = 0; j4 < VS / 4; ++j4) {
         const float4 v4 = src[j4];
-        st[4 * j4] = v4.x; st[4 * j4 + 1] = v4.y; st[4 * j4 + 2] = v4.z; st[4 * j4 + 3] = v4.w;
+        st[4 * j4] = v4.x;
+        st[4 * j4 + 1] = v4.y;
+        st[4 * j4 + 2] = v4.z;
+        st[4 * j4 + 3] = v4.w;
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < VS; ++j) st[j] = 0.f;
+      for (int jj = 0; jj < VS; ++jj) st[jj] = 0.f;
     }
-    auto write_st = [&]() {
+    auto write_st = [&]() {  // row d of S as bf16, MN-major 64-byte swizzle
 #pragma unroll
-      for (int j = 0; j < VS; ++j)
-        *reinterpret_cast<uint16_t*>(sm + OFF_ST + sw128_offset(j, d, VS)) = f2bf(st[j]);
+      for (int ch = 0; ch < 4; ++ch)
+        st_v4(sm + OFF_ST + mn_sw64_offset(d, 8 * ch), pack2(st[8 * ch], st[8 * ch + 1]),
+              pack2(st[8 * ch + 2], st[8 * ch + 3]), pack2(st[8 * ch + 4], st[8 * ch + 5]),
+              pack2(st[8 * ch + 6], st[8 * ch + 7]));
     };
     write_st();
     fence_proxy_async_smem();
-    named_bar_sync(NB_CHAIN, 128);
+    role_sync(NB_CHAIN);
 
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    bool failed = false;
-    bool aborted = false;
-    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;  // commits (elected thread) / waits
+    bool failed = false, aborted = false;
+    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
     auto timeout = [&]() {
       failed = true;
       atomicOr(p.status, kStatusTimeout);
     };
-    PROF_DECL
-    for (int n = 0; n < NT; ++n) {
-      const int s = n & 1;
-      uint8_t* set = sm + s * SET_BYTES;
-      const int rows = min(C, len - n * C);
-      // ---- X = W S, O = qd S ----
-      if (qt == 0) {
-        if (!mbar_wait(&bars[BAR_READY0 + s], (n >> 1) & 1, WAIT_LIMIT_NS)) {
-          timeout();
-        } else {
-          tc_fence_after();
-          constexpr uint32_t idesc = idesc_f16kind(64, VS);
-#pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t bd = sdesc_sw128(smem_u32(sm + OFF_ST + kb * 4096 + ks * 32));
-              const uint32_t koff = kb * 8192 + ks * 32;
-              umma_f16(tmem + TM_X, sdesc_sw128(smem_u32(set + OFF_WM + koff)), bd, idesc, (kb | ks) != 0);
-              umma_f16(tmem + TM_O0 + 32 * s, sdesc_sw128(smem_u32(set + OFF_QD + koff)), bd, idesc,
-                       (kb | ks) != 0);
-            }
-          umma_commit(&bars[BAR_A]);
-          ++a_issued;
+    // Record loads (thread qt == 0): chunk m goes to slot m & 1 once it is
+    // published by producer m % 4 (its record j = m / 4) and the slot is free.
+    int next_load = 0;       // first chunk whose load is not issued yet
+    int loads_done = 0;      // loads whose FULL phase was observed (and acknowledged)
+    auto pub_bar = [&](int m) { return &bars[B_PUB + 2 * (m % NSLICE) + ((m / NSLICE) & 1)]; };
+    auto issue_load = [&](int m) {
+      fence_proxy_async_global();
+      const int s = m & 1;
+      uint8_t* slot = sm + OFF_SLOT + s * SSLOT;
+      const uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
+      mbar_arrive_expect_tx(&bars[B_FULL + s], REC_TX);
+      bulk_load(slot + R_QD, gs + R_QD, R_TILES, &bars[B_FULL + s]);
+      bulk_load(slot + S_U, gs + G_U + rank * 4096, 4096, &bars[B_FULL + s]);
+      bulk_load(slot + S_GAM, gs + G_GAM, 512, &bars[B_FULL + s]);
+    };
+    // issue every load that is allowed (slot free: next_load < m_cur + 2); block only if `need`
+    auto pump_loads = [&](int m_cur, bool need) {
+      while (next_load < NT && next_load < m_cur + 2) {
+        const int m = next_load;
+        if (!mbar_try_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1)) {
+          if (!need || m != m_cur) return;
+          if (!mbar_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1, WAIT_LIMIT_NS)) {
+            timeout();
+            return;
+          }
         }
+        issue_load(m);
+        ++next_load;
+      }
+    };
+    // o rows of chunk m from TMEM buffer m & 1 (rewritten only by chunk m + 2's MMAs)
+    auto emit_o = [&](int m) {
+      const int rows = min(C, len - m * C);
+      float orr[32];
+      tmem_ld32(tmem_addr(tmem, 32 * qw, TM_O0 + 32 * (m & 1)), orr);
+      tmem_ld_wait();
+      const int c = 16 * qw + lane;
+      if (lane < 16 && c < rows) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok0 + m * C + c) * HV + hv) * VD + v0);
+#pragma unroll
+        for (int j8 = 0; j8 < VS / 8; ++j8)
+          dst[j8] = make_uint4(pack2(orr[8 * j8], orr[8 * j8 + 1]), pack2(orr[8 * j8 + 2], orr[8 * j8 + 3]),
+                               pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]), pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
+      }
+    };
+    PROF_DECL
+    if (qt == 0) pump_loads(0, false);
+    for (int m = 0; m < NT; ++m) {
+      const int s = m & 1;
+      uint8_t* slot = sm + OFF_SLOT + s * SSLOT;
+      if (qt == 0 && !failed) pump_loads(m, true);
+      __syncwarp();
+      if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout();
+      if (qt == 0 && !failed) {  // record m is in shared memory: release its ring slot
+        mbar_arrive_cluster(mapa_shared(smem_u32(&bars[B_ACK + ((m / NSLICE) & 1)]), static_cast<uint32_t>(m % NSLICE)));
+        ++loads_done;
       }
       PROF(0);
+      // ---- X = W S, O = qd S ----
+      if (qt == 0 && !failed) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_f16kind(64, VS) | IDESC_B_MN_MAJOR;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = sdesc(smem_u32(sm + OFF_ST + (kb * 4 + ks) * 1024), 8192, 512, 4);
+            umma_f16(tmem + TM_X, sdesc_sw128(smem_u32(slot + R_WM + kb * 8192 + ks * 32)), bd, idesc,
+                     (kb | ks) != 0);
+          }
+        umma_commit(&bars[B_A]);  // X alone: v_new needs it first
+        ++a_issued;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = sdesc(smem_u32(sm + OFF_ST + (kb * 4 + ks) * 1024), 8192, 512, 4);
+            umma_f16(tmem + TM_O0 + 32 * s, sdesc_sw128(smem_u32(slot + R_QD + kb * 8192 + ks * 32)), bd, idesc,
+                     (kb | ks) != 0);
+          }
+        pump_loads(m, false);
+      }
       __syncwarp();
-      if (!mbar_wait(&bars[BAR_A], n & 1, WAIT_LIMIT_NS)) timeout();
+      if (m > 0) emit_o(m - 1);  // previous chunk's rows, while this chunk's MMAs run
+      if (!mbar_wait(&bars[B_A], m & 1, WAIT_LIMIT_NS)) timeout();
       ++a_done;
       tc_fence_after();
       PROF(1);
-      // ---- v_new = U - X  ->  v_new^T (bf16 SW128) ----
+      // ---- v_new = U - X  ->  bf16 MN-major (row c = token) ----
       {
         float xr[32];
         tmem_ld32(tmem_addr(tmem, 32 * qw, TM_X), xr);
         tmem_ld_wait();
         if (lane < 16) {
           const int c = 16 * qw + lane;
-          const float4* urow = reinterpret_cast<const float4*>(set + OFF_U + c * (VS * 4));
+          const uint4* urow = reinterpret_cast<const uint4*>(slot + S_U + c * (VS * 2));
 #pragma unroll
-          for (int j4 = 0; j4 < VS / 4; ++j4) {
-            const float4 u4 = urow[j4];
-            const float vn[4] = {u4.x - xr[4 * j4], u4.y - xr[4 * j4 + 1], u4.z - xr[4 * j4 + 2],
-                                 u4.w - xr[4 * j4 + 3]};
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint4 u = urow[ch];
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+            uint32_t w[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-              *reinterpret_cast<uint16_t*>(sm + OFF_VNT + sw128_offset(4 * j4 + t, c, VS)) = f2bf(vn[t]);
+            for (int t = 0; t < 4; ++t) {
+              const float lo = bf2f(static_cast<uint16_t>(uw[t] & 0xFFFFu)) - xr[8 * ch + 2 * t];
+              const float hi = bf2f(static_cast<uint16_t>(uw[t] >> 16)) - xr[8 * ch + 2 * t + 1];
+              w[t] = pack2(lo, hi);
+            }
+            st_v4(sm + OFF_VNT + mn_sw64_offset(c, 8 * ch), w[0], w[1], w[2], w[3]);
           }
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      if (named_bar_any(NB_CHAIN, 128, failed)) {
+      if (role_any(NB_CHAIN, failed)) {
         aborted = true;
         break;
       }
@@ -568,66 +746,60 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       // ---- P = kr^T v_new ; O += Aqk v_new ----
       if (qt == 0) {
         tc_fence_after();
-        constexpr uint32_t idesc_p = idesc_f16kind(128, VS);
-        constexpr uint32_t idesc_o = idesc_f16kind(64, VS);
+        constexpr uint32_t idesc_p = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
+        constexpr uint32_t idesc_o = idesc_f16kind(64, VS) | IDESC_B_MN_MAJOR;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = sdesc_sw128(smem_u32(sm + OFF_VNT + ks * 32));
-          umma_f16(tmem + TM_P, sdesc_sw128(smem_u32(set + OFF_KRT + ks * 32)), bd, idesc_p, ks != 0);
-          umma_f16(tmem + TM_O0 + 32 * s, sdesc_sw128(smem_u32(set + OFF_AQK + ks * 32)), bd, idesc_o, 1u);
+          const uint64_t bd = sdesc(smem_u32(sm + OFF_VNT + ks * 1024), 4096, 512, 4);
+          umma_f16(tmem + TM_P, sdesc_sw128(smem_u32(slot + R_KRT + ks * 32)), bd, idesc_p, ks != 0);
+          umma_f16(tmem + TM_O0 + 32 * s, sdesc_sw128(smem_u32(slot + R_AQK + ks * 32)), bd, idesc_o, 1u);
         }
-        umma_commit(&bars[BAR_B]);
+        umma_commit(&bars[B_B]);
         ++b_issued;
       }
       __syncwarp();
-      if (!mbar_wait(&bars[BAR_B], n & 1, WAIT_LIMIT_NS)) timeout();
+      if (!mbar_wait(&bars[B_B], m & 1, WAIT_LIMIT_NS)) timeout();
       ++b_done;
       tc_fence_after();
       PROF(3);
-      // ---- S <- Diag(e^{g_last}) S + P ; refresh S^T ----
+      // ---- S <- Diag(e^{g_last}) S + P ; refresh the bf16 copy ----
       __syncwarp();
       {
         float pr[32];
         tmem_ld32(tmem_addr(tmem, 32 * qw, TM_P), pr);
         tmem_ld_wait();
-        const float gmm = gam[s * KD + d];
+        const float gmm = reinterpret_cast<const float*>(slot + S_GAM)[d];
 #pragma unroll
-        for (int j = 0; j < VS; ++j) st[j] = fmaf(gmm, st[j], pr[j]);
+        for (int jj = 0; jj < VS; ++jj) st[jj] = fmaf(gmm, st[jj], pr[jj]);
         write_st();
       }
-      PROF(4);
-      // ---- o rows of this chunk ----
-      {
-        float orr[32];
-        tmem_ld32(tmem_addr(tmem, 32 * qw, TM_O0 + 32 * s), orr);
-        tmem_ld_wait();
-        const int c = 16 * qw + lane;
-        if (lane < 16 && c < rows) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok0 + n * C + c) * HV + hv) * VD + v0);
-#pragma unroll
-          for (int j8 = 0; j8 < VS / 8; ++j8)
-            dst[j8] = make_uint4(pack2(orr[8 * j8], orr[8 * j8 + 1]), pack2(orr[8 * j8 + 2], orr[8 * j8 + 3]),
-                                 pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]), pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
-        }
-      }
-      PROF(5);
       fence_proxy_async_smem();
       tc_fence_before();
-      if (named_bar_any(NB_CHAIN, 128, failed)) {
+      if (role_any(NB_CHAIN, failed)) {
         aborted = true;
         break;
       }
-      if (qt == 0) mbar_arrive(&bars[BAR_FREE0 + s]);
-      PROF(6);
+      PROF(4);
+      tc_fence_before();
+      role_sync(NB_CHAIN);  // slot s is free again
+      if (qt == 0 && !failed) pump_loads(m + 1, false);
+      PROF(5);
     }
-    if (qt == 0) {  // drain MMAs still in flight after an abort
-      if (a_issued > a_done && !mbar_wait(&bars[BAR_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
+    if (!aborted && !failed && NT > 0) {
+      __syncwarp();
+      emit_o(NT - 1);
+    }
+    if (qt == 0) {  // drain copies and MMAs still in flight after an abort
+      if (a_issued > a_done && !mbar_wait(&bars[B_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
-      if (b_issued > b_done && !mbar_wait(&bars[BAR_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
+      if (b_issued > b_done && !mbar_wait(&bars[B_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
+      for (int m = loads_done; m < next_load; ++m)
+        if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
       PROF_STORE(16);
     }
-    if (p.sfin && !aborted) {
+    __syncwarp();
+    if (p.sfin && !aborted && !failed) {
       float4* dst = reinterpret_cast<float4*>(p.sfin + state_off + static_cast<size_t>(d) * VD + v0);
 #pragma unroll
       for (int j4 = 0; j4 < VS / 4; ++j4)
@@ -637,6 +809,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no CTA leaves while a peer may still arrive on its barriers
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -655,21 +828,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// 3-D map over a [tokens, heads, dim] bf16 tensor with a (box_x, 1, 64) box.
-bool make_map(CUtensorMap* m, const void* base, int dim, int heads, long tokens, int box_x, bool swizzle) {
+// 3-D map over a [tokens, heads, dim] bf16 tensor with a (64, 1, 64) box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int dim, int heads, long tokens) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(tokens)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 2, static_cast<cuuint64_t>(heads) * dim * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), 1, static_cast<cuuint32_t>(C)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(C)};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc
+
+size_t chunk_tc_ring_bytes(int num_seqs, int HV) {
+  return static_cast<size_t>(num_seqs) * HV * tc::RING * tc::GSLOT;
+}
 
 bool chunk_tc_supported(const FwdParams& p, bool bf16) {
   const long tokens = p.cu ? static_cast<long>(p.T) : static_cast<long>(p.num_seqs) * p.T;
@@ -679,9 +856,8 @@ bool chunk_tc_supported(const FwdParams& p, bool bf16) {
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
   const long tokens = p.cu ? static_cast<long>(p.T) : static_cast<long>(p.num_seqs) * p.T;
   tc::Maps maps;
-  if (!tc::make_map(&maps.q, p.q, tc::KD, p.H, tokens, 64, true) ||
-      !tc::make_map(&maps.k, p.k, tc::KD, p.H, tokens, 64, true) ||
-      !tc::make_map(&maps.v, p.v, tc::VD, p.HV, tokens, tc::VS, false))
+  if (!tc::make_map(&maps.q, p.q, tc::KD, p.H, tokens) || !tc::make_map(&maps.k, p.k, tc::KD, p.H, tokens) ||
+      !tc::make_map(&maps.v, p.v, tc::VD, p.HV, tokens))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {

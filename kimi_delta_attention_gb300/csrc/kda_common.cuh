@@ -12,8 +12,10 @@ namespace kda {
 constexpr uint32_t kStatusTimeout = 1u;   // a bounded on-chip wait gave up
 constexpr uint32_t kStatusBounds = 2u;    // cu_seqlens entry out of order / range
 
-// Workspace layout: [0, 4) status word; the rest is reserved.
-constexpr size_t kWorkspaceBytes = 256;
+// Workspace layout: [0, 4) status word, [8, 264) optional profile counters;
+// the tensor-core chunk kernel's record ring starts at kRingOffset.
+constexpr size_t kWorkspaceBytes = 256;   // minimum (status word only)
+constexpr size_t kRingOffset = 1024;
 
 struct FwdParams {
   const void* q;         // [tokens, H, K]   io type
@@ -26,6 +28,7 @@ struct FwdParams {
   void* out;             // [tokens, HV, V]  io type
   float* sfin;           // [NS, HV, K, V] or null
   uint32_t* status;      // device status word
+  uint8_t* ring;         // per-(sequence, value head) record ring (chunk kernel), or null
   float scale;
   int T;                 // tokens per sequence (fixed length) or packed total
   int H, HV, K, V;
