@@ -52,7 +52,8 @@ typedef enum {
   KDA_ERR_CUDA = 4,            /* a CUDA runtime call failed (launch, attribute, ...) */
   KDA_ERR_DEVICE_TIMEOUT = 5,  /* device status: a bounded on-chip wait gave up */
   KDA_ERR_WORKSPACE = 6,       /* workspace missing or smaller than required */
-  KDA_ERR_DEVICE_BOUNDS = 7    /* device status: cu_seqlens out of order or out of range */
+  KDA_ERR_DEVICE_BOUNDS = 7,   /* device status: cu_seqlens out of order or out of range */
+  KDA_ERR_STATIC_SCRATCH = 8   /* problem larger than kda_chunk_fwd_static_scratch can hold */
 } kda_status;
 
 typedef struct {
@@ -130,6 +131,45 @@ KDA_API const char* kda_status_string(kda_status status);
 
 /* Chunk size used by the tensor-core kernel (tokens per chunk). */
 KDA_API int kda_chunk_size(void);
+
+/*
+ * kda_chunk_fwd without a caller-provided workspace.  (Not part of the method
+ * on the pages: it is a convenience of this library.)
+ *
+ * Some callers cannot allocate device memory at the point where they run the
+ * forward: a host framework that owns every device allocation through its own
+ * pool and exposes none of it, a plugin called from code that must not pay
+ * for cudaMalloc's implicit device synchronisation, or a latency-critical
+ * loop that forbids allocation after start-up.  For them this entry point
+ * takes the same inputs and outputs as kda_chunk_fwd but keeps its scratch
+ * (the device status word and the chunk kernel's record rings) in one
+ * fixed-size array compiled into the library, on every device that loads the
+ * library, for the life of the process: about 36.5 MiB
+ * (KDA_STATIC_SCRATCH_MAX_UNITS record rings + 1 KiB).
+ *
+ *   - Capacity: at most KDA_STATIC_SCRATCH_MAX_UNITS (sequence, value head)
+ *     pairs per call (num_seqs or B, times HV); larger problems return
+ *     KDA_ERR_STATIC_SCRATCH before anything is enqueued.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *     The first call on each device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress) and caches it; make that first call outside any
+ *     stream capture.  Later calls only enqueue a 4-byte memset of the status
+ *     word and the kernel.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; the status word is cleared at the start of each call and the
+ *     rings need no clearing.  Calls whose work overlaps on the GPU (other
+ *     streams, other host threads) race on the array and corrupt each other:
+ *     order them on one stream.
+ *   - status_word: if not NULL, receives the device address of the status
+ *     word, to pass to kda_read_device_status().
+ */
+#define KDA_STATIC_SCRATCH_MAX_UNITS 32
+KDA_API kda_status kda_chunk_fwd_static_scratch(const kda_shape* shape, const void* q, const void* k,
+                                                const void* v, const float* g, const float* beta,
+                                                float scale, const float* initial_state,
+                                                const int32_t* cu_seqlens, void* out,
+                                                float* final_state, void* stream,
+                                                void** status_word);
 
 #ifdef __cplusplus
 }

@@ -24,11 +24,14 @@ KDA_BF16 = 1
 STATUS_NAMES = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIGNMENT",
     4: "KDA_ERR_CUDA", 5: "KDA_ERR_DEVICE_TIMEOUT", 6: "KDA_ERR_WORKSPACE", 7: "KDA_ERR_DEVICE_BOUNDS",
+    8: "KDA_ERR_STATIC_SCRATCH",
 }
+STATIC_SCRATCH_MAX_UNITS = 32
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
-           "kda_read_device_status", "kda_status_string", "kda_chunk_size")
+           "kda_read_device_status", "kda_status_string", "kda_chunk_size",
+           "kda_chunk_fwd_static_scratch")
 
 
 class KdaError(RuntimeError):
@@ -71,6 +74,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_chunk_size.argtypes = []
         lib.kda_chunk_size.restype = I
+        lib.kda_chunk_fwd_static_scratch.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, P, P,
+                                                     ctypes.POINTER(ctypes.c_void_p)]
+        lib.kda_chunk_fwd_static_scratch.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -155,3 +161,33 @@ def kda_read_device_status(workspace, stream=None) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(workspace.device).cuda_stream
     return int(load_library().kda_read_device_status(_ptr(workspace), ctypes.c_void_p(stream)))
+
+
+def kda_chunk_fwd_static_scratch(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                                 out=None, final_state=None, output_final_state=True, stream=None):
+    """kda_chunk_fwd for callers that cannot hand over device scratch: the library's
+    fixed array holds it (at most 32 (sequence, value head) pairs per call; calls
+    that overlap on the GPU race).  Returns (o, final_state, status_word_address)."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise KdaError(1, f"{name} must be a contiguous CUDA tensor")
+    shape = make_shape(q, v, cu_seqlens)
+    K = q.shape[3]
+    if scale is None:
+        scale = K ** -0.5
+    NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
+    HV, V = v.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((NS, HV, K, V), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    status = ctypes.c_void_p()
+    code = lib.kda_chunk_fwd_static_scratch(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.c_void_p(stream),
+        ctypes.byref(status))
+    _check(code)
+    return out, final_state, status.value

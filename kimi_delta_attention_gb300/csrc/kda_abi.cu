@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
@@ -110,6 +111,31 @@ kda_status run(bool use_tc, const kda_shape* s, const void* q, const void* k, co
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// ---- fixed scratch for kda_chunk_fwd_static_scratch ----
+constexpr size_t kStaticScratchBytes =
+    kda::kRingOffset + static_cast<size_t>(KDA_STATIC_SCRATCH_MAX_UNITS) * kda::kRingBytesPerUnit;
+
+// One copy per device that loads the library, alive until the process exits.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+uint8_t* g_static_ptr[kMaxDevices] = {};
+
+// Device address of the current device's array; looked up once per device
+// with that device current (host code may not use the symbol itself).
+uint8_t* static_scratch_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return nullptr;
+    g_static_ptr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  return g_static_ptr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -154,10 +180,26 @@ const char* kda_status_string(kda_status status) {
     case KDA_ERR_DEVICE_TIMEOUT: return "device: a bounded on-chip wait timed out";
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_DEVICE_BOUNDS: return "device: cu_seqlens out of order or out of range";
+    case KDA_ERR_STATIC_SCRATCH: return "more (sequence, value head) pairs than the static scratch holds";
   }
   return "unknown status";
 }
 
 int kda_chunk_size(void) { return 64; }
+
+kda_status kda_chunk_fwd_static_scratch(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                        const float* g, const float* beta, float scale,
+                                        const float* initial_state, const int32_t* cu_seqlens, void* out,
+                                        float* final_state, void* stream, void** status_word) {
+  if (!shape) return KDA_ERR_INVALID_ARG;
+  const long ns = shape->num_seqs > 0 ? shape->num_seqs : shape->B;
+  if (ns < 0 || shape->HV < 1) return KDA_ERR_INVALID_ARG;
+  if (ns * static_cast<long>(shape->HV) > KDA_STATIC_SCRATCH_MAX_UNITS) return KDA_ERR_STATIC_SCRATCH;
+  uint8_t* scratch = static_scratch_current_device();
+  if (!scratch) return KDA_ERR_CUDA;
+  if (status_word) *status_word = scratch;
+  return run(true, shape, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, scratch,
+             kStaticScratchBytes, stream);
+}
 
 }  // extern "C"

@@ -844,6 +844,8 @@ bool make_map(CUtensorMap* m, const void* base, int dim, int heads, long tokens)
 
 }  // namespace tc
 
+static_assert(static_cast<size_t>(tc::RING) * tc::GSLOT == kRingBytesPerUnit, "ring layout");
+
 size_t chunk_tc_ring_bytes(int num_seqs, int HV) {
   return static_cast<size_t>(num_seqs) * HV * tc::RING * tc::GSLOT;
 }

@@ -16,6 +16,7 @@ constexpr uint32_t kStatusBounds = 2u;    // cu_seqlens entry out of order / ran
 // the tensor-core chunk kernel's record ring starts at kRingOffset.
 constexpr size_t kWorkspaceBytes = 256;   // minimum (status word only)
 constexpr size_t kRingOffset = 1024;
+constexpr size_t kRingBytesPerUnit = 16 * 74752;  // record ring of one (sequence, value head)
 
 struct FwdParams {
   const void* q;         // [tokens, H, K]   io type
