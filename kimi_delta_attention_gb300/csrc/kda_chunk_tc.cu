@@ -51,16 +51,20 @@ constexpr int KD = 128;       // key dim
 constexpr int VD = 128;       // value dim
 constexpr int VS = 32;        // value columns per CTA
 constexpr int NSLICE = VD / VS;
-constexpr int NTHREADS = 256; // 4 producer warps, 4 chain warps
+constexpr int NTHREADS = 384; // 8 producer warps, 4 chain warps
+constexpr uint32_t NPROD = 256, NCHAIN = 128;
 constexpr int MB_LD = 68;     // padded row stride (floats) of the fp32 inverse buffer
 constexpr int RING = 16;      // record slots per head in the workspace ring
 
 // ---- record layout (global ring slot and shared slot share the first part) ----
-constexpr uint32_t R_QD = 0;          // [64 x 128] bf16 SW128
-constexpr uint32_t R_WM = 16384;      // [64 x 128] bf16 SW128
+// [W; qd] as one 128-row K-major operand: per 64-column K-block kb, W's 64
+// rows (8 KB) then qd's 64 rows (8 KB), so X = W S and qd S are one M=128 MMA.
+constexpr uint32_t R_WQ = 0;          // 2 K-blocks x [W rows | qd rows] bf16 SW128
+constexpr uint32_t R_W_KB = 16384;    // stride between the K-blocks
+constexpr uint32_t R_QD_IN_KB = 8192; // qd rows inside a K-block
 constexpr uint32_t R_KRT = 32768;     // [128 x 64] bf16 SW128 (kr transposed)
-constexpr uint32_t R_AQK = 49152;     // [64 x 64]  bf16 SW128
-constexpr uint32_t R_TILES = 57344;   // bytes of the four tiles above
+constexpr uint32_t R_AQK = 49152;     // [64 x 64]  bf16 SW128, right after kr^T rows 64..127
+constexpr uint32_t R_TILES = 57344;   // bytes of the tiles above
 constexpr uint32_t G_U = 57344;       // global: 4 slices of U, each [64 x 32] bf16 row-major
 constexpr uint32_t G_GAM = 57344 + 4 * 4096;  // global: e^{g_last} [128] fp32
 constexpr uint32_t GSLOT = 74752;             // global slot stride (1024-multiple)
@@ -77,13 +81,14 @@ constexpr uint32_t OFF_PV = OFF_PKD + 16384;              // 157696 raw v [64 x 
 constexpr uint32_t OFF_PB = OFF_PV + 16384;               // 174080 ki (raw k) | later M fp32 + A bf16
 constexpr uint32_t OFF_MB = OFF_PB;                       //        [64 x 68] fp32
 constexpr uint32_t OFF_AMAT = OFF_PB + 17408;             // 191488 [64 x 64] bf16 SW128; before it is
-constexpr uint32_t OFF_RS = OFF_AMAT;                     //        written: Aqk staging, then [16 x 48] fp32
-constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB staging: kr^T, later U slices
+constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB staging: kr^T, inverse scratch, U slices
+constexpr uint32_t OFF_RS = OFF_STG;                      //        8 x [16 x 8] fp32 scratch of the inverse
 constexpr uint32_t OFF_ST = OFF_STG + 16384;              // 216064 S  [128 x 32] bf16 MN-major SW64
 constexpr uint32_t OFF_VNT = OFF_ST + 8192;               // 224256 v_new [64 x 32] bf16 MN-major SW64
 constexpr uint32_t OFF_BETA = OFF_VNT + 4096;             // 228352 [64] fp32
-constexpr uint32_t OFF_BAR = OFF_BETA + 256;              // 228608 mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 228864 tmem base
+constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 228608 [2][128] fp32 half-chunk sums of g
+constexpr uint32_t OFF_BAR = OFF_GSUM + 1024;             // 229632 mbarriers
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 229888 tmem base
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;        // + alignment slack
 
@@ -94,10 +99,15 @@ constexpr int B_ACK = 10;    // [2] this CTA's record j loaded by all 4 CTAs: in
 constexpr int B_RAW = 12;    // producer raw q/k/v (tx)
 constexpr int B_PMMA = 13;   // producer MMA commits
 constexpr int B_A = 14;      // chain X/O MMA commit
-constexpr int B_B = 15;      // chain P/O MMA commit
+constexpr int B_B = 15;      // chain P MMA commit
+constexpr int B_C = 16;      // chain O += Aqk v_new commit
 
 // TMEM columns
-constexpr uint32_t TM_L = 0, TM_AQ = 64, TM_W = 0, TM_U = 128, TM_X = 256, TM_O0 = 288, TM_P = 352;
+// chain: X and P are each split over two accumulators (K halves) to shorten the
+// dependent MMA chains; O is double-buffered across chunks
+// chain: D_A[m & 1] holds X = W S in lanes 0-63 and o (qd S + Aqk v_new) in lanes
+// 64-127, double-buffered across chunks; P = kr^T v_new
+constexpr uint32_t TM_L = 0, TM_AQ = 64, TM_W = 0, TM_U = 128, TM_A0 = 256, TM_P = 320;
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t RAW_TX_BYTES = 3 * 16384;        // q, k, v tiles
@@ -155,51 +165,70 @@ __device__ __forceinline__ void st_v4_global(void* p, uint32_t a, uint32_t b, ui
 }
 
 // Role barriers: reconverge the warp first (bar.sync / bar.red are .aligned).
-__device__ __forceinline__ void role_sync(uint32_t id) {
+__device__ __forceinline__ void role_sync(uint32_t id, uint32_t count) {
   __syncwarp();
-  named_bar_sync(id, 128);
+  named_bar_sync(id, count);
 }
-__device__ __forceinline__ bool role_any(uint32_t id, bool pred) {
+__device__ __forceinline__ bool role_any(uint32_t id, uint32_t count, bool pred) {
   __syncwarp();
-  return named_bar_any(id, 128, pred);
+  return named_bar_any(id, count, pred);
 }
 
-// One block row (16 rows starting at 16*BI) of T = (I + M)^{-1}, with the rows
-// above already final in `mb` (M below the diagonal blocks, T elsewhere):
-//   R      = M[16BI.., 0..16BI) T[0..16BI, 0..16BI)
-//   T_row  = -T_ii R
-template <int BI>
-__device__ __forceinline__ void inverse_block_row(float* mb, float* rs, int pt) {
-  constexpr int NCOL = 16 * BI;
-  constexpr int PER = 2 * BI;
-  const int r = pt >> 3;
-  const int c0 = (pt & 7) * PER;
-  const float* mrow = mb + (16 * BI + r) * MB_LD;
-  float acc[PER];
+// Off-diagonal blocks of T = (I + M)^{-1} (64 x 64, 16 x 16 blocks), given the
+// inverted diagonal blocks T_ii on the diagonal of `mb` and M below it: block
+// column w is walked down its block rows i > w,
+//     T_iw = -T_ii sum_{k = w}^{i-1} M_ik T_kw,
+// which needs only column w itself and the diagonal blocks, so the two warps that
+// share a block column (8 columns each) run without block-wide barriers.  T_iw is
+// kept in the unused block (w, i) above the diagonal (row 16 w + r holds row r of
+// T_iw), so no warp overwrites M that another warp still reads, and block (w, k),
+// k >= w, is T_kw for the diagonal block as well.  Each T value is also written,
+// scaled by beta of its column, into the bf16 A tile.
+// Warp `pw` (0..7): block column w = pw & 3, columns 16 w + 8 (pw >> 2) + [0, 8);
+// lane: row l >> 1, columns +4 (l & 1) + [0, 4).  `rs`: 8 x [16 x 8] fp32 scratch.
+__device__ __forceinline__ void inverse_block_columns(float* mb, float* rs, const float* beta_s, uint8_t* amat,
+                                                      int pw, int lane) {
+  const int w = pw & 3;
+  const int c0 = 8 * (pw >> 2) + 4 * (lane & 1);  // this lane's first column within the block
+  const int r = lane >> 1;                        // row within a block
+  float* my_rs = rs + pw * 128;                   // [16 rows][8 cols]
+  const float* tcol = mb + 16 * w * MB_LD + c0;   // T_kw[rr][c0 + e] = tcol[rr * MB_LD + 16 k + e]
+  for (int i = w + 1; i < 4; ++i) {
+    // R = sum_{k = w}^{i-1} M_ik T_kw   (row r, columns c0 + [0, 4))
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* mrow = mb + (16 * i + r) * MB_LD;
+    for (int k = w; k < i; ++k) {
 #pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+      for (int rr = 0; rr < 16; ++rr) {
+        const float a = mrow[16 * k + rr];
+        const float4 t4 = *reinterpret_cast<const float4*>(tcol + rr * MB_LD + 16 * k);
+        acc[0] = fmaf(a, t4.x, acc[0]);
+        acc[1] = fmaf(a, t4.y, acc[1]);
+        acc[2] = fmaf(a, t4.z, acc[2]);
+        acc[3] = fmaf(a, t4.w, acc[3]);
+      }
+    }
+    *reinterpret_cast<float4*>(my_rs + r * 8 + (c0 & 7)) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    __syncwarp();
+    // T_iw = -T_ii R  (T_ii lower triangular)
+    float t[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* trow = mb + (16 * i + r) * MB_LD + 16 * i;
 #pragma unroll
-  for (int k = 0; k < NCOL; ++k) {
-    const float a = mrow[k];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = fmaf(a, mb[k * MB_LD + c0 + e], acc[e]);
+    for (int mm = 0; mm < 16; ++mm) {
+      const float a = trow[mm];
+      const float4 r4 = *reinterpret_cast<const float4*>(my_rs + mm * 8 + (c0 & 7));
+      t[0] = fmaf(a, r4.x, t[0]);
+      t[1] = fmaf(a, r4.y, t[1]);
+      t[2] = fmaf(a, r4.z, t[2]);
+      t[3] = fmaf(a, r4.w, t[3]);
+    }
+    *reinterpret_cast<float4*>(mb + (16 * w + r) * MB_LD + 16 * i + c0) = make_float4(-t[0], -t[1], -t[2], -t[3]);
+    const int col = 16 * w + c0;
+    uint32_t* a2 = reinterpret_cast<uint32_t*>(amat + sw128_offset(16 * i + r, col, 64));
+    a2[0] = pack2(-t[0] * beta_s[col], -t[1] * beta_s[col + 1]);
+    a2[1] = pack2(-t[2] * beta_s[col + 2], -t[3] * beta_s[col + 3]);
+    __syncwarp();  // R read by every lane before it is rewritten; T_iw visible to later rows
   }
-#pragma unroll
-  for (int e = 0; e < PER; ++e) rs[r * 48 + c0 + e] = acc[e];
-  role_sync(NB_PREP);
-  const float* trow = mb + (16 * BI + r) * MB_LD + 16 * BI;
-  float t[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) t[e] = 0.f;
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const float a = trow[m];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) t[e] = fmaf(a, rs[m * 48 + c0 + e], t[e]);
-  }
-#pragma unroll
-  for (int e = 0; e < PER; ++e) mb[(16 * BI + r) * MB_LD + c0 + e] = -t[e];
-  role_sync(NB_PREP);
 }
 
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
@@ -210,6 +239,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   float* beta_s = reinterpret_cast<float*>(sm + OFF_BETA);
   float* mb = reinterpret_cast<float*>(sm + OFF_MB);
+  float* gsum = reinterpret_cast<float*>(sm + OFF_GSUM);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hv = blockIdx.y, seq = blockIdx.z;
@@ -234,6 +264,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     mbar_init(&bars[B_PMMA], 1);
     mbar_init(&bars[B_A], 1);
     mbar_init(&bars[B_B], 1);
+    mbar_init(&bars[B_C], 1);
     fence_mbar_init();
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.k);
@@ -248,12 +279,24 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   cluster_sync_all();  // every CTA's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Shared-memory matrix descriptors, built once: adding (byte offset >> 4) to a
+  // descriptor moves its start address (all addresses stay below 256 KB).
+  const uint32_t sbase = smem_u32(sm);
+  const uint64_t D_SW128 = sdesc_sw128(sbase);                        // K-major, 128-B swizzle
+  const uint64_t D_ST = sdesc(sbase + OFF_ST, 8192, 512, 4);          // S, MN-major 64-B swizzle
+  const uint64_t D_VNT = sdesc(sbase + OFF_VNT, 4096, 512, 4);        // v_new, MN-major 64-B swizzle
+  const uint64_t D_KD_MN = sdesc(sbase + OFF_PKD, 8192, 1024, 2);     // kd as MN-major B
+  const uint64_t D_V_MN = sdesc(sbase + OFF_PV, 8192, 1024, 2);       // v as MN-major B
+  auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
   const size_t state_off = (static_cast<size_t>(seq) * HV + hv) * KD * VD;
 
-  if (warp < 4) {
+  if (warp < NPROD / 32) {
     // ============================== producer ===============================
-    const int pt = tid;   // key dim owned in the elementwise pass
-    const int pw = warp;  // TMEM lane quadrant
+    const int pt = tid;           // 0..255
+    const int dim = pt & 127;     // key dim owned in the elementwise pass
+    const int hr = pt >> 7;       // ... for rows [32 hr, 32 hr + 32)
+    const int quad = warp & 3;    // TMEM lane quadrant of this warp
+    const int cpart = warp >> 2;  // which half of a readout this warp takes
     const float scale = p.scale;
     uint32_t pmma_phase = 0, pmma_issued = 0;
     bool raw_pending = false;
@@ -277,16 +320,19 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       raw_pending = true;
       raw_pending_j = j;
     };
-    float gpre[C];
+    // g of this thread's 32 rows (and beta) arrive in registers in four 8-row
+    // parts issued at different points of the previous chunk, so that few loads
+    // are in flight at once
+    float gpre[32];
     float bpre = 0.f;
-    // g (and beta) of a chunk arrive in registers in four 16-row parts issued at
-    // different points of the previous chunk, so that few loads are in flight at once
     auto prefetch_gb = [&](int m, int part) {
       const int rows = min(C, len - m * C);
       const long base = tok0 + static_cast<long>(m) * C;
 #pragma unroll
-      for (int c = 16 * part; c < 16 * part + 16; ++c)
-        gpre[c] = (c < rows) ? __ldg(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD + pt) : 0.f;
+      for (int i = 8 * part; i < 8 * part + 8; ++i) {
+        const int c = 32 * hr + i;
+        gpre[i] = (c < rows) ? __ldg(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD + dim) : 0.f;
+      }
       if (part == 0 && pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
     };
     bool pub_pending = false;  // record j-1 stored but not yet published
@@ -312,34 +358,40 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     for (int m = first; m < NT; m += NSLICE, ++j) {
       uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
       const int rows = min(C, len - m * C);
+      const bool next = m + NSLICE < NT;
       // ---- 1. raw q, k, v of chunk m ----
       if (!mbar_wait(&bars[B_RAW], j & 1, WAIT_LIMIT_NS)) timeout();
       if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
-      if (role_any(NB_PREP, failed)) break;
+      if (pt < C) beta_s[pt] = bpre;
+      {
+        float hsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) hsum += gpre[i];
+        gsum[hr * KD + dim] = hsum;
+      }
+      if (role_any(NB_PREP, NPROD, failed)) break;
       if (pt == 0) raw_pending = false;
       PROF(0);
 
       // ---- 2. elementwise: cumsum, decayed operands; kr^T and e^{g_last} to the record ----
-      if (pt < C) beta_s[pt] = bpre;
-      float glast = 0.f;
-#pragma unroll
-      for (int c = 0; c < C; ++c) glast += gpre[c];
-      const float gamma = __expf(glast);
-      __stcg(reinterpret_cast<float*>(gs + G_GAM) + pt, gamma);
       {
-        float gc = 0.f;
+        const float g0 = gsum[dim];
+        const float glast = g0 + gsum[KD + dim];
+        const float gamma = __expf(glast);
+        if (hr == 0) __stcg(reinterpret_cast<float*>(gs + G_GAM) + dim, gamma);
+        float gc = hr ? g0 : 0.f;
         uint8_t* qd_t = sm + OFF_PQD;
         uint8_t* ki_t = sm + OFF_PB;
         uint8_t* kd_t = sm + OFF_PKD;
-        const uint32_t col_part = (pt >> 6) * 8192u + ((pt & 7) << 1);
-        const uint32_t chunk_part = (pt >> 3) & 7u;
+        const uint32_t col_part = (dim >> 6) * 8192u + ((dim & 7) << 1);
+        const uint32_t chunk_part = (dim >> 3) & 7u;
 #pragma unroll
-        for (int c8 = 0; c8 < C / 8; ++c8) {
+        for (int c8 = 0; c8 < 4; ++c8) {
           uint16_t kraw[8], qraw[8];
           uint32_t off[8];
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
-            const int c = c8 * 8 + cc;
+            const int c = 32 * hr + c8 * 8 + cc;
             off[cc] = col_part + c * 128u + ((chunk_part ^ (c & 7)) << 4);
             kraw[cc] = *reinterpret_cast<const uint16_t*>(ki_t + off[cc]);
             qraw[cc] = *reinterpret_cast<const uint16_t*>(qd_t + off[cc]);
@@ -347,8 +399,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
           float kdv[8], kiv[8], qdv[8], krv[8];
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
-            const int c = c8 * 8 + cc;
-            gc += gpre[c];
+            const int c = 32 * hr + c8 * 8 + cc;
+            gc += gpre[c8 * 8 + cc];
             const float e = __expf(gc);
             const float ie = __expf(-gc);
             const bool valid = c < rows;
@@ -365,15 +417,15 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
             *reinterpret_cast<uint16_t*>(ki_t + off[cc]) = f2bf(kiv[cc]);
             *reinterpret_cast<uint16_t*>(qd_t + off[cc]) = f2bf(qdv[cc]);
           }
-          st_v4(sm + OFF_STG + sw128_offset(pt, c8 * 8, 128), pack2(krv[0], krv[1]), pack2(krv[2], krv[3]),
-                pack2(krv[4], krv[5]), pack2(krv[6], krv[7]));
+          st_v4(sm + OFF_STG + sw128_offset(dim, 32 * hr + c8 * 8, 128), pack2(krv[0], krv[1]),
+                pack2(krv[2], krv[3]), pack2(krv[4], krv[5]), pack2(krv[6], krv[7]));
         }
       }
       fence_proxy_async_smem();
-      role_sync(NB_PREP);
+      role_sync(NB_PREP, NPROD);
       PROF(1);
 
-      // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd tile to the record ----
+      // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd and kr^T tiles to the record ----
       if (pt == 0) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_f16kind(64, 64);
@@ -382,120 +434,122 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t koff = kb * 8192 + ks * 32;
-            const uint64_t bd = sdesc_sw128(smem_u32(sm + OFF_PB + koff));
-            umma_f16(tmem + TM_L, sdesc_sw128(smem_u32(sm + OFF_PKD + koff)), bd, idesc, (kb | ks) != 0);
-            umma_f16(tmem + TM_AQ, sdesc_sw128(smem_u32(sm + OFF_PQD + koff)), bd, idesc, (kb | ks) != 0);
+            const uint64_t bd = d128(OFF_PB + koff);
+            umma_f16(tmem + TM_L, d128(OFF_PKD + koff), bd, idesc, (kb | ks) != 0);
+            umma_f16(tmem + TM_AQ, d128(OFF_PQD + koff), bd, idesc, (kb | ks) != 0);
           }
         umma_commit(&bars[B_PMMA]);
         ++pmma_issued;
-        bulk_store(gs + R_QD, sm + OFF_PQD, 16384);
+        bulk_store(gs + R_WQ + R_QD_IN_KB, sm + OFF_PQD, 8192);
+        bulk_store(gs + R_WQ + R_W_KB + R_QD_IN_KB, sm + OFF_PQD + 8192, 8192);
         bulk_store(gs + R_KRT, sm + OFF_STG, 16384);
         bulk_commit();
-        if (pub_pending) {  // the previous record's W/U stores (the older group) are complete
-          bulk_wait_group<1>();
-          publish(j - 1);
-          pub_pending = false;
-        }
       }
-      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 0);
+      if (next) prefetch_gb(m + NSLICE, 0);
       __syncwarp();
       if (!mbar_wait(&bars[B_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
       ++pmma_phase;
       tc_fence_after();
+      if (pt == 0) bulk_wait_read();  // qd (about to hold the Aqk staging) and kr^T have been read
       PROF(2);
 
-      // ---- 4. TMEM -> M (fp32, rows scaled by beta, strictly lower), Aqk -> record ----
-      __syncwarp();
+      // ---- 4. TMEM -> M (fp32, rows scaled by beta, strictly lower), Aqk -> staging ----
+      role_sync(NB_PREP, NPROD);
       {
-        const int i = 16 * pw + (lane & 15);
-        float r[32];
+        const int i = 16 * quad + (lane & 15);
+        const int j0 = 32 * cpart;  // this warp's 32 columns
+        float rl[32], ra[32];
+        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_L + j0), rl);
+        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_AQ + j0), ra);
+        tmem_ld_wait();
+        if (lane < 16) {
+          const float bi = beta_s[i];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_L + 32 * half), r);
-          tmem_ld_wait();
-          if (lane < 16) {
-            const float bi = beta_s[i];
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              float4 v4;
-              const int jj = 32 * half + 4 * j4;
-              v4.x = (jj + 0 < i) ? bi * r[4 * j4 + 0] : 0.f;
-              v4.y = (jj + 1 < i) ? bi * r[4 * j4 + 1] : 0.f;
-              v4.z = (jj + 2 < i) ? bi * r[4 * j4 + 2] : 0.f;
-              v4.w = (jj + 3 < i) ? bi * r[4 * j4 + 3] : 0.f;
-              *reinterpret_cast<float4*>(mb + i * MB_LD + jj) = v4;
-            }
+          for (int j4 = 0; j4 < 8; ++j4) {
+            float4 v4;
+            const int jj = j0 + 4 * j4;
+            v4.x = (jj + 0 < i) ? bi * rl[4 * j4 + 0] : 0.f;
+            v4.y = (jj + 1 < i) ? bi * rl[4 * j4 + 1] : 0.f;
+            v4.z = (jj + 2 < i) ? bi * rl[4 * j4 + 2] : 0.f;
+            v4.w = (jj + 3 < i) ? bi * rl[4 * j4 + 3] : 0.f;
+            *reinterpret_cast<float4*>(mb + i * MB_LD + jj) = v4;
           }
-          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_AQ + 32 * half), r);
-          tmem_ld_wait();
-          if (lane < 16) {
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8) {
-              uint32_t w[4];
+          for (int j8 = 0; j8 < 4; ++j8) {
+            uint32_t w[4];
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const int jj = 32 * half + 8 * j8 + 2 * t;
-                w[t] = pack2((jj <= i) ? r[8 * j8 + 2 * t] : 0.f, (jj + 1 <= i) ? r[8 * j8 + 2 * t + 1] : 0.f);
-              }
-              st_v4(sm + OFF_AMAT + sw128_offset(i, 32 * half + 8 * j8, 64), w[0], w[1], w[2], w[3]);
+            for (int t = 0; t < 4; ++t) {
+              const int jj = j0 + 8 * j8 + 2 * t;
+              w[t] = pack2((jj <= i) ? ra[8 * j8 + 2 * t] : 0.f, (jj + 1 <= i) ? ra[8 * j8 + 2 * t + 1] : 0.f);
             }
+            st_v4(sm + OFF_PQD + sw128_offset(i, j0 + 8 * j8, 64), w[0], w[1], w[2], w[3]);
           }
         }
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      if (role_any(NB_PREP, failed)) break;
+      if (role_any(NB_PREP, NPROD, failed)) break;
       if (pt == 0) {
-        bulk_store(gs + R_AQK, sm + OFF_AMAT, 8192);
+        bulk_store(gs + R_AQK, sm + OFF_PQD, 8192);
         bulk_commit();
+        if (pub_pending) {  // the previous record's W/U stores are older than the last two groups
+          PROF(3);
+          bulk_wait_group<2>();
+          PROF(10);
+#ifdef KDA_PROFILE
+          if (j - 1 >= 2) mbar_wait_cluster(&bars[B_ACK + ((j - 1) & 1)], ((j - 3) >> 1) & 1, WAIT_LIMIT_NS);
+          PROF(12);
+#endif
+          publish(j - 1);
+          PROF(11);
+          pub_pending = false;
+        }
       }
-      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 1);
+      if (next) prefetch_gb(m + NSLICE, 1);
       PROF(3);
 
-      // ---- 5. T = (I + M)^{-1}: 16x16 diagonal blocks by forward substitution, then block rows ----
-      if (lane < 16) {
-        const int b0 = 16 * pw, jc = lane;
-        float acc[16];
+      // ---- 5. T = (I + M)^{-1} and A = T Diag(beta): 16x16 diagonal blocks by forward
+      //         substitution (warps 0-3), zero blocks above the diagonal (warps 4-7),
+      //         then block rows ----
+      uint8_t* amat = sm + OFF_AMAT;
+      if (warp < 4) {
+        if (lane < 16) {
+          const int b0 = 16 * warp, jc = lane;
+          float acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = (i == jc) ? 1.f : 0.f;
+          for (int i = 0; i < 16; ++i) acc[i] = (i == jc) ? 1.f : 0.f;
 #pragma unroll
-        for (int mm = 0; mm < 16; ++mm) {
-          const float xm = acc[mm];  // final: column jc of T, row mm
+          for (int mm = 0; mm < 16; ++mm) {
+            const float xm = acc[mm];  // final: column jc of T, row mm
 #pragma unroll
-          for (int i = mm + 1; i < 16; ++i) acc[i] = fmaf(-mb[(b0 + i) * MB_LD + b0 + mm], xm, acc[i]);
-        }
-        __syncwarp(0x0000FFFFu);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
-      }
-      if (pt == 0) bulk_wait_read();  // the Aqk staging (reused as scratch next) has been read
-      role_sync(NB_PREP);
-      PROF(4);
-      {
-        float* rs = reinterpret_cast<float*>(sm + OFF_RS);
-        inverse_block_row<1>(mb, rs, pt);
-        inverse_block_row<2>(mb, rs, pt);
-        inverse_block_row<3>(mb, rs, pt);
-      }
-      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 2);
-      PROF(5);
-      {  // A = T Diag(beta) -> bf16 SW128
-        const int i = pt >> 1, jb = (pt & 1) * 32;
-#pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int jj = jb + 8 * j8 + 2 * t;
-            const float a = (jj <= i) ? mb[i * MB_LD + jj] * beta_s[jj] : 0.f;
-            const float b = (jj + 1 <= i) ? mb[i * MB_LD + jj + 1] * beta_s[jj + 1] : 0.f;
-            w[t] = pack2(a, b);
+            for (int i = mm + 1; i < 16; ++i) acc[i] = fmaf(-mb[(b0 + i) * MB_LD + b0 + mm], xm, acc[i]);
           }
-          st_v4(sm + OFF_AMAT + sw128_offset(i, jb + 8 * j8, 64), w[0], w[1], w[2], w[3]);
+          __syncwarp(0x0000FFFFu);
+          const float bj = beta_s[b0 + jc];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
+            *reinterpret_cast<uint16_t*>(amat + sw128_offset(b0 + i, b0 + jc, 64)) = f2bf(acc[i] * bj);
+          }
+        }
+      } else {
+        // blocks (row block br, column block bc > br): 6 blocks of 16 x 16 bf16 zeros,
+        // 2 chunks of 8 columns per row -> 6 * 16 * 2 = 192 16-byte stores over 128 threads
+        const int q = pt - 128;
+        for (int idx = q; idx < 192; idx += 128) {
+          const int blk = idx >> 5, rem = idx & 31, row = rem >> 1, half = rem & 1;
+          const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+          const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+          st_v4(amat + sw128_offset(16 * br + row, 16 * bc + 8 * half, 64), 0u, 0u, 0u, 0u);
         }
       }
+      role_sync(NB_PREP, NPROD);
+      PROF(4);
+      inverse_block_columns(mb, reinterpret_cast<float*>(sm + OFF_RS), beta_s, amat, warp, lane);
+      if (next) prefetch_gb(m + NSLICE, 2);
       fence_proxy_async_smem();
-      role_sync(NB_PREP);
+      role_sync(NB_PREP, NPROD);
+      PROF(5);
       PROF(6);
 
       // ---- 6. W = A kd, U = A v (kd and v as MN-major B operands) ----
@@ -504,65 +558,63 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = sdesc_sw128(smem_u32(sm + OFF_AMAT + ks * 32));
-          umma_f16(tmem + TM_W, ad, sdesc(smem_u32(sm + OFF_PKD + ks * 2048), 8192, 1024, 2), idesc, ks != 0);
-          umma_f16(tmem + TM_U, ad, sdesc(smem_u32(sm + OFF_PV + ks * 2048), 8192, 1024, 2), idesc, ks != 0);
+          const uint64_t ad = d128(OFF_AMAT + ks * 32);
+          umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+          umma_f16(tmem + TM_U, ad, D_V_MN + ((ks * 2048) >> 4), idesc, ks != 0);
         }
         umma_commit(&bars[B_PMMA]);
         ++pmma_issued;
       }
+      if (next) prefetch_gb(m + NSLICE, 3);
       __syncwarp();
       if (!mbar_wait(&bars[B_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
       ++pmma_phase;
       tc_fence_after();
       // raw buffers are free again: fetch the next own chunk
-      if (pt == 0 && m + NSLICE < NT && !failed) {
-        bulk_wait_read();  // the qd tile store has read its source
+      if (pt == 0 && next && !failed) {
+        bulk_wait_read();  // the Aqk staging (in the q buffer) has been read
         issue_raw(m + NSLICE, j + 1);
       }
-      if (m + NSLICE < NT) prefetch_gb(m + NSLICE, 3);
       PROF(7);
 
-      // ---- 7. W -> record (bf16 SW128), U -> record (4 slices of [64 x 32] bf16) ----
+      // ---- 7. W -> staging (bf16 SW128), U -> staging (4 slices of [64 x 32] bf16) ----
       __syncwarp();
       {
-        const int i = 16 * pw + (lane & 15);
-        float r[32];
+        const int i = 16 * quad + (lane & 15);
+        const uint32_t tcol = cpart == 0 ? TM_W : TM_U;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_W + 32 * q4), r);
+        for (int q2 = 0; q2 < 4; q2 += 2) {
+          float r0[32], r1[32];
+          tmem_ld32(tmem_addr(tmem, 32 * quad, tcol + 32 * q2), r0);
+          tmem_ld32(tmem_addr(tmem, 32 * quad, tcol + 32 * (q2 + 1)), r1);
           tmem_ld_wait();
           if (lane < 16) {
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8)
-              st_v4(sm + OFF_PKD + sw128_offset(i, 32 * q4 + 8 * j8, 64), pack2(r[8 * j8], r[8 * j8 + 1]),
-                    pack2(r[8 * j8 + 2], r[8 * j8 + 3]), pack2(r[8 * j8 + 4], r[8 * j8 + 5]),
-                    pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
-          }
-        }
+            for (int h = 0; h < 2; ++h) {
+              const float* r = h ? r1 : r0;
+              const int q4 = q2 + h;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld32(tmem_addr(tmem, 32 * pw, TM_U + 32 * q4), r);
-          tmem_ld_wait();
-          if (lane < 16) {
-            uint8_t* urow = sm + OFF_STG + q4 * 4096 + i * (VS * 2);
-#pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8)
-              st_v4(urow + 16 * j8, pack2(r[8 * j8], r[8 * j8 + 1]), pack2(r[8 * j8 + 2], r[8 * j8 + 3]),
-                    pack2(r[8 * j8 + 4], r[8 * j8 + 5]), pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
+              for (int j8 = 0; j8 < 4; ++j8) {
+                uint8_t* d8 = cpart == 0 ? sm + OFF_PKD + sw128_offset(i, 32 * q4 + 8 * j8, 64)
+                                         : sm + OFF_STG + q4 * 4096 + i * (VS * 2) + 16 * j8;
+                st_v4(d8, pack2(r[8 * j8], r[8 * j8 + 1]), pack2(r[8 * j8 + 2], r[8 * j8 + 3]),
+                      pack2(r[8 * j8 + 4], r[8 * j8 + 5]), pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
+              }
+            }
           }
         }
       }
       tc_fence_before();
       fence_proxy_async_smem();
       fence_proxy_async_global();  // e^{g_last} went out with plain stores
-      if (role_any(NB_PREP, failed)) break;
+      if (role_any(NB_PREP, NPROD, failed)) break;
       PROF(8);
 
-      // ---- 8. W/U to the ring; the record is published after the next chunk's
-      //         elementwise pass (or at the end), once these stores have landed ----
+      // ---- 8. W/U to the ring; the record is published during the next chunk
+      //         (or at the end), once these stores have landed ----
       if (pt == 0) {
-        bulk_store(gs + R_WM, sm + OFF_PKD, 16384);
+        bulk_store(gs + R_WQ, sm + OFF_PKD, 8192);
+        bulk_store(gs + R_WQ + R_W_KB, sm + OFF_PKD + 8192, 8192);
         bulk_store(gs + G_U, sm + OFF_STG, 16384);
         bulk_commit();
         pub_pending = true;
@@ -589,8 +641,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     __syncwarp();
   } else {
     // ================================ chain ================================
-    const int qt = tid - 128;  // state row d
-    const int qw = warp - 4;   // TMEM lane quadrant
+    const int qt = tid - NPROD;  // state row d
+    const int qw = warp & 3;     // TMEM lane quadrant
     const int d = qt;
     float st[VS];
     if (p.s0) {
@@ -616,11 +668,11 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     };
     write_st();
     fence_proxy_async_smem();
-    role_sync(NB_CHAIN);
+    role_sync(NB_CHAIN, NCHAIN);
 
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     bool failed = false, aborted = false;
-    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
+    int a_issued = 0, b_issued = 0, c_issued = 0, a_done = 0, b_done = 0, c_done = 0;
     auto timeout = [&]() {
       failed = true;
       atomicOr(p.status, kStatusTimeout);
@@ -636,7 +688,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       uint8_t* slot = sm + OFF_SLOT + s * SSLOT;
       const uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
       mbar_arrive_expect_tx(&bars[B_FULL + s], REC_TX);
-      bulk_load(slot + R_QD, gs + R_QD, R_TILES, &bars[B_FULL + s]);
+      bulk_load(slot + R_WQ, gs + R_WQ, R_TILES, &bars[B_FULL + s]);
       bulk_load(slot + S_U, gs + G_U + rank * 4096, 4096, &bars[B_FULL + s]);
       bulk_load(slot + S_GAM, gs + G_GAM, 512, &bars[B_FULL + s]);
     };
@@ -655,14 +707,19 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         ++next_load;
       }
     };
-    // o rows of chunk m from TMEM buffer m & 1 (rewritten only by chunk m + 2's MMAs)
+    // o rows of chunk m: lanes 64-127 of D_A[m & 1] (rewritten only by chunk m + 2's MMAs),
+    // read by the two warps of lane quadrants 2 and 3
     auto emit_o = [&](int m) {
       const int rows = min(C, len - m * C);
+      if (!mbar_wait(&bars[B_C], m & 1, WAIT_LIMIT_NS)) timeout();
+      ++c_done;
+      tc_fence_after();
+      if (qw < 2) return;
       float orr[32];
-      tmem_ld32(tmem_addr(tmem, 32 * qw, TM_O0 + 32 * (m & 1)), orr);
+      tmem_ld32(tmem_addr(tmem, 32 * qw, TM_A0 + 32 * (m & 1)), orr);
       tmem_ld_wait();
-      const int c = 16 * qw + lane;
-      if (lane < 16 && c < rows) {
+      const int c = 32 * (qw - 2) + lane;
+      if (c < rows) {
         uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok0 + m * C + c) * HV + hv) * VD + v0);
 #pragma unroll
         for (int j8 = 0; j8 < VS / 8; ++j8)
@@ -674,8 +731,10 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     if (qt == 0) pump_loads(0, false);
     for (int m = 0; m < NT; ++m) {
       const int s = m & 1;
-      uint8_t* slot = sm + OFF_SLOT + s * SSLOT;
+      const uint32_t so = OFF_SLOT + s * SSLOT;  // this chunk's record slot
+      uint8_t* slot = sm + so;
       if (qt == 0 && !failed) pump_loads(m, true);
+      PROF(6);
       __syncwarp();
       if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout();
       if (qt == 0 && !failed) {  // record m is in shared memory: release its ring slot
@@ -683,28 +742,18 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         ++loads_done;
       }
       PROF(0);
-      // ---- X = W S, O = qd S ----
+      // ---- [X ; O] = [W ; qd] S (one M = 128 accumulator) ----
       if (qt == 0 && !failed) {
         tc_fence_after();
-        constexpr uint32_t idesc = idesc_f16kind(64, VS) | IDESC_B_MN_MAJOR;
+        constexpr uint32_t idesc = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = sdesc(smem_u32(sm + OFF_ST + (kb * 4 + ks) * 1024), 8192, 512, 4);
-            umma_f16(tmem + TM_X, sdesc_sw128(smem_u32(slot + R_WM + kb * 8192 + ks * 32)), bd, idesc,
-                     (kb | ks) != 0);
-          }
-        umma_commit(&bars[B_A]);  // X alone: v_new needs it first
+          for (int ks = 0; ks < 4; ++ks)
+            umma_f16(tmem + TM_A0 + 32 * s, d128(so + R_WQ + kb * R_W_KB + ks * 32),
+                     D_ST + (((kb * 4 + ks) * 1024) >> 4), idesc, (kb | ks) != 0);
+        umma_commit(&bars[B_A]);
         ++a_issued;
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = sdesc(smem_u32(sm + OFF_ST + (kb * 4 + ks) * 1024), 8192, 512, 4);
-            umma_f16(tmem + TM_O0 + 32 * s, sdesc_sw128(smem_u32(slot + R_QD + kb * 8192 + ks * 32)), bd, idesc,
-                     (kb | ks) != 0);
-          }
         pump_loads(m, false);
       }
       __syncwarp();
@@ -713,13 +762,13 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       ++a_done;
       tc_fence_after();
       PROF(1);
-      // ---- v_new = U - X  ->  bf16 MN-major (row c = token) ----
-      {
+      // ---- v_new = U - X  ->  bf16 MN-major (row c = token; lane quadrants 0 and 1) ----
+      if (qw < 2) {
         float xr[32];
-        tmem_ld32(tmem_addr(tmem, 32 * qw, TM_X), xr);
+        tmem_ld32(tmem_addr(tmem, 32 * qw, TM_A0 + 32 * s), xr);
         tmem_ld_wait();
-        if (lane < 16) {
-          const int c = 16 * qw + lane;
+        {
+          const int c = 32 * qw + lane;
           const uint4* urow = reinterpret_cast<const uint4*>(slot + S_U + c * (VS * 2));
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -738,24 +787,28 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      if (role_any(NB_CHAIN, failed)) {
+      if (role_any(NB_CHAIN, NCHAIN, failed)) {
         aborted = true;
         break;
       }
       PROF(2);
-      // ---- P = kr^T v_new ; O += Aqk v_new ----
+      // ---- P = kr^T v_new ; o += Aqk v_new ----
+      // The second product uses the 128 rows starting 64 rows before Aqk (kr^T rows
+      // 64..127, then Aqk), so Aqk v_new lands in lanes 64-127 next to qd S; lanes
+      // 0-63 (X, already consumed) receive a harmless product.
       if (qt == 0) {
         tc_fence_after();
-        constexpr uint32_t idesc_p = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
-        constexpr uint32_t idesc_o = idesc_f16kind(64, VS) | IDESC_B_MN_MAJOR;
+        constexpr uint32_t idesc = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = sdesc(smem_u32(sm + OFF_VNT + ks * 1024), 4096, 512, 4);
-          umma_f16(tmem + TM_P, sdesc_sw128(smem_u32(slot + R_KRT + ks * 32)), bd, idesc_p, ks != 0);
-          umma_f16(tmem + TM_O0 + 32 * s, sdesc_sw128(smem_u32(slot + R_AQK + ks * 32)), bd, idesc_o, 1u);
-        }
-        umma_commit(&bars[B_B]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16(tmem + TM_P, d128(so + R_KRT + ks * 32), D_VNT + ((ks * 1024) >> 4), idesc, ks != 0);
+        umma_commit(&bars[B_B]);  // P alone: the state update needs it first
         ++b_issued;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16(tmem + TM_A0 + 32 * s, d128(so + R_AQK - 8192 + ks * 32), D_VNT + ((ks * 1024) >> 4), idesc, 1u);
+        umma_commit(&bars[B_C]);
+        ++c_issued;
       }
       __syncwarp();
       if (!mbar_wait(&bars[B_B], m & 1, WAIT_LIMIT_NS)) timeout();
@@ -775,13 +828,13 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      if (role_any(NB_CHAIN, failed)) {
+      if (role_any(NB_CHAIN, NCHAIN, failed)) {
         aborted = true;
         break;
       }
       PROF(4);
       tc_fence_before();
-      role_sync(NB_CHAIN);  // slot s is free again
+      role_sync(NB_CHAIN, NCHAIN);  // slot s is free again
       if (qt == 0 && !failed) pump_loads(m + 1, false);
       PROF(5);
     }
@@ -793,6 +846,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (a_issued > a_done && !mbar_wait(&bars[B_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
       if (b_issued > b_done && !mbar_wait(&bars[B_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
+        atomicOr(p.status, kStatusTimeout);
+      if (c_issued > c_done && !mbar_wait(&bars[B_C], (c_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
       for (int m = loads_done; m < next_load; ++m)
         if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
