@@ -82,7 +82,6 @@ constexpr uint32_t OFF_PB = OFF_PV + 16384;               // 174080 ki (raw k) |
 constexpr uint32_t OFF_MB = OFF_PB;                       //        [64 x 68] fp32
 constexpr uint32_t OFF_AMAT = OFF_PB + 17408;             // 191488 [64 x 64] bf16 SW128; before it is
 constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB staging: kr^T, inverse scratch, U slices
-constexpr uint32_t OFF_RS = OFF_STG;                      //        8 x [16 x 8] fp32 scratch of the inverse
 constexpr uint32_t OFF_ST = OFF_STG + 16384;              // 216064 S  [128 x 32] bf16 MN-major SW64
 constexpr uint32_t OFF_VNT = OFF_ST + 8192;               // 224256 v_new [64 x 32] bf16 MN-major SW64
 constexpr uint32_t OFF_BETA = OFF_VNT + 4096;             // 228352 [64] fp32
@@ -175,59 +174,72 @@ __device__ __forceinline__ bool role_any(uint32_t id, uint32_t count, bool pred)
 }
 
 // Off-diagonal blocks of T = (I + M)^{-1} (64 x 64, 16 x 16 blocks), given the
-// inverted diagonal blocks T_ii on the diagonal of `mb` and M below it: block
-// column w is walked down its block rows i > w,
-//     T_iw = -T_ii sum_{k = w}^{i-1} M_ik T_kw,
-// which needs only column w itself and the diagonal blocks, so the two warps that
-// share a block column (8 columns each) run without block-wide barriers.  T_iw is
-// kept in the unused block (w, i) above the diagonal (row 16 w + r holds row r of
-// T_iw), so no warp overwrites M that another warp still reads, and block (w, k),
-// k >= w, is T_kw for the diagonal block as well.  Each T value is also written,
-// scaled by beta of its column, into the bf16 A tile.
-// Warp `pw` (0..7): block column w = pw & 3, columns 16 w + 8 (pw >> 2) + [0, 8);
-// lane: row l >> 1, columns +4 (l & 1) + [0, 4).  `rs`: 8 x [16 x 8] fp32 scratch.
-__device__ __forceinline__ void inverse_block_columns(float* mb, float* rs, const float* beta_s, uint8_t* amat,
-                                                      int pw, int lane) {
-  const int w = pw & 3;
-  const int c0 = 8 * (pw >> 2) + 4 * (lane & 1);  // this lane's first column within the block
-  const int r = lane >> 1;                        // row within a block
-  float* my_rs = rs + pw * 128;                   // [16 rows][8 cols]
-  const float* tcol = mb + 16 * w * MB_LD + c0;   // T_kw[rr][c0 + e] = tcol[rr * MB_LD + 16 k + e]
+// inverted diagonal blocks T_ii on the diagonal of `mb` and M below it.  Warp w
+// (0..2) walks block column w down its block rows i > w, in transposed form:
+//     R^T = sum_{k = w}^{i-1} T_kw^T M_ik^T,    T_iw^T = -R^T T_ii^T,
+// as m16n8k8 TF32 MMAs (operands truncated to TF32, fp32 accumulation).  Block
+// column w needs only itself and the diagonal blocks, so the warps never wait on
+// one another.  R^T stays in registers: the accumulator of n-tile nt is the A
+// operand of k-step nt once the k index inside a step is read in the order
+// 0, 2, 4, 6, 1, 3, 5, 7 (thread (g, t) holds columns 2t and 2t + 1), so the B
+// operand rows are taken in that order too.  T_iw is kept transposed in the
+// unused block (w, i) above the diagonal (mb[16 w + col][16 i + row]), from where
+// it is the next A operand, and written, scaled by beta of its column, into the
+// bf16 A tile.
+__device__ __forceinline__ void inverse_block_columns(float* mb, const float* beta_s, uint8_t* amat, int w, int lane) {
+  const int g = lane >> 2, t = lane & 3;
   for (int i = w + 1; i < 4; ++i) {
-    // R = sum_{k = w}^{i-1} M_ik T_kw   (row r, columns c0 + [0, 4))
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* mrow = mb + (16 * i + r) * MB_LD;
+    float r[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // R^T, n-tile nt: rows 8 nt + [0, 8) of block i
     for (int k = w; k < i; ++k) {
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        const float a = mrow[16 * k + rr];
-        const float4 t4 = *reinterpret_cast<const float4*>(tcol + rr * MB_LD + 16 * k);
-        acc[0] = fmaf(a, t4.x, acc[0]);
-        acc[1] = fmaf(a, t4.y, acc[1]);
-        acc[2] = fmaf(a, t4.z, acc[2]);
-        acc[3] = fmaf(a, t4.w, acc[3]);
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t a[4];  // A = T_kw^T: m = column in block column w, kk = row in block k
+        if (k == w) {   // T_ww, row-major on the diagonal
+          const float* pa = mb + (16 * w + 8 * ks + t) * MB_LD + 16 * w + g;
+          a[0] = __float_as_uint(pa[0]);
+          a[1] = __float_as_uint(pa[8]);
+          a[2] = __float_as_uint(pa[4 * MB_LD]);
+          a[3] = __float_as_uint(pa[4 * MB_LD + 8]);
+        } else {  // T_kw, transposed in block (w, k)
+          const float* pa = mb + (16 * w + g) * MB_LD + 16 * k + 8 * ks + t;
+          a[0] = __float_as_uint(pa[0]);
+          a[1] = __float_as_uint(pa[8 * MB_LD]);
+          a[2] = __float_as_uint(pa[4]);
+          a[3] = __float_as_uint(pa[8 * MB_LD + 4]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {  // B = M_ik^T
+          const float* pb = mb + (16 * i + 8 * nt + g) * MB_LD + 16 * k + 8 * ks + t;
+          mma_tf32_m16n8k8(r[nt], a, __float_as_uint(pb[0]), __float_as_uint(pb[4]));
+        }
       }
     }
-    *reinterpret_cast<float4*>(my_rs + r * 8 + (c0 & 7)) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    __syncwarp();
-    // T_iw = -T_ii R  (T_ii lower triangular)
-    float t[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* trow = mb + (16 * i + r) * MB_LD + 16 * i;
+    float tv[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // -T_iw^T
 #pragma unroll
-    for (int mm = 0; mm < 16; ++mm) {
-      const float a = trow[mm];
-      const float4 r4 = *reinterpret_cast<const float4*>(my_rs + mm * 8 + (c0 & 7));
-      t[0] = fmaf(a, r4.x, t[0]);
-      t[1] = fmaf(a, r4.y, t[1]);
-      t[2] = fmaf(a, r4.z, t[2]);
-      t[3] = fmaf(a, r4.w, t[3]);
+    for (int ks = 0; ks < 2; ++ks) {
+      const uint32_t a[4] = {__float_as_uint(r[ks][0]), __float_as_uint(r[ks][2]), __float_as_uint(r[ks][1]),
+                             __float_as_uint(r[ks][3])};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {  // B = T_ii^T, rows 8 ks + 2t and 8 ks + 2t + 1
+        const float2 b = *reinterpret_cast<const float2*>(mb + (16 * i + 8 * nt + g) * MB_LD + 16 * i + 8 * ks + 2 * t);
+        mma_tf32_m16n8k8(tv[nt], a, __float_as_uint(b.x), __float_as_uint(b.y));
+      }
     }
-    *reinterpret_cast<float4*>(mb + (16 * w + r) * MB_LD + 16 * i + c0) = make_float4(-t[0], -t[1], -t[2], -t[3]);
-    const int col = 16 * w + c0;
-    uint32_t* a2 = reinterpret_cast<uint32_t*>(amat + sw128_offset(16 * i + r, col, 64));
-    a2[0] = pack2(-t[0] * beta_s[col], -t[1] * beta_s[col + 1]);
-    a2[1] = pack2(-t[2] * beta_s[col + 2], -t[3] * beta_s[col + 3]);
-    __syncwarp();  // R read by every lane before it is rewritten; T_iw visible to later rows
+    // tv[nt][e] = -T_iw[8 nt + 2t + (e & 1)][g + 8 (e >> 1)]
+    const float bl = beta_s[16 * w + g], bh = beta_s[16 * w + g + 8];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int row = 8 * nt + 2 * t;
+      *reinterpret_cast<float2*>(mb + (16 * w + g) * MB_LD + 16 * i + row) = make_float2(-tv[nt][0], -tv[nt][1]);
+      *reinterpret_cast<float2*>(mb + (16 * w + g + 8) * MB_LD + 16 * i + row) = make_float2(-tv[nt][2], -tv[nt][3]);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        *reinterpret_cast<uint16_t*>(amat + sw128_offset(16 * i + row + e, 16 * w + g, 64)) = f2bf(-tv[nt][e] * bl);
+        *reinterpret_cast<uint16_t*>(amat + sw128_offset(16 * i + row + e, 16 * w + g + 8, 64)) =
+            f2bf(-tv[nt][2 + e] * bh);
+      }
+    }
+    __syncwarp();  // T_iw visible to this warp's later block rows
   }
 }
 
@@ -308,6 +320,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     };
     PROF_DECL
 
+
     auto issue_raw = [&](int m, int j) {  // elected: TMA q, k, v tiles of chunk m (own chunk j)
       const int row0 = static_cast<int>(tok0) + m * C;
       mbar_arrive_expect_tx(&bars[B_RAW], RAW_TX_BYTES);
@@ -336,16 +349,22 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (part == 0 && pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
     };
     bool pub_pending = false;  // record j-1 stored but not yet published
-    auto publish = [&](int jp) {  // elected thread: record jp is complete in the ring
-      fence_proxy_async_global();
+    // Record jp is complete in the ring: tell the NSLICE consumers, one lane each
+    // (called by a whole warp; lane 0 first waits until record jp - 2, whose
+    // publish phase the consumers' barrier must have left, is loaded everywhere).
+    // A release arrive at cluster scope costs the issuing thread on the order of a
+    // thousand cycles, so the four go out as one warp instruction.
+    auto publish = [&](int jp) {
       bool ok = true;
-      if (jp >= 2) ok = mbar_wait_cluster(&bars[B_ACK + (jp & 1)], ((jp - 2) >> 1) & 1, WAIT_LIMIT_NS);
-      if (ok) {
-        const uint32_t pub = smem_u32(&bars[B_PUB + 2 * rank + (jp & 1)]);
-        for (uint32_t c = 0; c < NSLICE; ++c) mbar_arrive_cluster(mapa_shared(pub, c));
-      } else {
-        timeout();
+      if (lane == 0) {
+        fence_proxy_async_global();
+        if (jp >= 2) ok = mbar_wait_cluster(&bars[B_ACK + (jp & 1)], ((jp - 2) >> 1) & 1, WAIT_LIMIT_NS);
+        if (!ok) timeout();
       }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (ok && lane < NSLICE)
+        mbar_arrive_cluster(mapa_shared(smem_u32(&bars[B_PUB + 2 * rank + (jp & 1)]), static_cast<uint32_t>(lane)));
+      __syncwarp();
     };
 
     const int first = static_cast<int>(rank);
@@ -492,18 +511,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (pt == 0) {
         bulk_store(gs + R_AQK, sm + OFF_PQD, 8192);
         bulk_commit();
-        if (pub_pending) {  // the previous record's W/U stores are older than the last two groups
-          PROF(3);
-          bulk_wait_group<2>();
-          PROF(10);
-#ifdef KDA_PROFILE
-          if (j - 1 >= 2) mbar_wait_cluster(&bars[B_ACK + ((j - 1) & 1)], ((j - 3) >> 1) & 1, WAIT_LIMIT_NS);
-          PROF(12);
-#endif
-          publish(j - 1);
-          PROF(11);
-          pub_pending = false;
-        }
+        if (pub_pending) bulk_wait_group<2>();  // the previous record's W/U stores have landed
       }
       if (next) prefetch_gb(m + NSLICE, 1);
       PROF(3);
@@ -545,11 +553,22 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       role_sync(NB_PREP, NPROD);
       PROF(4);
-      inverse_block_columns(mb, reinterpret_cast<float*>(sm + OFF_RS), beta_s, amat, warp, lane);
+      // The previous record goes out from warp 3, which has no off-diagonal block
+      // column below (the arrives cost the issuing warp about a thousand cycles).
+      // Thread 0's wait on the record's stores is ordered before this by the
+      // barrier above.
+      if (pub_pending) {
+        if (warp == 3) publish(j - 1);
+        pub_pending = false;
+      }
+      // next chunk's g: requested here, so the loads are in flight during the
+      // inverse rather than in front of the barrier below
       if (next) prefetch_gb(m + NSLICE, 2);
+      PROF(10);
+      if (warp < 3) inverse_block_columns(mb, beta_s, amat, warp, lane);
+      PROF(5);
       fence_proxy_async_smem();
       role_sync(NB_PREP, NPROD);
-      PROF(5);
       PROF(6);
 
       // ---- 6. W = A kd, U = A v (kd and v as MN-major B operands) ----
@@ -617,13 +636,16 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         bulk_store(gs + R_WQ + R_W_KB, sm + OFF_PKD + 8192, 8192);
         bulk_store(gs + G_U, sm + OFF_STG, 16384);
         bulk_commit();
-        pub_pending = true;
       }
+      pub_pending = true;
       PROF(9);
     }
-    if (pt == 0 && pub_pending && !failed) {
-      bulk_wait_all();
-      publish(j - 1);
+    if (warp == 0 && pub_pending) {  // the last record (warp-uniform decision)
+      if (!__any_sync(0xFFFFFFFFu, failed)) {
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+        publish(j - 1);
+      }
       pub_pending = false;
     }
     // drain after an abort: copies and MMAs this role issued must finish first
@@ -637,6 +659,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         if (!mbar_wait_cluster(&bars[B_ACK + (jj & 1)], (jj >> 1) & 1, WAIT_LIMIT_NS))
           atomicOr(p.status, kStatusTimeout);
       PROF_STORE(0);
+
     }
     __syncwarp();
   } else {
@@ -737,10 +760,11 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       PROF(6);
       __syncwarp();
       if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout();
-      if (qt == 0 && !failed) {  // record m is in shared memory: release its ring slot
+      // record m is in shared memory: release its ring slot (from a warp that has
+      // slack until the state product completes)
+      if (qt == 96 && !failed)
         mbar_arrive_cluster(mapa_shared(smem_u32(&bars[B_ACK + ((m / NSLICE) & 1)]), static_cast<uint32_t>(m % NSLICE)));
-        ++loads_done;
-      }
+      if (qt == 0 && !failed) ++loads_done;
       PROF(0);
       // ---- [X ; O] = [W ; qd] S (one M = 128 accumulator) ----
       if (qt == 0 && !failed) {
