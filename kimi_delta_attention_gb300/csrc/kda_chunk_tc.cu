@@ -85,9 +85,9 @@ constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB stagin
 constexpr uint32_t OFF_ST = OFF_STG + 16384;              // 216064 S  [128 x 32] bf16 MN-major SW64
 constexpr uint32_t OFF_VNT = OFF_ST + 8192;               // 224256 v_new [64 x 32] bf16 MN-major SW64
 constexpr uint32_t OFF_BETA = OFF_VNT + 4096;             // 228352 [64] fp32
-constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 228608 [2][128] fp32 half-chunk sums of g
-constexpr uint32_t OFF_BAR = OFF_GSUM + 1024;             // 229632 mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 229888 tmem base
+constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 228608 [4][128] fp32 quarter-chunk sums of g
+constexpr uint32_t OFF_BAR = OFF_GSUM + 2048;             // 230656 mbarriers
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 230912 tmem base
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;        // + alignment slack
 
@@ -102,8 +102,6 @@ constexpr int B_B = 15;      // chain P MMA commit
 constexpr int B_C = 16;      // chain O += Aqk v_new commit
 
 // TMEM columns
-// chain: X and P are each split over two accumulators (K halves) to shorten the
-// dependent MMA chains; O is double-buffered across chunks
 // chain: D_A[m & 1] holds X = W S in lanes 0-63 and o (qd S + Aqk v_new) in lanes
 // 64-127, double-buffered across chunks; P = kr^T v_new
 constexpr uint32_t TM_L = 0, TM_AQ = 64, TM_W = 0, TM_U = 128, TM_A0 = 256, TM_P = 320;
@@ -151,10 +149,20 @@ struct Maps {
   } while (0)
 #endif
 
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+// two floats -> bf16 pair (lo in the low half), one paired conversion instruction
+// (float -> bf16 conversions issue at a fraction of the FMA rate)
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
@@ -185,11 +193,16 @@ __device__ __forceinline__ bool role_any(uint32_t id, uint32_t count, bool pred)
 // operand rows are taken in that order too.  T_iw is kept transposed in the
 // unused block (w, i) above the diagonal (mb[16 w + col][16 i + row]), from where
 // it is the next A operand, and written, scaled by beta of its column, into the
-// bf16 A tile.
-__device__ __forceinline__ void inverse_block_columns(float* mb, const float* beta_s, uint8_t* amat, int w, int lane) {
+// bf16 A tile.  The block column is a template argument so that every loop is
+// unrolled and the operand loads of a step are issued ahead of its MMAs (a
+// run-time block column measured 2.4x slower).
+template <int w>
+__device__ __forceinline__ void inverse_block_column(float* mb, const float* beta_s, uint8_t* amat, int lane) {
   const int g = lane >> 2, t = lane & 3;
+#pragma unroll
   for (int i = w + 1; i < 4; ++i) {
     float r[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // R^T, n-tile nt: rows 8 nt + [0, 8) of block i
+#pragma unroll
     for (int k = w; k < i; ++k) {
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
@@ -242,6 +255,11 @@ __device__ __forceinline__ void inverse_block_columns(float* mb, const float* be
     __syncwarp();  // T_iw visible to this warp's later block rows
   }
 }
+__device__ __forceinline__ void inverse_block_columns(float* mb, const float* beta_s, uint8_t* amat, int w, int lane) {
+  if (w == 0) inverse_block_column<0>(mb, beta_s, amat, lane);
+  else if (w == 1) inverse_block_column<1>(mb, beta_s, amat, lane);
+  else if (w == 2) inverse_block_column<2>(mb, beta_s, amat, lane);
+}
 
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
@@ -255,6 +273,9 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hv = blockIdx.y, seq = blockIdx.z;
+#ifdef KDA_PROFILE
+  const uint64_t kt0 = globaltimer_ns();
+#endif
   const uint32_t rank = cluster_ctarank();  // == blockIdx.x: the V slice and producer index
   const int HV = p.HV;
   const int hk = hv / (HV / p.H);
@@ -291,6 +312,10 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   cluster_sync_all();  // every CTA's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+#ifdef KDA_PROFILE
+  if (tid == 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
+    reinterpret_cast<uint64_t*>(p.status)[41] = globaltimer_ns() - kt0;
+#endif
   // Shared-memory matrix descriptors, built once: adding (byte offset >> 4) to a
   // descriptor moves its start address (all addresses stay below 256 KB).
   const uint32_t sbase = smem_u32(sm);
@@ -305,8 +330,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   if (warp < NPROD / 32) {
     // ============================== producer ===============================
     const int pt = tid;           // 0..255
-    const int dim = pt & 127;     // key dim owned in the elementwise pass
-    const int hr = pt >> 7;       // ... for rows [32 hr, 32 hr + 32)
+    const int dp = pt & 63;       // key dims 2 dp, 2 dp + 1 owned in the elementwise pass
+    const int hq = pt >> 6;       // ... for rows [16 hq, 16 hq + 16)
     const int quad = warp & 3;    // TMEM lane quadrant of this warp
     const int cpart = warp >> 2;  // which half of a readout this warp takes
     const float scale = p.scale;
@@ -319,6 +344,9 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       atomicOr(p.status, kStatusTimeout);
     };
     PROF_DECL
+#ifdef KDA_PROFILE
+    uint64_t ew_acc[2] = {0, 0};
+#endif
 
 
     auto issue_raw = [&](int m, int j) {  // elected: TMA q, k, v tiles of chunk m (own chunk j)
@@ -333,18 +361,19 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       raw_pending = true;
       raw_pending_j = j;
     };
-    // g of this thread's 32 rows (and beta) arrive in registers in four 8-row
-    // parts issued at different points of the previous chunk, so that few loads
-    // are in flight at once
-    float gpre[32];
+    // g of this thread's 16 rows x 2 dims (and beta) arrive in registers in four
+    // 4-row parts issued at different points of the previous chunk, so that few
+    // loads are in flight at once
+    float2 gpre[16];
     float bpre = 0.f;
     auto prefetch_gb = [&](int m, int part) {
       const int rows = min(C, len - m * C);
       const long base = tok0 + static_cast<long>(m) * C;
 #pragma unroll
-      for (int i = 8 * part; i < 8 * part + 8; ++i) {
-        const int c = 32 * hr + i;
-        gpre[i] = (c < rows) ? __ldg(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD + dim) : 0.f;
+      for (int i = 4 * part; i < 4 * part + 4; ++i) {
+        const int c = 16 * hq + i;
+        gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp)
+                             : make_float2(0.f, 0.f);
       }
       if (part == 0 && pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
     };
@@ -383,66 +412,99 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
       if (pt < C) beta_s[pt] = bpre;
       {
-        float hsum = 0.f;
+        float2 qsum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) hsum += gpre[i];
-        gsum[hr * KD + dim] = hsum;
+        for (int i = 0; i < 16; ++i) {
+          qsum.x += gpre[i].x;
+          qsum.y += gpre[i].y;
+        }
+        reinterpret_cast<float2*>(gsum + hq * KD)[dp] = qsum;
       }
       if (role_any(NB_PREP, NPROD, failed)) break;
       if (pt == 0) raw_pending = false;
       PROF(0);
+#ifdef KDA_PROFILE
+      const uint64_t ew_t0 = clock64();
+#endif
 
-      // ---- 2. elementwise: cumsum, decayed operands; kr^T and e^{g_last} to the record ----
+      // ---- 2. elementwise: cumsum, decayed operands; kr^T and e^{g_last} to the record.
+      //         Two adjacent key dims per thread (32-bit accesses of the SW128 tiles),
+      //         the cumulative sum kept in log2 units so each exponential is one ex2 ----
       {
-        const float g0 = gsum[dim];
-        const float glast = g0 + gsum[KD + dim];
-        const float gamma = __expf(glast);
-        if (hr == 0) __stcg(reinterpret_cast<float*>(gs + G_GAM) + dim, gamma);
-        float gc = hr ? g0 : 0.f;
+        float2 pre = make_float2(0.f, 0.f), all = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const float2 v = reinterpret_cast<const float2*>(gsum + qq * KD)[dp];
+          if (qq < hq) {
+            pre.x += v.x;
+            pre.y += v.y;
+          }
+          all.x += v.x;
+          all.y += v.y;
+        }
+        const float gam0 = ex2_approx(all.x * kLog2e), gam1 = ex2_approx(all.y * kLog2e);
+        if (hq == 0) __stcg(reinterpret_cast<float2*>(gs + G_GAM) + dp, make_float2(gam0, gam1));
+        float gl0 = pre.x * kLog2e, gl1 = pre.y * kLog2e;  // log2 of the decay up to the current row
         uint8_t* qd_t = sm + OFF_PQD;
         uint8_t* ki_t = sm + OFF_PB;
         uint8_t* kd_t = sm + OFF_PKD;
-        const uint32_t col_part = (dim >> 6) * 8192u + ((dim & 7) << 1);
-        const uint32_t chunk_part = (dim >> 3) & 7u;
+        const uint32_t kbase = static_cast<uint32_t>(dp >> 5) * 8192u + static_cast<uint32_t>(hq) * 16u * 128u +
+                               ((2u * dp) & 7u) * 2u;
+        const uint32_t chunk = ((2u * dp) & 63u) >> 3;
+        uint32_t kr0[8], kr1[8];  // kr of dims 2dp, 2dp+1 for the 16 rows, bf16 pairs along the rows
+        float kre0 = 0.f, kre1 = 0.f;  // kr of the previous (even) row
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint16_t kraw[8], qraw[8];
-          uint32_t off[8];
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const int c = 32 * hr + c8 * 8 + cc;
-            off[cc] = col_part + c * 128u + ((chunk_part ^ (c & 7)) << 4);
-            kraw[cc] = *reinterpret_cast<const uint16_t*>(ki_t + off[cc]);
-            qraw[cc] = *reinterpret_cast<const uint16_t*>(qd_t + off[cc]);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t off = kbase + i * 128u + ((chunk ^ (i & 7)) << 4);  // row 16 hq + i (16 hq is 0 mod 8)
+          const uint32_t kraw = *reinterpret_cast<const uint32_t*>(ki_t + off);
+          const uint32_t qraw = *reinterpret_cast<const uint32_t*>(qd_t + off);
+          gl0 = fmaf(gpre[i].x, kLog2e, gl0);
+          gl1 = fmaf(gpre[i].y, kLog2e, gl1);
+          const float e0 = ex2_approx(gl0), e1 = ex2_approx(gl1);
+          const float ie0 = ex2_approx(-gl0), ie1 = ex2_approx(-gl1);
+          const bool valid = 16 * hq + i < rows;
+          const float k0 = valid ? __uint_as_float(kraw << 16) : 0.f;
+          const float k1 = valid ? __uint_as_float(kraw & 0xFFFF0000u) : 0.f;
+          const float q0 = valid ? __uint_as_float(qraw << 16) : 0.f;
+          const float q1 = valid ? __uint_as_float(qraw & 0xFFFF0000u) : 0.f;
+          const float ki0 = k0 * ie0, ki1 = k1 * ie1;
+          *reinterpret_cast<uint32_t*>(kd_t + off) = pack2(k0 * e0, k1 * e1);
+          *reinterpret_cast<uint32_t*>(ki_t + off) = pack2(ki0, ki1);
+          *reinterpret_cast<uint32_t*>(qd_t + off) = pack2(q0 * e0 * scale, q1 * e1 * scale);
+          if (i & 1) {
+            kr0[i >> 1] = pack2(kre0, ki0 * gam0);
+            kr1[i >> 1] = pack2(kre1, ki1 * gam1);
+          } else {
+            kre0 = ki0 * gam0;
+            kre1 = ki1 * gam1;
           }
-          float kdv[8], kiv[8], qdv[8], krv[8];
+        }
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const int c = 32 * hr + c8 * 8 + cc;
-            gc += gpre[c8 * 8 + cc];
-            const float e = __expf(gc);
-            const float ie = __expf(-gc);
-            const bool valid = c < rows;
-            const float kv = valid ? bf2f(kraw[cc]) : 0.f;
-            const float qv = valid ? bf2f(qraw[cc]) : 0.f;
-            kdv[cc] = kv * e;
-            kiv[cc] = kv * ie;
-            krv[cc] = kiv[cc] * gamma;
-            qdv[cc] = qv * e * scale;
-          }
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            *reinterpret_cast<uint16_t*>(kd_t + off[cc]) = f2bf(kdv[cc]);
-            *reinterpret_cast<uint16_t*>(ki_t + off[cc]) = f2bf(kiv[cc]);
-            *reinterpret_cast<uint16_t*>(qd_t + off[cc]) = f2bf(qdv[cc]);
-          }
-          st_v4(sm + OFF_STG + sw128_offset(dim, 32 * hr + c8 * 8, 128), pack2(krv[0], krv[1]),
-                pack2(krv[2], krv[3]), pack2(krv[4], krv[5]), pack2(krv[6], krv[7]));
+        for (int h = 0; h < 2; ++h) {
+          st_v4(sm + OFF_STG + sw128_offset(2 * dp, 16 * hq + 8 * h, 128), kr0[4 * h], kr0[4 * h + 1], kr0[4 * h + 2],
+                kr0[4 * h + 3]);
+          st_v4(sm + OFF_STG + sw128_offset(2 * dp + 1, 16 * hq + 8 * h, 128), kr1[4 * h], kr1[4 * h + 1],
+                kr1[4 * h + 2], kr1[4 * h + 3]);
         }
       }
+#ifdef KDA_PROFILE
+      if (prof_on && lane == 0) ew_acc[0] += clock64() - ew_t0;
+#endif
+      if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's W/U stores have landed
+#ifdef KDA_PROFILE
+      if (prof_on && lane == 0) ew_acc[1] += clock64() - ew_t0;
+#endif
       fence_proxy_async_smem();
       role_sync(NB_PREP, NPROD);
       PROF(1);
+      // The previous record goes out from warp 3 while thread 0 issues the MMAs below
+      // (the cluster-scope arrives cost the issuing warp about a thousand cycles, and
+      // would also wait for its g loads, so it publishes before requesting them).
+      // Thread 0's wait on the record's stores is ordered before this by the barrier.
+      if (pub_pending) {
+        if (warp == 3) publish(j - 1);
+        pub_pending = false;
+      }
 
       // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd and kr^T tiles to the record ----
       if (pt == 0) {
@@ -511,7 +573,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (pt == 0) {
         bulk_store(gs + R_AQK, sm + OFF_PQD, 8192);
         bulk_commit();
-        if (pub_pending) bulk_wait_group<2>();  // the previous record's W/U stores have landed
       }
       if (next) prefetch_gb(m + NSLICE, 1);
       PROF(3);
@@ -523,14 +584,22 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (warp < 4) {
         if (lane < 16) {
           const int b0 = 16 * warp, jc = lane;
+          // row by row: T[i][jc] = [i == jc] - sum_{mm < i} M[i][mm] T[mm][jc], with
+          // M's row read four at a time and two partial sums
           float acc[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[i] = (i == jc) ? 1.f : 0.f;
+          for (int i = 0; i < 16; ++i) {
+            const float* row = mb + (b0 + i) * MB_LD + b0;
+            float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
-          for (int mm = 0; mm < 16; ++mm) {
-            const float xm = acc[mm];  // final: column jc of T, row mm
-#pragma unroll
-            for (int i = mm + 1; i < 16; ++i) acc[i] = fmaf(-mb[(b0 + i) * MB_LD + b0 + mm], xm, acc[i]);
+            for (int mm = 0; mm < i; mm += 4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(row + mm);
+              s0 = fmaf(-m4.x, acc[mm], s0);
+              if (mm + 1 < i) s1 = fmaf(-m4.y, acc[mm + 1], s1);
+              if (mm + 2 < i) s0 = fmaf(-m4.z, acc[mm + 2], s0);
+              if (mm + 3 < i) s1 = fmaf(-m4.w, acc[mm + 3], s1);
+            }
+            acc[i] = s0 + s1;
           }
           __syncwarp(0x0000FFFFu);
           const float bj = beta_s[b0 + jc];
@@ -553,14 +622,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       role_sync(NB_PREP, NPROD);
       PROF(4);
-      // The previous record goes out from warp 3, which has no off-diagonal block
-      // column below (the arrives cost the issuing warp about a thousand cycles).
-      // Thread 0's wait on the record's stores is ordered before this by the
-      // barrier above.
-      if (pub_pending) {
-        if (warp == 3) publish(j - 1);
-        pub_pending = false;
-      }
       // next chunk's g: requested here, so the loads are in flight during the
       // inverse rather than in front of the barrier below
       if (next) prefetch_gb(m + NSLICE, 2);
@@ -629,15 +690,22 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (role_any(NB_PREP, NPROD, failed)) break;
       PROF(8);
 
-      // ---- 8. W/U to the ring; the record is published during the next chunk
-      //         (or at the end), once these stores have landed ----
+      // ---- 8. W/U to the ring; the record is published early in the next chunk
+      //         (or at the end), once these stores have landed.  The first record
+      //         goes out at once: every chain of the cluster is waiting for it. ----
       if (pt == 0) {
         bulk_store(gs + R_WQ, sm + OFF_PKD, 8192);
         bulk_store(gs + R_WQ + R_W_KB, sm + OFF_PKD + 8192, 8192);
         bulk_store(gs + G_U, sm + OFF_STG, 16384);
         bulk_commit();
+        if (j == 0) bulk_wait_group<0>();
       }
       pub_pending = true;
+      if (j == 0) {
+        role_sync(NB_PREP, NPROD);
+        if (warp == 3) publish(0);
+        pub_pending = false;
+      }
       PROF(9);
     }
     if (warp == 0 && pub_pending) {  // the last record (warp-uniform decision)
@@ -659,8 +727,13 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         if (!mbar_wait_cluster(&bars[B_ACK + (jj & 1)], (jj >> 1) & 1, WAIT_LIMIT_NS))
           atomicOr(p.status, kStatusTimeout);
       PROF_STORE(0);
-
     }
+#ifdef KDA_PROFILE
+    if (prof_on && lane == 0) {
+      reinterpret_cast<uint64_t*>(p.status)[44 + warp] = ew_acc[0];
+      if (warp == 0) reinterpret_cast<uint64_t*>(p.status)[52] = ew_acc[1];
+    }
+#endif
     __syncwarp();
   } else {
     // ================================ chain ================================
@@ -862,6 +935,10 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (qt == 0 && !failed) pump_loads(m + 1, false);
       PROF(5);
     }
+#ifdef KDA_PROFILE
+    if (qt == 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
+      reinterpret_cast<uint64_t*>(p.status)[42] = globaltimer_ns() - kt0;
+#endif
     if (!aborted && !failed && NT > 0) {
       __syncwarp();
       emit_o(NT - 1);
@@ -888,9 +965,20 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 
   tc_fence_before();
   __syncthreads();
+#ifdef KDA_PROFILE
+  if (tid == 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
+    reinterpret_cast<uint64_t*>(p.status)[43] = globaltimer_ns() - kt0;
+#endif
   cluster_sync_all();  // no CTA leaves while a peer may still arrive on its barriers
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+#ifdef KDA_PROFILE
+  if (tid == 0 && rank == 0 && blockIdx.y + gridDim.y * blockIdx.z < 32) {
+    const int c = blockIdx.y + gridDim.y * blockIdx.z;
+    reinterpret_cast<uint64_t*>(p.status)[64 + 2 * c] = kt0;
+    reinterpret_cast<uint64_t*>(p.status)[65 + 2 * c] = globaltimer_ns();
+  }
+#endif
 }
 
 // ------------------------------------------------------------------ host ----
