@@ -773,8 +773,10 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       failed = true;
       atomicOr(p.status, kStatusTimeout);
     };
-    // Record loads (thread qt == 0): chunk m goes to slot m & 1 once it is
-    // published by producer m % 4 (its record j = m / 4) and the slot is free.
+    // Record loads (thread kLoader, in a warp that only emits o rows while the state
+    // product runs): chunk m goes to slot m & 1 once it is published by producer
+    // m % 4 (its record j = m / 4) and the slot is free.
+    constexpr int kLoader = 64;
     int next_load = 0;       // first chunk whose load is not issued yet
     int loads_done = 0;      // loads whose FULL phase was observed (and acknowledged)
     auto pub_bar = [&](int m) { return &bars[B_PUB + 2 * (m % NSLICE) + ((m / NSLICE) & 1)]; };
@@ -788,12 +790,14 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       bulk_load(slot + S_U, gs + G_U + rank * 4096, 4096, &bars[B_FULL + s]);
       bulk_load(slot + S_GAM, gs + G_GAM, 512, &bars[B_FULL + s]);
     };
-    // issue every load that is allowed (slot free: next_load < m_cur + 2); block only if `need`
-    auto pump_loads = [&](int m_cur, bool need) {
-      while (next_load < NT && next_load < m_cur + 2) {
+    // Issue the loads of chunks below `limit` that are published (chunk `need`, if
+    // not yet issued, is waited for).  Chunk m + 1 goes to the slot of chunk m - 1,
+    // so it is only issued once chunk m - 1's last MMA (B_C) has completed.
+    auto pump_loads = [&](int limit, int need) {
+      while (next_load < NT && next_load < limit) {
         const int m = next_load;
         if (!mbar_try_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1)) {
-          if (!need || m != m_cur) return;
+          if (m != need) return;
           if (!mbar_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1, WAIT_LIMIT_NS)) {
             timeout();
             return;
@@ -824,12 +828,12 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
     };
     PROF_DECL
-    if (qt == 0) pump_loads(0, false);
+    if (qt == kLoader) pump_loads(2, -1);
     for (int m = 0; m < NT; ++m) {
       const int s = m & 1;
       const uint32_t so = OFF_SLOT + s * SSLOT;  // this chunk's record slot
       uint8_t* slot = sm + so;
-      if (qt == 0 && !failed) pump_loads(m, true);
+      if (qt == kLoader && !failed) pump_loads(m + 1, m);
       PROF(6);
       __syncwarp();
       if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout();
@@ -837,7 +841,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       // slack until the state product completes)
       if (qt == 96 && !failed)
         mbar_arrive_cluster(mapa_shared(smem_u32(&bars[B_ACK + ((m / NSLICE) & 1)]), static_cast<uint32_t>(m % NSLICE)));
-      if (qt == 0 && !failed) ++loads_done;
+      if (qt == kLoader && !failed) ++loads_done;
       PROF(0);
       // ---- [X ; O] = [W ; qd] S (one M = 128 accumulator) ----
       if (qt == 0 && !failed) {
@@ -851,10 +855,12 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
                      D_ST + (((kb * 4 + ks) * 1024) >> 4), idesc, (kb | ks) != 0);
         umma_commit(&bars[B_A]);
         ++a_issued;
-        pump_loads(m, false);
       }
       __syncwarp();
       if (m > 0) emit_o(m - 1);  // previous chunk's rows, while this chunk's MMAs run
+      // chunk m - 1 is finished with its slot (its reads ended before the last
+      // barrier of that chunk, its last MMA with emit_o): chunk m + 1 may load
+      if (qt == kLoader && !failed) pump_loads(m + 2, -1);
       if (!mbar_wait(&bars[B_A], m & 1, WAIT_LIMIT_NS)) timeout();
       ++a_done;
       tc_fence_after();
@@ -930,10 +936,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         break;
       }
       PROF(4);
-      tc_fence_before();
-      role_sync(NB_CHAIN, NCHAIN);  // slot s is free again
-      if (qt == 0 && !failed) pump_loads(m + 1, false);
-      PROF(5);
     }
 #ifdef KDA_PROFILE
     if (qt == 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
@@ -950,10 +952,11 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         atomicOr(p.status, kStatusTimeout);
       if (c_issued > c_done && !mbar_wait(&bars[B_C], (c_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
-      for (int m = loads_done; m < next_load; ++m)
-        if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
       PROF_STORE(16);
     }
+    if (qt == kLoader)  // record loads still in flight after an abort
+      for (int m = loads_done; m < next_load; ++m)
+        if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
     __syncwarp();
     if (p.sfin && !aborted && !failed) {
       float4* dst = reinterpret_cast<float4*>(p.sfin + state_off + static_cast<size_t>(d) * VD + v0);
