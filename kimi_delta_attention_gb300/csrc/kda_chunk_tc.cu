@@ -68,7 +68,8 @@ constexpr uint32_t R_TILES = 57344;   // bytes of the tiles above
 constexpr uint32_t G_U = 57344;       // global: 4 slices of U, each [64 x 32] bf16 row-major
 constexpr uint32_t G_GAM = 57344 + 4 * 4096;  // global: e^{g_last} [128] fp32
 constexpr uint32_t GSLOT = 74752;             // global slot stride (1024-multiple)
-constexpr uint32_t S_U = 57344;       // shared slot: this CTA's U slice [64 x 32] bf16
+constexpr uint32_t S_U = 57344;       // shared slot: this CTA's U slice [64 x 32] bf16 row-major, replaced in
+                                      // place by v_new (same 64 B per row, MN-major 64-byte swizzle)
 constexpr uint32_t S_GAM = 61440;     // shared slot: e^{g_last} [128] fp32
 constexpr uint32_t SSLOT = 62464;     // shared slot stride (1024-multiple)
 constexpr uint32_t REC_TX = R_TILES + 4096 + 512;
@@ -83,8 +84,7 @@ constexpr uint32_t OFF_MB = OFF_PB;                       //        [64 x 68] fp
 constexpr uint32_t OFF_AMAT = OFF_PB + 17408;             // 191488 [64 x 64] bf16 SW128; before it is
 constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB staging: kr^T, inverse scratch, U slices
 constexpr uint32_t OFF_ST = OFF_STG + 16384;              // 216064 S  [128 x 32] bf16 MN-major SW64
-constexpr uint32_t OFF_VNT = OFF_ST + 8192;               // 224256 v_new [64 x 32] bf16 MN-major SW64
-constexpr uint32_t OFF_BETA = OFF_VNT + 4096;             // 228352 [64] fp32
+constexpr uint32_t OFF_BETA = OFF_ST + 8192;              // 224256 [64] fp32
 constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 228608 [4][128] fp32 quarter-chunk sums of g
 constexpr uint32_t OFF_BAR = OFF_GSUM + 2048;             // 230656 mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 230912 tmem base
@@ -321,7 +321,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   const uint32_t sbase = smem_u32(sm);
   const uint64_t D_SW128 = sdesc_sw128(sbase);                        // K-major, 128-B swizzle
   const uint64_t D_ST = sdesc(sbase + OFF_ST, 8192, 512, 4);          // S, MN-major 64-B swizzle
-  const uint64_t D_VNT = sdesc(sbase + OFF_VNT, 4096, 512, 4);        // v_new, MN-major 64-B swizzle
+  const uint64_t D_VNT = sdesc(sbase + OFF_SLOT + S_U, 4096, 512, 4);  // v_new of slot 0, MN-major 64-B swizzle
   const uint64_t D_KD_MN = sdesc(sbase + OFF_PKD, 8192, 1024, 2);     // kd as MN-major B
   const uint64_t D_V_MN = sdesc(sbase + OFF_PV, 8192, 1024, 2);       // v as MN-major B
   auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
@@ -777,6 +777,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     // product runs): chunk m goes to slot m & 1 once it is published by producer
     // m % 4 (its record j = m / 4) and the slot is free.
     constexpr int kLoader = 64;
+    constexpr int kIssuer = 96;  // MMA issue (warp 11, lane 0)
     int next_load = 0;       // first chunk whose load is not issued yet
     int loads_done = 0;      // loads whose FULL phase was observed (and acknowledged)
     auto pub_bar = [&](int m) { return &bars[B_PUB + 2 * (m % NSLICE) + ((m / NSLICE) & 1)]; };
@@ -811,10 +812,11 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     // read by the two warps of lane quadrants 2 and 3
     auto emit_o = [&](int m) {
       const int rows = min(C, len - m * C);
+      if (qw < 2) return;  // only the warps of lane quadrants 2 and 3 read o
       if (!mbar_wait(&bars[B_C], m & 1, WAIT_LIMIT_NS)) timeout();
       ++c_done;
+      __syncwarp();
       tc_fence_after();
-      if (qw < 2) return;
       float orr[32];
       tmem_ld32(tmem_addr(tmem, 32 * qw, TM_A0 + 32 * (m & 1)), orr);
       tmem_ld_wait();
@@ -827,6 +829,23 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
                                pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]), pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
       }
     };
+    // All chain MMAs are issued by one lane of a warp that otherwise only emits o rows,
+    // so the warps that compute v_new and the state never wait on an issue.  The
+    // o-side product of chunk m (Aqk v_new) is issued after chunk m + 1's state
+    // product, when it no longer delays anything on the recurrence.
+    auto issue_o_update = [&](int mc) {  // issuer: o rows of chunk mc += Aqk v_new
+      const int sc = mc & 1;
+      const uint32_t soc = OFF_SLOT + sc * SSLOT;
+      constexpr uint32_t idesc = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
+      // the 128 rows starting 64 rows before Aqk (kr^T rows 64..127, then Aqk): Aqk v_new
+      // lands in lanes 64-127 next to qd S; lanes 0-63 (X, consumed) take a harmless product
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_f16(tmem + TM_A0 + 32 * sc, d128(soc + R_AQK - 8192 + ks * 32),
+                 D_VNT + ((sc * SSLOT + ks * 1024) >> 4), idesc, 1u);
+      umma_commit(&bars[B_C]);
+      ++c_issued;
+    };
     PROF_DECL
     if (qt == kLoader) pump_loads(2, -1);
     for (int m = 0; m < NT; ++m) {
@@ -837,14 +856,15 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       PROF(6);
       __syncwarp();
       if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout();
-      // record m is in shared memory: release its ring slot (from a warp that has
-      // slack until the state product completes)
-      if (qt == 96 && !failed)
-        mbar_arrive_cluster(mapa_shared(smem_u32(&bars[B_ACK + ((m / NSLICE) & 1)]), static_cast<uint32_t>(m % NSLICE)));
       if (qt == kLoader && !failed) ++loads_done;
       PROF(0);
-      // ---- [X ; O] = [W ; qd] S (one M = 128 accumulator) ----
-      if (qt == 0 && !failed) {
+      // ---- [X ; O] = [W ; qd] S (one M = 128 accumulator), then chunk m - 1's o update ----
+      if (qt == kIssuer && !failed) {
+        // Record m is in shared memory (its bulk loads have completed): release its
+        // ring slot.  Nothing of the slot is read after this, so the arrive needs no
+        // ordering of its own.
+        mbar_arrive_cluster_relaxed(
+            mapa_shared(smem_u32(&bars[B_ACK + ((m / NSLICE) & 1)]), static_cast<uint32_t>(m % NSLICE)));
         tc_fence_after();
         constexpr uint32_t idesc = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
 #pragma unroll
@@ -855,6 +875,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
                      D_ST + (((kb * 4 + ks) * 1024) >> 4), idesc, (kb | ks) != 0);
         umma_commit(&bars[B_A]);
         ++a_issued;
+        if (m > 0) issue_o_update(m - 1);
       }
       __syncwarp();
       if (m > 0) emit_o(m - 1);  // previous chunk's rows, while this chunk's MMAs run
@@ -863,29 +884,31 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (qt == kLoader && !failed) pump_loads(m + 2, -1);
       if (!mbar_wait(&bars[B_A], m & 1, WAIT_LIMIT_NS)) timeout();
       ++a_done;
+      __syncwarp();
       tc_fence_after();
       PROF(1);
-      // ---- v_new = U - X  ->  bf16 MN-major (row c = token; lane quadrants 0 and 1) ----
+      // ---- v_new = U - X  ->  bf16 MN-major over the U rows (row c = token; lane
+      //      quadrants 0 and 1; each thread rewrites the 64 bytes of its own row) ----
       if (qw < 2) {
         float xr[32];
         tmem_ld32(tmem_addr(tmem, 32 * qw, TM_A0 + 32 * s), xr);
+        const int c = 32 * qw + lane;
+        uint8_t* urow = slot + S_U + c * (VS * 2);
+        uint4 u[4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) u[ch] = reinterpret_cast<const uint4*>(urow)[ch];
         tmem_ld_wait();
-        {
-          const int c = 32 * qw + lane;
-          const uint4* urow = reinterpret_cast<const uint4*>(slot + S_U + c * (VS * 2));
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const uint4 u = urow[ch];
-            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-            uint32_t w[4];
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t uw[4] = {u[ch].x, u[ch].y, u[ch].z, u[ch].w};
+          uint32_t w[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float lo = bf2f(static_cast<uint16_t>(uw[t] & 0xFFFFu)) - xr[8 * ch + 2 * t];
-              const float hi = bf2f(static_cast<uint16_t>(uw[t] >> 16)) - xr[8 * ch + 2 * t + 1];
-              w[t] = pack2(lo, hi);
-            }
-            st_v4(sm + OFF_VNT + mn_sw64_offset(c, 8 * ch), w[0], w[1], w[2], w[3]);
+          for (int t = 0; t < 4; ++t) {
+            const float lo = __uint_as_float(uw[t] << 16) - xr[8 * ch + 2 * t];
+            const float hi = __uint_as_float(uw[t] & 0xFFFF0000u) - xr[8 * ch + 2 * t + 1];
+            w[t] = pack2(lo, hi);
           }
+          st_v4(slot + S_U + mn_sw64_offset(c, 8 * ch), w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
@@ -895,36 +918,28 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         break;
       }
       PROF(2);
-      // ---- P = kr^T v_new ; o += Aqk v_new ----
-      // The second product uses the 128 rows starting 64 rows before Aqk (kr^T rows
-      // 64..127, then Aqk), so Aqk v_new lands in lanes 64-127 next to qd S; lanes
-      // 0-63 (X, already consumed) receive a harmless product.
-      if (qt == 0) {
+      // ---- P = kr^T v_new ----
+      if (qt == kIssuer) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_f16(tmem + TM_P, d128(so + R_KRT + ks * 32), D_VNT + ((ks * 1024) >> 4), idesc, ks != 0);
-        umma_commit(&bars[B_B]);  // P alone: the state update needs it first
+          umma_f16(tmem + TM_P, d128(so + R_KRT + ks * 32), D_VNT + ((s * SSLOT + ks * 1024) >> 4), idesc, ks != 0);
+        umma_commit(&bars[B_B]);
         ++b_issued;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_f16(tmem + TM_A0 + 32 * s, d128(so + R_AQK - 8192 + ks * 32), D_VNT + ((ks * 1024) >> 4), idesc, 1u);
-        umma_commit(&bars[B_C]);
-        ++c_issued;
       }
       __syncwarp();
       if (!mbar_wait(&bars[B_B], m & 1, WAIT_LIMIT_NS)) timeout();
       ++b_done;
+      __syncwarp();
       tc_fence_after();
       PROF(3);
       // ---- S <- Diag(e^{g_last}) S + P ; refresh the bf16 copy ----
-      __syncwarp();
       {
         float pr[32];
         tmem_ld32(tmem_addr(tmem, 32 * qw, TM_P), pr);
-        tmem_ld_wait();
         const float gmm = reinterpret_cast<const float*>(slot + S_GAM)[d];
+        tmem_ld_wait();
 #pragma unroll
         for (int jj = 0; jj < VS; ++jj) st[jj] = fmaf(gmm, st[jj], pr[jj]);
         write_st();
@@ -937,6 +952,10 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       PROF(4);
     }
+    if (!aborted && !failed && NT > 0 && qt == kIssuer) {
+      tc_fence_after();
+      issue_o_update(NT - 1);
+    }
 #ifdef KDA_PROFILE
     if (qt == 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
       reinterpret_cast<uint64_t*>(p.status)[42] = globaltimer_ns() - kt0;
@@ -945,15 +964,15 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       __syncwarp();
       emit_o(NT - 1);
     }
-    if (qt == 0) {  // drain copies and MMAs still in flight after an abort
+    if (qt == kIssuer) {  // drain MMAs still in flight after an abort
       if (a_issued > a_done && !mbar_wait(&bars[B_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
       if (b_issued > b_done && !mbar_wait(&bars[B_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
       if (c_issued > c_done && !mbar_wait(&bars[B_C], (c_issued - 1) & 1, WAIT_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
-      PROF_STORE(16);
     }
+    if (qt == 0) PROF_STORE(16);
     if (qt == kLoader)  // record loads still in flight after an abort
       for (int m = loads_done; m < next_load; ++m)
         if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
