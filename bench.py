@@ -30,8 +30,6 @@ WORKLOAD_INDEX = 1
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-# the kernel kda_chunk_fwd runs for the headline workload (one launch per step)
-DOMINANT_KERNEL = "kda_chunk_fused_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["kimi_delta_attention_gb300/csrc/kda_chunk_tc.cu",
                   "kimi_delta_attention_gb300/csrc/kda_recurrent.cu",
@@ -294,7 +292,7 @@ def run_gpu(args):
     alg_bytes = W.algorithmic_bytes(host, final_state=True) - 0  # initial state not read
     hbm_gbs, bf16_tf, peak_src = load_peaks()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    kernel_name = DOMINANT_KERNEL
+    kernel_name = kda.kda_chunk_fwd_kernel_name(shape)  # the one launch of each step
 
     # end to end through the public API with pinned host buffers
     e2e = e2e_measure(kda, host, dev, stream, max(3, min(args.steps, 20)))

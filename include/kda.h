@@ -86,14 +86,21 @@ typedef struct {
  *                 initial_state (each state slice is read before it is written)
  *   workspace     device scratch of at least kda_chunk_fwd_workspace_size()
  *                 bytes, owned by the caller: the device status word and, for
- *                 the tensor-core kernel, a ring of per-chunk records for each
- *                 (sequence, value head) (8 x 73 KiB each).  Nothing in it
- *                 needs initialising.  Calls that share a workspace must be
- *                 ordered on one stream.
+ *                 the tensor-core kernels, record flags and a ring of per-chunk
+ *                 records for each (sequence, value head) (16 x 73 KiB each).
+ *                 Nothing in it needs initialising.  Calls that share a
+ *                 workspace must be ordered on one stream.
  * Returns KDA_OK when the work was enqueued.  T = 0 (or all sequences empty)
  * copies initial_state (or zeros) to final_state.
- * bf16 with K = V = 128 runs the tensor-core chunk kernel; fp32 I/O and other
+ * bf16 with K = V = 128 runs a tensor-core chunk kernel; fp32 I/O and other
  * supported sizes run the token-recurrent CUDA-core kernel (same operation).
+ * Of the two tensor-core kernels, the split kernel (one CTA per (sequence,
+ * value head) carrying the state, the other SMs preparing chunk records) runs
+ * when there are at most 40 such units and they fill at most a quarter of the
+ * SMs; otherwise the cluster kernel (4 CTAs per unit) runs.  The environment
+ * variable KDA_CHUNK_SPLIT=0 or 1, read at each call, forces one of them (1
+ * only where the split kernel can hold the units).  Either kernel gives the
+ * same results up to rounding order.
  */
 KDA_API kda_status kda_chunk_fwd(const kda_shape* shape, const void* q, const void* k, const void* v,
                          const float* g, const float* beta, float scale,
@@ -131,6 +138,14 @@ KDA_API const char* kda_status_string(kda_status status);
 
 /* Chunk size used by the tensor-core kernel (tokens per chunk). */
 KDA_API int kda_chunk_size(void);
+
+/*
+ * Name of the kernel kda_chunk_fwd launches for `shape` on the current device
+ * (a static string; host-only, enqueues nothing): "kda_chunk_split_kernel",
+ * "kda_chunk_fused_kernel", "recurrent_fwd_kernel", or "none" when there is no
+ * work (or the shape is malformed).  For diagnostics and benchmarks.
+ */
+KDA_API const char* kda_chunk_fwd_kernel_name(const kda_shape* shape);
 
 /*
  * kda_chunk_fwd without a caller-provided workspace.  (Not part of the method

@@ -31,7 +31,7 @@ STATIC_SCRATCH_MAX_UNITS = 32
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
            "kda_read_device_status", "kda_status_string", "kda_chunk_size",
-           "kda_chunk_fwd_static_scratch")
+           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch")
 
 
 class KdaError(RuntimeError):
@@ -74,6 +74,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_chunk_size.argtypes = []
         lib.kda_chunk_size.restype = I
+        lib.kda_chunk_fwd_kernel_name.argtypes = [ctypes.POINTER(KdaShape)]
+        lib.kda_chunk_fwd_kernel_name.restype = ctypes.c_char_p
         lib.kda_chunk_fwd_static_scratch.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, P, P,
                                                      ctypes.POINTER(ctypes.c_void_p)]
         lib.kda_chunk_fwd_static_scratch.restype = I
@@ -111,6 +113,11 @@ def kda_chunk_fwd_workspace_size(shape: KdaShape) -> int:
 
 def kda_chunk_size() -> int:
     return int(load_library().kda_chunk_size())
+
+
+def kda_chunk_fwd_kernel_name(shape: KdaShape) -> str:
+    """Kernel kda_chunk_fwd launches for `shape` on the current device."""
+    return load_library().kda_chunk_fwd_kernel_name(ctypes.byref(shape)).decode()
 
 
 def _forward(entry: str, q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,

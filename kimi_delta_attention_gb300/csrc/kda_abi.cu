@@ -13,6 +13,7 @@ cudaError_t launch_recurrent_fwd(const FwdParams& p, bool bf16, cudaStream_t str
 bool chunk_tc_supported(const FwdParams& p, bool bf16);
 size_t chunk_tc_ring_bytes(int num_seqs, int HV);
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
+const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units);
 }  // namespace kda
 
 namespace {
@@ -102,12 +103,13 @@ kda_status run(bool use_tc, const kda_shape* s, const void* q, const void* k, co
   if (st != KDA_OK) return st;
   if (c.units == 0) return KDA_OK;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
   cudaError_t e;
-  if (use_tc && c.p.ring && kda::chunk_tc_supported(c.p, c.bf16))
-    e = kda::launch_chunk_tc_fwd(c.p, cs);
-  else
+  if (use_tc && c.p.ring && kda::chunk_tc_supported(c.p, c.bf16)) {
+    e = kda::launch_chunk_tc_fwd(c.p, cs);  // resets the status word itself
+  } else {
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
     e = kda::launch_recurrent_fwd(c.p, c.bf16, cs);
+  }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -186,6 +188,14 @@ const char* kda_status_string(kda_status status) {
 }
 
 int kda_chunk_size(void) { return 64; }
+
+const char* kda_chunk_fwd_kernel_name(const kda_shape* s) {
+  if (!s || s->B < 0 || s->T < 0 || s->HV < 1 || s->num_seqs < 0) return "none";
+  const long ns = s->num_seqs > 0 ? s->num_seqs : s->B;
+  const long tokens = s->num_seqs > 0 ? static_cast<long>(s->T) : static_cast<long>(s->B) * s->T;
+  if (ns * s->HV > (1L << 30)) return "none";
+  return kda::chunk_kernel_name(s->io_dtype == KDA_BF16, s->K, s->V, tokens, static_cast<int>(ns * s->HV));
+}
 
 kda_status kda_chunk_fwd_static_scratch(const kda_shape* shape, const void* q, const void* k, const void* v,
                                         const float* g, const float* beta, float scale,

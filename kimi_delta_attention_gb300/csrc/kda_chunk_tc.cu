@@ -40,6 +40,9 @@
 // its threads agree through bar.red.or, drain what they issued and return.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "sm103.cuh"
 
@@ -114,11 +117,16 @@ constexpr uint32_t NB_PREP = 1, NB_CHAIN = 2;
 
 struct Maps {
   CUtensorMap q, k, v;
+  CUtensorMap o;  // output tiles (split kernel)
 };
 
-// Optional per-phase cycle counters (build with -DKDA_PROFILE): thread 0 of the
-// producer and of the chain of block (0,0,0) accumulate clock64 deltas and
-// store them after the status word in the workspace (16 + 16 uint64 slots).
+// Optional instrumentation (build with -DKDA_PROFILE), stored as uint64 words after
+// the status word of the workspace: per-phase clock64 sums of one producer and one
+// chain thread ([1, 17) and [17, 33)); in the split kernel also, for unit 0, the
+// globaltimer stamps of each record's publication [200, 264), of its two copies'
+// issue [264, 328) and [330, 394), of the chain passing its full barrier [128, 192)
+// and of the chain's start [127]; and [400] the first timeout (block << 40 |
+// thread << 24 | chunk << 8 | wait site).
 #ifdef KDA_PROFILE
 #define PROF_DECL                                 \
   uint64_t prof_acc[16] = {0};                    \
@@ -1003,6 +1011,865 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 #endif
 }
 
+// ======================================================================
+// Split chunk kernel: the roles of the cluster kernel above on separate SMs.
+// One cooperative launch over every SM: CTA b < NU is the chain of unit b (one
+// (sequence, value head) with the whole K x V state, 16 warps); every other
+// CTA runs two independent 8-warp producer pipelines.  Records are produced in
+// chunk-major order over all units, written to the per-unit L2 ring and
+// announced with a GPU-scope ready flag; the chain raises a per-unit counter of
+// loaded chunks, which bounds how far producers may run ahead of it (a ring
+// slot is rewritten only after its previous record was loaded).  All CTAs are
+// resident at once (cooperative launch), and every wait is bounded.
+// ======================================================================
+// thread of chain 0 whose phase counters a -DKDA_PROFILE build stores
+#ifndef KDA_PROFILE_CHAIN_TID
+#define KDA_PROFILE_CHAIN_TID 0
+#endif
+namespace split {
+constexpr int NTHREADS = 512;
+// ring slots a unit's producers may fill ahead of its chain (of the RING slots the
+// workspace holds): few enough that a record is still in L2 when the chain loads it
+#ifndef SPLIT_RING
+#define SPLIT_RING 16
+#endif
+constexpr int SRING = SPLIT_RING;
+static_assert(SRING >= 2 && SRING <= RING, "split ring depth");
+constexpr uint32_t PIPE = 256;              // threads of one producer pipeline
+constexpr uint32_t R_U = 57344;             // record: U [64 x 128] bf16, 128-byte-swizzled rows (2 K-blocks)
+constexpr uint32_t R_GAM = R_U + 16384;     // record: e^{g_last} [128] fp32
+constexpr uint32_t REC_BYTES = R_GAM + 512; // 74,240 B
+static_assert(REC_BYTES <= GSLOT, "record fits a ring slot");
+// producer pipeline region (offsets from the region base, 1024-aligned)
+constexpr uint32_t P_Q = 0, P_KD = 16384, P_V = 32768, P_B = 49152, P_MB = P_B, P_AMAT = 66560,
+                   P_STG = 74752, P_BETA = 91136, P_GSUM = 91392, P_BAR = 93440, P_STRIDE = 94208;
+// chain region
+constexpr uint32_t C_SLOT = 0;                 // 2 record slots of GSLOT bytes
+constexpr uint32_t C_S = 2 * GSLOT;            // 149504 S [128 x 128] bf16 MN-major SW128 (32 KB)
+constexpr uint32_t C_VNT = C_S + 32768;        // 182272 v_new [64 x 128] bf16 MN-major SW128, x 2
+constexpr uint32_t C_BAR = C_VNT + 32768;      // 215040
+constexpr uint32_t C_MISC = C_BAR + 64;        // 215104 tmem base
+constexpr uint32_t SMEM_BYTES = C_MISC + 64;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
+static_assert(2 * P_STRIDE <= C_MISC, "producer regions stay below the tmem slot");
+constexpr int CB_FULL = 0, CB_A = 2, CB_B = 3, CB_C = 4;  // chain barriers
+constexpr int PB_RAW = 0, PB_PMMA = 1;                     // producer barriers (per pipeline)
+constexpr uint32_t NB_CHAIN_ALL = 3;
+
+struct Rec {
+  int m, u, seq, hv, hk, len;
+  long tok0;
+};
+// Record r of the chunk-major enumeration: chunk r / NU of unit r % NU; false when
+// the unit has no such chunk.
+__device__ __forceinline__ bool rec_at(const FwdParams& p, int NU, int r, Rec& x) {
+  x.m = r / NU;
+  x.u = r - x.m * NU;
+  x.seq = x.u / p.HV;
+  x.hv = x.u - x.seq * p.HV;
+  x.hk = x.hv / (p.HV / p.H);
+  seq_range(p, x.seq, x.tok0, x.len);
+  return x.m * C < x.len;
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* a, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// element (k, n) of an MN-major 128-byte-swizzled bf16 operand whose N = 128 columns
+// form two 64-column atoms `atom_stride` bytes apart (8-row K groups 1024 B apart)
+__device__ __forceinline__ uint32_t mn_sw128_offset(uint32_t k, uint32_t n, uint32_t atom_stride) {
+  return (n >> 6) * atom_stride + (k >> 3) * 1024u + (k & 7u) * 128u + (((((n & 63u) >> 3) ^ (k & 7u))) << 4) +
+         (n & 7u) * 2u;
+}
+
+// ------------------------------------------------------------ producer ----
+__device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, uint8_t* sm, uint32_t tmem,
+                                         int pipe, int q, int NQ, int NU, int NREC, uint32_t* flags) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pt = tid & 255;
+  const int pw = warp & 7;       // warp within the pipeline
+  const int dp = pt & 63;        // key dims 2 dp, 2 dp + 1 in the elementwise pass
+  const int hq = pt >> 6;        // ... rows [16 hq, 16 hq + 16)
+  const int quad = warp & 3;     // TMEM lane quadrant
+  const int cpart = pw >> 2;     // half of a readout
+  const uint32_t NB = 1 + static_cast<uint32_t>(pipe);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + P_BAR);
+  float* beta_s = reinterpret_cast<float*>(sm + P_BETA);
+  float* mb = reinterpret_cast<float*>(sm + P_MB);
+  float* gsum = reinterpret_cast<float*>(sm + P_GSUM);
+  const uint32_t sb = smem_u32(sm);
+  const uint64_t D_SW128 = sdesc_sw128(sb);
+  const uint64_t D_KD_MN = sdesc(sb + P_KD, 8192, 1024, 2);
+  const uint64_t D_V_MN = sdesc(sb + P_V, 8192, 1024, 2);
+  auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
+  const int HV = p.HV;
+  const float scale = p.scale;
+  uint32_t pmma_phase = 0, pmma_issued = 0;
+  bool raw_pending = false;
+  int raw_pending_j = 0;
+  bool failed = false;
+  auto timeout = [&]() {
+    failed = true;
+    atomicOr(p.status, kStatusTimeout);
+#ifdef KDA_PROFILE
+    atomicCAS(reinterpret_cast<unsigned long long*>(p.status) + 400, 0ull,
+              (static_cast<unsigned long long>(blockIdx.x) << 40) | (static_cast<unsigned long long>(threadIdx.x) << 24) | 20ull);
+#endif
+  };
+  auto issue_raw = [&](const Rec& x, int jj) {  // elected
+    const int row0 = static_cast<int>(x.tok0) + x.m * C;
+    mbar_arrive_expect_tx(&bars[PB_RAW], RAW_TX_BYTES);
+    tma_load_3d(sm + P_Q, &maps.q, &bars[PB_RAW], 0, x.hk, row0);
+    tma_load_3d(sm + P_Q + 8192, &maps.q, &bars[PB_RAW], 64, x.hk, row0);
+    tma_load_3d(sm + P_B, &maps.k, &bars[PB_RAW], 0, x.hk, row0);
+    tma_load_3d(sm + P_B + 8192, &maps.k, &bars[PB_RAW], 64, x.hk, row0);
+    tma_load_3d(sm + P_V, &maps.v, &bars[PB_RAW], 0, x.hv, row0);
+    tma_load_3d(sm + P_V + 8192, &maps.v, &bars[PB_RAW], 64, x.hv, row0);
+    raw_pending = true;
+    raw_pending_j = jj;
+  };
+  float2 gpre[16];
+  float bpre = 0.f;
+  auto prefetch_gb = [&](const Rec& x, int part) {
+    const int rows = min(C, x.len - x.m * C);
+    const long base = x.tok0 + static_cast<long>(x.m) * C;
+#pragma unroll
+    for (int i = 4 * part; i < 4 * part + 4; ++i) {
+      const int c = 16 * hq + i;
+      gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp)
+                           : make_float2(0.f, 0.f);
+    }
+    if (part == 0 && pt < C)
+      bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + x.hv) : 0.f;
+  };
+  auto next_valid = [&](int r, Rec& x) {
+    while (r < NREC && !rec_at(p, NU, r, x)) r += NQ;
+    return r;
+  };
+  // announce record (m, u): its tiles and e^{g_last} are in the ring (called by one
+  // thread after a barrier that follows the stores' completion and the writers' fences)
+  auto publish = [&](int m, int u) {
+    fence_proxy_async_global();
+    st_release_gpu(flags + u * 32 + (m % SRING), static_cast<uint32_t>(m + 1));
+#ifdef KDA_PROFILE
+    if (u == 0 && m < 64) reinterpret_cast<uint64_t*>(p.status)[200 + m] = globaltimer_ns();
+#endif
+  };
+
+  Rec cur, nx;
+  int r = next_valid(q, cur);
+  if (r < NREC) {
+    if (pt == 0) issue_raw(cur, 0);
+#pragma unroll
+    for (int part = 0; part < 4; ++part) prefetch_gb(cur, part);
+  }
+  bool pub_pending = false;
+  int pub_m = 0, pub_u = 0;
+  int j = 0;
+  for (; r < NREC; ++j) {
+    const int rn = next_valid(r + NQ, nx);
+    const bool next = rn < NREC;
+    uint8_t* gs = p.ring + (static_cast<size_t>(cur.u) * RING + (cur.m % SRING)) * GSLOT;
+    const int rows = min(C, cur.len - cur.m * C);
+    // ---- 1. raw tiles; the ring slot must have been loaded by the chain ----
+    if (!mbar_wait(&bars[PB_RAW], j & 1, WAIT_LIMIT_NS)) timeout();
+    if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
+    if (pt < C) beta_s[pt] = bpre;
+    {
+      float2 qsum = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        qsum.x += gpre[i].x;
+        qsum.y += gpre[i].y;
+      }
+      reinterpret_cast<float2*>(gsum + hq * KD)[dp] = qsum;
+    }
+    if (role_any(NB, PIPE, failed)) break;
+    if (pt == 0) raw_pending = false;
+
+    // ---- 2. elementwise (as in the cluster kernel); e^{g_last} is held until the
+    //         ring slot may be written ----
+    float gam0 = 0.f, gam1 = 0.f;
+    {
+      float2 pre = make_float2(0.f, 0.f), all = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const float2 v = reinterpret_cast<const float2*>(gsum + qq * KD)[dp];
+        if (qq < hq) {
+          pre.x += v.x;
+          pre.y += v.y;
+        }
+        all.x += v.x;
+        all.y += v.y;
+      }
+      gam0 = ex2_approx(all.x * kLog2e);
+      gam1 = ex2_approx(all.y * kLog2e);
+      float gl0 = pre.x * kLog2e, gl1 = pre.y * kLog2e;
+      uint8_t* qd_t = sm + P_Q;
+      uint8_t* ki_t = sm + P_B;
+      uint8_t* kd_t = sm + P_KD;
+      const uint32_t kbase = static_cast<uint32_t>(dp >> 5) * 8192u + static_cast<uint32_t>(hq) * 16u * 128u +
+                             ((2u * dp) & 7u) * 2u;
+      const uint32_t chunk = ((2u * dp) & 63u) >> 3;
+      uint32_t kr0[8], kr1[8];
+      float kre0 = 0.f, kre1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t off = kbase + i * 128u + ((chunk ^ (i & 7)) << 4);
+        const uint32_t kraw = *reinterpret_cast<const uint32_t*>(ki_t + off);
+        const uint32_t qraw = *reinterpret_cast<const uint32_t*>(qd_t + off);
+        gl0 = fmaf(gpre[i].x, kLog2e, gl0);
+        gl1 = fmaf(gpre[i].y, kLog2e, gl1);
+        const float e0 = ex2_approx(gl0), e1 = ex2_approx(gl1);
+        const float ie0 = ex2_approx(-gl0), ie1 = ex2_approx(-gl1);
+        const bool valid = 16 * hq + i < rows;
+        const float k0 = valid ? __uint_as_float(kraw << 16) : 0.f;
+        const float k1 = valid ? __uint_as_float(kraw & 0xFFFF0000u) : 0.f;
+        const float q0 = valid ? __uint_as_float(qraw << 16) : 0.f;
+        const float q1 = valid ? __uint_as_float(qraw & 0xFFFF0000u) : 0.f;
+        const float ki0 = k0 * ie0, ki1 = k1 * ie1;
+        *reinterpret_cast<uint32_t*>(kd_t + off) = pack2(k0 * e0, k1 * e1);
+        *reinterpret_cast<uint32_t*>(ki_t + off) = pack2(ki0, ki1);
+        *reinterpret_cast<uint32_t*>(qd_t + off) = pack2(q0 * e0 * scale, q1 * e1 * scale);
+        if (i & 1) {
+          kr0[i >> 1] = pack2(kre0, ki0 * gam0);
+          kr1[i >> 1] = pack2(kre1, ki1 * gam1);
+        } else {
+          kre0 = ki0 * gam0;
+          kre1 = ki1 * gam1;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        st_v4(sm + P_STG + sw128_offset(2 * dp, 16 * hq + 8 * h, 128), kr0[4 * h], kr0[4 * h + 1], kr0[4 * h + 2],
+              kr0[4 * h + 3]);
+        st_v4(sm + P_STG + sw128_offset(2 * dp + 1, 16 * hq + 8 * h, 128), kr1[4 * h], kr1[4 * h + 1],
+              kr1[4 * h + 2], kr1[4 * h + 3]);
+      }
+    }
+    if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's stores have landed
+    fence_proxy_async_smem();
+    role_sync(NB, PIPE);
+    if (pub_pending) {  // from warp 3 of the pipeline while thread 0 issues the MMAs
+      if (pw == 3 && lane == 0) publish(pub_m, pub_u);
+      pub_pending = false;
+    }
+
+    // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd and kr^T to the record.  The record's
+    //         ring slot is written only once the chain has loaded its previous
+    //         occupant; the previous record was published above, so a wait here
+    //         never holds back a record some chain needs ----
+    if (pt == 0) {
+      if (cur.m >= SRING && !wait_flag_geq(flags + cur.u * 32 + 16, static_cast<uint32_t>(cur.m - SRING + 1),
+                                          WAIT_LIMIT_NS))
+        timeout();
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_f16kind(64, 64);
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t koff = kb * 8192 + ks * 32;
+          const uint64_t bd = d128(P_B + koff);
+          umma_f16(tmem + TM_L, d128(P_KD + koff), bd, idesc, (kb | ks) != 0);
+          umma_f16(tmem + TM_AQ, d128(P_Q + koff), bd, idesc, (kb | ks) != 0);
+        }
+      umma_commit(&bars[PB_PMMA]);
+      ++pmma_issued;
+      bulk_store(gs + R_WQ + R_QD_IN_KB, sm + P_Q, 8192);
+      bulk_store(gs + R_WQ + R_W_KB + R_QD_IN_KB, sm + P_Q + 8192, 8192);
+      bulk_store(gs + R_KRT, sm + P_STG, 16384);
+      bulk_commit();
+    }
+    if (next) prefetch_gb(nx, 0);
+    __syncwarp();
+    if (!mbar_wait(&bars[PB_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
+    ++pmma_phase;
+    tc_fence_after();
+    if (pt == 0) bulk_wait_read();  // qd (about to hold the Aqk staging) and kr^T have been read
+
+    // ---- 4. TMEM -> M (fp32), Aqk -> staging ----
+    role_sync(NB, PIPE);
+    if (hq == 0) __stcg(reinterpret_cast<float2*>(gs + R_GAM) + dp, make_float2(gam0, gam1));
+    {
+      const int i = 16 * quad + (lane & 15);
+      const int j0 = 32 * cpart;
+      float rl[32], ra[32];
+      tmem_ld32(tmem_addr(tmem, 32 * quad, TM_L + j0), rl);
+      tmem_ld32(tmem_addr(tmem, 32 * quad, TM_AQ + j0), ra);
+      tmem_ld_wait();
+      if (lane < 16) {
+        const float bi = beta_s[i];
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          float4 v4;
+          const int jj = j0 + 4 * j4;
+          v4.x = (jj + 0 < i) ? bi * rl[4 * j4 + 0] : 0.f;
+          v4.y = (jj + 1 < i) ? bi * rl[4 * j4 + 1] : 0.f;
+          v4.z = (jj + 2 < i) ? bi * rl[4 * j4 + 2] : 0.f;
+          v4.w = (jj + 3 < i) ? bi * rl[4 * j4 + 3] : 0.f;
+          *reinterpret_cast<float4*>(mb + i * MB_LD + jj) = v4;
+        }
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int jj = j0 + 8 * j8 + 2 * t;
+            w[t] = pack2((jj <= i) ? ra[8 * j8 + 2 * t] : 0.f, (jj + 1 <= i) ? ra[8 * j8 + 2 * t + 1] : 0.f);
+          }
+          st_v4(sm + P_Q + sw128_offset(i, j0 + 8 * j8, 64), w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    if (role_any(NB, PIPE, failed)) break;
+    if (pt == 0) {
+      bulk_store(gs + R_AQK, sm + P_Q, 8192);
+      bulk_commit();
+    }
+    if (next) prefetch_gb(nx, 1);
+
+    // ---- 5. inverse and A = T Diag(beta) ----
+    uint8_t* amat = sm + P_AMAT;
+    if (pw < 4) {
+      if (lane < 16) {
+        const int b0 = 16 * pw, jc = lane;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float* row = mb + (b0 + i) * MB_LD + b0;
+          float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+          for (int mm = 0; mm < i; mm += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(row + mm);
+            s0 = fmaf(-m4.x, acc[mm], s0);
+            if (mm + 1 < i) s1 = fmaf(-m4.y, acc[mm + 1], s1);
+            if (mm + 2 < i) s0 = fmaf(-m4.z, acc[mm + 2], s0);
+            if (mm + 3 < i) s1 = fmaf(-m4.w, acc[mm + 3], s1);
+          }
+          acc[i] = s0 + s1;
+        }
+        __syncwarp(0x0000FFFFu);
+        const float bj = beta_s[b0 + jc];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
+          *reinterpret_cast<uint16_t*>(amat + sw128_offset(b0 + i, b0 + jc, 64)) = f2bf(acc[i] * bj);
+        }
+      }
+    } else {
+      const int qz = pt - 128;
+      for (int idx = qz; idx < 192; idx += 128) {
+        const int blk = idx >> 5, rem = idx & 31, row = rem >> 1, half = rem & 1;
+        const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        st_v4(amat + sw128_offset(16 * br + row, 16 * bc + 8 * half, 64), 0u, 0u, 0u, 0u);
+      }
+    }
+    role_sync(NB, PIPE);
+    if (next) prefetch_gb(nx, 2);
+    if (pw < 3) inverse_block_columns(mb, beta_s, amat, pw, lane);
+    fence_proxy_async_smem();
+    role_sync(NB, PIPE);
+
+    // ---- 6. W = A kd, U = A v ----
+    if (pt == 0) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t ad = d128(P_AMAT + ks * 32);
+        umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+        umma_f16(tmem + TM_U, ad, D_V_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+      }
+      umma_commit(&bars[PB_PMMA]);
+      ++pmma_issued;
+    }
+    if (next) prefetch_gb(nx, 3);
+    __syncwarp();
+    if (!mbar_wait(&bars[PB_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
+    ++pmma_phase;
+    tc_fence_after();
+    if (pt == 0 && next && !failed) {
+      bulk_wait_read();  // the Aqk staging (in the q buffer) has been read
+      issue_raw(nx, j + 1);
+    }
+
+    // ---- 7. W -> staging (bf16 SW128), U -> staging (bf16 SW128) ----
+    __syncwarp();
+    {
+      const int i = 16 * quad + (lane & 15);
+      const uint32_t tcol = cpart == 0 ? TM_W : TM_U;
+#pragma unroll
+      for (int q2 = 0; q2 < 4; q2 += 2) {
+        float r0[32], r1[32];
+        tmem_ld32(tmem_addr(tmem, 32 * quad, tcol + 32 * q2), r0);
+        tmem_ld32(tmem_addr(tmem, 32 * quad, tcol + 32 * (q2 + 1)), r1);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float* rr = h ? r1 : r0;
+            const int q4 = q2 + h;
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8) {
+              uint8_t* d8 = cpart == 0 ? sm + P_KD + sw128_offset(i, 32 * q4 + 8 * j8, 64)
+                                       : sm + P_STG + sw128_offset(i, 32 * q4 + 8 * j8, 64);
+              st_v4(d8, pack2(rr[8 * j8], rr[8 * j8 + 1]), pack2(rr[8 * j8 + 2], rr[8 * j8 + 3]),
+                    pack2(rr[8 * j8 + 4], rr[8 * j8 + 5]), pack2(rr[8 * j8 + 6], rr[8 * j8 + 7]));
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    fence_proxy_async_global();  // e^{g_last} went out with plain stores
+    if (role_any(NB, PIPE, failed)) break;
+
+    // ---- 8. W/U to the ring; published early in the next record (or at the end);
+    //         a pipeline's first record goes out at once ----
+    if (pt == 0) {
+      bulk_store(gs + R_WQ, sm + P_KD, 8192);
+      bulk_store(gs + R_WQ + R_W_KB, sm + P_KD + 8192, 8192);
+      bulk_store(gs + R_U, sm + P_STG, 16384);
+      bulk_commit();
+      if (j == 0) bulk_wait_group<0>();
+    }
+    pub_pending = true;
+    pub_m = cur.m;
+    pub_u = cur.u;
+    if (j == 0) {
+      role_sync(NB, PIPE);
+      if (pw == 3 && lane == 0) publish(pub_m, pub_u);
+      pub_pending = false;
+    }
+    r = rn;
+    cur = nx;
+  }
+  if (pt == 0) bulk_wait_all();
+  role_sync(NB, PIPE);
+  if (pub_pending && pw == 3 && lane == 0 && !failed) publish(pub_m, pub_u);
+  if (pt == 0) {  // drain what this pipeline issued
+    if (raw_pending && !mbar_wait(&bars[PB_RAW], raw_pending_j & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    if (pmma_issued > pmma_phase && !mbar_wait(&bars[PB_PMMA], (pmma_issued - 1) & 1, WAIT_LIMIT_NS))
+      atomicOr(p.status, kStatusTimeout);
+  }
+  __syncwarp();
+}
+
+// --------------------------------------------------------------- chain ----
+// 16 warps; warp w reads TMEM lane quadrant w % 4 and owns the 32 V columns
+// 32 (w / 4) + [0, 32).  Quadrants 0 and 1 (the X rows) compute v_new;
+// quadrants 2 and 3 (the o rows) emit o and carry the record loads.  The
+// fp32 state lives in TMEM (lanes = rows): it is scaled by e^{g_last} while the
+// chunk's first product runs, the state product accumulates into it, and only
+// its bf16 copy (the next chunk's MMA operand) is rewritten on the recurrence.
+constexpr int kIssuerWarp = 4;     // issues every chain MMA, warp-wide (a v_new warp: the issue hides under
+                                   // the MMAs' own latency)
+constexpr int kIssuer = kIssuerWarp * 32;
+constexpr int kLoader = 14 * 32;   // record loads ([W; qd]), an o-row warp
+constexpr int kLoaderB = 15 * 32;  // record loads (the rest), a second copy stream (an o-row warp)
+constexpr int kStorer = 10 * 32;   // o tile stores (an o-row warp)
+constexpr int CB_SCALED = 5;       // o-row warps have scaled their state rows (256 arrivals)
+constexpr int CB_FULLB = 6;        // [2] the rest of a record (after [W; qd], which completes CB_FULL)
+constexpr uint32_t REC_A_BYTES = 32768;  // [W; qd]
+constexpr uint32_t NB_VNEW = 4, NB_OROW = 5;
+
+__device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint8_t* sm, uint32_t tmem, int u,
+                                      uint32_t* flags) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3;
+  const int cb = warp >> 2;
+  const bool vw = quad < 2;
+  const int HV = p.HV;
+  const int seq = u / HV, hv = u - seq * HV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_BAR);
+  long tok0;
+  int len;
+  seq_range(p, seq, tok0, len);
+  const int NT = (len + C - 1) / C;
+  uint8_t* ring = p.ring + static_cast<size_t>(u) * RING * GSLOT;
+  uint32_t* ready = flags + u * 32;
+  uint32_t* consumed = ready + 16;
+  const uint32_t sb = smem_u32(sm);
+  const uint64_t D_SW128 = sdesc_sw128(sb);
+  const uint64_t D_S = sdesc(sb + C_S, 16384, 1024, 2);     // bf16 S as MN-major B (K = 128)
+  const uint64_t D_VNT = sdesc(sb + C_VNT, 8192, 1024, 2);  // v_new buffer 0 as MN-major B (K = 64)
+  auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
+  const int d = 32 * quad + lane;
+  const size_t state_off = static_cast<size_t>(u) * KD * VD;
+  constexpr uint32_t TA = 0, TS = 256;  // TMEM: [X; O] accumulators at 128 s, the fp32 state at 256
+  const uint32_t t_s = tmem_addr(tmem, 32 * quad, TS + 32 * cb);
+
+  auto write_copy = [&](const float (&v)[32]) {  // bf16 copy of this thread's state block
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+      st_v4(sm + C_S + mn_sw128_offset(d, 32 * cb + 8 * ch, 16384), pack2(v[8 * ch], v[8 * ch + 1]),
+            pack2(v[8 * ch + 2], v[8 * ch + 3]), pack2(v[8 * ch + 4], v[8 * ch + 5]),
+            pack2(v[8 * ch + 6], v[8 * ch + 7]));
+  };
+  {
+    float st[32];
+    if (p.s0) {
+      const float4* src = reinterpret_cast<const float4*>(p.s0 + state_off + static_cast<size_t>(d) * VD + 32 * cb);
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 v4 = src[j4];
+        st[4 * j4] = v4.x;
+        st[4 * j4 + 1] = v4.y;
+        st[4 * j4 + 2] = v4.z;
+        st[4 * j4 + 3] = v4.w;
+      }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) st[jj] = 0.f;
+    }
+    tmem_st32(t_s, st);
+    tmem_st_wait();
+    write_copy(st);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  role_sync(NB_CHAIN_ALL, NTHREADS);
+  tc_fence_after();
+
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  bool failed = false, aborted = false;
+  int a_issued = 0, b_issued = 0, c_issued = 0, a_done = 0, b_done = 0, c_done = 0;
+  auto timeout = [&](int id, int at) {
+    failed = true;
+    atomicOr(p.status, kStatusTimeout);
+#ifdef KDA_PROFILE
+    atomicCAS(reinterpret_cast<unsigned long long*>(p.status) + 400, 0ull,
+              (static_cast<unsigned long long>(blockIdx.x) << 40) | (static_cast<unsigned long long>(tid) << 24) |
+                  (static_cast<unsigned long long>(at) << 8) | static_cast<unsigned long long>(id));
+#endif
+  };
+  bool store_pending = false;
+  PROF_DECL
+  // Record loads, two copy streams on two lanes of o-row warps.  Part A ([W; qd]) is
+  // read only by the first product, so its slot is free again once that product has
+  // completed and part A goes two chunks ahead (lane kLoader, after CB_A); part B (the
+  // rest) is free once the o update has completed and goes one chunk ahead (lane
+  // kLoaderB, at the top of the iteration).  Issuing a copy stalls the issuing lane
+  // while the copy engine queues it, so both lanes issue where their warps wait anyway.
+  // The producer fenced its plain stores to the async proxy before publishing, and the
+  // flag is read with acquire: the copies need no proxy fence of their own.
+  const bool is_loader = tid == kLoader || tid == kLoaderB;
+  const int full_bar = tid == kLoader ? CB_FULL : CB_FULLB;
+  int next_load = 0;  // this lane's first chunk not issued yet
+  uint32_t pend = 0u;  // flag word of chunk pend_n, read ahead with an acquire load
+  int pend_n = -1;
+  auto prefetch_flag = [&](int n) {
+    if (n < NT) {
+      pend = ld_acquire_gpu(ready + (n % SRING));
+      pend_n = n;
+    }
+  };
+  // this lane's part of record n, waiting for its flag when `block` (else only if the
+  // flag read ahead already shows it); returns whether it was issued
+  auto issue_part = [&](int n, bool block) -> bool {
+    const uint32_t seen = pend_n == n ? pend : 0u;
+    if (seen < static_cast<uint32_t>(n + 1)) {
+      if (!block) {
+        prefetch_flag(n);
+        return false;
+      }
+      if (!wait_flag_geq(ready + (n % SRING), static_cast<uint32_t>(n + 1), WAIT_LIMIT_NS)) {
+        timeout(1, n);
+        return false;
+      }
+    }
+    const int sl = n & 1;
+    uint8_t* dst = sm + C_SLOT + sl * GSLOT;
+    const uint8_t* src = ring + static_cast<size_t>(n % SRING) * GSLOT;
+    if (tid == kLoader) {
+      mbar_arrive_expect_tx(&bars[CB_FULL + sl], REC_A_BYTES);
+      bulk_load(dst, src, REC_A_BYTES, &bars[CB_FULL + sl]);
+    } else {
+      mbar_arrive_expect_tx(&bars[CB_FULLB + sl], REC_BYTES - REC_A_BYTES);
+      bulk_load(dst + REC_A_BYTES, src + REC_A_BYTES, REC_BYTES - REC_A_BYTES, &bars[CB_FULLB + sl]);
+    }
+#ifdef KDA_PROFILE
+    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[(tid == kLoader ? 264 : 330) + n] = globaltimer_ns();
+#endif
+    ++next_load;
+    prefetch_flag(n + 1);
+    return true;
+  };
+  // o-issuer: o rows of chunk mc += Aqk v_new
+  auto issue_o_update = [&](int mc) {  // issuer warp
+    const int sc = mc & 1;
+    constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      umma_f16_warp(tmem + TA + 128 * sc, d128(C_SLOT + sc * GSLOT + R_AQK - 8192 + ks * 32),
+                    D_VNT + ((sc * 16384 + ks * 2048) >> 4), idesc, 1u);
+    umma_commit_warp(&bars[CB_C]);
+    ++c_issued;
+  };
+  // o-row warps: rows of chunk mc to the output (a full chunk through its v_new
+  // buffer, free once the o update has completed, and two TMA tile stores)
+  auto wait_o = [&](int mc) {
+    if (!mbar_wait(&bars[CB_C], mc & 1, WAIT_LIMIT_NS)) timeout(2, mc);
+    ++c_done;
+    __syncwarp();
+    tc_fence_after();
+  };
+  auto emit_o = [&](int mc) {  // after wait_o(mc)
+    const int rows = min(C, len - mc * C);
+    float orr[32];
+    tmem_ld32(tmem_addr(tmem, 32 * quad, TA + 128 * (mc & 1) + 32 * cb), orr);
+    tmem_ld_wait();
+    const int c = 32 * (quad - 2) + lane;
+    if (rows == C) {
+      uint8_t* stage = sm + C_VNT + (mc & 1) * 16384;
+#pragma unroll
+      for (int j8 = 0; j8 < 4; ++j8)
+        st_v4(stage + sw128_offset(c, 32 * cb + 8 * j8, 64), pack2(orr[8 * j8], orr[8 * j8 + 1]),
+              pack2(orr[8 * j8 + 2], orr[8 * j8 + 3]), pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]),
+              pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
+      fence_proxy_async_smem();
+      role_sync(NB_OROW, 256);
+      if (tid == kStorer) {
+        const int row0 = static_cast<int>(tok0) + mc * C;
+        tma_store_3d(&maps.o, stage, 0, hv, row0);
+        tma_store_3d(&maps.o, stage + 8192, 64, hv, row0);
+        bulk_commit();
+        store_pending = true;
+      }
+    } else if (c < rows) {
+      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok0 + mc * C + c) * HV + hv) * VD + 32 * cb);
+#pragma unroll
+      for (int j8 = 0; j8 < 4; ++j8)
+        dst[j8] = make_uint4(pack2(orr[8 * j8], orr[8 * j8 + 1]), pack2(orr[8 * j8 + 2], orr[8 * j8 + 3]),
+                             pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]), pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
+    }
+  };
+
+#ifdef KDA_PROFILE
+  if (tid == 0 && u == 0) reinterpret_cast<uint64_t*>(p.status)[127] = globaltimer_ns();
+#endif
+  if (is_loader && NT > 0) issue_part(0, true);
+  for (int m = 0; m < NT; ++m) {
+    const int s = m & 1;
+    const uint32_t so = C_SLOT + s * GSLOT;
+    uint8_t* slot = sm + so;
+    // part B of chunk m + 1 into the slot of chunk m - 1, once its o update has completed
+    if (tid == kLoaderB && !failed && next_load == m + 1 && m + 1 < NT) {
+      if (m > 0 && !mbar_wait(&bars[CB_C], (m - 1) & 1, WAIT_LIMIT_NS)) timeout(3, m);
+      if (!failed) issue_part(m + 1, true);
+    }
+    __syncwarp();
+    PROF(7);
+    if (warp == kIssuerWarp) {  // [X; O] = [W; qd] S
+      if (!mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
+      __syncwarp();
+    }
+    if (warp == kIssuerWarp && !__any_sync(0xFFFFFFFFu, failed)) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16_warp(tmem + TA + 128 * s, d128(so + R_WQ + kb * R_W_KB + ks * 32),
+                        D_S + (((kb * 4 + ks) * 2048) >> 4), idesc, (kb | ks) != 0);
+      umma_commit_warp(&bars[CB_A]);
+      ++a_issued;
+    }
+    __syncwarp();
+    if (!mbar_wait(&bars[CB_FULLB + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(5, m);
+#ifdef KDA_PROFILE
+    if (tid == 0 && u == 0 && m < 64) reinterpret_cast<uint64_t*>(p.status)[128 + m] = globaltimer_ns();
+#endif
+    PROF(0);
+    {  // S <- Diag(e^{g_last}) S in TMEM, before the state product adds to it
+      const float gmm = reinterpret_cast<const float*>(slot + R_GAM)[d];
+      float sv[32];
+      tmem_ld32(t_s, sv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) sv[jj] *= gmm;
+      tmem_st32(t_s, sv);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    PROF(1);
+    if (vw) {
+      // ---- v_new = U - X ----
+      if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(6, m);
+      ++a_done;
+      __syncwarp();
+      tc_fence_after();
+      PROF(5);
+      float xr[32];
+      tmem_ld32(tmem_addr(tmem, 32 * quad, TA + 128 * s + 32 * cb), xr);
+      const int c = 32 * quad + lane;
+      uint4 uu[4];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        uu[ch] = *reinterpret_cast<const uint4*>(slot + R_U + sw128_offset(c, 32 * cb + 8 * ch, 64));
+      tmem_ld_wait();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t uw[4] = {uu[ch].x, uu[ch].y, uu[ch].z, uu[ch].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float lo = __uint_as_float(uw[t] << 16) - xr[8 * ch + 2 * t];
+          const float hi = __uint_as_float(uw[t] & 0xFFFF0000u) - xr[8 * ch + 2 * t + 1];
+          w[t] = pack2(lo, hi);
+        }
+        st_v4(sm + C_VNT + s * 16384 + mn_sw128_offset(c, 32 * cb + 8 * ch, 8192), w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      PROF(6);
+      role_sync(NB_VNEW, 256);
+      PROF(2);
+      // ---- state product S += kr^T v_new (after the o-row warps scaled their rows),
+      //      then this chunk's o update queued behind it ----
+      if (warp == kIssuerWarp) {
+        if (!mbar_wait(&bars[CB_SCALED], m & 1, WAIT_LIMIT_NS)) timeout(7, m);
+        __syncwarp();
+        if (!__any_sync(0xFFFFFFFFu, failed)) {
+          tc_fence_after();
+          constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_f16_warp(tmem + TS, d128(so + R_KRT + ks * 32), D_VNT + ((s * 16384 + ks * 2048) >> 4), idesc,
+                          1u);
+          umma_commit_warp(&bars[CB_B]);
+          ++b_issued;
+          issue_o_update(m);
+        }
+      }
+    } else {
+      // ---- chunk m - 1's rows (its o update ran during the previous state copy).  The
+      //      wait comes before the arrival that lets this chunk's o update be issued:
+      //      once issued, it could complete first and the parity would repeat ----
+      if (m > 0) wait_o(m - 1);
+      mbar_arrive(&bars[CB_SCALED]);
+      // part A of chunks up to m + 2 once the first product of chunk m has completed
+      // (m + 1 waits for its record if it must, m + 2 goes only if already announced)
+      if (tid == kLoader && !failed) {
+        if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(8, m);
+        if (!failed) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
+        while (!failed && next_load <= m + 2 && next_load < NT)
+          if (!issue_part(next_load, next_load <= m + 1)) break;
+      }
+      if (m > 0) emit_o(m - 1);
+    }
+    __syncwarp();
+    if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
+    ++b_done;
+    __syncwarp();
+    tc_fence_after();
+    PROF(3);
+    {  // bf16 copy of the new state
+      float sv[32];
+      tmem_ld32(t_s, sv);
+      tmem_ld_wait();
+      write_copy(sv);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    if (tid == kStorer && store_pending) {
+      bulk_wait_read();  // the o tile staged in a v_new buffer has been read
+      store_pending = false;
+    }
+    PROF(7);
+    if (role_any(NB_CHAIN_ALL, NTHREADS, failed)) {
+      aborted = true;
+      break;
+    }
+    PROF(4);
+  }
+  if (!aborted && !failed && NT > 0 && !vw) {
+    __syncwarp();
+    wait_o(NT - 1);
+    emit_o(NT - 1);
+  }
+  if (tid == kIssuer) {  // drain MMAs still in flight after an abort
+    if (a_issued > a_done && !mbar_wait(&bars[CB_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
+      atomicOr(p.status, kStatusTimeout);
+    if (b_issued > b_done && !mbar_wait(&bars[CB_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
+      atomicOr(p.status, kStatusTimeout);
+    if (c_issued > 0 && !mbar_wait(&bars[CB_C], (c_issued - 1) & 1, WAIT_LIMIT_NS))
+      atomicOr(p.status, kStatusTimeout);
+  }
+  if (tid == KDA_PROFILE_CHAIN_TID) PROF_STORE(16);
+  if (is_loader)  // copies still in flight after an abort (a consumed phase returns at once)
+    for (int n = max(0, next_load - 2); n < next_load; ++n)
+      if (!mbar_wait(&bars[full_bar + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+  if (is_loader || tid == kStorer) bulk_wait_all();
+  __syncwarp();
+  if (p.sfin && !aborted && !failed) {
+    tc_fence_after();
+    float sv[32];
+    tmem_ld32(t_s, sv);
+    tmem_ld_wait();
+    float4* dst = reinterpret_cast<float4*>(p.sfin + state_off + static_cast<size_t>(d) * VD + 32 * cb);
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) dst[j4] = make_float4(sv[4 * j4], sv[4 * j4 + 1], sv[4 * j4 + 2], sv[4 * j4 + 3]);
+  }
+}
+}  // namespace split
+
+__global__ void __launch_bounds__(split::NTHREADS, 1)
+kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int NU, int NREC) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const bool is_chain = static_cast<int>(blockIdx.x) < NU;
+  uint32_t* flags = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.status) + kFlagOffset);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + split::C_MISC);
+  if (tid == 0) {
+    if (is_chain) {
+      uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
+      for (int i = 0; i < 5; ++i) mbar_init(&cb[i], 1);
+      mbar_init(&cb[split::CB_SCALED], 256);
+      mbar_init(&cb[split::CB_FULLB], 1);
+      mbar_init(&cb[split::CB_FULLB + 1], 1);
+      tma_prefetch_desc(&maps.o);
+    } else {
+      for (int pp = 0; pp < 2; ++pp) {
+        uint64_t* pb = reinterpret_cast<uint64_t*>(sm + pp * split::P_STRIDE + split::P_BAR);
+        mbar_init(&pb[split::PB_RAW], 1);
+        mbar_init(&pb[split::PB_PMMA], 1);
+      }
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (is_chain) {
+    split::chain(maps, p, sm, tmem, static_cast<int>(blockIdx.x), flags);
+  } else {
+    const int pipe = tid >> 8;
+    const int pb = static_cast<int>(blockIdx.x) - NU;
+    const int NQ = 2 * (static_cast<int>(gridDim.x) - NU);
+    split::producer(maps, p, sm + pipe * split::P_STRIDE, tmem + 256u * static_cast<uint32_t>(pipe), pipe,
+                    2 * pb + pipe, NQ, NU, NREC, flags);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
 // ------------------------------------------------------------------ host ----
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1044,12 +1911,85 @@ bool chunk_tc_supported(const FwdParams& p, bool bf16) {
   return bf16 && p.K == tc::KD && p.V == tc::VD && tokens > 0 && tc::encoder() != nullptr;
 }
 
+namespace {
+// Which chunk kernel runs: the split kernel (chain and producer roles on separate
+// SMs) when the units are few enough to leave three quarters of the SMs to the
+// producers, else the cluster kernel.  KDA_CHUNK_SPLIT=0 or 1 in the environment
+// forces one of them (1 still needs a unit count the split kernel can hold).
+int split_override() {
+  const char* e = std::getenv("KDA_CHUNK_SPLIT");
+  return e ? std::atoi(e) : -1;
+}
+struct DeviceInfo {
+  int sms = 0;
+  bool coop = false, split_fits = false;
+};
+const DeviceInfo& device_info() {
+  static std::mutex mu;
+  static DeviceInfo info[64];
+  static bool known[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!known[dev]) {
+    DeviceInfo& d = info[dev];
+    int coop = 0;
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    d.coop = coop != 0;
+    if (cudaFuncSetAttribute(tc::kda_chunk_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::split::SMEM_ALLOC) == cudaSuccess) {
+      int blocks = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tc::kda_chunk_split_kernel, tc::split::NTHREADS,
+                                                        tc::split::SMEM_ALLOC) == cudaSuccess)
+        d.split_fits = blocks >= 1;
+    }
+    cudaGetLastError();
+    known[dev] = true;
+  }
+  return info[dev];
+}
+}  // namespace
+
+// Whether the split kernel runs for NU (sequence, value head) units on the current device.
+bool use_split_kernel(int NU) {
+  const DeviceInfo& dev = device_info();
+  const int mode = split_override();
+  const bool split_ok = dev.coop && dev.split_fits && NU <= kMaxSplitUnits && NU <= dev.sms - 2;
+  return split_ok && (mode == 1 || (mode == -1 && 4 * NU <= dev.sms));
+}
+
+
+// Resets the status word (and the split kernel's record flags) and launches.
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
   const long tokens = p.cu ? static_cast<long>(p.T) : static_cast<long>(p.num_seqs) * p.T;
   tc::Maps maps;
   if (!tc::make_map(&maps.q, p.q, tc::KD, p.H, tokens) || !tc::make_map(&maps.k, p.k, tc::KD, p.H, tokens) ||
       !tc::make_map(&maps.v, p.v, tc::VD, p.HV, tokens))
     return cudaErrorInvalidValue;
+  const int NU = p.num_seqs * p.HV;
+  const DeviceInfo& dev = device_info();
+  if (use_split_kernel(NU)) {
+    // one memset: the status word, the profile words and the flags behind them
+    if (cudaMemsetAsync(p.status, 0, kFlagOffset + NU * kFlagBytesPerUnit, stream) != cudaSuccess)
+      return cudaGetLastError();
+    const int nt_max = (p.T + tc::C - 1) / tc::C;
+    const int nrec = nt_max * NU;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dev.sms);
+    cfg.blockDim = dim3(tc::split::NTHREADS);
+    cfg.dynamicSmemBytes = tc::split::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!tc::make_map(&maps.o, p.out, tc::VD, p.HV, tokens)) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel, maps, p, NU, nrec);
+  }
+  if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return cudaGetLastError();
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(tc::kda_chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1060,6 +2000,13 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
   dim3 grid(tc::NSLICE, p.HV, p.num_seqs);
   tc::kda_chunk_fused_kernel<<<grid, tc::NTHREADS, tc::SMEM_ALLOC, stream>>>(maps, p);
   return cudaGetLastError();
+}
+
+// Name of the kernel the chunked forward launches for this problem on the current device.
+const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units) {
+  if (tokens <= 0 || units <= 0) return "none";
+  if (!(bf16 && K == tc::KD && V == tc::VD && tc::encoder() != nullptr)) return "recurrent_fwd_kernel";
+  return use_split_kernel(units) ? "kda_chunk_split_kernel" : "kda_chunk_fused_kernel";
 }
 
 }  // namespace kda

@@ -12,11 +12,17 @@ namespace kda {
 constexpr uint32_t kStatusTimeout = 1u;   // a bounded on-chip wait gave up
 constexpr uint32_t kStatusBounds = 2u;    // cu_seqlens entry out of order / range
 
-// Workspace layout: [0, 4) status word, [8, 264) optional profile counters;
-// the tensor-core chunk kernel's record ring starts at kRingOffset.
+// Workspace layout: [0, 4) status word, [8, kFlagOffset) optional profile counters,
+// [kFlagOffset, kFlagOffset + kMaxSplitUnits * kFlagBytesPerUnit) the record
+// flags of the split chunk kernel (zeroed before each launch that uses them);
+// the tensor-core chunk kernels' record rings start at kRingOffset.
 constexpr size_t kWorkspaceBytes = 256;   // minimum (status word only)
-constexpr size_t kRingOffset = 1024;
+constexpr size_t kFlagOffset = 4096;
+constexpr int kMaxSplitUnits = 40;        // (sequence, value head) pairs the split kernel takes
+constexpr size_t kFlagBytesPerUnit = 128; // 16 ready flags + a consumed-chunk counter
+constexpr size_t kRingOffset = 16384;
 constexpr size_t kRingBytesPerUnit = 16 * 74752;  // record ring of one (sequence, value head)
+static_assert(kFlagOffset + kMaxSplitUnits * kFlagBytesPerUnit <= kRingOffset, "workspace layout");
 
 struct FwdParams {
   const void* q;         // [tokens, H, K]   io type

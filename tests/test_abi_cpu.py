@@ -49,6 +49,18 @@ def test_workspace_size_and_chunk(lib):
     assert kda.kda_chunk_size() in (16, 32, 64, 128)
 
 
+def test_kernel_name_query(lib):
+    """Host-only: names the kernel a shape dispatches to (no GPU needed)."""
+    f32 = _lib.KdaShape(1, 128, 2, 2, 64, 64, 0, _lib.KDA_F32)
+    assert kda.kda_chunk_fwd_kernel_name(f32) == "recurrent_fwd_kernel"
+    bf16 = _lib.KdaShape(1, 4096, 32, 32, 128, 128, 0, _lib.KDA_BF16)
+    assert kda.kda_chunk_fwd_kernel_name(bf16) in ("kda_chunk_split_kernel", "kda_chunk_fused_kernel",
+                                                   "recurrent_fwd_kernel")
+    empty = _lib.KdaShape(1, 0, 2, 2, 128, 128, 0, _lib.KDA_BF16)
+    assert kda.kda_chunk_fwd_kernel_name(empty) == "none"
+    assert lib.kda_chunk_fwd_kernel_name(None) == b"none"
+
+
 FAKE = 0x10000  # aligned, never dereferenced
 
 

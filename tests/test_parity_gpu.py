@@ -5,6 +5,8 @@ Small and headline workloads are compared in full; the large ones on sampled
 (sequence, value head) units the oracle computes one by one, in the same
 launch configuration the benchmark times.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +17,26 @@ from kda_testutil import assert_close, check_units, np32, oracle_full, seq_bound
 
 pytestmark = pytest.mark.gpu
 
-ENTRIES = {"chunk": kda.kda_chunk_fwd, "recurrent": kda.kda_recurrent_fwd}
+
+def _chunk_kernel(mode):
+    """kda_chunk_fwd with the tensor-core kernel forced: "0" the cluster kernel,
+    "1" the split kernel (chain and producer CTAs) where the unit count allows it."""
+    def call(*args, **kw):
+        old = os.environ.get("KDA_CHUNK_SPLIT")
+        os.environ["KDA_CHUNK_SPLIT"] = mode
+        try:
+            return kda.kda_chunk_fwd(*args, **kw)
+        finally:
+            if old is None:
+                del os.environ["KDA_CHUNK_SPLIT"]
+            else:
+                os.environ["KDA_CHUNK_SPLIT"] = old
+    return call
+
+
+ENTRIES = {"chunk": kda.kda_chunk_fwd, "chunk_cluster": _chunk_kernel("0"), "chunk_split": _chunk_kernel("1"),
+           "recurrent": kda.kda_recurrent_fwd}
+ALL = ["chunk", "chunk_cluster", "chunk_split", "recurrent"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -43,7 +64,7 @@ def workload(i):
     return _cache[i]
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 @pytest.mark.parametrize("idx", [0, 1])
 def test_workload_full(entry, idx):
     x = workload(idx)
@@ -72,7 +93,17 @@ def test_workload_sampled(entry, idx):
     assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ["chunk_cluster", "chunk_split"])
+def test_long_sequences_wrap_the_record_ring(entry):
+    """256 chunks per unit: the per-unit record ring wraps many times, so the
+    flow control between record producers and the chain is exercised."""
+    x = W.make_inputs(1, 16384, 2, 4, 128, 128, "bf16", seed=12, init_state=True)
+    o, S = run(entry, x)
+    check_units(x, o, S, [(0, 0), (0, 3)])
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+
+
+@pytest.mark.parametrize("entry", ALL)
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 100, 191, 257])
 def test_ragged_lengths(entry, T):
     x = W.make_inputs(2, T, 2, 4, 128, 128, "bf16", seed=T, init_state=True)
@@ -92,7 +123,7 @@ def test_head_dims_and_dtypes(entry, KV, io):
     assert_close(o.float().cpu().numpy(), S.cpu().numpy(), o_ref, S_ref, io, f"K={K} V={V} {io}")
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_varlen_with_empty_and_tiny_sequences(entry):
     lens = [0, 1, 64, 0, 77, 128, 3, 200, 0]
     x = W.make_inputs(1, 0, 2, 4, 128, 128, "bf16", seed=5, init_state=True, lengths=lens)
@@ -105,7 +136,7 @@ def test_varlen_with_empty_and_tiny_sequences(entry):
             assert np.array_equal(S[i].cpu().numpy(), s0[i])
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_gva(entry):
     x = W.make_inputs(2, 130, 2, 8, 128, 128, "bf16", seed=3, init_state=True)
     o, S = run(entry, x)
@@ -113,7 +144,7 @@ def test_gva(entry):
     assert_close(o.float().cpu().numpy(), S.cpu().numpy(), o_ref, S_ref, "bf16", "gva")
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_empty_sequence_copies_state(entry):
     x = W.make_inputs(2, 0, 1, 2, 128, 128, "bf16", seed=1, init_state=True)
     o, S = run(entry, x)
@@ -123,7 +154,7 @@ def test_empty_sequence_copies_state(entry):
     assert (S2 == 0).all()
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_in_place_state_and_no_final_state(entry):
     x = W.make_inputs(1, 200, 2, 2, 128, 128, "bf16", seed=4, init_state=True)
     o_ref, S_ref = oracle_full(x)
@@ -140,7 +171,7 @@ def test_in_place_state_and_no_final_state(entry):
     assert_close(o2.float().cpu().numpy(), None, o_ref, None, "bf16", "no final state")
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_split_sequence_continuity(entry):
     """Running [0, m) then [m, T) with the carried state equals one run over [0, T)."""
     x = W.make_inputs(1, 300, 2, 2, 128, 128, "bf16", seed=9, init_state=True)
@@ -157,7 +188,7 @@ def test_split_sequence_continuity(entry):
     assert ((S2 - S).norm() / S.norm()).item() <= 1e-2
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_beta_zero_pure_decay_full_size(entry):
     """Property at the headline size: with beta = 0 the state only decays,
     S_T = Diag(exp(sum_t g_t)) S_0.  The decay is scaled down (g = logsigmoid(N)/2000)
@@ -173,7 +204,7 @@ def test_beta_zero_pure_decay_full_size(entry):
     assert err <= 1e-2
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
+@pytest.mark.parametrize("entry", ALL)
 def test_bad_cu_seqlens_reports_device_status(entry):
     x = W.make_inputs(1, 0, 1, 2, 128, 128, "bf16", seed=6, init_state=True, lengths=[10, 20, 30])
     d = x.to("cuda")
