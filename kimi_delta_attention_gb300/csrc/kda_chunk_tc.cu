@@ -122,11 +122,11 @@ struct Maps {
 
 // Optional instrumentation (build with -DKDA_PROFILE), stored as uint64 words after
 // the status word of the workspace: per-phase clock64 sums of one producer and one
-// chain thread ([1, 17) and [17, 33)); in the split kernel also, for unit 0, the
-// globaltimer stamps of each record's publication [200, 264), of its two copies'
-// issue [264, 328) and [330, 394), of the chain passing its full barrier [128, 192)
-// and of the chain's start [127]; and [400] the first timeout (block << 40 |
-// thread << 24 | chunk << 8 | wait site).
+// chain thread of the cluster kernel ([1, 17) and [17, 33)); in the split kernel, for
+// unit 0, the globaltimer stamps of each record's publication [200, 264), of its two
+// copies' issue [264, 328) and [330, 394) and of the chain's start [127], the clock64
+// stamps of threads 0 and 256 at the numbered points of one chunk [432, 480), and
+// [400] the first timeout (block << 40 | thread << 24 | chunk << 8 | wait site).
 #ifdef KDA_PROFILE
 #define PROF_DECL                                 \
   uint64_t prof_acc[16] = {0};                    \
@@ -1022,10 +1022,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 // slot is rewritten only after its previous record was loaded).  All CTAs are
 // resident at once (cooperative launch), and every wait is bounded.
 // ======================================================================
-// thread of chain 0 whose phase counters a -DKDA_PROFILE build stores
-#ifndef KDA_PROFILE_CHAIN_TID
-#define KDA_PROFILE_CHAIN_TID 0
-#endif
 namespace split {
 constexpr int NTHREADS = 512;
 // ring slots a unit's producers may fill ahead of its chain (of the RING slots the
@@ -1036,23 +1032,30 @@ constexpr int NTHREADS = 512;
 constexpr int SRING = SPLIT_RING;
 static_assert(SRING >= 2 && SRING <= RING, "split ring depth");
 constexpr uint32_t PIPE = 256;              // threads of one producer pipeline
-constexpr uint32_t R_U = 57344;             // record: U [64 x 128] bf16, 128-byte-swizzled rows (2 K-blocks)
-constexpr uint32_t R_GAM = R_U + 16384;     // record: e^{g_last} [128] fp32
-constexpr uint32_t REC_BYTES = R_GAM + 512; // 74,240 B
+// Record of one chunk as the split kernel lays it out in a ring slot (bf16 tiles in the
+// 128-byte swizzle layout, each the byte image of a tcgen05 B operand).  Part A is
+// what the chain needs first and is copied on its own.
+constexpr uint32_t SR_QW = 0;                 // 2 K-blocks (16 KB apart) x [qd rows | W rows]
+constexpr uint32_t SR_KB = 16384;
+constexpr uint32_t SR_W_IN_KB = 8192;
+constexpr uint32_t SR_GAM = 32768;            // e^{g_last} [128] fp32
+constexpr uint32_t REC_A_BYTES = SR_GAM + 512;
+constexpr uint32_t SR_KRT = 33792;            // kr^T [128 x 64], then Aqk [64 x 64]: one 192-row operand
+constexpr uint32_t SR_AQK = SR_KRT + 16384;
+constexpr uint32_t SR_U = SR_AQK + 8192;      // U^T [128 x 64] (rows = value columns)
+constexpr uint32_t REC_BYTES = SR_U + 16384;  // 74,752 B
 static_assert(REC_BYTES <= GSLOT, "record fits a ring slot");
 // producer pipeline region (offsets from the region base, 1024-aligned)
 constexpr uint32_t P_Q = 0, P_KD = 16384, P_V = 32768, P_B = 49152, P_MB = P_B, P_AMAT = 66560,
                    P_STG = 74752, P_BETA = 91136, P_GSUM = 91392, P_BAR = 93440, P_STRIDE = 94208;
 // chain region
 constexpr uint32_t C_SLOT = 0;                 // 2 record slots of GSLOT bytes
-constexpr uint32_t C_S = 2 * GSLOT;            // 149504 S [128 x 128] bf16 MN-major SW128 (32 KB)
-constexpr uint32_t C_VNT = C_S + 32768;        // 182272 v_new [64 x 128] bf16 MN-major SW128, x 2
-constexpr uint32_t C_BAR = C_VNT + 32768;      // 215040
+constexpr uint32_t C_BAR = 215040;             // (the chain leaves [2 GSLOT, C_BAR) unused)
 constexpr uint32_t C_MISC = C_BAR + 64;        // 215104 tmem base
-constexpr uint32_t SMEM_BYTES = C_MISC + 64;
+constexpr uint32_t SMEM_BYTES = C_MISC + 448;        // tmem base; profile stamps at C_MISC + 64
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
 static_assert(2 * P_STRIDE <= C_MISC, "producer regions stay below the tmem slot");
-constexpr int CB_FULL = 0, CB_A = 2, CB_B = 3, CB_C = 4;  // chain barriers
+constexpr int CB_FULL = 0, CB_A = 2, CB_B = 3;  // chain barriers (CB_FULL: [2])
 constexpr int PB_RAW = 0, PB_PMMA = 1;                     // producer barriers (per pipeline)
 constexpr uint32_t NB_CHAIN_ALL = 3;
 
@@ -1275,9 +1278,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
         }
       umma_commit(&bars[PB_PMMA]);
       ++pmma_issued;
-      bulk_store(gs + R_WQ + R_QD_IN_KB, sm + P_Q, 8192);
-      bulk_store(gs + R_WQ + R_W_KB + R_QD_IN_KB, sm + P_Q + 8192, 8192);
-      bulk_store(gs + R_KRT, sm + P_STG, 16384);
+      bulk_store(gs + SR_QW, sm + P_Q, 8192);
+      bulk_store(gs + SR_QW + SR_KB, sm + P_Q + 8192, 8192);
+      bulk_store(gs + SR_KRT, sm + P_STG, 16384);
       bulk_commit();
     }
     if (next) prefetch_gb(nx, 0);
@@ -1289,7 +1292,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 
     // ---- 4. TMEM -> M (fp32), Aqk -> staging ----
     role_sync(NB, PIPE);
-    if (hq == 0) __stcg(reinterpret_cast<float2*>(gs + R_GAM) + dp, make_float2(gam0, gam1));
+    if (hq == 0) __stcg(reinterpret_cast<float2*>(gs + SR_GAM) + dp, make_float2(gam0, gam1));
     {
       const int i = 16 * quad + (lane & 15);
       const int j0 = 32 * cpart;
@@ -1325,7 +1328,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     fence_proxy_async_smem();
     if (role_any(NB, PIPE, failed)) break;
     if (pt == 0) {
-      bulk_store(gs + R_AQK, sm + P_Q, 8192);
+      bulk_store(gs + SR_AQK, sm + P_Q, 8192);
       bulk_commit();
     }
     if (next) prefetch_gb(nx, 1);
@@ -1373,15 +1376,17 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     fence_proxy_async_smem();
     role_sync(NB, PIPE);
 
-    // ---- 6. W = A kd, U = A v ----
+    // ---- 6. W = A kd (M = 64, kd as MN-major B) and U^T = v^T A^T (M = 128 value
+    //         columns, v as MN-major A, A as K-major B) ----
     if (pt == 0) {
       tc_fence_after();
-      constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+      constexpr uint32_t idesc_w = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+      constexpr uint32_t idesc_u = idesc_f16kind(128, 64) | IDESC_A_MN_MAJOR;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const uint64_t ad = d128(P_AMAT + ks * 32);
-        umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc, ks != 0);
-        umma_f16(tmem + TM_U, ad, D_V_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+        umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc_w, ks != 0);
+        umma_f16(tmem + TM_U, D_V_MN + ((ks * 2048) >> 4), ad, idesc_u, ks != 0);
       }
       umma_commit(&bars[PB_PMMA]);
       ++pmma_issued;
@@ -1396,16 +1401,16 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       issue_raw(nx, j + 1);
     }
 
-    // ---- 7. W -> staging (bf16 SW128), U -> staging (bf16 SW128) ----
+    // ---- 7. W -> staging (bf16 SW128, warps 0-3), U^T -> staging (warps 4-7: row v
+    //         of 64 tokens, 128-byte-swizzled) ----
     __syncwarp();
-    {
+    if (cpart == 0) {
       const int i = 16 * quad + (lane & 15);
-      const uint32_t tcol = cpart == 0 ? TM_W : TM_U;
 #pragma unroll
       for (int q2 = 0; q2 < 4; q2 += 2) {
         float r0[32], r1[32];
-        tmem_ld32(tmem_addr(tmem, 32 * quad, tcol + 32 * q2), r0);
-        tmem_ld32(tmem_addr(tmem, 32 * quad, tcol + 32 * (q2 + 1)), r1);
+        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_W + 32 * q2), r0);
+        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_W + 32 * (q2 + 1)), r1);
         tmem_ld_wait();
         if (lane < 16) {
 #pragma unroll
@@ -1413,14 +1418,26 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
             const float* rr = h ? r1 : r0;
             const int q4 = q2 + h;
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8) {
-              uint8_t* d8 = cpart == 0 ? sm + P_KD + sw128_offset(i, 32 * q4 + 8 * j8, 64)
-                                       : sm + P_STG + sw128_offset(i, 32 * q4 + 8 * j8, 64);
-              st_v4(d8, pack2(rr[8 * j8], rr[8 * j8 + 1]), pack2(rr[8 * j8 + 2], rr[8 * j8 + 3]),
-                    pack2(rr[8 * j8 + 4], rr[8 * j8 + 5]), pack2(rr[8 * j8 + 6], rr[8 * j8 + 7]));
-            }
+            for (int j8 = 0; j8 < 4; ++j8)
+              st_v4(sm + P_KD + sw128_offset(i, 32 * q4 + 8 * j8, 64), pack2(rr[8 * j8], rr[8 * j8 + 1]),
+                    pack2(rr[8 * j8 + 2], rr[8 * j8 + 3]), pack2(rr[8 * j8 + 4], rr[8 * j8 + 5]),
+                    pack2(rr[8 * j8 + 6], rr[8 * j8 + 7]));
           }
         }
+      }
+    } else {
+      const int v = 32 * quad + lane;
+      uint8_t* row = sm + P_STG + v * 128;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float rr[32];
+        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_U + 32 * h), rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8)
+          st_v4(row + (((4 * h + j8) ^ (v & 7)) << 4), pack2(rr[8 * j8], rr[8 * j8 + 1]),
+                pack2(rr[8 * j8 + 2], rr[8 * j8 + 3]), pack2(rr[8 * j8 + 4], rr[8 * j8 + 5]),
+                pack2(rr[8 * j8 + 6], rr[8 * j8 + 7]));
       }
     }
     tc_fence_before();
@@ -1431,9 +1448,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     // ---- 8. W/U to the ring; published early in the next record (or at the end);
     //         a pipeline's first record goes out at once ----
     if (pt == 0) {
-      bulk_store(gs + R_WQ, sm + P_KD, 8192);
-      bulk_store(gs + R_WQ + R_W_KB, sm + P_KD + 8192, 8192);
-      bulk_store(gs + R_U, sm + P_STG, 16384);
+      bulk_store(gs + SR_QW + SR_W_IN_KB, sm + P_KD, 8192);
+      bulk_store(gs + SR_QW + SR_KB + SR_W_IN_KB, sm + P_KD + 8192, 8192);
+      bulk_store(gs + SR_U, sm + P_STG, 16384);
       bulk_commit();
       if (j == 0) bulk_wait_group<0>();
     }
@@ -1460,29 +1477,53 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 }
 
 // --------------------------------------------------------------- chain ----
-// 16 warps; warp w reads TMEM lane quadrant w % 4 and owns the 32 V columns
-// 32 (w / 4) + [0, 32).  Quadrants 0 and 1 (the X rows) compute v_new;
-// quadrants 2 and 3 (the o rows) emit o and carry the record loads.  The
-// fp32 state lives in TMEM (lanes = rows): it is scaled by e^{g_last} while the
-// chunk's first product runs, the state product accumulates into it, and only
-// its bf16 copy (the next chunk's MMA operand) is rewritten on the recurrence.
-constexpr int kIssuerWarp = 4;     // issues every chain MMA, warp-wide (a v_new warp: the issue hides under
-                                   // the MMAs' own latency)
-constexpr int kIssuer = kIssuerWarp * 32;
-constexpr int kLoader = 14 * 32;   // record loads ([W; qd]), an o-row warp
-constexpr int kLoaderB = 15 * 32;  // record loads (the rest), a second copy stream (an o-row warp)
-constexpr int kStorer = 10 * 32;   // o tile stores (an o-row warp)
-constexpr int CB_SCALED = 5;       // o-row warps have scaled their state rows (256 arrivals)
-constexpr int CB_FULLB = 6;        // [2] the rest of a record (after [W; qd], which completes CB_FULL)
-constexpr uint32_t REC_A_BYTES = 32768;  // [W; qd]
-constexpr uint32_t NB_VNEW = 4, NB_OROW = 5;
+// The recurrence is carried transposed in TMEM (lanes = value columns v): S^T in fp32
+// and as a bf16 copy, v_new^T in bf16, and the products [O^T | X^T].  The bf16
+// matrices are the A operands of the chain's MMAs; their B operands are the record's
+// tiles in shared memory as the producer wrote them:
+//   [O^T | X^T] = S^T [qd; W]^T                         (N = 128, K = 128)
+//   [S^T | O^T] += v_new^T [kr^T; Aqk]^T                (N = 192, K = 64)
+// with S^T scaled by e^{g_last} between chunks.  Warps 0-7 carry the recurrence:
+// warp w reads TMEM lane quadrant w % 4 (v = 32 (w % 4) + lane) and takes half
+// h = w / 4 of the other dimension (tokens 32 h + [0, 32) of v_new, key dims
+// 64 h + [0, 64) of the state).  Warps 8-15 (same quadrants and halves) emit the o
+// rows and copy records ahead; all their waits are off the recurrence's path.
+constexpr int kIssuerWarp = 0;     // issues every chain MMA (a recurrence warp)
+constexpr int kLoaderA = 8 * 32;   // helper lane copying record part A ([qd; W], e^{g_last})
+constexpr int kLoaderB = 12 * 32;  // helper lane copying record part B (kr^T, Aqk, U^T)
+constexpr int CB_FULLB = 6;        // [2] part B of a record (part A completes CB_FULL)
+constexpr int kStorer = 13 * 32;   // helper lane issuing the o tile stores
+constexpr uint32_t NB_REC = 4;     // named barrier of the 8 recurrence warps
+constexpr uint32_t NB_HELP = 5;    // named barrier of the 8 helper warps
+constexpr uint32_t C_STG = 2 * GSLOT;  // two 16 KB o staging tiles ([token][v], two 64-column halves)
+constexpr uint32_t TS = 0, TOT = 128, TXT = 192, TSB = 256, TVN = 320;  // TMEM columns
+// -DKDA_PROFILE: clock64 stamps of threads 0 and 256 of chain 0 at numbered points of
+// one chunk, kept in shared memory (cheap enough not to disturb the timing)
+#ifndef KDA_STAMP_CHUNK
+#define KDA_STAMP_CHUNK 32
+#endif
+#ifdef KDA_PROFILE
+#define STAMP(i)                                                                                 \
+  do {                                                                                           \
+    if (m == KDA_STAMP_CHUNK && u == 0 && (tid == 0 || tid == 256)) {                            \
+      long long t_;                                                                              \
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(t_)::"memory");                               \
+      *reinterpret_cast<volatile long long*>(sm + C_MISC + 64 + (tid ? 192 : 0) + 8 * (i)) = t_;  \
+    }                                                                                            \
+  } while (0)
+#else
+#define STAMP(i) \
+  do {           \
+  } while (0)
+#endif
 
 __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint8_t* sm, uint32_t tmem, int u,
                                       uint32_t* flags) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3;
-  const int cb = warp >> 2;
-  const bool vw = quad < 2;
+  const bool rec = warp < 8;           // recurrence warp (else helper)
+  const int h = (warp >> 2) & 1;       // half of the non-lane dimension
+  const int vcol = 32 * quad + lane;   // this thread's value column
   const int HV = p.HV;
   const int seq = u / HV, hv = u - seq * HV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_BAR);
@@ -1495,49 +1536,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   uint32_t* consumed = ready + 16;
   const uint32_t sb = smem_u32(sm);
   const uint64_t D_SW128 = sdesc_sw128(sb);
-  const uint64_t D_S = sdesc(sb + C_S, 16384, 1024, 2);     // bf16 S as MN-major B (K = 128)
-  const uint64_t D_VNT = sdesc(sb + C_VNT, 8192, 1024, 2);  // v_new buffer 0 as MN-major B (K = 64)
   auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
-  const int d = 32 * quad + lane;
+  const uint32_t tl = tmem_addr(tmem, 32 * quad, 0);  // this warp's lane quadrant
   const size_t state_off = static_cast<size_t>(u) * KD * VD;
-  constexpr uint32_t TA = 0, TS = 256;  // TMEM: [X; O] accumulators at 128 s, the fp32 state at 256
-  const uint32_t t_s = tmem_addr(tmem, 32 * quad, TS + 32 * cb);
-
-  auto write_copy = [&](const float (&v)[32]) {  // bf16 copy of this thread's state block
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-      st_v4(sm + C_S + mn_sw128_offset(d, 32 * cb + 8 * ch, 16384), pack2(v[8 * ch], v[8 * ch + 1]),
-            pack2(v[8 * ch + 2], v[8 * ch + 3]), pack2(v[8 * ch + 4], v[8 * ch + 5]),
-            pack2(v[8 * ch + 6], v[8 * ch + 7]));
-  };
-  {
-    float st[32];
-    if (p.s0) {
-      const float4* src = reinterpret_cast<const float4*>(p.s0 + state_off + static_cast<size_t>(d) * VD + 32 * cb);
-#pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
-        const float4 v4 = src[j4];
-        st[4 * j4] = v4.x;
-        st[4 * j4 + 1] = v4.y;
-        st[4 * j4 + 2] = v4.z;
-        st[4 * j4 + 3] = v4.w;
-      }
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) st[jj] = 0.f;
-    }
-    tmem_st32(t_s, st);
-    tmem_st_wait();
-    write_copy(st);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  role_sync(NB_CHAIN_ALL, NTHREADS);
-  tc_fence_after();
-
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   bool failed = false, aborted = false;
-  int a_issued = 0, b_issued = 0, c_issued = 0, a_done = 0, b_done = 0, c_done = 0;
+  int a_issued = 0, b_issued = 0;
   auto timeout = [&](int id, int at) {
     failed = true;
     atomicOr(p.status, kStatusTimeout);
@@ -1547,36 +1551,26 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
                   (static_cast<unsigned long long>(at) << 8) | static_cast<unsigned long long>(id));
 #endif
   };
-  bool store_pending = false;
-  PROF_DECL
-  // Record loads, two copy streams on two lanes of o-row warps.  Part A ([W; qd]) is
-  // read only by the first product, so its slot is free again once that product has
-  // completed and part A goes two chunks ahead (lane kLoader, after CB_A); part B (the
-  // rest) is free once the o update has completed and goes one chunk ahead (lane
-  // kLoaderB, at the top of the iteration).  Issuing a copy stalls the issuing lane
-  // while the copy engine queues it, so both lanes issue where their warps wait anyway.
-  // The producer fenced its plain stores to the async proxy before publishing, and the
-  // flag is read with acquire: the copies need no proxy fence of their own.
-  const bool is_loader = tid == kLoader || tid == kLoaderB;
-  const int full_bar = tid == kLoader ? CB_FULL : CB_FULLB;
-  int next_load = 0;  // this lane's first chunk not issued yet
-  uint32_t pend = 0u;  // flag word of chunk pend_n, read ahead with an acquire load
+  // Record copies by two helper lanes, two chunks ahead, into the slot of the chunk
+  // just finished (its update product completed).  Each lane reads a record's flag
+  // with an acquire load (it stalls the lane's warp until the value arrives, which the
+  // helper warps can afford); the producer fenced its stores to the async proxy
+  // before publishing, so the copies need no fence of their own.
+  const bool is_loader = tid == kLoaderA || tid == kLoaderB;
+  const int full_bar = tid == kLoaderA ? CB_FULL : CB_FULLB;
+  int next_load = 0;   // this lane's first chunk not issued yet
+  uint32_t pend = 0u;  // flag word of chunk pend_n
   int pend_n = -1;
-  auto prefetch_flag = [&](int n) {
-    if (n < NT) {
-      pend = ld_acquire_gpu(ready + (n % SRING));
+  // this lane's part of record n, waiting for its flag when `block`; returns whether issued
+  auto issue_part = [&](int n, bool block) -> bool {
+    uint32_t seen = pend_n == n ? pend : 0u;
+    if (seen < static_cast<uint32_t>(n + 1)) {
+      seen = ld_acquire_gpu(ready + (n % SRING));
+      pend = seen;
       pend_n = n;
     }
-  };
-  // this lane's part of record n, waiting for its flag when `block` (else only if the
-  // flag read ahead already shows it); returns whether it was issued
-  auto issue_part = [&](int n, bool block) -> bool {
-    const uint32_t seen = pend_n == n ? pend : 0u;
     if (seen < static_cast<uint32_t>(n + 1)) {
-      if (!block) {
-        prefetch_flag(n);
-        return false;
-      }
+      if (!block) return false;
       if (!wait_flag_geq(ready + (n % SRING), static_cast<uint32_t>(n + 1), WAIT_LIMIT_NS)) {
         timeout(1, n);
         return false;
@@ -1585,236 +1579,264 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     const int sl = n & 1;
     uint8_t* dst = sm + C_SLOT + sl * GSLOT;
     const uint8_t* src = ring + static_cast<size_t>(n % SRING) * GSLOT;
-    if (tid == kLoader) {
-      mbar_arrive_expect_tx(&bars[CB_FULL + sl], REC_A_BYTES);
+    if (tid == kLoaderA) {
+      mbar_arrive_expect_tx_relaxed(&bars[CB_FULL + sl], REC_A_BYTES);
       bulk_load(dst, src, REC_A_BYTES, &bars[CB_FULL + sl]);
     } else {
-      mbar_arrive_expect_tx(&bars[CB_FULLB + sl], REC_BYTES - REC_A_BYTES);
-      bulk_load(dst + REC_A_BYTES, src + REC_A_BYTES, REC_BYTES - REC_A_BYTES, &bars[CB_FULLB + sl]);
+      mbar_arrive_expect_tx_relaxed(&bars[CB_FULLB + sl], REC_BYTES - SR_KRT);
+      bulk_load(dst + SR_KRT, src + SR_KRT, REC_BYTES - SR_KRT, &bars[CB_FULLB + sl]);
     }
 #ifdef KDA_PROFILE
-    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[(tid == kLoader ? 264 : 330) + n] = globaltimer_ns();
+    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[(tid == kLoaderA ? 264 : 330) + n] = globaltimer_ns();
 #endif
     ++next_load;
-    prefetch_flag(n + 1);
     return true;
   };
-  // o-issuer: o rows of chunk mc += Aqk v_new
-  auto issue_o_update = [&](int mc) {  // issuer warp
-    const int sc = mc & 1;
-    constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_B_MN_MAJOR;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      umma_f16_warp(tmem + TA + 128 * sc, d128(C_SLOT + sc * GSLOT + R_AQK - 8192 + ks * 32),
-                    D_VNT + ((sc * 16384 + ks * 2048) >> 4), idesc, 1u);
-    umma_commit_warp(&bars[CB_C]);
-    ++c_issued;
+  // copies up to chunk `upto`: the next one waits for its record if it must, later ones
+  // go only if already announced
+  auto pump = [&](int upto, int must) {
+    while (!failed && next_load <= upto && next_load < NT)
+      if (!issue_part(next_load, next_load <= must)) break;
   };
-  // o-row warps: rows of chunk mc to the output (a full chunk through its v_new
-  // buffer, free once the o update has completed, and two TMA tile stores)
-  auto wait_o = [&](int mc) {
-    if (!mbar_wait(&bars[CB_C], mc & 1, WAIT_LIMIT_NS)) timeout(2, mc);
-    ++c_done;
-    __syncwarp();
-    tc_fence_after();
-  };
-  auto emit_o = [&](int mc) {  // after wait_o(mc)
+
+  // o rows of chunk mc from `ob` (bf16 pairs of tokens 2 t, 2 t + 1 of this thread's value
+  // column): lane pairs (v, v + 1) swap halves, then the even lane stores the pair of value
+  // columns for tokens 2 t and the odd lane for tokens 2 t + 1 (64 contiguous bytes per half-warp)
+  auto store_o = [&](int mc, const uint32_t (&ob)[16]) {
     const int rows = min(C, len - mc * C);
-    float orr[32];
-    tmem_ld32(tmem_addr(tmem, 32 * quad, TA + 128 * (mc & 1) + 32 * cb), orr);
-    tmem_ld_wait();
-    const int c = 32 * (quad - 2) + lane;
-    if (rows == C) {
-      uint8_t* stage = sm + C_VNT + (mc & 1) * 16384;
+    const bool odd = lane & 1;
+    const int t0 = 32 * h + (odd ? 1 : 0);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + (static_cast<size_t>(tok0 + mc * C + t0) * HV + hv) * VD +
+                                                (vcol & ~1));
+    const size_t row2 = static_cast<size_t>(HV) * VD;  // two tokens, in 32-bit words
 #pragma unroll
-      for (int j8 = 0; j8 < 4; ++j8)
-        st_v4(stage + sw128_offset(c, 32 * cb + 8 * j8, 64), pack2(orr[8 * j8], orr[8 * j8 + 1]),
-              pack2(orr[8 * j8 + 2], orr[8 * j8 + 3]), pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]),
-              pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
-      fence_proxy_async_smem();
-      role_sync(NB_OROW, 256);
-      if (tid == kStorer) {
-        const int row0 = static_cast<int>(tok0) + mc * C;
-        tma_store_3d(&maps.o, stage, 0, hv, row0);
-        tma_store_3d(&maps.o, stage + 8192, 64, hv, row0);
-        bulk_commit();
-        store_pending = true;
-      }
-    } else if (c < rows) {
-      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok0 + mc * C + c) * HV + hv) * VD + 32 * cb);
-#pragma unroll
-      for (int j8 = 0; j8 < 4; ++j8)
-        dst[j8] = make_uint4(pack2(orr[8 * j8], orr[8 * j8 + 1]), pack2(orr[8 * j8 + 2], orr[8 * j8 + 3]),
-                             pack2(orr[8 * j8 + 4], orr[8 * j8 + 5]), pack2(orr[8 * j8 + 6], orr[8 * j8 + 7]));
+    for (int t = 0; t < 16; ++t) {
+      const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, ob[t], 1);
+      const uint32_t pairv = odd ? __byte_perm(got, ob[t], 0x7632) : __byte_perm(ob[t], got, 0x5410);
+      if (t0 + 2 * t < rows) dst[t * row2] = pairv;
     }
   };
+  if (is_loader && NT > 0) {
+    issue_part(0, true);
+    pump(1, -1);
+  }
+  if (rec) {  // S^T and its bf16 copy from the initial state (key dims 64 h + [0, 64))
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float st[16];
+      if (p.s0) {
+        const float* src = p.s0 + state_off + vcol;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) st[i] = src[static_cast<size_t>(64 * h + 16 * j + i) * VD];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) st[i] = 0.f;
+      }
+      uint32_t hb[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hb[i] = pack2(st[2 * i], st[2 * i + 1]);
+      tmem_st8u(tl + TSB + 32 * h + 8 * j, hb);
+      tmem_st16(tl + TS + 64 * h + 16 * j, st);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  role_sync(NB_CHAIN_ALL, NTHREADS);
+  tc_fence_after();
 
 #ifdef KDA_PROFILE
   if (tid == 0 && u == 0) reinterpret_cast<uint64_t*>(p.status)[127] = globaltimer_ns();
 #endif
-  if (is_loader && NT > 0) issue_part(0, true);
   for (int m = 0; m < NT; ++m) {
     const int s = m & 1;
     const uint32_t so = C_SLOT + s * GSLOT;
-    uint8_t* slot = sm + so;
-    // part B of chunk m + 1 into the slot of chunk m - 1, once its o update has completed
-    if (tid == kLoaderB && !failed && next_load == m + 1 && m + 1 < NT) {
-      if (m > 0 && !mbar_wait(&bars[CB_C], (m - 1) & 1, WAIT_LIMIT_NS)) timeout(3, m);
-      if (!failed) issue_part(m + 1, true);
-    }
-    __syncwarp();
-    PROF(7);
-    if (warp == kIssuerWarp) {  // [X; O] = [W; qd] S
-      if (!mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
-      __syncwarp();
-    }
-    if (warp == kIssuerWarp && !__any_sync(0xFFFFFFFFu, failed)) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_B_MN_MAJOR;
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_f16_warp(tmem + TA + 128 * s, d128(so + R_WQ + kb * R_W_KB + ks * 32),
-                        D_S + (((kb * 4 + ks) * 2048) >> 4), idesc, (kb | ks) != 0);
-      umma_commit_warp(&bars[CB_A]);
-      ++a_issued;
-    }
-    __syncwarp();
-    if (!mbar_wait(&bars[CB_FULLB + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(5, m);
-#ifdef KDA_PROFILE
-    if (tid == 0 && u == 0 && m < 64) reinterpret_cast<uint64_t*>(p.status)[128 + m] = globaltimer_ns();
-#endif
-    PROF(0);
-    {  // S <- Diag(e^{g_last}) S in TMEM, before the state product adds to it
-      const float gmm = reinterpret_cast<const float*>(slot + R_GAM)[d];
-      float sv[32];
-      tmem_ld32(t_s, sv);
-      tmem_ld_wait();
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) sv[jj] *= gmm;
-      tmem_st32(t_s, sv);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    PROF(1);
-    if (vw) {
-      // ---- v_new = U - X ----
-      if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(6, m);
-      ++a_done;
-      __syncwarp();
-      tc_fence_after();
-      PROF(5);
-      float xr[32];
-      tmem_ld32(tmem_addr(tmem, 32 * quad, TA + 128 * s + 32 * cb), xr);
-      const int c = 32 * quad + lane;
-      uint4 uu[4];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        uu[ch] = *reinterpret_cast<const uint4*>(slot + R_U + sw128_offset(c, 32 * cb + 8 * ch, 64));
-      tmem_ld_wait();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t uw[4] = {uu[ch].x, uu[ch].y, uu[ch].z, uu[ch].w};
-        uint32_t w[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float lo = __uint_as_float(uw[t] << 16) - xr[8 * ch + 2 * t];
-          const float hi = __uint_as_float(uw[t] & 0xFFFF0000u) - xr[8 * ch + 2 * t + 1];
-          w[t] = pack2(lo, hi);
-        }
-        st_v4(sm + C_VNT + s * 16384 + mn_sw128_offset(c, 32 * cb + 8 * ch, 8192), w[0], w[1], w[2], w[3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      PROF(6);
-      role_sync(NB_VNEW, 256);
-      PROF(2);
-      // ---- state product S += kr^T v_new (after the o-row warps scaled their rows),
-      //      then this chunk's o update queued behind it ----
-      if (warp == kIssuerWarp) {
-        if (!mbar_wait(&bars[CB_SCALED], m & 1, WAIT_LIMIT_NS)) timeout(7, m);
+    const uint8_t* slot = sm + so;
+    STAMP(0);
+    if (rec) {
+      if (warp == kIssuerWarp) {  // [O^T | X^T] = S^T [qd; W]^T
+        if (!mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
         __syncwarp();
         if (!__any_sync(0xFFFFFFFFu, failed)) {
           tc_fence_after();
-          constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_B_MN_MAJOR;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_f16_warp(tmem + TS, d128(so + R_KRT + ks * 32), D_VNT + ((s * 16384 + ks * 2048) >> 4), idesc,
-                          1u);
-          umma_commit_warp(&bars[CB_B]);
-          ++b_issued;
-          issue_o_update(m);
+          constexpr uint32_t kstep[4] = {0, 2, 4, 6};  // 32-byte K steps inside a 128-byte swizzled row
+          constexpr uint32_t idesc = idesc_f16kind(128, 128);
+          umma_ts_chain<4>(tmem + TOT, tmem + TSB, d128(so + SR_QW), kstep, idesc, 0u);
+          umma_ts_chain<4>(tmem + TOT, tmem + TSB + 32, d128(so + SR_QW + SR_KB), kstep, idesc, 1u);
+          umma_commit_warp(&bars[CB_A]);
+          ++a_issued;
         }
       }
-    } else {
-      // ---- chunk m - 1's rows (its o update ran during the previous state copy).  The
-      //      wait comes before the arrival that lets this chunk's o update be issued:
-      //      once issued, it could complete first and the parity would repeat ----
-      if (m > 0) wait_o(m - 1);
-      mbar_arrive(&bars[CB_SCALED]);
-      // part A of chunks up to m + 2 once the first product of chunk m has completed
-      // (m + 1 waits for its record if it must, m + 2 goes only if already announced)
-      if (tid == kLoader && !failed) {
-        if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(8, m);
-        if (!failed) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
-        while (!failed && next_load <= m + 2 && next_load < NT)
-          if (!issue_part(next_load, next_load <= m + 1)) break;
+      STAMP(1);
+      {  // S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)), while the first product runs
+        if (warp != kIssuerWarp && !mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
+        const float* gam = reinterpret_cast<const float*>(slot + SR_GAM) + 64 * h;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float sv[16];
+          tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
+          const float4* g4 = reinterpret_cast<const float4*>(gam + 16 * j);
+          float4 g[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) g[i] = g4[i];
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sv[4 * i] *= g[i].x;
+            sv[4 * i + 1] *= g[i].y;
+            sv[4 * i + 2] *= g[i].z;
+            sv[4 * i + 3] *= g[i].w;
+          }
+          tmem_st16(tl + TS + 64 * h + 16 * j, sv);
+        }
       }
-      if (m > 0) emit_o(m - 1);
+      // ---- v_new^T = U^T - X^T: tokens 32 h + [0, 32) of this thread's value column ----
+      if (!mbar_wait(&bars[CB_FULLB + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(5, m);
+      const uint8_t* urow = slot + SR_U + vcol * 128;  // U^T row v (64 tokens, 128-byte-swizzled)
+      STAMP(2);
+      if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(6, m);
+      __syncwarp();
+      tc_fence_after();
+      STAMP(3);
+      {
+        float xv[32];
+        tmem_ld16(tl + TXT + 32 * h, reinterpret_cast<float(&)[16]>(xv[0]));
+        tmem_ld16(tl + TXT + 32 * h + 16, reinterpret_cast<float(&)[16]>(xv[16]));
+        uint4 uu[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) uu[i] = *reinterpret_cast<const uint4*>(urow + (((4 * h + i) ^ (vcol & 7)) << 4));
+        tmem_ld_wait();
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {  // tokens 32 h + 16 q2 + [0, 16)
+          const uint32_t uw[8] = {uu[2 * q2].x, uu[2 * q2].y, uu[2 * q2].z, uu[2 * q2].w,
+                                  uu[2 * q2 + 1].x, uu[2 * q2 + 1].y, uu[2 * q2 + 1].z, uu[2 * q2 + 1].w};
+          uint32_t vn[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            vn[t] = pack2(__uint_as_float(uw[t] << 16) - xv[16 * q2 + 2 * t],
+                          __uint_as_float(uw[t] & 0xFFFF0000u) - xv[16 * q2 + 2 * t + 1]);
+          tmem_st8u(tl + TVN + 16 * h + 8 * q2, vn);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      STAMP(4);
+      role_sync(NB_REC, 256);
+      STAMP(5);
+      if (warp == kIssuerWarp && !__any_sync(0xFFFFFFFFu, failed)) {  // [S^T | O^T] += v_new^T [kr^T; Aqk]^T
+        tc_fence_after();
+        constexpr uint32_t kstep[4] = {0, 2, 4, 6};
+        umma_ts_chain<4>(tmem + TS, tmem + TVN, d128(so + SR_KRT), kstep, idesc_f16kind(128, 192), 1u);
+        umma_commit_warp(&bars[CB_B]);
+        ++b_issued;
+        if (lane == 0) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
+      }
+      STAMP(6);
+      // ---- bf16 copy of S^T for the next chunk's first product (its scaling by the next
+      //      e^{g_last} follows after the barrier, off this path) ----
+      const bool more = m + 1 < NT;
+      if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
+      __syncwarp();
+      tc_fence_after();
+      STAMP(7);
+      if (more) {
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+          float sa[32];
+          tmem_ld32(tl + TS + 64 * h + 16 * j, sa);
+          tmem_ld_wait();
+          uint32_t hb[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hb[i] = pack2(sa[2 * i], sa[2 * i + 1]);
+          tmem_st16u(tl + TSB + 32 * h + 8 * j, hb);
+        }
+        tmem_st_wait();
+      }
+      STAMP(8);
+    } else {
+      // ---- helpers: this chunk's o rows, read before the next chunk's first product
+      //      overwrites them and stored while the recurrence copies the state ----
+      if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
+      __syncwarp();
+      tc_fence_after();
+      const int rows = min(C, len - m * C);
+      if (rows == C) {
+        // o^T tiles to the staging buffer as [token][v] rows (8x8 blocks transposed by
+        // stmatrix; 128-byte swizzle, two 64-column halves), then two TMA tile stores
+        uint8_t* stage = sm + C_STG + (m & 1) * 16384;
+        const int mi = lane >> 3, mr = lane & 7;  // the matrix and row this lane addresses
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // tokens 32 h + 8 j + [0, 8)
+          uint32_t a[4], b[4];
+          tmem_ld_16x256b(tmem_addr(tmem, 32 * quad, TOT + 32 * h + 8 * j), a);
+          tmem_ld_16x256b(tmem_addr(tmem, 32 * quad + 16, TOT + 32 * h + 8 * j), b);
+          tmem_ld_wait();
+          const int c = 32 * h + 8 * j + mr, v = 32 * quad + 8 * mi;
+          stmatrix_x4_trans(smem_u32(stage + (v >> 6) * 8192 + c * 128 + ((((v & 63) >> 3) ^ (c & 7)) << 4)),
+                            pack2(__uint_as_float(a[0]), __uint_as_float(a[1])),
+                            pack2(__uint_as_float(a[2]), __uint_as_float(a[3])),
+                            pack2(__uint_as_float(b[0]), __uint_as_float(b[1])),
+                            pack2(__uint_as_float(b[2]), __uint_as_float(b[3])));
+        }
+        fence_proxy_async_smem();
+        role_sync(NB_HELP, 256);
+        if (tid == kStorer && !failed) {
+          const int row0 = static_cast<int>(tok0) + m * C;
+          tma_store_3d(&maps.o, stage, 0, hv, row0);
+          tma_store_3d(&maps.o, stage + 8192, 64, hv, row0);
+          bulk_commit();
+          bulk_wait_group_read<1>();  // the previous chunk's tiles have been read: its buffer is free
+        }
+      } else {  // a sequence's partial last chunk: plain stores of its rows
+        uint32_t ob[16];  // bf16 pairs (tokens 2 t, 2 t + 1) of this thread's value column
+        float ov[32];
+        tmem_ld32(tl + TOT + 32 * h, ov);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 16; ++t) ob[t] = pack2(ov[2 * t], ov[2 * t + 1]);
+        if (!failed) store_o(m, ob);
+      }
     }
-    __syncwarp();
-    if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
-    ++b_done;
-    __syncwarp();
-    tc_fence_after();
-    PROF(3);
-    {  // bf16 copy of the new state
-      float sv[32];
-      tmem_ld32(t_s, sv);
-      tmem_ld_wait();
-      write_copy(sv);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
-    if (tid == kStorer && store_pending) {
-      bulk_wait_read();  // the o tile staged in a v_new buffer has been read
-      store_pending = false;
-    }
-    PROF(7);
+    STAMP(9);
     if (role_any(NB_CHAIN_ALL, NTHREADS, failed)) {
       aborted = true;
       break;
     }
-    PROF(4);
+    STAMP(10);
+    // record copies into the slot of chunk m, after the barrier: every recurrence warp has
+    // passed its waits on chunk m's copies (so their parity cannot repeat under them), and
+    // the lanes' acquire loads stall only helper warps
+    if (is_loader) pump(m + 2, m + 1);
   }
-  if (!aborted && !failed && NT > 0 && !vw) {
-    __syncwarp();
-    wait_o(NT - 1);
-    emit_o(NT - 1);
-  }
-  if (tid == kIssuer) {  // drain MMAs still in flight after an abort
-    if (a_issued > a_done && !mbar_wait(&bars[CB_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
+  if (tid == kIssuerWarp * 32) {  // drain MMAs still in flight after an abort
+    if (a_issued > 0 && !mbar_wait(&bars[CB_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
       atomicOr(p.status, kStatusTimeout);
-    if (b_issued > b_done && !mbar_wait(&bars[CB_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
-      atomicOr(p.status, kStatusTimeout);
-    if (c_issued > 0 && !mbar_wait(&bars[CB_C], (c_issued - 1) & 1, WAIT_LIMIT_NS))
+    if (b_issued > 0 && !mbar_wait(&bars[CB_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
       atomicOr(p.status, kStatusTimeout);
   }
-  if (tid == KDA_PROFILE_CHAIN_TID) PROF_STORE(16);
+#ifdef KDA_PROFILE
+  __syncwarp();
+  if (u == 0 && (tid == 0 || tid == 256)) {  // the stamps of chunk KDA_STAMP_CHUNK
+    const long long* st = reinterpret_cast<const long long*>(sm + C_MISC + 64 + (tid ? 192 : 0));
+    for (int i = 0; i < 24; ++i) reinterpret_cast<long long*>(p.status)[432 + (tid ? 24 : 0) + i] = st[i];
+  }
+#endif
   if (is_loader)  // copies still in flight after an abort (a consumed phase returns at once)
     for (int n = max(0, next_load - 2); n < next_load; ++n)
       if (!mbar_wait(&bars[full_bar + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
-  if (is_loader || tid == kStorer) bulk_wait_all();
+  if (tid == kStorer) bulk_wait_all();
   __syncwarp();
-  if (p.sfin && !aborted && !failed) {
+  if (rec && p.sfin && !aborted && !failed) {  // S^T -> final state (for each k a warp writes 128 contiguous bytes)
     tc_fence_after();
-    float sv[32];
-    tmem_ld32(t_s, sv);
-    tmem_ld_wait();
-    float4* dst = reinterpret_cast<float4*>(p.sfin + state_off + static_cast<size_t>(d) * VD + 32 * cb);
+    float* dst = p.sfin + state_off + vcol;
 #pragma unroll
-    for (int j4 = 0; j4 < 8; ++j4) dst[j4] = make_float4(sv[4 * j4], sv[4 * j4 + 1], sv[4 * j4 + 2], sv[4 * j4 + 3]);
+    for (int j = 0; j < 2; ++j) {
+      float sv[32];
+      tmem_ld32(tl + TS + 64 * h + 32 * j, sv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(64 * h + 32 * j + i) * VD] = sv[i];
+    }
   }
 }
 }  // namespace split
@@ -1830,8 +1852,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   if (tid == 0) {
     if (is_chain) {
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
-      for (int i = 0; i < 5; ++i) mbar_init(&cb[i], 1);
-      mbar_init(&cb[split::CB_SCALED], 256);
+      for (int i = 0; i < 4; ++i) mbar_init(&cb[i], 1);
       mbar_init(&cb[split::CB_FULLB], 1);
       mbar_init(&cb[split::CB_FULLB + 1], 1);
       tma_prefetch_desc(&maps.o);

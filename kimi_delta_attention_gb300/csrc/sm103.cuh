@@ -37,6 +37,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// The same without release semantics: for a barrier whose phase carries only the
+// bytes of async copies (their complete_tx makes the data visible), so the arriving
+// thread need not wait for its own earlier memory operations.
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -47,6 +55,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// try_wait with a suspend-time hint: the thread may sleep (not issuing) until the phase
+// completes or about `hint_ns` pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait that leaves the issue slots to other warps while it waits.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 // Wait for the phase with the given parity to complete, giving up after
 // `limit_ns` nanoseconds of wall time.  Returns false on timeout.
@@ -132,6 +162,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
         "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
       : "r"(taddr));
 }
+// 16 lanes x 256 bit: thread t gets (lane t/4, columns 2 (t%4) and 2 (t%4) + 1) in r[0], r[1]
+// and the same columns of lane t/4 + 8 in r[2], r[3] -- the m16n8 accumulator fragment.
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 32 lanes x 32 bit, 32 consecutive columns per thread, stored to TMEM.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) {
@@ -145,6 +182,23 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) 
       "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]),
       "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31])
       : "memory");
+}
+// 32 lanes x 32 bit, 16 / 8 consecutive columns per thread, stored to TMEM.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&u)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]),
+      "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) {
+  tmem_st16u(taddr, reinterpret_cast<const uint32_t(&)[16]>(r));
+}
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&u)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(u[0]),
+               "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7])
+               : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -189,7 +243,8 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   d |= static_cast<uint64_t>(layout & 7u) << 61;
   return d;
 }
-// Instruction-descriptor bit selecting an MN-major B operand.
+// Instruction-descriptor bits selecting an MN-major A / B operand.
+constexpr uint32_t IDESC_A_MN_MAJOR = 1u << 15;
 constexpr uint32_t IDESC_B_MN_MAJOR = 1u << 16;
 
 // Byte offset of element (k, n) of an MN-major bf16 operand with N = 32 in the
@@ -219,6 +274,43 @@ __device__ __forceinline__ void umma_f16_warp(uint32_t d_tmem, uint64_t a_desc, 
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by a whole converged warp (one elected lane).
+// A is M lanes x K 16-bit elements packed two per 32-bit column; `a_tmem` addresses
+// lane 0 and the first column of the K-step.
+__device__ __forceinline__ void umma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// NK chained MMAs D (+)= A[tmem] * B[smem]^T issued by a converged warp from one asm block
+// (one elect, no control flow between the MMAs): step k reads the A columns
+// a_tmem + 8 k and the B tile at b_desc + b_step[k] (descriptor units of 16 bytes).
+// The first step accumulates if `accumulate`, the others always do.
+template <int NK>
+__device__ __forceinline__ void umma_ts_chain(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              const uint32_t (&b_step)[NK], uint32_t idesc, uint32_t accumulate);
+template <>
+__device__ __forceinline__ void umma_ts_chain<4>(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 const uint32_t (&b_step)[4], uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.u64 b1, %2, %5;\n\tadd.u64 b2, %2, %6;\n\tadd.u64 b3, %2, %7;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(static_cast<uint64_t>(b_step[1])),
+      "l"(static_cast<uint64_t>(b_step[2])), "l"(static_cast<uint64_t>(b_step[3]))
       : "memory");
 }
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread completes.
@@ -347,6 +439,24 @@ __device__ __forceinline__ void bulk_wait_group() {
 }
 // Wait until every committed bulk store has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Four 8x8 b16 matrices from m16n8-fragment registers to shared memory, transposed: row r
+// of the stored matrix i is column r of the fragment, written at the address lane 8 i + r gives.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+// Shared -> global tile store (bulk async-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 
 // ----------------------------------------------------- warp-level mma.sync ---
 // For products too small for tcgen05 (16 x 8 tiles inside one warp): the
@@ -375,12 +485,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
-}
-// Shared -> global tile store (bulk async-group completion).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
-               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
