@@ -1085,6 +1085,27 @@ __device__ __forceinline__ uint32_t mn_sw128_offset(uint32_t k, uint32_t n, uint
 }
 
 // ------------------------------------------------------------ producer ----
+constexpr int kRecStorer = 32;  // pipeline thread storing qd and kr^T to the ring (warp 1)
+// -DKDA_PROFILE: clock64 stamps of thread 0 of pipeline 0 at numbered points of its
+// record KDA_STAMP_RECORD, written straight to the workspace words [480, 498) (below the
+// record flags at byte kFlagOffset)
+#ifndef KDA_STAMP_RECORD
+#define KDA_STAMP_RECORD 4
+#endif
+#ifdef KDA_PROFILE
+#define PSTAMP(i)                                                                     \
+  do {                                                                                \
+    if (q == 0 && j == KDA_STAMP_RECORD && pt == 0) {                                 \
+      long long t_;                                                                   \
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(t_)::"memory");                    \
+      reinterpret_cast<volatile long long*>(p.status)[480 + (i)] = t_;                \
+    }                                                                                 \
+  } while (0)
+#else
+#define PSTAMP(i) \
+  do {            \
+  } while (0)
+#endif
 __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, uint8_t* sm, uint32_t tmem,
                                          int pipe, int q, int NQ, int NU, int NREC, uint32_t* flags) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1167,6 +1188,8 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
   }
   bool pub_pending = false;
   int pub_m = 0, pub_u = 0;
+  uint32_t flow_seen = 0u;  // consumed-chunk counter of record flow_n's unit, read ahead
+  int flow_n = -1;
   int j = 0;
   for (; r < NREC; ++j) {
     const int rn = next_valid(r + NQ, nx);
@@ -1174,7 +1197,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     uint8_t* gs = p.ring + (static_cast<size_t>(cur.u) * RING + (cur.m % SRING)) * GSLOT;
     const int rows = min(C, cur.len - cur.m * C);
     // ---- 1. raw tiles; the ring slot must have been loaded by the chain ----
+    PSTAMP(0);
     if (!mbar_wait(&bars[PB_RAW], j & 1, WAIT_LIMIT_NS)) timeout();
+    PSTAMP(1);
     if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
     if (pt < C) beta_s[pt] = bpre;
     {
@@ -1187,6 +1212,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       reinterpret_cast<float2*>(gsum + hq * KD)[dp] = qsum;
     }
     if (role_any(NB, PIPE, failed)) break;
+    PSTAMP(2);
     if (pt == 0) raw_pending = false;
 
     // ---- 2. elementwise (as in the cluster kernel); e^{g_last} is held until the
@@ -1251,7 +1277,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     }
     if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's stores have landed
     fence_proxy_async_smem();
+    PSTAMP(3);
     role_sync(NB, PIPE);
+    PSTAMP(4);
     if (pub_pending) {  // from warp 3 of the pipeline while thread 0 issues the MMAs
       if (pw == 3 && lane == 0) publish(pub_m, pub_u);
       pub_pending = false;
@@ -1261,10 +1289,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     //         ring slot is written only once the chain has loaded its previous
     //         occupant; the previous record was published above, so a wait here
     //         never holds back a record some chain needs ----
-    if (pt == 0) {
-      if (cur.m >= SRING && !wait_flag_geq(flags + cur.u * 32 + 16, static_cast<uint32_t>(cur.m - SRING + 1),
-                                          WAIT_LIMIT_NS))
-        timeout();
+    if (pw == 0) {  // the products, issued warp-wide (one elected lane)
       tc_fence_after();
       constexpr uint32_t idesc = idesc_f16kind(64, 64);
 #pragma unroll
@@ -1273,22 +1298,31 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t koff = kb * 8192 + ks * 32;
           const uint64_t bd = d128(P_B + koff);
-          umma_f16(tmem + TM_L, d128(P_KD + koff), bd, idesc, (kb | ks) != 0);
-          umma_f16(tmem + TM_AQ, d128(P_Q + koff), bd, idesc, (kb | ks) != 0);
+          umma_f16_warp(tmem + TM_L, d128(P_KD + koff), bd, idesc, (kb | ks) != 0);
+          umma_f16_warp(tmem + TM_AQ, d128(P_Q + koff), bd, idesc, (kb | ks) != 0);
         }
-      umma_commit(&bars[PB_PMMA]);
+      umma_commit_warp(&bars[PB_PMMA]);
       ++pmma_issued;
-      bulk_store(gs + SR_QW, sm + P_Q, 8192);
-      bulk_store(gs + SR_QW + SR_KB, sm + P_Q + 8192, 8192);
-      bulk_store(gs + SR_KRT, sm + P_STG, 16384);
-      bulk_commit();
+    } else if (pt == kRecStorer) {  // qd and kr^T to the ring slot, once its occupant has been loaded
+      const uint32_t need = static_cast<uint32_t>(cur.m - SRING + 1);
+      if (cur.m >= SRING && !(flow_n == r && flow_seen >= need) &&
+          !wait_flag_geq(flags + cur.u * 32 + 16, need, WAIT_LIMIT_NS))
+        timeout();
+      if (!failed) {
+        bulk_store(gs + SR_QW, sm + P_Q, 8192);
+        bulk_store(gs + SR_QW + SR_KB, sm + P_Q + 8192, 8192);
+        bulk_store(gs + SR_KRT, sm + P_STG, 16384);
+        bulk_commit();
+      }
     }
     if (next) prefetch_gb(nx, 0);
     __syncwarp();
+    PSTAMP(5);
     if (!mbar_wait(&bars[PB_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
     ++pmma_phase;
     tc_fence_after();
-    if (pt == 0) bulk_wait_read();  // qd (about to hold the Aqk staging) and kr^T have been read
+    PSTAMP(6);
+    if (pt == kRecStorer) bulk_wait_read();  // qd (about to hold the Aqk staging) and kr^T have been read
 
     // ---- 4. TMEM -> M (fp32), Aqk -> staging ----
     role_sync(NB, PIPE);
@@ -1326,7 +1360,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     }
     tc_fence_before();
     fence_proxy_async_smem();
+    PSTAMP(7);
     if (role_any(NB, PIPE, failed)) break;
+    PSTAMP(8);
     if (pt == 0) {
       bulk_store(gs + SR_AQK, sm + P_Q, 8192);
       bulk_commit();
@@ -1370,32 +1406,43 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
         st_v4(amat + sw128_offset(16 * br + row, 16 * bc + 8 * half, 64), 0u, 0u, 0u, 0u);
       }
     }
+    PSTAMP(9);
     role_sync(NB, PIPE);
+    PSTAMP(10);
     if (next) prefetch_gb(nx, 2);
     if (pw < 3) inverse_block_columns(mb, beta_s, amat, pw, lane);
     fence_proxy_async_smem();
+    PSTAMP(11);
     role_sync(NB, PIPE);
+    PSTAMP(12);
 
     // ---- 6. W = A kd (M = 64, kd as MN-major B) and U^T = v^T A^T (M = 128 value
     //         columns, v as MN-major A, A as K-major B) ----
-    if (pt == 0) {
+    if (pw == 0) {
       tc_fence_after();
       constexpr uint32_t idesc_w = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
       constexpr uint32_t idesc_u = idesc_f16kind(128, 64) | IDESC_A_MN_MAJOR;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const uint64_t ad = d128(P_AMAT + ks * 32);
-        umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc_w, ks != 0);
-        umma_f16(tmem + TM_U, D_V_MN + ((ks * 2048) >> 4), ad, idesc_u, ks != 0);
+        umma_f16_warp(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc_w, ks != 0);
+        umma_f16_warp(tmem + TM_U, D_V_MN + ((ks * 2048) >> 4), ad, idesc_u, ks != 0);
       }
-      umma_commit(&bars[PB_PMMA]);
+      umma_commit_warp(&bars[PB_PMMA]);
       ++pmma_issued;
+    } else if (pt == kRecStorer && next && nx.m >= SRING) {
+      // the next record's flow-control counter, read ahead while the products run (the
+      // acquire load stalls this warp, which waits for the products anyway)
+      flow_seen = ld_acquire_gpu(flags + nx.u * 32 + 16);
+      flow_n = rn;
     }
     if (next) prefetch_gb(nx, 3);
     __syncwarp();
+    PSTAMP(13);
     if (!mbar_wait(&bars[PB_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
     ++pmma_phase;
     tc_fence_after();
+    PSTAMP(14);
     if (pt == 0 && next && !failed) {
       bulk_wait_read();  // the Aqk staging (in the q buffer) has been read
       issue_raw(nx, j + 1);
@@ -1443,7 +1490,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     tc_fence_before();
     fence_proxy_async_smem();
     fence_proxy_async_global();  // e^{g_last} went out with plain stores
+    PSTAMP(15);
     if (role_any(NB, PIPE, failed)) break;
+    PSTAMP(16);
 
     // ---- 8. W/U to the ring; published early in the next record (or at the end);
     //         a pipeline's first record goes out at once ----
@@ -1462,6 +1511,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       if (pw == 3 && lane == 0) publish(pub_m, pub_u);
       pub_pending = false;
     }
+    PSTAMP(17);
     r = rn;
     cur = nx;
   }

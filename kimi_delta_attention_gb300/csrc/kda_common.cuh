@@ -18,6 +18,7 @@ constexpr uint32_t kStatusBounds = 2u;    // cu_seqlens entry out of order / ran
 // the tensor-core chunk kernels' record rings start at kRingOffset.
 constexpr size_t kWorkspaceBytes = 256;   // minimum (status word only)
 constexpr size_t kFlagOffset = 4096;
+static_assert(kFlagOffset >= 512 * 8, "profile words (uint64 [1, 512)) stay below the flags");
 constexpr int kMaxSplitUnits = 40;        // (sequence, value head) pairs the split kernel takes
 constexpr size_t kFlagBytesPerUnit = 128; // 16 ready flags + a consumed-chunk counter
 constexpr size_t kRingOffset = 16384;
