@@ -1528,25 +1528,28 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 
 // --------------------------------------------------------------- chain ----
 // The recurrence is carried transposed in TMEM (lanes = value columns v): S^T in fp32
-// and as a bf16 copy, v_new^T in bf16, and the products [O^T | X^T].  The bf16
-// matrices are the A operands of the chain's MMAs; their B operands are the record's
-// tiles in shared memory as the producer wrote them:
-//   [O^T | X^T] = S^T [qd; W]^T                         (N = 128, K = 128)
-//   [S^T | O^T] += v_new^T [kr^T; Aqk]^T                (N = 192, K = 64)
-// with S^T scaled by e^{g_last} between chunks.  Warps 0-7 carry the recurrence:
-// warp w reads TMEM lane quadrant w % 4 (v = 32 (w % 4) + lane) and takes half
-// h = w / 4 of the other dimension (tokens 32 h + [0, 32) of v_new, key dims
-// 64 h + [0, 64) of the state).  Warps 8-15 (same quadrants and halves) emit the o
-// rows and copy records ahead; all their waits are off the recurrence's path.
+// and as a bf16 copy, v_new^T in bf16, and the products [O^T | X^T] (two buffers, one
+// per chunk parity).  The bf16 matrices are the A operands of the chain's MMAs; their B
+// operands are the record's tiles in shared memory as the producer wrote them:
+//   [O^T | X^T] = S^T [qd; W]^T      (N = 128, K = 128)
+//   S^T += v_new^T kr                 (N = 128, K = 64)
+//   O^T += v_new^T Aqk^T              (N = 64,  K = 64)
+// with S^T scaled by e^{g_last} between chunks.  Warps 0-7 carry the recurrence: warp w
+// reads TMEM lane quadrant w % 4 (v = 32 (w % 4) + lane) and takes half h = w / 4 of
+// the other dimension (tokens 32 h + [0, 32) of v_new, key dims 64 h + [0, 64) of the
+// state).  The next chunk's first product is issued as soon as these 8 warps have
+// copied the state, into the other [O^T | X^T] buffer.  Warps 8-15 (same quadrants and
+// halves) emit the o rows and copy records ahead; their waits are off the recurrence.
 constexpr int kIssuerWarp = 0;     // issues every chain MMA (a recurrence warp)
 constexpr int kLoaderA = 8 * 32;   // helper lane copying record part A ([qd; W], e^{g_last})
 constexpr int kLoaderB = 12 * 32;  // helper lane copying record part B (kr^T, Aqk, U^T)
-constexpr int CB_FULLB = 6;        // [2] part B of a record (part A completes CB_FULL)
 constexpr int kStorer = 13 * 32;   // helper lane issuing the o tile stores
+constexpr int CB_C = 4;            // [2] o product of a chunk (one barrier per [O^T | X^T] buffer)
+constexpr int CB_FULLB = 6;        // [2] part B of a record (part A completes CB_FULL)
 constexpr uint32_t NB_REC = 4;     // named barrier of the 8 recurrence warps
 constexpr uint32_t NB_HELP = 5;    // named barrier of the 8 helper warps
 constexpr uint32_t C_STG = 2 * GSLOT;  // two 16 KB o staging tiles ([token][v], two 64-column halves)
-constexpr uint32_t TS = 0, TOT = 128, TXT = 192, TSB = 256, TVN = 320;  // TMEM columns
+constexpr uint32_t TS = 0, TSB = 128, TVN = 192, TXO = 256;  // TMEM columns (TXO: two 128-column buffers)
 // -DKDA_PROFILE: clock64 stamps of threads 0 and 256 of chain 0 at numbered points of
 // one chunk, kept in shared memory (cheap enough not to disturb the timing)
 #ifndef KDA_STAMP_CHUNK
@@ -1591,7 +1594,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   const size_t state_off = static_cast<size_t>(u) * KD * VD;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   bool failed = false, aborted = false;
-  int a_issued = 0, b_issued = 0;
+  int a_issued = 0, b_issued = 0, c_issued = 0;
   auto timeout = [&](int id, int at) {
     failed = true;
     atomicOr(p.status, kStatusTimeout);
@@ -1602,10 +1605,10 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
 #endif
   };
   // Record copies by two helper lanes, two chunks ahead, into the slot of the chunk
-  // just finished (its update product completed).  Each lane reads a record's flag
-  // with an acquire load (it stalls the lane's warp until the value arrives, which the
-  // helper warps can afford); the producer fenced its stores to the async proxy
-  // before publishing, so the copies need no fence of their own.
+  // just finished.  Each lane reads a record's flag with an acquire load (it stalls the
+  // lane's warp until the value arrives, which the helper warps can afford); the
+  // producer fenced its stores to the async proxy before publishing, so the copies
+  // need no fence of their own.
   const bool is_loader = tid == kLoaderA || tid == kLoaderB;
   const int full_bar = tid == kLoaderA ? CB_FULL : CB_FULLB;
   int next_load = 0;   // this lane's first chunk not issued yet
@@ -1648,7 +1651,6 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     while (!failed && next_load <= upto && next_load < NT)
       if (!issue_part(next_load, next_load <= must)) break;
   };
-
   // o rows of chunk mc from `ob` (bf16 pairs of tokens 2 t, 2 t + 1 of this thread's value
   // column): lane pairs (v, v + 1) swap halves, then the even lane stores the pair of value
   // columns for tokens 2 t and the odd lane for tokens 2 t + 1 (64 contiguous bytes per half-warp)
@@ -1666,9 +1668,20 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       if (t0 + 2 * t < rows) dst[t * row2] = pairv;
     }
   };
+  // K-step ks (key dims 16 ks + [0, 16)) of [O^T | X^T] (buffer of chunk mc) = S^T [qd; W]^T
+  auto issue_first_product_step = [&](int mc, int ks, bool first) {
+    const uint32_t so = C_SLOT + (mc & 1) * GSLOT;
+    umma_f16_ts_warp(tmem + TXO + 128 * (mc & 1), tmem + TSB + 8 * ks, d128(so + SR_QW + (ks >> 2) * SR_KB + (ks & 3) * 32),
+                     idesc_f16kind(128, 128), first ? 0u : 1u);
+  };
+
+  // Part A of chunk m + 1 is read during chunk m (the next first product is issued at
+  // its end), so that lane waits for record m + 2 at the end of chunk m; part B is
+  // read from chunk m + 1 on and may arrive one chunk later.
+  const int lead = tid == kLoaderA ? 2 : 1;
   if (is_loader && NT > 0) {
     issue_part(0, true);
-    pump(1, -1);
+    pump(1, lead - 1);
   }
   if (rec) {  // S^T and its bf16 copy from the initial state (key dims 64 h + [0, 64))
 #pragma unroll
@@ -1693,6 +1706,17 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   tc_fence_before();
   role_sync(NB_CHAIN_ALL, NTHREADS);
   tc_fence_after();
+  if (warp == kIssuerWarp && NT > 0) {  // the first chunk's first product
+    if (!mbar_wait(&bars[CB_FULL], 0, WAIT_LIMIT_NS)) timeout(4, 0);
+    __syncwarp();
+    if (!__any_sync(0xFFFFFFFFu, failed)) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) issue_first_product_step(0, ks, ks == 0);
+      umma_commit_warp(&bars[CB_A]);
+      ++a_issued;
+    }
+  }
 
 #ifdef KDA_PROFILE
   if (tid == 0 && u == 0) reinterpret_cast<uint64_t*>(p.status)[127] = globaltimer_ns();
@@ -1701,24 +1725,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     const int s = m & 1;
     const uint32_t so = C_SLOT + s * GSLOT;
     const uint8_t* slot = sm + so;
+    const bool more = m + 1 < NT;
     STAMP(0);
     if (rec) {
-      if (warp == kIssuerWarp) {  // [O^T | X^T] = S^T [qd; W]^T
-        if (!mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
-        __syncwarp();
-        if (!__any_sync(0xFFFFFFFFu, failed)) {
-          tc_fence_after();
-          constexpr uint32_t kstep[4] = {0, 2, 4, 6};  // 32-byte K steps inside a 128-byte swizzled row
-          constexpr uint32_t idesc = idesc_f16kind(128, 128);
-          umma_ts_chain<4>(tmem + TOT, tmem + TSB, d128(so + SR_QW), kstep, idesc, 0u);
-          umma_ts_chain<4>(tmem + TOT, tmem + TSB + 32, d128(so + SR_QW + SR_KB), kstep, idesc, 1u);
-          umma_commit_warp(&bars[CB_A]);
-          ++a_issued;
-        }
-      }
-      STAMP(1);
-      {  // S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)), while the first product runs
-        if (warp != kIssuerWarp && !mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
+      // ---- S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)), while the first product runs ----
+      if (!mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
+      {
         const float* gam = reinterpret_cast<const float*>(slot + SR_GAM) + 64 * h;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -1739,18 +1751,19 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
           tmem_st16(tl + TS + 64 * h + 16 * j, sv);
         }
       }
+      STAMP(1);
       // ---- v_new^T = U^T - X^T: tokens 32 h + [0, 32) of this thread's value column ----
       if (!mbar_wait(&bars[CB_FULLB + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(5, m);
       const uint8_t* urow = slot + SR_U + vcol * 128;  // U^T row v (64 tokens, 128-byte-swizzled)
-      STAMP(2);
       if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(6, m);
       __syncwarp();
       tc_fence_after();
-      STAMP(3);
+      STAMP(2);
       {
+        const uint32_t txt = TXO + 128 * s + 64;  // X^T of this chunk
         float xv[32];
-        tmem_ld16(tl + TXT + 32 * h, reinterpret_cast<float(&)[16]>(xv[0]));
-        tmem_ld16(tl + TXT + 32 * h + 16, reinterpret_cast<float(&)[16]>(xv[16]));
+        tmem_ld16(tl + txt + 32 * h, reinterpret_cast<float(&)[16]>(xv[0]));
+        tmem_ld16(tl + txt + 32 * h + 16, reinterpret_cast<float(&)[16]>(xv[16]));
         uint4 uu[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) uu[i] = *reinterpret_cast<const uint4*>(urow + (((4 * h + i) ^ (vcol & 7)) << 4));
@@ -1769,45 +1782,60 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       }
       tmem_st_wait();
       tc_fence_before();
-      STAMP(4);
+      STAMP(3);
       role_sync(NB_REC, 256);
-      STAMP(5);
-      if (warp == kIssuerWarp && !__any_sync(0xFFFFFFFFu, failed)) {  // [S^T | O^T] += v_new^T [kr^T; Aqk]^T
+      STAMP(4);
+      if (warp == kIssuerWarp && !__any_sync(0xFFFFFFFFu, failed)) {  // S^T += v_new^T kr, O^T += v_new^T Aqk^T
         tc_fence_after();
-        constexpr uint32_t kstep[4] = {0, 2, 4, 6};
-        umma_ts_chain<4>(tmem + TS, tmem + TVN, d128(so + SR_KRT), kstep, idesc_f16kind(128, 192), 1u);
+        constexpr uint32_t kstep[4] = {0, 2, 4, 6};  // 32-byte K steps inside a 128-byte swizzled row
+        umma_ts_chain<4>(tmem + TS, tmem + TVN, d128(so + SR_KRT), kstep, idesc_f16kind(128, 128), 1u);
         umma_commit_warp(&bars[CB_B]);
         ++b_issued;
+        umma_ts_chain<4>(tmem + TXO + 128 * s, tmem + TVN, d128(so + SR_AQK), kstep, idesc_f16kind(128, 64), 1u);
+        umma_commit_warp(&bars[CB_C + s]);
+        ++c_issued;
         if (lane == 0) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
       }
-      STAMP(6);
-      // ---- bf16 copy of S^T for the next chunk's first product (its scaling by the next
-      //      e^{g_last} follows after the barrier, off this path) ----
-      const bool more = m + 1 < NT;
+      STAMP(5);
+      // ---- bf16 copy of S^T, then the next chunk's first product into the other buffer ----
       if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
       __syncwarp();
       tc_fence_after();
-      STAMP(7);
+      STAMP(6);
       if (more) {
 #pragma unroll
-        for (int j = 0; j < 4; j += 2) {
-          float sa[32];
-          tmem_ld32(tl + TS + 64 * h + 16 * j, sa);
+        for (int j = 0; j < 4; ++j) {
+          float sv[16];
+          tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
           tmem_ld_wait();
-          uint32_t hb[16];
+          uint32_t hb[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) hb[i] = pack2(sa[2 * i], sa[2 * i + 1]);
-          tmem_st16u(tl + TSB + 32 * h + 8 * j, hb);
+          for (int i = 0; i < 8; ++i) hb[i] = pack2(sv[2 * i], sv[2 * i + 1]);
+          tmem_st8u(tl + TSB + 32 * h + 8 * j, hb);
         }
         tmem_st_wait();
+        tc_fence_before();
+        role_sync(NB_REC, 256);
+        if (warp == kIssuerWarp) {
+          if (!mbar_wait(&bars[CB_FULL + (s ^ 1)], ((m + 1) >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m + 1);
+          __syncwarp();
+          if (!__any_sync(0xFFFFFFFFu, failed)) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) issue_first_product_step(m + 1, ks, ks == 0);
+            umma_commit_warp(&bars[CB_A]);
+            ++a_issued;
+          }
+        }
       }
-      STAMP(8);
+      STAMP(7);
     } else {
-      // ---- helpers: this chunk's o rows, read before the next chunk's first product
-      //      overwrites them and stored while the recurrence copies the state ----
-      if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
+      // ---- helpers: this chunk's o rows once its o product has completed (the buffer is
+      //      rewritten by chunk m + 2's first product, after the barrier below) ----
+      if (!mbar_wait(&bars[CB_C + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(11, m);
       __syncwarp();
       tc_fence_after();
+      const uint32_t tot = TXO + 128 * s;  // O^T of this chunk
       const int rows = min(C, len - m * C);
       if (rows == C) {
         // o^T tiles to the staging buffer as [token][v] rows (8x8 blocks transposed by
@@ -1817,8 +1845,8 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // tokens 32 h + 8 j + [0, 8)
           uint32_t a[4], b[4];
-          tmem_ld_16x256b(tmem_addr(tmem, 32 * quad, TOT + 32 * h + 8 * j), a);
-          tmem_ld_16x256b(tmem_addr(tmem, 32 * quad + 16, TOT + 32 * h + 8 * j), b);
+          tmem_ld_16x256b(tmem_addr(tmem, 32 * quad, tot + 32 * h + 8 * j), a);
+          tmem_ld_16x256b(tmem_addr(tmem, 32 * quad + 16, tot + 32 * h + 8 * j), b);
           tmem_ld_wait();
           const int c = 32 * h + 8 * j + mr, v = 32 * quad + 8 * mi;
           stmatrix_x4_trans(smem_u32(stage + (v >> 6) * 8192 + c * 128 + ((((v & 63) >> 3) ^ (c & 7)) << 4)),
@@ -1839,7 +1867,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       } else {  // a sequence's partial last chunk: plain stores of its rows
         uint32_t ob[16];  // bf16 pairs (tokens 2 t, 2 t + 1) of this thread's value column
         float ov[32];
-        tmem_ld32(tl + TOT + 32 * h, ov);
+        tmem_ld32(tl + tot + 32 * h, ov);
         tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 16; ++t) ob[t] = pack2(ov[2 * t], ov[2 * t + 1]);
@@ -1847,22 +1875,24 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       }
     }
     tc_fence_before();
-    STAMP(9);
+    STAMP(8);
     if (role_any(NB_CHAIN_ALL, NTHREADS, failed)) {
       aborted = true;
       break;
     }
-    STAMP(10);
+    STAMP(9);
     // record copies into the slot of chunk m, after the barrier: every recurrence warp has
     // passed its waits on chunk m's copies (so their parity cannot repeat under them), and
     // the lanes' acquire loads stall only helper warps
-    if (is_loader) pump(m + 2, m + 1);
+    if (is_loader) pump(m + 2, m + lead);
   }
   if (tid == kIssuerWarp * 32) {  // drain MMAs still in flight after an abort
     if (a_issued > 0 && !mbar_wait(&bars[CB_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
       atomicOr(p.status, kStatusTimeout);
     if (b_issued > 0 && !mbar_wait(&bars[CB_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
       atomicOr(p.status, kStatusTimeout);
+    for (int n = max(0, c_issued - 2); n < c_issued; ++n)
+      if (!mbar_wait(&bars[CB_C + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
   }
 #ifdef KDA_PROFILE
   __syncwarp();
@@ -1902,9 +1932,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   if (tid == 0) {
     if (is_chain) {
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
-      for (int i = 0; i < 4; ++i) mbar_init(&cb[i], 1);
-      mbar_init(&cb[split::CB_FULLB], 1);
-      mbar_init(&cb[split::CB_FULLB + 1], 1);
+      for (int i = 0; i < 8; ++i) mbar_init(&cb[i], 1);  // CB_FULL[2], CB_A, CB_B, CB_C[2], CB_FULLB[2]
       tma_prefetch_desc(&maps.o);
     } else {
       for (int pp = 0; pp < 2; ++pp) {
