@@ -302,6 +302,9 @@ def run_gpu(args):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(w, ws), "tflops": tflops,
+        # the token recurrence's own arithmetic, 7 K V flop per token and value head: a
+        # lower bound on any evaluation, reported beside the chunked convention
+        "tflops_recurrent_lower_bound": ws * tokens * HV * 7 * K * V / (ms * 1e-3) / 1e12,
         "roofline_time_ms": max(alg_bytes / (hbm_gbs * 1e9), flops / (bf16_tf * 1e12)) * 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                      "frac": achieved / hbm_gbs, "traffic": load_traffic(kernel_name),
