@@ -1049,13 +1049,21 @@ static_assert(REC_BYTES <= GSLOT, "record fits a ring slot");
 constexpr uint32_t P_Q = 0, P_KD = 16384, P_V = 32768, P_B = 49152, P_MB = P_B, P_AMAT = 66560,
                    P_STG = 74752, P_BETA = 91136, P_GSUM = 91392, P_BAR = 93440, P_STRIDE = 94208;
 // chain region
-constexpr uint32_t C_SLOT = 0;                 // 2 record slots of GSLOT bytes
-constexpr uint32_t C_BAR = 215040;             // (the chain leaves [2 GSLOT, C_BAR) unused)
-constexpr uint32_t C_MISC = C_BAR + 64;        // 215104 tmem base
+// chain region: record part A ([qd; W], e^{g_last}) in three buffers, part B (kr^T, Aqk,
+// U^T) in two, then the o staging tiles
+constexpr uint32_t PA_STRIDE = 33792;          // REC_A_BYTES rounded up to 1 KB
+constexpr uint32_t PB_STRIDE = REC_BYTES - SR_KRT;
+constexpr uint32_t C_PA = 0;
+constexpr uint32_t C_PB = C_PA + 3 * PA_STRIDE;
+constexpr uint32_t C_STG = C_PB + 2 * PB_STRIDE;  // two 16 KB o staging tiles ([token][v], two 64-column halves)
+constexpr uint32_t C_BAR = C_STG + 2 * 16384;
+constexpr uint32_t C_MISC = C_BAR + 128;       // tmem base
 constexpr uint32_t SMEM_BYTES = C_MISC + 448;        // tmem base; profile stamps at C_MISC + 64
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
 static_assert(2 * P_STRIDE <= C_MISC, "producer regions stay below the tmem slot");
-constexpr int CB_FULL = 0, CB_A = 2, CB_B = 3;  // chain barriers (CB_FULL: [2])
+static_assert(PA_STRIDE >= REC_A_BYTES && PA_STRIDE % 1024 == 0 && PB_STRIDE % 1024 == 0 && C_PB % 1024 == 0,
+              "record buffers keep the 1 KB alignment of the swizzled operands");
+constexpr int CB_FULL = 0, CB_A = 3, CB_B = 4;  // chain barriers (CB_FULL: [3], one per part-A buffer)
 constexpr int PB_RAW = 0, PB_PMMA = 1;                     // producer barriers (per pipeline)
 constexpr uint32_t NB_CHAIN_ALL = 3;
 
@@ -1541,14 +1549,15 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 // copied the state, into the other [O^T | X^T] buffer.  Warps 8-15 (same quadrants and
 // halves) emit the o rows and copy records ahead; their waits are off the recurrence.
 constexpr int kIssuerWarp = 0;     // issues every chain MMA (a recurrence warp)
-constexpr int kLoaderA = 8 * 32;   // helper lane copying record part A ([qd; W], e^{g_last})
-constexpr int kLoaderB = 12 * 32;  // helper lane copying record part B (kr^T, Aqk, U^T)
+constexpr int kLoader = 8 * 32;    // helper lane copying the records
 constexpr int kStorer = 13 * 32;   // helper lane issuing the o tile stores
-constexpr int CB_C = 4;            // [2] o product of a chunk (one barrier per [O^T | X^T] buffer)
-constexpr int CB_FULLB = 6;        // [2] part B of a record (part A completes CB_FULL)
+constexpr int CB_C = 5;            // [2] o product of a chunk (one barrier per [O^T | X^T] buffer)
+constexpr int CB_FULLB = 7;        // [2] part B of a record (part A completes CB_FULL)
+constexpr int kChainBars = 9;
+static_assert(C_BAR + 8 * kChainBars <= C_MISC, "chain barriers stay below the tmem slot");
 constexpr uint32_t NB_REC = 4;     // named barrier of the 8 recurrence warps
 constexpr uint32_t NB_HELP = 5;    // named barrier of the 8 helper warps
-constexpr uint32_t C_STG = 2 * GSLOT;  // two 16 KB o staging tiles ([token][v], two 64-column halves)
+constexpr uint32_t NB_SCALED = 6;  // recurrence warps wait (v_new stored), helper warps arrive (S^T scaled)
 constexpr uint32_t TS = 0, TSB = 128, TVN = 192, TXO = 256;  // TMEM columns (TXO: two 128-column buffers)
 // -DKDA_PROFILE: clock64 stamps of threads 0 and 256 of chain 0 at numbered points of
 // one chunk, kept in shared memory (cheap enough not to disturb the timing)
@@ -1604,52 +1613,64 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
                   (static_cast<unsigned long long>(at) << 8) | static_cast<unsigned long long>(id));
 #endif
   };
-  // Record copies by two helper lanes, two chunks ahead, into the slot of the chunk
-  // just finished.  Each lane reads a record's flag with an acquire load (it stalls the
-  // lane's warp until the value arrives, which the helper warps can afford); the
-  // producer fenced its stores to the async proxy before publishing, so the copies
-  // need no fence of their own.
-  const bool is_loader = tid == kLoaderA || tid == kLoaderB;
-  const int full_bar = tid == kLoaderA ? CB_FULL : CB_FULLB;
-  int next_load = 0;   // this lane's first chunk not issued yet
-  uint32_t pend = 0u;  // flag word of chunk pend_n
-  int pend_n = -1;
-  // this lane's part of record n, waiting for its flag when `block`; returns whether issued
-  auto issue_part = [&](int n, bool block) -> bool {
-    uint32_t seen = pend_n == n ? pend : 0u;
-    if (seen < static_cast<uint32_t>(n + 1)) {
-      seen = ld_acquire_gpu(ready + (n % SRING));
-      pend = seen;
-      pend_n = n;
-    }
-    if (seen < static_cast<uint32_t>(n + 1)) {
-      if (!block) return false;
-      if (!wait_flag_geq(ready + (n % SRING), static_cast<uint32_t>(n + 1), WAIT_LIMIT_NS)) {
-        timeout(1, n);
-        return false;
+  // Record copies by one helper lane into the buffers of the chunk finished last: part A
+  // (three buffers) up to two chunks ahead, part B (two buffers) one chunk ahead.  The
+  // lane learns that records are ready from acquire loads of the flags, four ring slots
+  // (one aligned 16-byte group) per load, so that the load's round trip to L2, which
+  // stalls the warp, comes about once every four chunks; part B of a record follows its
+  // part A and needs no read of its own.  The producer fenced its stores to the async
+  // proxy before publishing, so the copies need no fence.
+  const bool is_loader = tid == kLoader;
+  int next_a = 0, next_b = 0;  // first chunk whose part A / part B is not issued yet
+  int known = 0;               // records [0, known) are known to be ready
+  auto read_flags = [&]() {    // the group of ring slots holding record `known`, from it on
+    const int s0 = known % SRING;
+    const uint4 f = ld_acquire_gpu_v4(ready + (s0 & ~3));
+    const uint32_t fv[4] = {f.x, f.y, f.z, f.w};
+    bool run = true;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j >= (s0 & 3) && run) {
+        run = fv[j] >= static_cast<uint32_t>(known + 1);
+        if (run) ++known;
       }
-    }
-    const int sl = n & 1;
-    uint8_t* dst = sm + C_SLOT + sl * GSLOT;
-    const uint8_t* src = ring + static_cast<size_t>(n % SRING) * GSLOT;
-    if (tid == kLoaderA) {
-      mbar_arrive_expect_tx_relaxed(&bars[CB_FULL + sl], REC_A_BYTES);
-      bulk_load(dst, src, REC_A_BYTES, &bars[CB_FULL + sl]);
-    } else {
-      mbar_arrive_expect_tx_relaxed(&bars[CB_FULLB + sl], REC_BYTES - SR_KRT);
-      bulk_load(dst + SR_KRT, src + SR_KRT, REC_BYTES - SR_KRT, &bars[CB_FULLB + sl]);
-    }
-#ifdef KDA_PROFILE
-    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[(tid == kLoaderA ? 264 : 330) + n] = globaltimer_ns();
-#endif
-    ++next_load;
-    return true;
   };
-  // copies up to chunk `upto`: the next one waits for its record if it must, later ones
-  // go only if already announced
-  auto pump = [&](int upto, int must) {
-    while (!failed && next_load <= upto && next_load < NT)
-      if (!issue_part(next_load, next_load <= must)) break;
+  auto issue_a = [&](int n) {
+    const int b = n % 3;
+    mbar_arrive_expect_tx_relaxed(&bars[CB_FULL + b], REC_A_BYTES);
+    bulk_load(sm + C_PA + b * PA_STRIDE, ring + static_cast<size_t>(n % SRING) * GSLOT, REC_A_BYTES, &bars[CB_FULL + b]);
+#ifdef KDA_PROFILE
+    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[264 + n] = globaltimer_ns();
+#endif
+  };
+  auto issue_b = [&](int n) {
+    const int b = n & 1;
+    mbar_arrive_expect_tx_relaxed(&bars[CB_FULLB + b], PB_STRIDE);
+    bulk_load(sm + C_PB + b * PB_STRIDE, ring + static_cast<size_t>(n % SRING) * GSLOT + SR_KRT, PB_STRIDE,
+              &bars[CB_FULLB + b]);
+#ifdef KDA_PROFILE
+    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[330 + n] = globaltimer_ns();
+#endif
+  };
+  auto pump_b = [&](int up_b) {
+    while (next_b <= up_b && next_b < next_a) issue_b(next_b++);
+  };
+  // part A up to chunk up_a (waiting for the records up to must_a), then part B up to up_b
+  auto pump = [&](int up_a, int must_a, int up_b) {
+    while (!failed && next_a <= up_a && next_a < NT) {
+      if (next_a >= known) read_flags();
+      if (next_a >= known) {
+        if (next_a > must_a) break;
+        const uint64_t t0 = globaltimer_ns();
+        while (next_a >= known && globaltimer_ns() - t0 <= WAIT_LIMIT_NS) read_flags();
+        if (next_a >= known) {
+          timeout(1, next_a);
+          break;
+        }
+      }
+      issue_a(next_a++);
+    }
+    if (!failed) pump_b(up_b);
   };
   // o rows of chunk mc from `ob` (bf16 pairs of tokens 2 t, 2 t + 1 of this thread's value
   // column): lane pairs (v, v + 1) swap halves, then the even lane stores the pair of value
@@ -1670,19 +1691,15 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   };
   // K-step ks (key dims 16 ks + [0, 16)) of [O^T | X^T] (buffer of chunk mc) = S^T [qd; W]^T
   auto issue_first_product_step = [&](int mc, int ks, bool first) {
-    const uint32_t so = C_SLOT + (mc & 1) * GSLOT;
+    const uint32_t so = C_PA + (mc % 3) * PA_STRIDE;
     umma_f16_ts_warp(tmem + TXO + 128 * (mc & 1), tmem + TSB + 8 * ks, d128(so + SR_QW + (ks >> 2) * SR_KB + (ks & 3) * 32),
                      idesc_f16kind(128, 128), first ? 0u : 1u);
   };
 
-  // Part A of chunk m + 1 is read during chunk m (the next first product is issued at
-  // its end), so that lane waits for record m + 2 at the end of chunk m; part B is
-  // read from chunk m + 1 on and may arrive one chunk later.
-  const int lead = tid == kLoaderA ? 2 : 1;
-  if (is_loader && NT > 0) {
-    issue_part(0, true);
-    pump(1, lead - 1);
-  }
+  // Part A of chunk m + 1 is read at the end of chunk m (the next first product), part B
+  // of chunk m from its start: during chunk m the lane must have issued part A of m + 1
+  // and part B of m, and may issue part A of m + 2 and part B of m + 1.
+  if (is_loader) pump(2, 0, 1);
   if (rec) {  // S^T and its bf16 copy from the initial state (key dims 64 h + [0, 64))
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -1707,7 +1724,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   role_sync(NB_CHAIN_ALL, NTHREADS);
   tc_fence_after();
   if (warp == kIssuerWarp && NT > 0) {  // the first chunk's first product
-    if (!mbar_wait(&bars[CB_FULL], 0, WAIT_LIMIT_NS)) timeout(4, 0);
+    if (!mbar_wait(&bars[CB_FULL], 0, WAIT_LIMIT_NS)) timeout(4, 0);  // part A of chunk 0
     __syncwarp();
     if (!__any_sync(0xFFFFFFFFu, failed)) {
       tc_fence_after();
@@ -1723,38 +1740,14 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
 #endif
   for (int m = 0; m < NT; ++m) {
     const int s = m & 1;
-    const uint32_t so = C_SLOT + s * GSLOT;
-    const uint8_t* slot = sm + so;
+    const uint32_t sa = C_PA + (m % 3) * PA_STRIDE;      // part A of this chunk
+    const uint32_t sbb = C_PB + s * PB_STRIDE - SR_KRT;  // part B of this chunk (record offsets)
     const bool more = m + 1 < NT;
     STAMP(0);
     if (rec) {
-      // ---- S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)), while the first product runs ----
-      if (!mbar_wait(&bars[CB_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m);
-      {
-        const float* gam = reinterpret_cast<const float*>(slot + SR_GAM) + 64 * h;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float sv[16];
-          tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
-          const float4* g4 = reinterpret_cast<const float4*>(gam + 16 * j);
-          float4 g[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) g[i] = g4[i];
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            sv[4 * i] *= g[i].x;
-            sv[4 * i + 1] *= g[i].y;
-            sv[4 * i + 2] *= g[i].z;
-            sv[4 * i + 3] *= g[i].w;
-          }
-          tmem_st16(tl + TS + 64 * h + 16 * j, sv);
-        }
-      }
-      STAMP(1);
       // ---- v_new^T = U^T - X^T: tokens 32 h + [0, 32) of this thread's value column ----
       if (!mbar_wait(&bars[CB_FULLB + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(5, m);
-      const uint8_t* urow = slot + SR_U + vcol * 128;  // U^T row v (64 tokens, 128-byte-swizzled)
+      const uint8_t* urow = sm + sbb + SR_U + vcol * 128;  // U^T row v (64 tokens, 128-byte-swizzled)
       if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(6, m);
       __syncwarp();
       tc_fence_after();
@@ -1783,18 +1776,21 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       tmem_st_wait();
       tc_fence_before();
       STAMP(3);
-      role_sync(NB_REC, 256);
+      named_bar_sync(NB_SCALED, NTHREADS);  // v_new^T stored; the helpers have scaled S^T
       STAMP(4);
       if (warp == kIssuerWarp && !__any_sync(0xFFFFFFFFu, failed)) {  // S^T += v_new^T kr, O^T += v_new^T Aqk^T
         tc_fence_after();
         constexpr uint32_t kstep[4] = {0, 2, 4, 6};  // 32-byte K steps inside a 128-byte swizzled row
-        umma_ts_chain<4>(tmem + TS, tmem + TVN, d128(so + SR_KRT), kstep, idesc_f16kind(128, 128), 1u);
+        umma_ts_chain<4>(tmem + TS, tmem + TVN, d128(sbb + SR_KRT), kstep, idesc_f16kind(128, 128), 1u);
         umma_commit_warp(&bars[CB_B]);
         ++b_issued;
-        umma_ts_chain<4>(tmem + TXO + 128 * s, tmem + TVN, d128(so + SR_AQK), kstep, idesc_f16kind(128, 64), 1u);
+        umma_ts_chain<4>(tmem + TXO + 128 * s, tmem + TVN, d128(sbb + SR_AQK), kstep, idesc_f16kind(128, 64), 1u);
         umma_commit_warp(&bars[CB_C + s]);
         ++c_issued;
         if (lane == 0) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
+      }
+      if (warp == kIssuerWarp && more) {  // part A of the next chunk (copied a chunk ago), while MMA_b runs
+        if (!mbar_wait(&bars[CB_FULL + (m + 1) % 3], ((m + 1) / 3) & 1, WAIT_LIMIT_NS)) timeout(4, m + 1);
       }
       STAMP(5);
       // ---- bf16 copy of S^T, then the next chunk's first product into the other buffer ----
@@ -1804,20 +1800,19 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       STAMP(6);
       if (more) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float sv[16];
-          tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
+        for (int j = 0; j < 2; ++j) {
+          float sv[32];
+          tmem_ld32(tl + TS + 64 * h + 32 * j, sv);
           tmem_ld_wait();
-          uint32_t hb[8];
+          uint32_t hb[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) hb[i] = pack2(sv[2 * i], sv[2 * i + 1]);
-          tmem_st8u(tl + TSB + 32 * h + 8 * j, hb);
+          for (int i = 0; i < 16; ++i) hb[i] = pack2(sv[2 * i], sv[2 * i + 1]);
+          tmem_st16u(tl + TSB + 32 * h + 16 * j, hb);
         }
         tmem_st_wait();
         tc_fence_before();
         role_sync(NB_REC, 256);
         if (warp == kIssuerWarp) {
-          if (!mbar_wait(&bars[CB_FULL + (s ^ 1)], ((m + 1) >> 1) & 1, WAIT_LIMIT_NS)) timeout(4, m + 1);
           __syncwarp();
           if (!__any_sync(0xFFFFFFFFu, failed)) {
             tc_fence_after();
@@ -1830,7 +1825,37 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       }
       STAMP(7);
     } else {
-      // ---- helpers: this chunk's o rows once its o product has completed (the buffer is
+      // ---- helpers: S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)) while the first
+      //      product runs (it reads the bf16 copy); the state copy of the previous chunk and
+      //      its state product are complete (barrier below) ----
+      if (is_loader) pump_b(m + 1);  // part B of the next chunk (its record is known ready)
+      if (!mbar_wait(&bars[CB_FULL + m % 3], (m / 3) & 1, WAIT_LIMIT_NS)) timeout(4, m);
+      tc_fence_after();
+      {
+        const float* gam = reinterpret_cast<const float*>(sm + sa + SR_GAM) + 64 * h;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float sv[16];
+          tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 g = reinterpret_cast<const float4*>(gam + 16 * j)[i];
+            sv[4 * i] *= g.x;
+            sv[4 * i + 1] *= g.y;
+            sv[4 * i + 2] *= g.z;
+            sv[4 * i + 3] *= g.w;
+          }
+          tmem_st16(tl + TS + 64 * h + 16 * j, sv);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_arrive(NB_SCALED, NTHREADS);
+      STAMP(1);
+      // record copies into the buffers of chunk m - 1 (free since the barrier below)
+      if (is_loader) pump(m + 2, m + 1, m + 1);
+      // ---- this chunk's o rows once its o product has completed (the buffer is
       //      rewritten by chunk m + 2's first product, after the barrier below) ----
       if (!mbar_wait(&bars[CB_C + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(11, m);
       __syncwarp();
@@ -1881,10 +1906,6 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       break;
     }
     STAMP(9);
-    // record copies into the slot of chunk m, after the barrier: every recurrence warp has
-    // passed its waits on chunk m's copies (so their parity cannot repeat under them), and
-    // the lanes' acquire loads stall only helper warps
-    if (is_loader) pump(m + 2, m + lead);
   }
   if (tid == kIssuerWarp * 32) {  // drain MMAs still in flight after an abort
     if (a_issued > 0 && !mbar_wait(&bars[CB_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
@@ -1901,9 +1922,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     for (int i = 0; i < 24; ++i) reinterpret_cast<long long*>(p.status)[432 + (tid ? 24 : 0) + i] = st[i];
   }
 #endif
-  if (is_loader)  // copies still in flight after an abort (a consumed phase returns at once)
-    for (int n = max(0, next_load - 2); n < next_load; ++n)
-      if (!mbar_wait(&bars[full_bar + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+  if (is_loader) {  // copies still in flight after an abort (a consumed phase returns at once)
+    for (int n = max(0, next_a - 3); n < next_a; ++n)
+      if (!mbar_wait(&bars[CB_FULL + n % 3], (n / 3) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    for (int n = max(0, next_b - 2); n < next_b; ++n)
+      if (!mbar_wait(&bars[CB_FULLB + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+  }
   if (tid == kStorer) bulk_wait_all();
   __syncwarp();
   if (rec && p.sfin && !aborted && !failed) {  // S^T -> final state (for each k a warp writes 128 contiguous bytes)
@@ -1932,7 +1956,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   if (tid == 0) {
     if (is_chain) {
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
-      for (int i = 0; i < 8; ++i) mbar_init(&cb[i], 1);  // CB_FULL[2], CB_A, CB_B, CB_C[2], CB_FULLB[2]
+      for (int i = 0; i < split::kChainBars; ++i) mbar_init(&cb[i], 1);  // CB_FULL[3], CB_A, CB_B, CB_C[2], CB_FULLB[2]
       tma_prefetch_desc(&maps.o);
     } else {
       for (int pp = 0; pp < 2; ++pp) {

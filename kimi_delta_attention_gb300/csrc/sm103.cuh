@@ -103,6 +103,11 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Arrive on a named barrier without waiting: the threads that bar.sync on it with the
+// same count wait for this arrival (and see this thread's earlier memory operations).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // Named barrier that also ORs a per-thread predicate across the `count`
 // participating threads; every thread receives the same result.
 __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
@@ -391,6 +396,15 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Four consecutive flags (16-byte aligned) read with one acquire load.
+__device__ __forceinline__ uint4 ld_acquire_gpu_v4(const uint32_t* p) {
+  uint4 v;
+  asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
   return v;
 }
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
