@@ -1063,7 +1063,7 @@ constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
 static_assert(2 * P_STRIDE <= C_MISC, "producer regions stay below the tmem slot");
 static_assert(PA_STRIDE >= REC_A_BYTES && PA_STRIDE % 1024 == 0 && PB_STRIDE % 1024 == 0 && C_PB % 1024 == 0,
               "record buffers keep the 1 KB alignment of the swizzled operands");
-constexpr int CB_FULL = 0, CB_A = 3, CB_B = 4;  // chain barriers (CB_FULL: [3], one per part-A buffer)
+constexpr int CB_FULL = 0, CB_B = 3;  // chain barriers (CB_FULL: [3], one per part-A buffer)
 constexpr int PB_RAW = 0, PB_PMMA = 1;                     // producer barriers (per pipeline)
 constexpr uint32_t NB_CHAIN_ALL = 3;
 
@@ -1551,13 +1551,17 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 constexpr int kIssuerWarp = 0;     // issues every chain MMA (a recurrence warp)
 constexpr int kLoader = 8 * 32;    // helper lane copying the records
 constexpr int kStorer = 13 * 32;   // helper lane issuing the o tile stores
-constexpr int CB_C = 5;            // [2] o product of a chunk (one barrier per [O^T | X^T] buffer)
-constexpr int CB_FULLB = 7;        // [2] part B of a record (part A completes CB_FULL)
+constexpr int CB_C = 4;            // [2] o product of a chunk (one barrier per [O^T | X^T] buffer)
+// [2] per chunk parity: part B of the chunk's record has landed and its first product has
+// completed (two arrivals: the copying lane's, with the bytes, and the product's commit)
+constexpr int CB_AB = 6;
+constexpr int CB_DRAIN = 8;        // every chain MMA issued has completed (end of the chain)
 constexpr int kChainBars = 9;
 static_assert(C_BAR + 8 * kChainBars <= C_MISC, "chain barriers stay below the tmem slot");
-constexpr uint32_t NB_REC = 4;     // named barrier of the 8 recurrence warps
 constexpr uint32_t NB_HELP = 5;    // named barrier of the 8 helper warps
 constexpr uint32_t NB_SCALED = 6;  // recurrence warps wait (v_new stored), helper warps arrive (S^T scaled)
+constexpr uint32_t NB_COPIED = 7;  // helper warps wait, recurrence warps arrive (bf16 copy of S^T taken)
+constexpr uint32_t NB_OREAD = 8;   // recurrence warps wait, helper warps arrive (O^T of the chunk before read)
 constexpr uint32_t TS = 0, TSB = 128, TVN = 192, TXO = 256;  // TMEM columns (TXO: two 128-column buffers)
 // -DKDA_PROFILE: clock64 stamps of threads 0 and 256 of chain 0 at numbered points of
 // one chunk, kept in shared memory (cheap enough not to disturb the timing)
@@ -1602,7 +1606,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   const uint32_t tl = tmem_addr(tmem, 32 * quad, 0);  // this warp's lane quadrant
   const size_t state_off = static_cast<size_t>(u) * KD * VD;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-  bool failed = false, aborted = false;
+  bool failed = false;
   int a_issued = 0, b_issued = 0, c_issued = 0;
   auto timeout = [&](int id, int at) {
     failed = true;
@@ -1613,11 +1617,16 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
                   (static_cast<unsigned long long>(at) << 8) | static_cast<unsigned long long>(id));
 #endif
   };
+  // a bounded wait, skipped once this thread has given up (the loop then runs to its end
+  // without work, passing every named barrier the same number of times as the others)
+  auto wait = [&](uint64_t* bar, uint32_t parity, int id, int at) {
+    if (!failed && !mbar_wait(bar, parity, WAIT_LIMIT_NS)) timeout(id, at);
+  };
   // Record copies by one helper lane into the buffers of the chunk finished last: part A
   // (three buffers) up to two chunks ahead, part B (two buffers) one chunk ahead.  The
-  // lane learns that records are ready from acquire loads of the flags, four ring slots
-  // (one aligned 16-byte group) per load, so that the load's round trip to L2, which
-  // stalls the warp, comes about once every four chunks; part B of a record follows its
+  // lane learns that records are ready from acquire loads of the flags, eight ring slots
+  // (one aligned 32-byte group) per load, so that the load's round trip to L2, which
+  // stalls the warp, comes about once every eight chunks; part B of a record follows its
   // part A and needs no read of its own.  The producer fenced its stores to the async
   // proxy before publishing, so the copies need no fence.
   const bool is_loader = tid == kLoader;
@@ -1625,12 +1634,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   int known = 0;               // records [0, known) are known to be ready
   auto read_flags = [&]() {    // the group of ring slots holding record `known`, from it on
     const int s0 = known % SRING;
-    const uint4 f = ld_acquire_gpu_v4(ready + (s0 & ~3));
-    const uint32_t fv[4] = {f.x, f.y, f.z, f.w};
+    uint32_t fv[8];
+    ld_acquire_gpu_v8(ready + (s0 & ~7), fv);
     bool run = true;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j >= (s0 & 3) && run) {
+    for (int j = 0; j < 8; ++j)
+      if (j >= (s0 & 7) && run) {
         run = fv[j] >= static_cast<uint32_t>(known + 1);
         if (run) ++known;
       }
@@ -1645,9 +1654,9 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   };
   auto issue_b = [&](int n) {
     const int b = n & 1;
-    mbar_arrive_expect_tx_relaxed(&bars[CB_FULLB + b], PB_STRIDE);
+    mbar_arrive_expect_tx_relaxed(&bars[CB_AB + b], PB_STRIDE);
     bulk_load(sm + C_PB + b * PB_STRIDE, ring + static_cast<size_t>(n % SRING) * GSLOT + SR_KRT, PB_STRIDE,
-              &bars[CB_FULLB + b]);
+              &bars[CB_AB + b]);
 #ifdef KDA_PROFILE
     if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[330 + n] = globaltimer_ns();
 #endif
@@ -1730,7 +1739,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) issue_first_product_step(0, ks, ks == 0);
-      umma_commit_warp(&bars[CB_A]);
+      umma_commit_warp(&bars[CB_AB]);
       ++a_issued;
     }
   }
@@ -1738,17 +1747,15 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
 #ifdef KDA_PROFILE
   if (tid == 0 && u == 0) reinterpret_cast<uint64_t*>(p.status)[127] = globaltimer_ns();
 #endif
-  for (int m = 0; m < NT; ++m) {
-    const int s = m & 1;
-    const uint32_t sa = C_PA + (m % 3) * PA_STRIDE;      // part A of this chunk
-    const uint32_t sbb = C_PB + s * PB_STRIDE - SR_KRT;  // part B of this chunk (record offsets)
-    const bool more = m + 1 < NT;
-    STAMP(0);
-    if (rec) {
+  if (rec) {
+    for (int m = 0; m < NT; ++m) {
+      const int s = m & 1;
+      const uint32_t sbb = C_PB + s * PB_STRIDE - SR_KRT;  // part B of this chunk (record offsets)
+      const bool more = m + 1 < NT;
+      STAMP(0);
       // ---- v_new^T = U^T - X^T: tokens 32 h + [0, 32) of this thread's value column ----
-      if (!mbar_wait(&bars[CB_FULLB + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(5, m);
+      wait(&bars[CB_AB + s], (m >> 1) & 1, 6, m);  // part B landed, X^T computed
       const uint8_t* urow = sm + sbb + SR_U + vcol * 128;  // U^T row v (64 tokens, 128-byte-swizzled)
-      if (!mbar_wait(&bars[CB_A], m & 1, WAIT_LIMIT_NS)) timeout(6, m);
       __syncwarp();
       tc_fence_after();
       STAMP(2);
@@ -1789,12 +1796,11 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         ++c_issued;
         if (lane == 0) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
       }
-      if (warp == kIssuerWarp && more) {  // part A of the next chunk (copied a chunk ago), while MMA_b runs
-        if (!mbar_wait(&bars[CB_FULL + (m + 1) % 3], ((m + 1) / 3) & 1, WAIT_LIMIT_NS)) timeout(4, m + 1);
-      }
+      if (warp == kIssuerWarp && more)  // part A of the next chunk (copied a chunk ago), while MMA_b runs
+        wait(&bars[CB_FULL + (m + 1) % 3], ((m + 1) / 3) & 1, 4, m + 1);
       STAMP(5);
       // ---- bf16 copy of S^T, then the next chunk's first product into the other buffer ----
-      if (!mbar_wait(&bars[CB_B], m & 1, WAIT_LIMIT_NS)) timeout(9, m);
+      wait(&bars[CB_B], m & 1, 9, m);
       __syncwarp();
       tc_fence_after();
       STAMP(6);
@@ -1811,61 +1817,38 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         }
         tmem_st_wait();
         tc_fence_before();
-        role_sync(NB_REC, 256);
+        named_bar_arrive(NB_COPIED, NTHREADS);  // the helpers may scale S^T for the next chunk
+        // the copy is complete, and the helpers have read O^T of chunk m - 1 from the buffer
+        // the next first product overwrites
+        named_bar_sync(NB_OREAD, NTHREADS);
         if (warp == kIssuerWarp) {
           __syncwarp();
           if (!__any_sync(0xFFFFFFFFu, failed)) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) issue_first_product_step(m + 1, ks, ks == 0);
-            umma_commit_warp(&bars[CB_A]);
+            umma_commit_warp(&bars[CB_AB + (s ^ 1)]);
             ++a_issued;
           }
         }
       }
       STAMP(7);
-    } else {
-      // ---- helpers: S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)) while the first
-      //      product runs (it reads the bf16 copy); the state copy of the previous chunk and
-      //      its state product are complete (barrier below) ----
-      if (is_loader) pump_b(m + 1);  // part B of the next chunk (its record is known ready)
-      if (!mbar_wait(&bars[CB_FULL + m % 3], (m / 3) & 1, WAIT_LIMIT_NS)) timeout(4, m);
-      tc_fence_after();
-      {
-        const float* gam = reinterpret_cast<const float*>(sm + sa + SR_GAM) + 64 * h;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float sv[16];
-          tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 g = reinterpret_cast<const float4*>(gam + 16 * j)[i];
-            sv[4 * i] *= g.x;
-            sv[4 * i + 1] *= g.y;
-            sv[4 * i + 2] *= g.z;
-            sv[4 * i + 3] *= g.w;
-          }
-          tmem_st16(tl + TS + 64 * h + 16 * j, sv);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      named_bar_arrive(NB_SCALED, NTHREADS);
-      STAMP(1);
-      // record copies into the buffers of chunk m - 1 (free since the barrier below)
-      if (is_loader) pump(m + 2, m + 1, m + 1);
-      // ---- this chunk's o rows once its o product has completed (the buffer is
-      //      rewritten by chunk m + 2's first product, after the barrier below) ----
-      if (!mbar_wait(&bars[CB_C + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout(11, m);
+    }
+  } else {
+    // ---- helpers, one step behind on the o rows: in step m the state scale of chunk m,
+    //      then the o rows of chunk m - 1 (its o product has completed; the buffer is
+    //      rewritten by the first product of chunk m + 1, issued after the arrival below),
+    //      then the record copies ----
+    auto emit_o = [&](int mc) {
+      wait(&bars[CB_C + (mc & 1)], (mc >> 1) & 1, 11, mc);
       __syncwarp();
       tc_fence_after();
-      const uint32_t tot = TXO + 128 * s;  // O^T of this chunk
-      const int rows = min(C, len - m * C);
+      const uint32_t tot = TXO + 128 * (mc & 1);  // O^T of this chunk
+      const int rows = min(C, len - mc * C);
       if (rows == C) {
         // o^T tiles to the staging buffer as [token][v] rows (8x8 blocks transposed by
         // stmatrix; 128-byte swizzle, two 64-column halves), then two TMA tile stores
-        uint8_t* stage = sm + C_STG + (m & 1) * 16384;
+        uint8_t* stage = sm + C_STG + (mc & 1) * 16384;
         const int mi = lane >> 3, mr = lane & 7;  // the matrix and row this lane addresses
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // tokens 32 h + 8 j + [0, 8)
@@ -1883,7 +1866,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         fence_proxy_async_smem();
         role_sync(NB_HELP, 256);
         if (tid == kStorer && !failed) {
-          const int row0 = static_cast<int>(tok0) + m * C;
+          const int row0 = static_cast<int>(tok0) + mc * C;
           tma_store_3d(&maps.o, stage, 0, hv, row0);
           tma_store_3d(&maps.o, stage + 8192, 64, hv, row0);
           bulk_commit();
@@ -1896,24 +1879,61 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 16; ++t) ob[t] = pack2(ov[2 * t], ov[2 * t + 1]);
-        if (!failed) store_o(m, ob);
+        if (!failed) store_o(mc, ob);
       }
+    };
+    for (int m = 0; m <= NT; ++m) {
+      const uint32_t sa = C_PA + (m % 3) * PA_STRIDE;  // part A of this chunk
+      STAMP(0);
+      if (m < NT) {
+        // ---- helpers: S^T <- S^T Diag(e^{g_last}) (key dims 64 h + [0, 64)) while the first
+        //      product runs (it reads the bf16 copy), once the previous chunk's state copy is
+        //      done (its state product completed before) ----
+        if (m > 0) named_bar_sync(NB_COPIED, NTHREADS);
+        tc_fence_after();
+        // part B of the next chunk (its record is known ready) into the buffer of chunk m - 1:
+        // that chunk's v_new preceded its state copy, its products completed before CB_C
+        if (is_loader) pump_b(m + 1);
+        wait(&bars[CB_FULL + m % 3], (m / 3) & 1, 4, m);
+        {
+          const float* gam = reinterpret_cast<const float*>(sm + sa + SR_GAM) + 64 * h;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float sv[16];
+            tmem_ld16(tl + TS + 64 * h + 16 * j, sv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 g = reinterpret_cast<const float4*>(gam + 16 * j)[i];
+              sv[4 * i] *= g.x;
+              sv[4 * i + 1] *= g.y;
+              sv[4 * i + 2] *= g.z;
+              sv[4 * i + 3] *= g.w;
+            }
+            tmem_st16(tl + TS + 64 * h + 16 * j, sv);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar_arrive(NB_SCALED, NTHREADS);
+        STAMP(1);
+      }
+      if (m > 0) {
+        if (m == NT) role_sync(NB_HELP, 256);  // the storer's last wait precedes the staging writes
+        emit_o(m - 1);
+      }
+      if (m + 1 < NT) {
+        tc_fence_before();
+        named_bar_arrive(NB_OREAD, NTHREADS);
+      }
+      // part A of chunk m + 2 into the buffer of chunk m - 1 (free, as above)
+      if (is_loader && m < NT) pump(m + 2, m + 1, m + 1);
+      STAMP(8);
     }
-    tc_fence_before();
-    STAMP(8);
-    if (role_any(NB_CHAIN_ALL, NTHREADS, failed)) {
-      aborted = true;
-      break;
-    }
-    STAMP(9);
   }
-  if (tid == kIssuerWarp * 32) {  // drain MMAs still in flight after an abort
-    if (a_issued > 0 && !mbar_wait(&bars[CB_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
-      atomicOr(p.status, kStatusTimeout);
-    if (b_issued > 0 && !mbar_wait(&bars[CB_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
-      atomicOr(p.status, kStatusTimeout);
-    for (int n = max(0, c_issued - 2); n < c_issued; ++n)
-      if (!mbar_wait(&bars[CB_C + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+  if (warp == kIssuerWarp && a_issued + b_issued + c_issued > 0) {  // MMAs still in flight after a failure
+    umma_commit_warp(&bars[CB_DRAIN]);
+    if (lane == 0 && !mbar_wait(&bars[CB_DRAIN], 0, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
   }
 #ifdef KDA_PROFILE
   __syncwarp();
@@ -1925,12 +1945,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   if (is_loader) {  // copies still in flight after an abort (a consumed phase returns at once)
     for (int n = max(0, next_a - 3); n < next_a; ++n)
       if (!mbar_wait(&bars[CB_FULL + n % 3], (n / 3) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
-    for (int n = max(0, next_b - 2); n < next_b; ++n)
-      if (!mbar_wait(&bars[CB_FULLB + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    for (int n = max(0, next_b - 2); n < next_b; ++n)  // (after a failure the phase may lack its commit)
+      if (!mbar_wait(&bars[CB_AB + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
   }
   if (tid == kStorer) bulk_wait_all();
   __syncwarp();
-  if (rec && p.sfin && !aborted && !failed) {  // S^T -> final state (for each k a warp writes 128 contiguous bytes)
+  if (rec && p.sfin && !failed) {  // S^T -> final state (for each k a warp writes 128 contiguous bytes)
     tc_fence_after();
     float* dst = p.sfin + state_off + vcol;
 #pragma unroll
@@ -1956,7 +1976,8 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   if (tid == 0) {
     if (is_chain) {
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
-      for (int i = 0; i < split::kChainBars; ++i) mbar_init(&cb[i], 1);  // CB_FULL[3], CB_A, CB_B, CB_C[2], CB_FULLB[2]
+      for (int i = 0; i < split::kChainBars; ++i)  // CB_FULL[3], CB_B, CB_C[2], CB_AB[2], CB_DRAIN
+        mbar_init(&cb[i], i == split::CB_AB || i == split::CB_AB + 1 ? 2 : 1);
       tma_prefetch_desc(&maps.o);
     } else {
       for (int pp = 0; pp < 2; ++pp) {
@@ -1980,7 +2001,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   const uint32_t tmem = *tmem_slot;
   if (is_chain) {
     split::chain(maps, p, sm, tmem, static_cast<int>(blockIdx.x), flags);
-  } else {
+  } else {  // records r = m NU + u, strided over the producer pipelines
     const int pipe = tid >> 8;
     const int pb = static_cast<int>(blockIdx.x) - NU;
     const int NQ = 2 * (static_cast<int>(gridDim.x) - NU);
