@@ -1892,8 +1892,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         if (m > 0) named_bar_sync(NB_COPIED, NTHREADS);
         tc_fence_after();
         // part B of the next chunk (its record is known ready) into the buffer of chunk m - 1:
-        // that chunk's v_new preceded its state copy, its products completed before CB_C
-        if (is_loader) pump_b(m + 1);
+        // that chunk's v_new preceded its state copy and its state product completed before
+        // it; its o product, which reads Aqk there, is waited for here
+        if (is_loader) {
+          if (m > 0) wait(&bars[CB_C + ((m - 1) & 1)], ((m - 1) >> 1) & 1, 11, m - 1);
+          pump_b(m + 1);
+        }
         wait(&bars[CB_FULL + m % 3], (m / 3) & 1, 4, m);
         {
           const float* gam = reinterpret_cast<const float*>(sm + sa + SR_GAM) + 64 * h;
