@@ -1547,7 +1547,10 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 // the other dimension (tokens 32 h + [0, 32) of v_new, key dims 64 h + [0, 64) of the
 // state).  The next chunk's first product is issued as soon as these 8 warps have
 // copied the state, into the other [O^T | X^T] buffer.  Warps 8-15 (same quadrants and
-// halves) emit the o rows and copy records ahead; their waits are off the recurrence.
+// halves) scale S^T for each chunk while its first product runs, emit the o rows one
+// chunk behind, and (one lane) copy the records ahead.  The two groups meet only on named
+// barriers that one side waits on and the other arrives at; each arrival of one group
+// follows the other group's passage of that barrier's previous phase.
 constexpr int kIssuerWarp = 0;     // issues every chain MMA (a recurrence warp)
 constexpr int kLoader = 8 * 32;    // helper lane copying the records
 constexpr int kStorer = 13 * 32;   // helper lane issuing the o tile stores
@@ -1817,10 +1820,12 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         }
         tmem_st_wait();
         tc_fence_before();
-        named_bar_arrive(NB_COPIED, NTHREADS);  // the helpers may scale S^T for the next chunk
         // the copy is complete, and the helpers have read O^T of chunk m - 1 from the buffer
-        // the next first product overwrites
+        // the next first product overwrites; only then may the helpers go on to the next
+        // chunk (scaling S^T for it), so that they never arrive at a named barrier before
+        // the recurrence warps have left its previous phase
         named_bar_sync(NB_OREAD, NTHREADS);
+        named_bar_arrive(NB_COPIED, NTHREADS);
         if (warp == kIssuerWarp) {
           __syncwarp();
           if (!__any_sync(0xFFFFFFFFu, failed)) {
