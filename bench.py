@@ -328,39 +328,57 @@ def run_gpu(args):
 def e2e_measure(kda, host, dev, stream, steps):
     """Same metric through kda_chunk_fwd with host buffers: every step copies the
     inputs from pinned host memory to the device, runs the forward and copies o
-    and the final state back."""
+    and the final state back.  Steps alternate between two streams with their own
+    device buffers and workspaces, so that one step's copies overlap the previous
+    step's forward; each stream keeps its own steps in order.  (Splitting a step's
+    input copies over several streams did not raise the host-to-device rate, ~195 GB/s.)"""
     import torch
     pin = lambda t: t.pin_memory()
     hq, hk, hv, hg, hb = (pin(t) for t in (host.q, host.k, host.v, host.g, host.beta))
-    dq, dk, dv, dg, db = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, hg, hb))
-    ho = torch.empty(host.v.shape, dtype=host.v.dtype).pin_memory()
     B, T, H, K = host.q.shape
     HV, V = host.v.shape[2], host.v.shape[3]
-    hs = torch.empty((B, HV, K, V), dtype=torch.float32).pin_memory()
-    do = torch.empty_like(dv)
-    ds = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
-    d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
-
-    def step():
-        for d, h in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb)):
-            d.copy_(h, non_blocking=True)
-        kda.kda_chunk_fwd(dq, dk, dv, dg, db, host.scale, out=do, final_state=ds, stream=stream.cuda_stream)
-        ho.copy_(do, non_blocking=True)
-        hs.copy_(ds, non_blocking=True)
-
+    shape = kda.make_shape(hq, hv)
+    wsz = kda.kda_chunk_fwd_workspace_size(shape)
+    streams = [stream, torch.cuda.Stream(dev)]
+    bufs = []
     for _ in range(2):
-        step()
+        d = {n: torch.empty_like(t, device=dev) for n, t in (("q", hq), ("k", hk), ("v", hv), ("g", hg), ("b", hb))}
+        d["o"] = torch.empty_like(d["v"])
+        d["s"] = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
+        d["ws"] = torch.empty(wsz, dtype=torch.uint8, device=dev)
+        d["ho"] = torch.empty(host.v.shape, dtype=host.v.dtype).pin_memory()
+        d["hs"] = torch.empty((B, HV, K, V), dtype=torch.float32).pin_memory()
+        bufs.append(d)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+    d2h = bufs[0]["ho"].numel() * bufs[0]["ho"].element_size() + bufs[0]["hs"].numel() * 4
+
+    def step(i):
+        d, st = bufs[i & 1], streams[i & 1]
+        with torch.cuda.stream(st):
+            for n, h in (("q", hq), ("k", hk), ("v", hv), ("g", hg), ("b", hb)):
+                d[n].copy_(h, non_blocking=True)
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], host.scale, out=d["o"], final_state=d["s"],
+                              workspace=d["ws"], stream=st.cuda_stream)
+            d["ho"].copy_(d["o"], non_blocking=True)
+            d["hs"].copy_(d["s"], non_blocking=True)
+
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for i in range(steps):
+        step(i)
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    status = max(kda.kda_read_device_status(d["ws"]) for d in bufs)
     return {"value": B * T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "overlap": "two streams, double-buffered: a step's copies overlap the previous step's forward",
+            "device_status": status}
 
 
 def main():
