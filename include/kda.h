@@ -160,7 +160,8 @@ KDA_API const char* kda_chunk_fwd_kernel_name(const kda_shape* shape);
  * (the device status word and the chunk kernel's record rings) in one
  * fixed-size array compiled into the library, on every device that loads the
  * library, for the life of the process: about 36.5 MiB
- * (KDA_STATIC_SCRATCH_MAX_UNITS record rings + 1 KiB).
+ * (KDA_STATIC_SCRATCH_MAX_UNITS record rings + 16 KiB of status word and
+ * record flags).
  *
  *   - Capacity: at most KDA_STATIC_SCRATCH_MAX_UNITS (sequence, value head)
  *     pairs per call (num_seqs or B, times HV); larger problems return
@@ -168,11 +169,12 @@ KDA_API const char* kda_chunk_fwd_kernel_name(const kda_shape* shape);
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *     The first call on each device looks up that device's copy of the array
  *     (cudaGetSymbolAddress) and caches it; make that first call outside any
- *     stream capture.  Later calls only enqueue a 4-byte memset of the status
- *     word and the kernel.
+ *     stream capture.  Later calls only enqueue a memset of the status word
+ *     (with the split kernel, also of its record flags: 4 KiB + 128 bytes per
+ *     unit) and the kernel.
  *   - Every call on a device shares the one array and leaves its contents
- *     behind; the status word is cleared at the start of each call and the
- *     rings need no clearing.  Calls whose work overlaps on the GPU (other
+ *     behind; the status word (and the split kernel's flags) are cleared at
+ *     the start of each call and the rings need no clearing.  Calls whose work overlaps on the GPU (other
  *     streams, other host threads) race on the array and corrupt each other:
  *     order them on one stream.
  *   - status_word: if not NULL, receives the device address of the status
