@@ -132,19 +132,30 @@ def _forward(entry: str, q, k, v, g, beta, scale=None, initial_state=None, cu_se
         scale = K ** -0.5
     NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
     HV, V = v.shape[2], v.shape[3]
+    made = []  # tensors allocated here, on the current stream's pool
     if out is None:
         out = torch.empty_like(v)
+        made.append(out)
     if final_state is None and output_final_state:
         final_state = torch.empty((NS, HV, K, V), dtype=torch.float32, device=q.device)
+        made.append(final_state)
     if workspace is None:
         workspace = torch.empty(kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device=q.device)
+        made.append(workspace)
+    current = torch.cuda.current_stream(q.device).cuda_stream
     if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
+        stream = current
     code = getattr(lib, entry)(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
         _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), ctypes.c_void_p(stream))
     _check(code)
+    if made and stream != current:
+        # the work runs on another stream: the caching allocator must not hand these blocks
+        # (the temporary workspace above all) to the current stream before that work is done
+        other = torch.cuda.ExternalStream(stream, device=q.device)
+        for t in made:
+            t.record_stream(other)
     return out, final_state
 
 

@@ -218,3 +218,22 @@ def test_bad_cu_seqlens_reports_device_status(entry):
     ENTRIES[entry](d.q, d.k, d.v, d.g, d.beta, d.scale, initial_state=d.initial_state,
                    cu_seqlens=d.cu_seqlens, workspace=ws)
     assert kda.kda_read_device_status(ws) == 0
+
+
+@pytest.mark.gpu
+def test_call_on_another_stream_keeps_its_temporaries():
+    """A call on a stream other than the current one, with the workspace left to the
+    binding, gives the same result as a call on the current stream, even when the
+    current stream allocates and overwrites memory right after the call returns."""
+    x = W.make_inputs(1, 1024, 4, 8, 128, 128, "bf16", seed=77, init_state=True)
+    d = x.to("cuda")
+    ref_o, ref_s = kda.kda_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.scale, initial_state=d.initial_state)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    o, s = kda.kda_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.scale, initial_state=d.initial_state,
+                             stream=side.cuda_stream)
+    junk = [torch.full((1 << 22,), 7, dtype=torch.int32, device="cuda") for _ in range(16)]
+    torch.cuda.synchronize()
+    del junk
+    assert torch.equal(o, ref_o) and torch.equal(s, ref_s)
