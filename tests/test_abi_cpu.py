@@ -105,3 +105,14 @@ def test_host_validation_rejects(lib, entry):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         _lib.load_library(str(tmp_path / "nope.so"))
+
+
+def test_binding_refuses_host_tensors(lib):
+    """The binding has no CPU path: host tensors are refused before any call."""
+    import torch
+    from kimi_delta_attention_gb300 import workloads as W
+    x = W.make_inputs(1, 64, 1, 1, 128, 128, "bf16", seed=1)
+    for fn in (kda.kda_chunk_fwd, kda.kda_recurrent_fwd):
+        with pytest.raises(_lib.KdaError):
+            fn(x.q, x.k, x.v, x.g, x.beta, x.scale)
+    assert not x.q.is_cuda and isinstance(x.q, torch.Tensor)
