@@ -16,7 +16,9 @@
  *    16-byte aligned (beta and cu_seqlens: 4-byte aligned).  The caller allocates and owns every buffer; the library
  *    never allocates or frees device memory and never synchronises the device.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
- *    and runs asynchronously.
+ *    and runs asynchronously.  The device that is current at the call must be
+ *    the one that holds the tensors and owns `stream`: launches, tensor maps and
+ *    per-device set-up follow the current device.
  *  - Arguments are validated on the host before anything is enqueued; on any
  *    error nothing is launched and nothing is written.
  *  - cu_seqlens is not read on the host (that would need a device sync); each
@@ -53,7 +55,8 @@ typedef enum {
   KDA_ERR_DEVICE_TIMEOUT = 5,  /* device status: a bounded on-chip wait gave up */
   KDA_ERR_WORKSPACE = 6,       /* workspace missing or smaller than required */
   KDA_ERR_DEVICE_BOUNDS = 7,   /* device status: cu_seqlens out of order or out of range */
-  KDA_ERR_STATIC_SCRATCH = 8   /* problem larger than kda_chunk_fwd_static_scratch can hold */
+  KDA_ERR_STATIC_SCRATCH = 8,  /* problem larger than kda_chunk_fwd_static_scratch can hold */
+  KDA_ERR_DECAY_RANGE = 9      /* device status: g decays faster than the chunk kernels support */
 } kda_status;
 
 typedef struct {
@@ -75,7 +78,15 @@ typedef struct {
  *
  *   q, k          [B, T, H, K]   io_dtype
  *   v             [B, T, HV, V]  io_dtype
- *   g             [B, T, HV, K]  fp32, log-space decay
+ *   g             [B, T, HV, K]  fp32, log-space decay (natural log, <= 0).  The
+ *                 tensor-core kernels form every decay factor relative to a point
+ *                 inside the 16-token block it spans, so they are exact for any
+ *                 decay whose sum over each 16-token block of a sequence (tokens
+ *                 16 j .. 16 j + 15 from the sequence start), per key dimension, is
+ *                 >= -83; the bounded gate g >= -5 per token satisfies this.  A
+ *                 block outside that range sets KDA_ERR_DECAY_RANGE in the device
+ *                 status (its outputs are then not meaningful); the
+ *                 token-recurrent kernel has no such limit.
  *   beta          [B, T, HV]     fp32
  *   scale         > 0 and finite (the listing's default is K^-0.5; pass it)
  *   initial_state [NS, HV, K, V] fp32 or NULL (zeros); NS = B, or num_seqs
@@ -128,8 +139,9 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape* shape);
 /*
  * Read the device status word a previous call left in `workspace`: enqueues a
  * 4-byte device-to-host copy on `stream` and waits for that stream.  Returns
- * KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_BOUNDS (diagnostics only;
- * not for the hot loop).
+ * KDA_OK, KDA_ERR_DEVICE_TIMEOUT, KDA_ERR_DEVICE_BOUNDS or KDA_ERR_DECAY_RANGE (diagnostics only;
+ * not for the hot loop).  With several bits set the first of timeout, bounds,
+ * decay range is reported.
  */
 KDA_API kda_status kda_read_device_status(const void* workspace, void* stream);
 

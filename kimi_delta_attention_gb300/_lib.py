@@ -24,7 +24,7 @@ KDA_BF16 = 1
 STATUS_NAMES = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIGNMENT",
     4: "KDA_ERR_CUDA", 5: "KDA_ERR_DEVICE_TIMEOUT", 6: "KDA_ERR_WORKSPACE", 7: "KDA_ERR_DEVICE_BOUNDS",
-    8: "KDA_ERR_STATIC_SCRATCH",
+    8: "KDA_ERR_STATIC_SCRATCH", 9: "KDA_ERR_DECAY_RANGE",
 }
 STATIC_SCRATCH_MAX_UNITS = 32
 
@@ -120,12 +120,29 @@ def kda_chunk_fwd_kernel_name(shape: KdaShape) -> str:
     return load_library().kda_chunk_fwd_kernel_name(ctypes.byref(shape)).decode()
 
 
-def _forward(entry: str, q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
-             out=None, final_state=None, output_final_state=True, workspace=None, stream=None):
-    lib = load_library()
+def _check_tensors(q, k, v, g, beta, others):
+    """Inputs must be contiguous CUDA tensors; every tensor handed to the library must
+    live on q's device (the call runs with that device current)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         if not t.is_cuda or not t.is_contiguous():
             raise KdaError(1, f"{name} must be a contiguous CUDA tensor")
+    for name, t in (("k", k), ("v", v), ("g", g), ("beta", beta)) + tuple(others):
+        if t is not None and t.device != q.device:
+            raise KdaError(1, f"{name} is on {t.device}, q on {q.device}")
+
+
+def _forward(entry: str, q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+             out=None, final_state=None, output_final_state=True, workspace=None, stream=None):
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, (("initial_state", initial_state), ("cu_seqlens", cu_seqlens),
+                                      ("out", out), ("final_state", final_state), ("workspace", workspace)))
+    with torch.cuda.device(q.device):
+        return _forward_on_device(lib, entry, q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
+                                  final_state, output_final_state, workspace, stream)
+
+
+def _forward_on_device(lib, entry, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                       output_final_state, workspace, stream):
     shape = make_shape(q, v, cu_seqlens)
     K = q.shape[3]
     if scale is None:
@@ -176,9 +193,10 @@ def kda_recurrent_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqle
 
 
 def kda_read_device_status(workspace, stream=None) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream(workspace.device).cuda_stream
-    return int(load_library().kda_read_device_status(_ptr(workspace), ctypes.c_void_p(stream)))
+    with torch.cuda.device(workspace.device):
+        if stream is None:
+            stream = torch.cuda.current_stream(workspace.device).cuda_stream
+        return int(load_library().kda_read_device_status(_ptr(workspace), ctypes.c_void_p(stream)))
 
 
 def kda_chunk_fwd_static_scratch(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
@@ -187,25 +205,25 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, scale=None, initial_state=Non
     fixed array holds it (at most 32 (sequence, value head) pairs per call; calls
     that overlap on the GPU race).  Returns (o, final_state, status_word_address)."""
     lib = load_library()
-    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise KdaError(1, f"{name} must be a contiguous CUDA tensor")
-    shape = make_shape(q, v, cu_seqlens)
-    K = q.shape[3]
-    if scale is None:
-        scale = K ** -0.5
-    NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
-    HV, V = v.shape[2], v.shape[3]
-    if out is None:
-        out = torch.empty_like(v)
-    if final_state is None and output_final_state:
-        final_state = torch.empty((NS, HV, K, V), dtype=torch.float32, device=q.device)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    status = ctypes.c_void_p()
-    code = lib.kda_chunk_fwd_static_scratch(
-        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
-        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.c_void_p(stream),
-        ctypes.byref(status))
-    _check(code)
+    _check_tensors(q, k, v, g, beta, (("initial_state", initial_state), ("cu_seqlens", cu_seqlens),
+                                      ("out", out), ("final_state", final_state)))
+    with torch.cuda.device(q.device):
+        shape = make_shape(q, v, cu_seqlens)
+        K = q.shape[3]
+        if scale is None:
+            scale = K ** -0.5
+        NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
+        HV, V = v.shape[2], v.shape[3]
+        if out is None:
+            out = torch.empty_like(v)
+        if final_state is None and output_final_state:
+            final_state = torch.empty((NS, HV, K, V), dtype=torch.float32, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device).cuda_stream
+        status = ctypes.c_void_p()
+        code = lib.kda_chunk_fwd_static_scratch(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+            _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.c_void_p(stream),
+            ctypes.byref(status))
+        _check(code)
     return out, final_state, status.value

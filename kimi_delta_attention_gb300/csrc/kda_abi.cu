@@ -2,6 +2,7 @@
 // workspace sizing, status reporting and dispatch to the forward kernels.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -35,6 +36,18 @@ size_t workspace_needed(const kda_shape* s, bool use_tc) {
   const int ns = s->num_seqs > 0 ? s->num_seqs : s->B;
   if (ns <= 0) return kda::kWorkspaceBytes;
   return kda::kRingOffset + kda::chunk_tc_ring_bytes(ns, s->HV);
+}
+
+// Limit of the kernels' bounded waits for work: 2 s, or KDA_WAIT_LIMIT_NS (a positive
+// integer, read at each call) for tests that make those waits run out.
+unsigned long long wait_limit_ns() {
+  const char* e = std::getenv("KDA_WAIT_LIMIT_NS");
+  if (e) {
+    char* end = nullptr;
+    const unsigned long long v = std::strtoull(e, &end, 10);
+    if (end != e && v > 0) return v;
+  }
+  return 2000000000ull;
 }
 
 struct Checked {
@@ -88,6 +101,7 @@ kda_status validate(bool use_tc, const kda_shape* s, const void* q, const void* 
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = s0; p.cu = cu;
   p.out = out; p.sfin = sfin; p.status = static_cast<uint32_t*>(ws);
   p.ring = ws_bytes > kda::kRingOffset ? static_cast<uint8_t*>(ws) + kda::kRingOffset : nullptr;
+  p.wait_ns = wait_limit_ns();
   p.scale = scale; p.T = s->T; p.H = s->H; p.HV = s->HV; p.K = s->K; p.V = s->V;
   p.num_seqs = static_cast<int>(ns);
   c.bf16 = s->io_dtype == KDA_BF16;
@@ -169,6 +183,7 @@ kda_status kda_read_device_status(const void* workspace, void* stream) {
   if (cudaStreamSynchronize(cs) != cudaSuccess) return KDA_ERR_CUDA;
   if (word & kda::kStatusTimeout) return KDA_ERR_DEVICE_TIMEOUT;
   if (word & kda::kStatusBounds) return KDA_ERR_DEVICE_BOUNDS;
+  if (word & kda::kStatusRange) return KDA_ERR_DECAY_RANGE;
   return KDA_OK;
 }
 
@@ -183,6 +198,7 @@ const char* kda_status_string(kda_status status) {
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_DEVICE_BOUNDS: return "device: cu_seqlens out of order or out of range";
     case KDA_ERR_STATIC_SCRATCH: return "more (sequence, value head) pairs than the static scratch holds";
+    case KDA_ERR_DECAY_RANGE: return "device: g decays faster than the chunk kernels support (16-token sum < -83)";
   }
   return "unknown status";
 }

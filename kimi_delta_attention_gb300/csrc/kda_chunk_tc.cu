@@ -78,21 +78,16 @@ constexpr uint32_t SSLOT = 62464;     // shared slot stride (1024-multiple)
 constexpr uint32_t REC_TX = R_TILES + 4096 + 512;
 
 // ---- shared memory map (offsets from a 1024-aligned base) ----
-constexpr uint32_t OFF_SLOT = 0;                          // 2 record slots
-constexpr uint32_t OFF_PQD = 2 * SSLOT;                   // 124928 producer q -> qd [64 x 128] SW128
-constexpr uint32_t OFF_PKD = OFF_PQD + 16384;             // 141312 kd [64 x 128] SW128
-constexpr uint32_t OFF_PV = OFF_PKD + 16384;              // 157696 raw v [64 x 128] as 2 SW128 boxes
-constexpr uint32_t OFF_PB = OFF_PV + 16384;               // 174080 ki (raw k) | later M fp32 + A bf16
-constexpr uint32_t OFF_MB = OFF_PB;                       //        [64 x 68] fp32
-constexpr uint32_t OFF_AMAT = OFF_PB + 17408;             // 191488 [64 x 64] bf16 SW128; before it is
-constexpr uint32_t OFF_STG = OFF_AMAT + 8192;             // 199680 16 KB staging: kr^T, inverse scratch, U slices
-constexpr uint32_t OFF_ST = OFF_STG + 16384;              // 216064 S  [128 x 32] bf16 MN-major SW64
-constexpr uint32_t OFF_BETA = OFF_ST + 8192;              // 224256 [64] fp32
-constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 228608 [4][128] fp32 quarter-chunk sums of g
-constexpr uint32_t OFF_BAR = OFF_GSUM + 2048;             // 230656 mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 230912 tmem base
+constexpr uint32_t OFF_SLOT = 0;                          // 2 record slots (chain)
+constexpr uint32_t OFF_PREP = 2 * SSLOT;                  // 124928 producer tiles (prep:: layout)
+constexpr uint32_t OFF_ST = OFF_PREP + 90112;             // 215040 S  [128 x 32] bf16 MN-major SW64 (chain)
+constexpr uint32_t OFF_BETA = OFF_ST + 8192;              // 223232 [64] fp32
+constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 223488 [4][128] fp32 quarter-chunk sums of g
+constexpr uint32_t OFF_BAR = OFF_GSUM + 2048;             // 225536 mbarriers
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 225792 tmem base
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;        // + alignment slack
+static_assert(OFF_PREP % 1024 == 0 && SMEM_ALLOC <= 232448, "cluster kernel shared memory");
 
 // barrier slots
 constexpr int B_FULL = 0;    // [2] record landed in shared slot s (tx)
@@ -103,6 +98,7 @@ constexpr int B_PMMA = 13;   // producer MMA commits
 constexpr int B_A = 14;      // chain X/O MMA commit
 constexpr int B_B = 15;      // chain P MMA commit
 constexpr int B_C = 16;      // chain O += Aqk v_new commit
+constexpr int B_RAWV = 17;   // producer raw v (tx)
 
 // TMEM columns
 // chain: D_A[m & 1] holds X = W S in lanes 0-63 and o (qd S + Aqk v_new) in lanes
@@ -111,13 +107,18 @@ constexpr uint32_t TM_L = 0, TM_AQ = 64, TM_W = 0, TM_U = 128, TM_A0 = 256, TM_P
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t RAW_TX_BYTES = 3 * 16384;        // q, k, v tiles
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s
+// Bounded waits.  A wait for work (a record, a flag, a product or tile this role has not
+// seen complete yet) gives up after p.wait_ns (2 s unless the caller's environment
+// sets KDA_WAIT_LIMIT_NS); a drain wait (for copies and products already issued, before
+// the block reuses or releases the memory they touch) always allows DRAIN_LIMIT_NS.
+constexpr uint64_t DRAIN_LIMIT_NS = 2000000000ull;   // 2 s
 
 constexpr uint32_t NB_PREP = 1, NB_CHAIN = 2;
 
 struct Maps {
-  CUtensorMap q, k, v;
-  CUtensorMap o;  // output tiles (split kernel)
+  CUtensorMap q32, k32;  // q, k with 32-token boxes (the stacked producer tile)
+  CUtensorMap v;         // v with 64-token boxes
+  CUtensorMap o;         // output tiles (split kernel)
 };
 
 // Optional instrumentation (build with -DKDA_PROFILE), stored as uint64 words after
@@ -269,6 +270,321 @@ __device__ __forceinline__ void inverse_block_columns(float* mb, const float* be
   else if (w == 2) inverse_block_column<2>(mb, beta_s, amat, lane);
 }
 
+// ======================================================================
+// Chunk preparation shared by both kernels' producers: the decayed operands, the
+// products L = kd ki^T and Aqk = qd ki^T, and their readout.
+//
+// Range.  A factorisation e^{gc_i - gc_j} = e^{gc_i - r} e^{r - gc_j} is exact only
+// while both factors are representable.  With one reference r per chunk (the chunk
+// start) e^{-gc_j} overflows once a chunk's cumulative decay passes about -88, which
+// the bounded gate of the method (g >= -5 per token, i.e. -320 over 64 tokens) reaches
+// easily.  So the lower triangles of L and Aqk are formed as three blocks, each with a
+// reference between its rows and its columns:
+//   * the two 32 x 32 diagonal halves, referenced at the half's middle row (the end of
+//     its first 16-row quarter): every factor is bounded by the decay over 16 tokens;
+//   * the 32 x 32 block below them (rows 32-63, columns 0-31), referenced at row 32:
+//     both factors are <= 1, and one that underflows pairs with a product that is
+//     negligible anyway.
+// The factors are built from the within-quarter cumsum x (0 >= x >= s_q, the quarter's
+// decay in log2 units) and per-quarter constants, so no intermediate leaves the range
+// either.  The supported range is therefore: the decay of every 16-token quarter of a
+// chunk (per key dimension) is >= kMinQuarterLog2 (about -83 in natural-log units);
+// the producers report a quarter outside it with kStatusRange.  The
+// chunk-start-referenced factors kd, qd and kr are all <= 1 (their underflow is
+// harmless) and stay as they were.
+//
+// Tile layout of a producer (offsets from its 1024-aligned base; bf16 K-major tiles in
+// the 128-byte swizzle layout, two 64-column K-blocks each):
+//   QK    stacked [k rows 0-31 | q rows 0-31 | k rows 32-63 | q rows 32-63], the raw tiles
+//         as TMA lands them (32-row boxes), rewritten in place as kA / qA (half-middle
+//         reference): the 128-row A operand of the diagonal product
+//   CA    cA = k e^{mid - gc} (64 rows): B operand of the diagonal product
+//   KD    kd = k e^{gc} (64 rows): MN-major B operand of W = A kd
+//   KBQB  [kB rows 32-63 | qB rows 32-63] (row-32 reference): A operand of the
+//         off-diagonal product
+//   CB    cB = k e^{gc_31 - gc} for rows 0-31: its B operand
+// and, once the products have read them,
+//   MB / AMAT  M (fp32) and A = T Diag(beta) (bf16) over QK;  AQK_STG (bf16 Aqk) over CA;
+//   VRAW  the raw v tiles (loaded after the L/Aqk products) over KBQB, then the U staging.
+// qd and kr^T are written by the elementwise pass straight into the record (global).
+// ======================================================================
+namespace prep {
+constexpr uint32_t QK = 0;
+constexpr uint32_t QK_KB = 16384;  // one K-block of the stacked 128-row tile
+constexpr uint32_t CA = 32768;
+constexpr uint32_t KDT = 49152;
+constexpr uint32_t KBQB = 65536;
+constexpr uint32_t CB = 81920;
+constexpr uint32_t BYTES = 90112;
+constexpr uint32_t MB = QK;
+constexpr uint32_t AMAT = QK + 17408;  // after M (64 x MB_LD fp32)
+constexpr uint32_t AQK_STG = CA;
+constexpr uint32_t VRAW = KBQB;
+constexpr uint32_t USTG = KBQB;
+static_assert(AMAT + 8192 <= CA && MB_LD * 64 * 4 <= 17408, "M and A fit the stacked tile");
+constexpr uint32_t QK_TX = 32768, V_TX = 16384;
+// TMEM columns of the two products (relative to the producer's TMEM base)
+constexpr uint32_t TM_DIAG = 0;    // M = 128, N = 64: lane r = stacked row r
+constexpr uint32_t TM_OFF = 64;    // M = 64, N = 32: row r at lane 32 (r / 16) + r % 16
+constexpr float kMinQuarterLog2 = -120.f;
+
+// q and k tiles of chunk rows [row0, row0 + 64) into the stacked tile (32-row boxes).
+__device__ __forceinline__ void issue_qk(uint8_t* base, const CUtensorMap* q32, const CUtensorMap* k32,
+                                         uint64_t* bar, int hk, int row0) {
+  mbar_arrive_expect_tx(bar, QK_TX);
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    uint8_t* t = base + QK + kb * QK_KB;
+    tma_load_3d(t, k32, bar, 64 * kb, hk, row0);
+    tma_load_3d(t + 4096, q32, bar, 64 * kb, hk, row0);
+    tma_load_3d(t + 8192, k32, bar, 64 * kb, hk, row0 + 32);
+    tma_load_3d(t + 12288, q32, bar, 64 * kb, hk, row0 + 32);
+  }
+}
+__device__ __forceinline__ void issue_v(uint8_t* base, const CUtensorMap* v, uint64_t* bar, int hv, int row0) {
+  mbar_arrive_expect_tx(bar, V_TX);
+  tma_load_3d(base + VRAW, v, bar, 0, hv, row0);
+  tma_load_3d(base + VRAW + 8192, v, bar, 64, hv, row0);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Elementwise pass of thread (dp, hq): key dims 2 dp, 2 dp + 1 of chunk rows
+// [16 hq, 16 hq + 16) (quarter hq).  gsum holds the four quarter sums of g (natural
+// log) per key dim; g holds this thread's 16 rows.  Writes kA/qA (in place), cA, kd
+// and kB/qB (hq >= 2) or cB (hq < 2) to the tiles, and qd, kr^T and (hq = 0)
+// e^{g_last} into the record: qd_rec + kb * qd_kb_stride + (SW128 row offset),
+// krt_rec + (SW128 offset in the [128 x 64] kr^T tile), gam_rec.  Sets range_bad when
+// this quarter decays faster than the factors can represent.
+//
+// With x the within-quarter cumsum (log2 units; 0 >= x >= sh, sh the quarter's sum),
+// pre the decay before the quarter and all the chunk's:
+//   kd, qd = (k, scale q) 2^pre 2^x            kr = k 2^{all - pre - sh} (2^sh 2^-x)
+//   kA, qA = (k, scale q) 2^x (2^-sh if hq even: the half's middle is the quarter's end)
+//   cA     = k 2^-x (2^sh if hq even)
+//   kB, qB = (k, scale q) 2^x (2^{s_2} if hq = 3)      [reference: row 32]
+//   cB     = k (2^sh 2^-x) (2^{s_1} if hq = 0)
+// where 2^sh 2^-x lies in [2^sh, 1] and every other product of two factors is <= 1.
+//
+// Addressing: every tile base is 1024-aligned and a row is 128 bytes, so the 128-byte
+// swizzle (16-byte chunk index XOR row % 8) is an XOR on address bits 4-6 that commutes
+// with adding the row and the tile offsets; one 32-bit shared address per row serves
+// all tiles.
+__device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, const float2 (&g)[16], int dp, int hq,
+                                            int rows, float scale, uint8_t* qd_rec, uint32_t qd_kb_stride,
+                                            uint8_t* krt_rec, float* gam_rec, bool& range_bad) {
+  float c_d[2], c_r[2], es[2], fa[2], fb[2];
+  const bool even = (hq & 1) == 0;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float s[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) s[qq] = gsum[qq * tc::KD + 2 * dp + e] * kLog2e;
+    const float all = (s[0] + s[1]) + (s[2] + s[3]);
+    const float pre = hq == 0 ? 0.f : hq == 1 ? s[0] : hq == 2 ? s[0] + s[1] : (s[0] + s[1]) + s[2];
+    const float sh = hq == 0 ? s[0] : hq == 1 ? s[1] : hq == 2 ? s[2] : s[3];
+    if (!(sh >= kMinQuarterLog2)) range_bad = true;
+    c_d[e] = ex2_approx(pre);
+    c_r[e] = ex2_approx(all - pre - sh);
+    es[e] = ex2_approx(sh);
+    fa[e] = even ? ex2_approx(-sh) : 1.f;                               // kA, qA
+    fb[e] = hq == 3 ? ex2_approx(s[2]) : hq == 0 ? ex2_approx(s[1]) : 1.f;  // kB, qB / cB
+    if (hq == 0) gam_rec[2 * dp + e] = ex2_approx(all);
+  }
+  const uint32_t kb = static_cast<uint32_t>(dp) >> 5;
+  const uint32_t r0 = 16u * static_cast<uint32_t>(hq);
+  const uint32_t lo = ((2u * dp) & 7u) * 2u;
+  const uint32_t c4 = (((2u * dp) & 63u) >> 3) << 4;  // unswizzled 16-byte chunk offset
+  // row r0 of each tile, before the swizzle XOR (tile offsets and rows keep bits 4-6 clear)
+  const uint32_t X = smem_u32(base) + r0 * 128u + lo + c4;
+  const uint32_t a_k = QK + kb * QK_KB + (hq >= 2 ? 32u : 0u) * 128u;  // stacked row of k row r0
+  const uint32_t a_64 = kb * 8192u;                                    // + CA / KDT
+  const uint32_t a_b = hq >= 2 ? KBQB + kb * 8192u - 32u * 128u : CB + kb * 4096u;
+  uint8_t* qdr = qd_rec + kb * qd_kb_stride + r0 * 128u + lo;
+  uint32_t kr[2][4];
+  float kre[2] = {0.f, 0.f};
+  float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t swz = (static_cast<uint32_t>(i) & 7u) << 4;
+    const uint32_t Y = (X ^ swz) + static_cast<uint32_t>(i) * 128u;  // row r0 + i, any tile
+    const uint32_t kraw = lds32(Y + a_k), qraw = lds32(Y + a_k + 4096u);
+    x0 = fmaf(g[i].x, kLog2e, x0);
+    x1 = fmaf(g[i].y, kLog2e, x1);
+    const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+    const float ie0 = ex2_approx(-x0), ie1 = ex2_approx(-x1);
+    const bool valid = static_cast<int>(r0) + i < rows;
+    const float k0 = valid ? __uint_as_float(kraw << 16) : 0.f;
+    const float k1 = valid ? __uint_as_float(kraw & 0xFFFF0000u) : 0.f;
+    const float q0 = valid ? __uint_as_float(qraw << 16) * scale : 0.f;
+    const float q1 = valid ? __uint_as_float(qraw & 0xFFFF0000u) * scale : 0.f;
+    const float p0 = ie0 * es[0], p1 = ie1 * es[1];  // 2^{sh - x}
+    {
+      const float a0 = e0 * fa[0], a1 = e1 * fa[1];
+      sts32(Y + a_k, pack2(k0 * a0, k1 * a1));
+      sts32(Y + a_k + 4096u, pack2(q0 * a0, q1 * a1));
+      const float cc0 = even ? p0 : ie0, cc1 = even ? p1 : ie1;
+      sts32(Y + a_64 + CA, pack2(k0 * cc0, k1 * cc1));
+    }
+    {
+      const float d0 = e0 * c_d[0], d1 = e1 * c_d[1];
+      sts32(Y + a_64 + KDT, pack2(k0 * d0, k1 * d1));
+      __stcg(reinterpret_cast<uint32_t*>(qdr + ((c4 ^ swz) + static_cast<uint32_t>(i) * 128u)), pack2(q0 * d0, q1 * d1));
+    }
+    if (hq >= 2) {
+      const float b0 = e0 * fb[0], b1 = e1 * fb[1];
+      sts32(Y + a_b, pack2(k0 * b0, k1 * b1));
+      sts32(Y + a_b + 4096u, pack2(q0 * b0, q1 * b1));
+    } else {
+      const float b0 = p0 * fb[0], b1 = p1 * fb[1];
+      sts32(Y + a_b, pack2(k0 * b0, k1 * b1));
+    }
+    const float kr0 = k0 * (p0 * c_r[0]), kr1 = k1 * (p1 * c_r[1]);
+    if (i & 1) {
+      kr[0][(i >> 1) & 3] = pack2(kre[0], kr0);
+      kr[1][(i >> 1) & 3] = pack2(kre[1], kr1);
+    } else {
+      kre[0] = kr0;
+      kre[1] = kr1;
+    }
+    if ((i & 7) == 7)  // tokens r0 + i - 7 .. r0 + i of kr^T rows 2 dp, 2 dp + 1
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        __stcg(reinterpret_cast<uint4*>(krt_rec + sw128_offset(2 * dp + e, r0 + (i & 8), 128)),
+               make_uint4(kr[e][0], kr[e][1], kr[e][2], kr[e][3]));
+  }
+}
+
+// The two products (issued by one converged warp): the diagonal halves of L and Aqk
+// (M = 128 over the stacked rows, N = 64) and the block below them (M = 64, N = 32).
+__device__ __forceinline__ void issue_lqk(uint32_t tmem, uint64_t d_sw128) {
+  auto d = [&](uint32_t off) { return d_sw128 + (off >> 4); };
+  constexpr uint32_t idesc_d = idesc_f16kind(128, 64), idesc_o = idesc_f16kind(64, 32);
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint32_t acc = (kb | ks) != 0;
+      umma_f16_warp(tmem + TM_DIAG, d(QK + kb * QK_KB + ks * 32), d(CA + kb * 8192 + ks * 32), idesc_d, acc);
+      umma_f16_warp(tmem + TM_OFF, d(KBQB + kb * 8192 + ks * 32), d(CB + kb * 4096 + ks * 32), idesc_o, acc);
+    }
+}
+
+// Readout by the 8 warps of a producer (quad = TMEM lane quadrant, cpart = which 16
+// columns): M = strict_tril(Diag(beta) L) as fp32 into MB (the upper-right 32 x 32 block
+// is not written: the inverse never reads it as M) and Aqk = tril(qd ki^T) as the bf16
+// SW128 tile AQK_STG (every element written).
+__device__ __forceinline__ void readout_lqk(uint8_t* base, uint32_t tmem, const float* beta_s, int quad, int cpart,
+                                            int lane) {
+  float* mb = reinterpret_cast<float*>(base + MB);
+  uint8_t* aq = base + AQK_STG;
+  const int half = quad >> 1;
+  const int c0 = 32 * half + 16 * cpart;  // diagonal-half columns of this warp
+  float dv[16], ov[16];
+  tmem_ld16(tmem_addr(tmem, 32 * quad, TM_DIAG + c0), dv);
+  tmem_ld16(tmem_addr(tmem, 32 * quad, TM_OFF + 16 * cpart), ov);
+  tmem_ld_wait();
+  const int i = 32 * half + lane;  // row of the diagonal half
+  if ((quad & 1) == 0) {           // L
+    const float bi = beta_s[i];
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      float4 v4;
+      const int c = c0 + 4 * j4;
+      v4.x = (c + 0 < i) ? bi * dv[4 * j4 + 0] : 0.f;
+      v4.y = (c + 1 < i) ? bi * dv[4 * j4 + 1] : 0.f;
+      v4.z = (c + 2 < i) ? bi * dv[4 * j4 + 2] : 0.f;
+      v4.w = (c + 3 < i) ? bi * dv[4 * j4 + 3] : 0.f;
+      *reinterpret_cast<float4*>(mb + i * MB_LD + c) = v4;
+    }
+  } else {  // Aqk (diagonal kept)
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int c = c0 + 8 * h8 + 2 * t;
+        w[t] = pack2((c <= i) ? dv[8 * h8 + 2 * t] : 0.f, (c + 1 <= i) ? dv[8 * h8 + 2 * t + 1] : 0.f);
+      }
+      st_v4(aq + sw128_offset(i, c0 + 8 * h8, 64), w[0], w[1], w[2], w[3]);
+    }
+    if (half == 0)  // Aqk rows 0-31, columns 32-63: zero
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8) st_v4(aq + sw128_offset(i, 32 + 16 * cpart + 8 * h8, 64), 0u, 0u, 0u, 0u);
+  }
+  if (lane < 16) {  // the block below the diagonal halves: rows 32-63, columns 0-31, no mask
+    const int io = 32 + 16 * (quad & 1) + lane;
+    const int cc = 16 * cpart;
+    if (half == 0) {  // L
+      const float bi = beta_s[io];
+#pragma unroll
+      for (int j4 = 0; j4 < 4; ++j4)
+        *reinterpret_cast<float4*>(mb + io * MB_LD + cc + 4 * j4) =
+            make_float4(bi * ov[4 * j4], bi * ov[4 * j4 + 1], bi * ov[4 * j4 + 2], bi * ov[4 * j4 + 3]);
+    } else {  // Aqk
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8)
+        st_v4(aq + sw128_offset(io, cc + 8 * h8, 64), pack2(ov[8 * h8], ov[8 * h8 + 1]),
+              pack2(ov[8 * h8 + 2], ov[8 * h8 + 3]), pack2(ov[8 * h8 + 4], ov[8 * h8 + 5]),
+              pack2(ov[8 * h8 + 6], ov[8 * h8 + 7]));
+    }
+  }
+}
+
+// Diagonal 16 x 16 blocks of T = (I + M)^{-1} by forward substitution (warps 0-3, one
+// column per lane of the first half-warp), written to MB and, scaled by beta of the
+// column, to AMAT; warps 4-7 zero the blocks of AMAT above the diagonal.
+__device__ __forceinline__ void inverse_diag_blocks(uint8_t* base, const float* beta_s, int pw, int pt, int lane) {
+  float* mb = reinterpret_cast<float*>(base + MB);
+  uint8_t* amat = base + AMAT;
+  if (pw < 4) {
+    if (lane < 16) {
+      const int b0 = 16 * pw, jc = lane;
+      // row by row: T[i][jc] = [i == jc] - sum_{mm < i} M[i][mm] T[mm][jc], with
+      // M's row read four at a time and two partial sums
+      float acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float* row = mb + (b0 + i) * MB_LD + b0;
+        float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < i; mm += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(row + mm);
+          s0 = fmaf(-m4.x, acc[mm], s0);
+          if (mm + 1 < i) s1 = fmaf(-m4.y, acc[mm + 1], s1);
+          if (mm + 2 < i) s0 = fmaf(-m4.z, acc[mm + 2], s0);
+          if (mm + 3 < i) s1 = fmaf(-m4.w, acc[mm + 3], s1);
+        }
+        acc[i] = s0 + s1;
+      }
+      __syncwarp(0x0000FFFFu);
+      const float bj = beta_s[b0 + jc];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
+        *reinterpret_cast<uint16_t*>(amat + sw128_offset(b0 + i, b0 + jc, 64)) = f2bf(acc[i] * bj);
+      }
+    }
+  } else {
+    // blocks (row block br, column block bc > br): 6 blocks of 16 x 16 bf16 zeros,
+    // 2 chunks of 8 columns per row -> 6 * 16 * 2 = 192 16-byte stores over 128 threads
+    for (int idx = pt - 128; idx < 192; idx += 128) {
+      const int blk = idx >> 5, rem = idx & 31, row = rem >> 1, hf = rem & 1;
+      const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      st_v4(amat + sw128_offset(16 * br + row, 16 * bc + 8 * hf, 64), 0u, 0u, 0u, 0u);
+    }
+  }
+}
+}  // namespace prep
+
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -276,7 +592,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   float* beta_s = reinterpret_cast<float*>(sm + OFF_BETA);
-  float* mb = reinterpret_cast<float*>(sm + OFF_MB);
   float* gsum = reinterpret_cast<float*>(sm + OFF_GSUM);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -302,13 +617,14 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     mbar_init(&bars[B_ACK], NSLICE);
     mbar_init(&bars[B_ACK + 1], NSLICE);
     mbar_init(&bars[B_RAW], 1);
+    mbar_init(&bars[B_RAWV], 1);
     mbar_init(&bars[B_PMMA], 1);
     mbar_init(&bars[B_A], 1);
     mbar_init(&bars[B_B], 1);
     mbar_init(&bars[B_C], 1);
     fence_mbar_init();
-    tma_prefetch_desc(&maps.q);
-    tma_prefetch_desc(&maps.k);
+    tma_prefetch_desc(&maps.q32);
+    tma_prefetch_desc(&maps.k32);
     tma_prefetch_desc(&maps.v);
   }
   if (warp == 0) {
@@ -330,42 +646,33 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   const uint64_t D_SW128 = sdesc_sw128(sbase);                        // K-major, 128-B swizzle
   const uint64_t D_ST = sdesc(sbase + OFF_ST, 8192, 512, 4);          // S, MN-major 64-B swizzle
   const uint64_t D_VNT = sdesc(sbase + OFF_SLOT + S_U, 4096, 512, 4);  // v_new of slot 0, MN-major 64-B swizzle
-  const uint64_t D_KD_MN = sdesc(sbase + OFF_PKD, 8192, 1024, 2);     // kd as MN-major B
-  const uint64_t D_V_MN = sdesc(sbase + OFF_PV, 8192, 1024, 2);       // v as MN-major B
   auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
   const size_t state_off = (static_cast<size_t>(seq) * HV + hv) * KD * VD;
 
   if (warp < NPROD / 32) {
     // ============================== producer ===============================
+    uint8_t* pb = sm + OFF_PREP;  // the prep:: tiles
     const int pt = tid;           // 0..255
     const int dp = pt & 63;       // key dims 2 dp, 2 dp + 1 owned in the elementwise pass
     const int hq = pt >> 6;       // ... for rows [16 hq, 16 hq + 16)
     const int quad = warp & 3;    // TMEM lane quadrant of this warp
     const int cpart = warp >> 2;  // which half of a readout this warp takes
     const float scale = p.scale;
+    const uint64_t D_PREP = sdesc_sw128(sbase + OFF_PREP);
+    const uint64_t D_KD_MN = sdesc(sbase + OFF_PREP + prep::KDT, 8192, 1024, 2);  // kd as MN-major B
+    const uint64_t D_V_MN = sdesc(sbase + OFF_PREP + prep::VRAW, 8192, 1024, 2);  // v as MN-major B
     uint32_t pmma_phase = 0, pmma_issued = 0;
-    bool raw_pending = false;
-    int raw_pending_j = 0;
-    bool failed = false;
+    bool raw_pending = false, v_pending = false;
+    int raw_pending_j = 0, v_pending_j = 0;
+    bool failed = false, range_bad = false;
     auto timeout = [&]() {
       failed = true;
       atomicOr(p.status, kStatusTimeout);
     };
     PROF_DECL
-#ifdef KDA_PROFILE
-    uint64_t ew_acc[2] = {0, 0};
-#endif
 
-
-    auto issue_raw = [&](int m, int j) {  // elected: TMA q, k, v tiles of chunk m (own chunk j)
-      const int row0 = static_cast<int>(tok0) + m * C;
-      mbar_arrive_expect_tx(&bars[B_RAW], RAW_TX_BYTES);
-      tma_load_3d(sm + OFF_PQD, &maps.q, &bars[B_RAW], 0, hk, row0);
-      tma_load_3d(sm + OFF_PQD + 8192, &maps.q, &bars[B_RAW], 64, hk, row0);
-      tma_load_3d(sm + OFF_PB, &maps.k, &bars[B_RAW], 0, hk, row0);
-      tma_load_3d(sm + OFF_PB + 8192, &maps.k, &bars[B_RAW], 64, hk, row0);
-      tma_load_3d(sm + OFF_PV, &maps.v, &bars[B_RAW], 0, hv, row0);
-      tma_load_3d(sm + OFF_PV + 8192, &maps.v, &bars[B_RAW], 64, hv, row0);
+    auto issue_raw = [&](int m, int j) {  // elected: TMA q, k tiles of chunk m (own chunk j)
+      prep::issue_qk(pb, &maps.q32, &maps.k32, &bars[B_RAW], hk, static_cast<int>(tok0) + m * C);
       raw_pending = true;
       raw_pending_j = j;
     };
@@ -395,7 +702,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       bool ok = true;
       if (lane == 0) {
         fence_proxy_async_global();
-        if (jp >= 2) ok = mbar_wait_cluster(&bars[B_ACK + (jp & 1)], ((jp - 2) >> 1) & 1, WAIT_LIMIT_NS);
+        if (jp >= 2) ok = mbar_wait_cluster(&bars[B_ACK + (jp & 1)], ((jp - 2) >> 1) & 1, p.wait_ns);
         if (!ok) timeout();
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -415,9 +722,9 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
       const int rows = min(C, len - m * C);
       const bool next = m + NSLICE < NT;
-      // ---- 1. raw q, k, v of chunk m ----
-      if (!mbar_wait(&bars[B_RAW], j & 1, WAIT_LIMIT_NS)) timeout();
-      if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
+      // ---- 1. raw q, k of chunk m ----
+      if (!mbar_wait(&bars[B_RAW], j & 1, p.wait_ns)) timeout();
+      if (pt == 0) bulk_wait_read();  // the previous record's Aqk, W and U stagings have been read
       if (pt < C) beta_s[pt] = bpre;
       {
         float2 qsum = make_float2(0.f, 0.f);
@@ -431,81 +738,20 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (role_any(NB_PREP, NPROD, failed)) break;
       if (pt == 0) raw_pending = false;
       PROF(0);
-#ifdef KDA_PROFILE
-      const uint64_t ew_t0 = clock64();
-#endif
 
-      // ---- 2. elementwise: cumsum, decayed operands; kr^T and e^{g_last} to the record.
-      //         Two adjacent key dims per thread (32-bit accesses of the SW128 tiles),
-      //         the cumulative sum kept in log2 units so each exponential is one ex2 ----
+      // ---- 2. elementwise: operand tiles; qd, kr^T and e^{g_last} straight into the
+      //         record (a slot is rewritten only after its previous record was loaded
+      //         everywhere: publish() of the record two before waited for that) ----
       {
-        float2 pre = make_float2(0.f, 0.f), all = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const float2 v = reinterpret_cast<const float2*>(gsum + qq * KD)[dp];
-          if (qq < hq) {
-            pre.x += v.x;
-            pre.y += v.y;
-          }
-          all.x += v.x;
-          all.y += v.y;
-        }
-        const float gam0 = ex2_approx(all.x * kLog2e), gam1 = ex2_approx(all.y * kLog2e);
-        if (hq == 0) __stcg(reinterpret_cast<float2*>(gs + G_GAM) + dp, make_float2(gam0, gam1));
-        float gl0 = pre.x * kLog2e, gl1 = pre.y * kLog2e;  // log2 of the decay up to the current row
-        uint8_t* qd_t = sm + OFF_PQD;
-        uint8_t* ki_t = sm + OFF_PB;
-        uint8_t* kd_t = sm + OFF_PKD;
-        const uint32_t kbase = static_cast<uint32_t>(dp >> 5) * 8192u + static_cast<uint32_t>(hq) * 16u * 128u +
-                               ((2u * dp) & 7u) * 2u;
-        const uint32_t chunk = ((2u * dp) & 63u) >> 3;
-        uint32_t kr0[8], kr1[8];  // kr of dims 2dp, 2dp+1 for the 16 rows, bf16 pairs along the rows
-        float kre0 = 0.f, kre1 = 0.f;  // kr of the previous (even) row
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t off = kbase + i * 128u + ((chunk ^ (i & 7)) << 4);  // row 16 hq + i (16 hq is 0 mod 8)
-          const uint32_t kraw = *reinterpret_cast<const uint32_t*>(ki_t + off);
-          const uint32_t qraw = *reinterpret_cast<const uint32_t*>(qd_t + off);
-          gl0 = fmaf(gpre[i].x, kLog2e, gl0);
-          gl1 = fmaf(gpre[i].y, kLog2e, gl1);
-          const float e0 = ex2_approx(gl0), e1 = ex2_approx(gl1);
-          const float ie0 = ex2_approx(-gl0), ie1 = ex2_approx(-gl1);
-          const bool valid = 16 * hq + i < rows;
-          const float k0 = valid ? __uint_as_float(kraw << 16) : 0.f;
-          const float k1 = valid ? __uint_as_float(kraw & 0xFFFF0000u) : 0.f;
-          const float q0 = valid ? __uint_as_float(qraw << 16) : 0.f;
-          const float q1 = valid ? __uint_as_float(qraw & 0xFFFF0000u) : 0.f;
-          const float ki0 = k0 * ie0, ki1 = k1 * ie1;
-          *reinterpret_cast<uint32_t*>(kd_t + off) = pack2(k0 * e0, k1 * e1);
-          *reinterpret_cast<uint32_t*>(ki_t + off) = pack2(ki0, ki1);
-          *reinterpret_cast<uint32_t*>(qd_t + off) = pack2(q0 * e0 * scale, q1 * e1 * scale);
-          if (i & 1) {
-            kr0[i >> 1] = pack2(kre0, ki0 * gam0);
-            kr1[i >> 1] = pack2(kre1, ki1 * gam1);
-          } else {
-            kre0 = ki0 * gam0;
-            kre1 = ki1 * gam1;
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          st_v4(sm + OFF_STG + sw128_offset(2 * dp, 16 * hq + 8 * h, 128), kr0[4 * h], kr0[4 * h + 1], kr0[4 * h + 2],
-                kr0[4 * h + 3]);
-          st_v4(sm + OFF_STG + sw128_offset(2 * dp + 1, 16 * hq + 8 * h, 128), kr1[4 * h], kr1[4 * h + 1],
-                kr1[4 * h + 2], kr1[4 * h + 3]);
-        }
+        prep::elementwise(pb, gsum, gpre, dp, hq, rows, scale, gs + R_WQ + R_QD_IN_KB, R_W_KB, gs + R_KRT,
+                          reinterpret_cast<float*>(gs + G_GAM), range_bad);
       }
-#ifdef KDA_PROFILE
-      if (prof_on && lane == 0) ew_acc[0] += clock64() - ew_t0;
-#endif
+      fence_proxy_async_global();  // the record's plain stores, read by the chains' bulk copies
       if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's W/U stores have landed
-#ifdef KDA_PROFILE
-      if (prof_on && lane == 0) ew_acc[1] += clock64() - ew_t0;
-#endif
       fence_proxy_async_smem();
       role_sync(NB_PREP, NPROD);
       PROF(1);
-      // The previous record goes out from warp 3 while thread 0 issues the MMAs below
+      // The previous record goes out from warp 3 while warp 0 issues the MMAs below
       // (the cluster-scope arrives cost the issuing warp about a thousand cycles, and
       // would also wait for its g loads, so it publishes before requesting them).
       // Thread 0's wait on the record's stores is ordered before this by the barrier.
@@ -514,127 +760,47 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         pub_pending = false;
       }
 
-      // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd and kr^T tiles to the record ----
-      if (pt == 0) {
+      // ---- 3. the diagonal halves and the block below them of L and Aqk ----
+      if (warp == 0) {
         tc_fence_after();
-        constexpr uint32_t idesc = idesc_f16kind(64, 64);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t koff = kb * 8192 + ks * 32;
-            const uint64_t bd = d128(OFF_PB + koff);
-            umma_f16(tmem + TM_L, d128(OFF_PKD + koff), bd, idesc, (kb | ks) != 0);
-            umma_f16(tmem + TM_AQ, d128(OFF_PQD + koff), bd, idesc, (kb | ks) != 0);
-          }
-        umma_commit(&bars[B_PMMA]);
+        prep::issue_lqk(tmem, D_PREP);
+        umma_commit_warp(&bars[B_PMMA]);
         ++pmma_issued;
-        bulk_store(gs + R_WQ + R_QD_IN_KB, sm + OFF_PQD, 8192);
-        bulk_store(gs + R_WQ + R_W_KB + R_QD_IN_KB, sm + OFF_PQD + 8192, 8192);
-        bulk_store(gs + R_KRT, sm + OFF_STG, 16384);
-        bulk_commit();
       }
       if (next) prefetch_gb(m + NSLICE, 0);
       __syncwarp();
-      if (!mbar_wait(&bars[B_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
-      ++pmma_phase;
+      if (mbar_wait(&bars[B_PMMA], pmma_phase & 1, p.wait_ns)) ++pmma_phase;  // else still in flight: drained below
+      else timeout();
       tc_fence_after();
-      if (pt == 0) bulk_wait_read();  // qd (about to hold the Aqk staging) and kr^T have been read
       PROF(2);
 
-      // ---- 4. TMEM -> M (fp32, rows scaled by beta, strictly lower), Aqk -> staging ----
-      role_sync(NB_PREP, NPROD);
-      {
-        const int i = 16 * quad + (lane & 15);
-        const int j0 = 32 * cpart;  // this warp's 32 columns
-        float rl[32], ra[32];
-        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_L + j0), rl);
-        tmem_ld32(tmem_addr(tmem, 32 * quad, TM_AQ + j0), ra);
-        tmem_ld_wait();
-        if (lane < 16) {
-          const float bi = beta_s[i];
-#pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            float4 v4;
-            const int jj = j0 + 4 * j4;
-            v4.x = (jj + 0 < i) ? bi * rl[4 * j4 + 0] : 0.f;
-            v4.y = (jj + 1 < i) ? bi * rl[4 * j4 + 1] : 0.f;
-            v4.z = (jj + 2 < i) ? bi * rl[4 * j4 + 2] : 0.f;
-            v4.w = (jj + 3 < i) ? bi * rl[4 * j4 + 3] : 0.f;
-            *reinterpret_cast<float4*>(mb + i * MB_LD + jj) = v4;
-          }
-#pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int jj = j0 + 8 * j8 + 2 * t;
-              w[t] = pack2((jj <= i) ? ra[8 * j8 + 2 * t] : 0.f, (jj + 1 <= i) ? ra[8 * j8 + 2 * t + 1] : 0.f);
-            }
-            st_v4(sm + OFF_PQD + sw128_offset(i, j0 + 8 * j8, 64), w[0], w[1], w[2], w[3]);
-          }
-        }
+      // ---- 4. raw v into the [kB; qB] tiles (read by now); TMEM -> M (fp32), Aqk ----
+      if (pt == 0 && !failed) {
+        prep::issue_v(pb, &maps.v, &bars[B_RAWV], hv, static_cast<int>(tok0) + m * C);
+        v_pending = true;
+        v_pending_j = j;
       }
+      prep::readout_lqk(pb, tmem, beta_s, quad, cpart, lane);
       tc_fence_before();
       fence_proxy_async_smem();
       if (role_any(NB_PREP, NPROD, failed)) break;
       if (pt == 0) {
-        bulk_store(gs + R_AQK, sm + OFF_PQD, 8192);
+        bulk_store(gs + R_AQK, pb + prep::AQK_STG, 8192);
         bulk_commit();
       }
       if (next) prefetch_gb(m + NSLICE, 1);
       PROF(3);
 
-      // ---- 5. T = (I + M)^{-1} and A = T Diag(beta): 16x16 diagonal blocks by forward
-      //         substitution (warps 0-3), zero blocks above the diagonal (warps 4-7),
-      //         then block rows ----
-      uint8_t* amat = sm + OFF_AMAT;
-      if (warp < 4) {
-        if (lane < 16) {
-          const int b0 = 16 * warp, jc = lane;
-          // row by row: T[i][jc] = [i == jc] - sum_{mm < i} M[i][mm] T[mm][jc], with
-          // M's row read four at a time and two partial sums
-          float acc[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float* row = mb + (b0 + i) * MB_LD + b0;
-            float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
-#pragma unroll
-            for (int mm = 0; mm < i; mm += 4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(row + mm);
-              s0 = fmaf(-m4.x, acc[mm], s0);
-              if (mm + 1 < i) s1 = fmaf(-m4.y, acc[mm + 1], s1);
-              if (mm + 2 < i) s0 = fmaf(-m4.z, acc[mm + 2], s0);
-              if (mm + 3 < i) s1 = fmaf(-m4.w, acc[mm + 3], s1);
-            }
-            acc[i] = s0 + s1;
-          }
-          __syncwarp(0x0000FFFFu);
-          const float bj = beta_s[b0 + jc];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
-            *reinterpret_cast<uint16_t*>(amat + sw128_offset(b0 + i, b0 + jc, 64)) = f2bf(acc[i] * bj);
-          }
-        }
-      } else {
-        // blocks (row block br, column block bc > br): 6 blocks of 16 x 16 bf16 zeros,
-        // 2 chunks of 8 columns per row -> 6 * 16 * 2 = 192 16-byte stores over 128 threads
-        const int q = pt - 128;
-        for (int idx = q; idx < 192; idx += 128) {
-          const int blk = idx >> 5, rem = idx & 31, row = rem >> 1, half = rem & 1;
-          const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-          const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-          st_v4(amat + sw128_offset(16 * br + row, 16 * bc + 8 * half, 64), 0u, 0u, 0u, 0u);
-        }
-      }
+      // ---- 5. T = (I + M)^{-1} and A = T Diag(beta): diagonal blocks, then the block columns ----
+      prep::inverse_diag_blocks(pb, beta_s, warp, pt, lane);
       role_sync(NB_PREP, NPROD);
       PROF(4);
       // next chunk's g: requested here, so the loads are in flight during the
       // inverse rather than in front of the barrier below
       if (next) prefetch_gb(m + NSLICE, 2);
       PROF(10);
-      if (warp < 3) inverse_block_columns(mb, beta_s, amat, warp, lane);
+      if (warp < 3)
+        inverse_block_columns(reinterpret_cast<float*>(pb + prep::MB), beta_s, pb + prep::AMAT, warp, lane);
       PROF(5);
       fence_proxy_async_smem();
       role_sync(NB_PREP, NPROD);
@@ -642,30 +808,33 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
 
       // ---- 6. W = A kd, U = A v (kd and v as MN-major B operands) ----
       if (pt == 0) {
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = d128(OFF_AMAT + ks * 32);
-          umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc, ks != 0);
-          umma_f16(tmem + TM_U, ad, D_V_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+        if (v_pending) {
+          if (!mbar_wait(&bars[B_RAWV], j & 1, p.wait_ns)) timeout();
+          v_pending = false;
         }
-        umma_commit(&bars[B_PMMA]);
-        ++pmma_issued;
+        if (!failed) {
+          tc_fence_after();
+          constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = D_PREP + ((prep::AMAT + ks * 32) >> 4);
+            umma_f16(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+            umma_f16(tmem + TM_U, ad, D_V_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+          }
+          umma_commit(&bars[B_PMMA]);
+          ++pmma_issued;
+        }
       }
       if (next) prefetch_gb(m + NSLICE, 3);
       __syncwarp();
-      if (!mbar_wait(&bars[B_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
-      ++pmma_phase;
+      if (mbar_wait(&bars[B_PMMA], pmma_phase & 1, p.wait_ns)) ++pmma_phase;  // else still in flight: drained below
+      else timeout();
       tc_fence_after();
-      // raw buffers are free again: fetch the next own chunk
-      if (pt == 0 && next && !failed) {
-        bulk_wait_read();  // the Aqk staging (in the q buffer) has been read
-        issue_raw(m + NSLICE, j + 1);
-      }
+      // the stacked tile (M and A by now) is free again: fetch the next own chunk
+      if (pt == 0 && next && !failed) issue_raw(m + NSLICE, j + 1);
       PROF(7);
 
-      // ---- 7. W -> staging (bf16 SW128), U -> staging (4 slices of [64 x 32] bf16) ----
+      // ---- 7. W -> staging over kd (bf16 SW128), U -> staging over v (4 slices of [64 x 32] bf16) ----
       __syncwarp();
       {
         const int i = 16 * quad + (lane & 15);
@@ -683,8 +852,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
               const int q4 = q2 + h;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
-                uint8_t* d8 = cpart == 0 ? sm + OFF_PKD + sw128_offset(i, 32 * q4 + 8 * j8, 64)
-                                         : sm + OFF_STG + q4 * 4096 + i * (VS * 2) + 16 * j8;
+                uint8_t* d8 = cpart == 0 ? pb + prep::KDT + sw128_offset(i, 32 * q4 + 8 * j8, 64)
+                                         : pb + prep::USTG + q4 * 4096 + i * (VS * 2) + 16 * j8;
                 st_v4(d8, pack2(r[8 * j8], r[8 * j8 + 1]), pack2(r[8 * j8 + 2], r[8 * j8 + 3]),
                       pack2(r[8 * j8 + 4], r[8 * j8 + 5]), pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
               }
@@ -694,7 +863,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      fence_proxy_async_global();  // e^{g_last} went out with plain stores
       if (role_any(NB_PREP, NPROD, failed)) break;
       PROF(8);
 
@@ -702,9 +870,9 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       //         (or at the end), once these stores have landed.  The first record
       //         goes out at once: every chain of the cluster is waiting for it. ----
       if (pt == 0) {
-        bulk_store(gs + R_WQ, sm + OFF_PKD, 8192);
-        bulk_store(gs + R_WQ + R_W_KB, sm + OFF_PKD + 8192, 8192);
-        bulk_store(gs + G_U, sm + OFF_STG, 16384);
+        bulk_store(gs + R_WQ, pb + prep::KDT, 8192);
+        bulk_store(gs + R_WQ + R_W_KB, pb + prep::KDT + 8192, 8192);
+        bulk_store(gs + G_U, pb + prep::USTG, 16384);
         bulk_commit();
         if (j == 0) bulk_wait_group<0>();
       }
@@ -716,6 +884,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       PROF(9);
     }
+    if (range_bad) atomicOr(p.status, kStatusRange);
     if (warp == 0 && pub_pending) {  // the last record (warp-uniform decision)
       if (!__any_sync(0xFFFFFFFFu, failed)) {
         if (lane == 0) bulk_wait_all();
@@ -726,22 +895,17 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     }
     // drain after an abort: copies and MMAs this role issued must finish first
     if (pt == 0) {
-      if (raw_pending && !mbar_wait(&bars[B_RAW], raw_pending_j & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
-      if (pmma_issued > pmma_phase && !mbar_wait(&bars[B_PMMA], (pmma_issued - 1) & 1, WAIT_LIMIT_NS))
+      if (raw_pending && !mbar_wait(&bars[B_RAW], raw_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+      if (v_pending && !mbar_wait(&bars[B_RAWV], v_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+      if (pmma_issued > pmma_phase && !mbar_wait(&bars[B_PMMA], (pmma_issued - 1) & 1, DRAIN_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
       bulk_wait_all();
       // records this CTA published must be loaded everywhere before it exits
       for (int jj = (j >= 2 ? j - 2 : 0); !failed && jj < j; ++jj)
-        if (!mbar_wait_cluster(&bars[B_ACK + (jj & 1)], (jj >> 1) & 1, WAIT_LIMIT_NS))
+        if (!mbar_wait_cluster(&bars[B_ACK + (jj & 1)], (jj >> 1) & 1, p.wait_ns))
           atomicOr(p.status, kStatusTimeout);
       PROF_STORE(0);
     }
-#ifdef KDA_PROFILE
-    if (prof_on && lane == 0) {
-      reinterpret_cast<uint64_t*>(p.status)[44 + warp] = ew_acc[0];
-      if (warp == 0) reinterpret_cast<uint64_t*>(p.status)[52] = ew_acc[1];
-    }
-#endif
     __syncwarp();
   } else {
     // ================================ chain ================================
@@ -807,7 +971,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         const int m = next_load;
         if (!mbar_try_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1)) {
           if (m != need) return;
-          if (!mbar_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1, WAIT_LIMIT_NS)) {
+          if (!mbar_wait_cluster(pub_bar(m), (m / NSLICE >> 1) & 1, p.wait_ns)) {
             timeout();
             return;
           }
@@ -821,8 +985,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     auto emit_o = [&](int m) {
       const int rows = min(C, len - m * C);
       if (qw < 2) return;  // only the warps of lane quadrants 2 and 3 read o
-      if (!mbar_wait(&bars[B_C], m & 1, WAIT_LIMIT_NS)) timeout();
-      ++c_done;
+      if (mbar_wait(&bars[B_C], m & 1, p.wait_ns)) ++c_done;  // else drained below
+      else timeout();
       __syncwarp();
       tc_fence_after();
       float orr[32];
@@ -863,7 +1027,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (qt == kLoader && !failed) pump_loads(m + 1, m);
       PROF(6);
       __syncwarp();
-      if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, WAIT_LIMIT_NS)) timeout();
+      if (!mbar_wait(&bars[B_FULL + s], (m >> 1) & 1, p.wait_ns)) timeout();
       if (qt == kLoader && !failed) ++loads_done;
       PROF(0);
       // ---- [X ; O] = [W ; qd] S (one M = 128 accumulator), then chunk m - 1's o update ----
@@ -890,8 +1054,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       // chunk m - 1 is finished with its slot (its reads ended before the last
       // barrier of that chunk, its last MMA with emit_o): chunk m + 1 may load
       if (qt == kLoader && !failed) pump_loads(m + 2, -1);
-      if (!mbar_wait(&bars[B_A], m & 1, WAIT_LIMIT_NS)) timeout();
-      ++a_done;
+      if (mbar_wait(&bars[B_A], m & 1, p.wait_ns)) ++a_done;  // else drained below
+      else timeout();
       __syncwarp();
       tc_fence_after();
       PROF(1);
@@ -937,8 +1101,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
         ++b_issued;
       }
       __syncwarp();
-      if (!mbar_wait(&bars[B_B], m & 1, WAIT_LIMIT_NS)) timeout();
-      ++b_done;
+      if (mbar_wait(&bars[B_B], m & 1, p.wait_ns)) ++b_done;  // else drained below
+      else timeout();
       __syncwarp();
       tc_fence_after();
       PROF(3);
@@ -973,17 +1137,17 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       emit_o(NT - 1);
     }
     if (qt == kIssuer) {  // drain MMAs still in flight after an abort
-      if (a_issued > a_done && !mbar_wait(&bars[B_A], (a_issued - 1) & 1, WAIT_LIMIT_NS))
+      if (a_issued > a_done && !mbar_wait(&bars[B_A], (a_issued - 1) & 1, DRAIN_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
-      if (b_issued > b_done && !mbar_wait(&bars[B_B], (b_issued - 1) & 1, WAIT_LIMIT_NS))
+      if (b_issued > b_done && !mbar_wait(&bars[B_B], (b_issued - 1) & 1, DRAIN_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
-      if (c_issued > c_done && !mbar_wait(&bars[B_C], (c_issued - 1) & 1, WAIT_LIMIT_NS))
+      if (c_issued > c_done && !mbar_wait(&bars[B_C], (c_issued - 1) & 1, DRAIN_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
     }
     if (qt == 0) PROF_STORE(16);
     if (qt == kLoader)  // record loads still in flight after an abort
       for (int m = loads_done; m < next_load; ++m)
-        if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+        if (!mbar_wait(&bars[B_FULL + (m & 1)], (m >> 1) & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
     __syncwarp();
     if (p.sfin && !aborted && !failed) {
       float4* dst = reinterpret_cast<float4*>(p.sfin + state_off + static_cast<size_t>(d) * VD + v0);
@@ -1045,9 +1209,10 @@ constexpr uint32_t SR_AQK = SR_KRT + 16384;
 constexpr uint32_t SR_U = SR_AQK + 8192;      // U^T [128 x 64] (rows = value columns)
 constexpr uint32_t REC_BYTES = SR_U + 16384;  // 74,752 B
 static_assert(REC_BYTES <= GSLOT, "record fits a ring slot");
-// producer pipeline region (offsets from the region base, 1024-aligned)
-constexpr uint32_t P_Q = 0, P_KD = 16384, P_V = 32768, P_B = 49152, P_MB = P_B, P_AMAT = 66560,
-                   P_STG = 74752, P_BETA = 91136, P_GSUM = 91392, P_BAR = 93440, P_STRIDE = 94208;
+// producer pipeline region (offsets from the region base, 1024-aligned): the prep:: tiles,
+// then beta, the quarter sums of g, barriers and the ring-slot flag
+constexpr uint32_t P_BETA = prep::BYTES, P_GSUM = P_BETA + 256, P_BAR = P_GSUM + 2048, P_STRIDE = 93184;
+static_assert(P_BAR + 64 <= P_STRIDE && P_STRIDE % 1024 == 0, "producer pipeline region");
 // chain region
 // chain region: record part A ([qd; W], e^{g_last}) in three buffers, part B (kr^T, Aqk,
 // U^T) in two, then the o staging tiles
@@ -1064,7 +1229,8 @@ static_assert(2 * P_STRIDE <= C_MISC, "producer regions stay below the tmem slot
 static_assert(PA_STRIDE >= REC_A_BYTES && PA_STRIDE % 1024 == 0 && PB_STRIDE % 1024 == 0 && C_PB % 1024 == 0,
               "record buffers keep the 1 KB alignment of the swizzled operands");
 constexpr int CB_FULL = 0, CB_B = 3;  // chain barriers (CB_FULL: [3], one per part-A buffer)
-constexpr int PB_RAW = 0, PB_PMMA = 1;                     // producer barriers (per pipeline)
+constexpr int PB_RAW = 0, PB_PMMA = 1, PB_RAWV = 2;        // producer barriers (per pipeline)
+constexpr uint32_t P_SLOT_FREE = P_BAR + 32;               // shared flag: the record's ring slot may be written
 constexpr uint32_t NB_CHAIN_ALL = 3;
 
 struct Rec {
@@ -1126,19 +1292,18 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
   const uint32_t NB = 1 + static_cast<uint32_t>(pipe);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + P_BAR);
   float* beta_s = reinterpret_cast<float*>(sm + P_BETA);
-  float* mb = reinterpret_cast<float*>(sm + P_MB);
   float* gsum = reinterpret_cast<float*>(sm + P_GSUM);
+  volatile uint32_t* slot_free = reinterpret_cast<volatile uint32_t*>(sm + P_SLOT_FREE);
   const uint32_t sb = smem_u32(sm);
-  const uint64_t D_SW128 = sdesc_sw128(sb);
-  const uint64_t D_KD_MN = sdesc(sb + P_KD, 8192, 1024, 2);
-  const uint64_t D_V_MN = sdesc(sb + P_V, 8192, 1024, 2);
-  auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
+  const uint64_t D_PREP = sdesc_sw128(sb);
+  const uint64_t D_KD_MN = sdesc(sb + prep::KDT, 8192, 1024, 2);
+  const uint64_t D_V_MN = sdesc(sb + prep::VRAW, 8192, 1024, 2);
   const int HV = p.HV;
   const float scale = p.scale;
   uint32_t pmma_phase = 0, pmma_issued = 0;
-  bool raw_pending = false;
-  int raw_pending_j = 0;
-  bool failed = false;
+  bool raw_pending = false, v_pending = false;
+  int raw_pending_j = 0, v_pending_j = 0;
+  bool failed = false, range_bad = false;
   auto timeout = [&]() {
     failed = true;
     atomicOr(p.status, kStatusTimeout);
@@ -1148,14 +1313,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 #endif
   };
   auto issue_raw = [&](const Rec& x, int jj) {  // elected
-    const int row0 = static_cast<int>(x.tok0) + x.m * C;
-    mbar_arrive_expect_tx(&bars[PB_RAW], RAW_TX_BYTES);
-    tma_load_3d(sm + P_Q, &maps.q, &bars[PB_RAW], 0, x.hk, row0);
-    tma_load_3d(sm + P_Q + 8192, &maps.q, &bars[PB_RAW], 64, x.hk, row0);
-    tma_load_3d(sm + P_B, &maps.k, &bars[PB_RAW], 0, x.hk, row0);
-    tma_load_3d(sm + P_B + 8192, &maps.k, &bars[PB_RAW], 64, x.hk, row0);
-    tma_load_3d(sm + P_V, &maps.v, &bars[PB_RAW], 0, x.hv, row0);
-    tma_load_3d(sm + P_V + 8192, &maps.v, &bars[PB_RAW], 64, x.hv, row0);
+    prep::issue_qk(sm, &maps.q32, &maps.k32, &bars[PB_RAW], x.hk, static_cast<int>(x.tok0) + x.m * C);
     raw_pending = true;
     raw_pending_j = jj;
   };
@@ -1204,11 +1362,12 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     const bool next = rn < NREC;
     uint8_t* gs = p.ring + (static_cast<size_t>(cur.u) * RING + (cur.m % SRING)) * GSLOT;
     const int rows = min(C, cur.len - cur.m * C);
-    // ---- 1. raw tiles; the ring slot must have been loaded by the chain ----
+    // ---- 1. raw q, k tiles; is the ring slot known to be free (its previous record
+    //         loaded by the chain, as the counter read ahead shows)? ----
     PSTAMP(0);
-    if (!mbar_wait(&bars[PB_RAW], j & 1, WAIT_LIMIT_NS)) timeout();
+    if (!mbar_wait(&bars[PB_RAW], j & 1, p.wait_ns)) timeout();
     PSTAMP(1);
-    if (pt == 0) bulk_wait_read();  // W/U staging of the previous record has been read
+    if (pt == 0) bulk_wait_read();  // the previous record's Aqk, W and U stagings have been read
     if (pt < C) beta_s[pt] = bpre;
     {
       float2 qsum = make_float2(0.f, 0.f);
@@ -1219,225 +1378,109 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       }
       reinterpret_cast<float2*>(gsum + hq * KD)[dp] = qsum;
     }
+    const uint32_t need = static_cast<uint32_t>(cur.m - SRING + 1);
+    if (pt == kRecStorer) *slot_free = (cur.m < SRING || (flow_n == r && flow_seen >= need)) ? 1u : 0u;
     if (role_any(NB, PIPE, failed)) break;
     PSTAMP(2);
     if (pt == 0) raw_pending = false;
-
-    // ---- 2. elementwise (as in the cluster kernel); e^{g_last} is held until the
-    //         ring slot may be written ----
-    float gam0 = 0.f, gam1 = 0.f;
-    {
-      float2 pre = make_float2(0.f, 0.f), all = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        const float2 v = reinterpret_cast<const float2*>(gsum + qq * KD)[dp];
-        if (qq < hq) {
-          pre.x += v.x;
-          pre.y += v.y;
-        }
-        all.x += v.x;
-        all.y += v.y;
+    if (*slot_free == 0u) {
+      // Not known: publish this pipeline's previous record first (a chain may be waiting
+      // for it, and the ring must never hold a record behind a wait on the chains), then
+      // wait for the slot.
+      if (pt == 0 && pub_pending) bulk_wait_group<0>();
+      role_sync(NB, PIPE);
+      if (pub_pending) {
+        if (pw == 3 && lane == 0) publish(pub_m, pub_u);
+        pub_pending = false;
       }
-      gam0 = ex2_approx(all.x * kLog2e);
-      gam1 = ex2_approx(all.y * kLog2e);
-      float gl0 = pre.x * kLog2e, gl1 = pre.y * kLog2e;
-      uint8_t* qd_t = sm + P_Q;
-      uint8_t* ki_t = sm + P_B;
-      uint8_t* kd_t = sm + P_KD;
-      const uint32_t kbase = static_cast<uint32_t>(dp >> 5) * 8192u + static_cast<uint32_t>(hq) * 16u * 128u +
-                             ((2u * dp) & 7u) * 2u;
-      const uint32_t chunk = ((2u * dp) & 63u) >> 3;
-      uint32_t kr0[8], kr1[8];
-      float kre0 = 0.f, kre1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t off = kbase + i * 128u + ((chunk ^ (i & 7)) << 4);
-        const uint32_t kraw = *reinterpret_cast<const uint32_t*>(ki_t + off);
-        const uint32_t qraw = *reinterpret_cast<const uint32_t*>(qd_t + off);
-        gl0 = fmaf(gpre[i].x, kLog2e, gl0);
-        gl1 = fmaf(gpre[i].y, kLog2e, gl1);
-        const float e0 = ex2_approx(gl0), e1 = ex2_approx(gl1);
-        const float ie0 = ex2_approx(-gl0), ie1 = ex2_approx(-gl1);
-        const bool valid = 16 * hq + i < rows;
-        const float k0 = valid ? __uint_as_float(kraw << 16) : 0.f;
-        const float k1 = valid ? __uint_as_float(kraw & 0xFFFF0000u) : 0.f;
-        const float q0 = valid ? __uint_as_float(qraw << 16) : 0.f;
-        const float q1 = valid ? __uint_as_float(qraw & 0xFFFF0000u) : 0.f;
-        const float ki0 = k0 * ie0, ki1 = k1 * ie1;
-        *reinterpret_cast<uint32_t*>(kd_t + off) = pack2(k0 * e0, k1 * e1);
-        *reinterpret_cast<uint32_t*>(ki_t + off) = pack2(ki0, ki1);
-        *reinterpret_cast<uint32_t*>(qd_t + off) = pack2(q0 * e0 * scale, q1 * e1 * scale);
-        if (i & 1) {
-          kr0[i >> 1] = pack2(kre0, ki0 * gam0);
-          kr1[i >> 1] = pack2(kre1, ki1 * gam1);
-        } else {
-          kre0 = ki0 * gam0;
-          kre1 = ki1 * gam1;
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        st_v4(sm + P_STG + sw128_offset(2 * dp, 16 * hq + 8 * h, 128), kr0[4 * h], kr0[4 * h + 1], kr0[4 * h + 2],
-              kr0[4 * h + 3]);
-        st_v4(sm + P_STG + sw128_offset(2 * dp + 1, 16 * hq + 8 * h, 128), kr1[4 * h], kr1[4 * h + 1],
-              kr1[4 * h + 2], kr1[4 * h + 3]);
-      }
+      if (pt == kRecStorer && !wait_flag_geq(flags + cur.u * 32 + 16, need, p.wait_ns)) timeout();
+      if (role_any(NB, PIPE, failed)) break;
     }
+
+    // ---- 2. elementwise: operand tiles; qd, kr^T and e^{g_last} straight into the record ----
+    {
+      prep::elementwise(sm, gsum, gpre, dp, hq, rows, scale, gs + SR_QW, SR_KB, gs + SR_KRT,
+                        reinterpret_cast<float*>(gs + SR_GAM), range_bad);
+    }
+    fence_proxy_async_global();  // the record's plain stores, read by the chain's bulk copies
     if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's stores have landed
     fence_proxy_async_smem();
     PSTAMP(3);
     role_sync(NB, PIPE);
     PSTAMP(4);
-    if (pub_pending) {  // from warp 3 of the pipeline while thread 0 issues the MMAs
+    if (pub_pending) {  // from warp 3 of the pipeline while warp 0 issues the MMAs
       if (pw == 3 && lane == 0) publish(pub_m, pub_u);
       pub_pending = false;
     }
 
-    // ---- 3. L = kd ki^T, Aqk = qd ki^T; qd and kr^T to the record.  The record's
-    //         ring slot is written only once the chain has loaded its previous
-    //         occupant; the previous record was published above, so a wait here
-    //         never holds back a record some chain needs ----
-    if (pw == 0) {  // the products, issued warp-wide (one elected lane)
+    // ---- 3. the diagonal halves and the block below them of L and Aqk ----
+    if (pw == 0) {
       tc_fence_after();
-      constexpr uint32_t idesc = idesc_f16kind(64, 64);
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t koff = kb * 8192 + ks * 32;
-          const uint64_t bd = d128(P_B + koff);
-          umma_f16_warp(tmem + TM_L, d128(P_KD + koff), bd, idesc, (kb | ks) != 0);
-          umma_f16_warp(tmem + TM_AQ, d128(P_Q + koff), bd, idesc, (kb | ks) != 0);
-        }
+      prep::issue_lqk(tmem, D_PREP);
       umma_commit_warp(&bars[PB_PMMA]);
       ++pmma_issued;
-    } else if (pt == kRecStorer) {  // qd and kr^T to the ring slot, once its occupant has been loaded
-      const uint32_t need = static_cast<uint32_t>(cur.m - SRING + 1);
-      if (cur.m >= SRING && !(flow_n == r && flow_seen >= need) &&
-          !wait_flag_geq(flags + cur.u * 32 + 16, need, WAIT_LIMIT_NS))
-        timeout();
-      if (!failed) {
-        bulk_store(gs + SR_QW, sm + P_Q, 8192);
-        bulk_store(gs + SR_QW + SR_KB, sm + P_Q + 8192, 8192);
-        bulk_store(gs + SR_KRT, sm + P_STG, 16384);
-        bulk_commit();
-      }
     }
     if (next) prefetch_gb(nx, 0);
     __syncwarp();
     PSTAMP(5);
-    if (!mbar_wait(&bars[PB_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
-    ++pmma_phase;
+    if (mbar_wait(&bars[PB_PMMA], pmma_phase & 1, p.wait_ns)) ++pmma_phase;  // else still in flight: drained below
+    else timeout();
     tc_fence_after();
     PSTAMP(6);
-    if (pt == kRecStorer) bulk_wait_read();  // qd (about to hold the Aqk staging) and kr^T have been read
 
-    // ---- 4. TMEM -> M (fp32), Aqk -> staging ----
-    role_sync(NB, PIPE);
-    if (hq == 0) __stcg(reinterpret_cast<float2*>(gs + SR_GAM) + dp, make_float2(gam0, gam1));
-    {
-      const int i = 16 * quad + (lane & 15);
-      const int j0 = 32 * cpart;
-      float rl[32], ra[32];
-      tmem_ld32(tmem_addr(tmem, 32 * quad, TM_L + j0), rl);
-      tmem_ld32(tmem_addr(tmem, 32 * quad, TM_AQ + j0), ra);
-      tmem_ld_wait();
-      if (lane < 16) {
-        const float bi = beta_s[i];
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          float4 v4;
-          const int jj = j0 + 4 * j4;
-          v4.x = (jj + 0 < i) ? bi * rl[4 * j4 + 0] : 0.f;
-          v4.y = (jj + 1 < i) ? bi * rl[4 * j4 + 1] : 0.f;
-          v4.z = (jj + 2 < i) ? bi * rl[4 * j4 + 2] : 0.f;
-          v4.w = (jj + 3 < i) ? bi * rl[4 * j4 + 3] : 0.f;
-          *reinterpret_cast<float4*>(mb + i * MB_LD + jj) = v4;
-        }
-#pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int jj = j0 + 8 * j8 + 2 * t;
-            w[t] = pack2((jj <= i) ? ra[8 * j8 + 2 * t] : 0.f, (jj + 1 <= i) ? ra[8 * j8 + 2 * t + 1] : 0.f);
-          }
-          st_v4(sm + P_Q + sw128_offset(i, j0 + 8 * j8, 64), w[0], w[1], w[2], w[3]);
-        }
-      }
+    // ---- 4. raw v into the [kB; qB] tiles (read by now); TMEM -> M (fp32), Aqk ----
+    if (pt == 0 && !failed) {
+      prep::issue_v(sm, &maps.v, &bars[PB_RAWV], cur.hv, static_cast<int>(cur.tok0) + cur.m * C);
+      v_pending = true;
+      v_pending_j = j;
     }
+    prep::readout_lqk(sm, tmem, beta_s, quad, cpart, lane);
     tc_fence_before();
     fence_proxy_async_smem();
     PSTAMP(7);
     if (role_any(NB, PIPE, failed)) break;
     PSTAMP(8);
     if (pt == 0) {
-      bulk_store(gs + SR_AQK, sm + P_Q, 8192);
+      bulk_store(gs + SR_AQK, sm + prep::AQK_STG, 8192);
       bulk_commit();
     }
     if (next) prefetch_gb(nx, 1);
 
     // ---- 5. inverse and A = T Diag(beta) ----
-    uint8_t* amat = sm + P_AMAT;
-    if (pw < 4) {
-      if (lane < 16) {
-        const int b0 = 16 * pw, jc = lane;
-        float acc[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float* row = mb + (b0 + i) * MB_LD + b0;
-          float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
-#pragma unroll
-          for (int mm = 0; mm < i; mm += 4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(row + mm);
-            s0 = fmaf(-m4.x, acc[mm], s0);
-            if (mm + 1 < i) s1 = fmaf(-m4.y, acc[mm + 1], s1);
-            if (mm + 2 < i) s0 = fmaf(-m4.z, acc[mm + 2], s0);
-            if (mm + 3 < i) s1 = fmaf(-m4.w, acc[mm + 3], s1);
-          }
-          acc[i] = s0 + s1;
-        }
-        __syncwarp(0x0000FFFFu);
-        const float bj = beta_s[b0 + jc];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          mb[(b0 + i) * MB_LD + b0 + jc] = acc[i];
-          *reinterpret_cast<uint16_t*>(amat + sw128_offset(b0 + i, b0 + jc, 64)) = f2bf(acc[i] * bj);
-        }
-      }
-    } else {
-      const int qz = pt - 128;
-      for (int idx = qz; idx < 192; idx += 128) {
-        const int blk = idx >> 5, rem = idx & 31, row = rem >> 1, half = rem & 1;
-        const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        st_v4(amat + sw128_offset(16 * br + row, 16 * bc + 8 * half, 64), 0u, 0u, 0u, 0u);
-      }
-    }
+    prep::inverse_diag_blocks(sm, beta_s, pw, pt, lane);
     PSTAMP(9);
     role_sync(NB, PIPE);
     PSTAMP(10);
     if (next) prefetch_gb(nx, 2);
-    if (pw < 3) inverse_block_columns(mb, beta_s, amat, pw, lane);
+    if (pw < 3) inverse_block_columns(reinterpret_cast<float*>(sm + prep::MB), beta_s, sm + prep::AMAT, pw, lane);
     fence_proxy_async_smem();
     PSTAMP(11);
     role_sync(NB, PIPE);
     PSTAMP(12);
 
     // ---- 6. W = A kd (M = 64, kd as MN-major B) and U^T = v^T A^T (M = 128 value
-    //         columns, v as MN-major A, A as K-major B) ----
+    //         columns, v as MN-major A, A as K-major B); v was issued in step 4, so
+    //         (every thread having passed that step's barrier) it is in flight ----
     if (pw == 0) {
-      tc_fence_after();
-      constexpr uint32_t idesc_w = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
-      constexpr uint32_t idesc_u = idesc_f16kind(128, 64) | IDESC_A_MN_MAJOR;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t ad = d128(P_AMAT + ks * 32);
-        umma_f16_warp(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc_w, ks != 0);
-        umma_f16_warp(tmem + TM_U, D_V_MN + ((ks * 2048) >> 4), ad, idesc_u, ks != 0);
+      if (mbar_wait(&bars[PB_RAWV], j & 1, p.wait_ns)) {
+        if (pt == 0) v_pending = false;
+      } else {
+        timeout();
       }
-      umma_commit_warp(&bars[PB_PMMA]);
-      ++pmma_issued;
+      __syncwarp();
+      if (!__any_sync(0xFFFFFFFFu, failed)) {
+        tc_fence_after();
+        constexpr uint32_t idesc_w = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+        constexpr uint32_t idesc_u = idesc_f16kind(128, 64) | IDESC_A_MN_MAJOR;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = D_PREP + ((prep::AMAT + ks * 32) >> 4);
+          umma_f16_warp(tmem + TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc_w, ks != 0);
+          umma_f16_warp(tmem + TM_U, D_V_MN + ((ks * 2048) >> 4), ad, idesc_u, ks != 0);
+        }
+        umma_commit_warp(&bars[PB_PMMA]);
+        ++pmma_issued;
+      }
     } else if (pt == kRecStorer && next && nx.m >= SRING) {
       // the next record's flow-control counter, read ahead while the products run (the
       // acquire load stalls this warp, which waits for the products anyway)
@@ -1447,17 +1490,15 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     if (next) prefetch_gb(nx, 3);
     __syncwarp();
     PSTAMP(13);
-    if (!mbar_wait(&bars[PB_PMMA], pmma_phase & 1, WAIT_LIMIT_NS)) timeout();
-    ++pmma_phase;
+    if (mbar_wait(&bars[PB_PMMA], pmma_phase & 1, p.wait_ns)) ++pmma_phase;  // else still in flight: drained below
+    else timeout();
     tc_fence_after();
     PSTAMP(14);
-    if (pt == 0 && next && !failed) {
-      bulk_wait_read();  // the Aqk staging (in the q buffer) has been read
-      issue_raw(nx, j + 1);
-    }
+    // the stacked tile (M and A by now) is free again: fetch the next record's q, k
+    if (pt == 0 && next && !failed) issue_raw(nx, j + 1);
 
-    // ---- 7. W -> staging (bf16 SW128, warps 0-3), U^T -> staging (warps 4-7: row v
-    //         of 64 tokens, 128-byte-swizzled) ----
+    // ---- 7. W -> staging over kd (bf16 SW128, warps 0-3), U^T -> staging over v (warps
+    //         4-7: row v of 64 tokens, 128-byte-swizzled) ----
     __syncwarp();
     if (cpart == 0) {
       const int i = 16 * quad + (lane & 15);
@@ -1474,7 +1515,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
             const int q4 = q2 + h;
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8)
-              st_v4(sm + P_KD + sw128_offset(i, 32 * q4 + 8 * j8, 64), pack2(rr[8 * j8], rr[8 * j8 + 1]),
+              st_v4(sm + prep::KDT + sw128_offset(i, 32 * q4 + 8 * j8, 64), pack2(rr[8 * j8], rr[8 * j8 + 1]),
                     pack2(rr[8 * j8 + 2], rr[8 * j8 + 3]), pack2(rr[8 * j8 + 4], rr[8 * j8 + 5]),
                     pack2(rr[8 * j8 + 6], rr[8 * j8 + 7]));
           }
@@ -1482,7 +1523,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       }
     } else {
       const int v = 32 * quad + lane;
-      uint8_t* row = sm + P_STG + v * 128;
+      uint8_t* row = sm + prep::USTG + v * 128;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float rr[32];
@@ -1497,7 +1538,6 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     }
     tc_fence_before();
     fence_proxy_async_smem();
-    fence_proxy_async_global();  // e^{g_last} went out with plain stores
     PSTAMP(15);
     if (role_any(NB, PIPE, failed)) break;
     PSTAMP(16);
@@ -1505,9 +1545,9 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     // ---- 8. W/U to the ring; published early in the next record (or at the end);
     //         a pipeline's first record goes out at once ----
     if (pt == 0) {
-      bulk_store(gs + SR_QW + SR_W_IN_KB, sm + P_KD, 8192);
-      bulk_store(gs + SR_QW + SR_KB + SR_W_IN_KB, sm + P_KD + 8192, 8192);
-      bulk_store(gs + SR_U, sm + P_STG, 16384);
+      bulk_store(gs + SR_QW + SR_W_IN_KB, sm + prep::KDT, 8192);
+      bulk_store(gs + SR_QW + SR_KB + SR_W_IN_KB, sm + prep::KDT + 8192, 8192);
+      bulk_store(gs + SR_U, sm + prep::USTG, 16384);
       bulk_commit();
       if (j == 0) bulk_wait_group<0>();
     }
@@ -1523,12 +1563,14 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     r = rn;
     cur = nx;
   }
+  if (range_bad) atomicOr(p.status, kStatusRange);
   if (pt == 0) bulk_wait_all();
   role_sync(NB, PIPE);
   if (pub_pending && pw == 3 && lane == 0 && !failed) publish(pub_m, pub_u);
   if (pt == 0) {  // drain what this pipeline issued
-    if (raw_pending && !mbar_wait(&bars[PB_RAW], raw_pending_j & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
-    if (pmma_issued > pmma_phase && !mbar_wait(&bars[PB_PMMA], (pmma_issued - 1) & 1, WAIT_LIMIT_NS))
+    if (raw_pending && !mbar_wait(&bars[PB_RAW], raw_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    if (v_pending && !mbar_wait(&bars[PB_RAWV], v_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    if (pmma_issued > pmma_phase && !mbar_wait(&bars[PB_PMMA], (pmma_issued - 1) & 1, DRAIN_LIMIT_NS))
       atomicOr(p.status, kStatusTimeout);
   }
   __syncwarp();
@@ -1623,7 +1665,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   // a bounded wait, skipped once this thread has given up (the loop then runs to its end
   // without work, passing every named barrier the same number of times as the others)
   auto wait = [&](uint64_t* bar, uint32_t parity, int id, int at) {
-    if (!failed && !mbar_wait(bar, parity, WAIT_LIMIT_NS)) timeout(id, at);
+    if (!failed && !mbar_wait(bar, parity, p.wait_ns)) timeout(id, at);
   };
   // Record copies by one helper lane into the buffers of the chunk finished last: part A
   // (three buffers) up to two chunks ahead, part B (two buffers) one chunk ahead.  The
@@ -1674,7 +1716,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
       if (next_a >= known) {
         if (next_a > must_a) break;
         const uint64_t t0 = globaltimer_ns();
-        while (next_a >= known && globaltimer_ns() - t0 <= WAIT_LIMIT_NS) read_flags();
+        while (next_a >= known && globaltimer_ns() - t0 <= p.wait_ns) read_flags();
         if (next_a >= known) {
           timeout(1, next_a);
           break;
@@ -1736,7 +1778,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   role_sync(NB_CHAIN_ALL, NTHREADS);
   tc_fence_after();
   if (warp == kIssuerWarp && NT > 0) {  // the first chunk's first product
-    if (!mbar_wait(&bars[CB_FULL], 0, WAIT_LIMIT_NS)) timeout(4, 0);  // part A of chunk 0
+    if (!mbar_wait(&bars[CB_FULL], 0, p.wait_ns)) timeout(4, 0);  // part A of chunk 0
     __syncwarp();
     if (!__any_sync(0xFFFFFFFFu, failed)) {
       tc_fence_after();
@@ -1942,7 +1984,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   }
   if (warp == kIssuerWarp && a_issued + b_issued + c_issued > 0) {  // MMAs still in flight after a failure
     umma_commit_warp(&bars[CB_DRAIN]);
-    if (lane == 0 && !mbar_wait(&bars[CB_DRAIN], 0, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    if (lane == 0 && !mbar_wait(&bars[CB_DRAIN], 0, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
   }
 #ifdef KDA_PROFILE
   __syncwarp();
@@ -1953,9 +1995,9 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
 #endif
   if (is_loader) {  // copies still in flight after an abort (a consumed phase returns at once)
     for (int n = max(0, next_a - 3); n < next_a; ++n)
-      if (!mbar_wait(&bars[CB_FULL + n % 3], (n / 3) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+      if (!mbar_wait(&bars[CB_FULL + n % 3], (n / 3) & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
     for (int n = max(0, next_b - 2); n < next_b; ++n)  // (after a failure the phase may lack its commit)
-      if (!mbar_wait(&bars[CB_AB + (n & 1)], (n >> 1) & 1, WAIT_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+      if (!mbar_wait(&bars[CB_AB + (n & 1)], (n >> 1) & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
   }
   if (tid == kStorer) bulk_wait_all();
   __syncwarp();
@@ -1993,9 +2035,10 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
         uint64_t* pb = reinterpret_cast<uint64_t*>(sm + pp * split::P_STRIDE + split::P_BAR);
         mbar_init(&pb[split::PB_RAW], 1);
         mbar_init(&pb[split::PB_PMMA], 1);
+        mbar_init(&pb[split::PB_RAWV], 1);
       }
-      tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.q32);
+      tma_prefetch_desc(&maps.k32);
       tma_prefetch_desc(&maps.v);
     }
     fence_mbar_init();
@@ -2037,14 +2080,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// 3-D map over a [tokens, heads, dim] bf16 tensor with a (64, 1, 64) box, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int dim, int heads, long tokens) {
+// 3-D map over a [tokens, heads, dim] bf16 tensor with a (64, 1, box_tokens) box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int dim, int heads, long tokens, int box_tokens = C) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(tokens)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 2, static_cast<cuuint64_t>(heads) * dim * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(C)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_tokens)};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -2076,6 +2119,7 @@ int split_override() {
 struct DeviceInfo {
   int sms = 0;
   bool coop = false, split_fits = false;
+  bool fused_attr = false;  // the cluster kernel's shared-memory attribute is set on this device
 };
 const DeviceInfo& device_info() {
   static std::mutex mu;
@@ -2098,6 +2142,8 @@ const DeviceInfo& device_info() {
                                                         tc::split::SMEM_ALLOC) == cudaSuccess)
         d.split_fits = blocks >= 1;
     }
+    d.fused_attr = cudaFuncSetAttribute(tc::kda_chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        tc::SMEM_ALLOC) == cudaSuccess;
     cudaGetLastError();
     known[dev] = true;
   }
@@ -2118,7 +2164,7 @@ bool use_split_kernel(int NU) {
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
   const long tokens = p.cu ? static_cast<long>(p.T) : static_cast<long>(p.num_seqs) * p.T;
   tc::Maps maps;
-  if (!tc::make_map(&maps.q, p.q, tc::KD, p.H, tokens) || !tc::make_map(&maps.k, p.k, tc::KD, p.H, tokens) ||
+  if (!tc::make_map(&maps.q32, p.q, tc::KD, p.H, tokens, 32) || !tc::make_map(&maps.k32, p.k, tc::KD, p.H, tokens, 32) ||
       !tc::make_map(&maps.v, p.v, tc::VD, p.HV, tokens))
     return cudaErrorInvalidValue;
   const int NU = p.num_seqs * p.HV;
@@ -2143,13 +2189,7 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel, maps, p, NU, nrec);
   }
   if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return cudaGetLastError();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc::kda_chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (!dev.fused_attr) return cudaErrorInvalidConfiguration;
   dim3 grid(tc::NSLICE, p.HV, p.num_seqs);
   tc::kda_chunk_fused_kernel<<<grid, tc::NTHREADS, tc::SMEM_ALLOC, stream>>>(maps, p);
   return cudaGetLastError();

@@ -11,6 +11,7 @@ namespace kda {
 // Device status word bits (the first 32-bit word of the workspace).
 constexpr uint32_t kStatusTimeout = 1u;   // a bounded on-chip wait gave up
 constexpr uint32_t kStatusBounds = 2u;    // cu_seqlens entry out of order / range
+constexpr uint32_t kStatusRange = 4u;     // a 16-token block of g decays faster than the chunk kernels support
 
 // Workspace layout: [0, 4) status word, [8, kFlagOffset) optional profile counters,
 // [kFlagOffset, kFlagOffset + kMaxSplitUnits * kFlagBytesPerUnit) the record
@@ -37,6 +38,7 @@ struct FwdParams {
   float* sfin;           // [NS, HV, K, V] or null
   uint32_t* status;      // device status word
   uint8_t* ring;         // per-(sequence, value head) record ring (chunk kernel), or null
+  unsigned long long wait_ns;  // limit of a bounded wait for work (drains have their own)
   float scale;
   int T;                 // tokens per sequence (fixed length) or packed total
   int H, HV, K, V;

@@ -109,10 +109,15 @@ def varlen_lengths(rng: np.random.Generator, num_seqs: int, max_len: int) -> np.
 
 def make_inputs(B: int, T: int, H: int, HV: int, K: int, V: int, io_dtype: str = "bf16",
                 seed: int = 0, init_state: bool = False, lengths=None,
-                g_scale: float = 1.0 / 8.0) -> Inputs:
+                g_scale: float = 1.0 / 8.0, gate: str = "logsigmoid", gate_value: float = -5.0) -> Inputs:
     """Draw one set of inputs.  ``lengths`` (a list of ints) selects varlen packing
-    (then B must be 1 and T is ignored).  ``g_scale`` divides nothing else; it is the
-    factor on logsigmoid(N(0,1)) (1/8 in every stated workload)."""
+    (then B must be 1 and T is ignored).  The decay g per (token, value head, key dim):
+      gate="logsigmoid": g = g_scale * logsigmoid(N(0,1))  (g_scale = 1/8 in every stated
+                         workload; 1 gives the unscaled gate)
+      gate="bounded":    g = gate_value * sigmoid(N(0,1))  (a lower-bounded gate, gate_value
+                         the bound, e.g. -5)
+      gate="const":      g = gate_value everywhere (the same normal draw is still taken, so
+                         the other tensors do not change with the gate)."""
     rng = np.random.default_rng(seed)
     cu = None
     if lengths is not None:
@@ -125,7 +130,15 @@ def make_inputs(B: int, T: int, H: int, HV: int, K: int, V: int, io_dtype: str =
     q = _l2norm(rng.standard_normal((B, T, H, K), dtype=np.float32))
     k = _l2norm(rng.standard_normal((B, T, H, K), dtype=np.float32))
     v = rng.standard_normal((B, T, HV, V), dtype=np.float32)
-    g = (_logsigmoid(rng.standard_normal((B, T, HV, K), dtype=np.float32)) * np.float32(g_scale))
+    gn = rng.standard_normal((B, T, HV, K), dtype=np.float32)
+    if gate == "logsigmoid":
+        g = _logsigmoid(gn) * np.float32(g_scale)
+    elif gate == "bounded":
+        g = np.float32(gate_value) * _sigmoid(gn)
+    elif gate == "const":
+        g = np.full_like(gn, np.float32(gate_value))
+    else:
+        raise ValueError(f"unknown gate {gate!r}")
     beta = _sigmoid(rng.standard_normal((B, T, HV), dtype=np.float32))
     s0 = None
     if init_state:

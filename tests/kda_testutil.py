@@ -75,3 +75,15 @@ def check_units(x, o_gpu, S_gpu, units, form="recurrent"):
                          what=f"unit {(s, h)}")
         worst = (max(worst[0], e[0]), max(worst[1], e[1]))
     return worst
+
+
+def check_all_units(x, o_gpu, S_gpu, block=64, form="recurrent"):
+    """Compare the GPU result with the oracle on every (sequence, value head) unit,
+    `block` units per oracle call (the oracle runs them on all host cores)."""
+    HV = x.v.shape[2]
+    units = [(s, h) for s in range(x.num_seqs) for h in range(HV)]
+    worst = (0.0, 0.0)
+    for i in range(0, len(units), block):
+        e = check_units(x, o_gpu, S_gpu, units[i:i + block], form=form)
+        worst = (max(worst[0], e[0]), max(worst[1], e[1]))
+    return worst

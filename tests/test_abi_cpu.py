@@ -37,7 +37,7 @@ def test_exports_match_header(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(10):
         s = kda.kda_status_string(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert kda.kda_status_string(99) == "unknown status"

@@ -1,9 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
 same seeded inputs, element by element.
 
-Small and headline workloads are compared in full; the large ones on sampled
-(sequence, value head) units the oracle computes one by one, in the same
-launch configuration the benchmark times.
+Every workload is compared in full with the chunk kernels: the small and
+headline ones in one oracle call, the large ones unit by unit, in the launch
+configuration the benchmark times.  The token-recurrent kernel is compared on
+sampled units of the large ones.
 """
 import os
 
@@ -13,7 +14,7 @@ import torch
 
 import kimi_delta_attention_gb300 as kda
 from kimi_delta_attention_gb300 import workloads as W
-from kda_testutil import assert_close, check_units, np32, oracle_full, seq_bounds
+from kda_testutil import assert_close, check_all_units, check_units, np32, oracle_full, seq_bounds
 
 pytestmark = pytest.mark.gpu
 
@@ -73,6 +74,16 @@ def test_workload_full(entry, idx):
     assert_close(o.float().cpu().numpy(), S.cpu().numpy(), o_ref, S_ref, x.io_dtype, f"w{idx} {entry}")
 
 
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_workload_every_unit(idx):
+    """The large workloads at full size, in the launch configuration the benchmark
+    uses (kda_chunk_fwd's own dispatch), compared with the oracle on every
+    (sequence, value head) unit: o row by row and each final state."""
+    x = workload(idx)
+    o, S = run("chunk", x)
+    check_all_units(x, o, S)
+
+
 SAMPLED = {
     2: [(0, 0), (1, 9), (2, 20), (3, 31)],
     3: "all_seqs",
@@ -80,11 +91,11 @@ SAMPLED = {
 }
 
 
-@pytest.mark.parametrize("entry", ["chunk", "recurrent"])
 @pytest.mark.parametrize("idx", [2, 3, 4])
-def test_workload_sampled(entry, idx):
+def test_workload_sampled_recurrent(idx):
+    """The token-recurrent kernel on the large workloads: sampled units."""
     x = workload(idx)
-    o, S = run(entry, x)
+    o, S = run("recurrent", x)
     units = SAMPLED[idx]
     if units == "all_seqs":
         units = [(s, (5 * s) % x.v.shape[2]) for s in range(x.num_seqs)]

@@ -2,7 +2,8 @@
 device memory (their host framework owns every allocation, or they must not pay
 for cudaMalloc's implicit synchronisation on the hot path).  Its scratch lives in
 a fixed array inside the library, so it must give the same results as
-kda_chunk_fwd with a caller-provided workspace, call after call.
+kda_chunk_fwd with a caller-provided workspace, and as the fp64 oracle, call
+after call.
 
 This file is collected last so that a stop-at-first-failure run has already
 run every other test when it gets here."""
@@ -15,6 +16,7 @@ import torch
 import kimi_delta_attention_gb300 as kda
 from kimi_delta_attention_gb300 import _lib
 from kimi_delta_attention_gb300 import workloads as W
+from kda_testutil import assert_close, oracle_full
 
 # same bar as the parity tests (bf16 I/O): o relative to max|o|, state in Frobenius norm
 O_TOL, S_TOL = 2e-2, 1e-2
@@ -45,27 +47,46 @@ def test_capacity_is_checked_on_the_host():
     assert code == 8 and kda.kda_status_string(code).startswith("more")
 
 
+CASES = [
+    dict(name="8 units, ragged tail", B=1, T=1000, H=8, HV=8, seed=21, init_state=False),
+    dict(name="32 units (the limit), grouped value heads", B=2, T=700, H=2, HV=16, seed=22, init_state=True),
+    dict(name="32 units, cluster kernel", B=2, T=700, H=2, HV=16, seed=23, init_state=True, split="0"),
+    dict(name="varlen, 4 sequences x 8 value heads", lengths=[1, 130, 64, 300], H=4, HV=8, seed=24,
+         init_state=True),
+]
+
+
 @pytest.mark.gpu
-def test_static_scratch_matches_workspace_entry_two_calls_in_a_row():
+@pytest.mark.parametrize("case", CASES, ids=[c["name"] for c in CASES])
+def test_static_scratch_matches_workspace_entry_two_calls_in_a_row(case, monkeypatch):
+    """Two calls in a row through the C ABI; each is compared with kda_chunk_fwd on a
+    caller-provided workspace and with the fp64 oracle."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     kda.build()
-    cases = [
-        dict(B=1, T=1000, H=8, HV=8, seed=21, init_state=False),     # 8 units, ragged tail
-        dict(B=2, T=700, H=2, HV=16, seed=22, init_state=True),      # 32 units (the limit), GVA
-    ]
-    for c in cases:
-        x = W.make_inputs(c["B"], c["T"], c["H"], c["HV"], 128, 128, "bf16", seed=c["seed"],
-                          init_state=c["init_state"]).to("cuda")
-        o_ref, s_ref = kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, x.scale, initial_state=x.initial_state)
-        o, s, status_addr = kda.kda_chunk_fwd_static_scratch(x.q, x.k, x.v, x.g, x.beta, x.scale,
-                                                             initial_state=x.initial_state)
+    if "split" in case:
+        monkeypatch.setenv("KDA_CHUNK_SPLIT", case["split"])
+    if "lengths" in case:
+        x = W.make_inputs(1, 0, case["H"], case["HV"], 128, 128, "bf16", seed=case["seed"],
+                          init_state=case["init_state"], lengths=case["lengths"])
+    else:
+        x = W.make_inputs(case["B"], case["T"], case["H"], case["HV"], 128, 128, "bf16", seed=case["seed"],
+                          init_state=case["init_state"])
+    o_or, s_or = oracle_full(x)
+    d = x.to("cuda")
+    o_ref, s_ref = kda.kda_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.scale, initial_state=d.initial_state,
+                                     cu_seqlens=d.cu_seqlens)
+    for call in range(2):
+        o, s, status_addr = kda.kda_chunk_fwd_static_scratch(d.q, d.k, d.v, d.g, d.beta, d.scale,
+                                                             initial_state=d.initial_state,
+                                                             cu_seqlens=d.cu_seqlens)
         torch.cuda.synchronize()
         assert status_addr
         assert _lib.load_library().kda_read_device_status(ctypes.c_void_p(status_addr), None) == 0
         assert torch.isfinite(o.float()).all()
-        assert _rel(o, o_ref) <= O_TOL, c
-        assert _frob(s, s_ref) <= S_TOL, c
+        assert _rel(o, o_ref) <= O_TOL, (case["name"], call)
+        assert _frob(s, s_ref) <= S_TOL, (case["name"], call)
+        assert_close(o.float().cpu().numpy(), s.cpu().numpy(), o_or, s_or, "bf16", f"{case['name']} call {call}")
 
 
 @pytest.mark.gpu
