@@ -98,7 +98,6 @@ constexpr int B_PMMA = 13;   // producer MMA commits
 constexpr int B_A = 14;      // chain X/O MMA commit
 constexpr int B_B = 15;      // chain P MMA commit
 constexpr int B_C = 16;      // chain O += Aqk v_new commit
-constexpr int B_RAWV = 17;   // producer raw v (tx)
 
 // TMEM columns
 // chain: D_A[m & 1] holds X = W S in lanes 0-63 and o (qd S + Aqk v_new) in lanes
@@ -278,60 +277,64 @@ __device__ __forceinline__ void inverse_block_columns(float* mb, const float* be
 // while both factors are representable.  With one reference r per chunk (the chunk
 // start) e^{-gc_j} overflows once a chunk's cumulative decay passes about -88, which
 // the bounded gate of the method (g >= -5 per token, i.e. -320 over 64 tokens) reaches
-// easily.  So the lower triangles of L and Aqk are formed as three blocks, each with a
-// reference between its rows and its columns:
-//   * the two 32 x 32 diagonal halves, referenced at the half's middle row (the end of
+// easily.  So the lower triangles of L and Aqk are formed as three blocks:
+//   * the two 32 x 32 diagonal halves, each referenced at its middle row (the end of
 //     its first 16-row quarter): every factor is bounded by the decay over 16 tokens;
-//   * the 32 x 32 block below them (rows 32-63, columns 0-31), referenced at row 32:
-//     both factors are <= 1, and one that underflows pairs with a product that is
-//     negligible anyway.
+//   * the 32 x 32 block below them (rows 32-63, columns 0-31), whose rows reuse the
+//     second half's operands (reference: row 48) and whose columns carry
+//     e^{gc_47 - gc_j} <= 1.  A column factor that flushes to zero (below 2^-126)
+//     drops a product smaller than 2^{-126} times the row factor, itself at most
+//     2^{-s_2} (s_2 the decay of rows 32-47, log2 units), so under the range below the
+//     dropped terms are under 2^-10, beneath the bf16 rounding of the operands.
 // The factors are built from the within-quarter cumsum x (0 >= x >= s_q, the quarter's
 // decay in log2 units) and per-quarter constants, so no intermediate leaves the range
 // either.  The supported range is therefore: the decay of every 16-token quarter of a
-// chunk (per key dimension) is >= kMinQuarterLog2 (about -83 in natural-log units);
-// the producers report a quarter outside it with kStatusRange.  The
-// chunk-start-referenced factors kd, qd and kr are all <= 1 (their underflow is
-// harmless) and stay as they were.
+// chunk (per key dimension) is >= kMinQuarterLog2 = -116 (-80.4 in natural-log
+// units), which g >= -5 per token meets; the producers report a quarter outside it
+// with kStatusRange.  The chunk-start-referenced factors kd, qd and kr are all <= 1
+// (their underflow is harmless) and stay as they were.
 //
 // Tile layout of a producer (offsets from its 1024-aligned base; bf16 K-major tiles in
 // the 128-byte swizzle layout, two 64-column K-blocks each):
 //   QK    stacked [k rows 0-31 | q rows 0-31 | k rows 32-63 | q rows 32-63], the raw tiles
 //         as TMA lands them (32-row boxes), rewritten in place as kA / qA (half-middle
-//         reference): the 128-row A operand of the diagonal product
-//   CA    cA = k e^{mid - gc} (64 rows): B operand of the diagonal product
-//   KD    kd = k e^{gc} (64 rows): MN-major B operand of W = A kd
-//   KBQB  [kB rows 32-63 | qB rows 32-63] (row-32 reference): A operand of the
-//         off-diagonal product
-//   CB    cB = k e^{gc_31 - gc} for rows 0-31: its B operand
+//         reference): the 128-row A operand of the L/Aqk product
+//   CC    [cA rows 0-63 | cB rows 0-31]: its 96-row B operand, cA = k e^{mid - gc}
+//         (reference: the row's own half) and cB = k e^{gc_47 - gc} (rows of the first half)
+//   KDT   kd = k e^{gc} (64 rows): MN-major B operand of W = A kd
+//   VRAW  the raw v tiles (loaded with q and k)
+//   QDS   (split kernel) qd staging, bulk-copied into the record
 // and, once the products have read them,
-//   MB / AMAT  M (fp32) and A = T Diag(beta) (bf16) over QK;  AQK_STG (bf16 Aqk) over CA;
-//   VRAW  the raw v tiles (loaded after the L/Aqk products) over KBQB, then the U staging.
-// qd and kr^T are written by the elementwise pass straight into the record (global).
+//   MB / AMAT  M (fp32) and A = T Diag(beta) (bf16) over QK;  AQK_STG (bf16 Aqk) and
+//   then the U staging over CC;  the W staging over KDT.
+// kr^T (and, in the cluster kernel, qd) is written by the elementwise pass straight into the
+// record (global).
 // ======================================================================
 namespace prep {
 constexpr uint32_t QK = 0;
 constexpr uint32_t QK_KB = 16384;  // one K-block of the stacked 128-row tile
-constexpr uint32_t CA = 32768;
-constexpr uint32_t KDT = 49152;
-constexpr uint32_t KBQB = 65536;
-constexpr uint32_t CB = 81920;
+constexpr uint32_t CC = 32768;     // [cA rows 0-63 | cB rows 0-31]: the 96-row B operand
+constexpr uint32_t CC_KB = 12288;  // one K-block of it
+constexpr uint32_t KDT = 57344;
+constexpr uint32_t VRAW = 73728;
 constexpr uint32_t BYTES = 90112;
+constexpr uint32_t QDS = BYTES;        // optional qd staging tile (64 rows), right after the others
 constexpr uint32_t MB = QK;
 constexpr uint32_t AMAT = QK + 17408;  // after M (64 x MB_LD fp32)
-constexpr uint32_t AQK_STG = CA;
-constexpr uint32_t VRAW = KBQB;
-constexpr uint32_t USTG = KBQB;
-static_assert(AMAT + 8192 <= CA && MB_LD * 64 * 4 <= 17408, "M and A fit the stacked tile");
-constexpr uint32_t QK_TX = 32768, V_TX = 16384;
-// TMEM columns of the two products (relative to the producer's TMEM base)
-constexpr uint32_t TM_DIAG = 0;    // M = 128, N = 64: lane r = stacked row r
-constexpr uint32_t TM_OFF = 64;    // M = 64, N = 32: row r at lane 32 (r / 16) + r % 16
-constexpr float kMinQuarterLog2 = -120.f;
+constexpr uint32_t AQK_STG = CC;
+constexpr uint32_t USTG = CC;          // after the Aqk staging has been read
+static_assert(AMAT + 8192 <= CC && MB_LD * 64 * 4 <= 17408, "M and A fit the stacked tile");
+static_assert(CC + 2 * CC_KB <= KDT && KDT + 16384 <= VRAW && VRAW + 16384 <= BYTES, "producer tiles");
+constexpr uint32_t RAW_TX = 32768 + 16384;  // q, k and v tiles of one chunk
+// TMEM columns of the L/Aqk product (relative to the producer's TMEM base): M = 128, N = 96,
+// lane r = stacked row r; columns 0-63 against cA, 64-95 against cB
+constexpr uint32_t TM_LQ = 0;
+constexpr float kMinQuarterLog2 = -116.f;
 
-// q and k tiles of chunk rows [row0, row0 + 64) into the stacked tile (32-row boxes).
-__device__ __forceinline__ void issue_qk(uint8_t* base, const CUtensorMap* q32, const CUtensorMap* k32,
-                                         uint64_t* bar, int hk, int row0) {
-  mbar_arrive_expect_tx(bar, QK_TX);
+// q, k (into the stacked tile, 32-row boxes) and v tiles of chunk rows [row0, row0 + 64).
+__device__ __forceinline__ void issue_raw(uint8_t* base, const CUtensorMap* q32, const CUtensorMap* k32,
+                                          const CUtensorMap* v, uint64_t* bar, int hk, int hv, int row0) {
+  mbar_arrive_expect_tx(bar, RAW_TX);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb) {
     uint8_t* t = base + QK + kb * QK_KB;
@@ -340,11 +343,31 @@ __device__ __forceinline__ void issue_qk(uint8_t* base, const CUtensorMap* q32, 
     tma_load_3d(t + 8192, k32, bar, 64 * kb, hk, row0 + 32);
     tma_load_3d(t + 12288, q32, bar, 64 * kb, hk, row0 + 32);
   }
-}
-__device__ __forceinline__ void issue_v(uint8_t* base, const CUtensorMap* v, uint64_t* bar, int hv, int row0) {
-  mbar_arrive_expect_tx(bar, V_TX);
   tma_load_3d(base + VRAW, v, bar, 0, hv, row0);
   tma_load_3d(base + VRAW + 8192, v, bar, 64, hv, row0);
+}
+
+// Two fp32 lanes in one 64-bit register: the packed (.f32x2) multiply of sm_100 and later
+// does both dims of a thread in one instruction.
+__device__ __forceinline__ unsigned long long f2u(float lo, float hi) {
+  unsigned long long u;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(lo), "f"(hi));
+  return u;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// bf16 pair (lo in the low half) of a packed fp32 pair
+__device__ __forceinline__ uint32_t pack2u(unsigned long long u) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(u));
+  return pack2(lo, hi);
+}
+// the two fp32 values of a bf16 pair, as a packed fp32 pair
+__device__ __forceinline__ unsigned long long bf2u(uint32_t b) {
+  return f2u(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -358,25 +381,26 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 
 // Elementwise pass of thread (dp, hq): key dims 2 dp, 2 dp + 1 of chunk rows
 // [16 hq, 16 hq + 16) (quarter hq).  gsum holds the four quarter sums of g (natural
-// log) per key dim; g holds this thread's 16 rows.  Writes kA/qA (in place), cA, kd
-// and kB/qB (hq >= 2) or cB (hq < 2) to the tiles, and qd, kr^T and (hq = 0)
-// e^{g_last} into the record: qd_rec + kb * qd_kb_stride + (SW128 row offset),
-// krt_rec + (SW128 offset in the [128 x 64] kr^T tile), gam_rec.  Sets range_bad when
-// this quarter decays faster than the factors can represent.
+// log) per key dim; g holds this thread's 16 rows.  Writes kA/qA (in place), cA, kd and
+// (hq < 2) cB to the tiles, kr^T and (hq = 0) e^{g_last} into the record (krt_rec +
+// SW128 offset in the [128 x 64] kr^T tile, gam_rec), and qd either to the tile QDS
+// (QD_SMEM, for a bulk copy) or into the record (qd_rec + kb * qd_kb_stride + SW128 row
+// offset).  Sets range_bad when this quarter decays faster
+// than the factors can represent.
 //
 // With x the within-quarter cumsum (log2 units; 0 >= x >= sh, sh the quarter's sum),
 // pre the decay before the quarter and all the chunk's:
 //   kd, qd = (k, scale q) 2^pre 2^x            kr = k 2^{all - pre - sh} (2^sh 2^-x)
 //   kA, qA = (k, scale q) 2^x (2^-sh if hq even: the half's middle is the quarter's end)
 //   cA     = k 2^-x (2^sh if hq even)
-//   kB, qB = (k, scale q) 2^x (2^{s_2} if hq = 3)      [reference: row 32]
-//   cB     = k (2^sh 2^-x) (2^{s_1} if hq = 0)
-// where 2^sh 2^-x lies in [2^sh, 1] and every other product of two factors is <= 1.
+//   cB     = k (2^sh 2^-x) 2^{s_2} (2^{s_1} if hq = 0)      [reference: row 48]
+// where 2^sh 2^-x lies in [2^sh, 1] and every other product of factors is <= 1.
 //
 // Addressing: every tile base is 1024-aligned and a row is 128 bytes, so the 128-byte
 // swizzle (16-byte chunk index XOR row % 8) is an XOR on address bits 4-6 that commutes
 // with adding the row and the tile offsets; one 32-bit shared address per row serves
 // all tiles.
+template <bool QD_SMEM>
 __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, const float2 (&g)[16], int dp, int hq,
                                             int rows, float scale, uint8_t* qd_rec, uint32_t qd_kb_stride,
                                             uint8_t* krt_rec, float* gam_rec, bool& range_bad) {
@@ -394,10 +418,13 @@ __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, co
     c_d[e] = ex2_approx(pre);
     c_r[e] = ex2_approx(all - pre - sh);
     es[e] = ex2_approx(sh);
-    fa[e] = even ? ex2_approx(-sh) : 1.f;                               // kA, qA
-    fb[e] = hq == 3 ? ex2_approx(s[2]) : hq == 0 ? ex2_approx(s[1]) : 1.f;  // kB, qB / cB
+    fa[e] = even ? ex2_approx(-sh) : 1.f;                       // kA, qA
+    fb[e] = ex2_approx(hq == 0 ? s[1] + s[2] : s[2]);           // cB (hq < 2)
     if (hq == 0) gam_rec[2 * dp + e] = ex2_approx(all);
   }
+  // the per-dim constants as packed pairs
+  const unsigned long long CD = f2u(c_d[0], c_d[1]), CR = f2u(c_r[0], c_r[1]), ES = f2u(es[0], es[1]),
+                           FA = f2u(fa[0], fa[1]), FB = f2u(fb[0], fb[1]), SC = f2u(scale, scale);
   const uint32_t kb = static_cast<uint32_t>(dp) >> 5;
   const uint32_t r0 = 16u * static_cast<uint32_t>(hq);
   const uint32_t lo = ((2u * dp) & 7u) * 2u;
@@ -405,56 +432,55 @@ __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, co
   // row r0 of each tile, before the swizzle XOR (tile offsets and rows keep bits 4-6 clear)
   const uint32_t X = smem_u32(base) + r0 * 128u + lo + c4;
   const uint32_t a_k = QK + kb * QK_KB + (hq >= 2 ? 32u : 0u) * 128u;  // stacked row of k row r0
-  const uint32_t a_64 = kb * 8192u;                                    // + CA / KDT
-  const uint32_t a_b = hq >= 2 ? KBQB + kb * 8192u - 32u * 128u : CB + kb * 4096u;
+  const uint32_t a_c = CC + kb * CC_KB;                                // cA row r0 (cB: + 64 rows)
+  const uint32_t a_d = KDT + kb * 8192u;                               // kd (and the qd staging: + QDS - KDT)
   uint8_t* qdr = qd_rec + kb * qd_kb_stride + r0 * 128u + lo;
+  const int nvalid = rows - static_cast<int>(r0);  // rows of this quarter that exist (may be <= 0 or > 16)
   uint32_t kr[2][4];
-  float kre[2] = {0.f, 0.f};
+  uint32_t kre = 0u;  // kr of the previous (even) row, bf16 pair (dims 2 dp, 2 dp + 1)
   float x0 = 0.f, x1 = 0.f;
+  uint32_t kn = lds32(X + a_k), qn = lds32(X + a_k + 4096u);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint32_t swz = (static_cast<uint32_t>(i) & 7u) << 4;
     const uint32_t Y = (X ^ swz) + static_cast<uint32_t>(i) * 128u;  // row r0 + i, any tile
-    const uint32_t kraw = lds32(Y + a_k), qraw = lds32(Y + a_k + 4096u);
+    const uint32_t vm = i < nvalid ? 0xFFFFFFFFu : 0u;                // rows past the end act as k = q = 0
+    const uint32_t kraw = kn & vm, qraw = qn & vm;
+    if (i < 15) {  // the next row's raw values, ahead of this row's stores
+      const uint32_t Yn = (X ^ ((static_cast<uint32_t>(i + 1) & 7u) << 4)) + static_cast<uint32_t>(i + 1) * 128u;
+      kn = lds32(Yn + a_k);
+      qn = lds32(Yn + a_k + 4096u);
+    }
     x0 = fmaf(g[i].x, kLog2e, x0);
     x1 = fmaf(g[i].y, kLog2e, x1);
-    const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-    const float ie0 = ex2_approx(-x0), ie1 = ex2_approx(-x1);
-    const bool valid = static_cast<int>(r0) + i < rows;
-    const float k0 = valid ? __uint_as_float(kraw << 16) : 0.f;
-    const float k1 = valid ? __uint_as_float(kraw & 0xFFFF0000u) : 0.f;
-    const float q0 = valid ? __uint_as_float(qraw << 16) * scale : 0.f;
-    const float q1 = valid ? __uint_as_float(qraw & 0xFFFF0000u) * scale : 0.f;
-    const float p0 = ie0 * es[0], p1 = ie1 * es[1];  // 2^{sh - x}
+    const unsigned long long E = f2u(ex2_approx(x0), ex2_approx(x1));
+    const unsigned long long IE = f2u(ex2_approx(-x0), ex2_approx(-x1));
+    const unsigned long long Kv = bf2u(kraw), Qv = mul2(bf2u(qraw), SC);
+    const unsigned long long Pv = mul2(IE, ES);  // 2^{sh - x}
     {
-      const float a0 = e0 * fa[0], a1 = e1 * fa[1];
-      sts32(Y + a_k, pack2(k0 * a0, k1 * a1));
-      sts32(Y + a_k + 4096u, pack2(q0 * a0, q1 * a1));
-      const float cc0 = even ? p0 : ie0, cc1 = even ? p1 : ie1;
-      sts32(Y + a_64 + CA, pack2(k0 * cc0, k1 * cc1));
+      const unsigned long long Av = even ? mul2(E, FA) : E;
+      sts32(Y + a_k, pack2u(mul2(Kv, Av)));
+      sts32(Y + a_k + 4096u, pack2u(mul2(Qv, Av)));
+      sts32(Y + a_c, pack2u(mul2(Kv, even ? Pv : IE)));
     }
     {
-      const float d0 = e0 * c_d[0], d1 = e1 * c_d[1];
-      sts32(Y + a_64 + KDT, pack2(k0 * d0, k1 * d1));
-      __stcg(reinterpret_cast<uint32_t*>(qdr + ((c4 ^ swz) + static_cast<uint32_t>(i) * 128u)), pack2(q0 * d0, q1 * d1));
+      const unsigned long long Dv = mul2(E, CD);
+      sts32(Y + a_d, pack2u(mul2(Kv, Dv)));
+      if (QD_SMEM)
+        sts32(Y + a_d + (QDS - KDT), pack2u(mul2(Qv, Dv)));
+      else
+        __stcg(reinterpret_cast<uint32_t*>(qdr + ((c4 ^ swz) + static_cast<uint32_t>(i) * 128u)), pack2u(mul2(Qv, Dv)));
     }
-    if (hq >= 2) {
-      const float b0 = e0 * fb[0], b1 = e1 * fb[1];
-      sts32(Y + a_b, pack2(k0 * b0, k1 * b1));
-      sts32(Y + a_b + 4096u, pack2(q0 * b0, q1 * b1));
-    } else {
-      const float b0 = p0 * fb[0], b1 = p1 * fb[1];
-      sts32(Y + a_b, pack2(k0 * b0, k1 * b1));
-    }
-    const float kr0 = k0 * (p0 * c_r[0]), kr1 = k1 * (p1 * c_r[1]);
+    if (hq < 2) sts32(Y + a_c + 64u * 128u, pack2u(mul2(Kv, mul2(Pv, FB))));
+    // kr^T rows 2 dp and 2 dp + 1: bf16 pairs along the tokens
+    const uint32_t krp = pack2u(mul2(Kv, mul2(Pv, CR)));
     if (i & 1) {
-      kr[0][(i >> 1) & 3] = pack2(kre[0], kr0);
-      kr[1][(i >> 1) & 3] = pack2(kre[1], kr1);
+      kr[0][(i >> 1) & 3] = __byte_perm(kre, krp, 0x5410);
+      kr[1][(i >> 1) & 3] = __byte_perm(kre, krp, 0x7632);
     } else {
-      kre[0] = kr0;
-      kre[1] = kr1;
+      kre = krp;
     }
-    if ((i & 7) == 7)  // tokens r0 + i - 7 .. r0 + i of kr^T rows 2 dp, 2 dp + 1
+    if ((i & 7) == 7)  // tokens r0 + i - 7 .. r0 + i
 #pragma unroll
       for (int e = 0; e < 2; ++e)
         __stcg(reinterpret_cast<uint4*>(krt_rec + sw128_offset(2 * dp + e, r0 + (i & 8), 128)),
@@ -462,37 +488,38 @@ __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, co
   }
 }
 
-// The two products (issued by one converged warp): the diagonal halves of L and Aqk
-// (M = 128 over the stacked rows, N = 64) and the block below them (M = 64, N = 32).
+// The L/Aqk product (issued by one converged warp): the stacked [kA; qA] rows (M = 128)
+// against [cA; cB] (N = 96).  Columns 0-63 hold the diagonal halves of L and Aqk
+// (rows and columns of the same half), columns 64-95 of lanes 64-127 the block below
+// them (rows 32-63 of L and Aqk against columns 0-31).
 __device__ __forceinline__ void issue_lqk(uint32_t tmem, uint64_t d_sw128) {
   auto d = [&](uint32_t off) { return d_sw128 + (off >> 4); };
-  constexpr uint32_t idesc_d = idesc_f16kind(128, 64), idesc_o = idesc_f16kind(64, 32);
+  constexpr uint32_t idesc = idesc_f16kind(128, 96);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint32_t acc = (kb | ks) != 0;
-      umma_f16_warp(tmem + TM_DIAG, d(QK + kb * QK_KB + ks * 32), d(CA + kb * 8192 + ks * 32), idesc_d, acc);
-      umma_f16_warp(tmem + TM_OFF, d(KBQB + kb * 8192 + ks * 32), d(CB + kb * 4096 + ks * 32), idesc_o, acc);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      umma_f16_warp(tmem + TM_LQ, d(QK + kb * QK_KB + ks * 32), d(CC + kb * CC_KB + ks * 32), idesc, (kb | ks) != 0);
 }
 
-// Readout by the 8 warps of a producer (quad = TMEM lane quadrant, cpart = which 16
-// columns): M = strict_tril(Diag(beta) L) as fp32 into MB (the upper-right 32 x 32 block
-// is not written: the inverse never reads it as M) and Aqk = tril(qd ki^T) as the bf16
-// SW128 tile AQK_STG (every element written).
+// Readout by the 8 warps of a producer (quad = TMEM lane quadrant = which 32 stacked
+// rows, cpart = which 16 columns): M = strict_tril(Diag(beta) L) as fp32 into MB (the
+// upper-right 32 x 32 block is not written: the inverse never reads it as M) and
+// Aqk = tril(qd ki^T) as the bf16 SW128 tile AQK_STG (every element written).
 __device__ __forceinline__ void readout_lqk(uint8_t* base, uint32_t tmem, const float* beta_s, int quad, int cpart,
                                             int lane) {
   float* mb = reinterpret_cast<float*>(base + MB);
   uint8_t* aq = base + AQK_STG;
   const int half = quad >> 1;
+  const int i = 32 * half + lane;         // row of L (quad 0, 2) or Aqk (quad 1, 3)
   const int c0 = 32 * half + 16 * cpart;  // diagonal-half columns of this warp
   float dv[16], ov[16];
-  tmem_ld16(tmem_addr(tmem, 32 * quad, TM_DIAG + c0), dv);
-  tmem_ld16(tmem_addr(tmem, 32 * quad, TM_OFF + 16 * cpart), ov);
+  tmem_ld16(tmem_addr(tmem, 32 * quad, TM_LQ + c0), dv);
+  // columns 16 cpart + [0, 16) of the block below the halves (used by quadrants 2 and 3; the
+  // load is unconditional, which keeps the compiler's register allocation simple)
+  tmem_ld16(tmem_addr(tmem, 32 * quad, TM_LQ + 64 + 16 * cpart), ov);
   tmem_ld_wait();
-  const int i = 32 * half + lane;  // row of the diagonal half
-  if ((quad & 1) == 0) {           // L
+  if ((quad & 1) == 0) {  // L
     const float bi = beta_s[i];
 #pragma unroll
     for (int j4 = 0; j4 < 4; ++j4) {
@@ -504,6 +531,11 @@ __device__ __forceinline__ void readout_lqk(uint8_t* base, uint32_t tmem, const 
       v4.w = (c + 3 < i) ? bi * dv[4 * j4 + 3] : 0.f;
       *reinterpret_cast<float4*>(mb + i * MB_LD + c) = v4;
     }
+    if (half)  // the block below the halves: no mask
+#pragma unroll
+      for (int j4 = 0; j4 < 4; ++j4)
+        *reinterpret_cast<float4*>(mb + i * MB_LD + 16 * cpart + 4 * j4) =
+            make_float4(bi * ov[4 * j4], bi * ov[4 * j4 + 1], bi * ov[4 * j4 + 2], bi * ov[4 * j4 + 3]);
   } else {  // Aqk (diagonal kept)
 #pragma unroll
     for (int h8 = 0; h8 < 2; ++h8) {
@@ -515,25 +547,14 @@ __device__ __forceinline__ void readout_lqk(uint8_t* base, uint32_t tmem, const 
       }
       st_v4(aq + sw128_offset(i, c0 + 8 * h8, 64), w[0], w[1], w[2], w[3]);
     }
-    if (half == 0)  // Aqk rows 0-31, columns 32-63: zero
 #pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) st_v4(aq + sw128_offset(i, 32 + 16 * cpart + 8 * h8, 64), 0u, 0u, 0u, 0u);
-  }
-  if (lane < 16) {  // the block below the diagonal halves: rows 32-63, columns 0-31, no mask
-    const int io = 32 + 16 * (quad & 1) + lane;
-    const int cc = 16 * cpart;
-    if (half == 0) {  // L
-      const float bi = beta_s[io];
-#pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4)
-        *reinterpret_cast<float4*>(mb + io * MB_LD + cc + 4 * j4) =
-            make_float4(bi * ov[4 * j4], bi * ov[4 * j4 + 1], bi * ov[4 * j4 + 2], bi * ov[4 * j4 + 3]);
-    } else {  // Aqk
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8)
-        st_v4(aq + sw128_offset(io, cc + 8 * h8, 64), pack2(ov[8 * h8], ov[8 * h8 + 1]),
+    for (int h8 = 0; h8 < 2; ++h8) {
+      if (half)  // rows 32-63, columns 0-31: the block below the halves
+        st_v4(aq + sw128_offset(i, 16 * cpart + 8 * h8, 64), pack2(ov[8 * h8], ov[8 * h8 + 1]),
               pack2(ov[8 * h8 + 2], ov[8 * h8 + 3]), pack2(ov[8 * h8 + 4], ov[8 * h8 + 5]),
               pack2(ov[8 * h8 + 6], ov[8 * h8 + 7]));
+      else  // rows 0-31, columns 32-63: zero
+        st_v4(aq + sw128_offset(i, 32 + 16 * cpart + 8 * h8, 64), 0u, 0u, 0u, 0u);
     }
   }
 }
@@ -617,7 +638,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     mbar_init(&bars[B_ACK], NSLICE);
     mbar_init(&bars[B_ACK + 1], NSLICE);
     mbar_init(&bars[B_RAW], 1);
-    mbar_init(&bars[B_RAWV], 1);
     mbar_init(&bars[B_PMMA], 1);
     mbar_init(&bars[B_A], 1);
     mbar_init(&bars[B_B], 1);
@@ -662,8 +682,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     const uint64_t D_KD_MN = sdesc(sbase + OFF_PREP + prep::KDT, 8192, 1024, 2);  // kd as MN-major B
     const uint64_t D_V_MN = sdesc(sbase + OFF_PREP + prep::VRAW, 8192, 1024, 2);  // v as MN-major B
     uint32_t pmma_phase = 0, pmma_issued = 0;
-    bool raw_pending = false, v_pending = false;
-    int raw_pending_j = 0, v_pending_j = 0;
+    bool raw_pending = false;
+    int raw_pending_j = 0;
     bool failed = false, range_bad = false;
     auto timeout = [&]() {
       failed = true;
@@ -671,8 +691,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     };
     PROF_DECL
 
-    auto issue_raw = [&](int m, int j) {  // elected: TMA q, k tiles of chunk m (own chunk j)
-      prep::issue_qk(pb, &maps.q32, &maps.k32, &bars[B_RAW], hk, static_cast<int>(tok0) + m * C);
+    auto issue_raw = [&](int m, int j) {  // elected: TMA q, k, v tiles of chunk m (own chunk j)
+      prep::issue_raw(pb, &maps.q32, &maps.k32, &maps.v, &bars[B_RAW], hk, hv, static_cast<int>(tok0) + m * C);
       raw_pending = true;
       raw_pending_j = j;
     };
@@ -722,7 +742,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
       const int rows = min(C, len - m * C);
       const bool next = m + NSLICE < NT;
-      // ---- 1. raw q, k of chunk m ----
+      // ---- 1. raw q, k, v of chunk m ----
       if (!mbar_wait(&bars[B_RAW], j & 1, p.wait_ns)) timeout();
       if (pt == 0) bulk_wait_read();  // the previous record's Aqk, W and U stagings have been read
       if (pt < C) beta_s[pt] = bpre;
@@ -743,8 +763,8 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       //         record (a slot is rewritten only after its previous record was loaded
       //         everywhere: publish() of the record two before waited for that) ----
       {
-        prep::elementwise(pb, gsum, gpre, dp, hq, rows, scale, gs + R_WQ + R_QD_IN_KB, R_W_KB, gs + R_KRT,
-                          reinterpret_cast<float*>(gs + G_GAM), range_bad);
+        prep::elementwise<false>(pb, gsum, gpre, dp, hq, rows, scale, gs + R_WQ + R_QD_IN_KB, R_W_KB, gs + R_KRT,
+                                 reinterpret_cast<float*>(gs + G_GAM), range_bad);
       }
       fence_proxy_async_global();  // the record's plain stores, read by the chains' bulk copies
       if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's W/U stores have landed
@@ -774,12 +794,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       tc_fence_after();
       PROF(2);
 
-      // ---- 4. raw v into the [kB; qB] tiles (read by now); TMEM -> M (fp32), Aqk ----
-      if (pt == 0 && !failed) {
-        prep::issue_v(pb, &maps.v, &bars[B_RAWV], hv, static_cast<int>(tok0) + m * C);
-        v_pending = true;
-        v_pending_j = j;
-      }
+      // ---- 4. TMEM -> M (fp32), Aqk ----
       prep::readout_lqk(pb, tmem, beta_s, quad, cpart, lane);
       tc_fence_before();
       fence_proxy_async_smem();
@@ -802,16 +817,13 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (warp < 3)
         inverse_block_columns(reinterpret_cast<float*>(pb + prep::MB), beta_s, pb + prep::AMAT, warp, lane);
       PROF(5);
+      if (pt == 0) bulk_wait_read();  // the Aqk staging has been read: its buffer takes U next
       fence_proxy_async_smem();
       role_sync(NB_PREP, NPROD);
       PROF(6);
 
       // ---- 6. W = A kd, U = A v (kd and v as MN-major B operands) ----
       if (pt == 0) {
-        if (v_pending) {
-          if (!mbar_wait(&bars[B_RAWV], j & 1, p.wait_ns)) timeout();
-          v_pending = false;
-        }
         if (!failed) {
           tc_fence_after();
           constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
@@ -830,11 +842,11 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (mbar_wait(&bars[B_PMMA], pmma_phase & 1, p.wait_ns)) ++pmma_phase;  // else still in flight: drained below
       else timeout();
       tc_fence_after();
-      // the stacked tile (M and A by now) is free again: fetch the next own chunk
+      // the stacked tile (M and A by now) and v are free again: fetch the next own chunk
       if (pt == 0 && next && !failed) issue_raw(m + NSLICE, j + 1);
       PROF(7);
 
-      // ---- 7. W -> staging over kd (bf16 SW128), U -> staging over v (4 slices of [64 x 32] bf16) ----
+      // ---- 7. W -> staging over kd (bf16 SW128), U -> staging over cA (4 slices of [64 x 32] bf16) ----
       __syncwarp();
       {
         const int i = 16 * quad + (lane & 15);
@@ -896,7 +908,6 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     // drain after an abort: copies and MMAs this role issued must finish first
     if (pt == 0) {
       if (raw_pending && !mbar_wait(&bars[B_RAW], raw_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
-      if (v_pending && !mbar_wait(&bars[B_RAWV], v_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
       if (pmma_issued > pmma_phase && !mbar_wait(&bars[B_PMMA], (pmma_issued - 1) & 1, DRAIN_LIMIT_NS))
         atomicOr(p.status, kStatusTimeout);
       bulk_wait_all();
@@ -1211,7 +1222,7 @@ constexpr uint32_t REC_BYTES = SR_U + 16384;  // 74,752 B
 static_assert(REC_BYTES <= GSLOT, "record fits a ring slot");
 // producer pipeline region (offsets from the region base, 1024-aligned): the prep:: tiles,
 // then beta, the quarter sums of g, barriers and the ring-slot flag
-constexpr uint32_t P_BETA = prep::BYTES, P_GSUM = P_BETA + 256, P_BAR = P_GSUM + 2048, P_STRIDE = 93184;
+constexpr uint32_t P_BETA = prep::QDS + 16384, P_GSUM = P_BETA + 256, P_BAR = P_GSUM + 2048, P_STRIDE = 109568;
 static_assert(P_BAR + 64 <= P_STRIDE && P_STRIDE % 1024 == 0, "producer pipeline region");
 // chain region
 // chain region: record part A ([qd; W], e^{g_last}) in three buffers, part B (kr^T, Aqk,
@@ -1223,13 +1234,15 @@ constexpr uint32_t C_PB = C_PA + 3 * PA_STRIDE;
 constexpr uint32_t C_STG = C_PB + 2 * PB_STRIDE;  // two 16 KB o staging tiles ([token][v], two 64-column halves)
 constexpr uint32_t C_BAR = C_STG + 2 * 16384;
 constexpr uint32_t C_MISC = C_BAR + 128;       // tmem base
-constexpr uint32_t SMEM_BYTES = C_MISC + 448;        // tmem base; profile stamps at C_MISC + 64
+// the TMEM base address lives past both roles' regions (chain profile stamps at C_MISC + 64)
+constexpr uint32_t TMEM_SLOT = (2 * P_STRIDE > C_MISC + 448 ? 2 * P_STRIDE : C_MISC + 448);
+constexpr uint32_t SMEM_BYTES = TMEM_SLOT + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
-static_assert(2 * P_STRIDE <= C_MISC, "producer regions stay below the tmem slot");
+static_assert(SMEM_ALLOC <= 232448, "split kernel shared memory");
 static_assert(PA_STRIDE >= REC_A_BYTES && PA_STRIDE % 1024 == 0 && PB_STRIDE % 1024 == 0 && C_PB % 1024 == 0,
               "record buffers keep the 1 KB alignment of the swizzled operands");
 constexpr int CB_FULL = 0, CB_B = 3;  // chain barriers (CB_FULL: [3], one per part-A buffer)
-constexpr int PB_RAW = 0, PB_PMMA = 1, PB_RAWV = 2;        // producer barriers (per pipeline)
+constexpr int PB_RAW = 0, PB_PMMA = 1;                     // producer barriers (per pipeline)
 constexpr uint32_t P_SLOT_FREE = P_BAR + 32;               // shared flag: the record's ring slot may be written
 constexpr uint32_t NB_CHAIN_ALL = 3;
 
@@ -1301,8 +1314,8 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
   const int HV = p.HV;
   const float scale = p.scale;
   uint32_t pmma_phase = 0, pmma_issued = 0;
-  bool raw_pending = false, v_pending = false;
-  int raw_pending_j = 0, v_pending_j = 0;
+  bool raw_pending = false;
+  int raw_pending_j = 0;
   bool failed = false, range_bad = false;
   auto timeout = [&]() {
     failed = true;
@@ -1313,7 +1326,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 #endif
   };
   auto issue_raw = [&](const Rec& x, int jj) {  // elected
-    prep::issue_qk(sm, &maps.q32, &maps.k32, &bars[PB_RAW], x.hk, static_cast<int>(x.tok0) + x.m * C);
+    prep::issue_raw(sm, &maps.q32, &maps.k32, &maps.v, &bars[PB_RAW], x.hk, x.hv, static_cast<int>(x.tok0) + x.m * C);
     raw_pending = true;
     raw_pending_j = jj;
   };
@@ -1362,12 +1375,12 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     const bool next = rn < NREC;
     uint8_t* gs = p.ring + (static_cast<size_t>(cur.u) * RING + (cur.m % SRING)) * GSLOT;
     const int rows = min(C, cur.len - cur.m * C);
-    // ---- 1. raw q, k tiles; is the ring slot known to be free (its previous record
+    // ---- 1. raw q, k, v tiles; is the ring slot known to be free (its previous record
     //         loaded by the chain, as the counter read ahead shows)? ----
     PSTAMP(0);
     if (!mbar_wait(&bars[PB_RAW], j & 1, p.wait_ns)) timeout();
     PSTAMP(1);
-    if (pt == 0) bulk_wait_read();  // the previous record's Aqk, W and U stagings have been read
+    if (pt == 0 || pt == kRecStorer) bulk_wait_read();  // the previous record's stagings have been read
     if (pt < C) beta_s[pt] = bpre;
     {
       float2 qsum = make_float2(0.f, 0.f);
@@ -1387,7 +1400,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       // Not known: publish this pipeline's previous record first (a chain may be waiting
       // for it, and the ring must never hold a record behind a wait on the chains), then
       // wait for the slot.
-      if (pt == 0 && pub_pending) bulk_wait_group<0>();
+      if ((pt == 0 || pt == kRecStorer) && pub_pending) bulk_wait_group<0>();
       role_sync(NB, PIPE);
       if (pub_pending) {
         if (pw == 3 && lane == 0) publish(pub_m, pub_u);
@@ -1399,11 +1412,11 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 
     // ---- 2. elementwise: operand tiles; qd, kr^T and e^{g_last} straight into the record ----
     {
-      prep::elementwise(sm, gsum, gpre, dp, hq, rows, scale, gs + SR_QW, SR_KB, gs + SR_KRT,
-                        reinterpret_cast<float*>(gs + SR_GAM), range_bad);
+      prep::elementwise<true>(sm, gsum, gpre, dp, hq, rows, scale, gs + SR_QW, SR_KB, gs + SR_KRT,
+                              reinterpret_cast<float*>(gs + SR_GAM), range_bad);
     }
     fence_proxy_async_global();  // the record's plain stores, read by the chain's bulk copies
-    if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's stores have landed
+    if ((pt == 0 || pt == kRecStorer) && pub_pending) bulk_wait_group<0>();  // the previous record's stores have landed
     fence_proxy_async_smem();
     PSTAMP(3);
     role_sync(NB, PIPE);
@@ -1411,6 +1424,11 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     if (pub_pending) {  // from warp 3 of the pipeline while warp 0 issues the MMAs
       if (pw == 3 && lane == 0) publish(pub_m, pub_u);
       pub_pending = false;
+    }
+    if (pt == kRecStorer) {  // qd to the record
+      bulk_store(gs + SR_QW, sm + prep::QDS, 8192);
+      bulk_store(gs + SR_QW + SR_KB, sm + prep::QDS + 8192, 8192);
+      bulk_commit();
     }
 
     // ---- 3. the diagonal halves and the block below them of L and Aqk ----
@@ -1428,12 +1446,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     tc_fence_after();
     PSTAMP(6);
 
-    // ---- 4. raw v into the [kB; qB] tiles (read by now); TMEM -> M (fp32), Aqk ----
-    if (pt == 0 && !failed) {
-      prep::issue_v(sm, &maps.v, &bars[PB_RAWV], cur.hv, static_cast<int>(cur.tok0) + cur.m * C);
-      v_pending = true;
-      v_pending_j = j;
-    }
+    // ---- 4. TMEM -> M (fp32), Aqk ----
     prep::readout_lqk(sm, tmem, beta_s, quad, cpart, lane);
     tc_fence_before();
     fence_proxy_async_smem();
@@ -1453,21 +1466,15 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     PSTAMP(10);
     if (next) prefetch_gb(nx, 2);
     if (pw < 3) inverse_block_columns(reinterpret_cast<float*>(sm + prep::MB), beta_s, sm + prep::AMAT, pw, lane);
+    if (pt == 0) bulk_wait_read();  // the Aqk staging has been read: its buffer takes U^T next
     fence_proxy_async_smem();
     PSTAMP(11);
     role_sync(NB, PIPE);
     PSTAMP(12);
 
     // ---- 6. W = A kd (M = 64, kd as MN-major B) and U^T = v^T A^T (M = 128 value
-    //         columns, v as MN-major A, A as K-major B); v was issued in step 4, so
-    //         (every thread having passed that step's barrier) it is in flight ----
+    //         columns, v as MN-major A, A as K-major B) ----
     if (pw == 0) {
-      if (mbar_wait(&bars[PB_RAWV], j & 1, p.wait_ns)) {
-        if (pt == 0) v_pending = false;
-      } else {
-        timeout();
-      }
-      __syncwarp();
       if (!__any_sync(0xFFFFFFFFu, failed)) {
         tc_fence_after();
         constexpr uint32_t idesc_w = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
@@ -1494,10 +1501,10 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     else timeout();
     tc_fence_after();
     PSTAMP(14);
-    // the stacked tile (M and A by now) is free again: fetch the next record's q, k
+    // the stacked tile (M and A by now) and v are free again: fetch the next record's tiles
     if (pt == 0 && next && !failed) issue_raw(nx, j + 1);
 
-    // ---- 7. W -> staging over kd (bf16 SW128, warps 0-3), U^T -> staging over v (warps
+    // ---- 7. W -> staging over kd (bf16 SW128, warps 0-3), U^T -> staging over cA (warps
     //         4-7: row v of 64 tokens, 128-byte-swizzled) ----
     __syncwarp();
     if (cpart == 0) {
@@ -1551,6 +1558,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       bulk_commit();
       if (j == 0) bulk_wait_group<0>();
     }
+    if (pt == kRecStorer && j == 0) bulk_wait_group<0>();  // (the first record is published below)
     pub_pending = true;
     pub_m = cur.m;
     pub_u = cur.u;
@@ -1564,12 +1572,11 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     cur = nx;
   }
   if (range_bad) atomicOr(p.status, kStatusRange);
-  if (pt == 0) bulk_wait_all();
+  if (pt == 0 || pt == kRecStorer) bulk_wait_all();
   role_sync(NB, PIPE);
   if (pub_pending && pw == 3 && lane == 0 && !failed) publish(pub_m, pub_u);
   if (pt == 0) {  // drain what this pipeline issued
     if (raw_pending && !mbar_wait(&bars[PB_RAW], raw_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
-    if (v_pending && !mbar_wait(&bars[PB_RAWV], v_pending_j & 1, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
     if (pmma_issued > pmma_phase && !mbar_wait(&bars[PB_PMMA], (pmma_issued - 1) & 1, DRAIN_LIMIT_NS))
       atomicOr(p.status, kStatusTimeout);
   }
@@ -2023,7 +2030,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool is_chain = static_cast<int>(blockIdx.x) < NU;
   uint32_t* flags = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.status) + kFlagOffset);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + split::C_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + split::TMEM_SLOT);
   if (tid == 0) {
     if (is_chain) {
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
@@ -2035,7 +2042,6 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
         uint64_t* pb = reinterpret_cast<uint64_t*>(sm + pp * split::P_STRIDE + split::P_BAR);
         mbar_init(&pb[split::PB_RAW], 1);
         mbar_init(&pb[split::PB_PMMA], 1);
-        mbar_init(&pb[split::PB_RAWV], 1);
       }
       tma_prefetch_desc(&maps.q32);
       tma_prefetch_desc(&maps.k32);
