@@ -1,11 +1,13 @@
 #!/usr/bin/env python
 """Benchmark of the KDA chunked forward on one GB300 (or N, as independent replicas).
 
-One step = one kda_chunk_fwd call over the headline workload (B=1, T=4096,
-H=HV=32, K=V=128, bf16 q/k/v/o, fp32 g/beta/state), inputs resident in HBM.
+One step = one kda_chunk_fwd call over one workload, inputs resident in HBM: by
+default the headline workload (B=1, T=4096, H=HV=32, K=V=128, bf16 q/k/v/o, fp32
+g/beta/state); --workload selects another of the five (2: B=4 T=16384 with an
+initial state, 3: 16 packed sequences, 4: grouped value heads B=2 T=32768).
 Prints one JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl reference]
 
 --impl reference times the fp64 CPU oracle (the only other implementation of
 the method here) on the host cores, on a bounded sample of the same workload.
@@ -139,15 +141,15 @@ def load_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def load_traffic(kernel_name: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+def load_traffic(kernel_name: str, workload: str):
+    """Per-launch DRAM bytes of `kernel_name` on `workload` from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(kernel_name)
+    e = d.get(f"{kernel_name}@{workload}")
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
     return e.get("bytes_per_launch")
@@ -160,29 +162,45 @@ def dist_env():
     return ws, rank, local
 
 
-def cpu_baseline(x=None, units: int | None = None):
+def sample_units(x, n):
+    """n (sequence, value head) units spread over the workload: value heads in turn,
+    sequences in turn (every unit of a small workload when n covers it)."""
+    NS, HV = x.num_seqs, x.v.shape[2]
+    units = [(s, h) for s in range(NS) for h in range(HV)]
+    if n >= len(units):
+        return units
+    step = len(units) / n
+    return [units[int(i * step)] for i in range(n)]
+
+
+def unit_tokens(x, units):
+    if x.cu_seqlens is None:
+        return len(units) * x.q.shape[1]
+    cu = x.cu_seqlens.numpy()
+    return int(sum(int(cu[s + 1] - cu[s]) for s, _ in units))
+
+
+def cpu_baseline(x, units: int | None = None):
     """Time the fp64 oracle (chunked form, C = 64) on a bounded sample of the
-    headline workload: `units` value heads of the single sequence, one thread
-    per head.  Returns (tokens/s scaled to all heads, cores, sample text, s)."""
+    workload: `units` (sequence, value head) units, one thread each.  Returns
+    (tokens/s scaled so that a token counts all value heads, cores, sample text, s)."""
     import oracle
-    from kimi_delta_attention_gb300 import workloads as W
-    if x is None:
-        x = W.workload_inputs(WORKLOAD_INDEX)
     cores = os.cpu_count() or 1
-    if units is None:
-        units = min(cores, x.v.shape[2])
-    f = lambda t: t.float().numpy()
-    args = [f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta)]
-    sel = [(0, h) for h in range(units)]
-    t0 = time.perf_counter()
-    oracle.forward_units(*args, x.scale, sel, form="chunked", chunk=64, nthreads=units)
-    dt = time.perf_counter() - t0
     HV = x.v.shape[2]
-    tokens_equiv = x.tokens() * units / HV
-    sample = (f"{units} of {HV} value heads x {x.tokens()} tokens of the headline workload, "
-              f"fp64 chunked oracle (C=64), {units} threads; {dt:.2f} s wall; "
-              f"tokens/s counts a token as all {HV} heads")
-    return tokens_equiv / dt, units, sample, dt
+    if units is None:
+        units = min(cores, x.num_seqs * HV)
+    f = lambda t: None if t is None else t.float().numpy()
+    sel = sample_units(x, units)
+    t0 = time.perf_counter()
+    oracle.forward_units(f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta), x.scale, sel, initial_state=f(x.initial_state),
+                         cu_seqlens=None if x.cu_seqlens is None else x.cu_seqlens.numpy(), form="chunked", chunk=64,
+                         nthreads=units)
+    dt = time.perf_counter() - t0
+    token_heads = unit_tokens(x, sel)
+    sample = (f"{len(sel)} of {x.num_seqs * HV} (sequence, value head) units ({token_heads} token-heads) of "
+              f"{x.meta.get('workload', 'the workload')}, fp64 chunked oracle (C=64), {units} threads; "
+              f"{dt:.2f} s wall; tokens/s counts a token as all {HV} value heads")
+    return token_heads / HV / dt, units, sample, dt
 
 
 # --------------------------------------------------------------------- arms --
@@ -191,14 +209,14 @@ def run_reference(args):
     if rank != 0:
         return 0
     from kimi_delta_attention_gb300 import workloads as W
-    w = W.WORKLOADS[WORKLOAD_INDEX]
-    x = W.workload_inputs(WORKLOAD_INDEX)
+    w = W.WORKLOADS[args.workload]
+    x = W.workload_inputs(args.workload)
     vals, times = [], []
     cores = None
     sample = None
     n_steps = max(1, args.steps)
     for i in range(max(0, args.warmup) + n_steps):
-        v, cores, sample, dt = cpu_baseline(x=x)
+        v, cores, sample, dt = cpu_baseline(x)
         if i >= args.warmup:
             vals.append(v)
             times.append(dt)
@@ -207,7 +225,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": n_steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_dict(w, args.gpus),
+        "data": "synthetic", "config": config_dict(w, x, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -216,12 +234,16 @@ def run_reference(args):
     return 0
 
 
-def config_dict(w, n):
-    return {"workload": w.name, "model": None, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
-            "V": w.V, "global_batch": w.B * n, "seq_len": w.T, "chunk": 64,
-            "parallelism": f"replicas x{n} (independent problems per GPU)",
-            "l2": "flushed between timed steps (256 MiB device write outside the step events)",
-            "initial_state": "zeros (not read)", "final_state": "written"}
+def config_dict(w, x, n):
+    d = {"workload": w.name, "model": None, "B": w.B, "T": int(x.q.shape[1]), "H": w.H, "HV": w.HV, "K": w.K,
+         "V": w.V, "global_batch": x.num_seqs * n, "seq_len": w.T if not w.num_seqs else None, "chunk": 64,
+         "parallelism": f"replicas x{n} (independent problems per GPU)",
+         "l2": "flushed between timed steps (256 MiB device write outside the step events)",
+         "initial_state": "read (0.1 N(0,1))" if w.init_state else "zeros (not read)", "final_state": "written"}
+    if w.num_seqs:
+        lens = [int(v) for v in (x.cu_seqlens[1:] - x.cu_seqlens[:-1]).tolist()]
+        d.update({"num_seqs": w.num_seqs, "seq_lens": lens, "packed_tokens": int(x.q.shape[1])})
+    return d
 
 
 def run_gpu(args):
@@ -236,20 +258,22 @@ def run_gpu(args):
     from kimi_delta_attention_gb300 import workloads as W
     kda.build()
     kda.load_library()
-    w = W.WORKLOADS[WORKLOAD_INDEX]
-    host = W.workload_inputs(WORKLOAD_INDEX)
+    w = W.WORKLOADS[args.workload]
+    host = W.workload_inputs(args.workload)
     x = host.to(dev)
     B, T, H, K = x.q.shape
     HV, V = x.v.shape[2], x.v.shape[3]
+    NS = x.num_seqs
     out = torch.empty_like(x.v)
-    fin = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
-    shape = kda.make_shape(x.q, x.v)
+    fin = torch.empty((NS, HV, K, V), dtype=torch.float32, device=dev)
+    shape = kda.make_shape(x.q, x.v, x.cu_seqlens)
     wsp = torch.empty(kda.kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, x.scale, out=out, final_state=fin, workspace=wsp,
+        kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, x.scale, initial_state=x.initial_state,
+                          cu_seqlens=x.cu_seqlens, out=out, final_state=fin, workspace=wsp,
                           stream=stream.cuda_stream)
 
     for _ in range(max(3, args.warmup)):
@@ -285,29 +309,29 @@ def run_gpu(args):
         ms = float(t.item())
     status = kda.kda_read_device_status(wsp)
 
-    tokens = B * T
+    tokens = host.tokens()
     value = ws * tokens / (ms * 1e-3)
     flops = W.flops_convention(host)
     tflops = ws * flops / (ms * 1e-3) / 1e12
-    alg_bytes = W.algorithmic_bytes(host, final_state=True) - 0  # initial state not read
+    alg_bytes = W.algorithmic_bytes(host, final_state=True)  # the initial state counts only when it is read
     hbm_gbs, bf16_tf, peak_src = load_peaks()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     kernel_name = kda.kda_chunk_fwd_kernel_name(shape)  # the one launch of each step
 
     # end to end through the public API with pinned host buffers
-    e2e = e2e_measure(kda, host, dev, stream, max(3, min(args.steps, 20)))
+    e2e = e2e_measure(kda, host, dev, stream, max(3, min(args.steps, 20 if tokens <= 1 << 16 else 5)))
 
     line = {
         "impl": "kda_gb300", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w, ws), "tflops": tflops,
+        "config": config_dict(w, host, ws), "tflops": tflops,
         # the token recurrence's own arithmetic, 7 K V flop per token and value head: a
         # lower bound on any evaluation, reported beside the chunked convention
         "tflops_recurrent_lower_bound": ws * tokens * HV * 7 * K * V / (ms * 1e-3) / 1e12,
         "roofline_time_ms": max(alg_bytes / (hbm_gbs * 1e9), flops / (bf16_tf * 1e12)) * 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": load_traffic(kernel_name),
+                     "frac": achieved / hbm_gbs, "traffic": load_traffic(kernel_name, w.name),
                      "kernel": kernel_name, "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
@@ -315,7 +339,7 @@ def run_gpu(args):
         "device_status": status, "wall_s_timed_region": t_wall,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, cores, sample, _ = cpu_baseline(x=host)
+        v, cores, sample, _ = cpu_baseline(host)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -327,38 +351,44 @@ def run_gpu(args):
 
 def e2e_measure(kda, host, dev, stream, steps):
     """Same metric through kda_chunk_fwd with host buffers: every step copies the
-    inputs from pinned host memory to the device, runs the forward and copies o
-    and the final state back.  Steps alternate between two streams with their own
-    device buffers and workspaces, so that one step's copies overlap the previous
-    step's forward; each stream keeps its own steps in order.  (Splitting a step's
-    input copies over several streams did not raise the host-to-device rate, ~195 GB/s.)"""
+    inputs (and the initial state and cu_seqlens when the workload has them) from
+    pinned host memory to the device, runs the forward and copies o and the final
+    state back.  Steps alternate between two streams with their own device buffers
+    and workspaces, so that one step's copies overlap the previous step's forward;
+    each stream keeps its own steps in order.  (Splitting a step's input copies over
+    several streams did not raise the host-to-device rate, ~195 GB/s.)"""
     import torch
-    pin = lambda t: t.pin_memory()
-    hq, hk, hv, hg, hb = (pin(t) for t in (host.q, host.k, host.v, host.g, host.beta))
+    pin = lambda t: None if t is None else t.pin_memory()
+    names = ("q", "k", "v", "g", "b", "s0", "cu")
+    hsrc = dict(zip(names, (pin(t) for t in (host.q, host.k, host.v, host.g, host.beta, host.initial_state,
+                                              host.cu_seqlens))))
     B, T, H, K = host.q.shape
     HV, V = host.v.shape[2], host.v.shape[3]
-    shape = kda.make_shape(hq, hv)
+    NS = host.num_seqs
+    shape = kda.make_shape(hsrc["q"], hsrc["v"], hsrc["cu"])
     wsz = kda.kda_chunk_fwd_workspace_size(shape)
     streams = [stream, torch.cuda.Stream(dev)]
     bufs = []
     for _ in range(2):
-        d = {n: torch.empty_like(t, device=dev) for n, t in (("q", hq), ("k", hk), ("v", hv), ("g", hg), ("b", hb))}
+        d = {n: (None if t is None else torch.empty_like(t, device=dev)) for n, t in hsrc.items()}
         d["o"] = torch.empty_like(d["v"])
-        d["s"] = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
+        d["s"] = torch.empty((NS, HV, K, V), dtype=torch.float32, device=dev)
         d["ws"] = torch.empty(wsz, dtype=torch.uint8, device=dev)
         d["ho"] = torch.empty(host.v.shape, dtype=host.v.dtype).pin_memory()
-        d["hs"] = torch.empty((B, HV, K, V), dtype=torch.float32).pin_memory()
+        d["hs"] = torch.empty((NS, HV, K, V), dtype=torch.float32).pin_memory()
         bufs.append(d)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+    h2d = sum(t.numel() * t.element_size() for t in hsrc.values() if t is not None)
     d2h = bufs[0]["ho"].numel() * bufs[0]["ho"].element_size() + bufs[0]["hs"].numel() * 4
 
     def step(i):
         d, st = bufs[i & 1], streams[i & 1]
         with torch.cuda.stream(st):
-            for n, h in (("q", hq), ("k", hk), ("v", hv), ("g", hg), ("b", hb)):
-                d[n].copy_(h, non_blocking=True)
-            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], host.scale, out=d["o"], final_state=d["s"],
-                              workspace=d["ws"], stream=st.cuda_stream)
+            for n, h in hsrc.items():
+                if h is not None:
+                    d[n].copy_(h, non_blocking=True)
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], host.scale, initial_state=d["s0"],
+                              cu_seqlens=d["cu"], out=d["o"], final_state=d["s"], workspace=d["ws"],
+                              stream=st.cuda_stream)
             d["ho"].copy_(d["o"], non_blocking=True)
             d["hs"].copy_(d["s"], non_blocking=True)
 
@@ -375,7 +405,7 @@ def e2e_measure(kda, host, dev, stream, steps):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     status = max(kda.kda_read_device_status(d["ws"]) for d in bufs)
-    return {"value": B * T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    return {"value": host.tokens() / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
             "overlap": "two streams, double-buffered: a step's copies overlap the previous step's forward",
             "device_status": status}
@@ -388,6 +418,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kda_gb300", choices=["kda_gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
+                    help="workload index (0-4); 1, the headline, is the default bench line")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
