@@ -411,6 +411,66 @@ def e2e_measure(kda, host, dev, stream, steps):
             "device_status": status}
 
 
+DECODE_METRIC = "KDA decode step (recurrent, state in place) tokens/s on 1 GB300 (B=128, T=1, H=HV=32, K=V=128); % roofline"
+
+
+def run_decode(args):
+    """One step = one kda_decode call: one new token for each of 128 sequences x 32
+    value heads against fp32 states (537 MB read and written per step, more than L2).
+    HBM-bound on the state."""
+    import torch
+    import kimi_delta_attention_gb300 as kda
+    from kimi_delta_attention_gb300 import workloads as W
+    kda.build()
+    kda.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, T, H, HV, K, V = 128, 1, 32, 32, 128, 128
+    host = W.make_inputs(B, T, H, HV, K, V, "bf16", seed=11, init_state=True)
+    x = host.to(dev)
+    state = x.initial_state.clone()
+    out = torch.empty_like(x.v)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.kda_decode(x.q, x.k, x.v, x.g, x.beta, state, x.scale, out=out, stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    el = lambda t: t.numel() * t.element_size()
+    alg = 2 * el(x.initial_state) + el(x.q) + el(x.k) + el(x.v) + el(x.g) + el(x.beta) + el(out)
+    hbm_gbs, _, peak_src = load_peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "kda_gb300", "metric": DECODE_METRIC, "value": B * T / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "decode_B128_T1_H32_K128", "B": B, "T": T, "H": H, "HV": HV, "K": K, "V": V,
+                   "io": "bf16 q/k/v/o, fp32 g/beta/state", "l2": "flushed between timed steps; the state "
+                   "(537 MB) is larger than L2 anyway"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": None, "kernel": "decode_kernel",
+                     "algorithmic_bytes_per_launch": alg, "peak_source": peak_src},
+        "clocks": sampler.summary(), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -418,11 +478,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kda_gb300", choices=["kda_gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="forward", choices=["forward", "decode"],
+                    help="decode: time kda_decode (one token per sequence) instead of the chunked forward")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (0-4); 1, the headline, is the default bench line")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "decode":
+        return run_decode(args)
     return run_gpu(args)
 
 

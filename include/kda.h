@@ -131,6 +131,27 @@ KDA_API kda_status kda_recurrent_fwd(const kda_shape* shape, const void* q, cons
                              float* final_state, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/*
+ * Recurrent step for inference: T (typically 1) new tokens of each of B sequences
+ * against their resident states, which are updated in place.  The same recurrence
+ * as kda_chunk_fwd (page "手撕KDA", section "1 Naive"; its section 5 validates the
+ * chunked kernels against this recurrent form), evaluated token by token on CUDA
+ * cores in fp32 with the state held in registers for the call's tokens:
+ *
+ *   q, k    [B, T, H, K]   io_dtype          v  [B, T, HV, V]  io_dtype
+ *   g       [B, T, HV, K]  fp32              beta [B, T, HV]   fp32
+ *   state   [B, HV, K, V]  fp32, required: read, then overwritten with the state
+ *           after the T tokens (must not overlap any other argument)
+ *   out     [B, T, HV, V]  io_dtype
+ * shape->num_seqs must be 0 (no packing: every sequence advances by T tokens);
+ * K and V in {64, 128}.  No workspace, no device-side status: every check is on
+ * the host.  At T = 1 and K = V = 128 a call moves 128 KiB of state per
+ * (sequence, value head) and is bound by HBM bandwidth.
+ */
+KDA_API kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, float scale, float* state, void* out,
+                              void* stream);
+
 /* Bytes of device workspace kda_chunk_fwd needs for `shape` (>= 256; also
  * enough for kda_recurrent_fwd).  Depends on the number of sequences and value
  * heads, not on T. */

@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     kda_chunk_fwd_workspace_size,
     kda_chunk_size,
     kda_chunk_fwd_kernel_name,
+    kda_decode,
     kda_read_device_status,
     kda_recurrent_fwd,
     kda_status_string,

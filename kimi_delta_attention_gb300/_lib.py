@@ -31,7 +31,7 @@ STATIC_SCRATCH_MAX_UNITS = 32
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
            "kda_read_device_status", "kda_status_string", "kda_chunk_size",
-           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch")
+           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode")
 
 
 class KdaError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_chunk_fwd_static_scratch.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, P, P,
                                                      ctypes.POINTER(ctypes.c_void_p)]
         lib.kda_chunk_fwd_static_scratch.restype = I
+        lib.kda_decode.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P]
+        lib.kda_decode.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -227,3 +229,23 @@ def kda_chunk_fwd_static_scratch(q, k, v, g, beta, scale=None, initial_state=Non
             ctypes.byref(status))
         _check(code)
     return out, final_state, status.value
+
+
+def kda_decode(q, k, v, g, beta, state, scale=None, out=None, stream=None):
+    """Recurrent step for inference: q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV,K] fp32;
+    beta [B,T,HV] fp32; state [B,HV,K,V] fp32, updated in place.  Returns o [B,T,HV,V]."""
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, (("state", state), ("out", out)))
+    if state is None or not state.is_contiguous() or state.dtype != torch.float32:
+        raise KdaError(1, "state must be a contiguous fp32 CUDA tensor")
+    with torch.cuda.device(q.device):
+        shape = make_shape(q, v)
+        if scale is None:
+            scale = q.shape[3] ** -0.5
+        if out is None:
+            out = torch.empty_like(v)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device).cuda_stream
+        _check(lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                              ctypes.c_float(scale), _ptr(state), _ptr(out), ctypes.c_void_p(stream)))
+    return out

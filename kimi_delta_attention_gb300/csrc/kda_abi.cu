@@ -15,6 +15,9 @@ bool chunk_tc_supported(const FwdParams& p, bool bf16);
 size_t chunk_tc_ring_bytes(int num_seqs, int HV);
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
 const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units);
+cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                          float* state, void* out, float scale, int B, int T, int H, int HV, int K, int V,
+                          bool bf16, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -211,6 +214,37 @@ const char* kda_chunk_fwd_kernel_name(const kda_shape* s) {
   const long tokens = s->num_seqs > 0 ? static_cast<long>(s->T) : static_cast<long>(s->B) * s->T;
   if (ns * s->HV > (1L << 30)) return "none";
   return kda::chunk_kernel_name(s->io_dtype == KDA_BF16, s->K, s->V, tokens, static_cast<int>(ns * s->HV));
+}
+
+kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, float* state, void* out, void* stream) {
+  if (!s) return KDA_ERR_INVALID_ARG;
+  if (s->B < 0 || s->T < 0 || s->H < 1 || s->HV < 1 || s->K < 1 || s->V < 1 || s->num_seqs != 0)
+    return KDA_ERR_INVALID_ARG;
+  if (s->HV % s->H != 0) return KDA_ERR_INVALID_ARG;
+  if (s->io_dtype != KDA_F32 && s->io_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+  if ((s->K != 64 && s->K != 128) || (s->V != 64 && s->V != 128)) return KDA_ERR_UNSUPPORTED;
+  const size_t B = static_cast<size_t>(s->B), tokens = B * s->T;
+  const size_t es = s->io_dtype == KDA_BF16 ? 2 : 4;
+  const size_t n_qk = tokens * s->H * s->K * es, n_v = tokens * s->HV * s->V * es;
+  const size_t n_g = tokens * s->HV * s->K * 4, n_b = tokens * s->HV * 4;
+  const size_t n_s = B * s->HV * s->K * s->V * 4;
+  if (B == 0) return KDA_OK;
+  if (!state) return KDA_ERR_INVALID_ARG;
+  if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  const void* ptrs16[] = {q, k, v, g, out, state};
+  for (const void* ptr : ptrs16)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  if (beta && !aligned(beta, 4)) return KDA_ERR_ALIGNMENT;
+  const void* ins[] = {q, k, v, g, beta};
+  const size_t nins[] = {n_qk, n_qk, n_v, n_g, n_b};
+  for (int i = 0; i < 5; ++i)
+    if (overlaps(out, n_v, ins[i], nins[i]) || overlaps(state, n_s, ins[i], nins[i])) return KDA_ERR_INVALID_ARG;
+  if (overlaps(state, n_s, out, n_v)) return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, scale, s->B, s->T, s->H, s->HV, s->K,
+                                           s->V, s->io_dtype == KDA_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_chunk_fwd_static_scratch(const kda_shape* shape, const void* q, const void* k, const void* v,

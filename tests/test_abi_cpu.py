@@ -116,3 +116,22 @@ def test_binding_refuses_host_tensors(lib):
         with pytest.raises(_lib.KdaError):
             fn(x.q, x.k, x.v, x.g, x.beta, x.scale)
     assert not x.q.is_cuda and isinstance(x.q, torch.Tensor)
+
+
+def test_decode_validation_on_host(lib):
+    """kda_decode rejects bad arguments before touching CUDA (fake, never-dereferenced pointers)."""
+    P = ctypes.c_void_p
+    f = [P(0x200000 * (i + 1)) for i in range(7)]
+    sc = ctypes.c_float(0.088)
+
+    def call(shape, state=f[5], out=f[6]):
+        return lib.kda_decode(ctypes.byref(shape), f[0], f[1], f[2], f[3], f[4], sc, state, out, None)
+
+    ok = _lib.KdaShape(2, 1, 2, 4, 128, 128, 0, _lib.KDA_BF16)
+    assert call(ok, state=None) == 1                                               # state is required
+    assert call(_lib.KdaShape(1, 1, 2, 4, 128, 128, 1, _lib.KDA_BF16)) == 1         # no packed sequences
+    assert call(_lib.KdaShape(2, 1, 3, 4, 128, 128, 0, _lib.KDA_BF16)) == 1         # HV % H != 0
+    assert call(_lib.KdaShape(2, 1, 2, 4, 96, 128, 0, _lib.KDA_BF16)) == 2          # K not compiled
+    assert call(ok, state=P(0x200000 * 6 + 4)) == 3                                # misaligned state
+    assert call(ok, out=f[5]) == 1                                                 # out aliases the state
+    assert call(_lib.KdaShape(0, 1, 2, 4, 128, 128, 0, _lib.KDA_BF16)) == 0         # no sequences: nothing to do
