@@ -17,6 +17,11 @@ Forms
     section "1 Naive").
 ``chunked``: the chunked WY/UT evaluation in the order of that listing, for
     any chunk size.
+``prestage`` / ``forward_gated``: the activations applied to raw projections
+    before the forward (q/k L2 normalisation with eps 1e-6, the bounded gate
+    lower_bound * sigmoid(exp(A_log) (g_raw + dt_bias)) or the softplus gate
+    -exp(A_log) softplus(g_raw + dt_bias), beta = sigmoid(beta_raw)); page
+    "手撕KDA", sections 2 and 5, and page "KDA源码剖析之FlashKDA（上）", part 7.
 
 Parity status: pinned by the ``-m "not gpu"`` tests in tests/test_oracle_pins.py
 (brute-force Kronecker transition, closed forms, textbook delta rule,
@@ -66,6 +71,9 @@ def _load():
             lib.kda_oracle_run.restype = ctypes.c_int
             lib.kda_oracle_tri_inverse.argtypes = [ctypes.c_int, P, P]
             lib.kda_oracle_tri_inverse.restype = None
+            lib.kda_oracle_prestage.argtypes = [ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                P, P, P, P, P, P, ctypes.c_int, ctypes.c_double, P, P, P, P]
+            lib.kda_oracle_prestage.restype = None
             _lib = lib
     return _lib
 
@@ -155,3 +163,34 @@ def forward(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
         o[t0:t0 + L, h, :] = ou
         S[s, h] = su
     return o.reshape(B, T, HV, V), S
+
+
+GATES = {"bounded": 0, "softplus": 1}
+
+
+def prestage(q_raw, k_raw, g_raw, beta_raw, A_log, dt_bias, gate: str = "bounded", lower_bound: float = -5.0):
+    """The forward's inputs from raw projections, in fp64 (see kda_oracle_prestage).
+    q_raw, k_raw [B, T, H, K]; g_raw [B, T, HV, K]; beta_raw [B, T, HV]; A_log [HV];
+    dt_bias [HV, K].  Returns (q, k, g, beta) as float64 arrays of the same shapes."""
+    q_raw, k_raw, g_raw, beta_raw, A_log, dt_bias = (_f32(x) for x in (q_raw, k_raw, g_raw, beta_raw, A_log, dt_bias))
+    B, T, H, K = q_raw.shape
+    HV = g_raw.shape[2]
+    n = B * T
+    q = np.zeros(q_raw.shape, dtype=np.float64)
+    k = np.zeros(k_raw.shape, dtype=np.float64)
+    g = np.zeros(g_raw.shape, dtype=np.float64)
+    beta = np.zeros(beta_raw.shape, dtype=np.float64)
+    _load().kda_oracle_prestage(n, H, HV, K, _ptr(q_raw), _ptr(k_raw), _ptr(g_raw), _ptr(beta_raw), _ptr(A_log),
+                                _ptr(dt_bias), GATES[gate], float(lower_bound), _ptr(q), _ptr(k), _ptr(g), _ptr(beta))
+    return q, k, g, beta
+
+
+def forward_gated(q_raw, k_raw, v, g_raw, beta_raw, A_log, dt_bias, scale, gate: str = "bounded",
+                  lower_bound: float = -5.0, initial_state=None, cu_seqlens=None, form: str = "recurrent",
+                  chunk: int = 64, nthreads: int | None = None):
+    """prestage() then forward().  The pre-stage is evaluated in fp64; forward() reads
+    its results rounded to fp32 (a relative change of at most 6e-8, far below any
+    tolerance this oracle is used with)."""
+    q, k, g, beta = prestage(q_raw, k_raw, g_raw, beta_raw, A_log, dt_bias, gate, lower_bound)
+    return forward(q, k, v, g, beta, scale, initial_state=initial_state, cu_seqlens=cu_seqlens, form=form,
+                   chunk=chunk, nthreads=nthreads)

@@ -30,6 +30,10 @@
  *      exp(gc_i) and exp(-gc_j), so the oracle has no overflow regime of its
  *      own.  A partial last chunk simply has fewer rows.
  *
+ *  (3) kda_oracle_prestage -- the activations of the gated forward (q/k L2
+ *      normalisation, the bounded or softplus gate, the beta sigmoid), applied
+ *      to raw projections before (1) or (2).
+ *
  * Readings where the pages are silent (also listed in the design notes):
  *  - q and k of value head hv come from key head hv / (HV / H)
  *    (repeat_interleave in the listing).
@@ -334,4 +338,60 @@ int kda_oracle_run(int form, int chunk, int H, int HV, int K, int V,
     free(th);
     pthread_mutex_destroy(&J.lock);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Pre-stage of the gated forward.                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The activations that turn raw projections into the forward's inputs, as the
+ * pages apply them before the chunk computation: the CPU reference's pre-stage
+ * ("手撕KDA", section 2, forward_bh: l2norm, beta sigmoid, gate activation) and
+ * the bounded gate of the FlashKDA walk-through ("KDA源码剖析之FlashKDA（上）",
+ * part 7, gate activation) and of "手撕KDA" section 5 (k_prepare_v8):
+ *
+ *   q^ = q / sqrt(sum_d q_d^2 + 1e-6)        per (token, key head); k^ likewise
+ *   bounded gate  (gate_kind 0):  g = lower_bound * sigmoid(exp(A_log[hv]) * (g_raw + dt_bias[hv, d]))
+ *   softplus gate (gate_kind 1):  g = -exp(A_log[hv]) * softplus(g_raw + dt_bias[hv, d])
+ *   beta = sigmoid(beta_raw)
+ *
+ * with sigmoid(x) = 1 / (1 + exp(-x)) and softplus(x) = log(1 + exp(x)).  The
+ * gate parameters belong to the value head (g is [tokens, HV, K]).  Layouts as in
+ * the forward: q_raw, k_raw [n_tok, H, K]; g_raw [n_tok, HV, K]; beta_raw [n_tok, HV];
+ * A_log [HV]; dt_bias [HV, K].  Everything in double precision.
+ */
+static double sigmoid_d(double x) { return 1.0 / (1.0 + exp(-x)); }
+static double softplus_d(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+void kda_oracle_prestage(long n_tok, int H, int HV, int K,
+                         const float* q_raw, const float* k_raw, const float* g_raw, const float* beta_raw,
+                         const float* A_log, const float* dt_bias, int gate_kind, double lower_bound,
+                         double* q_out, double* k_out, double* g_out, double* beta_out)
+{
+    for (long t = 0; t < n_tok; ++t) {
+        for (int h = 0; h < H; ++h) {
+            const float* qr = q_raw + (t * H + h) * K;
+            const float* kr = k_raw + (t * H + h) * K;
+            double sq = 0.0, sk = 0.0;
+            for (int d = 0; d < K; ++d) {
+                sq += (double)qr[d] * (double)qr[d];
+                sk += (double)kr[d] * (double)kr[d];
+            }
+            const double nq = sqrt(sq + 1e-6), nk = sqrt(sk + 1e-6);
+            for (int d = 0; d < K; ++d) {
+                q_out[(t * H + h) * K + d] = (double)qr[d] / nq;
+                k_out[(t * H + h) * K + d] = (double)kr[d] / nk;
+            }
+        }
+        for (int hv = 0; hv < HV; ++hv) {
+            const double a = exp((double)A_log[hv]);
+            for (int d = 0; d < K; ++d) {
+                const double x = (double)g_raw[(t * HV + hv) * K + d] + (double)dt_bias[hv * K + d];
+                g_out[(t * HV + hv) * K + d] =
+                    gate_kind == 0 ? lower_bound * sigmoid_d(a * x) : -a * softplus_d(x);
+            }
+            beta_out[t * HV + hv] = sigmoid_d((double)beta_raw[t * HV + hv]);
+        }
+    }
 }

@@ -220,3 +220,104 @@ def test_zero_padded_row_is_identity():
     _, S2 = oracle.forward(pad(q, 1.0), pad(k, 0.0), pad(v, 1.0), pad(g, 0.0), pad(beta, 0.5),
                            0.5, S0, form="chunked", chunk=4)
     assert np.abs(S - S2).max() <= 1e-12 * np.abs(S).max()
+
+
+# ---------------------------------------------------------------- pre-stage --
+# The activations of the gated forward (q/k L2 normalisation, the bounded and the
+# softplus gate, the beta sigmoid), pinned by closed forms chosen so that a slip
+# (eps outside the root, the norm over the wrong axis, A_log not exponentiated,
+# dt_bias added after the scale, dt_bias transposed, the wrong head's parameters)
+# changes a checked value.
+
+def _prestage(q=None, k=None, g=None, b=None, A_log=None, dt=None, gate="bounded", lb=-5.0,
+              B=1, T=2, H=1, HV=2, K=4):
+    z = lambda *s: np.zeros(s, dtype=np.float32)
+    q = z(B, T, H, K) if q is None else q
+    k = z(B, T, H, K) if k is None else k
+    g = z(B, T, HV, K) if g is None else g
+    b = z(B, T, HV) if b is None else b
+    A_log = z(HV) if A_log is None else A_log
+    dt = z(HV, K) if dt is None else dt
+    return oracle.prestage(q, k, g, b, A_log, dt, gate=gate, lower_bound=lb)
+
+
+def test_prestage_l2_norm_closed_form():
+    q = np.zeros((1, 2, 2, 4), dtype=np.float32)
+    q[0, 0, 0, 2] = 3.0                       # one non-zero entry: 3 / sqrt(9 + 1e-6)
+    q[0, 0, 1] = [1.0, 2.0, 2.0, 4.0]         # |q|^2 = 25, the other key head
+    q[0, 1, 0] = [1e-4, 0.0, 0.0, 0.0]        # |q|^2 = 1e-8, well below eps
+    qn, kn, _, _ = _prestage(q=q, k=q * 7, H=2, HV=2)
+    assert qn[0, 0, 0, 2] == pytest.approx(3.0 / np.sqrt(9.0 + 1e-6), rel=1e-15)
+    assert np.count_nonzero(qn[0, 0, 0]) == 1
+    np.testing.assert_allclose(qn[0, 0, 1], np.array([1, 2, 2, 4]) / np.sqrt(25.0 + 1e-6), rtol=1e-15)
+    assert qn[0, 1, 0, 0] == pytest.approx(1e-4 / np.sqrt(1e-8 + 1e-6), rel=1e-6)   # eps dominates: ~0.0995
+    assert np.all(qn[0, 1, 1] == 0.0)        # an all-zero row stays zero
+    np.testing.assert_allclose(kn[0, 0, 1], 7 * np.array([1, 2, 2, 4]) / np.sqrt(49 * 25.0 + 1e-6), rtol=1e-15)
+
+
+def test_prestage_beta_sigmoid():
+    b = np.array([[[0.0, np.log(3.0)], [-np.log(3.0), 40.0]]], dtype=np.float32)
+    _, _, _, beta = _prestage(b=b)
+    assert beta[0, 0, 0] == 0.5
+    assert beta[0, 0, 1] == pytest.approx(0.75, rel=1e-7)     # 1 / (1 + 1/3); ln 3 rounded to fp32
+    assert beta[0, 1, 0] == pytest.approx(0.25, rel=1e-6)
+    assert beta[0, 1, 1] == pytest.approx(1.0, abs=1e-17)
+
+
+def test_prestage_bounded_gate_closed_forms():
+    HV, K = 2, 4
+    ln3 = np.log(3.0)
+    A_log = np.array([np.log(2.0), 0.0], dtype=np.float32)           # a = 2 for head 0, a = 1 for head 1
+    dt = np.zeros((HV, K), dtype=np.float32)
+    dt[0] = [ln3 / 2, 0.0, 0.0, -ln3 / 2]                             # per dim, head 0 only
+    g = np.zeros((1, 2, HV, K), dtype=np.float32)
+    g[0, 1, 0, 1] = ln3 / 2
+    g[0, 1, 1, 2] = ln3
+    g[0, 1, 1, 3] = 60.0
+    _, _, ga, _ = _prestage(g=g, A_log=A_log, dt=dt, lb=-5.0)
+    # token 0: sigmoid(a * dt): head 0 dims 0 and 3 -> sigmoid(+-ln 3) = 3/4, 1/4; else 1/2
+    np.testing.assert_allclose(ga[0, 0, 0], [-3.75, -2.5, -2.5, -1.25], rtol=1e-6)
+    np.testing.assert_allclose(ga[0, 0, 1], [-2.5] * 4, rtol=1e-15)
+    # token 1: head 0 dim 1 -> a * (ln3/2 + 0) = ln 3; head 1 dim 2 -> ln 3, dim 3 -> 60 (saturates at lb)
+    assert ga[0, 1, 0, 1] == pytest.approx(-3.75, rel=1e-6)
+    assert ga[0, 1, 1, 2] == pytest.approx(-3.75, rel=1e-6)
+    assert ga[0, 1, 1, 3] == pytest.approx(-5.0, rel=1e-15)
+    assert np.all(ga <= 0.0) and np.all(ga >= -5.0)
+
+
+def test_prestage_softplus_gate_closed_forms():
+    HV, K = 2, 4
+    A_log = np.array([np.log(2.0), -50.0], dtype=np.float32)         # a = 2 (to fp32 rounding); a ~ 2e-22
+    a = np.exp(np.float64(A_log[0]))                                   # exactly what the oracle is handed
+    x1 = np.float64(np.float32(np.log(np.e - 1.0)))
+    g = np.zeros((1, 2, HV, K), dtype=np.float32)
+    g[0, 0, 0] = [0.0, x1, 40.0, -40.0]
+    g[0, 1, 1] = [100.0, 0.0, 0.0, 0.0]
+    _, _, ga, _ = _prestage(g=g, A_log=A_log, gate="softplus")
+    assert abs(a - 2.0) < 1e-8
+    assert ga[0, 0, 0, 0] == pytest.approx(-a * np.log(2.0), rel=1e-15)       # softplus(0) = ln 2
+    assert ga[0, 0, 0, 1] == pytest.approx(-a * np.log(np.exp(x1) + 1.0), rel=1e-14)
+    assert ga[0, 0, 0, 1] == pytest.approx(-2.0, rel=1e-7)                     # softplus(ln(e - 1)) = 1
+    assert ga[0, 0, 0, 2] == pytest.approx(-a * 40.0, rel=1e-15)               # softplus(x) = x + O(e^-x)
+    assert ga[0, 0, 0, 3] == pytest.approx(-a * np.exp(-40.0), rel=1e-12)     # softplus(x) = e^x + O(e^2x)
+    assert abs(ga[0, 1, 1, 0]) < 1e-19                                          # a ~ 0: no decay at all
+
+
+def test_gated_forward_reduces_to_exact_delta_rule_retrieval():
+    """A vanishing gate (a = e^-60) and beta_raw = 40 (beta = 1 - 4e-18) make the gated
+    forward the plain delta rule with unit-norm keys: after token t the state maps
+    k^_t to v_t (up to the 1e-6 inside the norm), k^_t^T S_t = v_t^T."""
+    rng = np.random.default_rng(21)
+    B, T, H, HV, K, V = 1, 6, 1, 1, 8, 5
+    q = rng.standard_normal((B, T, H, K)).astype(np.float32)
+    k = rng.standard_normal((B, T, H, K)).astype(np.float32)
+    v = rng.standard_normal((B, T, HV, V)).astype(np.float32)
+    g = rng.standard_normal((B, T, HV, K)).astype(np.float32)
+    b = np.full((B, T, HV), 40.0, dtype=np.float32)
+    A_log = np.array([-60.0], dtype=np.float32)
+    dt = np.zeros((HV, K), dtype=np.float32)
+    for t in range(1, T + 1):
+        sl = lambda a: a[:, :t]
+        _, S = oracle.forward_gated(sl(q), sl(k), sl(v), sl(g), sl(b), A_log, dt, 1.0, gate="softplus")
+        kn = k[0, t - 1, 0].astype(np.float64) / np.sqrt(np.sum(k[0, t - 1, 0].astype(np.float64) ** 2) + 1e-6)
+        np.testing.assert_allclose(kn @ S[0, 0], v[0, t - 1, 0], atol=2e-5)
