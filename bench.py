@@ -180,9 +180,10 @@ def unit_tokens(x, units):
     return int(sum(int(cu[s + 1] - cu[s]) for s, _ in units))
 
 
-def cpu_baseline(x, units: int | None = None):
+def cpu_baseline(x, units: int | None = None, gate=None):
     """Time the fp64 oracle (chunked form, C = 64) on a bounded sample of the
-    workload: `units` (sequence, value head) units, one thread each.  Returns
+    workload: `units` (sequence, value head) units, one thread each (with `gate`, the
+    oracle's pre-stage over the whole input first, then the sample).  Returns
     (tokens/s scaled so that a token counts all value heads, cores, sample text, s)."""
     import oracle
     cores = os.cpu_count() or 1
@@ -192,13 +193,19 @@ def cpu_baseline(x, units: int | None = None):
     f = lambda t: None if t is None else t.float().numpy()
     sel = sample_units(x, units)
     t0 = time.perf_counter()
-    oracle.forward_units(f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta), x.scale, sel, initial_state=f(x.initial_state),
+    if gate is None:
+        q, k, g, beta = f(x.q), f(x.k), f(x.g), f(x.beta)
+    else:
+        q, k, g, beta = oracle.prestage(f(x.q), f(x.k), f(x.g_raw), f(x.beta_raw), f(x.A_log), f(x.dt_bias),
+                                        gate=gate[0], lower_bound=gate[1])
+    oracle.forward_units(q, k, f(x.v), g, beta, x.scale, sel, initial_state=f(x.initial_state),
                          cu_seqlens=None if x.cu_seqlens is None else x.cu_seqlens.numpy(), form="chunked", chunk=64,
                          nthreads=units)
     dt = time.perf_counter() - t0
     token_heads = unit_tokens(x, sel)
     sample = (f"{len(sel)} of {x.num_seqs * HV} (sequence, value head) units ({token_heads} token-heads) of "
-              f"{x.meta.get('workload', 'the workload')}, fp64 chunked oracle (C=64), {units} threads; "
+              f"{x.meta.get('workload', 'the workload')}, fp64 {'pre-stage + ' if gate else ''}chunked oracle "
+              f"(C=64), {units} threads; "
               f"{dt:.2f} s wall; tokens/s counts a token as all {HV} value heads")
     return token_heads / HV / dt, units, sample, dt
 
@@ -259,7 +266,8 @@ def run_gpu(args):
     kda.build()
     kda.load_library()
     w = W.WORKLOADS[args.workload]
-    host = W.workload_inputs(args.workload)
+    gate = ("bounded", -5.0) if args.gated else None
+    host = W.workload_raw_inputs(args.workload) if args.gated else W.workload_inputs(args.workload)
     x = host.to(dev)
     B, T, H, K = x.q.shape
     HV, V = x.v.shape[2], x.v.shape[3]
@@ -272,9 +280,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, x.scale, initial_state=x.initial_state,
-                          cu_seqlens=x.cu_seqlens, out=out, final_state=fin, workspace=wsp,
-                          stream=stream.cuda_stream)
+        forward(kda, x, gate, out=out, final_state=fin, workspace=wsp, stream=stream.cuda_stream)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -311,21 +317,23 @@ def run_gpu(args):
 
     tokens = host.tokens()
     value = ws * tokens / (ms * 1e-3)
-    flops = W.flops_convention(host)
+    flops = tokens * HV * (6 * K * V + 6 * 64 * K + 4 * 64 * V)  # the flop convention (workloads.flops_convention)
     tflops = ws * flops / (ms * 1e-3) / 1e12
-    alg_bytes = W.algorithmic_bytes(host, final_state=True)  # the initial state counts only when it is read
+    alg_bytes = input_bytes(host) + 2 * x.v.numel() + NS * HV * K * V * 4  # inputs once, o and the final state
     hbm_gbs, bf16_tf, peak_src = load_peaks()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     kernel_name = kda.kda_chunk_fwd_kernel_name(shape)  # the one launch of each step
 
     # end to end through the public API with pinned host buffers
-    e2e = e2e_measure(kda, host, dev, stream, max(3, min(args.steps, 20 if tokens <= 1 << 16 else 5)))
+    e2e = e2e_measure(kda, host, gate, dev, stream, max(3, min(args.steps, 20 if tokens <= 1 << 16 else 5)))
 
     line = {
         "impl": "kda_gb300", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w, host, ws), "tflops": tflops,
+        "config": dict(config_dict(w, host, ws), **({"prestage": "fused: raw bf16 q, k, g_raw; bounded gate "
+                                                        "lower_bound -5; beta sigmoid"} if gate else {})),
+        "tflops": tflops,
         # the token recurrence's own arithmetic, 7 K V flop per token and value head: a
         # lower bound on any evaluation, reported beside the chunked convention
         "tflops_recurrent_lower_bound": ws * tokens * HV * 7 * K * V / (ms * 1e-3) / 1e12,
@@ -339,7 +347,7 @@ def run_gpu(args):
         "device_status": status, "wall_s_timed_region": t_wall,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, cores, sample, _ = cpu_baseline(host)
+        v, cores, sample, _ = cpu_baseline(host, gate=gate)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -349,28 +357,51 @@ def run_gpu(args):
     return 0
 
 
-def e2e_measure(kda, host, dev, stream, steps):
-    """Same metric through kda_chunk_fwd with host buffers: every step copies the
-    inputs (and the initial state and cu_seqlens when the workload has them) from
+def input_tensors(x):
+    """(name, tensor) of every input a forward reads, in the order of the call."""
+    if hasattr(x, "g_raw"):
+        names = ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias", "initial_state", "cu_seqlens")
+    else:
+        names = ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")
+    return [(n, getattr(x, n)) for n in names]
+
+
+def input_bytes(x):
+    return sum(t.numel() * t.element_size() for _, t in input_tensors(x) if t is not None)
+
+
+def forward(kda, d, gate, **kw):
+    """One forward on device tensors `d` (an Inputs, a RawInputs or a dict with the same
+    fields) through the public entry point."""
+    g = d.get if isinstance(d, dict) else (lambda n: getattr(d, n))
+    if gate is None:
+        return kda.kda_chunk_fwd(g("q"), g("k"), g("v"), g("g"), g("beta"), g("scale"), initial_state=g("initial_state"),
+                                 cu_seqlens=g("cu_seqlens"), **kw)
+    return kda.kda_chunk_fwd_gated(g("q"), g("k"), g("v"), g("g_raw"), g("beta_raw"), g("A_log"), g("dt_bias"),
+                                   gate=gate[0], lower_bound=gate[1], scale=g("scale"),
+                                   initial_state=g("initial_state"), cu_seqlens=g("cu_seqlens"), **kw)
+
+
+def e2e_measure(kda, host, gate, dev, stream, steps):
+    """Same metric through the public entry point with host buffers: every step copies
+    the inputs (with the initial state and cu_seqlens when the workload has them) from
     pinned host memory to the device, runs the forward and copies o and the final
     state back.  Steps alternate between two streams with their own device buffers
     and workspaces, so that one step's copies overlap the previous step's forward;
     each stream keeps its own steps in order.  (Splitting a step's input copies over
     several streams did not raise the host-to-device rate, ~195 GB/s.)"""
     import torch
-    pin = lambda t: None if t is None else t.pin_memory()
-    names = ("q", "k", "v", "g", "b", "s0", "cu")
-    hsrc = dict(zip(names, (pin(t) for t in (host.q, host.k, host.v, host.g, host.beta, host.initial_state,
-                                              host.cu_seqlens))))
+    hsrc = {n: (None if t is None else t.pin_memory()) for n, t in input_tensors(host)}
     B, T, H, K = host.q.shape
     HV, V = host.v.shape[2], host.v.shape[3]
     NS = host.num_seqs
-    shape = kda.make_shape(hsrc["q"], hsrc["v"], hsrc["cu"])
+    shape = kda.make_shape(hsrc["q"], hsrc["v"], hsrc["cu_seqlens"])
     wsz = kda.kda_chunk_fwd_workspace_size(shape)
     streams = [stream, torch.cuda.Stream(dev)]
     bufs = []
     for _ in range(2):
         d = {n: (None if t is None else torch.empty_like(t, device=dev)) for n, t in hsrc.items()}
+        d["scale"] = host.scale
         d["o"] = torch.empty_like(d["v"])
         d["s"] = torch.empty((NS, HV, K, V), dtype=torch.float32, device=dev)
         d["ws"] = torch.empty(wsz, dtype=torch.uint8, device=dev)
@@ -386,9 +417,7 @@ def e2e_measure(kda, host, dev, stream, steps):
             for n, h in hsrc.items():
                 if h is not None:
                     d[n].copy_(h, non_blocking=True)
-            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], host.scale, initial_state=d["s0"],
-                              cu_seqlens=d["cu"], out=d["o"], final_state=d["s"], workspace=d["ws"],
-                              stream=st.cuda_stream)
+            forward(kda, d, gate, out=d["o"], final_state=d["s"], workspace=d["ws"], stream=st.cuda_stream)
             d["ho"].copy_(d["o"], non_blocking=True)
             d["hs"].copy_(d["s"], non_blocking=True)
 
@@ -478,6 +507,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kda_gb300", choices=["kda_gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gated", action="store_true",
+                    help="raw bf16 inputs through kda_chunk_fwd_gated (pre-stage fused, bounded gate)")
     ap.add_argument("--mode", default="forward", choices=["forward", "decode"],
                     help="decode: time kda_decode (one token per sequence) instead of the chunked forward")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,

@@ -119,6 +119,42 @@ KDA_API kda_status kda_chunk_fwd(const kda_shape* shape, const void* q, const vo
                          float* final_state, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* Gate activations of kda_chunk_fwd_gated. */
+typedef enum {
+  KDA_GATE_BOUNDED = 0,   /* g = lower_bound * sigmoid(exp(A_log[hv]) * (g_raw + dt_bias[hv, d])) */
+  KDA_GATE_SOFTPLUS = 1   /* g = -exp(A_log[hv]) * softplus(g_raw + dt_bias[hv, d])            */
+} kda_gate_kind;
+
+typedef struct {
+  kda_gate_kind kind;
+  const float* A_log;     /* [HV] fp32, device                                       */
+  const float* dt_bias;   /* [HV, K] fp32, device                                    */
+  float lower_bound;      /* bounded gate only: < 0 (the pages use -5)               */
+} kda_gate;
+
+/*
+ * kda_chunk_fwd with the pre-stage fused into the chunk kernels: the raw
+ * projections go in, the activations are applied where the chunks are prepared
+ * (page "手撕KDA", section 2: l2norm, beta sigmoid and gate activation before the
+ * chunk computation; section 5 and page "KDA源码剖析之FlashKDA（上）", part 7: the
+ * bounded gate, computed in the kernel that builds the chunk):
+ *
+ *   q, k      [B, T, H, K]  bf16, raw: each row is scaled by 1 / sqrt(|row|^2 + 1e-6)
+ *   v         [B, T, HV, V] bf16
+ *   g_raw     [B, T, HV, K] bf16: the gate input (half the bytes of an fp32 g)
+ *   beta_raw  [B, T, HV]    fp32: beta = sigmoid(beta_raw)
+ *   gate      the activation and its parameters (per value head)
+ * and everything else as kda_chunk_fwd (same workspace size).  Requires bf16 I/O
+ * and K = V = 128 (the tensor-core kernels); other shapes return
+ * KDA_ERR_UNSUPPORTED.  The decay range of kda_chunk_fwd applies to the activated
+ * g; the bounded gate with lower_bound >= -5 always meets it.
+ */
+KDA_API kda_status kda_chunk_fwd_gated(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                       const void* g_raw, const float* beta_raw, const kda_gate* gate,
+                                       float scale, const float* initial_state, const int32_t* cu_seqlens,
+                                       void* out, float* final_state, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
 /*
  * Token-recurrent forward: the defining recurrence evaluated token by token on
  * CUDA cores in fp32 (same arguments and results as kda_chunk_fwd; its

@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     KdaError,
     KdaShape,
     kda_chunk_fwd,
+    kda_chunk_fwd_gated,
     kda_chunk_fwd_static_scratch,
     kda_chunk_fwd_workspace_size,
     kda_chunk_size,

@@ -31,7 +31,8 @@ STATIC_SCRATCH_MAX_UNITS = 32
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
            "kda_read_device_status", "kda_status_string", "kda_chunk_size",
-           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode")
+           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode", "kda_chunk_fwd_gated")
+GATE_KINDS = {"bounded": 0, "softplus": 1}
 
 
 class KdaError(RuntimeError):
@@ -44,6 +45,11 @@ class KdaShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("HV", ctypes.c_int),
                 ("K", ctypes.c_int), ("V", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("io_dtype", ctypes.c_int)]
+
+
+class KdaGate(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("lower_bound", ctypes.c_float)]
 
 
 def library_path() -> str:
@@ -81,6 +87,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_chunk_fwd_static_scratch.restype = I
         lib.kda_decode.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P]
         lib.kda_decode.restype = I
+        lib.kda_chunk_fwd_gated.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, ctypes.POINTER(KdaGate), F,
+                                            P, P, P, P, P, S, P]
+        lib.kda_chunk_fwd_gated.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -249,3 +258,49 @@ def kda_decode(q, k, v, g, beta, state, scale=None, out=None, stream=None):
         _check(lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                               ctypes.c_float(scale), _ptr(state), _ptr(out), ctypes.c_void_p(stream)))
     return out
+
+
+def kda_chunk_fwd_gated(q, k, v, g_raw, beta_raw, A_log, dt_bias, gate="bounded", lower_bound=-5.0, scale=None,
+                        initial_state=None, cu_seqlens=None, out=None, final_state=None, output_final_state=True,
+                        workspace=None, stream=None):
+    """Chunked forward with the pre-stage fused in: raw q, k [B,T,H,K] bf16 (L2-normalised
+    in the kernel), v [B,T,HV,V] bf16, g_raw [B,T,HV,K] bf16, beta_raw [B,T,HV] fp32,
+    A_log [HV] and dt_bias [HV,K] fp32; gate "bounded" (lower_bound sigmoid(exp(A_log)
+    (g_raw + dt_bias))) or "softplus" (-exp(A_log) softplus(g_raw + dt_bias))."""
+    lib = load_library()
+    _check_tensors(q, k, v, g_raw, beta_raw, (("A_log", A_log), ("dt_bias", dt_bias),
+                                              ("initial_state", initial_state), ("cu_seqlens", cu_seqlens),
+                                              ("out", out), ("final_state", final_state), ("workspace", workspace)))
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise KdaError(1, f"{name} must be a contiguous fp32 CUDA tensor")
+    with torch.cuda.device(q.device):
+        shape = make_shape(q, v, cu_seqlens)
+        K = q.shape[3]
+        if scale is None:
+            scale = K ** -0.5
+        NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
+        HV, V = v.shape[2], v.shape[3]
+        made = []
+        if out is None:
+            out = torch.empty_like(v)
+            made.append(out)
+        if final_state is None and output_final_state:
+            final_state = torch.empty((NS, HV, K, V), dtype=torch.float32, device=q.device)
+            made.append(final_state)
+        if workspace is None:
+            workspace = torch.empty(kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device=q.device)
+            made.append(workspace)
+        current = torch.cuda.current_stream(q.device).cuda_stream
+        if stream is None:
+            stream = current
+        gs = KdaGate(GATE_KINDS[gate], A_log.data_ptr(), dt_bias.data_ptr(), float(lower_bound))
+        _check(lib.kda_chunk_fwd_gated(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), ctypes.byref(gs),
+            ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+            _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()), ctypes.c_void_p(stream)))
+        if made and stream != current:
+            other = torch.cuda.ExternalStream(stream, device=q.device)
+            for t in made:
+                t.record_stream(other)
+    return out, final_state

@@ -59,9 +59,10 @@ struct Checked {
   size_t units;  // sequences * value heads
 };
 
+// g_elem: bytes per element of g (4: the log-space decay; 2: the gated entry's bf16 gate input)
 kda_status validate(bool use_tc, const kda_shape* s, const void* q, const void* k, const void* v,
-                    const float* g, const float* beta, float scale, const float* s0, const int32_t* cu,
-                    void* out, float* sfin, void* ws, size_t ws_bytes, Checked& c) {
+                    const void* g, const float* beta, float scale, const float* s0, const int32_t* cu,
+                    void* out, float* sfin, void* ws, size_t ws_bytes, Checked& c, size_t g_elem = 4) {
   if (!s) return KDA_ERR_INVALID_ARG;
   if (s->B < 0 || s->T < 0 || s->H < 1 || s->HV < 1 || s->K < 1 || s->V < 1) return KDA_ERR_INVALID_ARG;
   if (s->HV % s->H != 0) return KDA_ERR_INVALID_ARG;
@@ -79,7 +80,7 @@ kda_status validate(bool use_tc, const kda_shape* s, const void* q, const void* 
   const size_t tokens = cu ? static_cast<size_t>(s->T) : static_cast<size_t>(s->B) * s->T;
   const size_t es = s->io_dtype == KDA_BF16 ? 2 : 4;
   const size_t n_qk = tokens * s->H * s->K * es, n_v = tokens * s->HV * s->V * es;
-  const size_t n_g = tokens * s->HV * s->K * 4, n_b = tokens * s->HV * 4;
+  const size_t n_g = tokens * s->HV * s->K * g_elem, n_b = tokens * s->HV * 4;
   const size_t n_s = ns * s->HV * s->K * s->V * 4;
   if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
   // tensors read or written in 16-byte vectors / TMA tiles need 16-byte
@@ -101,7 +102,7 @@ kda_status validate(bool use_tc, const kda_shape* s, const void* q, const void* 
 
   kda::FwdParams& p = c.p;
   std::memset(&p, 0, sizeof(p));
-  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = s0; p.cu = cu;
+  p.q = q; p.k = k; p.v = v; p.g = static_cast<const float*>(g); p.beta = beta; p.s0 = s0; p.cu = cu;
   p.out = out; p.sfin = sfin; p.status = static_cast<uint32_t*>(ws);
   p.ring = ws_bytes > kda::kRingOffset ? static_cast<uint8_t*>(ws) + kda::kRingOffset : nullptr;
   p.wait_ns = wait_limit_ns();
@@ -214,6 +215,38 @@ const char* kda_chunk_fwd_kernel_name(const kda_shape* s) {
   const long tokens = s->num_seqs > 0 ? static_cast<long>(s->T) : static_cast<long>(s->B) * s->T;
   if (ns * s->HV > (1L << 30)) return "none";
   return kda::chunk_kernel_name(s->io_dtype == KDA_BF16, s->K, s->V, tokens, static_cast<int>(ns * s->HV));
+}
+
+kda_status kda_chunk_fwd_gated(const kda_shape* shape, const void* q, const void* k, const void* v,
+                               const void* g_raw, const float* beta_raw, const kda_gate* gate, float scale,
+                               const float* initial_state, const int32_t* cu_seqlens, void* out,
+                               float* final_state, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!shape || !gate) return KDA_ERR_INVALID_ARG;
+  if (gate->kind != KDA_GATE_BOUNDED && gate->kind != KDA_GATE_SOFTPLUS) return KDA_ERR_INVALID_ARG;
+  if (gate->kind == KDA_GATE_BOUNDED && !(gate->lower_bound < 0.f && std::isfinite(gate->lower_bound)))
+    return KDA_ERR_INVALID_ARG;
+  if (!gate->A_log || !gate->dt_bias) return KDA_ERR_INVALID_ARG;
+  if (!aligned(gate->A_log, 4) || !aligned(gate->dt_bias, 16)) return KDA_ERR_ALIGNMENT;
+  // g_raw (bf16) takes the place of g in the common checks, at its own size
+  Checked c;
+  kda_status st = validate(true, shape, q, k, v, g_raw, beta_raw, scale, initial_state, cu_seqlens, out,
+                           final_state, workspace, workspace_bytes, c, 2);
+  if (st != KDA_OK) return st;
+  if (c.units == 0) return KDA_OK;
+  const long tokens = cu_seqlens ? static_cast<long>(shape->T) : static_cast<long>(shape->B) * shape->T;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (tokens == 0) {  // nothing to activate: the state copy of an empty forward
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
+    return kda::launch_recurrent_fwd(c.p, c.bf16, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
+  if (!c.p.ring || !kda::chunk_tc_supported(c.p, c.bf16)) return KDA_ERR_UNSUPPORTED;
+  c.p.prestage = gate->kind == KDA_GATE_BOUNDED ? 1 : 2;
+  c.p.g_raw = static_cast<const uint16_t*>(g_raw);
+  c.p.g = nullptr;
+  c.p.A_log = gate->A_log;
+  c.p.dt_bias = gate->dt_bias;
+  c.p.lower_bound = gate->lower_bound;
+  return kda::launch_chunk_tc_fwd(c.p, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,

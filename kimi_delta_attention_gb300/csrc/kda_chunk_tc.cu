@@ -83,8 +83,9 @@ constexpr uint32_t OFF_PREP = 2 * SSLOT;                  // 124928 producer til
 constexpr uint32_t OFF_ST = OFF_PREP + 90112;             // 215040 S  [128 x 32] bf16 MN-major SW64 (chain)
 constexpr uint32_t OFF_BETA = OFF_ST + 8192;              // 223232 [64] fp32
 constexpr uint32_t OFF_GSUM = OFF_BETA + 256;             // 223488 [4][128] fp32 quarter-chunk sums of g
-constexpr uint32_t OFF_BAR = OFF_GSUM + 2048;             // 225536 mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 225792 tmem base
+constexpr uint32_t OFF_RN = OFF_GSUM + 2048;              // 225536 [128] fp32 row norms of the raw q, k (pre-stage)
+constexpr uint32_t OFF_BAR = OFF_RN + 512;                // 226048 mbarriers
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;              // 226304 tmem base
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;        // + alignment slack
 static_assert(OFF_PREP % 1024 == 0 && SMEM_ALLOC <= 232448, "cluster kernel shared memory");
@@ -164,6 +165,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+constexpr float kLn2 = 0.6931471805599453f;
+__device__ __forceinline__ float rcp_approx(float x) {  // 1 / x (PTX rcp.approx; 1 / inf = 0)
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// sigmoid(x) = 1 / (1 + e^-x) = (1 + tanh(x / 2)) / 2: one special-function instruction
+__device__ __forceinline__ float sigmoid_approx(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 // two floats -> bf16 pair (lo in the low half), one paired conversion instruction
@@ -379,13 +398,64 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Pre-stage of the gated forward, on the thread's 16 rows x 2 dims of raw gate input
+// (g: raw values in, activated g out; rows past the end become 0) and, for the first
+// 64 threads, its row's raw beta: the bounded gate lower_bound sigmoid(a (g + dt)) or
+// the softplus gate -a softplus(g + dt), a = exp(A_log) of the value head, and beta =
+// sigmoid(beta).  (Pages "手撕KDA" section 2 and "KDA源码剖析之FlashKDA（上）" part 7.)
+__device__ __forceinline__ void activate(float2 (&g)[16], float& beta, int kind, float lb, float a, float2 dt,
+                                         int hq, int pt, int rows) {
+  const int nvalid = rows - 16 * hq;
+  if (kind == 1) {  // lb sigmoid(a x) = lb/2 + (lb/2) tanh(a x / 2)
+    const float ha = 0.5f * a, hl = 0.5f * lb;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float x0 = fmaf(hl, tanh_approx(ha * (g[i].x + dt.x)), hl);
+      const float x1 = fmaf(hl, tanh_approx(ha * (g[i].y + dt.y)), hl);
+      g[i] = i < nvalid ? make_float2(x0, x1) : make_float2(0.f, 0.f);
+    }
+  } else {
+    auto softplus = [](float x) {  // log(1 + e^x), with its two asymptotes
+      return x > 20.f ? x : (x < -20.f ? ex2_approx(x * kLog2e) : lg2_approx(1.f + ex2_approx(x * kLog2e)) * kLn2);
+    };
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float x0 = -a * softplus(g[i].x + dt.x), x1 = -a * softplus(g[i].y + dt.y);
+      g[i] = i < nvalid ? make_float2(x0, x1) : make_float2(0.f, 0.f);
+    }
+  }
+  if (pt < C) beta = pt < rows ? sigmoid_approx(beta) : 0.f;
+}
+
+// 1 / sqrt(|row|^2 + 1e-6) of every row of the stacked raw tile (k and q rows), into
+// rn[stacked row]: thread pt sums the squares of K-block pt & 1 of stacked row pt / 2,
+// its neighbour lane the other K-block.
+__device__ __forceinline__ void row_norms(const uint8_t* base, float* rn, int pt) {
+  const int srow = pt >> 1, kb = pt & 1;
+  const uint4* r = reinterpret_cast<const uint4*>(base + QK + kb * QK_KB + srow * 128);
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 u = r[c];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float lo = __uint_as_float(w[t] << 16), hi = __uint_as_float(w[t] & 0xFFFF0000u);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
+  }
+  ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+  if (kb == 0) rn[srow] = rsqrtf(ss + 1e-6f);
+}
+
 // Elementwise pass of thread (dp, hq): key dims 2 dp, 2 dp + 1 of chunk rows
 // [16 hq, 16 hq + 16) (quarter hq).  gsum holds the four quarter sums of g (natural
 // log) per key dim; g holds this thread's 16 rows.  Writes kA/qA (in place), cA, kd and
 // (hq < 2) cB to the tiles, kr^T and (hq = 0) e^{g_last} into the record (krt_rec +
 // SW128 offset in the [128 x 64] kr^T tile, gam_rec), and qd either to the tile QDS
 // (QD_SMEM, for a bulk copy) or into the record (qd_rec + kb * qd_kb_stride + SW128 row
-// offset).  Sets range_bad when this quarter decays faster
+// offset).  With NORM, k and q rows are first scaled by their rn[] entries (the
+// pre-stage's L2 normalisation).  Sets range_bad when this quarter decays faster
 // than the factors can represent.
 //
 // With x the within-quarter cumsum (log2 units; 0 >= x >= sh, sh the quarter's sum),
@@ -400,10 +470,10 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 // swizzle (16-byte chunk index XOR row % 8) is an XOR on address bits 4-6 that commutes
 // with adding the row and the tile offsets; one 32-bit shared address per row serves
 // all tiles.
-template <bool QD_SMEM>
+template <bool QD_SMEM, bool NORM>
 __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, const float2 (&g)[16], int dp, int hq,
                                             int rows, float scale, uint8_t* qd_rec, uint32_t qd_kb_stride,
-                                            uint8_t* krt_rec, float* gam_rec, bool& range_bad) {
+                                            uint8_t* krt_rec, float* gam_rec, const float* rn, bool& range_bad) {
   float c_d[2], c_r[2], es[2], fa[2], fb[2];
   const bool even = (hq & 1) == 0;
 #pragma unroll
@@ -455,7 +525,13 @@ __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, co
     x1 = fmaf(g[i].y, kLog2e, x1);
     const unsigned long long E = f2u(ex2_approx(x0), ex2_approx(x1));
     const unsigned long long IE = f2u(ex2_approx(-x0), ex2_approx(-x1));
-    const unsigned long long Kv = bf2u(kraw), Qv = mul2(bf2u(qraw), SC);
+    unsigned long long Kv = bf2u(kraw), Qv = mul2(bf2u(qraw), SC);
+    if (NORM) {
+      const uint32_t srow = (hq >= 2 ? 32u : 0u) + r0 + i;  // stacked row of k row r0 + i (q: + 32)
+      const float rk = rn[srow], rq = rn[srow + 32];
+      Kv = mul2(Kv, f2u(rk, rk));
+      Qv = mul2(Qv, f2u(rq, rq));
+    }
     const unsigned long long Pv = mul2(IE, ES);  // 2^{sh - x}
     {
       const unsigned long long Av = even ? mul2(E, FA) : E;
@@ -606,6 +682,10 @@ __device__ __forceinline__ void inverse_diag_blocks(uint8_t* base, const float* 
 }
 }  // namespace prep
 
+// PRE: the pre-stage of the gated forward is fused in (p.prestage != 0): raw bf16 gate
+// input, beta sigmoid and q/k L2 normalisation (a separate instantiation, so that the
+// plain forward carries none of it)
+template <bool PRE>
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -614,6 +694,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   float* beta_s = reinterpret_cast<float*>(sm + OFF_BETA);
   float* gsum = reinterpret_cast<float*>(sm + OFF_GSUM);
+  float* rn = reinterpret_cast<float*>(sm + OFF_RN);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hv = blockIdx.y, seq = blockIdx.z;
@@ -704,11 +785,22 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     auto prefetch_gb = [&](int m, int part) {
       const int rows = min(C, len - m * C);
       const long base = tok0 + static_cast<long>(m) * C;
+      if (PRE) {  // raw gate input, bf16 pairs
 #pragma unroll
-      for (int i = 4 * part; i < 4 * part + 4; ++i) {
-        const int c = 16 * hq + i;
-        gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp)
-                             : make_float2(0.f, 0.f);
+        for (int i = 4 * part; i < 4 * part + 4; ++i) {
+          const int c = 16 * hq + i;
+          const uint32_t w =
+              (c < rows) ? __ldg(reinterpret_cast<const uint32_t*>(p.g_raw + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp)
+                         : 0u;
+          gpre[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        }
+      } else {
+#pragma unroll
+        for (int i = 4 * part; i < 4 * part + 4; ++i) {
+          const int c = 16 * hq + i;
+          gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp)
+                               : make_float2(0.f, 0.f);
+        }
       }
       if (part == 0 && pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
     };
@@ -742,9 +834,19 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       uint8_t* gs = ring + static_cast<size_t>(m % RING) * GSLOT;
       const int rows = min(C, len - m * C);
       const bool next = m + NSLICE < NT;
-      // ---- 1. raw q, k, v of chunk m ----
+      // ---- 1. raw q, k, v of chunk m (and the gate parameters of the pre-stage) ----
+      float a_log = 0.f;
+      float2 dt = make_float2(0.f, 0.f);
+      if (PRE) {
+        a_log = __ldg(p.A_log + hv);
+        dt = __ldg(reinterpret_cast<const float2*>(p.dt_bias + static_cast<size_t>(hv) * KD) + dp);
+      }
       if (!mbar_wait(&bars[B_RAW], j & 1, p.wait_ns)) timeout();
       if (pt == 0) bulk_wait_read();  // the previous record's Aqk, W and U stagings have been read
+      if (PRE) {  // activations, and the raw q, k row norms (read before the pass rewrites the rows)
+        prep::activate(gpre, bpre, p.prestage, p.lower_bound, expf(a_log), dt, hq, pt, rows);
+        prep::row_norms(pb, rn, pt);
+      }
       if (pt < C) beta_s[pt] = bpre;
       {
         float2 qsum = make_float2(0.f, 0.f);
@@ -763,8 +865,12 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       //         record (a slot is rewritten only after its previous record was loaded
       //         everywhere: publish() of the record two before waited for that) ----
       {
-        prep::elementwise<false>(pb, gsum, gpre, dp, hq, rows, scale, gs + R_WQ + R_QD_IN_KB, R_W_KB, gs + R_KRT,
-                                 reinterpret_cast<float*>(gs + G_GAM), range_bad);
+        if (PRE)
+          prep::elementwise<false, true>(pb, gsum, gpre, dp, hq, rows, scale, gs + R_WQ + R_QD_IN_KB, R_W_KB,
+                                         gs + R_KRT, reinterpret_cast<float*>(gs + G_GAM), rn, range_bad);
+        else
+          prep::elementwise<false, false>(pb, gsum, gpre, dp, hq, rows, scale, gs + R_WQ + R_QD_IN_KB, R_W_KB,
+                                          gs + R_KRT, reinterpret_cast<float*>(gs + G_GAM), nullptr, range_bad);
       }
       fence_proxy_async_global();  // the record's plain stores, read by the chains' bulk copies
       if (pt == 0 && pub_pending) bulk_wait_group<0>();  // the previous record's W/U stores have landed
@@ -1222,7 +1328,8 @@ constexpr uint32_t REC_BYTES = SR_U + 16384;  // 74,752 B
 static_assert(REC_BYTES <= GSLOT, "record fits a ring slot");
 // producer pipeline region (offsets from the region base, 1024-aligned): the prep:: tiles,
 // then beta, the quarter sums of g, barriers and the ring-slot flag
-constexpr uint32_t P_BETA = prep::QDS + 16384, P_GSUM = P_BETA + 256, P_BAR = P_GSUM + 2048, P_STRIDE = 109568;
+constexpr uint32_t P_BETA = prep::QDS + 16384, P_GSUM = P_BETA + 256, P_RN = P_GSUM + 2048, P_BAR = P_RN + 512,
+                   P_STRIDE = 109568;
 static_assert(P_BAR + 64 <= P_STRIDE && P_STRIDE % 1024 == 0, "producer pipeline region");
 // chain region
 // chain region: record part A ([qd; W], e^{g_last}) in three buffers, part B (kr^T, Aqk,
@@ -1293,6 +1400,7 @@ constexpr int kRecStorer = 32;  // pipeline thread storing qd and kr^T to the ri
   do {            \
   } while (0)
 #endif
+template <bool PRE>
 __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, uint8_t* sm, uint32_t tmem,
                                          int pipe, int q, int NQ, int NU, int NREC, uint32_t* flags) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1306,6 +1414,7 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + P_BAR);
   float* beta_s = reinterpret_cast<float*>(sm + P_BETA);
   float* gsum = reinterpret_cast<float*>(sm + P_GSUM);
+  float* rnorm = reinterpret_cast<float*>(sm + P_RN);  // row norms of the raw q, k (pre-stage)
   volatile uint32_t* slot_free = reinterpret_cast<volatile uint32_t*>(sm + P_SLOT_FREE);
   const uint32_t sb = smem_u32(sm);
   const uint64_t D_PREP = sdesc_sw128(sb);
@@ -1335,11 +1444,22 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
   auto prefetch_gb = [&](const Rec& x, int part) {
     const int rows = min(C, x.len - x.m * C);
     const long base = x.tok0 + static_cast<long>(x.m) * C;
+    if (PRE) {  // raw gate input, bf16 pairs
 #pragma unroll
-    for (int i = 4 * part; i < 4 * part + 4; ++i) {
-      const int c = 16 * hq + i;
-      gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp)
-                           : make_float2(0.f, 0.f);
+      for (int i = 4 * part; i < 4 * part + 4; ++i) {
+        const int c = 16 * hq + i;
+        const uint32_t w =
+            (c < rows) ? __ldg(reinterpret_cast<const uint32_t*>(p.g_raw + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp)
+                       : 0u;
+        gpre[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+      }
+    } else {
+#pragma unroll
+      for (int i = 4 * part; i < 4 * part + 4; ++i) {
+        const int c = 16 * hq + i;
+        gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp)
+                             : make_float2(0.f, 0.f);
+      }
     }
     if (part == 0 && pt < C)
       bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + x.hv) : 0.f;
@@ -1377,10 +1497,20 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     const int rows = min(C, cur.len - cur.m * C);
     // ---- 1. raw q, k, v tiles; is the ring slot known to be free (its previous record
     //         loaded by the chain, as the counter read ahead shows)? ----
+    float a_log = 0.f;  // gate parameters of the pre-stage, requested before the wait
+    float2 dt = make_float2(0.f, 0.f);
+    if (PRE) {
+      a_log = __ldg(p.A_log + cur.hv);
+      dt = __ldg(reinterpret_cast<const float2*>(p.dt_bias + static_cast<size_t>(cur.hv) * KD) + dp);
+    }
     PSTAMP(0);
     if (!mbar_wait(&bars[PB_RAW], j & 1, p.wait_ns)) timeout();
     PSTAMP(1);
     if (pt == 0 || pt == kRecStorer) bulk_wait_read();  // the previous record's stagings have been read
+    if (PRE) {  // activations, and the raw q, k row norms (read before the pass rewrites the rows)
+      prep::activate(gpre, bpre, p.prestage, p.lower_bound, expf(a_log), dt, hq, pt, rows);
+      prep::row_norms(sm, rnorm, pt);
+    }
     if (pt < C) beta_s[pt] = bpre;
     {
       float2 qsum = make_float2(0.f, 0.f);
@@ -1412,8 +1542,12 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 
     // ---- 2. elementwise: operand tiles; qd, kr^T and e^{g_last} straight into the record ----
     {
-      prep::elementwise<true>(sm, gsum, gpre, dp, hq, rows, scale, gs + SR_QW, SR_KB, gs + SR_KRT,
-                              reinterpret_cast<float*>(gs + SR_GAM), range_bad);
+      if (PRE)
+        prep::elementwise<true, true>(sm, gsum, gpre, dp, hq, rows, scale, gs + SR_QW, SR_KB, gs + SR_KRT,
+                                      reinterpret_cast<float*>(gs + SR_GAM), rnorm, range_bad);
+      else
+        prep::elementwise<true, false>(sm, gsum, gpre, dp, hq, rows, scale, gs + SR_QW, SR_KB, gs + SR_KRT,
+                                       reinterpret_cast<float*>(gs + SR_GAM), nullptr, range_bad);
     }
     fence_proxy_async_global();  // the record's plain stores, read by the chain's bulk copies
     if ((pt == 0 || pt == kRecStorer) && pub_pending) bulk_wait_group<0>();  // the previous record's stores have landed
@@ -2023,6 +2157,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
 }
 }  // namespace split
 
+template <bool PRE>
 __global__ void __launch_bounds__(split::NTHREADS, 1)
 kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int NU, int NREC) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -2063,7 +2198,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
     const int pipe = tid >> 8;
     const int pb = static_cast<int>(blockIdx.x) - NU;
     const int NQ = 2 * (static_cast<int>(gridDim.x) - NU);
-    split::producer(maps, p, sm + pipe * split::P_STRIDE, tmem + 256u * static_cast<uint32_t>(pipe), pipe,
+    split::producer<PRE>(maps, p, sm + pipe * split::P_STRIDE, tmem + 256u * static_cast<uint32_t>(pipe), pipe,
                     2 * pb + pipe, NQ, NU, NREC, flags);
   }
   tc_fence_before();
@@ -2141,15 +2276,20 @@ const DeviceInfo& device_info() {
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     d.coop = coop != 0;
-    if (cudaFuncSetAttribute(tc::kda_chunk_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::split::SMEM_ALLOC) == cudaSuccess) {
+    d.split_fits = true;
+    for (auto kern : {tc::kda_chunk_split_kernel<false>, tc::kda_chunk_split_kernel<true>}) {
       int blocks = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tc::kda_chunk_split_kernel, tc::split::NTHREADS,
-                                                        tc::split::SMEM_ALLOC) == cudaSuccess)
-        d.split_fits = blocks >= 1;
+      d.split_fits = d.split_fits &&
+                     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::split::SMEM_ALLOC) ==
+                         cudaSuccess &&
+                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, tc::split::NTHREADS,
+                                                                   tc::split::SMEM_ALLOC) == cudaSuccess &&
+                     blocks >= 1;
     }
-    d.fused_attr = cudaFuncSetAttribute(tc::kda_chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        tc::SMEM_ALLOC) == cudaSuccess;
+    d.fused_attr = true;
+    for (auto kern : {tc::kda_chunk_fused_kernel<false>, tc::kda_chunk_fused_kernel<true>})
+      d.fused_attr = d.fused_attr && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          tc::SMEM_ALLOC) == cudaSuccess;
     cudaGetLastError();
     known[dev] = true;
   }
@@ -2192,12 +2332,16 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!tc::make_map(&maps.o, p.out, tc::VD, p.HV, tokens)) return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel, maps, p, NU, nrec);
+    return p.prestage ? cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<true>, maps, p, NU, nrec)
+                      : cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<false>, maps, p, NU, nrec);
   }
   if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return cudaGetLastError();
   if (!dev.fused_attr) return cudaErrorInvalidConfiguration;
   dim3 grid(tc::NSLICE, p.HV, p.num_seqs);
-  tc::kda_chunk_fused_kernel<<<grid, tc::NTHREADS, tc::SMEM_ALLOC, stream>>>(maps, p);
+  if (p.prestage)
+    tc::kda_chunk_fused_kernel<true><<<grid, tc::NTHREADS, tc::SMEM_ALLOC, stream>>>(maps, p);
+  else
+    tc::kda_chunk_fused_kernel<false><<<grid, tc::NTHREADS, tc::SMEM_ALLOC, stream>>>(maps, p);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,14 @@ struct FwdParams {
   uint32_t* status;      // device status word
   uint8_t* ring;         // per-(sequence, value head) record ring (chunk kernel), or null
   unsigned long long wait_ns;  // limit of a bounded wait for work (drains have their own)
+  // Pre-stage (kda_chunk_fwd_gated): 0 = inputs used as given; 1 = bounded gate, 2 =
+  // softplus gate.  Then g_raw replaces g, beta holds raw values (sigmoid applied in
+  // the kernel) and q, k are L2-normalised per row in the kernel.
+  int prestage;
+  const uint16_t* g_raw;  // [tokens, HV, K] bf16
+  const float* A_log;     // [HV]
+  const float* dt_bias;   // [HV, K]
+  float lower_bound;      // bounded gate: g = lower_bound * sigmoid(exp(A_log) (g_raw + dt_bias))
   float scale;
   int T;                 // tokens per sequence (fixed length) or packed total
   int H, HV, K, V;

@@ -153,6 +153,76 @@ def make_inputs(B: int, T: int, H: int, HV: int, K: int, V: int, io_dtype: str =
         io_dtype=io_dtype)
 
 
+@dataclass
+class RawInputs:
+    """Raw projections for the forward with the pre-stage fused in."""
+    q: torch.Tensor          # [B, T, H, K] unnormalised
+    k: torch.Tensor
+    v: torch.Tensor
+    g_raw: torch.Tensor      # [B, T, HV, K] bf16 gate input
+    beta_raw: torch.Tensor   # [B, T, HV] fp32
+    A_log: torch.Tensor      # [HV] fp32
+    dt_bias: torch.Tensor    # [HV, K] fp32
+    scale: float
+    initial_state: torch.Tensor | None
+    cu_seqlens: torch.Tensor | None
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "RawInputs":
+        f = lambda t: None if t is None else t.to(device)
+        return RawInputs(f(self.q), f(self.k), f(self.v), f(self.g_raw), f(self.beta_raw), f(self.A_log),
+                         f(self.dt_bias), self.scale, f(self.initial_state), f(self.cu_seqlens), dict(self.meta))
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.cu_seqlens.numel() - 1) if self.cu_seqlens is not None else int(self.q.shape[0])
+
+    def tokens(self) -> int:
+        return int(self.q.shape[0] * self.q.shape[1])
+
+
+def make_raw_inputs(B: int, T: int, H: int, HV: int, K: int, V: int, seed: int = 0, init_state: bool = False,
+                    lengths=None, param_scale: float = 0.1) -> RawInputs:
+    """Raw projections (bf16 q, k, v and gate input) for the gated forward.  Recipe:
+    numpy PCG64 seeded with `seed`; draw order q, k, v, g_raw, beta_raw, A_log, dt_bias,
+    initial state.  q, k, v, g_raw ~ N(0, 1) (q and k NOT normalised: the pre-stage
+    does it), beta_raw ~ N(0, 1), A_log and dt_bias ~ param_scale * N(0, 1), initial
+    state 0.1 N(0, 1).  With the bounded gate and lower bound -5 this gives
+    g = -5 sigmoid(~N(0, 1)) per element."""
+    rng = np.random.default_rng(seed)
+    cu = None
+    if lengths is not None:
+        assert B == 1
+        lengths = np.asarray(lengths, dtype=np.int64)
+        cu = np.zeros(len(lengths) + 1, dtype=np.int64)
+        cu[1:] = np.cumsum(lengths)
+        T = int(cu[-1])
+    n_seq = len(lengths) if lengths is not None else B
+    q = rng.standard_normal((B, T, H, K), dtype=np.float32)
+    k = rng.standard_normal((B, T, H, K), dtype=np.float32)
+    v = rng.standard_normal((B, T, HV, V), dtype=np.float32)
+    g = rng.standard_normal((B, T, HV, K), dtype=np.float32)
+    beta = rng.standard_normal((B, T, HV), dtype=np.float32)
+    A_log = rng.standard_normal(HV, dtype=np.float32) * np.float32(param_scale)
+    dt = rng.standard_normal((HV, K), dtype=np.float32) * np.float32(param_scale)
+    s0 = rng.standard_normal((n_seq, HV, K, V), dtype=np.float32) * np.float32(0.1) if init_state else None
+    bf = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    return RawInputs(bf(q), bf(k), bf(v), bf(g), torch.from_numpy(beta), torch.from_numpy(A_log), torch.from_numpy(dt),
+                     float(K) ** -0.5, None if s0 is None else torch.from_numpy(s0),
+                     None if cu is None else torch.from_numpy(cu.astype(np.int32)))
+
+
+def workload_raw_inputs(index: int) -> RawInputs:
+    """Raw projections with the shapes of workload `index` (for the gated forward)."""
+    w = WORKLOADS[index]
+    lengths = None
+    if w.num_seqs:
+        lengths = varlen_lengths(np.random.default_rng(1000 + index), w.num_seqs, w.max_len)
+    x = make_raw_inputs(w.B, w.T, w.H, w.HV, w.K, w.V, seed=index, init_state=w.init_state, lengths=lengths)
+    x.meta["workload"] = w.name + "_gated"
+    return x
+
+
 def workload_inputs(index: int) -> Inputs:
     """Inputs of workload ``index`` (0..4), seeded with the index."""
     w = WORKLOADS[index]

@@ -135,3 +135,22 @@ def test_decode_validation_on_host(lib):
     assert call(ok, state=P(0x200000 * 6 + 4)) == 3                                # misaligned state
     assert call(ok, out=f[5]) == 1                                                 # out aliases the state
     assert call(_lib.KdaShape(0, 1, 2, 4, 128, 128, 0, _lib.KDA_BF16)) == 0         # no sequences: nothing to do
+
+
+def test_gated_validation_on_host(lib):
+    """kda_chunk_fwd_gated rejects a missing or malformed gate before touching CUDA."""
+    P = ctypes.c_void_p
+    f = [P(0x300000 * (i + 1)) for i in range(9)]
+    shape = _lib.KdaShape(1, 64, 2, 2, 128, 128, 0, _lib.KDA_BF16)
+
+    def call(gate):
+        return lib.kda_chunk_fwd_gated(ctypes.byref(shape), f[0], f[1], f[2], f[3], f[4], gate,
+                                       ctypes.c_float(0.088), None, None, f[5], f[6], f[7],
+                                       ctypes.c_size_t(1 << 30), None)
+
+    G = _lib.KdaGate
+    assert call(None) == 1
+    assert call(ctypes.byref(G(0, 0x400000, 0x500000, 0.0))) == 1      # bounded gate needs lower_bound < 0
+    assert call(ctypes.byref(G(7, 0x400000, 0x500000, -5.0))) == 1     # unknown gate kind
+    assert call(ctypes.byref(G(1, None, 0x500000, 0.0))) == 1          # A_log missing
+    assert call(ctypes.byref(G(1, 0x400000, 0x500008, 0.0))) == 3      # dt_bias not 16-byte aligned
