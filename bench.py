@@ -500,6 +500,85 @@ def run_decode(args):
     return 0
 
 
+TWOPASS_METRIC = ("KDA chunked fwd in two passes (state scan writing h[n], then the parallel output kernel) "
+                  "tokens/s on 1 GB300 (T=4096,H=32,K=V=128); % roofline")
+
+
+def run_twopass(args):
+    """One step = kda_chunk_states (the serial scan, writing the state entering every
+    chunk, bf16) + kda_chunk_output (every chunk's output from those states, in parallel)
+    over the headline workload.  Each pass is also timed on its own."""
+    import torch
+    import kimi_delta_attention_gb300 as kda
+    from kimi_delta_attention_gb300 import workloads as W
+    kda.build()
+    kda.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.WORKLOADS[args.workload]
+    host = W.workload_inputs(args.workload)
+    if host.cu_seqlens is not None:
+        raise SystemExit("the two-pass forward takes fixed-length workloads")
+    x = host.to(dev)
+    B, T, H, K = x.q.shape
+    HV, V = x.v.shape[2], x.v.shape[3]
+    h = torch.empty((B, HV, (T + 63) // 64, K, V), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((B, HV, K, V), dtype=torch.float32, device=dev)
+    out = torch.empty_like(x.v)
+    wsp = torch.empty(kda.kda_chunk_fwd_workspace_size(kda.make_shape(x.q, x.v)), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(256, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def states():
+        kda.kda_chunk_states(x.q, x.k, x.v, x.g, x.beta, initial_state=x.initial_state, h=h, final_state=fin,
+                             workspace=wsp, stream=stream.cuda_stream)
+
+    def output():
+        kda.kda_chunk_output(x.q, x.k, x.v, x.g, x.beta, h, x.scale, out=out, workspace=ws2, stream=stream.cuda_stream)
+
+    def timed(fns):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            for f in fns:
+                f()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    ms = timed([states, output])
+    sampler.stop()
+    ms_states, ms_output = timed([states]), timed([output])
+    alg = W.algorithmic_bytes(host, final_state=True)
+    h_bytes = h.numel() * 2
+    hbm_gbs, _, peak_src = load_peaks()
+    line = {
+        "impl": "kda_gb300", "metric": TWOPASS_METRIC, "value": host.tokens() / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "ms_states_pass": ms_states, "ms_output_pass": ms_output, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_dict(w, host, 1), h_bytes=h_bytes),
+        "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": alg / (ms * 1e-3) / 1e9 / hbm_gbs, "traffic": None,
+                     "kernel": "kda_chunk_*_kernel (state pass) + kda_chunk_output_kernel",
+                     "algorithmic_bytes_per_launch": alg,
+                     "note": "the forward's algorithmic bytes; the two passes also write and read h once and "
+                             "read the inputs twice", "peak_source": peak_src},
+        "clocks": sampler.summary(), "gpu_launches": 2 * args.steps,
+        "device_status": max(kda.kda_read_device_status(wsp), kda.kda_read_device_status(ws2)),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,7 +588,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gated", action="store_true",
                     help="raw bf16 inputs through kda_chunk_fwd_gated (pre-stage fused, bounded gate)")
-    ap.add_argument("--mode", default="forward", choices=["forward", "decode"],
+    ap.add_argument("--mode", default="forward", choices=["forward", "decode", "twopass"],
                     help="decode: time kda_decode (one token per sequence) instead of the chunked forward")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (0-4); 1, the headline, is the default bench line")
@@ -518,6 +597,8 @@ def main():
         return run_reference(args)
     if args.mode == "decode":
         return run_decode(args)
+    if args.mode == "twopass":
+        return run_twopass(args)
     return run_gpu(args)
 
 

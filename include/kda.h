@@ -156,6 +156,30 @@ KDA_API kda_status kda_chunk_fwd_gated(const kda_shape* shape, const void* q, co
                                        void* stream);
 
 /*
+ * The forward in two passes, through the per-chunk states.  The chunked form carries
+ * the state from chunk to chunk and, given the state entering a chunk, computes that
+ * chunk's output on its own (page "手撕KDA", section "1 Naive": the chunk loop; section
+ * 1.1, the C++ port, keeps the state entering every chunk):
+ *
+ *   kda_chunk_states: the serial state scan only.  h [B, HV, NT, K, V] bf16 receives
+ *     the state entering each chunk (NT = ceil(T / 64); h[.., 0] is the initial state),
+ *     final_state (optional) the state after the last token; no output.  Same
+ *     workspace as kda_chunk_fwd.  The states are also what a backward pass reads.
+ *   kda_chunk_output: o [B, T, HV, V] from h, every chunk in parallel
+ *     (o_n = qd_n h[n] + Aqk_n (U_n - W_n h[n])); workspace: the 256-byte status word.
+ *
+ * Both take bf16 I/O, K = V = 128 and fixed-length sequences (num_seqs = 0); other
+ * shapes return KDA_ERR_UNSUPPORTED.  kda_chunk_states_size gives the bytes of h.
+ */
+KDA_API size_t kda_chunk_states_size(const kda_shape* shape);
+KDA_API kda_status kda_chunk_states(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const float* initial_state, void* h,
+                                    float* final_state, void* workspace, size_t workspace_bytes, void* stream);
+KDA_API kda_status kda_chunk_output(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, float scale, const void* h, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Token-recurrent forward: the defining recurrence evaluated token by token on
  * CUDA cores in fp32 (same arguments and results as kda_chunk_fwd; its
  * workspace needs only the 256-byte status word).  Kept as the

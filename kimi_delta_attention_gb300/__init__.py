@@ -9,6 +9,8 @@ from ._lib import (  # noqa: F401
     KdaShape,
     kda_chunk_fwd,
     kda_chunk_fwd_gated,
+    kda_chunk_output,
+    kda_chunk_states,
     kda_chunk_fwd_static_scratch,
     kda_chunk_fwd_workspace_size,
     kda_chunk_size,

@@ -31,7 +31,8 @@ STATIC_SCRATCH_MAX_UNITS = 32
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
            "kda_read_device_status", "kda_status_string", "kda_chunk_size",
-           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode", "kda_chunk_fwd_gated")
+           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode", "kda_chunk_fwd_gated",
+           "kda_chunk_states_size", "kda_chunk_states", "kda_chunk_output")
 GATE_KINDS = {"bounded": 0, "softplus": 1}
 
 
@@ -90,6 +91,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_chunk_fwd_gated.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, ctypes.POINTER(KdaGate), F,
                                             P, P, P, P, P, S, P]
         lib.kda_chunk_fwd_gated.restype = I
+        lib.kda_chunk_states_size.argtypes = [ctypes.POINTER(KdaShape)]
+        lib.kda_chunk_states_size.restype = S
+        lib.kda_chunk_states.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, P, P, P, P, S, P]
+        lib.kda_chunk_states.restype = I
+        lib.kda_chunk_output.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, S, P]
+        lib.kda_chunk_output.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -304,3 +311,50 @@ def kda_chunk_fwd_gated(q, k, v, g_raw, beta_raw, A_log, dt_bias, gate="bounded"
             for t in made:
                 t.record_stream(other)
     return out, final_state
+
+
+def kda_chunk_states(q, k, v, g, beta, initial_state=None, h=None, final_state=None, output_final_state=True,
+                     workspace=None, stream=None):
+    """The state scan alone: h [B, HV, NT, K, V] bf16 (the state entering each chunk of 64
+    tokens) and the final state.  Fixed-length bf16, K = V = 128.  Returns (h, final_state)."""
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, (("initial_state", initial_state), ("h", h), ("final_state", final_state),
+                                      ("workspace", workspace)))
+    with torch.cuda.device(q.device):
+        shape = make_shape(q, v)
+        B, T, H, K = q.shape
+        HV, V = v.shape[2], v.shape[3]
+        if h is None:
+            h = torch.empty((B, HV, (T + 63) // 64, K, V), dtype=torch.bfloat16, device=q.device)
+        if final_state is None and output_final_state:
+            final_state = torch.empty((B, HV, K, V), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = torch.empty(kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device).cuda_stream
+        _check(lib.kda_chunk_states(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    _ptr(initial_state), _ptr(h), _ptr(final_state), _ptr(workspace),
+                                    ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                    ctypes.c_void_p(stream)))
+    return h, final_state
+
+
+def kda_chunk_output(q, k, v, g, beta, h, scale=None, out=None, workspace=None, stream=None):
+    """o of every chunk in parallel from the states h (as kda_chunk_states writes them)."""
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, (("h", h), ("out", out), ("workspace", workspace)))
+    with torch.cuda.device(q.device):
+        shape = make_shape(q, v)
+        if scale is None:
+            scale = q.shape[3] ** -0.5
+        if out is None:
+            out = torch.empty_like(v)
+        if workspace is None:
+            workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device).cuda_stream
+        _check(lib.kda_chunk_output(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    ctypes.c_float(scale), _ptr(h), _ptr(out), _ptr(workspace),
+                                    ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                    ctypes.c_void_p(stream)))
+    return out

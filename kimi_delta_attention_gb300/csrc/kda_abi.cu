@@ -15,6 +15,7 @@ bool chunk_tc_supported(const FwdParams& p, bool bf16);
 size_t chunk_tc_ring_bytes(int num_seqs, int HV);
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
 const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units);
+cudaError_t launch_chunk_output(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                           float* state, void* out, float scale, int B, int T, int H, int HV, int K, int V,
                           bool bf16, cudaStream_t stream);
@@ -247,6 +248,78 @@ kda_status kda_chunk_fwd_gated(const kda_shape* shape, const void* q, const void
   c.p.dt_bias = gate->dt_bias;
   c.p.lower_bound = gate->lower_bound;
   return kda::launch_chunk_tc_fwd(c.p, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t kda_chunk_states_size(const kda_shape* s) {
+  if (!s || s->B < 0 || s->T < 0 || s->HV < 1 || s->K < 1 || s->V < 1 || s->num_seqs != 0) return 0;
+  const size_t nt = (static_cast<size_t>(s->T) + 63) / 64;
+  return static_cast<size_t>(s->B) * s->HV * nt * s->K * s->V * 2;
+}
+
+namespace {
+// The state pass and the output kernel take fixed-length bf16 batches at K = V = 128.
+kda_status states_shape_ok(const kda_shape* s) {
+  if (!s) return KDA_ERR_INVALID_ARG;
+  if (s->num_seqs != 0) return KDA_ERR_UNSUPPORTED;
+  if (s->io_dtype != KDA_BF16 || s->K != 128 || s->V != 128) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+}  // namespace
+
+kda_status kda_chunk_states(const kda_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* initial_state, void* h, float* final_state,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  kda_status st = states_shape_ok(shape);
+  if (st != KDA_OK) return st;
+  if (!h && shape->B > 0 && shape->T > 0) return KDA_ERR_INVALID_ARG;
+  // h takes the place of the output in the common checks (alignment, overlaps at o's size),
+  // then is checked at its own size
+  Checked c;
+  st = validate(true, shape, q, k, v, g, beta, 1.f, initial_state, nullptr, h, final_state, workspace,
+                workspace_bytes, c);
+  if (st != KDA_OK) return st;
+  const size_t nh = kda_chunk_states_size(shape);
+  const size_t tokens = static_cast<size_t>(shape->B) * shape->T;
+  const size_t n_qk = tokens * shape->H * shape->K * 2, n_v = tokens * shape->HV * shape->V * 2;
+  const size_t n_g = tokens * shape->HV * shape->K * 4, n_b = tokens * shape->HV * 4;
+  const size_t n_s = static_cast<size_t>(shape->B) * shape->HV * shape->K * shape->V * 4;
+  const void* others[] = {q, k, v, g, beta, initial_state, final_state, workspace};
+  const size_t nothers[] = {n_qk, n_qk, n_v, n_g, n_b, n_s, n_s, workspace_bytes};
+  for (int i = 0; i < 8; ++i)
+    if (overlaps(h, nh, others[i], nothers[i])) return KDA_ERR_INVALID_ARG;
+  if (c.units == 0) return KDA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (tokens == 0) {  // no chunks: the final state is the initial one
+    c.p.out = nullptr;
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
+    return kda::launch_recurrent_fwd(c.p, true, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
+  if (!c.p.ring || !kda::chunk_tc_supported(c.p, c.bf16)) return KDA_ERR_UNSUPPORTED;
+  c.p.out = nullptr;
+  c.p.h = static_cast<uint16_t*>(h);
+  c.p.h_chunks = static_cast<int>((shape->T + 63) / 64);
+  return kda::launch_chunk_tc_fwd(c.p, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_chunk_output(const kda_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, const void* h, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  kda_status st = states_shape_ok(shape);
+  if (st != KDA_OK) return st;
+  Checked c;
+  st = validate(false, shape, q, k, v, g, beta, scale, nullptr, nullptr, out, nullptr, workspace, workspace_bytes, c);
+  if (st != KDA_OK) return st;
+  const size_t tokens = static_cast<size_t>(shape->B) * shape->T;
+  if (c.units == 0 || tokens == 0) return KDA_OK;
+  if (!h) return KDA_ERR_INVALID_ARG;
+  if (!aligned(h, 16)) return KDA_ERR_ALIGNMENT;
+  const size_t nh = kda_chunk_states_size(shape);
+  if (overlaps(h, nh, out, tokens * shape->HV * shape->V * 2) || overlaps(h, nh, workspace, workspace_bytes))
+    return KDA_ERR_INVALID_ARG;
+  if (!kda::chunk_tc_supported(c.p, c.bf16)) return KDA_ERR_UNSUPPORTED;
+  c.p.h = static_cast<uint16_t*>(const_cast<void*>(h));
+  c.p.h_chunks = static_cast<int>((shape->T + 63) / 64);
+  return kda::launch_chunk_output(c.p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,

@@ -41,6 +41,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -454,7 +455,7 @@ __device__ __forceinline__ void row_norms(const uint8_t* base, float* rn, int pt
 // (hq < 2) cB to the tiles, kr^T and (hq = 0) e^{g_last} into the record (krt_rec +
 // SW128 offset in the [128 x 64] kr^T tile, gam_rec), and qd either to the tile QDS
 // (QD_SMEM, for a bulk copy) or into the record (qd_rec + kb * qd_kb_stride + SW128 row
-// offset).  With NORM, k and q rows are first scaled by their rn[] entries (the
+// offset); without KR, kr^T and e^{g_last} are not written.  With NORM, k and q rows are first scaled by their rn[] entries (the
 // pre-stage's L2 normalisation).  Sets range_bad when this quarter decays faster
 // than the factors can represent.
 //
@@ -470,7 +471,7 @@ __device__ __forceinline__ void row_norms(const uint8_t* base, float* rn, int pt
 // swizzle (16-byte chunk index XOR row % 8) is an XOR on address bits 4-6 that commutes
 // with adding the row and the tile offsets; one 32-bit shared address per row serves
 // all tiles.
-template <bool QD_SMEM, bool NORM>
+template <bool QD_SMEM, bool NORM, bool KR = true>
 __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, const float2 (&g)[16], int dp, int hq,
                                             int rows, float scale, uint8_t* qd_rec, uint32_t qd_kb_stride,
                                             uint8_t* krt_rec, float* gam_rec, const float* rn, bool& range_bad) {
@@ -490,7 +491,7 @@ __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, co
     es[e] = ex2_approx(sh);
     fa[e] = even ? ex2_approx(-sh) : 1.f;                       // kA, qA
     fb[e] = ex2_approx(hq == 0 ? s[1] + s[2] : s[2]);           // cB (hq < 2)
-    if (hq == 0) gam_rec[2 * dp + e] = ex2_approx(all);
+    if (KR && hq == 0) gam_rec[2 * dp + e] = ex2_approx(all);
   }
   // the per-dim constants as packed pairs
   const unsigned long long CD = f2u(c_d[0], c_d[1]), CR = f2u(c_r[0], c_r[1]), ES = f2u(es[0], es[1]),
@@ -556,7 +557,7 @@ __device__ __forceinline__ void elementwise(uint8_t* base, const float* gsum, co
     } else {
       kre = krp;
     }
-    if ((i & 7) == 7)  // tokens r0 + i - 7 .. r0 + i
+    if (KR && (i & 7) == 7)  // tokens r0 + i - 7 .. r0 + i
 #pragma unroll
       for (int e = 0; e < 2; ++e)
         __stcg(reinterpret_cast<uint4*>(krt_rec + sw128_offset(2 * dp + e, r0 + (i & 8), 128)),
@@ -1104,6 +1105,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       if (qw < 2) return;  // only the warps of lane quadrants 2 and 3 read o
       if (mbar_wait(&bars[B_C], m & 1, p.wait_ns)) ++c_done;  // else drained below
       else timeout();
+      if (p.h) return;  // state pass: no output
       __syncwarp();
       tc_fence_after();
       float orr[32];
@@ -1128,10 +1130,11 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       constexpr uint32_t idesc = idesc_f16kind(128, VS) | IDESC_B_MN_MAJOR;
       // the 128 rows starting 64 rows before Aqk (kr^T rows 64..127, then Aqk): Aqk v_new
       // lands in lanes 64-127 next to qd S; lanes 0-63 (X, consumed) take a harmless product
+      if (!p.h)  // (the state pass keeps the commit, so the barrier's phases stay in step)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma_f16(tmem + TM_A0 + 32 * sc, d128(soc + R_AQK - 8192 + ks * 32),
-                 D_VNT + ((sc * SSLOT + ks * 1024) >> 4), idesc, 1u);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16(tmem + TM_A0 + 32 * sc, d128(soc + R_AQK - 8192 + ks * 32),
+                   D_VNT + ((sc * SSLOT + ks * 1024) >> 4), idesc, 1u);
       umma_commit(&bars[B_C]);
       ++c_issued;
     };
@@ -1141,6 +1144,14 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       const int s = m & 1;
       const uint32_t so = OFF_SLOT + s * SSLOT;  // this chunk's record slot
       uint8_t* slot = sm + so;
+      if (p.h) {  // state pass: row d, columns v0 .. v0 + 31 of the state entering chunk m
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.h + ((static_cast<size_t>(seq) * HV + hv) * p.h_chunks + m) * KD * VD + static_cast<size_t>(d) * VD + v0);
+#pragma unroll
+        for (int j8 = 0; j8 < VS / 8; ++j8)
+          dst[j8] = make_uint4(pack2(st[8 * j8], st[8 * j8 + 1]), pack2(st[8 * j8 + 2], st[8 * j8 + 3]),
+                               pack2(st[8 * j8 + 4], st[8 * j8 + 5]), pack2(st[8 * j8 + 6], st[8 * j8 + 7]));
+      }
       if (qt == kLoader && !failed) pump_loads(m + 1, m);
       PROF(6);
       __syncwarp();
@@ -1977,7 +1988,8 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         umma_ts_chain<4>(tmem + TS, tmem + TVN, d128(sbb + SR_KRT), kstep, idesc_f16kind(128, 128), 1u);
         umma_commit_warp(&bars[CB_B]);
         ++b_issued;
-        umma_ts_chain<4>(tmem + TXO + 128 * s, tmem + TVN, d128(sbb + SR_AQK), kstep, idesc_f16kind(128, 64), 1u);
+        if (!p.h)  // (the state pass keeps the commit, so the barrier's phases stay in step)
+          umma_ts_chain<4>(tmem + TXO + 128 * s, tmem + TVN, d128(sbb + SR_AQK), kstep, idesc_f16kind(128, 64), 1u);
         umma_commit_warp(&bars[CB_C + s]);
         ++c_issued;
         if (lane == 0) st_relaxed_gpu(consumed, static_cast<uint32_t>(m + 1));  // record m is in shared memory
@@ -2029,6 +2041,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     //      then the record copies ----
     auto emit_o = [&](int mc) {
       wait(&bars[CB_C + (mc & 1)], (mc >> 1) & 1, 11, mc);
+      if (p.h) return;  // state pass: no output (every helper returns here alike)
       __syncwarp();
       tc_fence_after();
       const uint32_t tot = TXO + 128 * (mc & 1);  // O^T of this chunk
@@ -2087,6 +2100,14 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
           pump_b(m + 1);
         }
         wait(&bars[CB_FULL + m % 3], (m / 3) & 1, 4, m);
+        // state pass: the bf16 copy of S^T (the state entering chunk m, as the chain's MMAs
+        // read it; rewritten only by this chunk's state copy, after the arrival below),
+        // key dims 64 h + [0, 64) of value column vcol as 32 bf16 pairs along k
+        uint32_t hs[32];
+        if (p.h) {
+          tmem_ld32(tl + TSB + 32 * h, reinterpret_cast<float(&)[32]>(hs));
+          tmem_ld_wait();
+        }
         {
           const float* gam = reinterpret_cast<const float*>(sm + sa + SR_GAM) + 64 * h;
 #pragma unroll
@@ -2109,6 +2130,20 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
         tc_fence_before();
         named_bar_arrive(NB_SCALED, NTHREADS);
         STAMP(1);
+        if (p.h) {
+          // h[m] rows k = 64 h + 2c, 2c + 1: lane pairs (v, v + 1) swap their words, then the
+          // even lane stores (S[2c][v], S[2c][v + 1]) and the odd lane (S[2c+1][v - 1], S[2c+1][v])
+          // (64 contiguous bytes per half-warp and store)
+          const bool odd = lane & 1;
+          uint16_t* hb = p.h + ((static_cast<size_t>(seq) * HV + hv) * p.h_chunks + m) * KD * VD + (vcol & ~1);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t t = __shfl_xor_sync(0xFFFFFFFFu, hs[c], 1);
+            const int kk = 64 * h + 2 * c + (odd ? 1 : 0);
+            *reinterpret_cast<uint32_t*>(hb + static_cast<size_t>(kk) * VD) =
+                odd ? __byte_perm(t, hs[c], 0x7632) : __byte_perm(hs[c], t, 0x5410);
+          }
+        }
       }
       if (m > 0) {
         if (m == NT) role_sync(NB_HELP, 256);  // the storer's last wait precedes the staging writes
@@ -2171,7 +2206,7 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
       for (int i = 0; i < split::kChainBars; ++i)  // CB_FULL[3], CB_B, CB_C[2], CB_AB[2], CB_DRAIN
         mbar_init(&cb[i], i == split::CB_AB || i == split::CB_AB + 1 ? 2 : 1);
-      tma_prefetch_desc(&maps.o);
+      if (!p.h) tma_prefetch_desc(&maps.o);
     } else {
       for (int pp = 0; pp < 2; ++pp) {
         uint64_t* pb = reinterpret_cast<uint64_t*>(sm + pp * split::P_STRIDE + split::P_BAR);
@@ -2207,6 +2242,282 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ======================================================================
+// Parallel output kernel: o of every chunk from the state entering it.
+//
+// With h[n] (the state entering chunk n, from the state pass) the chunks no longer
+// depend on each other:  o_n = qd_n h[n] + Aqk_n (U_n - W_n h[n])  (the a8 output of the
+// chunked form with its a7 v_new, page "手撕KDA", section "1 Naive"; the per-chunk
+// states of the C++ port in section 1.1).  One CTA of 8 warps per (chunk, value head,
+// sequence), two per SM: it prepares the chunk as a producer pipeline does (the prep::
+// steps: elementwise pass, the L/Aqk product, the inverse, W = A kd and U = A v), loads
+// h[n] (bf16, MN-major) over the stacked tile those steps no longer need, and runs
+//   X = W h[n] (M = 64, N = 128, K = 128),  v_new = U - X (bf16, over the raw v tile),
+//   O = qd h[n] + Aqk v_new (M = 64, N = 128, K = 128 then 64)
+// with fp32 accumulators in TMEM.  Waits are bounded (p.wait_ns); a timed-out wait
+// sets kStatusTimeout, later products are not issued, and what was issued is drained.
+// ======================================================================
+namespace outk {
+constexpr int NTHREADS = 256;
+constexpr uint32_t O_BETA = prep::QDS + 16384, O_GSUM = O_BETA + 256, O_BAR = O_GSUM + 2048;
+constexpr uint32_t O_MISC = O_BAR + 64, SMEM_BYTES = O_MISC + 64, SMEM_ALLOC = SMEM_BYTES + 1024;
+static_assert(2 * SMEM_ALLOC <= 232448, "two output CTAs per SM");
+constexpr int OB_RAW = 0, OB_MMA = 1, OB_H = 2;
+constexpr uint32_t TM_W = 0, TM_U = 128, TM_X = 0, TM_O = 128, TMEM_COLS = 256;
+constexpr uint32_t H_TX = 32768;
+
+struct Maps {
+  CUtensorMap q32, k32, v;  // as the chunk kernels'
+  CUtensorMap h;            // h as [rows of 128 value columns], (64, 128) boxes
+};
+}  // namespace outk
+
+__global__ void __launch_bounds__(outk::NTHREADS, 2)
+kda_chunk_output_kernel(const __grid_constant__ outk::Maps maps, const FwdParams p) {
+  using namespace outk;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + O_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + O_MISC);
+  float* beta_s = reinterpret_cast<float*>(sm + O_BETA);
+  float* gsum = reinterpret_cast<float*>(sm + O_GSUM);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pt = tid, dp = pt & 63, hq = pt >> 6, quad = warp & 3, cpart = warp >> 2;
+  const int m = blockIdx.x, hv = blockIdx.y, seq = blockIdx.z;
+  const int HV = p.HV, hk = hv / (HV / p.H);
+  const long tok0 = static_cast<long>(seq) * p.T + static_cast<long>(m) * C;
+  const int rows = min(C, p.T - m * C);
+
+  if (tid == 0) {
+    mbar_init(&bars[OB_RAW], 1);
+    mbar_init(&bars[OB_MMA], 1);
+    mbar_init(&bars[OB_H], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, outk::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sb = smem_u32(sm);
+  const uint64_t D_PREP = sdesc_sw128(sb);
+  auto d128 = [&](uint32_t off) { return D_PREP + (off >> 4); };
+  const uint64_t D_KD_MN = sdesc(sb + prep::KDT, 8192, 1024, 2);
+  const uint64_t D_V_MN = sdesc(sb + prep::VRAW, 8192, 1024, 2);  // raw v, then v_new
+  const uint64_t D_H_MN = sdesc(sb + prep::QK, 16384, 1024, 2);   // h[n]: key dims as K, value columns as N
+  bool failed = false, raw_issued = false, h_issued = false;
+  uint32_t mma_issued = 0, mma_done = 0;
+  auto mma_wait = [&]() {  // all threads: the products issued so far have completed
+    if (!failed) {
+      if (mbar_wait(&bars[OB_MMA], mma_done & 1, p.wait_ns)) ++mma_done;
+      else { failed = true; atomicOr(p.status, kStatusTimeout); }
+    }
+    tc_fence_after();
+  };
+
+  // ---- 1. raw tiles (TMA), g and beta (registers) ----
+  if (tid == 0) {
+    prep::issue_raw(sm, &maps.q32, &maps.k32, &maps.v, &bars[OB_RAW], hk, hv, static_cast<int>(tok0));
+    raw_issued = true;
+  }
+  float2 g[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int c = 16 * hq + i;
+    g[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(tok0 + c) * HV + hv) * KD) + dp)
+                      : make_float2(0.f, 0.f);
+  }
+  if (pt < C) beta_s[pt] = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(tok0 + pt) * HV + hv) : 0.f;
+  {
+    float2 qsum = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      qsum.x += g[i].x;
+      qsum.y += g[i].y;
+    }
+    reinterpret_cast<float2*>(gsum + hq * KD)[dp] = qsum;
+  }
+  if (!mbar_wait(&bars[OB_RAW], 0, p.wait_ns)) {
+    failed = true;
+    atomicOr(p.status, kStatusTimeout);
+  }
+  failed = __syncthreads_or(failed);
+
+  // ---- 2. elementwise pass (qd to its tile; no record) ----
+  bool range_bad = false;
+  if (!failed)
+    prep::elementwise<true, false, false>(sm, gsum, g, dp, hq, rows, p.scale, sm, 0, sm, reinterpret_cast<float*>(sm), nullptr,
+                                          range_bad);
+  if (range_bad) atomicOr(p.status, kStatusRange);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- 3. L and Aqk; readout ----
+  if (warp == 0 && !failed) {
+    prep::issue_lqk(tmem, D_PREP);
+    umma_commit_warp(&bars[OB_MMA]);
+    ++mma_issued;
+  }
+  mma_wait();
+  if (!failed) prep::readout_lqk(sm, tmem, beta_s, quad, cpart, lane);
+  tc_fence_before();
+  fence_proxy_async_smem();
+  failed = __syncthreads_or(failed);
+
+  // ---- 4. T = (I + M)^{-1}, A = T Diag(beta) ----
+  if (!failed) prep::inverse_diag_blocks(sm, beta_s, warp, pt, lane);
+  __syncthreads();
+  if (!failed && warp < 3) inverse_block_columns(reinterpret_cast<float*>(sm + prep::MB), beta_s, sm + prep::AMAT, warp, lane);
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ---- 5. W = A kd, U = A v ----
+  if (tid == 0 && !failed) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t ad = d128(prep::AMAT + ks * 32);
+      umma_f16(tmem + outk::TM_W, ad, D_KD_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+      umma_f16(tmem + outk::TM_U, ad, D_V_MN + ((ks * 2048) >> 4), idesc, ks != 0);
+    }
+    umma_commit(&bars[OB_MMA]);
+    ++mma_issued;
+  }
+  mma_wait();
+  // h[n] over the stacked tile (M and A are no longer read)
+  if (tid == 0 && !failed) {
+    const int hrow = ((seq * HV + hv) * p.h_chunks + m) * KD;
+    mbar_arrive_expect_tx(&bars[OB_H], H_TX);
+    tma_load_2d(sm + prep::QK, &maps.h, &bars[OB_H], 0, hrow);
+    tma_load_2d(sm + prep::QK + 16384, &maps.h, &bars[OB_H], 64, hrow);
+    h_issued = true;
+  }
+  // W -> bf16 K-major tile over kd (the A operand of X = W h)
+  if (!failed) {
+    const int i = 16 * quad + (lane & 15);
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      float r[32];
+      tmem_ld32(tmem_addr(tmem, 32 * quad, outk::TM_W + 64 * cpart + 32 * q2), r);
+      tmem_ld_wait();
+      if (lane < 16) {
+        const int c0 = 64 * cpart + 32 * q2;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8)
+          st_v4(sm + prep::KDT + sw128_offset(i, c0 + 8 * j8, 64), pack2(r[8 * j8], r[8 * j8 + 1]),
+                pack2(r[8 * j8 + 2], r[8 * j8 + 3]), pack2(r[8 * j8 + 4], r[8 * j8 + 5]),
+                pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
+      }
+    }
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ---- 6. X = W h[n] ----
+  if (!failed && h_issued && !mbar_wait(&bars[OB_H], 0, p.wait_ns)) {
+    failed = true;
+    atomicOr(p.status, kStatusTimeout);
+  }
+  if (tid == 0 && !failed) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_f16(tmem + outk::TM_X, d128(prep::KDT + kb * 8192 + ks * 32), D_H_MN + (((kb * 4 + ks) * 2048) >> 4), idesc,
+                 (kb | ks) != 0);
+    umma_commit(&bars[OB_MMA]);
+    ++mma_issued;
+  }
+  failed = __syncthreads_or(failed);
+  mma_wait();
+
+  // ---- 7. v_new = U - X as bf16 over the raw v tile (MN-major: rows = tokens) ----
+  if (!failed) {
+    const int i = 16 * quad + (lane & 15);
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int c0 = 64 * cpart + 32 * q2;
+      float ur[32], xr[32];
+      tmem_ld32(tmem_addr(tmem, 32 * quad, outk::TM_U + c0), ur);
+      tmem_ld32(tmem_addr(tmem, 32 * quad, outk::TM_X + c0), xr);
+      tmem_ld_wait();
+      if (lane < 16) {
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          const int c = c0 + 8 * j8;
+          st_v4(sm + prep::VRAW + (c >> 6) * 8192 + sw128_offset(i, c & 63, 64),
+                pack2(ur[8 * j8] - xr[8 * j8], ur[8 * j8 + 1] - xr[8 * j8 + 1]),
+                pack2(ur[8 * j8 + 2] - xr[8 * j8 + 2], ur[8 * j8 + 3] - xr[8 * j8 + 3]),
+                pack2(ur[8 * j8 + 4] - xr[8 * j8 + 4], ur[8 * j8 + 5] - xr[8 * j8 + 5]),
+                pack2(ur[8 * j8 + 6] - xr[8 * j8 + 6], ur[8 * j8 + 7] - xr[8 * j8 + 7]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ---- 8. O = qd h[n] + Aqk v_new (over U's columns, read by now) ----
+  if (tid == 0 && !failed) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_f16kind(64, 128) | IDESC_B_MN_MAJOR;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_f16(tmem + outk::TM_O, d128(prep::QDS + kb * 8192 + ks * 32), D_H_MN + (((kb * 4 + ks) * 2048) >> 4), idesc,
+                 (kb | ks) != 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      umma_f16(tmem + outk::TM_O, d128(prep::AQK_STG + ks * 32), D_V_MN + ((ks * 2048) >> 4), idesc, 1u);
+    umma_commit(&bars[OB_MMA]);
+    ++mma_issued;
+  }
+  mma_wait();
+
+  // ---- 9. o rows (bf16) ----
+  if (!failed) {
+    const int i = 16 * quad + (lane & 15);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int c0 = 64 * cpart + 32 * q2;
+      float r[32];
+      tmem_ld32(tmem_addr(tmem, 32 * quad, outk::TM_O + c0), r);
+      tmem_ld_wait();
+      if (lane < 16 && i < rows) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok0 + i) * HV + hv) * VD + c0);
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8)
+          dst[j8] = make_uint4(pack2(r[8 * j8], r[8 * j8 + 1]), pack2(r[8 * j8 + 2], r[8 * j8 + 3]),
+                               pack2(r[8 * j8 + 4], r[8 * j8 + 5]), pack2(r[8 * j8 + 6], r[8 * j8 + 7]));
+      }
+    }
+  }
+
+  // drain what was issued before releasing the memory it touches
+  if (tid == 0) {
+    if (raw_issued && !mbar_wait(&bars[OB_RAW], 0, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    if (h_issued && !mbar_wait(&bars[OB_H], 0, DRAIN_LIMIT_NS)) atomicOr(p.status, kStatusTimeout);
+    if (mma_issued > mma_done && !mbar_wait(&bars[OB_MMA], (mma_issued - 1) & 1, DRAIN_LIMIT_NS))
+      atomicOr(p.status, kStatusTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, outk::TMEM_COLS);
+}
+
 // ------------------------------------------------------------------ host ----
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -2235,9 +2546,51 @@ bool make_map(CUtensorMap* m, const void* base, int dim, int heads, long tokens,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over h as rows of 128 bf16 value columns, (64, 128) boxes, 128-byte swizzle.
+bool make_map_h(CUtensorMap* m, const void* base, long rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(VD), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(VD) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 
 static_assert(static_cast<size_t>(tc::RING) * tc::GSLOT == kRingBytesPerUnit, "ring layout");
+
+// The parallel output kernel: one CTA per (chunk, value head, sequence); fixed-length
+// sequences (p.cu == nullptr), p.h holding p.h_chunks states per (sequence, value head).
+cudaError_t launch_chunk_output(const FwdParams& p, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && !attr[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(tc::kda_chunk_output_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::outk::SMEM_ALLOC);
+      if (e != cudaSuccess) return e;
+      attr[dev] = true;
+    }
+  }
+  const long tokens = static_cast<long>(p.num_seqs) * p.T;
+  tc::outk::Maps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if (!tc::make_map(&maps.q32, p.q, tc::KD, p.H, tokens, 32) || !tc::make_map(&maps.k32, p.k, tc::KD, p.H, tokens, 32) ||
+      !tc::make_map(&maps.v, p.v, tc::VD, p.HV, tokens) ||
+      !tc::make_map_h(&maps.h, p.h, static_cast<long>(p.num_seqs) * p.HV * p.h_chunks * tc::KD))
+    return cudaErrorInvalidValue;
+  if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return cudaGetLastError();
+  const dim3 grid(p.h_chunks, p.HV, p.num_seqs);
+  tc::kda_chunk_output_kernel<<<grid, tc::outk::NTHREADS, tc::outk::SMEM_ALLOC, stream>>>(maps, p);
+  return cudaGetLastError();
+}
 
 size_t chunk_tc_ring_bytes(int num_seqs, int HV) {
   return static_cast<size_t>(num_seqs) * HV * tc::RING * tc::GSLOT;
@@ -2310,6 +2663,7 @@ bool use_split_kernel(int NU) {
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
   const long tokens = p.cu ? static_cast<long>(p.T) : static_cast<long>(p.num_seqs) * p.T;
   tc::Maps maps;
+  std::memset(&maps, 0, sizeof(maps));
   if (!tc::make_map(&maps.q32, p.q, tc::KD, p.H, tokens, 32) || !tc::make_map(&maps.k32, p.k, tc::KD, p.H, tokens, 32) ||
       !tc::make_map(&maps.v, p.v, tc::VD, p.HV, tokens))
     return cudaErrorInvalidValue;
@@ -2331,7 +2685,7 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!tc::make_map(&maps.o, p.out, tc::VD, p.HV, tokens)) return cudaErrorInvalidValue;
+    if (!p.h && !tc::make_map(&maps.o, p.out, tc::VD, p.HV, tokens)) return cudaErrorInvalidValue;
     return p.prestage ? cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<true>, maps, p, NU, nrec)
                       : cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<false>, maps, p, NU, nrec);
   }

@@ -47,6 +47,10 @@ struct FwdParams {
   const float* A_log;     // [HV]
   const float* dt_bias;   // [HV, K]
   float lower_bound;      // bounded gate: g = lower_bound * sigmoid(exp(A_log) (g_raw + dt_bias))
+  // State pass (kda_chunk_states): when h is set, the chains write the state entering
+  // every chunk (bf16 [NS, HV, h_chunks, K, V]) and no output.
+  uint16_t* h;
+  int h_chunks;
   float scale;
   int T;                 // tokens per sequence (fixed length) or packed total
   int H, HV, K, V;
