@@ -17,6 +17,9 @@ Forms
     section "1 Naive").
 ``chunked``: the chunked WY/UT evaluation in the order of that listing, for
     any chunk size.
+``backward``: the gradients of sum <do, o> + <dS_final, S_final> with respect to
+    q, k, v, g, beta and the initial state, by reverse mode through the token
+    recurrence (the forward re-run with every state kept).
 ``prestage`` / ``forward_gated``: the activations applied to raw projections
     before the forward (q/k L2 normalisation with eps 1e-6, the bounded gate
     lower_bound * sigmoid(exp(A_log) (g_raw + dt_bias)) or the softplus gate
@@ -74,6 +77,11 @@ def _load():
             lib.kda_oracle_prestage.argtypes = [ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 P, P, P, P, P, P, ctypes.c_int, ctypes.c_double, P, P, P, P]
             lib.kda_oracle_prestage.restype = None
+            lib.kda_oracle_unit_backward.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                P, ctypes.c_long, P, ctypes.c_long, P, ctypes.c_long, P, ctypes.c_long, P, ctypes.c_long,
+                ctypes.c_double, P, P, P, ctypes.c_long, P, P, P, P, P, P]
+            lib.kda_oracle_unit_backward.restype = None
             _lib = lib
     return _lib
 
@@ -194,3 +202,48 @@ def forward_gated(q_raw, k_raw, v, g_raw, beta_raw, A_log, dt_bias, scale, gate:
     q, k, g, beta = prestage(q_raw, k_raw, g_raw, beta_raw, A_log, dt_bias, gate, lower_bound)
     return forward(q, k, v, g, beta, scale, initial_state=initial_state, cu_seqlens=cu_seqlens, form=form,
                    chunk=chunk, nthreads=nthreads)
+
+
+def backward(q, k, v, g, beta, scale, do, d_final_state=None, initial_state=None, cu_seqlens=None):
+    """Gradients of sum_t <do_t, o_t> + <d_final_state, S_final> (see kda_oracle_unit_backward).
+    Shapes as forward(); do [B, T, HV, V]; d_final_state [NS, HV, K, V] or None.  dq and dk
+    of a key head sum the contributions of the value heads that share it.  Returns
+    (dq [B,T,H,K], dk [B,T,H,K], dv [B,T,HV,V], dg [B,T,HV,K], dbeta [B,T,HV],
+    d_initial_state [NS,HV,K,V]), all float64."""
+    q, k, v, g, beta, do = (_f32(x) for x in (q, k, v, g, beta, do))
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    G = HV // H
+    seqs = _seq_bounds(B, T, cu_seqlens)
+    qf, kf, vf, gf, bf, dof = (a.reshape((B * T,) + a.shape[2:]) for a in (q, k, v, g, beta, do))
+    dq = np.zeros((B * T, H, K))
+    dk = np.zeros((B * T, H, K))
+    dv = np.zeros((B * T, HV, V))
+    dg = np.zeros((B * T, HV, K))
+    db = np.zeros((B * T, HV))
+    ds0 = np.zeros((len(seqs), HV, K, V))
+    lib = _load()
+    for s, (t0, L) in enumerate(seqs):
+        for h in range(HV):
+            hk = h // G
+            s0 = None if initial_state is None else np.ascontiguousarray(np.asarray(initial_state)[s, h], dtype=np.float64)
+            dfin = None if d_final_state is None else np.ascontiguousarray(np.asarray(d_final_state)[s, h], dtype=np.float64)
+            do_u = np.ascontiguousarray(dof[t0:t0 + L, h], dtype=np.float64)
+            dq_u, dk_u, dv_u = np.zeros((L, K)), np.zeros((L, K)), np.zeros((L, V))
+            dg_u, db_u, ds_u = np.zeros((L, K)), np.zeros(L), np.zeros((K, V))
+            if L:
+                lib.kda_oracle_unit_backward(
+                    L, K, V, _ptr(np.ascontiguousarray(qf[t0:t0 + L, hk])), K, _ptr(np.ascontiguousarray(kf[t0:t0 + L, hk])), K,
+                    _ptr(np.ascontiguousarray(vf[t0:t0 + L, h])), V, _ptr(np.ascontiguousarray(gf[t0:t0 + L, h])), K,
+                    _ptr(np.ascontiguousarray(bf[t0:t0 + L, h])), 1, float(scale), _ptr(s0), _ptr(dfin), _ptr(do_u), V,
+                    _ptr(dq_u), _ptr(dk_u), _ptr(dv_u), _ptr(dg_u), _ptr(db_u), _ptr(ds_u))
+            else:
+                ds_u = np.zeros((K, V)) if dfin is None else dfin.copy()
+            dq[t0:t0 + L, hk] += dq_u
+            dk[t0:t0 + L, hk] += dk_u
+            dv[t0:t0 + L, h] = dv_u
+            dg[t0:t0 + L, h] = dg_u
+            db[t0:t0 + L, h] = db_u
+            ds0[s, h] = ds_u
+    r = lambda a: a.reshape((B, T) + a.shape[1:])
+    return r(dq), r(dk), r(dv), r(dg), r(db), ds0

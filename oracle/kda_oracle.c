@@ -395,3 +395,108 @@ void kda_oracle_prestage(long n_tok, int H, int HV, int K,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward of the recurrence (reverse mode).                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Gradients of one unit's token recurrence (1) with respect to its inputs, for the
+ * loss sum_t <do_t, o_t> + <dS_final, S_len>.  The forward is re-run and every state
+ * kept; then, from the last token back, with Sp the state before token t,
+ * P = Diag(e^{g_t}) Sp, u = P^T k, r = v - u and S = P + beta k r^T:
+ *     dq_t   = scale S do_t                          (o_t = scale S^T q_t)
+ *     dS    += scale q_t do_t^T
+ *     dbeta_t = k^T dS r,     dr = beta dS^T k,      dv_t = dr
+ *     dk_t   = beta dS r - P dr                       (through r and through u = P^T k)
+ *     dP     = dS - k dr^T,   dg_t,i = sum_j dP_ij P_ij,   dS <- Diag(e^{g_t}) dP
+ * and dS after the first token is the initial state's gradient.  The pages' backward
+ * ("手撕KDA", section 2, backward_bh; section 4) works on the chunked form; this is the
+ * same derivative taken through the recurrence that form evaluates.
+ * s0, dfinal: K*V (NULL: zeros).  do_: len rows of V.  Outputs are written (dq, dk per
+ * token of this unit: the caller sums over value heads that share a key head).
+ */
+void kda_oracle_unit_backward(int len, int K, int V,
+                              const float* q, long q_rs, const float* k, long k_rs,
+                              const float* v, long v_rs, const float* g, long g_rs,
+                              const float* beta, long beta_rs, double scale,
+                              const double* s0, const double* dfinal, const double* do_, long do_rs,
+                              double* dq, double* dk, double* dv, double* dg, double* dbeta, double* ds0)
+{
+    const size_t KV = (size_t)K * V;
+    double* S = (double*)calloc((size_t)(len + 1) * KV, sizeof(double));
+    double* dS = (double*)calloc(KV, sizeof(double));
+    double* P = (double*)malloc(KV * sizeof(double));
+    double* r = (double*)malloc((size_t)V * sizeof(double));
+    double* dr = (double*)malloc((size_t)V * sizeof(double));
+    if (s0) memcpy(S, s0, KV * sizeof(double));
+    for (int t = 0; t < len; ++t) {   /* forward, keeping every state */
+        const double* Sp = S + (size_t)t * KV;
+        double* Sn = S + (size_t)(t + 1) * KV;
+        const float* kt = k + (long)t * k_rs;
+        const float* vt = v + (long)t * v_rs;
+        const float* gt = g + (long)t * g_rs;
+        const double bt = (double)beta[(long)t * beta_rs];
+        for (int i = 0; i < K; ++i)
+            for (int j = 0; j < V; ++j) Sn[(size_t)i * V + j] = exp((double)gt[i]) * Sp[(size_t)i * V + j];
+        for (int j = 0; j < V; ++j) {
+            double u = 0.0;
+            for (int i = 0; i < K; ++i) u += Sn[(size_t)i * V + j] * (double)kt[i];
+            r[j] = (double)vt[j] - u;
+        }
+        for (int i = 0; i < K; ++i)
+            for (int j = 0; j < V; ++j) Sn[(size_t)i * V + j] += bt * (double)kt[i] * r[j];
+    }
+    if (dfinal) memcpy(dS, dfinal, KV * sizeof(double));
+    for (int t = len - 1; t >= 0; --t) {
+        const double* Sp = S + (size_t)t * KV;
+        const double* St = S + (size_t)(t + 1) * KV;
+        const float* qt = q + (long)t * q_rs;
+        const float* kt = k + (long)t * k_rs;
+        const float* vt = v + (long)t * v_rs;
+        const float* gt = g + (long)t * g_rs;
+        const double bt = (double)beta[(long)t * beta_rs];
+        const double* dot = do_ + (long)t * do_rs;
+        for (int i = 0; i < K; ++i) {
+            const double e = exp((double)gt[i]);
+            for (int j = 0; j < V; ++j) P[(size_t)i * V + j] = e * Sp[(size_t)i * V + j];
+        }
+        for (int j = 0; j < V; ++j) {
+            double u = 0.0;
+            for (int i = 0; i < K; ++i) u += P[(size_t)i * V + j] * (double)kt[i];
+            r[j] = (double)vt[j] - u;
+        }
+        for (int i = 0; i < K; ++i) {   /* dq = scale S do; then the output's share of dS */
+            double a = 0.0;
+            for (int j = 0; j < V; ++j) a += St[(size_t)i * V + j] * dot[j];
+            dq[(long)t * K + i] = scale * a;
+            for (int j = 0; j < V; ++j) dS[(size_t)i * V + j] += scale * (double)qt[i] * dot[j];
+        }
+        double db = 0.0;
+        for (int j = 0; j < V; ++j) {
+            double a = 0.0;
+            for (int i = 0; i < K; ++i) a += dS[(size_t)i * V + j] * (double)kt[i];
+            dr[j] = bt * a;
+            db += a * r[j];
+            dv[(long)t * V + j] = dr[j];
+        }
+        dbeta[t] = db;
+        for (int i = 0; i < K; ++i) {
+            double a = 0.0, c = 0.0, d = 0.0;
+            for (int j = 0; j < V; ++j) {
+                a += dS[(size_t)i * V + j] * r[j];
+                c += P[(size_t)i * V + j] * dr[j];
+            }
+            dk[(long)t * K + i] = bt * a - c;
+            const double e = exp((double)gt[i]);
+            for (int j = 0; j < V; ++j) {
+                const double dP = dS[(size_t)i * V + j] - (double)kt[i] * dr[j];
+                d += dP * P[(size_t)i * V + j];
+                dS[(size_t)i * V + j] = e * dP;
+            }
+            dg[(long)t * K + i] = d;
+        }
+    }
+    memcpy(ds0, dS, KV * sizeof(double));
+    free(S); free(dS); free(P); free(r); free(dr);
+}

@@ -321,3 +321,50 @@ def test_gated_forward_reduces_to_exact_delta_rule_retrieval():
         _, S = oracle.forward_gated(sl(q), sl(k), sl(v), sl(g), sl(b), A_log, dt, 1.0, gate="softplus")
         kn = k[0, t - 1, 0].astype(np.float64) / np.sqrt(np.sum(k[0, t - 1, 0].astype(np.float64) ** 2) + 1e-6)
         np.testing.assert_allclose(kn @ S[0, 0], v[0, t - 1, 0], atol=2e-5)
+
+
+# ----------------------------------------------------------------- backward --
+def _loss(q, k, v, g, b, s0, do, dsf, scale, cu=None):
+    o, S = oracle.forward(q, k, v, g, b, scale, initial_state=s0, cu_seqlens=cu, form="recurrent")
+    return float(np.sum(o * do) + np.sum(S * dsf))
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_backward_matches_central_differences(varlen):
+    """Every input entry of a tiny problem (grouped value heads, an initial state, a
+    final-state gradient; with varlen, an empty and a one-token sequence) against the
+    central difference of the forward's loss sum <do, o> + <dS_final, S_final>.  The
+    step is taken on the fp32 inputs the oracle reads, and divided by its exact size."""
+    rng = np.random.default_rng(31)
+    H, HV, K, V = 1, 2, 3, 2
+    if varlen:
+        lens = [3, 0, 1, 4]
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        B, T, NS = 1, int(cu[-1]), len(lens)
+    else:
+        cu, B, T = None, 2, 5
+        NS = B
+    q, k, v, g, b, s0 = rand_inputs(rng, B, T, H, HV, K, V, g_scale=0.5, s0=True, n_seq=NS)
+    b = np.clip(b, 0.05, 0.95).astype(np.float32)
+    do = rng.standard_normal(v.shape).astype(np.float32)
+    dsf = rng.standard_normal(s0.shape).astype(np.float32)
+    scale = 0.7
+    grads = oracle.backward(q, k, v, g, b, scale, do, d_final_state=dsf, initial_state=s0, cu_seqlens=cu)
+    args = [q, k, v, g, b, s0]
+    for ai, (arr, grad) in enumerate(zip(args, (grads[0], grads[1], grads[2], grads[3], grads[4], grads[5]))):
+        for idx in np.ndindex(arr.shape):
+            x0 = float(arr[idx])
+            hstep = 1e-3 * max(1.0, abs(x0))
+            up, dn = [a.copy() for a in args], [a.copy() for a in args]
+            up[ai][idx] = np.float32(x0 + hstep)
+            dn[ai][idx] = np.float32(x0 - hstep)
+            step = float(up[ai][idx]) - float(dn[ai][idx])
+            fd = (_loss(*up, do, dsf, scale, cu) - _loss(*dn, do, dsf, scale, cu)) / step
+            assert abs(fd - grad[idx]) <= 2e-5 * max(1.0, abs(fd)), (ai, idx, fd, grad[idx])
+
+
+def test_backward_of_an_empty_sequence_passes_the_state_gradient_through():
+    q, k, v, g, b, s0 = rand_inputs(np.random.default_rng(3), 1, 0, 1, 1, 2, 2, s0=True)
+    dsf = np.arange(4, dtype=np.float32).reshape(1, 1, 2, 2)
+    *_, ds0 = oracle.backward(q, k, v, g, b, 1.0, np.zeros(v.shape, np.float32), d_final_state=dsf, initial_state=s0)
+    assert np.array_equal(ds0, dsf.astype(np.float64))
