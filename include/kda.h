@@ -180,6 +180,33 @@ KDA_API kda_status kda_chunk_output(const kda_shape* shape, const void* q, const
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward: the gradients of the loss sum_t <d_out_t, o_t> + <d_final_state, S_final>
+ * with respect to every input of kda_chunk_fwd (same shapes and conventions; the
+ * method's recurrence, page "手撕KDA" section "1 Naive"; the pages' own backward,
+ * sections 2 and 4 of that page, works on the chunked form).  Reverse mode through
+ * the token recurrence on CUDA cores in fp32: a forward sweep keeps the fp32 state
+ * entering every 64-token chunk in the workspace, then each chunk's token states are
+ * recomputed and swept in reverse.
+ *
+ *   d_out          [B, T, HV, V]  io_dtype
+ *   d_final_state  [NS, HV, K, V] fp32 or NULL (zeros)
+ *   dq, dk         [B, T, H, K]   fp32: summed over the value heads sharing a key head
+ *   dv             [B, T, HV, V]  fp32;   dg [B, T, HV, K] fp32;   dbeta [B, T, HV] fp32
+ *   d_initial_state [NS, HV, K, V] fp32 or NULL (not written)
+ *   workspace      at least kda_backward_workspace_size() bytes: the status word and,
+ *                  per (sequence, value head), ceil(T / 64) + 64 states of K x V fp32
+ *                  (with cu_seqlens, T is the packed total: the bound of any sequence)
+ * Any io_dtype and K, V in {64, 128}.  The gradients must not overlap each other or
+ * any input.
+ */
+KDA_API size_t kda_backward_workspace_size(const kda_shape* shape);
+KDA_API kda_status kda_backward(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, float scale, const float* initial_state,
+                                const int32_t* cu_seqlens, const void* d_out, const float* d_final_state,
+                                float* dq, float* dk, float* dv, float* dg, float* dbeta, float* d_initial_state,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Token-recurrent forward: the defining recurrence evaluated token by token on
  * CUDA cores in fp32 (same arguments and results as kda_chunk_fwd; its
  * workspace needs only the 256-byte status word).  Kept as the

@@ -7,6 +7,8 @@ from ._lib import (  # noqa: F401
     EXPORTS,
     KdaError,
     KdaShape,
+    kda_backward,
+    kda_backward_workspace_size,
     kda_chunk_fwd,
     kda_chunk_fwd_gated,
     kda_chunk_output,

@@ -32,7 +32,8 @@ STATIC_SCRATCH_MAX_UNITS = 32
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
            "kda_read_device_status", "kda_status_string", "kda_chunk_size",
            "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode", "kda_chunk_fwd_gated",
-           "kda_chunk_states_size", "kda_chunk_states", "kda_chunk_output")
+           "kda_chunk_states_size", "kda_chunk_states", "kda_chunk_output", "kda_backward_workspace_size",
+           "kda_backward")
 GATE_KINDS = {"bounded": 0, "softplus": 1}
 
 
@@ -97,6 +98,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_chunk_states.restype = I
         lib.kda_chunk_output.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, S, P]
         lib.kda_chunk_output.restype = I
+        lib.kda_backward_workspace_size.argtypes = [ctypes.POINTER(KdaShape)]
+        lib.kda_backward_workspace_size.restype = S
+        lib.kda_backward.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, P,
+                                     P, P, P, P, P, P, P, S, P]
+        lib.kda_backward.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -358,3 +364,51 @@ def kda_chunk_output(q, k, v, g, beta, h, scale=None, out=None, workspace=None, 
                                     ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                     ctypes.c_void_p(stream)))
     return out
+
+
+def kda_backward_workspace_size(shape: KdaShape) -> int:
+    return int(load_library().kda_backward_workspace_size(ctypes.byref(shape)))
+
+
+def kda_backward(q, k, v, g, beta, d_out, scale=None, initial_state=None, cu_seqlens=None, d_final_state=None,
+                 output_d_initial_state=True, workspace=None, stream=None):
+    """Gradients of sum <d_out, o> + <d_final_state, S_final> for the forward with the same
+    arguments.  d_out [B,T,HV,V] in q's dtype, d_final_state [NS,HV,K,V] fp32 or None.
+    Returns (dq, dk, dv, dg, dbeta, d_initial_state), all fp32, in the inputs' shapes."""
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, (("d_out", d_out), ("initial_state", initial_state),
+                                      ("cu_seqlens", cu_seqlens), ("d_final_state", d_final_state),
+                                      ("workspace", workspace)))
+    if not d_out.is_contiguous() or d_out.dtype != q.dtype:
+        raise KdaError(1, "d_out must be contiguous with q's dtype")
+    with torch.cuda.device(q.device):
+        shape = make_shape(q, v, cu_seqlens)
+        K = q.shape[3]
+        if scale is None:
+            scale = K ** -0.5
+        NS = q.shape[0] if cu_seqlens is None else shape.num_seqs
+        HV, V = v.shape[2], v.shape[3]
+        f32 = dict(dtype=torch.float32, device=q.device)
+        dq = torch.empty(q.shape, **f32)
+        dk = torch.empty(k.shape, **f32)
+        dv = torch.empty(v.shape, **f32)
+        dg = torch.empty(g.shape, **f32)
+        dbeta = torch.empty(beta.shape, **f32)
+        ds0 = torch.empty((NS, HV, K, V), **f32) if output_d_initial_state else None
+        made = [dq, dk, dv, dg, dbeta] + ([ds0] if ds0 is not None else [])
+        if workspace is None:
+            workspace = torch.empty(kda_backward_workspace_size(shape), dtype=torch.uint8, device=q.device)
+            made.append(workspace)
+        current = torch.cuda.current_stream(q.device).cuda_stream
+        if stream is None:
+            stream = current
+        _check(lib.kda_backward(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+            _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(dg), _ptr(dbeta), _ptr(ds0), _ptr(workspace),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), ctypes.c_void_p(stream)))
+        if stream != current:
+            other = torch.cuda.ExternalStream(stream, device=q.device)
+            for t in made:
+                t.record_stream(other)
+    return dq, dk, dv, dg, dbeta, ds0

@@ -16,6 +16,12 @@ size_t chunk_tc_ring_bytes(int num_seqs, int HV);
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
 const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units);
 cudaError_t launch_chunk_output(const FwdParams& p, cudaStream_t stream);
+size_t backward_unit_floats(long max_len, int K, int V);
+cudaError_t launch_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const float* s0, const int32_t* cu, const void* d_out, const float* d_fin, float* dq,
+                            float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* scratch,
+                            size_t unit_floats, uint32_t* status, float scale, int T, int H, int HV, int K, int V,
+                            int num_seqs, bool bf16, cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                           float* state, void* out, float scale, int B, int T, int H, int HV, int K, int V,
                           bool bf16, cudaStream_t stream);
@@ -320,6 +326,61 @@ kda_status kda_chunk_output(const kda_shape* shape, const void* q, const void* k
   c.p.h = static_cast<uint16_t*>(const_cast<void*>(h));
   c.p.h_chunks = static_cast<int>((shape->T + 63) / 64);
   return kda::launch_chunk_output(c.p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t kda_backward_workspace_size(const kda_shape* s) {
+  if (!s || s->B < 0 || s->T < 0 || s->HV < 1 || s->K < 1 || s->V < 1 || s->num_seqs < 0) return 0;
+  const size_t ns = s->num_seqs > 0 ? s->num_seqs : s->B;
+  return 256 + ns * s->HV * kda::backward_unit_floats(s->T, s->K, s->V) * sizeof(float);
+}
+
+kda_status kda_backward(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float scale, const float* initial_state, const int32_t* cu_seqlens,
+                        const void* d_out, const float* d_final_state, float* dq, float* dk, float* dv, float* dg,
+                        float* dbeta, float* d_initial_state, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  // the forward's own checks (shapes, alignment, aliasing among the inputs) with d_out in the
+  // place of the output; the gradients are then checked against everything else
+  Checked c;
+  kda_status st = validate(false, s, q, k, v, g, beta, scale, initial_state, cu_seqlens, const_cast<void*>(d_out),
+                           nullptr, workspace, workspace_bytes, c);
+  if (st != KDA_OK) return st;
+  if (workspace_bytes < kda_backward_workspace_size(s)) return KDA_ERR_WORKSPACE;
+  const size_t ns = cu_seqlens ? static_cast<size_t>(s->num_seqs) : static_cast<size_t>(s->B);
+  const size_t tokens = cu_seqlens ? static_cast<size_t>(s->T) : static_cast<size_t>(s->B) * s->T;
+  const size_t es = s->io_dtype == KDA_BF16 ? 2 : 4;
+  const size_t n_qk = tokens * s->H * s->K * es, n_v = tokens * s->HV * s->V * es;
+  const size_t n_g = tokens * s->HV * s->K * 4, n_b = tokens * s->HV * 4, n_s = ns * s->HV * s->K * s->V * 4;
+  const size_t f_qk = tokens * s->H * s->K * 4, f_v = tokens * s->HV * s->V * 4;
+  if (tokens > 0 && (!dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_INVALID_ARG;
+  const void* outs[] = {dq, dk, dv, dg, dbeta, d_initial_state};
+  const size_t nouts[] = {f_qk, f_qk, f_v, n_g, n_b, n_s};
+  for (const void* ptr : outs)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  if (d_final_state && !aligned(d_final_state, 16)) return KDA_ERR_ALIGNMENT;
+  const void* ins[] = {q, k, v, g, beta, initial_state, d_out, d_final_state, workspace};
+  const size_t nins[] = {n_qk, n_qk, n_v, n_g, n_b, n_s, n_v, n_s, workspace_bytes};
+  for (int j = 0; j < 8; ++j)  // the scratch is written while the inputs are read
+    if (overlaps(workspace, workspace_bytes, ins[j], nins[j])) return KDA_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i) {
+    for (int j = 0; j < 9; ++j)
+      if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return KDA_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 6; ++j)
+      if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return KDA_ERR_INVALID_ARG;
+  }
+  if (c.units == 0) return KDA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint32_t* status = static_cast<uint32_t*>(workspace);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
+  // dq and dk gather the value heads that share a key head: zero them first
+  if (tokens > 0 && (cudaMemsetAsync(dq, 0, f_qk, cs) != cudaSuccess || cudaMemsetAsync(dk, 0, f_qk, cs) != cudaSuccess))
+    return KDA_ERR_CUDA;
+  float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+  const cudaError_t e = kda::launch_backward(
+      q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta, d_initial_state,
+      scratch, kda::backward_unit_floats(s->T, s->K, s->V), status, scale, s->T, s->H, s->HV, s->K, s->V,
+      static_cast<int>(ns), s->io_dtype == KDA_BF16, cs);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,

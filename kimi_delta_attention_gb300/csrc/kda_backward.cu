@@ -1,0 +1,328 @@
+// kda_backward.cu -- gradients of the forward with respect to q, k, v, g, beta and
+// the initial state, by reverse mode through the token recurrence, on CUDA cores in
+// fp32.
+//
+// For the loss sum_t <do_t, o_t> + <dS_final, S_final>, going back from the last token,
+// with Sp the state before token t, P = Diag(e^{g_t}) Sp, u = P^T k, r = v - u and
+// S = P + beta k r^T (the recurrence of page "手撕KDA", section "1 Naive"):
+//     dq_t = scale S do_t;  dS += scale q_t do_t^T
+//     kd = dS^T k;  dbeta_t = r . kd;  dr = beta kd;  dv_t = dr
+//     dk_t = beta dS r - P dr;  dP = dS - k dr^T;  dg_t,i = sum_j dP_ij P_ij;  dS = Diag(e^{g_t}) dP
+// and dS after the first token is the initial state's gradient.  (The pages' backward,
+// "手撕KDA" sections 2 and 4, works on the chunked form; this is the same derivative
+// taken through the recurrence it evaluates.)
+//
+// One CTA per (sequence, value head), 256 threads, each holding 4 adjacent value
+// columns of K / (1024 / V) state rows (as the decode kernel).  The states the
+// reverse sweep needs are recomputed: a forward sweep stores the fp32 state entering
+// every 64-token chunk in the workspace, then, chunk by chunk from the last, the
+// chunk's 64 token states are recomputed into the workspace and swept in reverse.
+// Reductions over K go through shared memory, reductions over V are warp shuffles (a
+// halving reduce-scatter: 16 row sums in 16 shuffles).  dq and dk are summed over the
+// value heads that share a key head with atomics (the launcher zeroes them first).
+#include "kda_common.cuh"
+
+namespace kda {
+namespace bwd {
+
+constexpr int NT = 256;
+constexpr int CH = 64;  // tokens per checkpoint
+
+struct Params {
+  const void* q;       // [tokens, H, K]  io type
+  const void* k;
+  const void* v;       // [tokens, HV, V]
+  const float* g;      // [tokens, HV, K]
+  const float* beta;   // [tokens, HV]
+  const float* s0;     // [NS, HV, K, V] or null
+  const int32_t* cu;   // [NS + 1] or null
+  const void* d_out;   // [tokens, HV, V]  io type
+  const float* d_fin;  // [NS, HV, K, V] or null
+  float* dq;           // [tokens, H, K]  fp32, accumulated
+  float* dk;
+  float* dv;           // [tokens, HV, V]
+  float* dg;           // [tokens, HV, K]
+  float* dbeta;        // [tokens, HV]
+  float* ds0;          // [NS, HV, K, V] or null
+  float* scratch;      // per unit: (max chunks + CH) x K x V fp32
+  uint32_t* status;
+  size_t unit_floats;  // floats of scratch per unit
+  float scale;
+  int T, H, HV, num_seqs;
+};
+
+__device__ __forceinline__ bool seq_bounds(const Params& p, int seq, long& tok0, int& len) {
+  if (!p.cu) {
+    tok0 = static_cast<long>(seq) * p.T;
+    len = p.T;
+    return true;
+  }
+  const int a = p.cu[seq], b = p.cu[seq + 1];
+  if (a < 0 || b < a || b > p.T || (seq == 0 && a != 0) || (seq == p.num_seqs - 1 && b != p.T)) {
+    atomicOr(p.status, kStatusBounds);
+    tok0 = 0;
+    len = 0;
+    return false;
+  }
+  tok0 = a;
+  len = b - a;
+  return true;
+}
+
+// Sums over the L lanes of a row group of N values per lane (xor masks M, M/2, .. 1 with
+// M = L / 2): while more than one value is left each step keeps half and sends half, so
+// every lane ends with the full sum of one value, index `idx`.
+template <int N, int M>
+struct Halve {
+  static __device__ __forceinline__ void run(float* v, int lane, int& idx) {
+    if constexpr (N > 1) {
+      const bool up = (lane & M) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[i + N / 2];
+        const float keep = up ? v[i + N / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, M);
+      }
+      if (up) idx += N / 2;
+      if constexpr (M > 1) Halve<N / 2, M / 2>::run(v, lane, idx);
+    } else {
+      v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], M);
+      if constexpr (M > 1) Halve<1, M / 2>::run(v, lane, idx);
+    }
+  }
+};
+// lanes that hold a distinct sum after Halve<N, L/2> (the others repeat one of them)
+template <int N, int L>
+__device__ __forceinline__ bool halve_writer(int lane) {
+  int plain = 0;  // masks of the steps that only added
+  int n = N;
+  for (int m = L / 2; m >= 1; m /= 2) {
+    if (n > 1) n /= 2;
+    else plain |= m;
+  }
+  return (lane & plain) == 0;
+}
+
+template <typename IO, int K, int V>
+__global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
+  constexpr int TPR = V / 4;    // threads across a state row
+  constexpr int RG = NT / TPR;  // row groups
+  constexpr int RPT = K / RG;   // rows per thread: rg + RG i
+  static_assert(RPT * RG == K && TPR * 4 == V && (TPR == 32 || TPR == 16), "backward tiling");
+  const int hv = blockIdx.x, seq = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int cg = tid % TPR, rg = tid / TPR;
+  const int hk = hv / (p.HV / p.H);
+  const IO* q = static_cast<const IO*>(p.q);
+  const IO* k = static_cast<const IO*>(p.k);
+  const IO* v = static_cast<const IO*>(p.v);
+  const IO* dout = static_cast<const IO*>(p.d_out);
+
+  __shared__ float s_q[K], s_k[K], s_e[K], s_v[V], s_do[V], s_b;
+  __shared__ __align__(16) float red[RG][V];
+  __shared__ __align__(16) float col[V];   // a reduced V-vector (u, then kd)
+
+  long tok0;
+  int len;
+  seq_bounds(p, seq, tok0, len);
+  const int nch = (len + CH - 1) / CH;
+  const size_t unit = static_cast<size_t>(seq) * p.HV + hv;
+  float* ckpt = p.scratch + unit * p.unit_floats;           // [nch][K][V]
+  float* toks = ckpt + static_cast<size_t>(nch > 0 ? nch : 1) * K * V;  // [CH][K][V]
+  auto slot = [&](float* base, int i) { return base + static_cast<size_t>(rg + RG * i) * V + 4 * cg; };
+
+  auto stage = [&](int t) {  // token t of the sequence: q, k, e^g, v, do, beta
+    const size_t tok = static_cast<size_t>(tok0 + t);
+    if (tid < K) {
+      s_q[tid] = to_f32(q[(tok * p.H + hk) * K + tid]);
+      s_k[tid] = to_f32(k[(tok * p.H + hk) * K + tid]);
+      s_e[tid] = expf(p.g[(tok * p.HV + hv) * K + tid]);
+    } else if (tid < K + V) {
+      s_v[tid - K] = to_f32(v[(tok * p.HV + hv) * V + (tid - K)]);
+      s_do[tid - K] = to_f32(dout[(tok * p.HV + hv) * V + (tid - K)]);
+    }
+    if (tid == NT - 1) s_b = p.beta[tok * p.HV + hv];
+  };
+  // u = P^T k over this thread's rows -> col[] (all rows); P = Diag(e) S in place
+  auto reduce_k = [&](const float4 (&x)[RPT]) {
+    float4 pu = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float kd = s_k[rg + RG * i];
+      pu.x = fmaf(kd, x[i].x, pu.x); pu.y = fmaf(kd, x[i].y, pu.y);
+      pu.z = fmaf(kd, x[i].z, pu.z); pu.w = fmaf(kd, x[i].w, pu.w);
+    }
+    *reinterpret_cast<float4*>(&red[rg][4 * cg]) = pu;
+    __syncthreads();
+    if (tid < V) {
+      float a = 0.f;
+#pragma unroll
+      for (int r = 0; r < RG; ++r) a += red[r][tid];
+      col[tid] = a;
+    }
+    __syncthreads();
+  };
+  // one forward step on the state held in s (token staged)
+  auto forward_step = [&](float4 (&s)[RPT]) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float e = s_e[rg + RG * i];
+      s[i].x *= e; s[i].y *= e; s[i].z *= e; s[i].w *= e;
+    }
+    reduce_k(s);
+    const float bt = s_b;
+    const float4 br = make_float4(bt * (s_v[4 * cg] - col[4 * cg]), bt * (s_v[4 * cg + 1] - col[4 * cg + 1]),
+                                  bt * (s_v[4 * cg + 2] - col[4 * cg + 2]), bt * (s_v[4 * cg + 3] - col[4 * cg + 3]));
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float kd = s_k[rg + RG * i];
+      s[i].x = fmaf(kd, br.x, s[i].x); s[i].y = fmaf(kd, br.y, s[i].y);
+      s[i].z = fmaf(kd, br.z, s[i].z); s[i].w = fmaf(kd, br.w, s[i].w);
+    }
+  };
+
+  // ---- 1. forward sweep: the fp32 state entering every chunk ----
+  float4 s[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i)
+    s[i] = p.s0 ? *reinterpret_cast<const float4*>(p.s0 + unit * K * V + static_cast<size_t>(rg + RG * i) * V + 4 * cg)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t = 0; t < len; ++t) {
+    if (t % CH == 0) {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(ckpt + static_cast<size_t>(t / CH) * K * V, i)) = s[i];
+    }
+    __syncthreads();  // the previous step's reads of the staged token are done
+    stage(t);
+    __syncthreads();
+    forward_step(s);
+  }
+
+  // ---- 2. reverse sweep, one chunk at a time ----
+  float4 ds[RPT];  // the state's gradient
+#pragma unroll
+  for (int i = 0; i < RPT; ++i)
+    ds[i] = p.d_fin ? *reinterpret_cast<const float4*>(p.d_fin + unit * K * V + static_cast<size_t>(rg + RG * i) * V + 4 * cg)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool writer = halve_writer<RPT, TPR>(lane);
+  for (int n = nch - 1; n >= 0; --n) {
+    const int t0 = n * CH, t1 = min(len, t0 + CH);
+    // recompute the chunk's token states (the state before each token)
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float4*>(slot(ckpt + static_cast<size_t>(n) * K * V, i));
+    for (int t = t0; t < t1; ++t) {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(toks + static_cast<size_t>(t - t0) * K * V, i)) = s[i];
+      if (t + 1 == t1) break;  // the last token's successor is not needed
+      __syncthreads();
+      stage(t);
+      __syncthreads();
+      forward_step(s);
+    }
+    for (int t = t1 - 1; t >= t0; --t) {
+      __syncthreads();
+      stage(t);
+      float4 P[RPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) P[i] = *reinterpret_cast<const float4*>(slot(toks + static_cast<size_t>(t - t0) * K * V, i));
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const float e = s_e[rg + RG * i];
+        P[i].x *= e; P[i].y *= e; P[i].z *= e; P[i].w *= e;
+      }
+      reduce_k(P);  // col = u
+      const float bt = s_b, sc = p.scale;
+      const float4 r = make_float4(s_v[4 * cg] - col[4 * cg], s_v[4 * cg + 1] - col[4 * cg + 1],
+                                   s_v[4 * cg + 2] - col[4 * cg + 2], s_v[4 * cg + 3] - col[4 * cg + 3]);
+      const float4 dov = *reinterpret_cast<const float4*>(&s_do[4 * cg]);
+      // dq = scale (P + beta k r^T) do, per row; then dS += scale q do^T
+      float acc[RPT];
+      const float rdo = bt * (r.x * dov.x + r.y * dov.y + r.z * dov.z + r.w * dov.w);
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int d = rg + RG * i;
+        acc[i] = P[i].x * dov.x + P[i].y * dov.y + P[i].z * dov.z + P[i].w * dov.w + s_k[d] * rdo;
+        const float qs = sc * s_q[d];
+        ds[i].x = fmaf(qs, dov.x, ds[i].x); ds[i].y = fmaf(qs, dov.y, ds[i].y);
+        ds[i].z = fmaf(qs, dov.z, ds[i].z); ds[i].w = fmaf(qs, dov.w, ds[i].w);
+      }
+      const size_t tok = static_cast<size_t>(tok0 + t);
+      {
+        int idx = 0;
+        Halve<RPT, TPR / 2>::run(acc, lane, idx);
+        if (writer) atomicAdd(p.dq + (tok * p.H + hk) * K + rg + RG * idx, sc * acc[0]);
+      }
+      // kd = dS^T k (all rows) -> col;  dr = beta kd;  dbeta = r . kd
+      __syncthreads();  // col (u) has been read by every thread
+      reduce_k(ds);
+      const float4 kdv = *reinterpret_cast<const float4*>(&col[4 * cg]);
+      const float4 dr = make_float4(bt * kdv.x, bt * kdv.y, bt * kdv.z, bt * kdv.w);
+      if (rg == 0) *reinterpret_cast<float4*>(p.dv + (tok * p.HV + hv) * V + 4 * cg) = dr;
+      {  // dbeta: every row group holds all V columns of r and kd; row group 0's sum is kept
+        float db = r.x * kdv.x + r.y * kdv.y + r.z * kdv.z + r.w * kdv.w;
+#pragma unroll
+        for (int m = TPR / 2; m >= 1; m >>= 1) db += __shfl_xor_sync(0xFFFFFFFFu, db, m);
+        if (tid == 0) p.dbeta[tok * p.HV + hv] = db;
+      }
+      // dk = beta dS r - P dr;  dP = dS - k dr^T;  dg = sum_j dP P;  dS = Diag(e) dP
+      float dkv[RPT], dgv[RPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int d = rg + RG * i;
+        const float kd = s_k[d], e = s_e[d];
+        dkv[i] = bt * (ds[i].x * r.x + ds[i].y * r.y + ds[i].z * r.z + ds[i].w * r.w) -
+                 (P[i].x * dr.x + P[i].y * dr.y + P[i].z * dr.z + P[i].w * dr.w);
+        float4 dp = make_float4(ds[i].x - kd * dr.x, ds[i].y - kd * dr.y, ds[i].z - kd * dr.z, ds[i].w - kd * dr.w);
+        dgv[i] = dp.x * P[i].x + dp.y * P[i].y + dp.z * P[i].z + dp.w * P[i].w;
+        ds[i] = make_float4(e * dp.x, e * dp.y, e * dp.z, e * dp.w);
+      }
+      {
+        int idx = 0;
+        Halve<RPT, TPR / 2>::run(dkv, lane, idx);
+        if (writer) atomicAdd(p.dk + (tok * p.H + hk) * K + rg + RG * idx, dkv[0]);
+      }
+      {
+        int idx = 0;
+        Halve<RPT, TPR / 2>::run(dgv, lane, idx);
+        if (writer) p.dg[(tok * p.HV + hv) * K + rg + RG * idx] = dgv[0];
+      }
+    }
+  }
+  if (p.ds0) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+      *reinterpret_cast<float4*>(p.ds0 + unit * K * V + static_cast<size_t>(rg + RG * i) * V + 4 * cg) = ds[i];
+  }
+}
+
+template <typename IO>
+cudaError_t launch_io(const Params& p, int K, int V, cudaStream_t stream) {
+  const dim3 grid(p.HV, p.num_seqs);
+  if (K == 128 && V == 128) recurrent_bwd_kernel<IO, 128, 128><<<grid, NT, 0, stream>>>(p);
+  else if (K == 128 && V == 64) recurrent_bwd_kernel<IO, 128, 64><<<grid, NT, 0, stream>>>(p);
+  else if (K == 64 && V == 128) recurrent_bwd_kernel<IO, 64, 128><<<grid, NT, 0, stream>>>(p);
+  else recurrent_bwd_kernel<IO, 64, 64><<<grid, NT, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+// floats of backward scratch per (sequence, value head): the chunk checkpoints of the
+// longest possible sequence plus one chunk of token states
+size_t backward_unit_floats(long max_len, int K, int V) {
+  const long nch = (max_len + bwd::CH - 1) / bwd::CH;
+  return static_cast<size_t>((nch > 0 ? nch : 1) + bwd::CH) * K * V;
+}
+
+cudaError_t launch_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const float* s0, const int32_t* cu, const void* d_out, const float* d_fin, float* dq,
+                            float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* scratch,
+                            size_t unit_floats, uint32_t* status, float scale, int T, int H, int HV, int K, int V,
+                            int num_seqs, bool bf16, cudaStream_t stream) {
+  bwd::Params p{q, k, v, g, beta, s0, cu, d_out, d_fin, dq, dk, dv, dg, dbeta, ds0, scratch, status, unit_floats,
+                scale, T, H, HV, num_seqs};
+  return bf16 ? bwd::launch_io<__nv_bfloat16>(p, K, V, stream) : bwd::launch_io<float>(p, K, V, stream);
+}
+
+}  // namespace kda

@@ -154,3 +154,31 @@ def test_gated_validation_on_host(lib):
     assert call(ctypes.byref(G(7, 0x400000, 0x500000, -5.0))) == 1     # unknown gate kind
     assert call(ctypes.byref(G(1, None, 0x500000, 0.0))) == 1          # A_log missing
     assert call(ctypes.byref(G(1, 0x400000, 0x500008, 0.0))) == 3      # dt_bias not 16-byte aligned
+
+
+def test_backward_validation_on_host(lib):
+    """kda_backward sizes its workspace and rejects bad gradients before touching CUDA."""
+    P = ctypes.c_void_p
+    f = [P(0x10000000 * (i + 1)) for i in range(16)]
+    shape = _lib.KdaShape(1, 64, 2, 2, 128, 128, 0, _lib.KDA_BF16)
+    need = lib.kda_backward_workspace_size(ctypes.byref(shape))
+    assert need == 256 + 2 * (1 + 64) * 128 * 128 * 4            # 1 checkpoint + 64 token states per unit
+    sc = ctypes.c_float(0.088)
+
+    def call(ws_bytes=need, **kw):
+        a = dict(q=f[0], k=f[1], v=f[2], g=f[3], beta=f[4], s0=None, cu=None, do=f[5], dfin=None,
+                 dq=f[6], dk=f[7], dv=f[8], dg=f[9], db=f[10], ds0=f[11], ws=f[12])
+        a.update(kw)
+        return lib.kda_backward(ctypes.byref(shape), a["q"], a["k"], a["v"], a["g"], a["beta"], sc, a["s0"],
+                                a["cu"], a["do"], a["dfin"], a["dq"], a["dk"], a["dv"], a["dg"], a["db"],
+                                a["ds0"], a["ws"], ctypes.c_size_t(ws_bytes), None)
+
+    assert call(ws_bytes=need - 1) == 6                    # workspace too small
+    assert call(dq=None) == 1                              # gradients are required
+    assert call(dq=f[0]) == 1                              # dq aliases q
+    assert call(dk=f[6]) == 1                              # dk aliases dq
+    assert call(ds0=f[5]) == 1                             # d_initial_state aliases d_out
+    assert call(ws=f[2]) == 1                              # the scratch overlaps v
+    assert call(dg=P(0x10000000 * 10 + 8)) == 3            # misaligned dg
+    assert call(dfin=P(0x10000000 * 14 + 4)) == 3          # misaligned d_final_state
+    assert call(do=None) == 1                              # d_out is required

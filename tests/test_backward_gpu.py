@@ -1,0 +1,112 @@
+"""GPU parity of kda_backward: the gradients of sum <d_out, o> + <dS_final, S_final>
+with respect to q, k, v, g, beta and the initial state, compared with the fp64
+oracle's reverse mode through the token recurrence (itself pinned by central
+differences) on the same inputs.
+
+The kernel computes in fp32 whatever the I/O type (bf16 inputs reach both sides as
+the same rounded values), so every gradient is held to 1e-4 of its largest magnitude:
+the recurrence forgets within a few tens of tokens at these gates, and the fp32
+rounding of sums of O(K V) terms over such a window stays near 1e-6.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_gb300 as kda
+import oracle
+from kimi_delta_attention_gb300 import workloads as W
+from kda_testutil import np32
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.build()
+    kda.load_library()
+
+
+def _grads_in(x, seed, with_dfin=True):
+    rng = np.random.default_rng(seed)
+    do = rng.standard_normal(x.v.shape, dtype=np.float32)
+    NS = x.q.shape[0] if x.cu_seqlens is None else len(x.cu_seqlens) - 1
+    dfin = rng.standard_normal((NS,) + tuple(x.v.shape[2:3]) + (x.q.shape[3], x.v.shape[3]),
+                               dtype=np.float32) if with_dfin else None
+    dt = torch.bfloat16 if x.io_dtype == "bf16" else torch.float32
+    return torch.from_numpy(do).to(dt), None if dfin is None else torch.from_numpy(dfin)
+
+
+def _run(x, do, dfin):
+    d = x.to("cuda")
+    got = kda.kda_backward(d.q, d.k, d.v, d.g, d.beta, do.to("cuda"), d.scale, initial_state=d.initial_state,
+                           cu_seqlens=d.cu_seqlens, d_final_state=None if dfin is None else dfin.to("cuda"))
+    torch.cuda.synchronize()
+    ref = oracle.backward(np32(x.q), np32(x.k), np32(x.v), np32(x.g), np32(x.beta), x.scale, np32(do),
+                          d_final_state=np32(dfin), initial_state=np32(x.initial_state),
+                          cu_seqlens=None if x.cu_seqlens is None else x.cu_seqlens.numpy())
+    return [t.cpu().numpy() for t in got], ref
+
+
+def _assert_grads(got, ref, what):
+    for name, a, r in zip(NAMES, got, ref):
+        assert a.shape == r.shape, f"{what} {name}: shape {a.shape} != {r.shape}"
+        assert np.all(np.isfinite(a)), f"{what} {name}: non-finite"
+        if r.size == 0:
+            continue
+        err = np.abs(a - r).max() / max(np.abs(r).max(), 1e-30)
+        assert err <= TOL, f"{what} {name}: error {err:.3e} > {TOL}"
+
+
+@pytest.mark.parametrize("KV", [(128, 128), (64, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_backward_matches_oracle(KV, io):
+    K, V = KV
+    x = W.make_inputs(2, 150, 2, 4, K, V, io, seed=300 + K + V, init_state=True)   # 3 chunks, ragged tail, GVA
+    do, dfin = _grads_in(x, 1)
+    got, ref = _run(x, do, dfin)
+    _assert_grads(got, ref, f"K={K} V={V} {io}")
+
+
+def test_backward_varlen_with_empty_and_edge_lengths():
+    x = W.make_inputs(1, 0, 2, 4, 128, 128, "bf16", seed=301, init_state=True, lengths=[0, 1, 63, 64, 65, 200])
+    do, dfin = _grads_in(x, 2)
+    got, ref = _run(x, do, dfin)
+    _assert_grads(got, ref, "varlen")
+    # the empty sequence passes the final state's gradient straight through
+    assert np.array_equal(got[5][0], dfin[0].numpy())
+
+
+def test_backward_without_initial_or_final_state():
+    x = W.make_inputs(3, 97, 1, 2, 128, 128, "bf16", seed=302, init_state=False)
+    do, _ = _grads_in(x, 3, with_dfin=False)
+    got, ref = _run(x, do, None)
+    _assert_grads(got, ref, "no states")
+
+
+def test_backward_strong_decay():
+    """A gate bounded at -5: the chunk cumsum of the decay passes -88 (exp underflow in
+    fp32); the token recurrence has no such limit and neither does its reverse."""
+    x = W.make_inputs(2, 130, 2, 2, 128, 128, "f32", seed=303, init_state=True, gate="bounded", gate_value=-5.0)
+    do, dfin = _grads_in(x, 4)
+    got, ref = _run(x, do, dfin)
+    _assert_grads(got, ref, "strong decay")
+
+
+def test_backward_long_sequence():
+    """64 checkpoints and the recompute of every chunk."""
+    x = W.make_inputs(1, 4096, 1, 2, 128, 128, "bf16", seed=304, init_state=True)
+    do, dfin = _grads_in(x, 5)
+    got, ref = _run(x, do, dfin)
+    _assert_grads(got, ref, "T=4096")
+
+
+def test_backward_zero_tokens():
+    x = W.make_inputs(2, 0, 2, 4, 64, 64, "f32", seed=305, init_state=True)
+    do, dfin = _grads_in(x, 6)
+    got, _ = _run(x, do, dfin)
+    assert np.array_equal(got[5], dfin.numpy())
