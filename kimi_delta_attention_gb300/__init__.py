@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     kda_chunk_fwd_workspace_size,
     kda_chunk_size,
     kda_chunk_fwd_kernel_name,
+    kda_chunk_fwd_kernel_launches,
     kda_decode,
     kda_read_device_status,
     kda_recurrent_fwd,

@@ -31,7 +31,7 @@ STATIC_SCRATCH_MAX_UNITS = 32
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_workspace_size",
            "kda_read_device_status", "kda_status_string", "kda_chunk_size",
-           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_static_scratch", "kda_decode", "kda_chunk_fwd_gated",
+           "kda_chunk_fwd_kernel_name", "kda_chunk_fwd_kernel_launches", "kda_chunk_fwd_static_scratch", "kda_decode", "kda_chunk_fwd_gated",
            "kda_chunk_states_size", "kda_chunk_states", "kda_chunk_output", "kda_backward_workspace_size",
            "kda_backward")
 GATE_KINDS = {"bounded": 0, "softplus": 1}
@@ -84,6 +84,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.kda_chunk_size.restype = I
         lib.kda_chunk_fwd_kernel_name.argtypes = [ctypes.POINTER(KdaShape)]
         lib.kda_chunk_fwd_kernel_name.restype = ctypes.c_char_p
+        lib.kda_chunk_fwd_kernel_launches.argtypes = [ctypes.POINTER(KdaShape)]
+        lib.kda_chunk_fwd_kernel_launches.restype = I
         lib.kda_chunk_fwd_static_scratch.argtypes = [ctypes.POINTER(KdaShape), P, P, P, P, P, F, P, P, P, P, P,
                                                      ctypes.POINTER(ctypes.c_void_p)]
         lib.kda_chunk_fwd_static_scratch.restype = I
@@ -142,6 +144,11 @@ def kda_chunk_size() -> int:
 def kda_chunk_fwd_kernel_name(shape: KdaShape) -> str:
     """Kernel kda_chunk_fwd launches for `shape` on the current device."""
     return load_library().kda_chunk_fwd_kernel_name(ctypes.byref(shape)).decode()
+
+
+def kda_chunk_fwd_kernel_launches(shape: KdaShape) -> int:
+    """How many launches of that kernel one kda_chunk_fwd call makes."""
+    return int(load_library().kda_chunk_fwd_kernel_launches(ctypes.byref(shape)))
 
 
 def _check_tensors(q, k, v, g, beta, others):

@@ -14,7 +14,8 @@ cudaError_t launch_recurrent_fwd(const FwdParams& p, bool bf16, cudaStream_t str
 bool chunk_tc_supported(const FwdParams& p, bool bf16);
 size_t chunk_tc_ring_bytes(int num_seqs, int HV);
 cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream);
-const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units);
+const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int num_seqs, int HV, bool packed);
+int chunk_kernel_launches(bool bf16, int K, int V, long tokens, int num_seqs, int HV, bool packed);
 cudaError_t launch_chunk_output(const FwdParams& p, cudaStream_t stream);
 size_t backward_unit_floats(long max_len, int K, int V);
 cudaError_t launch_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -220,8 +221,18 @@ const char* kda_chunk_fwd_kernel_name(const kda_shape* s) {
   if (!s || s->B < 0 || s->T < 0 || s->HV < 1 || s->num_seqs < 0) return "none";
   const long ns = s->num_seqs > 0 ? s->num_seqs : s->B;
   const long tokens = s->num_seqs > 0 ? static_cast<long>(s->T) : static_cast<long>(s->B) * s->T;
-  if (ns * s->HV > (1L << 30)) return "none";
-  return kda::chunk_kernel_name(s->io_dtype == KDA_BF16, s->K, s->V, tokens, static_cast<int>(ns * s->HV));
+  if (ns * s->HV > (1L << 30) || ns == 0) return "none";
+  return kda::chunk_kernel_name(s->io_dtype == KDA_BF16, s->K, s->V, tokens, static_cast<int>(ns), s->HV,
+                                s->num_seqs > 0);
+}
+
+int kda_chunk_fwd_kernel_launches(const kda_shape* s) {
+  if (!s || s->B < 0 || s->T < 0 || s->HV < 1 || s->num_seqs < 0) return 0;
+  const long ns = s->num_seqs > 0 ? s->num_seqs : s->B;
+  const long tokens = s->num_seqs > 0 ? static_cast<long>(s->T) : static_cast<long>(s->B) * s->T;
+  if (ns * s->HV > (1L << 30) || ns == 0) return 0;
+  return kda::chunk_kernel_launches(s->io_dtype == KDA_BF16, s->K, s->V, tokens, static_cast<int>(ns), s->HV,
+                                    s->num_seqs > 0);
 }
 
 kda_status kda_chunk_fwd_gated(const kda_shape* shape, const void* q, const void* k, const void* v,

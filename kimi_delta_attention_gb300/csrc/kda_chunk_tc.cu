@@ -1368,13 +1368,15 @@ struct Rec {
   int m, u, seq, hv, hk, len;
   long tok0;
 };
-// Record r of the chunk-major enumeration: chunk r / NU of unit r % NU; false when
-// the unit has no such chunk.
+// Record r of the chunk-major enumeration: chunk r / NU of the launch's unit r % NU (x.u,
+// which indexes the ring and the flags; the unit of the problem is p.unit0 + x.u); false
+// when the unit has no such chunk.
 __device__ __forceinline__ bool rec_at(const FwdParams& p, int NU, int r, Rec& x) {
   x.m = r / NU;
   x.u = r - x.m * NU;
-  x.seq = x.u / p.HV;
-  x.hv = x.u - x.seq * p.HV;
+  const int ug = p.unit0 + x.u;
+  x.seq = ug / p.HV;
+  x.hv = ug - x.seq * p.HV;
   x.hk = x.hv / (p.HV / p.H);
   seq_range(p, x.seq, x.tok0, x.len);
   return x.m * C < x.len;
@@ -1396,6 +1398,9 @@ constexpr int kRecStorer = 32;  // pipeline thread storing qd and kr^T to the ri
 // record flags at byte kFlagOffset)
 #ifndef KDA_STAMP_RECORD
 #define KDA_STAMP_RECORD 4
+#endif
+#ifndef KDA_STAMP_M0  // first of the 64 chunks of unit 0 whose publication and copies are stamped
+#define KDA_STAMP_M0 0
 #endif
 #ifdef KDA_PROFILE
 #define PSTAMP(i)                                                                     \
@@ -1485,7 +1490,8 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     fence_proxy_async_global();
     st_release_gpu(flags + u * 32 + (m % SRING), static_cast<uint32_t>(m + 1));
 #ifdef KDA_PROFILE
-    if (u == 0 && m < 64) reinterpret_cast<uint64_t*>(p.status)[200 + m] = globaltimer_ns();
+    if (u == 0 && m >= KDA_STAMP_M0 && m < KDA_STAMP_M0 + 64)
+      reinterpret_cast<uint64_t*>(p.status)[200 + m - KDA_STAMP_M0] = globaltimer_ns();
 #endif
   };
 
@@ -1788,7 +1794,8 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   const int h = (warp >> 2) & 1;       // half of the non-lane dimension
   const int vcol = 32 * quad + lane;   // this thread's value column
   const int HV = p.HV;
-  const int seq = u / HV, hv = u - seq * HV;
+  const int ug = p.unit0 + u;          // the unit of the problem (u: of this launch)
+  const int seq = ug / HV, hv = ug - seq * HV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_BAR);
   long tok0;
   int len;
@@ -1801,7 +1808,7 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
   const uint64_t D_SW128 = sdesc_sw128(sb);
   auto d128 = [&](uint32_t off) { return D_SW128 + (off >> 4); };
   const uint32_t tl = tmem_addr(tmem, 32 * quad, 0);  // this warp's lane quadrant
-  const size_t state_off = static_cast<size_t>(u) * KD * VD;
+  const size_t state_off = static_cast<size_t>(ug) * KD * VD;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   bool failed = false;
   int a_issued = 0, b_issued = 0, c_issued = 0;
@@ -1846,7 +1853,8 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     mbar_arrive_expect_tx_relaxed(&bars[CB_FULL + b], REC_A_BYTES);
     bulk_load(sm + C_PA + b * PA_STRIDE, ring + static_cast<size_t>(n % SRING) * GSLOT, REC_A_BYTES, &bars[CB_FULL + b]);
 #ifdef KDA_PROFILE
-    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[264 + n] = globaltimer_ns();
+    if (u == 0 && n >= KDA_STAMP_M0 && n < KDA_STAMP_M0 + 64)
+      reinterpret_cast<uint64_t*>(p.status)[264 + n - KDA_STAMP_M0] = globaltimer_ns();
 #endif
   };
   auto issue_b = [&](int n) {
@@ -1855,7 +1863,8 @@ __device__ __forceinline__ void chain(const Maps& maps, const FwdParams& p, uint
     bulk_load(sm + C_PB + b * PB_STRIDE, ring + static_cast<size_t>(n % SRING) * GSLOT + SR_KRT, PB_STRIDE,
               &bars[CB_AB + b]);
 #ifdef KDA_PROFILE
-    if (u == 0 && n < 64) reinterpret_cast<uint64_t*>(p.status)[330 + n] = globaltimer_ns();
+    if (u == 0 && n >= KDA_STAMP_M0 && n < KDA_STAMP_M0 + 64)
+      reinterpret_cast<uint64_t*>(p.status)[330 + n - KDA_STAMP_M0] = globaltimer_ns();
 #endif
   };
   auto pump_b = [&](int up_b) {
@@ -2201,6 +2210,12 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   const bool is_chain = static_cast<int>(blockIdx.x) < NU;
   uint32_t* flags = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.status) + kFlagOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + split::TMEM_SLOT);
+#ifdef KDA_PROFILE
+  // [120] entry of CTA 0, [121] entry of the first producer CTA, [122] the last CTA's exit,
+  // [123] chain 0's exit, [124] the last producer's exit
+  if (tid == 0 && (blockIdx.x == 0 || static_cast<int>(blockIdx.x) == NU))
+    reinterpret_cast<uint64_t*>(p.status)[blockIdx.x == 0 ? 120 : 121] = globaltimer_ns();
+#endif
   if (tid == 0) {
     if (is_chain) {
       uint64_t* cb = reinterpret_cast<uint64_t*>(sm + split::C_BAR);
@@ -2240,6 +2255,15 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+#ifdef KDA_PROFILE
+  if (tid == 0) {
+    const unsigned long long t = globaltimer_ns();
+    unsigned long long* w = reinterpret_cast<unsigned long long*>(p.status);
+    atomicMax(w + 122, t);
+    if (blockIdx.x == 0) w[123] = t;
+    if (!is_chain) atomicMax(w + 124, t);
+  }
+#endif
 }
 
 // ======================================================================
@@ -2650,12 +2674,41 @@ const DeviceInfo& device_info() {
 }
 }  // namespace
 
-// Whether the split kernel runs for NU (sequence, value head) units on the current device.
-bool use_split_kernel(int NU) {
+// How the split kernel covers the NS x HV (sequence, value head) units, of about `chunks`
+// chunks each, on the current device: `launches` stream-ordered launches of at most
+// `per_launch` consecutive units (their chains take one SM each; automatic plans leave
+// three quarters of the SMs to the producers), or launches == 0 when the cluster kernel
+// runs instead.  A launch takes whole sequences where a sequence's heads fit one.  More
+// units than one launch holds pay a launch's start (~20 us before its chains have
+// records) per launch, which long sequences of one length amortise: fixed-length
+// problems with at least kMinBatchedChunks chunks per sequence run as several launches;
+// packed sequences (a launch lasts as long as its longest one) and shorter ones run the
+// cluster kernel.
+constexpr long kMinBatchedChunks = 16;
+struct SplitPlan {
+  int launches = 0, per_launch = 0;
+};
+SplitPlan split_plan(int NS, int HV, long chunks, bool packed) {
   const DeviceInfo& dev = device_info();
   const int mode = split_override();
-  const bool split_ok = dev.coop && dev.split_fits && NU <= kMaxSplitUnits && NU <= dev.sms - 2;
-  return split_ok && (mode == 1 || (mode == -1 && 4 * NU <= dev.sms));
+  const int NU = NS * HV;
+  SplitPlan plan;
+  if (!dev.coop || !dev.split_fits || mode == 0 || NU < 1) return plan;
+  const int cap = std::min(kMaxSplitUnits, mode == 1 ? dev.sms - 2 : dev.sms / 4);
+  if (cap < 1 || (NU > cap && mode != 1 && (packed || chunks < kMinBatchedChunks))) return plan;
+  if (HV <= cap) {  // whole sequences per launch, spread evenly
+    const int seqs_cap = cap / HV;
+    plan.launches = (NS + seqs_cap - 1) / seqs_cap;
+    plan.per_launch = ((NS + plan.launches - 1) / plan.launches) * HV;
+  } else {
+    plan.launches = (NU + cap - 1) / cap;
+    plan.per_launch = (NU + plan.launches - 1) / plan.launches;
+  }
+  return plan;
+}
+long chunks_per_unit(const FwdParams& p) {  // per sequence (the mean, with cu_seqlens)
+  const long len = p.cu ? static_cast<long>(p.T) / std::max(p.num_seqs, 1) : static_cast<long>(p.T);
+  return (len + tc::C - 1) / tc::C;
 }
 
 
@@ -2669,12 +2722,13 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const int NU = p.num_seqs * p.HV;
   const DeviceInfo& dev = device_info();
-  if (use_split_kernel(NU)) {
-    // one memset: the status word, the profile words and the flags behind them
-    if (cudaMemsetAsync(p.status, 0, kFlagOffset + NU * kFlagBytesPerUnit, stream) != cudaSuccess)
+  const SplitPlan plan = split_plan(p.num_seqs, p.HV, chunks_per_unit(p), p.cu != nullptr);
+  if (plan.launches > 0) {
+    // one memset: the status word, the profile words and the flags behind them; a later
+    // launch resets its flags only, so that the status word gathers every launch's reports
+    if (cudaMemsetAsync(p.status, 0, kFlagOffset + plan.per_launch * kFlagBytesPerUnit, stream) != cudaSuccess)
       return cudaGetLastError();
     const int nt_max = (p.T + tc::C - 1) / tc::C;
-    const int nrec = nt_max * NU;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(dev.sms);
     cfg.blockDim = dim3(tc::split::NTHREADS);
@@ -2686,8 +2740,20 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!p.h && !tc::make_map(&maps.o, p.out, tc::VD, p.HV, tokens)) return cudaErrorInvalidValue;
-    return p.prestage ? cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<true>, maps, p, NU, nrec)
-                      : cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<false>, maps, p, NU, nrec);
+    for (int b = 0; b < plan.launches; ++b) {
+      FwdParams pb = p;
+      pb.unit0 = b * plan.per_launch;
+      const int nu = std::min(plan.per_launch, NU - pb.unit0);
+      if (nu <= 0) break;
+      if (b > 0 && cudaMemsetAsync(reinterpret_cast<uint8_t*>(p.status) + kFlagOffset, 0, nu * kFlagBytesPerUnit,
+                                   stream) != cudaSuccess)
+        return cudaGetLastError();
+      const cudaError_t e = p.prestage
+                                ? cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<true>, maps, pb, nu, nt_max * nu)
+                                : cudaLaunchKernelEx(&cfg, tc::kda_chunk_split_kernel<false>, maps, pb, nu, nt_max * nu);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   }
   if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return cudaGetLastError();
   if (!dev.fused_attr) return cudaErrorInvalidConfiguration;
@@ -2700,10 +2766,23 @@ cudaError_t launch_chunk_tc_fwd(const FwdParams& p, cudaStream_t stream) {
 }
 
 // Name of the kernel the chunked forward launches for this problem on the current device.
-const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int units) {
+const char* chunk_kernel_name(bool bf16, int K, int V, long tokens, int num_seqs, int HV, bool packed) {
+  const int units = num_seqs * HV;
   if (tokens <= 0 || units <= 0) return "none";
   if (!(bf16 && K == tc::KD && V == tc::VD && tc::encoder() != nullptr)) return "recurrent_fwd_kernel";
-  return use_split_kernel(units) ? "kda_chunk_split_kernel" : "kda_chunk_fused_kernel";
+  const long len = tokens / num_seqs;
+  return split_plan(num_seqs, HV, (len + tc::C - 1) / tc::C, packed).launches > 0 ? "kda_chunk_split_kernel"
+                                                                                 : "kda_chunk_fused_kernel";
+}
+
+// Launches of that kernel per call (the split kernel covers many units in several).
+int chunk_kernel_launches(bool bf16, int K, int V, long tokens, int num_seqs, int HV, bool packed) {
+  const int units = num_seqs * HV;
+  if (tokens <= 0 || units <= 0) return 0;
+  if (!(bf16 && K == tc::KD && V == tc::VD && tc::encoder() != nullptr)) return 1;
+  const long len = tokens / num_seqs;
+  const SplitPlan plan = split_plan(num_seqs, HV, (len + tc::C - 1) / tc::C, packed);
+  return plan.launches > 0 ? plan.launches : 1;
 }
 
 }  // namespace kda

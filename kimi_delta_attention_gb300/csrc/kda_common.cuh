@@ -55,6 +55,9 @@ struct FwdParams {
   int T;                 // tokens per sequence (fixed length) or packed total
   int H, HV, K, V;
   int num_seqs;          // NS
+  // Split chunk kernel: the launch takes the (sequence, value head) units [unit0, unit0 + NU)
+  // of the sequence-major enumeration (larger problems run as several launches).
+  int unit0;
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

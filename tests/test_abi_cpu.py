@@ -59,6 +59,9 @@ def test_kernel_name_query(lib):
     empty = _lib.KdaShape(1, 0, 2, 2, 128, 128, 0, _lib.KDA_BF16)
     assert kda.kda_chunk_fwd_kernel_name(empty) == "none"
     assert lib.kda_chunk_fwd_kernel_name(None) == b"none"
+    assert kda.kda_chunk_fwd_kernel_launches(f32) == 1
+    assert kda.kda_chunk_fwd_kernel_launches(empty) == 0
+    assert lib.kda_chunk_fwd_kernel_launches(None) == 0
 
 
 FAKE = 0x10000  # aligned, never dereferenced

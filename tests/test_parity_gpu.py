@@ -248,3 +248,31 @@ def test_call_on_another_stream_keeps_its_temporaries():
     torch.cuda.synchronize()
     del junk
     assert torch.equal(o, ref_o) and torch.equal(s, ref_s)
+
+
+def test_split_kernel_over_several_launches():
+    """More units than one split launch holds: launches of whole sequences on the same
+    workspace (the status word gathers every launch's report)."""
+    x = W.make_inputs(3, 1100, 2, 16, 128, 128, "bf16", seed=21, init_state=True)   # 48 units, 18 chunks
+    d = x.to("cuda")
+    shape = kda.make_shape(d.q, d.v)
+    assert kda.kda_chunk_fwd_kernel_name(shape) == "kda_chunk_split_kernel"
+    assert kda.kda_chunk_fwd_kernel_launches(shape) >= 2
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    o, S = kda.kda_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.scale, initial_state=d.initial_state, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.kda_read_device_status(ws) == 0
+    o_ref, S_ref = oracle_full(x)
+    assert_close(o.float().cpu().numpy(), S.cpu().numpy(), o_ref, S_ref, "bf16", "split launches")
+
+
+def test_split_kernel_launches_varlen():
+    """Packed sequences of mixed lengths (empty ones included), the split kernel forced:
+    several launches of whole sequences."""
+    lens = [0, 1, 300, 64, 777, 129, 2, 1000, 65]
+    x = W.make_inputs(1, 0, 2, 8, 128, 128, "bf16", seed=22, init_state=True, lengths=lens)   # 72 units
+    o, S = run("chunk_split", x)
+    o_ref, S_ref = oracle_full(x)
+    assert_close(o.float().cpu().numpy(), S.cpu().numpy(), o_ref, S_ref, "bf16", "split launches varlen")
+    s0 = x.initial_state.numpy()
+    assert np.array_equal(S[0].cpu().numpy(), s0[0])
