@@ -35,6 +35,8 @@ L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["kimi_delta_attention_gb300/csrc/kda_chunk_tc.cu",
                   "kimi_delta_attention_gb300/csrc/kda_recurrent.cu",
+                  "kimi_delta_attention_gb300/csrc/kda_decode.cu",
+                  "kimi_delta_attention_gb300/csrc/kda_backward.cu",
                   "kimi_delta_attention_gb300/csrc/sm103.cuh",
                   "kimi_delta_attention_gb300/csrc/kda_common.cuh"]
 
@@ -322,7 +324,11 @@ def run_gpu(args):
     alg_bytes = input_bytes(host) + 2 * x.v.numel() + NS * HV * K * V * 4  # inputs once, o and the final state
     hbm_gbs, bf16_tf, peak_src = load_peaks()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    kernel_name = kda.kda_chunk_fwd_kernel_name(shape)  # the one launch of each step
+    kernel_name = kda.kda_chunk_fwd_kernel_name(shape)
+    # launches of that kernel per step (several for the split kernel over many units): a
+    # launch moves its share of the step's bytes in its share of the step's time, so the
+    # per-launch roofline fraction is the step's
+    launches = kda.kda_chunk_fwd_kernel_launches(shape)
 
     # end to end through the public API with pinned host buffers
     e2e = e2e_measure(kda, host, gate, dev, stream, max(3, min(args.steps, 20 if tokens <= 1 << 16 else 5)))
@@ -340,10 +346,11 @@ def run_gpu(args):
         "roofline_time_ms": max(alg_bytes / (hbm_gbs * 1e9), flops / (bf16_tf * 1e12)) * 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                      "frac": achieved / hbm_gbs, "traffic": load_traffic(kernel_name, w.name),
-                     "kernel": kernel_name, "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel": kernel_name, "launches_per_step": launches,
+                     "algorithmic_bytes_per_launch": alg_bytes / launches,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
-        "clocks": sampler.summary(), "e2e": e2e, "gpu_launches": args.steps * 1,
+        "clocks": sampler.summary(), "e2e": e2e, "gpu_launches": args.steps * launches,
         "device_status": status, "wall_s_timed_region": t_wall,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
