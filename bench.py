@@ -586,6 +586,83 @@ def run_twopass(args):
     return 0
 
 
+BACKWARD_METRIC = ("KDA backward (gradients of q, k, v, g, beta and the initial state through the token "
+                   "recurrence, fp32) tokens/s on 1 GB300 (T=4096, H=HV=32, K=V=128); % of fp32 CUDA-core peak")
+# fp32 CUDA-core peak the backward is reported against: 152 SMs x 128 fp32 lanes x 2 flop
+# (one FMA) x 2.07 GHz, the maximum SM clock
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def backward_flops(tokens_heads: int, K: int, V: int) -> float:
+    """Arithmetic of the backward as the kernel evaluates it, per (token, value head): a
+    forward sweep and a recompute of each token state (decay, P^T k, rank-1 update: 5 K V
+    each) and the reverse step (P, u, dq, dS += q do^T, dS^T k, dk's two products, dP, dg,
+    the decayed dS: 18 K V)."""
+    return tokens_heads * 28.0 * K * V
+
+
+def run_backward(args):
+    """One step = one kda_backward call on the headline shape (bf16 q, k, v, d_out; fp32 g,
+    beta; a final-state gradient), L2 flushed between steps."""
+    import numpy as np
+    import torch
+    import kimi_delta_attention_gb300 as kda
+    from kimi_delta_attention_gb300 import workloads as W
+    kda.build()
+    kda.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, T, H, HV, K, V = 1, 4096, 32, 32, 128, 128
+    host = W.make_inputs(B, T, H, HV, K, V, "bf16", seed=21, init_state=False)
+    rng = np.random.default_rng(22)
+    do_h = torch.from_numpy(rng.standard_normal((B, T, HV, V), dtype=np.float32)).to(torch.bfloat16)
+    dfin_h = torch.from_numpy(rng.standard_normal((B, HV, K, V), dtype=np.float32))
+    x = host.to(dev)
+    do, dfin = do_h.to(dev), dfin_h.to(dev)
+    shape = kda.make_shape(x.q, x.v)
+    ws = torch.empty(kda.kda_backward_workspace_size(shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return kda.kda_backward(x.q, x.k, x.v, x.g, x.beta, do, x.scale, d_final_state=dfin, workspace=ws,
+                                stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    tokens = B * T
+    flops = backward_flops(tokens * HV, K, V)
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "kda_gb300", "metric": BACKWARD_METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "backward_bf16_T4096_H32_K128", "B": B, "T": T, "H": H, "HV": HV, "K": K, "V": V,
+                   "io": "bf16 q/k/v/d_out, fp32 g/beta/d_final_state; fp32 gradients",
+                   "l2": "flushed between timed steps"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None, "kernel": "recurrent_bwd_kernel",
+                     "flops_per_launch": flops,
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"},
+        "clocks": sampler.summary(), "gpu_launches": args.steps,
+        "device_status": kda.kda_read_device_status(ws),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,7 +672,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gated", action="store_true",
                     help="raw bf16 inputs through kda_chunk_fwd_gated (pre-stage fused, bounded gate)")
-    ap.add_argument("--mode", default="forward", choices=["forward", "decode", "twopass"],
+    ap.add_argument("--mode", default="forward", choices=["forward", "decode", "twopass", "backward"],
                     help="decode: time kda_decode (one token per sequence) instead of the chunked forward")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (0-4); 1, the headline, is the default bench line")
@@ -604,6 +681,8 @@ def main():
         return run_reference(args)
     if args.mode == "decode":
         return run_decode(args)
+    if args.mode == "backward":
+        return run_backward(args)
     if args.mode == "twopass":
         return run_twopass(args)
     return run_gpu(args)
