@@ -271,10 +271,11 @@ KDA_API const char* kda_chunk_fwd_kernel_name(const kda_shape* shape);
  * How many times kda_chunk_fwd launches that kernel for `shape` (0 when there is no
  * work; host-only).  The split kernel gives every (sequence, value head) unit of a
  * launch its own SM for the serial state scan, at most 38 units per launch on a 152-SM
- * GB300 (three quarters of the SMs prepare chunks).  Fixed-length problems with more
- * units and at least 16 chunks per sequence run as several launches of whole sequences,
- * stream-ordered on the caller's stream; packed sequences and shorter problems with
- * more units run the cluster kernel once.
+ * GB300 (three quarters of the SMs prepare chunks).  Problems with more units and at
+ * least 16 chunks per sequence (on average) run as several launches of whole sequences,
+ * stream-ordered on the caller's stream (packed sequences only when a launch holds one
+ * sequence, i.e. more than 19 value heads); other problems with more units run the
+ * cluster kernel once.
  */
 KDA_API int kda_chunk_fwd_kernel_launches(const kda_shape* shape);
 

@@ -1418,7 +1418,7 @@ constexpr int kRecStorer = 32;  // pipeline thread storing qd and kr^T to the ri
 #endif
 template <bool PRE>
 __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, uint8_t* sm, uint32_t tmem,
-                                         int pipe, int q, int NQ, int NU, int NREC, uint32_t* flags) {
+                                         int pipe, int q, int NQ, int NU, int NREC_BOUND, uint32_t* flags) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pt = tid & 255;
   const int pw = warp & 7;       // warp within the pipeline
@@ -1480,6 +1480,20 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
     if (part == 0 && pt < C)
       bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + x.hv) : 0.f;
   };
+  // Records of this launch: chunk-major over its units, up to the longest of their
+  // sequences (the host passes a bound; with cu_seqlens the lengths are read here, so
+  // that no pipeline walks the empty tail of a bound set by the packed total)
+  int NREC = NREC_BOUND;
+  if (p.cu) {
+    int mx = 0;
+    for (int sq = p.unit0 / HV; sq <= (p.unit0 + NU - 1) / HV; ++sq) {
+      long t0;
+      int len;
+      seq_range(p, sq, t0, len);
+      mx = max(mx, (len + C - 1) / C);
+    }
+    NREC = min(NREC_BOUND, mx * NU);
+  }
   auto next_valid = [&](int r, Rec& x) {
     while (r < NREC && !rec_at(p, NU, r, x)) r += NQ;
     return r;
@@ -2680,10 +2694,11 @@ const DeviceInfo& device_info() {
 // three quarters of the SMs to the producers), or launches == 0 when the cluster kernel
 // runs instead.  A launch takes whole sequences where a sequence's heads fit one.  More
 // units than one launch holds pay a launch's start (~20 us before its chains have
-// records) per launch, which long sequences of one length amortise: fixed-length
-// problems with at least kMinBatchedChunks chunks per sequence run as several launches;
-// packed sequences (a launch lasts as long as its longest one) and shorter ones run the
-// cluster kernel.
+// records) per launch, which long sequences amortise: problems with at least
+// kMinBatchedChunks chunks per sequence (on average) run as several launches.  With
+// packed sequences a launch lasts as long as its longest one, so they take that path
+// only when a launch holds one sequence (HV > cap / 2); other packed problems with more
+// units, and shorter ones, run the cluster kernel.
 constexpr long kMinBatchedChunks = 16;
 struct SplitPlan {
   int launches = 0, per_launch = 0;
@@ -2695,7 +2710,7 @@ SplitPlan split_plan(int NS, int HV, long chunks, bool packed) {
   SplitPlan plan;
   if (!dev.coop || !dev.split_fits || mode == 0 || NU < 1) return plan;
   const int cap = std::min(kMaxSplitUnits, mode == 1 ? dev.sms - 2 : dev.sms / 4);
-  if (cap < 1 || (NU > cap && mode != 1 && (packed || chunks < kMinBatchedChunks))) return plan;
+  if (cap < 1 || (NU > cap && mode != 1 && ((packed && 2 * HV <= cap) || chunks < kMinBatchedChunks))) return plan;
   if (HV <= cap) {  // whole sequences per launch, spread evenly
     const int seqs_cap = cap / HV;
     plan.launches = (NS + seqs_cap - 1) / seqs_cap;
