@@ -428,6 +428,24 @@ __device__ __forceinline__ void activate(float2 (&g)[16], float& beta, int kind,
   if (pt < C) beta = pt < rows ? sigmoid_approx(beta) : 0.f;
 }
 
+// The gate rows a thread prefetched (rows 16 hq + [0, 16), key dims 2 dp, 2 dp + 1) are
+// loaded unconditionally from row min(c, rows - 1), so that no instruction waits for
+// them before their first use: with PRE the raw bf16 pair sits in .x; rows past the end
+// become 0, as does beta there.
+template <bool PRE>
+__device__ __forceinline__ void finish_gate_rows(float2 (&g)[16], float& beta, int hq, int pt, int rows) {
+  const int nvalid = rows - 16 * hq;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (PRE) {
+      const uint32_t w = __float_as_uint(g[i].x);
+      g[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+    if (i >= nvalid) g[i] = make_float2(0.f, 0.f);
+  }
+  if (pt >= rows) beta = 0.f;
+}
+
 // 1 / sqrt(|row|^2 + 1e-6) of every row of the stacked raw tile (k and q rows), into
 // rn[stacked row]: thread pt sums the squares of K-block pt & 1 of stacked row pt / 2,
 // its neighbour lane the other K-block.
@@ -786,24 +804,22 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
     auto prefetch_gb = [&](int m, int part) {
       const int rows = min(C, len - m * C);
       const long base = tok0 + static_cast<long>(m) * C;
-      if (PRE) {  // raw gate input, bf16 pairs
+      // unconditional loads (rows past the end read the last row; finish_gate_rows masks them)
+      if (PRE) {  // raw gate input, bf16 pairs (kept raw in .x)
 #pragma unroll
         for (int i = 4 * part; i < 4 * part + 4; ++i) {
-          const int c = 16 * hq + i;
-          const uint32_t w =
-              (c < rows) ? __ldg(reinterpret_cast<const uint32_t*>(p.g_raw + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp)
-                         : 0u;
-          gpre[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+          const int c = min(16 * hq + i, rows - 1);
+          gpre[i].x = __uint_as_float(
+              __ldg(reinterpret_cast<const uint32_t*>(p.g_raw + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp));
         }
       } else {
 #pragma unroll
         for (int i = 4 * part; i < 4 * part + 4; ++i) {
-          const int c = 16 * hq + i;
-          gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp)
-                               : make_float2(0.f, 0.f);
+          const int c = min(16 * hq + i, rows - 1);
+          gpre[i] = __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + hv) * KD) + dp);
         }
       }
-      if (part == 0 && pt < C) bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + hv) : 0.f;
+      if (part == 0 && pt < C) bpre = __ldg(p.beta + static_cast<size_t>(base + min(pt, rows - 1)) * HV + hv);
     };
     bool pub_pending = false;  // record j-1 stored but not yet published
     // Record jp is complete in the ring: tell the NSLICE consumers, one lane each
@@ -844,6 +860,7 @@ kda_chunk_fused_kernel(const __grid_constant__ Maps maps, const FwdParams p) {
       }
       if (!mbar_wait(&bars[B_RAW], j & 1, p.wait_ns)) timeout();
       if (pt == 0) bulk_wait_read();  // the previous record's Aqk, W and U stagings have been read
+      prep::finish_gate_rows<PRE>(gpre, bpre, hq, pt, rows);
       if (PRE) {  // activations, and the raw q, k row norms (read before the pass rewrites the rows)
         prep::activate(gpre, bpre, p.prestage, p.lower_bound, expf(a_log), dt, hq, pt, rows);
         prep::row_norms(pb, rn, pt);
@@ -1460,26 +1477,24 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
   auto prefetch_gb = [&](const Rec& x, int part) {
     const int rows = min(C, x.len - x.m * C);
     const long base = x.tok0 + static_cast<long>(x.m) * C;
-    if (PRE) {  // raw gate input, bf16 pairs
+    // unconditional loads (rows past the end read the last row; finish_gate_rows masks them)
+    if (PRE) {  // raw gate input, bf16 pairs (kept raw in .x)
 #pragma unroll
       for (int i = 4 * part; i < 4 * part + 4; ++i) {
-        const int c = 16 * hq + i;
-        const uint32_t w =
-            (c < rows) ? __ldg(reinterpret_cast<const uint32_t*>(p.g_raw + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp)
-                       : 0u;
-        gpre[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        const int c = min(16 * hq + i, rows - 1);
+        gpre[i].x = __uint_as_float(
+            __ldg(reinterpret_cast<const uint32_t*>(p.g_raw + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp));
       }
     } else {
 #pragma unroll
       for (int i = 4 * part; i < 4 * part + 4; ++i) {
-        const int c = 16 * hq + i;
-        gpre[i] = (c < rows) ? __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp)
-                             : make_float2(0.f, 0.f);
+        const int c = min(16 * hq + i, rows - 1);
+        gpre[i] = __ldg(reinterpret_cast<const float2*>(p.g + (static_cast<size_t>(base + c) * HV + x.hv) * KD) + dp);
       }
     }
-    if (part == 0 && pt < C)
-      bpre = (pt < rows) ? __ldg(p.beta + static_cast<size_t>(base + pt) * HV + x.hv) : 0.f;
+    if (part == 0 && pt < C) bpre = __ldg(p.beta + static_cast<size_t>(base + min(pt, rows - 1)) * HV + x.hv);
   };
+
   // Records of this launch: chunk-major over its units, up to the longest of their
   // sequences (the host passes a bound; with cu_seqlens the lengths are read here, so
   // that no pipeline walks the empty tail of a bound set by the packed total)
@@ -1511,10 +1526,20 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
 
   Rec cur, nx;
   int r = next_valid(q, cur);
+#ifdef KDA_PROFILE
+  // [116] the first pipeline found its first record, [117] issued its raw tiles, [118] its gate loads
+  if (q == 0 && pt == 0) reinterpret_cast<uint64_t*>(p.status)[116] = globaltimer_ns();
+#endif
   if (r < NREC) {
     if (pt == 0) issue_raw(cur, 0);
+#ifdef KDA_PROFILE
+    if (q == 0 && pt == 0) reinterpret_cast<uint64_t*>(p.status)[117] = globaltimer_ns();
+#endif
 #pragma unroll
     for (int part = 0; part < 4; ++part) prefetch_gb(cur, part);
+#ifdef KDA_PROFILE
+    if (q == 0 && pt == 0) reinterpret_cast<uint64_t*>(p.status)[118] = globaltimer_ns();
+#endif
   }
   bool pub_pending = false;
   int pub_m = 0, pub_u = 0;
@@ -1535,9 +1560,17 @@ __device__ __forceinline__ void producer(const Maps& maps, const FwdParams& p, u
       dt = __ldg(reinterpret_cast<const float2*>(p.dt_bias + static_cast<size_t>(cur.hv) * KD) + dp);
     }
     PSTAMP(0);
+#ifdef KDA_PROFILE
+    // [125] the first producer pipeline's first record: loop top, [126] its raw tiles landed
+    if (q == 0 && j == 0 && pt == 0) reinterpret_cast<uint64_t*>(p.status)[125] = globaltimer_ns();
+#endif
     if (!mbar_wait(&bars[PB_RAW], j & 1, p.wait_ns)) timeout();
+#ifdef KDA_PROFILE
+    if (q == 0 && j == 0 && pt == 0) reinterpret_cast<uint64_t*>(p.status)[126] = globaltimer_ns();
+#endif
     PSTAMP(1);
     if (pt == 0 || pt == kRecStorer) bulk_wait_read();  // the previous record's stagings have been read
+    prep::finish_gate_rows<PRE>(gpre, bpre, hq, pt, rows);
     if (PRE) {  // activations, and the raw q, k row norms (read before the pass rewrites the rows)
       prep::activate(gpre, bpre, p.prestage, p.lower_bound, expf(a_log), dt, hq, pt, rows);
       prep::row_norms(sm, rnorm, pt);
@@ -2256,6 +2289,10 @@ kda_chunk_split_kernel(const __grid_constant__ Maps maps, const FwdParams p, int
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+#ifdef KDA_PROFILE
+  // [119] the first producer CTA past its TMEM allocation and the block barrier
+  if (tid == 0 && static_cast<int>(blockIdx.x) == NU) reinterpret_cast<uint64_t*>(p.status)[119] = globaltimer_ns();
+#endif
   if (is_chain) {
     split::chain(maps, p, sm, tmem, static_cast<int>(blockIdx.x), flags);
   } else {  // records r = m NU + u, strided over the producer pipelines
