@@ -184,9 +184,10 @@ KDA_API kda_status kda_chunk_output(const kda_shape* shape, const void* q, const
  * with respect to every input of kda_chunk_fwd (same shapes and conventions; the
  * method's recurrence, page "手撕KDA" section "1 Naive"; the pages' own backward,
  * sections 2 and 4 of that page, works on the chunked form).  Reverse mode through
- * the token recurrence on CUDA cores in fp32: a forward sweep keeps the fp32 state
- * entering every 64-token chunk in the workspace, then each chunk's token states are
- * recomputed and swept in reverse.
+ * the token recurrence on CUDA cores in fp32, one CTA per 32 value columns of a
+ * (sequence, value head): a forward sweep keeps the fp32 state entering every 64-token
+ * chunk in the workspace, then each chunk's token states are recomputed and swept in
+ * reverse.
  *
  *   d_out          [B, T, HV, V]  io_dtype
  *   d_final_state  [NS, HV, K, V] fp32 or NULL (zeros)

@@ -383,8 +383,10 @@ kda_status kda_backward(const kda_shape* s, const void* q, const void* k, const 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint32_t* status = static_cast<uint32_t*>(workspace);
   if (cudaMemsetAsync(status, 0, sizeof(uint32_t), cs) != cudaSuccess) return KDA_ERR_CUDA;
-  // dq and dk gather the value heads that share a key head: zero them first
-  if (tokens > 0 && (cudaMemsetAsync(dq, 0, f_qk, cs) != cudaSuccess || cudaMemsetAsync(dk, 0, f_qk, cs) != cudaSuccess))
+  // dq and dk gather the value heads that share a key head, and dq, dk, dg and dbeta the
+  // kernel's value-column slices: zero them first
+  if (tokens > 0 && (cudaMemsetAsync(dq, 0, f_qk, cs) != cudaSuccess || cudaMemsetAsync(dk, 0, f_qk, cs) != cudaSuccess ||
+                     cudaMemsetAsync(dg, 0, n_g, cs) != cudaSuccess || cudaMemsetAsync(dbeta, 0, n_b, cs) != cudaSuccess))
     return KDA_ERR_CUDA;
   float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
   const cudaError_t e = kda::launch_backward(

@@ -12,14 +12,17 @@
 // "手撕KDA" sections 2 and 4, works on the chunked form; this is the same derivative
 // taken through the recurrence it evaluates.)
 //
-// One CTA per (sequence, value head), 256 threads, each holding 4 adjacent value
-// columns of K / (1024 / V) state rows (as the decode kernel).  The states the
-// reverse sweep needs are recomputed: a forward sweep stores the fp32 state entering
-// every 64-token chunk in the workspace, then, chunk by chunk from the last, the
-// chunk's 64 token states are recomputed into the workspace and swept in reverse.
-// Reductions over K go through shared memory, reductions over V are warp shuffles (a
-// halving reduce-scatter: 16 row sums in 16 shuffles).  dq and dk are summed over the
-// value heads that share a key head with atomics (the launcher zeroes them first).
+// The state recurrence and its reverse are independent across value columns; only dq,
+// dk, dg and dbeta sum over them.  So each (sequence, value head) is split into V / 32
+// slices of 32 value columns, one CTA each: 256 threads, each holding 4 adjacent columns
+// of K / 32 state rows.  The states the reverse sweep needs are recomputed: a forward
+// sweep stores the fp32 state slice entering every 64-token chunk in the workspace,
+// then, chunk by chunk from the last, the chunk's 64 token states are recomputed into
+// the workspace and swept in reverse.  Reductions over K go through shared memory,
+// reductions over a slice's columns are warp shuffles among the row's 8 lanes (a
+// halving reduce-scatter: one row sum per lane pair); the slices' partial dq, dk, dg
+// and dbeta (and those of the value heads sharing a key head, for dq and dk) meet in
+// fp32 atomics on outputs the launcher zeroes first.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -27,6 +30,7 @@ namespace bwd {
 
 constexpr int NT = 256;
 constexpr int CH = 64;  // tokens per checkpoint
+constexpr int VS = 32;  // value columns per CTA
 
 struct Params {
   const void* q;       // [tokens, H, K]  io type
@@ -44,7 +48,7 @@ struct Params {
   float* dg;           // [tokens, HV, K]
   float* dbeta;        // [tokens, HV]
   float* ds0;          // [NS, HV, K, V] or null
-  float* scratch;      // per unit: (max chunks + CH) x K x V fp32
+  float* scratch;      // per unit: (max chunks + CH) x K x V fp32 (V / 32 slices of it)
   uint32_t* status;
   size_t unit_floats;  // floats of scratch per unit
   float scale;
@@ -105,11 +109,13 @@ __device__ __forceinline__ bool halve_writer(int lane) {
 
 template <typename IO, int K, int V>
 __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
-  constexpr int TPR = V / 4;    // threads across a state row
+  constexpr int TPR = VS / 4;   // threads across a state row of the slice
   constexpr int RG = NT / TPR;  // row groups
   constexpr int RPT = K / RG;   // rows per thread: rg + RG i
-  static_assert(RPT * RG == K && TPR * 4 == V && (TPR == 32 || TPR == 16), "backward tiling");
-  const int hv = blockIdx.x, seq = blockIdx.y;
+  constexpr int NSPLIT = V / VS;
+  static_assert(RPT * RG == K && TPR == 8 && NSPLIT * VS == V && K + VS <= NT, "backward tiling");
+  const int slice = blockIdx.x, hv = blockIdx.y, seq = blockIdx.z;
+  const int v0 = VS * slice;
   const int tid = threadIdx.x, lane = tid & 31;
   const int cg = tid % TPR, rg = tid / TPR;
   const int hk = hv / (p.HV / p.H);
@@ -118,30 +124,49 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
   const IO* v = static_cast<const IO*>(p.v);
   const IO* dout = static_cast<const IO*>(p.d_out);
 
-  __shared__ float s_q[K], s_k[K], s_e[K], s_v[V], s_do[V], s_b;
-  __shared__ __align__(16) float red[RG][V];
-  __shared__ __align__(16) float col[V];   // a reduced V-vector (u, then kd)
+  __shared__ float s_q[K], s_k[K], s_e[K], s_v[VS], s_do[VS], s_b;
+  constexpr int NW = NT / 32;
+  __shared__ __align__(16) float red[NW][VS];
+  __shared__ __align__(16) float col[VS];   // a reduced vector over the slice's columns (u, then kd)
 
   long tok0;
   int len;
   seq_bounds(p, seq, tok0, len);
   const int nch = (len + CH - 1) / CH;
   const size_t unit = static_cast<size_t>(seq) * p.HV + hv;
-  float* ckpt = p.scratch + unit * p.unit_floats;           // [nch][K][V]
-  float* toks = ckpt + static_cast<size_t>(nch > 0 ? nch : 1) * K * V;  // [CH][K][V]
-  auto slot = [&](float* base, int i) { return base + static_cast<size_t>(rg + RG * i) * V + 4 * cg; };
+  const size_t state_col = unit * K * V + v0 + 4 * cg;  // this thread's columns in a [K][V] state
+  float* ckpt = p.scratch + unit * p.unit_floats + slice * (p.unit_floats / NSPLIT);  // [nch][K][VS]
+  float* toks = ckpt + static_cast<size_t>(nch > 0 ? nch : 1) * K * VS;              // [CH][K][VS]
+  auto slot = [&](float* base, int i) { return base + static_cast<size_t>(rg + RG * i) * VS + 4 * cg; };
 
-  auto stage = [&](int t) {  // token t of the sequence: q, k, e^g, v, do, beta
+  // Token inputs (q, k, g; the slice of v and do; beta) are fetched into registers one
+  // token ahead and staged into shared memory at the next step, so that no step waits
+  // for its own global loads: fetch(t) issues the loads, stage() writes the values.
+  float f0 = 0.f, f1 = 0.f, f2 = 0.f;
+  auto fetch = [&](int t) {
     const size_t tok = static_cast<size_t>(tok0 + t);
     if (tid < K) {
-      s_q[tid] = to_f32(q[(tok * p.H + hk) * K + tid]);
-      s_k[tid] = to_f32(k[(tok * p.H + hk) * K + tid]);
-      s_e[tid] = expf(p.g[(tok * p.HV + hv) * K + tid]);
-    } else if (tid < K + V) {
-      s_v[tid - K] = to_f32(v[(tok * p.HV + hv) * V + (tid - K)]);
-      s_do[tid - K] = to_f32(dout[(tok * p.HV + hv) * V + (tid - K)]);
+      f0 = to_f32(q[(tok * p.H + hk) * K + tid]);
+      f1 = to_f32(k[(tok * p.H + hk) * K + tid]);
+      f2 = p.g[(tok * p.HV + hv) * K + tid];
+    } else if (tid < K + VS) {
+      f0 = to_f32(v[(tok * p.HV + hv) * V + v0 + (tid - K)]);
+      f1 = to_f32(dout[(tok * p.HV + hv) * V + v0 + (tid - K)]);
+    } else if (tid == NT - 1) {
+      f0 = p.beta[tok * p.HV + hv];
     }
-    if (tid == NT - 1) s_b = p.beta[tok * p.HV + hv];
+  };
+  auto stage = [&]() {
+    if (tid < K) {
+      s_q[tid] = f0;
+      s_k[tid] = f1;
+      s_e[tid] = expf(f2);
+    } else if (tid < K + VS) {
+      s_v[tid - K] = f0;
+      s_do[tid - K] = f1;
+    } else if (tid == NT - 1) {
+      s_b = f0;
+    }
   };
   // u = P^T k over this thread's rows -> col[] (all rows); P = Diag(e) S in place
   auto reduce_k = [&](const float4 (&x)[RPT]) {
@@ -152,12 +177,20 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
       pu.x = fmaf(kd, x[i].x, pu.x); pu.y = fmaf(kd, x[i].y, pu.y);
       pu.z = fmaf(kd, x[i].z, pu.z); pu.w = fmaf(kd, x[i].w, pu.w);
     }
-    *reinterpret_cast<float4*>(&red[rg][4 * cg]) = pu;
+    // the warp's four row groups (lanes 8 apart hold the same columns), then the warps
+#pragma unroll
+    for (int m = TPR; m < 32; m <<= 1) {
+      pu.x += __shfl_xor_sync(0xFFFFFFFFu, pu.x, m);
+      pu.y += __shfl_xor_sync(0xFFFFFFFFu, pu.y, m);
+      pu.z += __shfl_xor_sync(0xFFFFFFFFu, pu.z, m);
+      pu.w += __shfl_xor_sync(0xFFFFFFFFu, pu.w, m);
+    }
+    if (lane < TPR) *reinterpret_cast<float4*>(&red[tid >> 5][4 * cg]) = pu;
     __syncthreads();
-    if (tid < V) {
+    if (tid < VS) {
       float a = 0.f;
 #pragma unroll
-      for (int r = 0; r < RG; ++r) a += red[r][tid];
+      for (int w = 0; w < NW; ++w) a += red[w][tid];
       col[tid] = a;
     }
     __syncthreads();
@@ -185,15 +218,17 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
   float4 s[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
-    s[i] = p.s0 ? *reinterpret_cast<const float4*>(p.s0 + unit * K * V + static_cast<size_t>(rg + RG * i) * V + 4 * cg)
+    s[i] = p.s0 ? *reinterpret_cast<const float4*>(p.s0 + state_col + static_cast<size_t>(rg + RG * i) * V)
                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (len > 0) fetch(0);
   for (int t = 0; t < len; ++t) {
     if (t % CH == 0) {
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(ckpt + static_cast<size_t>(t / CH) * K * V, i)) = s[i];
+      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(ckpt + static_cast<size_t>(t / CH) * K * VS, i)) = s[i];
     }
     __syncthreads();  // the previous step's reads of the staged token are done
-    stage(t);
+    stage();
+    if (t + 1 < len) fetch(t + 1);
     __syncthreads();
     forward_step(s);
   }
@@ -202,29 +237,41 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
   float4 ds[RPT];  // the state's gradient
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
-    ds[i] = p.d_fin ? *reinterpret_cast<const float4*>(p.d_fin + unit * K * V + static_cast<size_t>(rg + RG * i) * V + 4 * cg)
+    ds[i] = p.d_fin ? *reinterpret_cast<const float4*>(p.d_fin + state_col + static_cast<size_t>(rg + RG * i) * V)
                     : make_float4(0.f, 0.f, 0.f, 0.f);
   const bool writer = halve_writer<RPT, TPR>(lane);
   for (int n = nch - 1; n >= 0; --n) {
     const int t0 = n * CH, t1 = min(len, t0 + CH);
     // recompute the chunk's token states (the state before each token)
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float4*>(slot(ckpt + static_cast<size_t>(n) * K * V, i));
+    for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float4*>(slot(ckpt + static_cast<size_t>(n) * K * VS, i));
+    if (t0 + 1 < t1) fetch(t0);
     for (int t = t0; t < t1; ++t) {
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(toks + static_cast<size_t>(t - t0) * K * V, i)) = s[i];
+      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(toks + static_cast<size_t>(t - t0) * K * VS, i)) = s[i];
       if (t + 1 == t1) break;  // the last token's successor is not needed
       __syncthreads();
-      stage(t);
+      stage();
+      if (t + 2 < t1) fetch(t + 1);
       __syncthreads();
       forward_step(s);
     }
+    // the token states are read one token ahead too (this thread wrote them above)
+    fetch(t1 - 1);
+    float4 Pn[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) Pn[i] = *reinterpret_cast<const float4*>(slot(toks + static_cast<size_t>(t1 - 1 - t0) * K * VS, i));
     for (int t = t1 - 1; t >= t0; --t) {
       __syncthreads();
-      stage(t);
+      stage();
+      if (t > t0) fetch(t - 1);
       float4 P[RPT];
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) P[i] = *reinterpret_cast<const float4*>(slot(toks + static_cast<size_t>(t - t0) * K * V, i));
+      for (int i = 0; i < RPT; ++i) P[i] = Pn[i];
+      if (t > t0) {
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) Pn[i] = *reinterpret_cast<const float4*>(slot(toks + static_cast<size_t>(t - 1 - t0) * K * VS, i));
+      }
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
@@ -258,12 +305,12 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
       reduce_k(ds);
       const float4 kdv = *reinterpret_cast<const float4*>(&col[4 * cg]);
       const float4 dr = make_float4(bt * kdv.x, bt * kdv.y, bt * kdv.z, bt * kdv.w);
-      if (rg == 0) *reinterpret_cast<float4*>(p.dv + (tok * p.HV + hv) * V + 4 * cg) = dr;
-      {  // dbeta: every row group holds all V columns of r and kd; row group 0's sum is kept
+      if (rg == 0) *reinterpret_cast<float4*>(p.dv + (tok * p.HV + hv) * V + v0 + 4 * cg) = dr;
+      {  // dbeta: every row group holds the slice's columns of r and kd; row group 0's sum is kept
         float db = r.x * kdv.x + r.y * kdv.y + r.z * kdv.z + r.w * kdv.w;
 #pragma unroll
         for (int m = TPR / 2; m >= 1; m >>= 1) db += __shfl_xor_sync(0xFFFFFFFFu, db, m);
-        if (tid == 0) p.dbeta[tok * p.HV + hv] = db;
+        if (tid == 0) atomicAdd(p.dbeta + tok * p.HV + hv, db);
       }
       // dk = beta dS r - P dr;  dP = dS - k dr^T;  dg = sum_j dP P;  dS = Diag(e) dP
       float dkv[RPT], dgv[RPT];
@@ -285,20 +332,20 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
       {
         int idx = 0;
         Halve<RPT, TPR / 2>::run(dgv, lane, idx);
-        if (writer) p.dg[(tok * p.HV + hv) * K + rg + RG * idx] = dgv[0];
+        if (writer) atomicAdd(p.dg + (tok * p.HV + hv) * K + rg + RG * idx, dgv[0]);
       }
     }
   }
   if (p.ds0) {
 #pragma unroll
     for (int i = 0; i < RPT; ++i)
-      *reinterpret_cast<float4*>(p.ds0 + unit * K * V + static_cast<size_t>(rg + RG * i) * V + 4 * cg) = ds[i];
+      *reinterpret_cast<float4*>(p.ds0 + state_col + static_cast<size_t>(rg + RG * i) * V) = ds[i];
   }
 }
 
 template <typename IO>
 cudaError_t launch_io(const Params& p, int K, int V, cudaStream_t stream) {
-  const dim3 grid(p.HV, p.num_seqs);
+  const dim3 grid(V / VS, p.HV, p.num_seqs);
   if (K == 128 && V == 128) recurrent_bwd_kernel<IO, 128, 128><<<grid, NT, 0, stream>>>(p);
   else if (K == 128 && V == 64) recurrent_bwd_kernel<IO, 128, 64><<<grid, NT, 0, stream>>>(p);
   else if (K == 64 && V == 128) recurrent_bwd_kernel<IO, 64, 128><<<grid, NT, 0, stream>>>(p);
