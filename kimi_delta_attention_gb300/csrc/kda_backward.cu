@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
   const IO* v = static_cast<const IO*>(p.v);
   const IO* dout = static_cast<const IO*>(p.d_out);
 
-  __shared__ float s_q[K], s_k[K], s_e[K], s_v[VS], s_do[VS], s_b;
+  // token inputs, double-buffered by step parity: a step stages the next token into the
+  // other buffer between the two barriers of one of its reductions over K
+  __shared__ float s_q[2][K], s_k[2][K], s_e[2][K], s_v[2][VS], s_do[2][VS], s_b[2];
   constexpr int NW = NT / 32;
   __shared__ __align__(16) float red[NW][VS];
   __shared__ __align__(16) float col[VS];   // a reduced vector over the slice's columns (u, then kd)
@@ -156,24 +158,27 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
       f0 = p.beta[tok * p.HV + hv];
     }
   };
-  auto stage = [&]() {
+  auto stage = [&](int b) {
     if (tid < K) {
-      s_q[tid] = f0;
-      s_k[tid] = f1;
-      s_e[tid] = expf(f2);
+      s_q[b][tid] = f0;
+      s_k[b][tid] = f1;
+      s_e[b][tid] = expf(f2);
     } else if (tid < K + VS) {
-      s_v[tid - K] = f0;
-      s_do[tid - K] = f1;
+      s_v[b][tid - K] = f0;
+      s_do[b][tid - K] = f1;
     } else if (tid == NT - 1) {
-      s_b = f0;
+      s_b[b] = f0;
     }
   };
-  // u = P^T k over this thread's rows -> col[] (all rows); P = Diag(e) S in place
-  auto reduce_k = [&](const float4 (&x)[RPT]) {
+  // x^T k over all rows (of the token in buffer b) -> col[].  Between its two barriers
+  // (every thread has finished the previous step after the first) the fetched token goes
+  // into buffer sb (if sb >= 0) and token ft is fetched (if ft >= 0); the second barrier
+  // makes the staged values visible.
+  auto reduce_k = [&](const float4 (&x)[RPT], int b, int sb, int ft) {
     float4 pu = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const float kd = s_k[rg + RG * i];
+      const float kd = s_k[b][rg + RG * i];
       pu.x = fmaf(kd, x[i].x, pu.x); pu.y = fmaf(kd, x[i].y, pu.y);
       pu.z = fmaf(kd, x[i].z, pu.z); pu.w = fmaf(kd, x[i].w, pu.w);
     }
@@ -193,22 +198,26 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
       for (int w = 0; w < NW; ++w) a += red[w][tid];
       col[tid] = a;
     }
+    if (sb >= 0) {
+      stage(sb);
+      if (ft >= 0) fetch(ft);
+    }
     __syncthreads();
   };
-  // one forward step on the state held in s (token staged)
-  auto forward_step = [&](float4 (&s)[RPT]) {
+  // one forward step on the state held in s (token in buffer b)
+  auto forward_step = [&](float4 (&s)[RPT], int b, int sb, int ft) {
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const float e = s_e[rg + RG * i];
+      const float e = s_e[b][rg + RG * i];
       s[i].x *= e; s[i].y *= e; s[i].z *= e; s[i].w *= e;
     }
-    reduce_k(s);
-    const float bt = s_b;
-    const float4 br = make_float4(bt * (s_v[4 * cg] - col[4 * cg]), bt * (s_v[4 * cg + 1] - col[4 * cg + 1]),
-                                  bt * (s_v[4 * cg + 2] - col[4 * cg + 2]), bt * (s_v[4 * cg + 3] - col[4 * cg + 3]));
+    reduce_k(s, b, sb, ft);
+    const float bt = s_b[b];
+    const float4 br = make_float4(bt * (s_v[b][4 * cg] - col[4 * cg]), bt * (s_v[b][4 * cg + 1] - col[4 * cg + 1]),
+                                  bt * (s_v[b][4 * cg + 2] - col[4 * cg + 2]), bt * (s_v[b][4 * cg + 3] - col[4 * cg + 3]));
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const float kd = s_k[rg + RG * i];
+      const float kd = s_k[b][rg + RG * i];
       s[i].x = fmaf(kd, br.x, s[i].x); s[i].y = fmaf(kd, br.y, s[i].y);
       s[i].z = fmaf(kd, br.z, s[i].z); s[i].w = fmaf(kd, br.w, s[i].w);
     }
@@ -220,17 +229,20 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
   for (int i = 0; i < RPT; ++i)
     s[i] = p.s0 ? *reinterpret_cast<const float4*>(p.s0 + state_col + static_cast<size_t>(rg + RG * i) * V)
                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  if (len > 0) fetch(0);
+  if (len > 0) {
+    fetch(0);
+    stage(0);
+    if (len > 1) fetch(1);
+  }
+  __syncthreads();
   for (int t = 0; t < len; ++t) {
     if (t % CH == 0) {
 #pragma unroll
       for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(ckpt + static_cast<size_t>(t / CH) * K * VS, i)) = s[i];
     }
-    __syncthreads();  // the previous step's reads of the staged token are done
-    stage();
-    if (t + 1 < len) fetch(t + 1);
-    __syncthreads();
-    forward_step(s);
+    const int b = t & 1;
+    // token t + 1 into the other buffer, token t + 2 fetched
+    forward_step(s, b, t + 1 < len ? (b ^ 1) : -1, t + 2 < len ? t + 2 : -1);
   }
 
   // ---- 2. reverse sweep, one chunk at a time ----
@@ -245,26 +257,33 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
     // recompute the chunk's token states (the state before each token)
 #pragma unroll
     for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float4*>(slot(ckpt + static_cast<size_t>(n) * K * VS, i));
-    if (t0 + 1 < t1) fetch(t0);
+    // (the previous sweep's readers of both buffers are done before anything is staged)
+    __syncthreads();
+    if (t0 + 1 < t1) {
+      fetch(t0);
+      stage(0);
+      if (t0 + 2 < t1) fetch(t0 + 1);
+    }
+    __syncthreads();
     for (int t = t0; t < t1; ++t) {
 #pragma unroll
       for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(slot(toks + static_cast<size_t>(t - t0) * K * VS, i)) = s[i];
       if (t + 1 == t1) break;  // the last token's successor is not needed
-      __syncthreads();
-      stage();
-      if (t + 2 < t1) fetch(t + 1);
-      __syncthreads();
-      forward_step(s);
+      const int b = (t - t0) & 1;
+      forward_step(s, b, t + 2 < t1 ? (b ^ 1) : -1, t + 3 < t1 ? t + 2 : -1);
     }
-    // the token states are read one token ahead too (this thread wrote them above)
+    // reverse: the inputs and the token states are read one token ahead too (this thread
+    // wrote the states above)
+    __syncthreads();
     fetch(t1 - 1);
+    stage(0);
+    if (t1 - 1 > t0) fetch(t1 - 2);
     float4 Pn[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) Pn[i] = *reinterpret_cast<const float4*>(slot(toks + static_cast<size_t>(t1 - 1 - t0) * K * VS, i));
+    __syncthreads();
     for (int t = t1 - 1; t >= t0; --t) {
-      __syncthreads();
-      stage();
-      if (t > t0) fetch(t - 1);
+      const int b = (t1 - 1 - t) & 1;
       float4 P[RPT];
 #pragma unroll
       for (int i = 0; i < RPT; ++i) P[i] = Pn[i];
@@ -272,25 +291,24 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
 #pragma unroll
         for (int i = 0; i < RPT; ++i) Pn[i] = *reinterpret_cast<const float4*>(slot(toks + static_cast<size_t>(t - 1 - t0) * K * VS, i));
       }
-      __syncthreads();
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
-        const float e = s_e[rg + RG * i];
+        const float e = s_e[b][rg + RG * i];
         P[i].x *= e; P[i].y *= e; P[i].z *= e; P[i].w *= e;
       }
-      reduce_k(P);  // col = u
-      const float bt = s_b, sc = p.scale;
-      const float4 r = make_float4(s_v[4 * cg] - col[4 * cg], s_v[4 * cg + 1] - col[4 * cg + 1],
-                                   s_v[4 * cg + 2] - col[4 * cg + 2], s_v[4 * cg + 3] - col[4 * cg + 3]);
-      const float4 dov = *reinterpret_cast<const float4*>(&s_do[4 * cg]);
+      reduce_k(P, b, -1, -1);  // col = u
+      const float bt = s_b[b], sc = p.scale;
+      const float4 r = make_float4(s_v[b][4 * cg] - col[4 * cg], s_v[b][4 * cg + 1] - col[4 * cg + 1],
+                                   s_v[b][4 * cg + 2] - col[4 * cg + 2], s_v[b][4 * cg + 3] - col[4 * cg + 3]);
+      const float4 dov = *reinterpret_cast<const float4*>(&s_do[b][4 * cg]);
       // dq = scale (P + beta k r^T) do, per row; then dS += scale q do^T
       float acc[RPT];
       const float rdo = bt * (r.x * dov.x + r.y * dov.y + r.z * dov.z + r.w * dov.w);
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int d = rg + RG * i;
-        acc[i] = P[i].x * dov.x + P[i].y * dov.y + P[i].z * dov.z + P[i].w * dov.w + s_k[d] * rdo;
-        const float qs = sc * s_q[d];
+        acc[i] = P[i].x * dov.x + P[i].y * dov.y + P[i].z * dov.z + P[i].w * dov.w + s_k[b][d] * rdo;
+        const float qs = sc * s_q[b][d];
         ds[i].x = fmaf(qs, dov.x, ds[i].x); ds[i].y = fmaf(qs, dov.y, ds[i].y);
         ds[i].z = fmaf(qs, dov.z, ds[i].z); ds[i].w = fmaf(qs, dov.w, ds[i].w);
       }
@@ -300,9 +318,10 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
         Halve<RPT, TPR / 2>::run(acc, lane, idx);
         if (writer) atomicAdd(p.dq + (tok * p.H + hk) * K + rg + RG * idx, sc * acc[0]);
       }
-      // kd = dS^T k (all rows) -> col;  dr = beta kd;  dbeta = r . kd
-      __syncthreads();  // col (u) has been read by every thread
-      reduce_k(ds);
+      // kd = dS^T k (all rows) -> col;  dr = beta kd;  dbeta = r . kd.  (Every thread has read
+      // col (u) before it reaches the first barrier inside, after which col is rewritten;
+      // the token before goes into the other buffer between the two.)
+      reduce_k(ds, b, t > t0 ? (b ^ 1) : -1, t - 1 > t0 ? t - 2 : -1);
       const float4 kdv = *reinterpret_cast<const float4*>(&col[4 * cg]);
       const float4 dr = make_float4(bt * kdv.x, bt * kdv.y, bt * kdv.z, bt * kdv.w);
       if (rg == 0) *reinterpret_cast<float4*>(p.dv + (tok * p.HV + hv) * V + v0 + 4 * cg) = dr;
@@ -317,7 +336,7 @@ __global__ void __launch_bounds__(NT) recurrent_bwd_kernel(const Params p) {
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int d = rg + RG * i;
-        const float kd = s_k[d], e = s_e[d];
+        const float kd = s_k[b][d], e = s_e[b][d];
         dkv[i] = bt * (ds[i].x * r.x + ds[i].y * r.y + ds[i].z * r.z + ds[i].w * r.w) -
                  (P[i].x * dr.x + P[i].y * dr.y + P[i].z * dr.z + P[i].w * dr.w);
         float4 dp = make_float4(ds[i].x - kd * dr.x, ds[i].y - kd * dr.y, ds[i].z - kd * dr.z, ds[i].w - kd * dr.w);
