@@ -407,13 +407,17 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void activate(float2 (&g)[16], float& beta, int kind, float lb, float a, float2 dt,
                                          int hq, int pt, int rows) {
   const int nvalid = rows - 16 * hq;
-  if (kind == 1) {  // lb sigmoid(a x) = lb/2 + (lb/2) tanh(a x / 2)
+  if (kind == 1) {  // lb sigmoid(a x) = lb/2 + (lb/2) tanh(a x / 2), a x / 2 = ha g + ha dt
     const float ha = 0.5f * a, hl = 0.5f * lb;
+    const float hdx = ha * dt.x, hdy = ha * dt.y;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float x0 = fmaf(hl, tanh_approx(ha * (g[i].x + dt.x)), hl);
-      const float x1 = fmaf(hl, tanh_approx(ha * (g[i].y + dt.y)), hl);
-      g[i] = i < nvalid ? make_float2(x0, x1) : make_float2(0.f, 0.f);
+    for (int i = 0; i < 16; ++i)
+      g[i] = make_float2(fmaf(hl, tanh_approx(fmaf(ha, g[i].x, hdx)), hl),
+                         fmaf(hl, tanh_approx(fmaf(ha, g[i].y, hdy)), hl));
+    if (nvalid < 16) {  // a sequence's partial last chunk: rows past the end act as g = 0
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i >= nvalid) g[i] = make_float2(0.f, 0.f);
     }
   } else {
     auto softplus = [](float x) {  // log(1 + e^x), with its two asymptotes
