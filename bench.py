@@ -499,7 +499,8 @@ def run_decode(args):
                    "io": "bf16 q/k/v/o, fp32 g/beta/state", "l2": "flushed between timed steps; the state "
                    "(537 MB) is larger than L2 anyway"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": None, "kernel": "decode_kernel",
+                     "frac": achieved / hbm_gbs, "traffic": load_traffic("decode_kernel", "decode_B128_T1_H32_K128"),
+                     "kernel": "decode_kernel",
                      "algorithmic_bytes_per_launch": alg, "peak_source": peak_src},
         "clocks": sampler.summary(), "gpu_launches": args.steps,
     }
@@ -653,7 +654,8 @@ def run_backward(args):
                    "io": "bf16 q/k/v/d_out, fp32 g/beta/d_final_state; fp32 gradients",
                    "l2": "flushed between timed steps"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None, "kernel": "recurrent_bwd_kernel",
+                     "frac": achieved / FP32_PEAK_TFLOPS, "kernel": "recurrent_bwd_kernel",
+                     "traffic": load_traffic("recurrent_bwd_kernel", "backward_bf16_T4096_H32_K128"),
                      "flops_per_launch": flops,
                      "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"},
         "clocks": sampler.summary(), "gpu_launches": args.steps,
