@@ -182,33 +182,46 @@ def unit_tokens(x, units):
     return int(sum(int(cu[s + 1] - cu[s]) for s, _ in units))
 
 
-def cpu_baseline(x, units: int | None = None, gate=None):
+def cpu_baseline(x, units: int | None = None, gate=None, min_cpu_s: float = 0.0):
     """Time the fp64 oracle (chunked form, C = 64) on a bounded sample of the
-    workload: `units` (sequence, value head) units, one thread each (with `gate`, the
-    oracle's pre-stage over the whole input first, then the sample).  Returns
-    (tokens/s scaled so that a token counts all value heads, cores, sample text, s)."""
+    workload: batches of `units` (sequence, value head) units, one thread each, taken in
+    turn over the workload until the batches have used `min_cpu_s` thread-seconds or
+    every unit is done (with `gate`, the oracle's pre-stage over the whole input first).
+    Returns (tokens/s scaled so that a token counts all value heads, cores, sample text,
+    wall s)."""
     import oracle
     cores = os.cpu_count() or 1
     HV = x.v.shape[2]
+    total = x.num_seqs * HV
     if units is None:
-        units = min(cores, x.num_seqs * HV)
+        units = min(cores, total)
     f = lambda t: None if t is None else t.float().numpy()
-    sel = sample_units(x, units)
+    order = sample_units(x, total)
+    if min_cpu_s <= 0.0:
+        order = sample_units(x, units)
+    cu = None if x.cu_seqlens is None else x.cu_seqlens.numpy()
     t0 = time.perf_counter()
     if gate is None:
         q, k, g, beta = f(x.q), f(x.k), f(x.g), f(x.beta)
     else:
         q, k, g, beta = oracle.prestage(f(x.q), f(x.k), f(x.g_raw), f(x.beta_raw), f(x.A_log), f(x.dt_bias),
                                         gate=gate[0], lower_bound=gate[1])
-    oracle.forward_units(q, k, f(x.v), g, beta, x.scale, sel, initial_state=f(x.initial_state),
-                         cu_seqlens=None if x.cu_seqlens is None else x.cu_seqlens.numpy(), form="chunked", chunk=64,
-                         nthreads=units)
+    v, h0 = f(x.v), f(x.initial_state)
+    done = 0
+    while done < len(order):
+        sel = order[done:done + units]
+        oracle.forward_units(q, k, v, g, beta, x.scale, sel, initial_state=h0, cu_seqlens=cu, form="chunked",
+                             chunk=64, nthreads=len(sel))
+        done += len(sel)
+        if (time.perf_counter() - t0) * units >= min_cpu_s:
+            break
     dt = time.perf_counter() - t0
+    sel = order[:done]
     token_heads = unit_tokens(x, sel)
-    sample = (f"{len(sel)} of {x.num_seqs * HV} (sequence, value head) units ({token_heads} token-heads) of "
+    sample = (f"{len(sel)} of {total} (sequence, value head) units ({token_heads} token-heads) of "
               f"{x.meta.get('workload', 'the workload')}, fp64 {'pre-stage + ' if gate else ''}chunked oracle "
-              f"(C=64), {units} threads; "
-              f"{dt:.2f} s wall; tokens/s counts a token as all {HV} value heads")
+              f"(C=64), {units} threads; {dt:.2f} s wall (~{dt * units:.0f} thread-s); tokens/s counts a "
+              f"token as all {HV} value heads")
     return token_heads / HV / dt, units, sample, dt
 
 
@@ -354,7 +367,7 @@ def run_gpu(args):
         "device_status": status, "wall_s_timed_region": t_wall,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, cores, sample, _ = cpu_baseline(host, gate=gate)
+        v, cores, sample, _ = cpu_baseline(host, gate=gate, min_cpu_s=10.0)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
