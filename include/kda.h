@@ -182,23 +182,28 @@ KDA_API kda_status kda_chunk_output(const kda_shape* shape, const void* q, const
 /*
  * Backward: the gradients of the loss sum_t <d_out_t, o_t> + <d_final_state, S_final>
  * with respect to every input of kda_chunk_fwd (same shapes and conventions; the
- * method's recurrence, page "手撕KDA" section "1 Naive"; the pages' own backward,
- * sections 2 and 4 of that page, works on the chunked form).  Reverse mode through
- * the token recurrence on CUDA cores in fp32, one CTA per 32 value columns of a
- * (sequence, value head): a forward sweep keeps the fp32 state entering every 64-token
- * chunk in the workspace, then each chunk's token states are recomputed and swept in
- * reverse.
+ * method's recurrence, page "手撕KDA" section "1 Naive"), in the chunk form of that
+ * page's sections 2 and 4: per 64-token chunk the forward's products are recomputed,
+ * the states entering the chunks and the state gradients leaving them are carried by
+ * two chains (S' = Q S + R forward, dS = Q^T dS' + B backward), and every chunk's
+ * gradients follow in parallel.  Products on the tensor cores in TF32 with each operand
+ * split into high and low parts (fp32 accuracy); five launches.  Blocks of 16 tokens
+ * whose decay passes about -80 (natural log) per key dimension set status bit 4, as
+ * the forward's chunk kernels do.
  *
  *   d_out          [B, T, HV, V]  io_dtype
  *   d_final_state  [NS, HV, K, V] fp32 or NULL (zeros)
  *   dq, dk         [B, T, H, K]   fp32: summed over the value heads sharing a key head
  *   dv             [B, T, HV, V]  fp32;   dg [B, T, HV, K] fp32;   dbeta [B, T, HV] fp32
  *   d_initial_state [NS, HV, K, V] fp32 or NULL (not written)
- *   workspace      at least kda_backward_workspace_size() bytes: the status word and,
- *                  per (sequence, value head), ceil(T / 64) + 64 states of K x V fp32
- *                  (with cu_seqlens, T is the packed total: the bound of any sequence)
+ *   workspace      at least kda_backward_workspace_size() bytes: the status word and a
+ *                  slot of fp32 intermediates per (chunk, value head) (about 457 KB at
+ *                  K = V = 128; with cu_seqlens, ceil(T / 64) + NS chunks are reserved)
  * Any io_dtype and K, V in {64, 128}.  The gradients must not overlap each other or
- * any input.
+ * any input.  With the environment variable KDA_BACKWARD=recurrent (read at each call)
+ * the same gradients come from reverse mode through the token recurrence instead (fp32
+ * on CUDA cores, one CTA per 32 value columns; slower), which the workspace size also
+ * covers.
  */
 KDA_API size_t kda_backward_workspace_size(const kda_shape* shape);
 KDA_API kda_status kda_backward(const kda_shape* shape, const void* q, const void* k, const void* v,

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libkda.so")
-SOURCES = ["kda_abi.cu", "kda_recurrent.cu", "kda_chunk_tc.cu", "kda_decode.cu", "kda_backward.cu"]
+SOURCES = ["kda_abi.cu", "kda_recurrent.cu", "kda_chunk_tc.cu", "kda_decode.cu", "kda_backward.cu", "kda_backward_chunk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

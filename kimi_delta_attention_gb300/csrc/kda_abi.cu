@@ -23,6 +23,13 @@ cudaError_t launch_backward(const void* q, const void* k, const void* v, const f
                             float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* scratch,
                             size_t unit_floats, uint32_t* status, float scale, int T, int H, int HV, int K, int V,
                             int num_seqs, bool bf16, cudaStream_t stream);
+size_t backward_chunk_slots(long T, int num_seqs_or_B, bool varlen, int HV);
+size_t backward_chunk_slot_floats(int K, int V);
+cudaError_t launch_backward_chunk(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  const float* s0, const int32_t* cu, const void* d_out, const float* d_fin, float* dq,
+                                  float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* ws,
+                                  uint32_t* status, float scale, int T, int H, int HV, int K, int V, int num_seqs,
+                                  bool bf16, cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                           float* state, void* out, float scale, int B, int T, int H, int HV, int K, int V,
                           bool bf16, cudaStream_t stream);
@@ -59,6 +66,12 @@ unsigned long long wait_limit_ns() {
     if (end != e && v > 0) return v;
   }
   return 2000000000ull;
+}
+
+// KDA_BACKWARD=recurrent (read at each call) selects the token-recurrence backward.
+bool backward_recurrent() {
+  const char* e = std::getenv("KDA_BACKWARD");
+  return e && std::strcmp(e, "recurrent") == 0;
 }
 
 struct Checked {
@@ -342,7 +355,10 @@ kda_status kda_chunk_output(const kda_shape* shape, const void* q, const void* k
 size_t kda_backward_workspace_size(const kda_shape* s) {
   if (!s || s->B < 0 || s->T < 0 || s->HV < 1 || s->K < 1 || s->V < 1 || s->num_seqs < 0) return 0;
   const size_t ns = s->num_seqs > 0 ? s->num_seqs : s->B;
-  return 256 + ns * s->HV * kda::backward_unit_floats(s->T, s->K, s->V) * sizeof(float);
+  const size_t recurrent = ns * s->HV * kda::backward_unit_floats(s->T, s->K, s->V);
+  const size_t chunk = kda::backward_chunk_slots(s->T, static_cast<int>(ns), s->num_seqs > 0, s->HV) *
+                       kda::backward_chunk_slot_floats(s->K, s->V);
+  return 256 + (recurrent > chunk ? recurrent : chunk) * sizeof(float);
 }
 
 kda_status kda_backward(const kda_shape* s, const void* q, const void* k, const void* v, const float* g,
@@ -389,6 +405,12 @@ kda_status kda_backward(const kda_shape* s, const void* q, const void* k, const 
                      cudaMemsetAsync(dg, 0, n_g, cs) != cudaSuccess || cudaMemsetAsync(dbeta, 0, n_b, cs) != cudaSuccess))
     return KDA_ERR_CUDA;
   float* scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+  if (!backward_recurrent()) {
+    const cudaError_t e = kda::launch_backward_chunk(
+        q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta, d_initial_state,
+        scratch, status, scale, s->T, s->H, s->HV, s->K, s->V, static_cast<int>(ns), s->io_dtype == KDA_BF16, cs);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
   const cudaError_t e = kda::launch_backward(
       q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta, d_initial_state,
       scratch, kda::backward_unit_floats(s->T, s->K, s->V), status, scale, s->T, s->H, s->HV, s->K, s->V,

@@ -1,0 +1,1012 @@
+// kda_backward_chunk.cu -- the backward in chunk form: gradients of
+// sum_t <do_t, o_t> + <dS_final, S_final> with respect to q, k, v, g, beta and the
+// initial state, chunk by chunk (C = 64), with every contraction on the tensor cores
+// (warp-level m16n8k8 TF32 products, each operand split into a TF32 high and low part
+// so that three products give fp32 accuracy).
+//
+// The forward of a chunk (page "手撕KDA", section "1 Naive": the chunked form; gc the
+// cumulative sum of g inside the chunk, gl its last row, S the state entering it):
+//     kd = k e^{gc}, ki = k e^{-gc}, qd = scale q e^{gc}, kr = k e^{gl - gc}
+//     M = strict_tril(Diag(beta) kd ki^T), T = (I + M)^{-1}, A = T Diag(beta)
+//     W = A kd, U = A v, v_new = U - W S, Aqk = tril(qd ki^T)
+//     o = qd S + Aqk v_new,   S' = Diag(e^{gl}) S + kr^T v_new.
+// So S' = Q S + R with Q = Diag(e^{gl}) - kr^T W and R = kr^T U, and going back,
+//     dv_new = Aqk^T do + kr dS',   dS = Q^T dS' + B,   B = qd^T do - W^T Aqk^T do,
+// and the section "2 Backward" chain rule through the chunk's products:
+//     dAqk = tril(do v_new^T), dW = -dv_new S^T, dA = dW kd^T + dv_new v^T,
+//     dv = A^T dv_new, dkd = A^T dW, dbeta_j += sum_i T_ij dA_ij,
+//     dM = -strict_tril(T^T dA A^T), dbeta_i += sum_j dM_ij (kd ki^T)_ij,
+//     dq = scale e^{gc} (do S^T + dAqk ki),  dk = e^{gc} (dkd + dMb ki) + e^{-gc} (dAqk^T qd + dMb^T kd)
+//          + e^{gl - gc} (v_new dS'^T),   dMb = Diag(beta) dM,
+//     dgc = q dq + k (dk_e^{gc} - dk_e^{-gc} - dk_e^{gl-gc}),  dgl += e^{gl} sum_v S dS' + sum_i k dk_e^{gl-gc},
+//     dg = the reverse cumulative sum of dgc (dgl added at the chunk's last row).
+//
+// Range.  The factors e^{gc_i - gc_j} of the products over a chunk's rows are formed
+// block by block (16-row blocks b with reference points s_b, e_b: gc just before and at
+// the end of the block), each factor between 0 and e^{-(decay of one block)}, the
+// limit the forward kernels also have; e^{gc}, e^{gl - gc} never exceed 1.
+//
+// Five launches, each parallel over (chunk, value head) except the chains:
+//   prep_kernel     Q, R, B of every chunk, and W, U, Aqk^T do, T and kd ki^T for the
+//                   gradient kernels (workspace slot per (chunk, value head));
+//   chain_kernel    the states entering each chunk (h_{n+1} = Q_n h_n + R_n) and the
+//                   state gradients leaving it (dS_n = Q_n^T dS_{n+1} + B_n), one CTA per
+//                   32 value columns and direction (the columns are independent);
+//   grad_v_kernel   v_new, dv_new and the products with S and dS' (dv final);
+//   grad_cc_kernel  dA, dM and dbeta (C x C);
+//   grad_k_kernel   dq, dk, dg (per 64 key dims).
+#include "kda_common.cuh"
+#include "sm103.cuh"
+
+namespace kda {
+namespace cbwd {
+
+constexpr int NT = 256, NW = 8, C = 64;  // 16-row blocks inside a chunk
+constexpr int LC = C + 4;  // padded row of a C x C fp32 tile (row stride = 4 mod 32 banks)
+constexpr float kLog2e = 1.4426950408889634f;
+#ifndef KDA_CBWD_SPLIT
+#define KDA_CBWD_SPLIT 1
+#endif
+constexpr bool kSplit = KDA_CBWD_SPLIT != 0;
+// The decay of one 16-row block that the block factors hold (log2 units, as the forward
+// kernels): beyond it a chunk raises the status range bit.
+constexpr float kMinBlockLog2 = -116.f;
+
+struct Params {
+  const void* q;       // [tokens, H, K]  io type
+  const void* k;
+  const void* v;       // [tokens, HV, V]  io type
+  const float* g;      // [tokens, HV, K]
+  const float* beta;   // [tokens, HV]
+  const float* s0;     // [NS, HV, K, V] or null
+  const int32_t* cu;   // [NS + 1] or null
+  const void* d_out;   // [tokens, HV, V]  io type
+  const float* d_fin;  // [NS, HV, K, V] or null
+  float* dq;           // [tokens, H, K]  accumulated (zeroed by the launcher)
+  float* dk;
+  float* dv;           // [tokens, HV, V]
+  float* dg;           // [tokens, HV, K]
+  float* dbeta;        // [tokens, HV]
+  float* ds0;          // [NS, HV, K, V] or null
+  float* ws;           // slots, one per (flat chunk, value head)
+  uint32_t* status;
+  size_t slot_floats;
+  float scale;
+  int T, H, HV, num_seqs;
+  int nc;              // chunks per sequence (fixed length)
+};
+
+// Per-slot layout (floats, dense rows): the chains' operands, then what the gradient
+// kernels hand on.  RH holds R until the forward chain replaces it by the state
+// entering the chunk, BD holds B until the reverse chain replaces it by dS'.
+template <int K, int V>
+struct Slot {
+  static constexpr size_t Q = 0, RH = Q + K * K, BD = RH + K * V, W = BD + K * V, U = W + C * K, E = U + C * V,
+                          T = E + C * V, KK = T + C * C, DH = KK + C * C, DW = DH + C * K, DKR = DW + C * K,
+                          DAQK = DKR + C * K, DAV = DAQK + C * C, DMB = DAV + C * C, DGL = DMB + C * C,
+                          FLOATS = DGL + K;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+}
+
+// Flat chunk f (chunks numbered sequence by sequence) -> its sequence, chunk within the
+// sequence, first token and rows; false past the last chunk or on a bad cu_seqlens.
+__device__ bool find_chunk(const Params& p, int f, int& seq, int& m, long& tok0, int& rows) {
+  if (!p.cu) {
+    seq = f / p.nc;
+    m = f - seq * p.nc;
+    if (seq >= p.num_seqs) return false;
+    tok0 = static_cast<long>(seq) * p.T + static_cast<long>(m) * C;
+    rows = min(C, p.T - m * C);
+    return true;
+  }
+  int f0 = 0;
+  for (int s = 0; s < p.num_seqs; ++s) {
+    const int a = p.cu[s], b = p.cu[s + 1];
+    if (a < 0 || b < a || b > p.T || (s == 0 && a != 0) || (s == p.num_seqs - 1 && b != p.T)) {
+      atomicOr(p.status, kStatusBounds);
+      return false;
+    }
+    const int n = (b - a + C - 1) / C;
+    if (f < f0 + n) {
+      seq = s;
+      m = f - f0;
+      tok0 = a + static_cast<long>(m) * C;
+      rows = min(C, b - a - m * C);
+      return true;
+    }
+    f0 += n;
+  }
+  return false;
+}
+// First flat chunk and chunk count of sequence `seq`.
+__device__ bool seq_chunks(const Params& p, int seq, int& f0, int& nch) {
+  if (!p.cu) {
+    f0 = seq * p.nc;
+    nch = p.nc;
+    return true;
+  }
+  f0 = 0;
+  for (int s = 0; s <= seq; ++s) {
+    const int a = p.cu[s], b = p.cu[s + 1];
+    if (a < 0 || b < a || b > p.T || (s == 0 && a != 0) || (s == p.num_seqs - 1 && b != p.T)) {
+      atomicOr(p.status, kStatusBounds);
+      return false;
+    }
+    nch = (b - a + C - 1) / C;
+    if (s < seq) f0 += nch;
+  }
+  return true;
+}
+
+// C rows of N columns (io type) into fp32 shared memory with row stride N + 4; rows
+// past `rows` are zero.
+template <typename IO, int N>
+__device__ __forceinline__ void load_rows(float* dst, const IO* src, long row0, int rows, size_t row_stride,
+                                          size_t col0) {
+  for (int idx = threadIdx.x; idx < C * (N / 4); idx += NT) {
+    const int r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < rows) x = load4(src + static_cast<size_t>(row0 + r) * row_stride + col0 + c4);
+    *reinterpret_cast<float4*>(dst + r * (N + 4) + c4) = x;
+  }
+}
+// rows x N dense fp32 (global) <-> shared memory with row stride LD
+template <int N, int LD>
+__device__ __forceinline__ void copy_in(float* dst, const float* src, int rows) {
+  for (int idx = threadIdx.x; idx < rows * (N / 4); idx += NT) {
+    const int r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    *reinterpret_cast<float4*>(dst + r * LD + c4) = load4(src + static_cast<size_t>(r) * N + c4);
+  }
+}
+template <int N, int LD>
+__device__ __forceinline__ void copy_out(float* dst, const float* src, int rows) {
+  for (int idx = threadIdx.x; idx < rows * (N / 4); idx += NT) {
+    const int r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * N + c4) = *reinterpret_cast<const float4*>(src + r * LD + c4);
+  }
+}
+
+// In-place cumulative sum down the C rows of columns [0, N) (stride LD), in log2 units.
+template <int N, int LD>
+__device__ __forceinline__ void cumsum_log2(float* x) {
+  for (int d = threadIdx.x; d < N; d += NT) {
+    float s = 0.f;
+#pragma unroll 16
+    for (int i = 0; i < C; ++i) {
+      s = fmaf(x[i * LD + d], kLog2e, s);
+      x[i * LD + d] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------------ warp products --
+// One warp accumulates the 16 x (8 NT8) tile at (m0, n0) of sum_k A(m, k) B(k, n) over
+// k in [kb, ke) (multiples of 8).  fa(m, k, n0) and fb(k, n, m0) return fp32 operands;
+// each is split into TF32 high and low parts and the three products hi*hi, hi*lo,
+// lo*hi accumulate in fp32 (kSplit), else a single TF32 product.
+template <int NT8, class FA, class FB>
+__device__ __forceinline__ void tile_mma(float (&acc)[NT8][4], const FA& fa, const FB& fb, int m0, int n0, int kb,
+                                         int ke) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+  for (int k = kb; k < ke; k += 8) {
+    const float av[4] = {fa(m0 + g, k + t, n0), fa(m0 + g + 8, k + t, n0), fa(m0 + g, k + t + 4, n0),
+                         fa(m0 + g + 8, k + t + 4, n0)};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ah[e] = to_tf32(av[e]);
+      if (kSplit) al[e] = to_tf32(av[e] - __uint_as_float(ah[e]));
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+      const int n = n0 + 8 * nt + g;
+      const float b0 = fb(k + t, n, m0), b1 = fb(k + t + 4, n, m0);
+      const uint32_t bh0 = to_tf32(b0), bh1 = to_tf32(b1);
+      if (kSplit) {
+        mma_tf32_m16n8k8(acc[nt], al, bh0, bh1);
+        mma_tf32_m16n8k8(acc[nt], ah, to_tf32(b0 - __uint_as_float(bh0)), to_tf32(b1 - __uint_as_float(bh1)));
+      }
+      mma_tf32_m16n8k8(acc[nt], ah, bh0, bh1);
+    }
+  }
+}
+// accumulator element e of n-tile nt: row m0 + g + 8 (e >> 1), column n0 + 8 nt + 2 t + (e & 1)
+template <int NT8, class FI>
+__device__ __forceinline__ void tile_init(float (&acc)[NT8][4], const FI& init, int m0, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = init(m0 + g + 8 * (e >> 1), n0 + 8 * nt + 2 * t + (e & 1));
+}
+template <int NT8, class FE>
+__device__ __forceinline__ void tile_epi(const float (&acc)[NT8][4], const FE& epi, int m0, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT8; ++nt) {
+    epi(m0 + g, n0 + 8 * nt + 2 * t, acc[nt][0], acc[nt][1]);
+    epi(m0 + g + 8, n0 + 8 * nt + 2 * t, acc[nt][2], acc[nt][3]);
+  }
+}
+// The whole M x N product over the CTA's warps, tile by tile: init, the k range
+// krange(m0, n0) (int2), epilogue on column pairs.  Tiles for which live(m0, n0) is
+// false keep their init values.
+template <int M, int N, int NT8, class FA, class FB, class FL, class FR, class FI, class FE>
+__device__ __forceinline__ void cta_gemm(const FA& fa, const FB& fb, const FL& live, const FR& krange, const FI& init,
+                                         const FE& epi) {
+  constexpr int TN = N / (8 * NT8), TILES = (M / 16) * TN;
+  const int warp = threadIdx.x >> 5;
+  for (int tile = warp; tile < TILES; tile += NW) {
+    const int m0 = (tile / TN) * 16, n0 = (tile % TN) * (8 * NT8);
+    float acc[NT8][4];
+    tile_init<NT8>(acc, init, m0, n0);
+    if (live(m0, n0)) {
+      const int2 kr = krange(m0, n0);
+      tile_mma<NT8>(acc, fa, fb, m0, n0, kr.x, kr.y);
+    }
+    tile_epi<NT8>(acc, epi, m0, n0);
+  }
+}
+
+// ---------------------------------------------------------------- prep ----
+template <int K, int V>
+struct PrepSmem {
+  static constexpr int LK = K + 4, LV = V + 4, LX = (K > V ? K : V) + 4;
+  static constexpr int B0 = 0, B1 = B0 + C * LX, B2 = B1 + C * LX, B3 = B2 + C * LX, B4 = B3 + C * LX,
+                       X1 = B4 + C * LX, X2 = X1 + C * LC, X3 = X2 + C * LC, F = X3 + C * LC, G = F + 4 * K,
+                       D = G + 4 * K, EG = D + 10 * K, BS = EG + K, FLOATS = BS + C;
+  static_assert(8 * K <= C * LC, "block references fit in the T tile");
+};
+__device__ __forceinline__ int pair_index(int bi, int bj) { return bi * (bi + 1) / 2 + bj; }
+
+// q, k, g rows of a chunk -> gc (log2 units, in place of g), the block references
+// (refs: s_b [4][N], e_b [4][N]) and the tables Lk = k e^{gc - s_b}, Lq = scale q e^{gc - s_b}
+// (in place of k and q) and R = k e^{e_b - gc}.  Columns [0, N) of stride LD.
+template <int N, int LD>
+__device__ __forceinline__ void make_tables(float* kL, float* qL, float* gc, float* R, float* refs, float scale) {
+  cumsum_log2<N, LD>(gc);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 4 * N; idx += NT) {
+    const int b = idx / N, d = idx - b * N;
+    refs[4 * N + idx] = gc[(16 * b + 15) * LD + d];
+    refs[idx] = b == 0 ? 0.f : gc[(16 * b - 1) * LD + d];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < C * N; idx += NT) {
+    const int i = idx / N, d = idx - i * N, b = i >> 4;
+    const float x = gc[i * LD + d], s = refs[b * N + d], e = refs[(4 + b) * N + d];
+    const float kk = kL[i * LD + d];
+    const float f = ex2(x - s);
+    kL[i * LD + d] = kk * f;
+    if (qL) qL[i * LD + d] = scale * qL[i * LD + d] * f;
+    R[i * LD + d] = kk * ex2(e - x);
+  }
+}
+
+// T = (I + M)^{-1}, M = strict_tril(Diag(beta) KKd), into Tm (C x C, stride LC): the
+// 16 x 16 diagonal blocks by forward substitution, then block rows a > b level by level:
+// T_ab = -T_aa sum_{c=b}^{a-1} M_ac T_cb.  tmp: 3 x 256 floats.
+__device__ __forceinline__ void tri_inverse(const float* KKd, const float* bs, float* Tm, float* tmp) {
+  const int tid = threadIdx.x;
+  if (tid < 64) {
+    const int bb = tid >> 4, jc = tid & 15, o = 16 * bb;
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float s = (i == jc) ? 1.f : 0.f;
+      const float bi = bs[o + i];
+#pragma unroll
+      for (int mm = 0; mm < i; ++mm) s = fmaf(-bi * KKd[(o + i) * LC + o + mm], acc[mm], s);
+      acc[i] = s;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Tm[(o + i) * LC + o + jc] = acc[i];
+  }
+  for (int idx = tid; idx < C * C; idx += NT) {
+    const int r = idx >> 6, c = idx & 63;
+    if ((c >> 4) > (r >> 4)) Tm[r * LC + c] = 0.f;
+  }
+  __syncthreads();
+  for (int L = 1; L < 4; ++L) {
+    const int nb = 4 - L;
+    for (int idx = tid; idx < nb * 256; idx += NT) {
+      const int b = idx >> 8, r = (idx >> 4) & 15, c = idx & 15, a = b + L;
+      const float ba = bs[16 * a + r];
+      float s = 0.f;
+      for (int mm = 16 * b; mm < 16 * a; ++mm) s = fmaf(ba * KKd[(16 * a + r) * LC + mm], Tm[mm * LC + 16 * b + c], s);
+      tmp[idx] = s;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nb * 256; idx += NT) {
+      const int b = idx >> 8, r = (idx >> 4) & 15, c = idx & 15, a = b + L;
+      float s = 0.f;
+      for (int mm = 0; mm <= r; ++mm) s = fmaf(Tm[(16 * a + r) * LC + 16 * a + mm], tmp[(b << 8) + (mm << 4) + c], s);
+      Tm[(16 * a + r) * LC + 16 * b + c] = -s;
+    }
+    __syncthreads();
+  }
+}
+
+template <typename IO, int K, int V>
+__global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
+  using S = Slot<K, V>;
+  using L = PrepSmem<K, V>;
+  constexpr int LK = L::LK, LV = L::LV;
+  extern __shared__ __align__(16) float sm[];
+  float *B0 = sm + L::B0, *B1 = sm + L::B1, *B2 = sm + L::B2, *B3 = sm + L::B3, *B4 = sm + L::B4;
+  float *X1 = sm + L::X1, *X2 = sm + L::X2, *X3 = sm + L::X3;
+  float *F = sm + L::F, *G = sm + L::G, *D = sm + L::D, *EG = sm + L::EG, *bs = sm + L::BS;
+  int seq, m, rows;
+  long tok0;
+  const int f = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
+  if (!find_chunk(p, f, seq, m, tok0, rows)) return;
+  const int hk = hv / (p.HV / p.H);
+  float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
+  const auto zero = [](int, int) { return 0.f; };
+  const auto all = [](int, int) { return true; };
+
+  // 1. rows of k, q, g; the tables (Lk in B0, Lq in B1, R in B3; gc in B2)
+  load_rows<IO, K>(B0, static_cast<const IO*>(p.k), tok0, rows, static_cast<size_t>(p.H) * K, static_cast<size_t>(hk) * K);
+  load_rows<IO, K>(B1, static_cast<const IO*>(p.q), tok0, rows, static_cast<size_t>(p.H) * K, static_cast<size_t>(hk) * K);
+  load_rows<float, K>(B2, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K);
+  if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
+  __syncthreads();
+  float* refs = X3;  // s_b, e_b until T is formed
+  make_tables<K, LK>(B0, B1, B2, B3, refs, p.scale);
+  for (int idx = tid; idx < 4 * K; idx += NT) {
+    const int b = idx / K, d = idx - b * K;
+    F[idx] = ex2(refs[idx]);                               // e^{s_b}
+    G[idx] = ex2(refs[7 * K + d] - refs[(4 + b) * K + d]);  // e^{gl - e_b}
+    if (b == 0) EG[d] = ex2(refs[7 * K + d]);               // e^{gl}
+  }
+  for (int idx = tid; idx < 4 * K; idx += NT)
+    if (!(refs[4 * K + idx] - refs[idx] >= kMinBlockLog2)) atomicOr(p.status, kStatusRange);
+  for (int idx = tid; idx < 10 * K; idx += NT) {
+    const int pr = idx / K, d = idx - pr * K;
+    const int bi = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0, bj = pr - bi * (bi + 1) / 2;
+    D[idx] = ex2(refs[bi * K + d] - refs[(4 + bj) * K + d]);  // e^{s_bi - e_bj}, bj <= bi
+  }
+  __syncthreads();
+
+  // 2. KKd = strict_tril(kd ki^T) (X1) and Aqk = tril(qd ki^T) (X2), block by block:
+  //    (i, j) in blocks (bi, bj): sum_d Lk_i e^{s_bi - e_bj} R_j
+  {
+    const auto rb = [&](int kk, int nn, int) { return B3[nn * LK + kk]; };
+    const auto lower = [](int m0, int n0) { return n0 <= m0; };
+    const auto kr = [](int, int) { return make_int2(0, K); };
+    cta_gemm<C, C, 2>([&](int mm, int kk, int n0) { return B0[mm * LK + kk] * D[pair_index(mm >> 4, n0 >> 4) * K + kk]; },
+                      rb, lower, kr, zero, [&](int r, int c, float x0, float x1) {
+                        X1[r * LC + c] = c < r ? x0 : 0.f;
+                        X1[r * LC + c + 1] = c + 1 < r ? x1 : 0.f;
+                      });
+    cta_gemm<C, C, 2>([&](int mm, int kk, int n0) { return B1[mm * LK + kk] * D[pair_index(mm >> 4, n0 >> 4) * K + kk]; },
+                      rb, lower, kr, zero, [&](int r, int c, float x0, float x1) {
+                        X2[r * LC + c] = c <= r ? x0 : 0.f;
+                        X2[r * LC + c + 1] = c + 1 <= r ? x1 : 0.f;
+                      });
+  }
+  __syncthreads();
+  // 3. T (X3), with B2's first 768 floats as scratch (gc is no longer needed)
+  tri_inverse(X1, bs, X3, B2);
+  // 4. W = A kd (B2): A = T Diag(beta), kd = Lk e^{s_b}
+  const auto fa_A = [&](int i, int j, int) { return X3[i * LC + j] * bs[j]; };
+  const auto kr_tril = [](int m0, int) { return make_int2(0, m0 + 16); };
+  cta_gemm<C, K, 4>(fa_A, [&](int j, int d, int) { return B0[j * LK + d] * F[(j >> 4) * K + d]; }, all, kr_tril, zero,
+                    [&](int r, int c, float x0, float x1) {
+                      B2[r * LK + c] = x0;
+                      B2[r * LK + c + 1] = x1;
+                    });
+  __syncthreads();
+  // 5. Q = Diag(e^{gl}) - kr^T W (kr = R e^{gl - e_b}); W to the slot
+  const auto fa_krT = [&](int d, int i, int) { return B3[i * LK + d] * G[(i >> 4) * K + d]; };
+  const auto kr_all = [](int, int) { return make_int2(0, C); };
+  cta_gemm<K, K, 4>(fa_krT, [&](int i, int e, int) { return B2[i * LK + e]; }, all, kr_all, zero,
+                    [&](int r, int c, float x0, float x1) {
+                      *reinterpret_cast<float2*>(slot + S::Q + static_cast<size_t>(r) * K + c) =
+                          make_float2((r == c ? EG[r] : 0.f) - x0, (r == c + 1 ? EG[r] : 0.f) - x1);
+                    });
+  copy_out<K, LK>(slot + S::W, B2, C);
+  __syncthreads();
+  // 6. U = A v (B4), R = kr^T U to the slot
+  load_rows<IO, V>(B0, static_cast<const IO*>(p.v), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
+  __syncthreads();
+  cta_gemm<C, V, 4>(fa_A, [&](int j, int vv, int) { return B0[j * LV + vv]; }, all, kr_tril, zero,
+                    [&](int r, int c, float x0, float x1) {
+                      B4[r * LV + c] = x0;
+                      B4[r * LV + c + 1] = x1;
+                    });
+  __syncthreads();
+  cta_gemm<K, V, 4>(fa_krT, [&](int i, int vv, int) { return B4[i * LV + vv]; }, all, kr_all, zero,
+                    [&](int r, int c, float x0, float x1) {
+                      *reinterpret_cast<float2*>(slot + S::RH + static_cast<size_t>(r) * V + c) = make_float2(x0, x1);
+                    });
+  copy_out<V, LV>(slot + S::U, B4, C);
+  __syncthreads();
+  // 7. E = Aqk^T do (B4), B = qd^T do - W^T E to the slot
+  load_rows<IO, V>(B0, static_cast<const IO*>(p.d_out), tok0, rows, static_cast<size_t>(p.HV) * V,
+                   static_cast<size_t>(hv) * V);
+  __syncthreads();
+  cta_gemm<C, V, 4>([&](int j, int i, int) { return X2[i * LC + j]; }, [&](int i, int vv, int) { return B0[i * LV + vv]; },
+                    all, [](int m0, int) { return make_int2(m0, C); }, zero, [&](int r, int c, float x0, float x1) {
+                      B4[r * LV + c] = x0;
+                      B4[r * LV + c + 1] = x1;
+                    });
+  __syncthreads();
+  cta_gemm<K, V, 4>(
+      [&](int d, int kk, int) { return kk < C ? B1[kk * LK + d] * F[(kk >> 4) * K + d] : -B2[(kk - C) * LK + d]; },
+      [&](int kk, int vv, int) { return kk < C ? B0[kk * LV + vv] : B4[(kk - C) * LV + vv]; }, all,
+      [](int, int) { return make_int2(0, 2 * C); }, zero, [&](int r, int c, float x0, float x1) {
+        *reinterpret_cast<float2*>(slot + S::BD + static_cast<size_t>(r) * V + c) = make_float2(x0, x1);
+      });
+  copy_out<V, LV>(slot + S::E, B4, C);
+  copy_out<C, LC>(slot + S::T, X3, C);
+  copy_out<C, LC>(slot + S::KK, X1, C);
+}
+
+// --------------------------------------------------------------- chains ----
+constexpr int VS = 32;  // value columns per chain CTA
+template <int K>
+struct ChainSmem {
+  static constexpr int LK = K + 4, LS = VS + 4;
+  static constexpr int Q0 = 0, Q1 = K * LK, A0 = 2 * K * LK, A1 = A0 + K * LS, X = A1 + K * LS, FLOATS = X + K * LS;
+};
+template <int K, int V>
+__global__ void __launch_bounds__(NT, 1) chain_kernel(Params p) {
+  using S = Slot<K, V>;
+  using L = ChainSmem<K>;
+  constexpr int LK = L::LK, LS = L::LS;
+  constexpr int NT8 = K == 128 ? 4 : 2;  // one 16 x (8 NT8) tile of the K x 32 product per warp
+  extern __shared__ __align__(16) float sm[];
+  auto Qb = [&](int b) { return sm + (b ? L::Q1 : L::Q0); };
+  auto Ab = [&](int b) { return sm + (b ? L::A1 : L::A0); };
+  float* X = sm + L::X;
+  const int v0 = blockIdx.x * VS, hv = blockIdx.y, seq = blockIdx.z >> 1, dir = blockIdx.z & 1, tid = threadIdx.x;
+  int f0, nch;
+  if (!seq_chunks(p, seq, f0, nch)) return;
+  const float* x0 = dir == 0 ? p.s0 : p.d_fin;
+  const size_t state0 = (static_cast<size_t>(seq) * p.HV + hv) * K * V + v0;
+  for (int idx = tid; idx < K * VS; idx += NT) {
+    const int r = idx / VS, c = idx - r * VS;
+    X[r * LS + c] = x0 ? x0[state0 + static_cast<size_t>(r) * V + c] : 0.f;
+  }
+  const size_t add = dir == 0 ? S::RH : S::BD;
+  auto slot = [&](int mm) { return p.ws + (static_cast<size_t>(f0 + mm) * p.HV + hv) * p.slot_floats; };
+  auto issue = [&](int step, int buf) {
+    const float* s = slot(dir == 0 ? step : nch - 1 - step);
+    for (int idx = tid; idx < K * (K / 4); idx += NT) {
+      const int r = idx / (K / 4), c4 = (idx - r * (K / 4)) * 4;
+      cp_async16(Qb(buf) + r * LK + c4, s + S::Q + static_cast<size_t>(r) * K + c4);
+    }
+    for (int idx = tid; idx < K * (VS / 4); idx += NT) {
+      const int r = idx / (VS / 4), c4 = (idx - r * (VS / 4)) * 4;
+      cp_async16(Ab(buf) + r * LS + c4, s + add + static_cast<size_t>(r) * V + v0 + c4);
+    }
+    cp_async_commit();
+  };
+  if (nch > 0) issue(0, 0);
+  const int warp = tid >> 5;
+  const int m0 = K == 128 ? 16 * warp : 16 * (warp >> 1), n0 = K == 128 ? 0 : 16 * (warp & 1);
+  for (int step = 0; step < nch; ++step) {
+    const int buf = step & 1;
+    float* s = slot(dir == 0 ? step : nch - 1 - step);
+    if (step + 1 < nch) {
+      issue(step + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // this chunk's Q and addend (and X) visible to every thread
+    // the state entering the chunk (forward) / the gradient leaving it (reverse) takes
+    // the addend's place in the slot
+    for (int idx = tid; idx < K * (VS / 4); idx += NT) {
+      const int r = idx / (VS / 4), c4 = (idx - r * (VS / 4)) * 4;
+      *reinterpret_cast<float4*>(s + add + static_cast<size_t>(r) * V + v0 + c4) =
+          *reinterpret_cast<const float4*>(X + r * LS + c4);
+    }
+    const float* Q = Qb(buf);
+    const float* Ad = Ab(buf);
+    float acc[NT8][4];
+    tile_init<NT8>(acc, [&](int r, int c) { return Ad[r * LS + c]; }, m0, n0);
+    if (dir == 0)
+      tile_mma<NT8>(acc, [&](int d, int e, int) { return Q[d * LK + e]; }, [&](int e, int c, int) { return X[e * LS + c]; },
+                    m0, n0, 0, K);
+    else
+      tile_mma<NT8>(acc, [&](int d, int e, int) { return Q[e * LK + d]; }, [&](int e, int c, int) { return X[e * LS + c]; },
+                    m0, n0, 0, K);
+    __syncthreads();  // every warp has read X (and stored it)
+    tile_epi<NT8>(acc, [&](int r, int c, float a, float b) { *reinterpret_cast<float2*>(X + r * LS + c) = make_float2(a, b); },
+                  m0, n0);
+  }
+  if (dir == 1 && p.ds0) {
+    __syncthreads();
+    for (int idx = tid; idx < K * VS; idx += NT) {
+      const int r = idx / VS, c = idx - r * VS;
+      p.ds0[state0 + static_cast<size_t>(r) * V + c] = X[r * LS + c];
+    }
+  }
+}
+
+// -------------------------------------------------------- value gradients --
+constexpr int SR = 16;  // rows of S and dS' per streamed slice
+template <int K, int V>
+struct GvSmem {
+  static constexpr int LK = K + 4, LV = V + 4, LX = (K > V ? K : V) + 4;
+  static constexpr int B0 = 0, B1 = B0 + C * LX, B2 = B1 + C * LX, B3 = B2 + C * LX, B4 = B3 + C * LX,
+                       H0 = B4 + C * LX, H1 = H0 + SR * LV, D0 = H1 + SR * LV, D1 = D0 + SR * LV, GL = D1 + SR * LV,
+                       BS = GL + K, FLOATS = BS + C;
+};
+template <typename IO, int K, int V>
+__global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
+  using S = Slot<K, V>;
+  using L = GvSmem<K, V>;
+  constexpr int LK = L::LK, LV = L::LV;
+  constexpr int NT8 = V == 128 ? 8 : 4;  // v_new / dv_new: one 16 x (V / 2) tile per warp
+  extern __shared__ __align__(16) float sm[];
+  float *B0 = sm + L::B0, *B1 = sm + L::B1, *B2 = sm + L::B2, *B3 = sm + L::B3, *B4 = sm + L::B4;
+  auto Hs = [&](int b) { return sm + (b ? L::H1 : L::H0); };
+  auto Ds = [&](int b) { return sm + (b ? L::D1 : L::D0); };
+  float *gl2 = sm + L::GL, *bs = sm + L::BS;
+  int seq, m, rows;
+  long tok0;
+  const int f = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (!find_chunk(p, f, seq, m, tok0, rows)) return;
+  const int hk = hv / (p.HV / p.H);
+  float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
+  const auto zero = [](int, int) { return 0.f; };
+  const auto all = [](int, int) { return true; };
+
+  // 1. W (B0), U (B2), E (B3) from the slot, do (B4); kr = k e^{gl - gc} (B1)
+  copy_in<K, LK>(B0, slot + S::W, C);
+  copy_in<V, LV>(B2, slot + S::U, C);
+  copy_in<V, LV>(B3, slot + S::E, C);
+  load_rows<IO, V>(B4, static_cast<const IO*>(p.d_out), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
+  load_rows<float, K>(B1, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K);
+  __syncthreads();
+  cumsum_log2<K, LK>(B1);
+  __syncthreads();
+  if (tid < K) gl2[tid] = B1[(C - 1) * LK + tid];
+  __syncthreads();
+  const IO* kp = static_cast<const IO*>(p.k);
+  for (int idx = tid; idx < C * K; idx += NT) {
+    const int i = idx / K, d = idx - i * K;
+    const float kk = i < rows ? load1(kp + static_cast<size_t>(tok0 + i) * p.H * K + static_cast<size_t>(hk) * K + d) : 0.f;
+    B1[i * LK + d] = kk * ex2(gl2[d] - B1[i * LK + d]);
+  }
+  // slices of S (entering) and dS' (leaving) in SR-row pieces
+  const float* hsrc = slot + S::RH;
+  const float* dsrc = slot + S::BD;
+  auto issue = [&](int sl, int buf) {
+    for (int idx = tid; idx < SR * (V / 4); idx += NT) {
+      const int r = idx / (V / 4), c4 = (idx - r * (V / 4)) * 4;
+      const size_t o = static_cast<size_t>(sl * SR + r) * V + c4;
+      cp_async16(Hs(buf) + r * LV + c4, hsrc + o);
+      cp_async16(Ds(buf) + r * LV + c4, dsrc + o);
+    }
+    cp_async_commit();
+  };
+  constexpr int NSL = K / SR;
+  const int vm0 = 16 * (warp >> 1), vn0 = (V / 2) * (warp & 1);
+  float avn[NT8][4], adv[NT8][4];
+  // 2. pass 1: v_new = U - W S, dv_new = E + kr dS', DH = do S^T, dgl = e^{gl} sum_v S dS'
+  __syncthreads();
+  tile_init<NT8>(avn, [&](int r, int c) { return B2[r * LV + c]; }, vm0, vn0);
+  tile_init<NT8>(adv, [&](int r, int c) { return B3[r * LV + c]; }, vm0, vn0);
+  issue(0, 0);
+  for (int sl = 0; sl < NSL; ++sl) {
+    const int buf = sl & 1;
+    if (sl + 1 < NSL) {
+      issue(sl + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const float* h = Hs(buf);
+    const float* ds = Ds(buf);
+    const int d0 = sl * SR;
+    tile_mma<NT8>(avn, [&](int i, int kk, int) { return -B0[i * LK + d0 + kk]; },
+                  [&](int kk, int vv, int) { return h[kk * LV + vv]; }, vm0, vn0, 0, SR);
+    tile_mma<NT8>(adv, [&](int i, int kk, int) { return B1[i * LK + d0 + kk]; },
+                  [&](int kk, int vv, int) { return ds[kk * LV + vv]; }, vm0, vn0, 0, SR);
+    {  // DH[:, slice]: 8 tiles of 16 x 8
+      float a1[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      const int m0 = 16 * (warp >> 1), n0 = 8 * (warp & 1);
+      tile_mma<1>(a1, [&](int i, int vv, int) { return B4[i * LV + vv]; }, [&](int vv, int dd, int) { return h[dd * LV + vv]; },
+                  m0, n0, 0, V);
+      tile_epi<1>(a1, [&](int r, int c, float x0, float x1) {
+        *reinterpret_cast<float2*>(slot + S::DH + static_cast<size_t>(r) * K + d0 + c) = make_float2(x0, x1);
+      }, m0, n0);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {  // dgl for rows 2 warp, 2 warp + 1 of the slice
+      const int r = 2 * warp + rr;
+      float s = 0.f;
+      for (int vv = lane; vv < V; vv += 32) s = fmaf(h[r * LV + vv], ds[r * LV + vv], s);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+      if (lane == 0) slot[S::DGL + d0 + r] = ex2(gl2[d0 + r]) * s;
+    }
+    __syncthreads();  // the slice buffers may be refilled
+  }
+  tile_epi<NT8>(avn, [&](int r, int c, float x0, float x1) { *reinterpret_cast<float2*>(B2 + r * LV + c) = make_float2(x0, x1); },
+                vm0, vn0);
+  tile_epi<NT8>(adv, [&](int r, int c, float x0, float x1) { *reinterpret_cast<float2*>(B3 + r * LV + c) = make_float2(x0, x1); },
+                vm0, vn0);
+  // 3. pass 2: dW = -dv_new S^T, dkr = v_new dS'^T
+  issue(0, 0);
+  for (int sl = 0; sl < NSL; ++sl) {
+    const int buf = sl & 1;
+    if (sl + 1 < NSL) {
+      issue(sl + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // (first slice: v_new and dv_new written too)
+    const float* h = Hs(buf);
+    const float* ds = Ds(buf);
+    const int d0 = sl * SR;
+    const int m0 = 16 * (warp >> 1), n0 = 8 * (warp & 1);
+    float a1[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    tile_mma<1>(a1, [&](int i, int vv, int) { return -B3[i * LV + vv]; }, [&](int vv, int dd, int) { return h[dd * LV + vv]; },
+                m0, n0, 0, V);
+    tile_epi<1>(a1, [&](int r, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(slot + S::DW + static_cast<size_t>(r) * K + d0 + c) = make_float2(x0, x1);
+    }, m0, n0);
+    float a2[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    tile_mma<1>(a2, [&](int i, int vv, int) { return B2[i * LV + vv]; }, [&](int vv, int dd, int) { return ds[dd * LV + vv]; },
+                m0, n0, 0, V);
+    tile_epi<1>(a2, [&](int r, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(slot + S::DKR + static_cast<size_t>(r) * K + d0 + c) = make_float2(x0, x1);
+    }, m0, n0);
+    __syncthreads();
+  }
+  // 4. v (B0), T (B1); dAqk = tril(do v_new^T), dAv = tril(dv_new v^T), dv = A^T dv_new
+  load_rows<IO, V>(B0, static_cast<const IO*>(p.v), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
+  copy_in<C, LC>(B1, slot + S::T, C);
+  if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
+  __syncthreads();
+  const auto lower = [](int m0, int n0) { return n0 <= m0; };
+  const auto kv = [](int, int) { return make_int2(0, V); };
+  cta_gemm<C, C, 2>([&](int i, int vv, int) { return B4[i * LV + vv]; }, [&](int vv, int j, int) { return B2[j * LV + vv]; },
+                    lower, kv, zero, [&](int r, int c, float x0, float x1) {
+                      *reinterpret_cast<float2*>(slot + S::DAQK + r * C + c) =
+                          make_float2(c <= r ? x0 : 0.f, c + 1 <= r ? x1 : 0.f);
+                    });
+  cta_gemm<C, C, 2>([&](int i, int vv, int) { return B3[i * LV + vv]; }, [&](int vv, int j, int) { return B0[j * LV + vv]; },
+                    lower, kv, zero, [&](int r, int c, float x0, float x1) {
+                      *reinterpret_cast<float2*>(slot + S::DAV + r * C + c) =
+                          make_float2(c <= r ? x0 : 0.f, c + 1 <= r ? x1 : 0.f);
+                    });
+  cta_gemm<C, V, 4>([&](int j, int i, int) { return B1[i * LC + j] * bs[j]; }, [&](int i, int vv, int) { return B3[i * LV + vv]; },
+                    all, [](int m0, int) { return make_int2(m0, C); }, zero, [&](int r, int c, float x0, float x1) {
+                      if (r < rows)
+                        *reinterpret_cast<float2*>(p.dv + (static_cast<size_t>(tok0 + r) * p.HV + hv) * V + c) =
+                            make_float2(x0, x1);
+                    });
+}
+
+// ------------------------------------------------------------- C x C stage --
+template <int K>
+struct GcSmem {
+  static constexpr int LK = K + 4;
+  static constexpr int B0 = 0, B1 = C * LK, XT = 2 * C * LK, XA = XT + C * LC, XY = XA + C * LC, XM = XY + C * LC,
+                       XK = XM + C * LC, BS = XK + C * LC, DBC = BS + C, FLOATS = DBC + C;
+};
+template <typename IO, int K, int V>
+__global__ void __launch_bounds__(NT, 1) grad_cc_kernel(Params p) {
+  using S = Slot<K, V>;
+  using L = GcSmem<K>;
+  constexpr int LK = L::LK;
+  extern __shared__ __align__(16) float sm[];
+  float *B0 = sm + L::B0, *B1 = sm + L::B1, *XT = sm + L::XT, *XA = sm + L::XA, *XY = sm + L::XY, *XM = sm + L::XM,
+        *XK = sm + L::XK, *bs = sm + L::BS, *dbc = sm + L::DBC;
+  int seq, m, rows;
+  long tok0;
+  const int f = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
+  if (!find_chunk(p, f, seq, m, tok0, rows)) return;
+  const int hk = hv / (p.HV / p.H);
+  float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
+  const auto lower = [](int m0, int n0) { return n0 <= m0; };
+
+  load_rows<float, K>(B0, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K);
+  copy_in<K, LK>(B1, slot + S::DW, C);
+  copy_in<C, LC>(XT, slot + S::T, C);
+  copy_in<C, LC>(XA, slot + S::DAV, C);
+  copy_in<C, LC>(XK, slot + S::KK, C);
+  if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
+  __syncthreads();
+  cumsum_log2<K, LK>(B0);
+  __syncthreads();
+  const IO* kp = static_cast<const IO*>(p.k);
+  for (int idx = tid; idx < C * K; idx += NT) {  // kd = k e^{gc}
+    const int i = idx / K, d = idx - i * K;
+    const float kk = i < rows ? load1(kp + static_cast<size_t>(tok0 + i) * p.H * K + static_cast<size_t>(hk) * K + d) : 0.f;
+    B0[i * LK + d] = kk * ex2(B0[i * LK + d]);
+  }
+  __syncthreads();
+  // dA = dW kd^T + dAv (lower, diagonal included), in place of dAv
+  cta_gemm<C, C, 2>([&](int i, int d, int) { return B1[i * LK + d]; }, [&](int d, int j, int) { return B0[j * LK + d]; }, lower,
+                    [](int, int) { return make_int2(0, K); }, [&](int r, int c) { return XA[r * LC + c]; },
+                    [&](int r, int c, float x0, float x1) {
+                      XA[r * LC + c] = c <= r ? x0 : 0.f;
+                      XA[r * LC + c + 1] = c + 1 <= r ? x1 : 0.f;
+                    });
+  __syncthreads();
+  if (tid < C) {  // dbeta_j from A = T Diag(beta): sum_i T_ij dA_ij
+    float s = 0.f;
+    for (int i = tid; i < C; ++i) s = fmaf(XT[i * LC + tid], XA[i * LC + tid], s);
+    dbc[tid] = s;
+  }
+  // Y = dA A^T (lower tiles): Y_aj = sum_{b <= j} dA_ab T_jb beta_b
+  cta_gemm<C, C, 2>([&](int a, int b, int) { return XA[a * LC + b]; }, [&](int b, int j, int) { return XT[j * LC + b] * bs[b]; },
+                    lower, [](int, int n0) { return make_int2(0, n0 + 16); }, [](int, int) { return 0.f; },
+                    [&](int r, int c, float x0, float x1) {
+                      XY[r * LC + c] = x0;
+                      XY[r * LC + c + 1] = x1;
+                    });
+  __syncthreads();
+  // dM = -strict_tril(T^T Y): dM_ij = -sum_{a >= i} T_ai Y_aj
+  cta_gemm<C, C, 2>([&](int i, int a, int) { return XT[a * LC + i]; }, [&](int a, int j, int) { return XY[a * LC + j]; }, lower,
+                    [](int m0, int) { return make_int2(m0, C); }, [](int, int) { return 0.f; },
+                    [&](int r, int c, float x0, float x1) {
+                      XM[r * LC + c] = c < r ? -x0 : 0.f;
+                      XM[r * LC + c + 1] = c + 1 < r ? -x1 : 0.f;
+                    });
+  __syncthreads();
+  if (tid < C) {  // dbeta_i from M = Diag(beta) KKd: sum_j dM_ij KKd_ij
+    float s = dbc[tid];
+    for (int j = 0; j < tid; ++j) s = fmaf(XM[tid * LC + j], XK[tid * LC + j], s);
+    if (tid < rows) p.dbeta[(tok0 + tid) * p.HV + hv] = s;
+  }
+  for (int idx = tid; idx < C * C; idx += NT) {
+    const int r = idx >> 6, c = idx & 63;
+    slot[S::DMB + idx] = bs[r] * XM[r * LC + c];
+  }
+}
+
+// ------------------------------------------------------------ key gradients --
+constexpr int DK = 64;  // key dims per grad_k CTA
+constexpr int LD = DK + 4;
+struct GkSmem {
+  static constexpr int GC = 0, LKT = GC + C * LD, LQT = LKT + C * LD, RT = LQT + C * LD, KR = RT + C * LD,
+                       QR = KR + C * LD, DW = QR + C * LD, DKA = DW + C * LD, DGA = DKA + C * LD, XT = DGA + C * LD,
+                       XQ = XT + C * LC, XM = XQ + C * LC, REF = XM + C * LC, BS = REF + 8 * DK, FLOATS = BS + C;
+};
+template <typename IO, int K, int V>
+__global__ void __launch_bounds__(NT, 1) grad_k_kernel(Params p) {
+  using S = Slot<K, V>;
+  using L = GkSmem;
+  extern __shared__ __align__(16) float sm[];
+  float *GC = sm + L::GC, *LKt = sm + L::LKT, *LQt = sm + L::LQT, *RT = sm + L::RT, *KR = sm + L::KR, *QR = sm + L::QR,
+        *DWs = sm + L::DW, *DKA = sm + L::DKA, *DGA = sm + L::DGA, *XT = sm + L::XT, *XQ = sm + L::XQ, *XM = sm + L::XM,
+        *refs = sm + L::REF, *bs = sm + L::BS;
+  int seq, m, rows;
+  long tok0;
+  const int f = blockIdx.x, hv = blockIdx.y, d0 = blockIdx.z * DK, tid = threadIdx.x, warp = tid >> 5;
+  if (!find_chunk(p, f, seq, m, tok0, rows)) return;
+  const int hk = hv / (p.HV / p.H);
+  const float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
+  const size_t qk_row = static_cast<size_t>(p.H) * K, qk_col = static_cast<size_t>(hk) * K + d0;
+
+  load_rows<IO, DK>(KR, static_cast<const IO*>(p.k), tok0, rows, qk_row, qk_col);
+  load_rows<IO, DK>(QR, static_cast<const IO*>(p.q), tok0, rows, qk_row, qk_col);
+  load_rows<float, DK>(GC, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K + d0);
+  for (int idx = tid; idx < C * (DK / 4); idx += NT) {
+    const int r = idx / (DK / 4), c4 = (idx - r * (DK / 4)) * 4;
+    *reinterpret_cast<float4*>(DWs + r * LD + c4) = load4(slot + S::DW + static_cast<size_t>(r) * K + d0 + c4);
+  }
+  copy_in<C, LC>(XT, slot + S::T, C);
+  copy_in<C, LC>(XQ, slot + S::DAQK, C);
+  copy_in<C, LC>(XM, slot + S::DMB, C);
+  if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
+  __syncthreads();
+  // tables: Lk, Lq from copies of the raw rows (the raw rows stay for the final pass)
+  for (int idx = tid; idx < C * DK; idx += NT) {
+    const int i = idx / DK, d = idx - i * DK;
+    LKt[i * LD + d] = KR[i * LD + d];
+    LQt[i * LD + d] = QR[i * LD + d];
+  }
+  __syncthreads();
+  make_tables<DK, LD>(LKt, LQt, GC, RT, refs, p.scale);
+  __syncthreads();
+  const int m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1), bi0 = m0 >> 4;  // one 16 x 32 tile of C x 64 per warp
+  const int lane = tid & 31, g = lane >> 2, t = lane & 3;
+  // 1. dkd = A^T dW -> dk_acc = e^{gc} dkd, dgc_acc = k e^{gc} dkd
+  {
+    float acc[4][4];
+    tile_init<4>(acc, [](int, int) { return 0.f; }, m0, n0);
+    tile_mma<4>(acc, [&](int j, int i, int) { return XT[i * LC + j] * bs[j]; }, [&](int i, int d, int) { return DWs[i * LD + d]; },
+                m0, n0, m0, C);
+    tile_epi<4>(acc, [&](int r, int c, float x0, float x1) {
+      const float y0 = ex2(GC[r * LD + c]) * x0, y1 = ex2(GC[r * LD + c + 1]) * x1;
+      DKA[r * LD + c] = y0;
+      DKA[r * LD + c + 1] = y1;
+      DGA[r * LD + c] = KR[r * LD + c] * y0;
+      DGA[r * LD + c + 1] = KR[r * LD + c + 1] * y1;
+    }, m0, n0);
+  }
+  // 2. row side: X_i = sum_j P_ij k_j e^{gc_i - gc_j} for P = dMb (dk) and dAqk (dq), by
+  //    column blocks with the accumulator rescaled between them
+  {
+    float ak[4][4], aq[4][4];
+    tile_init<4>(ak, [](int, int) { return 0.f; }, m0, n0);
+    tile_init<4>(aq, [](int, int) { return 0.f; }, m0, n0);
+    for (int bj = 0; bj <= bi0; ++bj) {
+      if (bj > 0) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = n0 + 8 * nt + 2 * t + (e & 1);
+            const float s = ex2(refs[(4 + bj) * DK + d] - refs[(3 + bj) * DK + d]);
+            ak[nt][e] *= s;
+            aq[nt][e] *= s;
+          }
+      }
+      const auto fb = [&](int j, int d, int) { return RT[j * LD + d]; };
+      tile_mma<4>(ak, [&](int i, int j, int) { return XM[i * LC + j]; }, fb, m0, n0, 16 * bj, 16 * bj + 16);
+      tile_mma<4>(aq, [&](int i, int j, int) { return XQ[i * LC + j]; }, fb, m0, n0, 16 * bj, 16 * bj + 16);
+    }
+    const float scale = p.scale;
+    float* dqp = p.dq + static_cast<size_t>(tok0) * qk_row + qk_col;
+    const float* dh = slot + S::DH + d0;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + g + 8 * (e >> 1), d = n0 + 8 * nt + 2 * t + (e & 1);
+        const float x = GC[r * LD + d];
+        const float fr = ex2(x - refs[(4 + bi0) * DK + d]);
+        const float dkr = ak[nt][e] * fr;
+        DKA[r * LD + d] += dkr;
+        DGA[r * LD + d] += KR[r * LD + d] * dkr;
+        const float dq = scale * (ex2(x) * dh[static_cast<size_t>(r) * K + d] + aq[nt][e] * fr);
+        DGA[r * LD + d] += QR[r * LD + d] * dq;
+        if (r < rows) atomicAdd(dqp + static_cast<size_t>(r) * qk_row + d, dq);
+      }
+  }
+  // 3. column side: Y_j = sum_i (dAqk_ij scale q_i + dMb_ij k_i) e^{gc_i - gc_j}, by row
+  //    blocks from the last, rescaled between them
+  {
+    float ac[4][4];
+    tile_init<4>(ac, [](int, int) { return 0.f; }, m0, n0);
+    for (int bi = 3; bi >= bi0; --bi) {
+      if (bi < 3) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = n0 + 8 * nt + 2 * t + (e & 1);
+            ac[nt][e] *= ex2(refs[(bi + 1) * DK + d] - refs[bi * DK + d]);
+          }
+      }
+      tile_mma<4>(ac, [&](int j, int i, int) { return XQ[i * LC + j]; }, [&](int i, int d, int) { return LQt[i * LD + d]; }, m0, n0,
+                  16 * bi, 16 * bi + 16);
+      tile_mma<4>(ac, [&](int j, int i, int) { return XM[i * LC + j]; }, [&](int i, int d, int) { return LKt[i * LD + d]; }, m0, n0,
+                  16 * bi, 16 * bi + 16);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + g + 8 * (e >> 1), d = n0 + 8 * nt + 2 * t + (e & 1);
+        const float y = ac[nt][e] * ex2(refs[bi0 * DK + d] - GC[r * LD + d]);
+        DKA[r * LD + d] += y;
+        DGA[r * LD + d] -= KR[r * LD + d] * y;
+      }
+  }
+  // 4. dk_e^{gl-gc} = dkr e^{gl - gc}; dk out; dgc; dg = reverse cumulative sum
+  {
+    const float* dkr = slot + S::DKR + d0;
+    float* dkp = p.dk + static_cast<size_t>(tok0) * qk_row + qk_col;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + g + 8 * (e >> 1), d = n0 + 8 * nt + 2 * t + (e & 1);
+        const float x = dkr[static_cast<size_t>(r) * K + d] * ex2(refs[7 * DK + d] - GC[r * LD + d]);
+        const float dkv = DKA[r * LD + d] + x;
+        DGA[r * LD + d] -= KR[r * LD + d] * x;
+        DKA[r * LD + d] = KR[r * LD + d] * x;  // (now k dk_e^{gl-gc}, summed over rows below)
+        if (r < rows) atomicAdd(dkp + static_cast<size_t>(r) * qk_row + d, dkv);
+      }
+  }
+  __syncthreads();
+  if (tid < DK) {
+    float s = slot[S::DGL + d0 + tid];
+    for (int i = 0; i < C; ++i) s += DKA[i * LD + tid];
+    float* dgp = p.dg + static_cast<size_t>(tok0) * p.HV * K + static_cast<size_t>(hv) * K + d0 + tid;
+    for (int i = C - 1; i >= 0; --i) {
+      s += DGA[i * LD + tid];
+      if (i < rows) dgp[static_cast<size_t>(i) * p.HV * K] = s;
+    }
+  }
+}
+
+template <typename IO, int K, int V>
+cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
+  const size_t s_prep = PrepSmem<K, V>::FLOATS * 4, s_chain = ChainSmem<K>::FLOATS * 4, s_gv = GvSmem<K, V>::FLOATS * 4,
+               s_gc = GcSmem<K>::FLOATS * 4, s_gk = GkSmem::FLOATS * 4;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(prep_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_prep)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(chain_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_chain)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(grad_v_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gv)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(grad_cc_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gc)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(grad_k_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gk)) != cudaSuccess)
+    return e;
+  if (chunks > 0) {
+    prep_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_prep, st>>>(p);
+  }
+  chain_kernel<K, V><<<dim3(V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
+  if (chunks > 0) {
+    grad_v_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gv, st>>>(p);
+    grad_cc_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gc, st>>>(p);
+    grad_k_kernel<IO, K, V><<<dim3(chunks, p.HV, K / DK), NT, s_gk, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace cbwd
+
+// Flat chunk slots the chunk-form backward needs: every chunk of every sequence (a bound
+// when the lengths are on the device: T / 64 + one partial chunk per sequence).
+size_t backward_chunk_slots(long T, int num_seqs_or_B, bool varlen, int HV) {
+  const long nc = (T + cbwd::C - 1) / cbwd::C;
+  const long chunks = varlen ? nc + num_seqs_or_B : nc * num_seqs_or_B;
+  return static_cast<size_t>(chunks) * HV;
+}
+size_t backward_chunk_slot_floats(int K, int V) {
+  if (K == 128 && V == 128) return cbwd::Slot<128, 128>::FLOATS;
+  if (K == 128 && V == 64) return cbwd::Slot<128, 64>::FLOATS;
+  if (K == 64 && V == 128) return cbwd::Slot<64, 128>::FLOATS;
+  return cbwd::Slot<64, 64>::FLOATS;
+}
+
+cudaError_t launch_backward_chunk(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  const float* s0, const int32_t* cu, const void* d_out, const float* d_fin, float* dq,
+                                  float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* ws,
+                                  uint32_t* status, float scale, int T, int H, int HV, int K, int V, int num_seqs,
+                                  bool bf16, cudaStream_t stream) {
+  const int nc = (T + cbwd::C - 1) / cbwd::C;
+  const int chunks = cu ? nc + num_seqs : nc * num_seqs;
+  cbwd::Params p{q, k, v, g, beta, s0, cu, d_out, d_fin, dq, dk, dv, dg, dbeta, ds0, ws, status,
+                 backward_chunk_slot_floats(K, V), scale, T, H, HV, num_seqs, nc};
+  if (bf16) {
+    if (K == 128 && V == 128) return cbwd::launch_kv<__nv_bfloat16, 128, 128>(p, chunks, stream);
+    if (K == 128 && V == 64) return cbwd::launch_kv<__nv_bfloat16, 128, 64>(p, chunks, stream);
+    if (K == 64 && V == 128) return cbwd::launch_kv<__nv_bfloat16, 64, 128>(p, chunks, stream);
+    return cbwd::launch_kv<__nv_bfloat16, 64, 64>(p, chunks, stream);
+  }
+  if (K == 128 && V == 128) return cbwd::launch_kv<float, 128, 128>(p, chunks, stream);
+  if (K == 128 && V == 64) return cbwd::launch_kv<float, 128, 64>(p, chunks, stream);
+  if (K == 64 && V == 128) return cbwd::launch_kv<float, 64, 128>(p, chunks, stream);
+  return cbwd::launch_kv<float, 64, 64>(p, chunks, stream);
+}
+
+}  // namespace kda

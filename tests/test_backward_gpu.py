@@ -1,12 +1,15 @@
 """GPU parity of kda_backward: the gradients of sum <d_out, o> + <dS_final, S_final>
 with respect to q, k, v, g, beta and the initial state, compared with the fp64
 oracle's reverse mode through the token recurrence (itself pinned by central
-differences) on the same inputs.
+differences) on the same inputs.  Every case runs both backward paths: the chunk form
+(the default: tensor-core products in TF32 with high/low operand splitting) and the
+token recurrence (KDA_BACKWARD=recurrent, fp32 on CUDA cores).
 
-The kernel computes in fp32 whatever the I/O type (bf16 inputs reach both sides as
+Both compute in fp32 accuracy whatever the I/O type (bf16 inputs reach both sides as
 the same rounded values), so every gradient is held to 1e-4 of its largest magnitude:
 the recurrence forgets within a few tens of tokens at these gates, and the fp32
-rounding of sums of O(K V) terms over such a window stays near 1e-6.
+rounding of sums of O(K V) terms over such a window stays near 1e-6 (the split TF32
+products carry about 2^-21 relative error per term, the same order).
 """
 import numpy as np
 import pytest
@@ -29,6 +32,15 @@ def _built():
         pytest.skip("no CUDA device")
     kda.build()
     kda.load_library()
+
+
+@pytest.fixture(autouse=True, params=["chunk", "recurrent"])
+def path(request, monkeypatch):
+    if request.param == "recurrent":
+        monkeypatch.setenv("KDA_BACKWARD", "recurrent")
+    else:
+        monkeypatch.delenv("KDA_BACKWARD", raising=False)
+    return request.param
 
 
 def _grads_in(x, seed, with_dfin=True):
@@ -110,3 +122,21 @@ def test_backward_zero_tokens():
     do, dfin = _grads_in(x, 6)
     got, _ = _run(x, do, dfin)
     assert np.array_equal(got[5], dfin.numpy())
+
+
+def test_backward_many_sequences_gva():
+    """Eight packed sequences of mixed lengths with G = 4 value heads per key head:
+    the chunk path's flat chunk numbering across sequences and the key-head sums."""
+    x = W.make_inputs(1, 0, 2, 8, 128, 128, "bf16", seed=306, init_state=True,
+                      lengths=[5, 64, 130, 300, 1, 77, 256, 190])
+    do, dfin = _grads_in(x, 7)
+    got, ref = _run(x, do, dfin)
+    _assert_grads(got, ref, "many sequences")
+
+
+def test_backward_strong_decay_long():
+    """The bounded gate at its limit over several chunks: block factors in every chunk."""
+    x = W.make_inputs(1, 700, 1, 2, 128, 128, "bf16", seed=307, init_state=True, gate="bounded", gate_value=-5.0)
+    do, dfin = _grads_in(x, 8)
+    got, ref = _run(x, do, dfin)
+    _assert_grads(got, ref, "strong decay, 700 tokens")
