@@ -31,7 +31,7 @@
 //                   gradient kernels (workspace slot per (chunk, value head));
 //   chain_kernel    the states entering each chunk (h_{n+1} = Q_n h_n + R_n) and the
 //                   state gradients leaving it (dS_n = Q_n^T dS_{n+1} + B_n), one CTA per
-//                   32 value columns and direction (the columns are independent);
+//                   64 value columns and direction (the columns are independent);
 //   grad_v_kernel   v_new, dv_new and the products with S and dS' (dv final);
 //   grad_cc_kernel  dA, dM and dbeta (C x C);
 //   grad_k_kernel   dq, dk, dg (per 64 key dims).
@@ -107,10 +107,6 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
   return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
                      __uint_as_float(u.y & 0xFFFF0000u));
 }
-__device__ __forceinline__ float load1(const float* p) { return *p; }
-__device__ __forceinline__ float load1(const __nv_bfloat16* p) {
-  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
-}
 
 // Flat chunk f (chunks numbered sequence by sequence) -> its sequence, chunk within the
 // sequence, first token and rows; false past the last chunk or on a bad cu_seqlens.
@@ -164,27 +160,45 @@ __device__ bool seq_chunks(const Params& p, int seq, int& f0, int& nch) {
 
 // C rows of N columns (io type) into fp32 shared memory with row stride N + 4; rows
 // past `rows` are zero.
+// (all of a thread's loads are issued before its stores: C N / 4 is a multiple of NT)
 template <typename IO, int N>
 __device__ __forceinline__ void load_rows(float* dst, const IO* src, long row0, int rows, size_t row_stride,
                                           size_t col0) {
-  for (int idx = threadIdx.x; idx < C * (N / 4); idx += NT) {
-    const int r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < rows) x = load4(src + static_cast<size_t>(row0 + r) * row_stride + col0 + c4);
-    *reinterpret_cast<float4*>(dst + r * (N + 4) + c4) = x;
+  constexpr int PER = C * (N / 4) / NT;
+  static_assert(C * (N / 4) % NT == 0, "whole passes");
+  float4 x[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = threadIdx.x + u * NT, r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < rows) x[u] = load4(src + static_cast<size_t>(row0 + r) * row_stride + col0 + c4);
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = threadIdx.x + u * NT, r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    *reinterpret_cast<float4*>(dst + r * (N + 4) + c4) = x[u];
   }
 }
 // rows x N dense fp32 (global) <-> shared memory with row stride LD
 template <int N, int LD>
-__device__ __forceinline__ void copy_in(float* dst, const float* src, int rows) {
-  for (int idx = threadIdx.x; idx < rows * (N / 4); idx += NT) {
-    const int r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
-    *reinterpret_cast<float4*>(dst + r * LD + c4) = load4(src + static_cast<size_t>(r) * N + c4);
+__device__ __forceinline__ void copy_in(float* dst, const float* src) {
+  constexpr int PER = C * (N / 4) / NT;
+  static_assert(C * (N / 4) % NT == 0, "whole passes");
+  float4 x[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = threadIdx.x + u * NT, r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    x[u] = load4(src + static_cast<size_t>(r) * N + c4);
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = threadIdx.x + u * NT, r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
+    *reinterpret_cast<float4*>(dst + r * LD + c4) = x[u];
   }
 }
 template <int N, int LD>
-__device__ __forceinline__ void copy_out(float* dst, const float* src, int rows) {
-  for (int idx = threadIdx.x; idx < rows * (N / 4); idx += NT) {
+__device__ __forceinline__ void copy_out(float* dst, const float* src) {
+  for (int idx = threadIdx.x; idx < C * (N / 4); idx += NT) {
     const int r = idx / (N / 4), c4 = (idx - r * (N / 4)) * 4;
     *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * N + c4) = *reinterpret_cast<const float4*>(src + r * LD + c4);
   }
@@ -204,36 +218,60 @@ __device__ __forceinline__ void cumsum_log2(float* x) {
 }
 
 // ------------------------------------------------------------ warp products --
-// One warp accumulates the 16 x (8 NT8) tile at (m0, n0) of sum_k A(m, k) B(k, n) over
-// k in [kb, ke) (multiples of 8).  fa(m, k, n0) and fb(k, n, m0) return fp32 operands;
-// each is split into TF32 high and low parts and the three products hi*hi, hi*lo,
-// lo*hi accumulate in fp32 (kSplit), else a single TF32 product.
-template <int NT8, class FA, class FB>
-__device__ __forceinline__ void tile_mma(float (&acc)[NT8][4], const FA& fa, const FB& fb, int m0, int n0, int kb,
+// One warp accumulates MT stacked 16 x (8 NT8) tiles at (m0 + 16 mt, n0) of
+// sum_k A(m, k) B(k, n) over k in [kb, ke) (multiples of 8).  fa(m, k, n0) and
+// fb(k, n, m0) return fp32 operands; each is split into TF32 high and low parts and the
+// three products lo*hi, hi*lo, hi*hi accumulate in fp32 (kSplit), else a single TF32
+// product.  The fragments of a k-step are loaded first, then the products run in passes
+// over all accumulators, so that no product waits on the one before it.
+template <int MT, int NT8, class FA, class FB>
+__device__ __forceinline__ void tile_mma(float (&acc)[MT][NT8][4], const FA& fa, const FB& fb, int m0, int n0, int kb,
                                          int ke) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll 2
   for (int k = kb; k < ke; k += 8) {
-    const float av[4] = {fa(m0 + g, k + t, n0), fa(m0 + g + 8, k + t, n0), fa(m0 + g, k + t + 4, n0),
-                         fa(m0 + g + 8, k + t + 4, n0)};
-    uint32_t ah[4], al[4];
+    uint32_t ah[MT][4], al[MT][4], bh[NT8][2], bl[NT8][2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      ah[e] = to_tf32(av[e]);
-      if (kSplit) al[e] = to_tf32(av[e] - __uint_as_float(ah[e]));
+    for (int mt = 0; mt < MT; ++mt) {
+      const int m = m0 + 16 * mt + g;
+      const float av[4] = {fa(m, k + t, n0), fa(m + 8, k + t, n0), fa(m, k + t + 4, n0), fa(m + 8, k + t + 4, n0)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ah[mt][e] = to_tf32(av[e]);
+        if (kSplit) al[mt][e] = to_tf32(av[e] - __uint_as_float(ah[mt][e]));
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < NT8; ++nt) {
       const int n = n0 + 8 * nt + g;
-      const float b0 = fb(k + t, n, m0), b1 = fb(k + t + 4, n, m0);
-      const uint32_t bh0 = to_tf32(b0), bh1 = to_tf32(b1);
-      if (kSplit) {
-        mma_tf32_m16n8k8(acc[nt], al, bh0, bh1);
-        mma_tf32_m16n8k8(acc[nt], ah, to_tf32(b0 - __uint_as_float(bh0)), to_tf32(b1 - __uint_as_float(bh1)));
+      const float bv[2] = {fb(k + t, n, m0), fb(k + t + 4, n, m0)};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        bh[nt][e] = to_tf32(bv[e]);
+        if (kSplit) bl[nt][e] = to_tf32(bv[e] - __uint_as_float(bh[nt][e]));
       }
-      mma_tf32_m16n8k8(acc[nt], ah, bh0, bh1);
     }
+    if (kSplit) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(acc[mt][nt], al[mt], bh[nt][0], bh[nt][1]);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(acc[mt][nt], ah[mt], bl[nt][0], bl[nt][1]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(acc[mt][nt], ah[mt], bh[nt][0], bh[nt][1]);
   }
+}
+// single 16-row tile
+template <int NT8, class FA, class FB>
+__device__ __forceinline__ void tile_mma(float (&acc)[NT8][4], const FA& fa, const FB& fb, int m0, int n0, int kb,
+                                         int ke) {
+  tile_mma<1, NT8>(reinterpret_cast<float(&)[1][NT8][4]>(acc), fa, fb, m0, n0, kb, ke);
 }
 // accumulator element e of n-tile nt: row m0 + g + 8 (e >> 1), column n0 + 8 nt + 2 t + (e & 1)
 template <int NT8, class FI>
@@ -253,24 +291,31 @@ __device__ __forceinline__ void tile_epi(const float (&acc)[NT8][4], const FE& e
     epi(m0 + g + 8, n0 + 8 * nt + 2 * t, acc[nt][2], acc[nt][3]);
   }
 }
-// The whole M x N product over the CTA's warps, tile by tile: init, the k range
-// krange(m0, n0) (int2), epilogue on column pairs.  Tiles for which live(m0, n0) is
-// false keep their init values.
+// The whole M x N product over the CTA's warps, tile by tile (MT x 16 rows by 8 NT8
+// columns): init, the k range krange(m0, n0) (int2), epilogue on column pairs.  Tiles for
+// which live(m0, n0) is false keep their init values.
+template <int M, int N, int NT8, int MT, class FA, class FB, class FL, class FR, class FI, class FE>
+__device__ __forceinline__ void cta_gemm(const FA& fa, const FB& fb, const FL& live, const FR& krange, const FI& init,
+                                         const FE& epi) {
+  constexpr int TN = N / (8 * NT8), TILES = (M / (16 * MT)) * TN;
+  const int warp = threadIdx.x >> 5;
+  for (int tile = warp; tile < TILES; tile += NW) {
+    const int m0 = (tile / TN) * 16 * MT, n0 = (tile % TN) * (8 * NT8);
+    float acc[MT][NT8][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) tile_init<NT8>(acc[mt], init, m0 + 16 * mt, n0);
+    if (live(m0, n0)) {
+      const int2 kr = krange(m0, n0);
+      tile_mma<MT, NT8>(acc, fa, fb, m0, n0, kr.x, kr.y);
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) tile_epi<NT8>(acc[mt], epi, m0 + 16 * mt, n0);
+  }
+}
 template <int M, int N, int NT8, class FA, class FB, class FL, class FR, class FI, class FE>
 __device__ __forceinline__ void cta_gemm(const FA& fa, const FB& fb, const FL& live, const FR& krange, const FI& init,
                                          const FE& epi) {
-  constexpr int TN = N / (8 * NT8), TILES = (M / 16) * TN;
-  const int warp = threadIdx.x >> 5;
-  for (int tile = warp; tile < TILES; tile += NW) {
-    const int m0 = (tile / TN) * 16, n0 = (tile % TN) * (8 * NT8);
-    float acc[NT8][4];
-    tile_init<NT8>(acc, init, m0, n0);
-    if (live(m0, n0)) {
-      const int2 kr = krange(m0, n0);
-      tile_mma<NT8>(acc, fa, fb, m0, n0, kr.x, kr.y);
-    }
-    tile_epi<NT8>(acc, epi, m0, n0);
-  }
+  cta_gemm<M, N, NT8, 1>(fa, fb, live, krange, init, epi);
 }
 
 // ---------------------------------------------------------------- prep ----
@@ -397,14 +442,14 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
   //    (i, j) in blocks (bi, bj): sum_d Lk_i e^{s_bi - e_bj} R_j
   {
     const auto rb = [&](int kk, int nn, int) { return B3[nn * LK + kk]; };
-    const auto lower = [](int m0, int n0) { return n0 <= m0; };
+    const auto lower = [](int m0, int n0) { return n0 <= m0 + 16; };
     const auto kr = [](int, int) { return make_int2(0, K); };
-    cta_gemm<C, C, 2>([&](int mm, int kk, int n0) { return B0[mm * LK + kk] * D[pair_index(mm >> 4, n0 >> 4) * K + kk]; },
+    cta_gemm<C, C, 2, 2>([&](int mm, int kk, int n0) { return B0[mm * LK + kk] * D[pair_index(mm >> 4, n0 >> 4) * K + kk]; },
                       rb, lower, kr, zero, [&](int r, int c, float x0, float x1) {
                         X1[r * LC + c] = c < r ? x0 : 0.f;
                         X1[r * LC + c + 1] = c + 1 < r ? x1 : 0.f;
                       });
-    cta_gemm<C, C, 2>([&](int mm, int kk, int n0) { return B1[mm * LK + kk] * D[pair_index(mm >> 4, n0 >> 4) * K + kk]; },
+    cta_gemm<C, C, 2, 2>([&](int mm, int kk, int n0) { return B1[mm * LK + kk] * D[pair_index(mm >> 4, n0 >> 4) * K + kk]; },
                       rb, lower, kr, zero, [&](int r, int c, float x0, float x1) {
                         X2[r * LC + c] = c <= r ? x0 : 0.f;
                         X2[r * LC + c + 1] = c + 1 <= r ? x1 : 0.f;
@@ -415,8 +460,8 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
   tri_inverse(X1, bs, X3, B2);
   // 4. W = A kd (B2): A = T Diag(beta), kd = Lk e^{s_b}
   const auto fa_A = [&](int i, int j, int) { return X3[i * LC + j] * bs[j]; };
-  const auto kr_tril = [](int m0, int) { return make_int2(0, m0 + 16); };
-  cta_gemm<C, K, 4>(fa_A, [&](int j, int d, int) { return B0[j * LK + d] * F[(j >> 4) * K + d]; }, all, kr_tril, zero,
+  const auto kr_tril = [](int m0, int) { return make_int2(0, m0 + 32); };
+  cta_gemm<C, K, 4, 2>(fa_A, [&](int j, int d, int) { return B0[j * LK + d] * F[(j >> 4) * K + d]; }, all, kr_tril, zero,
                     [&](int r, int c, float x0, float x1) {
                       B2[r * LK + c] = x0;
                       B2[r * LK + c + 1] = x1;
@@ -425,127 +470,146 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
   // 5. Q = Diag(e^{gl}) - kr^T W (kr = R e^{gl - e_b}); W to the slot
   const auto fa_krT = [&](int d, int i, int) { return B3[i * LK + d] * G[(i >> 4) * K + d]; };
   const auto kr_all = [](int, int) { return make_int2(0, C); };
-  cta_gemm<K, K, 4>(fa_krT, [&](int i, int e, int) { return B2[i * LK + e]; }, all, kr_all, zero,
+  cta_gemm<K, K, 4, 2>(fa_krT, [&](int i, int e, int) { return B2[i * LK + e]; }, all, kr_all, zero,
                     [&](int r, int c, float x0, float x1) {
                       *reinterpret_cast<float2*>(slot + S::Q + static_cast<size_t>(r) * K + c) =
                           make_float2((r == c ? EG[r] : 0.f) - x0, (r == c + 1 ? EG[r] : 0.f) - x1);
                     });
-  copy_out<K, LK>(slot + S::W, B2, C);
+  copy_out<K, LK>(slot + S::W, B2);
   __syncthreads();
   // 6. U = A v (B4), R = kr^T U to the slot
   load_rows<IO, V>(B0, static_cast<const IO*>(p.v), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
   __syncthreads();
-  cta_gemm<C, V, 4>(fa_A, [&](int j, int vv, int) { return B0[j * LV + vv]; }, all, kr_tril, zero,
+  cta_gemm<C, V, 4, 2>(fa_A, [&](int j, int vv, int) { return B0[j * LV + vv]; }, all, kr_tril, zero,
                     [&](int r, int c, float x0, float x1) {
                       B4[r * LV + c] = x0;
                       B4[r * LV + c + 1] = x1;
                     });
   __syncthreads();
-  cta_gemm<K, V, 4>(fa_krT, [&](int i, int vv, int) { return B4[i * LV + vv]; }, all, kr_all, zero,
+  cta_gemm<K, V, 4, 2>(fa_krT, [&](int i, int vv, int) { return B4[i * LV + vv]; }, all, kr_all, zero,
                     [&](int r, int c, float x0, float x1) {
                       *reinterpret_cast<float2*>(slot + S::RH + static_cast<size_t>(r) * V + c) = make_float2(x0, x1);
                     });
-  copy_out<V, LV>(slot + S::U, B4, C);
+  copy_out<V, LV>(slot + S::U, B4);
   __syncthreads();
   // 7. E = Aqk^T do (B4), B = qd^T do - W^T E to the slot
   load_rows<IO, V>(B0, static_cast<const IO*>(p.d_out), tok0, rows, static_cast<size_t>(p.HV) * V,
                    static_cast<size_t>(hv) * V);
   __syncthreads();
-  cta_gemm<C, V, 4>([&](int j, int i, int) { return X2[i * LC + j]; }, [&](int i, int vv, int) { return B0[i * LV + vv]; },
+  cta_gemm<C, V, 4, 2>([&](int j, int i, int) { return X2[i * LC + j]; }, [&](int i, int vv, int) { return B0[i * LV + vv]; },
                     all, [](int m0, int) { return make_int2(m0, C); }, zero, [&](int r, int c, float x0, float x1) {
                       B4[r * LV + c] = x0;
                       B4[r * LV + c + 1] = x1;
                     });
   __syncthreads();
-  cta_gemm<K, V, 4>(
+  cta_gemm<K, V, 4, 2>(
       [&](int d, int kk, int) { return kk < C ? B1[kk * LK + d] * F[(kk >> 4) * K + d] : -B2[(kk - C) * LK + d]; },
       [&](int kk, int vv, int) { return kk < C ? B0[kk * LV + vv] : B4[(kk - C) * LV + vv]; }, all,
       [](int, int) { return make_int2(0, 2 * C); }, zero, [&](int r, int c, float x0, float x1) {
         *reinterpret_cast<float2*>(slot + S::BD + static_cast<size_t>(r) * V + c) = make_float2(x0, x1);
       });
-  copy_out<V, LV>(slot + S::E, B4, C);
-  copy_out<C, LC>(slot + S::T, X3, C);
-  copy_out<C, LC>(slot + S::KK, X1, C);
+  copy_out<V, LV>(slot + S::E, B4);
+  copy_out<C, LC>(slot + S::T, X3);
+  copy_out<C, LC>(slot + S::KK, X1);
 }
 
 // --------------------------------------------------------------- chains ----
-constexpr int VS = 32;  // value columns per chain CTA
+// One CTA per 64 value columns and direction: X (K x 64, two buffers) in shared memory,
+// Q of the next chunk prefetched by cp.async while the current one is applied, the
+// addend (R or B) read straight into the accumulators' registers.
+constexpr int VS = 64;  // value columns per chain CTA
 template <int K>
 struct ChainSmem {
   static constexpr int LK = K + 4, LS = VS + 4;
-  static constexpr int Q0 = 0, Q1 = K * LK, A0 = 2 * K * LK, A1 = A0 + K * LS, X = A1 + K * LS, FLOATS = X + K * LS;
+  static constexpr int Q0 = 0, Q1 = K * LK, X0 = 2 * K * LK, X1 = X0 + K * LS, FLOATS = X1 + K * LS;
 };
 template <int K, int V>
 __global__ void __launch_bounds__(NT, 1) chain_kernel(Params p) {
   using S = Slot<K, V>;
   using L = ChainSmem<K>;
   constexpr int LK = L::LK, LS = L::LS;
-  constexpr int NT8 = K == 128 ? 4 : 2;  // one 16 x (8 NT8) tile of the K x 32 product per warp
+  constexpr int VC = V < VS ? V : VS;       // value columns of this CTA
+  constexpr int RB = K / 16;                // 16-row blocks of the K x VC product
+  constexpr int WPR = NW / RB;              // warps per row block
+  constexpr int NT8 = VC / (8 * WPR);       // one 16 x (8 NT8) tile per warp
+  static_assert(NW % RB == 0 && VC % (8 * WPR) == 0, "tiles");
   extern __shared__ __align__(16) float sm[];
   auto Qb = [&](int b) { return sm + (b ? L::Q1 : L::Q0); };
-  auto Ab = [&](int b) { return sm + (b ? L::A1 : L::A0); };
-  float* X = sm + L::X;
-  const int v0 = blockIdx.x * VS, hv = blockIdx.y, seq = blockIdx.z >> 1, dir = blockIdx.z & 1, tid = threadIdx.x;
+  auto Xb = [&](int b) { return sm + (b ? L::X1 : L::X0); };
+  const int v0 = blockIdx.x * VC, hv = blockIdx.y, seq = blockIdx.z >> 1, dir = blockIdx.z & 1, tid = threadIdx.x;
   int f0, nch;
   if (!seq_chunks(p, seq, f0, nch)) return;
   const float* x0 = dir == 0 ? p.s0 : p.d_fin;
   const size_t state0 = (static_cast<size_t>(seq) * p.HV + hv) * K * V + v0;
-  for (int idx = tid; idx < K * VS; idx += NT) {
-    const int r = idx / VS, c = idx - r * VS;
-    X[r * LS + c] = x0 ? x0[state0 + static_cast<size_t>(r) * V + c] : 0.f;
+  for (int idx = tid; idx < K * VC; idx += NT) {
+    const int r = idx / VC, c = idx - r * VC;
+    Xb(0)[r * LS + c] = x0 ? x0[state0 + static_cast<size_t>(r) * V + c] : 0.f;
   }
   const size_t add = dir == 0 ? S::RH : S::BD;
-  auto slot = [&](int mm) { return p.ws + (static_cast<size_t>(f0 + mm) * p.HV + hv) * p.slot_floats; };
+  auto slot = [&](int step) {
+    return p.ws + (static_cast<size_t>(f0 + (dir == 0 ? step : nch - 1 - step)) * p.HV + hv) * p.slot_floats;
+  };
   auto issue = [&](int step, int buf) {
-    const float* s = slot(dir == 0 ? step : nch - 1 - step);
+    const float* s = slot(step);
     for (int idx = tid; idx < K * (K / 4); idx += NT) {
       const int r = idx / (K / 4), c4 = (idx - r * (K / 4)) * 4;
       cp_async16(Qb(buf) + r * LK + c4, s + S::Q + static_cast<size_t>(r) * K + c4);
     }
-    for (int idx = tid; idx < K * (VS / 4); idx += NT) {
-      const int r = idx / (VS / 4), c4 = (idx - r * (VS / 4)) * 4;
-      cp_async16(Ab(buf) + r * LS + c4, s + add + static_cast<size_t>(r) * V + v0 + c4);
-    }
     cp_async_commit();
   };
   if (nch > 0) issue(0, 0);
-  const int warp = tid >> 5;
-  const int m0 = K == 128 ? 16 * warp : 16 * (warp >> 1), n0 = K == 128 ? 0 : 16 * (warp & 1);
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int m0 = 16 * (warp / WPR), n0 = (warp % WPR) * 8 * NT8;
+  int cur = 0;
   for (int step = 0; step < nch; ++step) {
-    const int buf = step & 1;
-    float* s = slot(dir == 0 ? step : nch - 1 - step);
+    float* s = slot(step);
     if (step + 1 < nch) {
-      issue(step + 1, buf ^ 1);
+      issue(step + 1, (step + 1) & 1);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
-    __syncthreads();  // this chunk's Q and addend (and X) visible to every thread
-    // the state entering the chunk (forward) / the gradient leaving it (reverse) takes
-    // the addend's place in the slot
-    for (int idx = tid; idx < K * (VS / 4); idx += NT) {
-      const int r = idx / (VS / 4), c4 = (idx - r * (VS / 4)) * 4;
-      *reinterpret_cast<float4*>(s + add + static_cast<size_t>(r) * V + v0 + c4) =
-          *reinterpret_cast<const float4*>(X + r * LS + c4);
-    }
-    const float* Q = Qb(buf);
-    const float* Ad = Ab(buf);
+    __syncthreads();  // Q of this chunk and X visible to every thread
+    float2 ad[NT8][2];  // this tile's addend
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        ad[nt][h] = *reinterpret_cast<const float2*>(s + add + static_cast<size_t>(m0 + g + 8 * h) * V + v0 + n0 + 8 * nt + 2 * t);
+    const float* Q = Qb(step & 1);
+    const float* X = Xb(cur);
     float acc[NT8][4];
-    tile_init<NT8>(acc, [&](int r, int c) { return Ad[r * LS + c]; }, m0, n0);
+    tile_init<NT8>(acc, [](int, int) { return 0.f; }, m0, n0);
     if (dir == 0)
       tile_mma<NT8>(acc, [&](int d, int e, int) { return Q[d * LK + e]; }, [&](int e, int c, int) { return X[e * LS + c]; },
                     m0, n0, 0, K);
     else
       tile_mma<NT8>(acc, [&](int d, int e, int) { return Q[e * LK + d]; }, [&](int e, int c, int) { return X[e * LS + c]; },
                     m0, n0, 0, K);
-    __syncthreads();  // every warp has read X (and stored it)
-    tile_epi<NT8>(acc, [&](int r, int c, float a, float b) { *reinterpret_cast<float2*>(X + r * LS + c) = make_float2(a, b); },
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+      acc[nt][0] += ad[nt][0].x;
+      acc[nt][1] += ad[nt][0].y;
+      acc[nt][2] += ad[nt][1].x;
+      acc[nt][3] += ad[nt][1].y;
+    }
+    __syncthreads();  // every thread has its addend: the slot's addend place may be overwritten
+    // the state entering the chunk (forward) / the gradient leaving it (reverse)
+    for (int idx = tid; idx < K * (VC / 4); idx += NT) {
+      const int r = idx / (VC / 4), c4 = (idx - r * (VC / 4)) * 4;
+      *reinterpret_cast<float4*>(s + add + static_cast<size_t>(r) * V + v0 + c4) =
+          *reinterpret_cast<const float4*>(X + r * LS + c4);
+    }
+    float* Xn = Xb(cur ^ 1);
+    tile_epi<NT8>(acc, [&](int r, int c, float a, float b) { *reinterpret_cast<float2*>(Xn + r * LS + c) = make_float2(a, b); },
                   m0, n0);
+    cur ^= 1;
   }
   if (dir == 1 && p.ds0) {
     __syncthreads();
-    for (int idx = tid; idx < K * VS; idx += NT) {
-      const int r = idx / VS, c = idx - r * VS;
+    const float* X = Xb(cur);
+    for (int idx = tid; idx < K * VC; idx += NT) {
+      const int r = idx / VC, c = idx - r * VC;
       p.ds0[state0 + static_cast<size_t>(r) * V + c] = X[r * LS + c];
     }
   }
@@ -565,7 +629,7 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
   using S = Slot<K, V>;
   using L = GvSmem<K, V>;
   constexpr int LK = L::LK, LV = L::LV;
-  constexpr int NT8 = V == 128 ? 8 : 4;  // v_new / dv_new: one 16 x (V / 2) tile per warp
+  constexpr int NT8 = V / 32;  // v_new / dv_new: one 32 x (V / 4) tile per warp
   extern __shared__ __align__(16) float sm[];
   float *B0 = sm + L::B0, *B1 = sm + L::B1, *B2 = sm + L::B2, *B3 = sm + L::B3, *B4 = sm + L::B4;
   auto Hs = [&](int b) { return sm + (b ? L::H1 : L::H0); };
@@ -581,22 +645,22 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
   const auto all = [](int, int) { return true; };
 
   // 1. W (B0), U (B2), E (B3) from the slot, do (B4); kr = k e^{gl - gc} (B1)
-  copy_in<K, LK>(B0, slot + S::W, C);
-  copy_in<V, LV>(B2, slot + S::U, C);
-  copy_in<V, LV>(B3, slot + S::E, C);
+  copy_in<K, LK>(B0, slot + S::W);
+  copy_in<V, LV>(B3, slot + S::E);
   load_rows<IO, V>(B4, static_cast<const IO*>(p.d_out), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
   load_rows<float, K>(B1, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K);
+  load_rows<IO, K>(B2, static_cast<const IO*>(p.k), tok0, rows, static_cast<size_t>(p.H) * K, static_cast<size_t>(hk) * K);
   __syncthreads();
   cumsum_log2<K, LK>(B1);
   __syncthreads();
   if (tid < K) gl2[tid] = B1[(C - 1) * LK + tid];
   __syncthreads();
-  const IO* kp = static_cast<const IO*>(p.k);
   for (int idx = tid; idx < C * K; idx += NT) {
     const int i = idx / K, d = idx - i * K;
-    const float kk = i < rows ? load1(kp + static_cast<size_t>(tok0 + i) * p.H * K + static_cast<size_t>(hk) * K + d) : 0.f;
-    B1[i * LK + d] = kk * ex2(gl2[d] - B1[i * LK + d]);
+    B1[i * LK + d] = B2[i * LK + d] * ex2(gl2[d] - B1[i * LK + d]);
   }
+  __syncthreads();
+  copy_in<V, LV>(B2, slot + S::U);
   // slices of S (entering) and dS' (leaving) in SR-row pieces
   const float* hsrc = slot + S::RH;
   const float* dsrc = slot + S::BD;
@@ -610,12 +674,15 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
     cp_async_commit();
   };
   constexpr int NSL = K / SR;
-  const int vm0 = 16 * (warp >> 1), vn0 = (V / 2) * (warp & 1);
-  float avn[NT8][4], adv[NT8][4];
+  const int vm0 = 32 * (warp >> 2), vn0 = (V / 4) * (warp & 3);
+  float avn[2][NT8][4], adv[2][NT8][4];
   // 2. pass 1: v_new = U - W S, dv_new = E + kr dS', DH = do S^T, dgl = e^{gl} sum_v S dS'
   __syncthreads();
-  tile_init<NT8>(avn, [&](int r, int c) { return B2[r * LV + c]; }, vm0, vn0);
-  tile_init<NT8>(adv, [&](int r, int c) { return B3[r * LV + c]; }, vm0, vn0);
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    tile_init<NT8>(avn[mt], [&](int r, int c) { return B2[r * LV + c]; }, vm0 + 16 * mt, vn0);
+    tile_init<NT8>(adv[mt], [&](int r, int c) { return B3[r * LV + c]; }, vm0 + 16 * mt, vn0);
+  }
   issue(0, 0);
   for (int sl = 0; sl < NSL; ++sl) {
     const int buf = sl & 1;
@@ -629,9 +696,9 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
     const float* h = Hs(buf);
     const float* ds = Ds(buf);
     const int d0 = sl * SR;
-    tile_mma<NT8>(avn, [&](int i, int kk, int) { return -B0[i * LK + d0 + kk]; },
+    tile_mma<2, NT8>(avn, [&](int i, int kk, int) { return -B0[i * LK + d0 + kk]; },
                   [&](int kk, int vv, int) { return h[kk * LV + vv]; }, vm0, vn0, 0, SR);
-    tile_mma<NT8>(adv, [&](int i, int kk, int) { return B1[i * LK + d0 + kk]; },
+    tile_mma<2, NT8>(adv, [&](int i, int kk, int) { return B1[i * LK + d0 + kk]; },
                   [&](int kk, int vv, int) { return ds[kk * LV + vv]; }, vm0, vn0, 0, SR);
     {  // DH[:, slice]: 8 tiles of 16 x 8
       float a1[1][4] = {{0.f, 0.f, 0.f, 0.f}};
@@ -653,10 +720,15 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
     }
     __syncthreads();  // the slice buffers may be refilled
   }
-  tile_epi<NT8>(avn, [&](int r, int c, float x0, float x1) { *reinterpret_cast<float2*>(B2 + r * LV + c) = make_float2(x0, x1); },
-                vm0, vn0);
-  tile_epi<NT8>(adv, [&](int r, int c, float x0, float x1) { *reinterpret_cast<float2*>(B3 + r * LV + c) = make_float2(x0, x1); },
-                vm0, vn0);
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    tile_epi<NT8>(avn[mt], [&](int r, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(B2 + r * LV + c) = make_float2(x0, x1);
+    }, vm0 + 16 * mt, vn0);
+    tile_epi<NT8>(adv[mt], [&](int r, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(B3 + r * LV + c) = make_float2(x0, x1);
+    }, vm0 + 16 * mt, vn0);
+  }
   // 3. pass 2: dW = -dv_new S^T, dkr = v_new dS'^T
   issue(0, 0);
   for (int sl = 0; sl < NSL; ++sl) {
@@ -688,22 +760,22 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
   }
   // 4. v (B0), T (B1); dAqk = tril(do v_new^T), dAv = tril(dv_new v^T), dv = A^T dv_new
   load_rows<IO, V>(B0, static_cast<const IO*>(p.v), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
-  copy_in<C, LC>(B1, slot + S::T, C);
+  copy_in<C, LC>(B1, slot + S::T);
   if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
   __syncthreads();
-  const auto lower = [](int m0, int n0) { return n0 <= m0; };
+  const auto lower = [](int m0, int n0) { return n0 <= m0 + 16; };
   const auto kv = [](int, int) { return make_int2(0, V); };
-  cta_gemm<C, C, 2>([&](int i, int vv, int) { return B4[i * LV + vv]; }, [&](int vv, int j, int) { return B2[j * LV + vv]; },
+  cta_gemm<C, C, 2, 2>([&](int i, int vv, int) { return B4[i * LV + vv]; }, [&](int vv, int j, int) { return B2[j * LV + vv]; },
                     lower, kv, zero, [&](int r, int c, float x0, float x1) {
                       *reinterpret_cast<float2*>(slot + S::DAQK + r * C + c) =
                           make_float2(c <= r ? x0 : 0.f, c + 1 <= r ? x1 : 0.f);
                     });
-  cta_gemm<C, C, 2>([&](int i, int vv, int) { return B3[i * LV + vv]; }, [&](int vv, int j, int) { return B0[j * LV + vv]; },
+  cta_gemm<C, C, 2, 2>([&](int i, int vv, int) { return B3[i * LV + vv]; }, [&](int vv, int j, int) { return B0[j * LV + vv]; },
                     lower, kv, zero, [&](int r, int c, float x0, float x1) {
                       *reinterpret_cast<float2*>(slot + S::DAV + r * C + c) =
                           make_float2(c <= r ? x0 : 0.f, c + 1 <= r ? x1 : 0.f);
                     });
-  cta_gemm<C, V, 4>([&](int j, int i, int) { return B1[i * LC + j] * bs[j]; }, [&](int i, int vv, int) { return B3[i * LV + vv]; },
+  cta_gemm<C, V, 4, 2>([&](int j, int i, int) { return B1[i * LC + j] * bs[j]; }, [&](int i, int vv, int) { return B3[i * LV + vv]; },
                     all, [](int m0, int) { return make_int2(m0, C); }, zero, [&](int r, int c, float x0, float x1) {
                       if (r < rows)
                         *reinterpret_cast<float2*>(p.dv + (static_cast<size_t>(tok0 + r) * p.HV + hv) * V + c) =
@@ -732,26 +804,26 @@ __global__ void __launch_bounds__(NT, 1) grad_cc_kernel(Params p) {
   if (!find_chunk(p, f, seq, m, tok0, rows)) return;
   const int hk = hv / (p.HV / p.H);
   float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
-  const auto lower = [](int m0, int n0) { return n0 <= m0; };
+  const auto lower = [](int m0, int n0) { return n0 <= m0 + 16; };
 
   load_rows<float, K>(B0, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K);
-  copy_in<K, LK>(B1, slot + S::DW, C);
-  copy_in<C, LC>(XT, slot + S::T, C);
-  copy_in<C, LC>(XA, slot + S::DAV, C);
-  copy_in<C, LC>(XK, slot + S::KK, C);
+  load_rows<IO, K>(B1, static_cast<const IO*>(p.k), tok0, rows, static_cast<size_t>(p.H) * K, static_cast<size_t>(hk) * K);
+  copy_in<C, LC>(XT, slot + S::T);
+  copy_in<C, LC>(XA, slot + S::DAV);
+  copy_in<C, LC>(XK, slot + S::KK);
   if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
   __syncthreads();
   cumsum_log2<K, LK>(B0);
   __syncthreads();
-  const IO* kp = static_cast<const IO*>(p.k);
   for (int idx = tid; idx < C * K; idx += NT) {  // kd = k e^{gc}
     const int i = idx / K, d = idx - i * K;
-    const float kk = i < rows ? load1(kp + static_cast<size_t>(tok0 + i) * p.H * K + static_cast<size_t>(hk) * K + d) : 0.f;
-    B0[i * LK + d] = kk * ex2(B0[i * LK + d]);
+    B0[i * LK + d] = B1[i * LK + d] * ex2(B0[i * LK + d]);
   }
   __syncthreads();
+  copy_in<K, LK>(B1, slot + S::DW);
+  __syncthreads();
   // dA = dW kd^T + dAv (lower, diagonal included), in place of dAv
-  cta_gemm<C, C, 2>([&](int i, int d, int) { return B1[i * LK + d]; }, [&](int d, int j, int) { return B0[j * LK + d]; }, lower,
+  cta_gemm<C, C, 2, 2>([&](int i, int d, int) { return B1[i * LK + d]; }, [&](int d, int j, int) { return B0[j * LK + d]; }, lower,
                     [](int, int) { return make_int2(0, K); }, [&](int r, int c) { return XA[r * LC + c]; },
                     [&](int r, int c, float x0, float x1) {
                       XA[r * LC + c] = c <= r ? x0 : 0.f;
@@ -764,7 +836,7 @@ __global__ void __launch_bounds__(NT, 1) grad_cc_kernel(Params p) {
     dbc[tid] = s;
   }
   // Y = dA A^T (lower tiles): Y_aj = sum_{b <= j} dA_ab T_jb beta_b
-  cta_gemm<C, C, 2>([&](int a, int b, int) { return XA[a * LC + b]; }, [&](int b, int j, int) { return XT[j * LC + b] * bs[b]; },
+  cta_gemm<C, C, 2, 2>([&](int a, int b, int) { return XA[a * LC + b]; }, [&](int b, int j, int) { return XT[j * LC + b] * bs[b]; },
                     lower, [](int, int n0) { return make_int2(0, n0 + 16); }, [](int, int) { return 0.f; },
                     [&](int r, int c, float x0, float x1) {
                       XY[r * LC + c] = x0;
@@ -772,7 +844,7 @@ __global__ void __launch_bounds__(NT, 1) grad_cc_kernel(Params p) {
                     });
   __syncthreads();
   // dM = -strict_tril(T^T Y): dM_ij = -sum_{a >= i} T_ai Y_aj
-  cta_gemm<C, C, 2>([&](int i, int a, int) { return XT[a * LC + i]; }, [&](int a, int j, int) { return XY[a * LC + j]; }, lower,
+  cta_gemm<C, C, 2, 2>([&](int i, int a, int) { return XT[a * LC + i]; }, [&](int a, int j, int) { return XY[a * LC + j]; }, lower,
                     [](int m0, int) { return make_int2(m0, C); }, [](int, int) { return 0.f; },
                     [&](int r, int c, float x0, float x1) {
                       XM[r * LC + c] = c < r ? -x0 : 0.f;
@@ -821,9 +893,9 @@ __global__ void __launch_bounds__(NT, 1) grad_k_kernel(Params p) {
     const int r = idx / (DK / 4), c4 = (idx - r * (DK / 4)) * 4;
     *reinterpret_cast<float4*>(DWs + r * LD + c4) = load4(slot + S::DW + static_cast<size_t>(r) * K + d0 + c4);
   }
-  copy_in<C, LC>(XT, slot + S::T, C);
-  copy_in<C, LC>(XQ, slot + S::DAQK, C);
-  copy_in<C, LC>(XM, slot + S::DMB, C);
+  copy_in<C, LC>(XT, slot + S::T);
+  copy_in<C, LC>(XQ, slot + S::DAQK);
+  copy_in<C, LC>(XM, slot + S::DMB);
   if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
   __syncthreads();
   // tables: Lk, Lq from copies of the raw rows (the raw rows stay for the final pass)
@@ -963,7 +1035,7 @@ cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
   if (chunks > 0) {
     prep_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_prep, st>>>(p);
   }
-  chain_kernel<K, V><<<dim3(V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
+  chain_kernel<K, V><<<dim3(V < VS ? 1 : V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
   if (chunks > 0) {
     grad_v_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gv, st>>>(p);
     grad_cc_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gc, st>>>(p);
