@@ -41,9 +41,13 @@ KERNEL_SOURCES = ["kimi_delta_attention_gb300/csrc/kda_chunk_tc.cu",
                   "kimi_delta_attention_gb300/csrc/kda_common.cuh"]
 
 
-def kernel_source_hash() -> str:
+# sources that only some entries depend on (the chunk-form backward's five kernels)
+KERNEL_EXTRA_SOURCES = {"kda_backward_chunk": ["kimi_delta_attention_gb300/csrc/kda_backward_chunk.cu"]}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES + KERNEL_EXTRA_SOURCES.get(kernel, []):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -152,7 +156,7 @@ def load_traffic(kernel_name: str, workload: str):
     except (OSError, ValueError):
         return None
     e = d.get(f"{kernel_name}@{workload}")
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel_name):
         return None
     return e.get("bytes_per_launch")
 
@@ -600,19 +604,28 @@ def run_twopass(args):
     return 0
 
 
-BACKWARD_METRIC = ("KDA backward (gradients of q, k, v, g, beta and the initial state through the token "
-                   "recurrence, fp32) tokens/s on 1 GB300 (T=4096, H=HV=32, K=V=128); % of fp32 CUDA-core peak")
-# fp32 CUDA-core peak the backward is reported against: 152 SMs x 128 fp32 lanes x 2 flop
-# (one FMA) x 2.07 GHz, the maximum SM clock
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+BACKWARD_METRIC = ("KDA backward (gradients of q, k, v, g, beta and the initial state, chunk form with "
+                   "split-TF32 tensor-core products) tokens/s on 1 GB300 (T=4096, H=HV=32, K=V=128); "
+                   "% of the TF32 tensor peak")
+# nominal dense TF32 / bf16 tensor rates of the part (1.1 and 2.25 PFLOP/s): the TF32 peak
+# is the measured bf16 peak scaled by their ratio
+TF32_PER_BF16 = 1.1 / 2.25
+BACKWARD_LAUNCHES = 5  # prep, chain, value-side, C x C and key-side gradient kernels
+BACKWARD_KERNELS = "prep_kernel, chain_kernel, grad_v_kernel, grad_cc_kernel, grad_k_kernel"
 
 
-def backward_flops(tokens_heads: int, K: int, V: int) -> float:
-    """Arithmetic of the backward as the kernel evaluates it, per (token, value head): a
-    forward sweep and a recompute of each token state (decay, P^T k, rank-1 update: 5 K V
-    each) and the reverse step (P, u, dq, dS += q do^T, dS^T k, dk's two products, dP, dg,
-    the decayed dS: 18 K V)."""
-    return tokens_heads * 28.0 * K * V
+def backward_flops(tokens_heads: int, K: int, V: int, C: int = 64) -> float:
+    """Arithmetic of the chunk-form backward per (token, value head), every product counted
+    once (triangular ones in full), per chunk of C tokens:
+      prep      L and Aqk, W (2 C^2 K each), U, Aqk^T do (2 C^2 V each), Q (2 K^2 C),
+                R (2 K C V), B (4 K C V);
+      chains    the state and the state gradient (2 K^2 V each);
+      value     v_new, dv_new, do S^T, dW, dkr (2 C K V each), dAqk, dAv, dv (2 C^2 V each);
+      C x C     dA (2 C^2 K), dA A^T and T^T Y (2 C^3 each);
+      key       A^T dW, two row-side and two column-side decayed products (2 C^2 K each).
+    The split-TF32 evaluation issues three tensor products for each of these."""
+    per_chunk = 18 * C * C * K + 10 * C * C * V + 2 * K * K * C + 16 * K * C * V + 4 * K * K * V + 4 * C ** 3
+    return tokens_heads / C * per_chunk
 
 
 def run_backward(args):
@@ -659,19 +672,22 @@ def run_backward(args):
     tokens = B * T
     flops = backward_flops(tokens * HV, K, V)
     achieved = flops / (ms * 1e-3) / 1e12
+    _, bf16_tf, peak_src = load_peaks()
+    tf32_peak = bf16_tf * TF32_PER_BF16
     line = {
         "impl": "kda_gb300", "metric": BACKWARD_METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s",
         "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "backward_bf16_T4096_H32_K128", "B": B, "T": T, "H": H, "HV": HV, "K": K, "V": V,
                    "io": "bf16 q/k/v/d_out, fp32 g/beta/d_final_state; fp32 gradients",
+                   "products": "TF32 tensor cores, each operand split into high and low parts (3 products)",
                    "l2": "flushed between timed steps"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_PEAK_TFLOPS, "kernel": "recurrent_bwd_kernel",
-                     "traffic": load_traffic("recurrent_bwd_kernel", "backward_bf16_T4096_H32_K128"),
-                     "flops_per_launch": flops,
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"},
-        "clocks": sampler.summary(), "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tf32_peak, "kernel": f"the whole step ({BACKWARD_KERNELS})",
+                     "traffic": load_traffic("kda_backward_chunk", "backward_bf16_T4096_H32_K128"),
+                     "flops_per_step": flops, "launches_per_step": BACKWARD_LAUNCHES,
+                     "peak_source": (f"{peak_src} bf16 peak x {TF32_PER_BF16:.3f} (nominal dense TF32 / bf16)")},
+        "clocks": sampler.summary(), "gpu_launches": args.steps * BACKWARD_LAUNCHES,
         "device_status": kda.kda_read_device_status(ws),
     }
     print(json.dumps(line), flush=True)
