@@ -28,8 +28,8 @@ size_t backward_chunk_slot_floats(int K, int V);
 cudaError_t launch_backward_chunk(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                   const float* s0, const int32_t* cu, const void* d_out, const float* d_fin, float* dq,
                                   float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* ws,
-                                  uint32_t* status, float scale, int T, int H, int HV, int K, int V, int num_seqs,
-                                  bool bf16, cudaStream_t stream);
+                                  uint32_t* status, unsigned long long wait_ns, float scale, int T, int H, int HV,
+                                  int K, int V, int num_seqs, bool bf16, cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                           float* state, void* out, float scale, int B, int T, int H, int HV, int K, int V,
                           bool bf16, cudaStream_t stream);
@@ -408,7 +408,8 @@ kda_status kda_backward(const kda_shape* s, const void* q, const void* k, const 
   if (!backward_recurrent()) {
     const cudaError_t e = kda::launch_backward_chunk(
         q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta, d_initial_state,
-        scratch, status, scale, s->T, s->H, s->HV, s->K, s->V, static_cast<int>(ns), s->io_dtype == KDA_BF16, cs);
+        scratch, status, wait_limit_ns(), scale, s->T, s->H, s->HV, s->K, s->V, static_cast<int>(ns),
+        s->io_dtype == KDA_BF16, cs);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
   const cudaError_t e = kda::launch_backward(

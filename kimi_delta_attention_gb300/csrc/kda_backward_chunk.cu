@@ -71,6 +71,7 @@ struct Params {
   float* ws;           // slots, one per (flat chunk, value head)
   uint32_t* status;
   size_t slot_floats;
+  unsigned long long wait_ns;  // limit of a bounded wait (tcgen05 chains)
   float scale;
   int T, H, HV, num_seqs;
   int nc;              // chunks per sequence (fixed length)
@@ -86,6 +87,14 @@ struct Slot {
                           DAQK = DKR + C * K, DAV = DAQK + C * C, DMB = DAV + C * C, DGL = DMB + C * C,
                           FLOATS = DGL + K;
 };
+
+// Element (key row d, value column v) of the K x V regions RH and BD: 64-column slices
+// stored one after the other (each K x 64, rows of 64), so that a chain CTA's slice is
+// one contiguous block.
+template <int K>
+__device__ __forceinline__ size_t kv_off(int d, int v) {
+  return static_cast<size_t>(v >> 6) * (K * 64) + static_cast<size_t>(d) * 64 + (v & 63);
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -328,6 +337,9 @@ struct PrepSmem {
   static_assert(8 * K <= C * LC, "block references fit in the T tile");
 };
 __device__ __forceinline__ int pair_index(int bi, int bj) { return bi * (bi + 1) / 2 + bj; }
+// K = 128: the slot's Q region holds Q as two bf16 tiles (high part, then the low part
+// at kQLow bytes), K-major with the 128-byte swizzle (64-column blocks of 128 rows)
+constexpr uint32_t kQLow = 32768;
 
 // q, k, g rows of a chunk -> gc (log2 units, in place of g), the block references
 // (refs: s_b [4][N], e_b [4][N]) and the tables Lk = k e^{gc - s_b}, Lq = scale q e^{gc - s_b}
@@ -472,8 +484,18 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
   const auto kr_all = [](int, int) { return make_int2(0, C); };
   cta_gemm<K, K, 4, 2>(fa_krT, [&](int i, int e, int) { return B2[i * LK + e]; }, all, kr_all, zero,
                     [&](int r, int c, float x0, float x1) {
-                      *reinterpret_cast<float2*>(slot + S::Q + static_cast<size_t>(r) * K + c) =
-                          make_float2((r == c ? EG[r] : 0.f) - x0, (r == c + 1 ? EG[r] : 0.f) - x1);
+                      const float y0 = (r == c ? EG[r] : 0.f) - x0, y1 = (r == c + 1 ? EG[r] : 0.f) - x1;
+                      if (K == 128) {  // bf16 high / low parts, K-major 128-B swizzled (the tcgen05 chain's A)
+                        uint8_t* qb = reinterpret_cast<uint8_t*>(slot + S::Q);
+                        const uint32_t o = sw128_offset(r, c, K);
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+                        const __nv_bfloat162 l =
+                            __floats2bfloat162_rn(y0 - __low2float(h), y1 - __high2float(h));
+                        *reinterpret_cast<__nv_bfloat162*>(qb + o) = h;
+                        *reinterpret_cast<__nv_bfloat162*>(qb + kQLow + o) = l;
+                      } else {
+                        *reinterpret_cast<float2*>(slot + S::Q + static_cast<size_t>(r) * K + c) = make_float2(y0, y1);
+                      }
                     });
   copy_out<K, LK>(slot + S::W, B2);
   __syncthreads();
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
   __syncthreads();
   cta_gemm<K, V, 4, 2>(fa_krT, [&](int i, int vv, int) { return B4[i * LV + vv]; }, all, kr_all, zero,
                     [&](int r, int c, float x0, float x1) {
-                      *reinterpret_cast<float2*>(slot + S::RH + static_cast<size_t>(r) * V + c) = make_float2(x0, x1);
+                      *reinterpret_cast<float2*>(slot + S::RH + kv_off<K>(r, c)) = make_float2(x0, x1);
                     });
   copy_out<V, LV>(slot + S::U, B4);
   __syncthreads();
@@ -506,7 +528,7 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
       [&](int d, int kk, int) { return kk < C ? B1[kk * LK + d] * F[(kk >> 4) * K + d] : -B2[(kk - C) * LK + d]; },
       [&](int kk, int vv, int) { return kk < C ? B0[kk * LV + vv] : B4[(kk - C) * LV + vv]; }, all,
       [](int, int) { return make_int2(0, 2 * C); }, zero, [&](int r, int c, float x0, float x1) {
-        *reinterpret_cast<float2*>(slot + S::BD + static_cast<size_t>(r) * V + c) = make_float2(x0, x1);
+        *reinterpret_cast<float2*>(slot + S::BD + kv_off<K>(r, c)) = make_float2(x0, x1);
       });
   copy_out<V, LV>(slot + S::E, B4);
   copy_out<C, LC>(slot + S::T, X3);
@@ -575,7 +597,7 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(Params p) {
     for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        ad[nt][h] = *reinterpret_cast<const float2*>(s + add + static_cast<size_t>(m0 + g + 8 * h) * V + v0 + n0 + 8 * nt + 2 * t);
+        ad[nt][h] = *reinterpret_cast<const float2*>(s + add + kv_off<K>(m0 + g + 8 * h, v0 + n0 + 8 * nt + 2 * t));
     const float* Q = Qb(step & 1);
     const float* X = Xb(cur);
     float acc[NT8][4];
@@ -597,7 +619,7 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(Params p) {
     // the state entering the chunk (forward) / the gradient leaving it (reverse)
     for (int idx = tid; idx < K * (VC / 4); idx += NT) {
       const int r = idx / (VC / 4), c4 = (idx - r * (VC / 4)) * 4;
-      *reinterpret_cast<float4*>(s + add + static_cast<size_t>(r) * V + v0 + c4) =
+      *reinterpret_cast<float4*>(s + add + kv_off<K>(r, v0 + c4)) =
           *reinterpret_cast<const float4*>(X + r * LS + c4);
     }
     float* Xn = Xb(cur ^ 1);
@@ -612,6 +634,182 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(Params p) {
       const int r = idx / VC, c = idx - r * VC;
       p.ds0[state0 + static_cast<size_t>(r) * V + c] = X[r * LS + c];
     }
+  }
+}
+
+// ------------------------------------------------------ chains (tcgen05) ----
+// K = 128.  The CTA's 64 value columns of X are the fp32 accumulator of a tcgen05 product
+// in TMEM (lane = key row, 64 columns).  Per chunk: D = addend (tcgen05.st) +
+// Q X (forward) or Q^T X (reverse) as the three bf16 products Qh Xh + Qh Xl + Ql Xh of
+// the high/low splits (M = 128, N = 64, K = 128).  Q's splits arrive by bulk copy two
+// chunks ahead; the same K-major tiles are Q^T as MN-major A operands.  X's splits are
+// written back to shared memory (MN-major B, 128-byte swizzle) after each product.
+namespace tcc {
+constexpr uint32_t QBUF = 65536;                       // Q high + low
+constexpr uint32_t ABUF = 32768;                       // the addend slice, 128 x 64 fp32
+constexpr uint32_t BUF = QBUF + ABUF;
+constexpr uint32_t XH = 2 * BUF, XL = XH + 16384, BAR = XL + 16384, SMEM = BAR + 64 + 1024;
+}  // namespace tcc
+template <int V>
+__global__ void __launch_bounds__(NT, 1) chain_tc_kernel(Params p) {
+  constexpr int K = 128, VC = 64;
+  using S = Slot<K, V>;
+  extern __shared__ __align__(16) uint8_t smraw[];
+  uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + tcc::BAR);  // [0], [1]: buffer full; [2]: products done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + tcc::BAR + 32);
+  volatile uint32_t* failed = reinterpret_cast<volatile uint32_t*>(sm + tcc::BAR + 40);
+  const int v0 = blockIdx.x * VC, hv = blockIdx.y, seq = blockIdx.z >> 1, dir = blockIdx.z & 1, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  int f0, nch;
+  if (!seq_chunks(p, seq, f0, nch)) return;
+  const int row = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);  // this thread's key row and 32 columns
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
+    *failed = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot, tm_row = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + c0;
+  const uint32_t sb = smem_u32(sm);
+  const size_t add = (dir == 0 ? S::RH : S::BD) + kv_off<K>(0, v0);  // this CTA's 128 x 64 slice
+  auto slot = [&](int step) {
+    return p.ws + (static_cast<size_t>(f0 + (dir == 0 ? step : nch - 1 - step)) * p.HV + hv) * p.slot_floats;
+  };
+  auto issue = [&](int step) {  // thread 0: Q and the addend slice of this step's chunk into buffer step & 1
+    const float* s = slot(step);
+    const uint8_t* qs = reinterpret_cast<const uint8_t*>(s + S::Q);
+    const uint8_t* as = reinterpret_cast<const uint8_t*>(s + add);
+    uint8_t* dst = sm + (step & 1) * tcc::BUF;
+    mbar_arrive_expect_tx(&bars[step & 1], tcc::BUF);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bulk_load(dst + q * 16384, qs + q * 16384, 16384, &bars[step & 1]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) bulk_load(dst + tcc::QBUF + q * 16384, as + q * 16384, 16384, &bars[step & 1]);
+  };
+  auto put_x = [&](const float (&x)[32]) {  // X's splits for the next product (key row `row`)
+#pragma unroll
+    for (int j8 = 0; j8 < 4; ++j8) {
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(x[8 * j8 + 2 * e], x[8 * j8 + 2 * e + 1]);
+        const __nv_bfloat162 lb =
+            __floats2bfloat162_rn(x[8 * j8 + 2 * e] - __low2float(hb), x[8 * j8 + 2 * e + 1] - __high2float(hb));
+        h[e] = *reinterpret_cast<const uint32_t*>(&hb);
+        l[e] = *reinterpret_cast<const uint32_t*>(&lb);
+      }
+      const uint32_t off = (row >> 3) * 1024u + (row & 7) * 128u + ((((c0 >> 3) + j8) ^ (row & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + tcc::XH + off) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(sm + tcc::XL + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+  };
+  float x[32];
+  {
+    const float* x0 = dir == 0 ? p.s0 : p.d_fin;
+    const float* xp = x0 ? x0 + (static_cast<size_t>(seq) * p.HV + hv) * K * V + static_cast<size_t>(row) * V + v0 + c0 : nullptr;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 v4 = xp ? *reinterpret_cast<const float4*>(xp + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[4 * j] = v4.x;
+      x[4 * j + 1] = v4.y;
+      x[4 * j + 2] = v4.z;
+      x[4 * j + 3] = v4.w;
+    }
+  }
+  put_x(x);
+  int issued = nch < 2 ? nch : 2;  // steps [0, issued) have had their loads issued (thread 0's count)
+  bool pending = false;            // products committed and not yet seen complete (thread 0)
+  if (tid == 0)
+    for (int s2 = 0; s2 < issued; ++s2) issue(s2);
+  // descriptors of the k = 0 step (16-byte units added per step): A = Q's splits (K-major,
+  // or MN-major for Q^T), B = X's splits (MN-major)
+  const uint32_t idesc = idesc_f16kind(128, 64) | IDESC_B_MN_MAJOR | (dir ? IDESC_A_MN_MAJOR : 0u);
+  const uint64_t dq0 = dir == 0 ? sdesc_sw128(sb) : sdesc(sb, 16384, 1024, 2);
+  const uint64_t dxh = sdesc(sb + tcc::XH, 16384, 1024, 2), dxl = sdesc(sb + tcc::XL, 16384, 1024, 2);
+  int step = 0;
+  for (; step < nch; ++step) {
+    const int b = step & 1;
+    const uint8_t* buf = sm + b * tcc::BUF;
+    // this chunk's Q and addend have landed (every thread reads the addend)
+    if (!mbar_wait(&bars[b], (step >> 1) & 1, p.wait_ns)) {
+      atomicOr(p.status, kStatusTimeout);
+      *failed = 1u;
+    }
+    // the addend into D; the state entering the chunk (forward) / the gradient leaving
+    // it (reverse) into the addend's place in the slot (its bulk read has completed)
+    float a[32];
+    const float* as = reinterpret_cast<const float*>(buf + tcc::QBUF) + row * 64 + c0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 v4 = *reinterpret_cast<const float4*>(as + 4 * j);
+      a[4 * j] = v4.x;
+      a[4 * j + 1] = v4.y;
+      a[4 * j + 2] = v4.z;
+      a[4 * j + 3] = v4.w;
+    }
+    tmem_st32(tm_row, a);
+    float* ap = slot(step) + add + row * 64 + c0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(ap + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    tmem_st_wait();
+    fence_proxy_async_smem();  // X's splits (generic stores) before the products read them
+    tc_fence_before();
+    __syncthreads();
+    if (*failed) break;
+    if (tid == 0) {
+      tc_fence_after();
+      const uint64_t qh = dq0 + ((b * tcc::BUF) >> 4), ql = qh + (kQLow >> 4);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ao = dir == 0 ? ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4 : (ks * 2048) >> 4;
+        const uint32_t bo = (ks * 2048) >> 4;
+        umma_f16(tmem, qh + ao, dxh + bo, idesc, 1u);
+        umma_f16(tmem, qh + ao, dxl + bo, idesc, 1u);
+        umma_f16(tmem, ql + ao, dxh + bo, idesc, 1u);
+      }
+      umma_commit(&bars[2]);
+      pending = true;
+    }
+    if (mbar_wait(&bars[2], step & 1, p.wait_ns)) {
+      pending = false;
+    } else {
+      atomicOr(p.status, kStatusTimeout);
+      *failed = 1u;
+    }
+    tc_fence_after();
+    __syncthreads();  // every thread has seen the products complete (or the failure) and read its addend
+    if (*failed) break;
+    if (tid == 0 && step + 2 < nch) {
+      issue(step + 2);
+      issued = step + 3;
+    }
+    tmem_ld32(tm_row, x);
+    tmem_ld_wait();
+    put_x(x);
+  }
+  if (tid == 0 && step < nch) {  // after a failure: the loads issued for later steps, and the products,
+                                 // complete (bounded waits) before the CTA releases its memory
+    for (int s2 = step; s2 < issued; ++s2) mbar_wait(&bars[s2 & 1], (s2 >> 1) & 1, p.wait_ns);
+    if (pending) mbar_wait(&bars[2], step & 1, p.wait_ns);
+  }
+  if (dir == 1 && p.ds0 && !*failed) {
+    float* dp = p.ds0 + (static_cast<size_t>(seq) * p.HV + hv) * K * V + static_cast<size_t>(row) * V + v0 + c0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(dp + 4 * j) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
   }
 }
 
@@ -667,7 +865,7 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
   auto issue = [&](int sl, int buf) {
     for (int idx = tid; idx < SR * (V / 4); idx += NT) {
       const int r = idx / (V / 4), c4 = (idx - r * (V / 4)) * 4;
-      const size_t o = static_cast<size_t>(sl * SR + r) * V + c4;
+      const size_t o = kv_off<K>(sl * SR + r, c4);
       cp_async16(Hs(buf) + r * LV + c4, hsrc + o);
       cp_async16(Ds(buf) + r * LV + c4, dsrc + o);
     }
@@ -1023,11 +1221,14 @@ __global__ void __launch_bounds__(NT, 1) grad_k_kernel(Params p) {
 
 template <typename IO, int K, int V>
 cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
-  const size_t s_prep = PrepSmem<K, V>::FLOATS * 4, s_chain = ChainSmem<K>::FLOATS * 4, s_gv = GvSmem<K, V>::FLOATS * 4,
+  const size_t s_prep = PrepSmem<K, V>::FLOATS * 4, s_chain = K == 128 ? tcc::SMEM : ChainSmem<K>::FLOATS * 4,
+               s_gv = GvSmem<K, V>::FLOATS * 4,
                s_gc = GcSmem<K>::FLOATS * 4, s_gk = GkSmem::FLOATS * 4;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(prep_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_prep)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(chain_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_chain)) != cudaSuccess ||
+      (e = K == 128 ? cudaFuncSetAttribute(chain_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_chain)
+                    : cudaFuncSetAttribute(chain_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_chain)) !=
+          cudaSuccess ||
       (e = cudaFuncSetAttribute(grad_v_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gv)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(grad_cc_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gc)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(grad_k_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gk)) != cudaSuccess)
@@ -1035,7 +1236,10 @@ cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
   if (chunks > 0) {
     prep_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_prep, st>>>(p);
   }
-  chain_kernel<K, V><<<dim3(V < VS ? 1 : V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
+  if (K == 128)
+    chain_tc_kernel<V><<<dim3(V < VS ? 1 : V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
+  else
+    chain_kernel<K, V><<<dim3(V < VS ? 1 : V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
   if (chunks > 0) {
     grad_v_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gv, st>>>(p);
     grad_cc_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gc, st>>>(p);
@@ -1063,12 +1267,12 @@ size_t backward_chunk_slot_floats(int K, int V) {
 cudaError_t launch_backward_chunk(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                   const float* s0, const int32_t* cu, const void* d_out, const float* d_fin, float* dq,
                                   float* dk, float* dv, float* dg, float* dbeta, float* ds0, float* ws,
-                                  uint32_t* status, float scale, int T, int H, int HV, int K, int V, int num_seqs,
-                                  bool bf16, cudaStream_t stream) {
+                                  uint32_t* status, unsigned long long wait_ns, float scale, int T, int H, int HV,
+                                  int K, int V, int num_seqs, bool bf16, cudaStream_t stream) {
   const int nc = (T + cbwd::C - 1) / cbwd::C;
   const int chunks = cu ? nc + num_seqs : nc * num_seqs;
-  cbwd::Params p{q, k, v, g, beta, s0, cu, d_out, d_fin, dq, dk, dv, dg, dbeta, ds0, ws, status,
-                 backward_chunk_slot_floats(K, V), scale, T, H, HV, num_seqs, nc};
+  cbwd::Params p{q,  k,  v,  g,     beta,   s0,  cu, d_out, d_fin, dq, dk, dv, dg, dbeta, ds0, ws, status,
+                 backward_chunk_slot_floats(K, V), wait_ns, scale, T, H, HV, num_seqs, nc};
   if (bf16) {
     if (K == 128 && V == 128) return cbwd::launch_kv<__nv_bfloat16, 128, 128>(p, chunks, stream);
     if (K == 128 && V == 64) return cbwd::launch_kv<__nv_bfloat16, 128, 64>(p, chunks, stream);

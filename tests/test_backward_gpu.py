@@ -140,3 +140,24 @@ def test_backward_strong_decay_long():
     do, dfin = _grads_in(x, 8)
     got, ref = _run(x, do, dfin)
     _assert_grads(got, ref, "strong decay, 700 tokens")
+
+
+def test_backward_headline_size_sampled_heads():
+    """The headline shape (B=1, T=4096, H=HV=32, K=V=128, bf16) in one call, in the launch
+    configuration the benchmark times; three value heads compared with the oracle run on
+    those heads alone (G = 1: a head's gradients depend on that head only)."""
+    x = W.make_inputs(1, 4096, 32, 32, 128, 128, "bf16", seed=21, init_state=True)
+    do, dfin = _grads_in(x, 9)
+    d = x.to("cuda")
+    got = kda.kda_backward(d.q, d.k, d.v, d.g, d.beta, do.to("cuda"), d.scale, initial_state=d.initial_state,
+                           d_final_state=dfin.to("cuda"))
+    torch.cuda.synchronize()
+    got = [t.cpu().numpy() for t in got]
+    for h in (0, 17, 31):
+        sl = slice(h, h + 1)
+        ref = oracle.backward(np32(x.q[:, :, sl]), np32(x.k[:, :, sl]), np32(x.v[:, :, sl]), np32(x.g[:, :, sl]),
+                              np32(x.beta[:, :, sl]), x.scale, np32(do[:, :, sl]), d_final_state=np32(dfin[:, sl]),
+                              initial_state=np32(x.initial_state[:, sl]))
+        mine = [got[0][:, :, sl], got[1][:, :, sl], got[2][:, :, sl], got[3][:, :, sl], got[4][:, :, sl],
+                got[5][:, sl]]
+        _assert_grads(mine, ref, f"headline head {h}")
