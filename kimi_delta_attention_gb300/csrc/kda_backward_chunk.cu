@@ -234,46 +234,82 @@ __device__ __forceinline__ void cumsum_log2(float* x) {
 // product.  The fragments of a k-step are loaded first, then the products run in passes
 // over all accumulators, so that no product waits on the one before it.
 template <int MT, int NT8, class FA, class FB>
-__device__ __forceinline__ void tile_mma(float (&acc)[MT][NT8][4], const FA& fa, const FB& fb, int m0, int n0, int kb,
-                                         int ke) {
+__device__ __forceinline__ void kstep_mma(float (&a0)[MT][NT8][4], float (&a1)[MT][NT8][4], float (&a2)[MT][NT8][4],
+                                          const FA& fa, const FB& fb, int m0, int n0, int k) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 2
-  for (int k = kb; k < ke; k += 8) {
-    uint32_t ah[MT][4], al[MT][4], bh[NT8][2], bl[NT8][2];
+  uint32_t ah[MT][4], al[MT][4], bh[NT8][2], bl[NT8][2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int m = m0 + 16 * mt + g;
-      const float av[4] = {fa(m, k + t, n0), fa(m + 8, k + t, n0), fa(m, k + t + 4, n0), fa(m + 8, k + t + 4, n0)};
+  for (int mt = 0; mt < MT; ++mt) {
+    const int m = m0 + 16 * mt + g;
+    const float av[4] = {fa(m, k + t, n0), fa(m + 8, k + t, n0), fa(m, k + t + 4, n0), fa(m + 8, k + t + 4, n0)};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ah[mt][e] = to_tf32(av[e]);
-        if (kSplit) al[mt][e] = to_tf32(av[e] - __uint_as_float(ah[mt][e]));
-      }
+    for (int e = 0; e < 4; ++e) {
+      ah[mt][e] = to_tf32(av[e]);
+      if (kSplit) al[mt][e] = to_tf32(av[e] - __uint_as_float(ah[mt][e]));
     }
+  }
 #pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) {
-      const int n = n0 + 8 * nt + g;
-      const float bv[2] = {fb(k + t, n, m0), fb(k + t + 4, n, m0)};
+  for (int nt = 0; nt < NT8; ++nt) {
+    const int n = n0 + 8 * nt + g;
+    const float bv[2] = {fb(k + t, n, m0), fb(k + t + 4, n, m0)};
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        bh[nt][e] = to_tf32(bv[e]);
-        if (kSplit) bl[nt][e] = to_tf32(bv[e] - __uint_as_float(bh[nt][e]));
-      }
+    for (int e = 0; e < 2; ++e) {
+      bh[nt][e] = to_tf32(bv[e]);
+      if (kSplit) bl[nt][e] = to_tf32(bv[e] - __uint_as_float(bh[nt][e]));
     }
-    if (kSplit) {
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(acc[mt][nt], al[mt], bh[nt][0], bh[nt][1]);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(acc[mt][nt], ah[mt], bl[nt][0], bl[nt][1]);
-    }
+  }
+  if (kSplit) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(acc[mt][nt], ah[mt], bh[nt][0], bh[nt][1]);
+      for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(a1[mt][nt], al[mt], bh[nt][0], bh[nt][1]);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(a2[mt][nt], ah[mt], bl[nt][0], bl[nt][1]);
+  }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) mma_tf32_m16n8k8(a0[mt][nt], ah[mt], bh[nt][0], bh[nt][1]);
+}
+// One warp accumulates MT stacked 16 x (8 NT8) tiles at (m0 + 16 mt, n0) of
+// sum_k A(m, k) B(k, n) over k in [kb, ke) (multiples of 8).  fa(m, k, n0) and
+// fb(k, n, m0) return fp32 operands; each is split into TF32 high and low parts and the
+// three products lo*hi, hi*lo, hi*hi accumulate in fp32 (kSplit), else a single TF32
+// product.  The fragments of a k-step are loaded first, then the products run in passes
+// over all accumulators, so that no product waits on the one before it; tiles with at
+// most two accumulators spread the three products and alternate k-steps over six
+// partial sums (added at the end), which keeps as many products independent.
+template <int MT, int NT8, class FA, class FB>
+__device__ __forceinline__ void tile_mma(float (&acc)[MT][NT8][4], const FA& fa, const FB& fb, int m0, int n0, int kb,
+                                         int ke) {
+  if constexpr (MT * NT8 <= 2) {
+    float p[5][MT][NT8][4];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[i][mt][nt][e] = 0.f;
+    int k = kb;
+    for (; k + 16 <= ke; k += 16) {
+      kstep_mma<MT, NT8>(acc, p[0], p[1], fa, fb, m0, n0, k);
+      kstep_mma<MT, NT8>(p[2], p[3], p[4], fa, fb, m0, n0, k + 8);
+    }
+    if (k < ke) kstep_mma<MT, NT8>(acc, p[0], p[1], fa, fb, m0, n0, k);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          acc[mt][nt][e] += ((p[0][mt][nt][e] + p[1][mt][nt][e]) + (p[2][mt][nt][e] + p[3][mt][nt][e])) + p[4][mt][nt][e];
+  } else {
+#pragma unroll 2
+    for (int k = kb; k < ke; k += 8) kstep_mma<MT, NT8>(acc, acc, acc, fa, fb, m0, n0, k);
   }
 }
 // single 16-row tile
