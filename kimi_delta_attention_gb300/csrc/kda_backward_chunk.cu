@@ -370,7 +370,11 @@ struct PrepSmem {
   static constexpr int B0 = 0, B1 = B0 + C * LX, B2 = B1 + C * LX, B3 = B2 + C * LX, B4 = B3 + C * LX,
                        X1 = B4 + C * LX, X2 = X1 + C * LC, X3 = X2 + C * LC, F = X3 + C * LC, G = F + 4 * K,
                        D = G + 4 * K, EG = D + 10 * K, BS = EG + K, FLOATS = BS + C;
+  // + an mbarrier and the TMEM slot after the floats, and up to 1 KB to align the base
+  // (the 64 x (K + 4) buffers then start on 1 KB boundaries, as swizzled operands need)
+  static constexpr int BYTES = FLOATS * 4 + 16 + 1024;
   static_assert(8 * K <= C * LC, "block references fit in the T tile");
+  static_assert((C * LX * 4) % 1024 == 0 && (FLOATS * 4) % 8 == 0, "aligned buffers");
 };
 __device__ __forceinline__ int pair_index(int bi, int bj) { return bi * (bi + 1) / 2 + bj; }
 // K = 128: the slot's Q region holds Q as two bf16 tiles (high part, then the low part
@@ -445,19 +449,207 @@ __device__ __forceinline__ void tri_inverse(const float* KKd, const float* bs, f
   }
 }
 
+// In place: the fp32 64 x 128 tile `buf` (row stride LD) -> its bf16 high and low parts as
+// MN-major tcgen05 operands (K = the 64 rows, M or N = the 128 columns; 128-byte
+// swizzle, 64-column atoms 8 KB apart; the high part at byte 0, the low part at 16 KB).
+// val(i, c, x) gives the value of element (i, c) from its stored x.  Ends with a barrier
+// before the writes only: the caller orders the writes with later readers.
+template <int LD, class FV>
+__device__ __forceinline__ void split_mn(float* buf, const FV& val) {
+  float v[4][8];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = threadIdx.x + NT * u, i = c >> 4, n = (c & 15) << 3;
+    const float4 a = *reinterpret_cast<const float4*>(buf + i * LD + n);
+    const float4 b = *reinterpret_cast<const float4*>(buf + i * LD + n + 4);
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[u][e] = val(i, n + e, x[e]);
+  }
+  __syncthreads();
+  uint8_t* base = reinterpret_cast<uint8_t*>(buf);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = threadIdx.x + NT * u, i = c >> 4, n = (c & 15) << 3;
+    const uint32_t off = (n >> 6) * 8192u + (i >> 3) * 1024u + (i & 7) * 128u + ((((n & 63) >> 3) ^ (i & 7)) << 4);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 hb = __floats2bfloat162_rn(v[u][2 * e], v[u][2 * e + 1]);
+      const __nv_bfloat162 lb = __floats2bfloat162_rn(v[u][2 * e] - __low2float(hb), v[u][2 * e + 1] - __high2float(hb));
+      h[e] = *reinterpret_cast<const uint32_t*>(&hb);
+      l[e] = *reinterpret_cast<const uint32_t*>(&lb);
+    }
+    *reinterpret_cast<uint4*>(base + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(base + 16384 + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+// D[tmem] (=) A B for two split operands made by split_mn (A: M = 128 from its columns,
+// B: N = 128 from its columns, K = 64 rows): Ah Bh + Ah Bl + Al Bh, issued by one thread.
+__device__ __forceinline__ void issue_split_mn(uint32_t d_tmem, uint32_t a, uint32_t b) {
+  constexpr uint32_t idesc = idesc_f16kind(128, 128) | IDESC_A_MN_MAJOR | IDESC_B_MN_MAJOR;
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const uint64_t ah = sdesc(a + ks * 2048, 8192, 1024, 2), al = sdesc(a + 16384 + ks * 2048, 8192, 1024, 2);
+    const uint64_t bh = sdesc(b + ks * 2048, 8192, 1024, 2), bl = sdesc(b + 16384 + ks * 2048, 8192, 1024, 2);
+    umma_f16(d_tmem, ah, bh, idesc, ks > 0 ? 1u : 0u);
+    umma_f16(d_tmem, ah, bl, idesc, 1u);
+    umma_f16(d_tmem, al, bh, idesc, 1u);
+  }
+}
+
+// prep_kernel's products with K = V = 128 (after W): Q = Diag(e^{gl}) - kr^T W,
+// R = kr^T U and B = qd^T do - W^T E on tcgen05 (fp32 accumulators in 512 TMEM columns),
+// from operands split in place; U and E by warp products in between.
+template <typename IO>
+__device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* slot, long tok0, int rows, int hv,
+                                            const float* X1, const float* X2, const float* X3, float* B0, float* B1,
+                                            float* B2, float* B3, float* B4, const float* F, const float* G,
+                                            const float* EG, const float* bs, uint64_t* mbar, uint32_t* tslot) {
+  constexpr int K = 128, V = 128, LK = K + 4, LV = V + 4;
+  using S = Slot<K, V>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const auto zero = [](int, int) { return 0.f; };
+  const auto all = [](int, int) { return true; };
+  const auto fa_A = [&](int i, int j, int) { return X3[i * LC + j] * bs[j]; };
+  const auto kr_tril = [](int m0, int) { return make_int2(0, m0 + 32); };
+  // W (fp32) to the slot, then W and kr = R e^{gl - e_b} split; Q's products
+  copy_out<K, LK>(slot + S::W, B2);
+  split_mn<LK>(B2, [](int, int, float x) { return x; });
+  split_mn<LK>(B3, [&](int i, int d, float x) { return x * G[(i >> 4) * K + d]; });
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    issue_split_mn(tmem, smem_u32(B3), smem_u32(B2));
+  }
+  // U = A v (B4), to the slot, split; R's products
+  load_rows<IO, V>(B0, static_cast<const IO*>(p.v), tok0, rows, static_cast<size_t>(p.HV) * V, static_cast<size_t>(hv) * V);
+  __syncthreads();
+  cta_gemm<C, V, 4, 2>(fa_A, [&](int j, int vv, int) { return B0[j * LV + vv]; }, all, kr_tril, zero,
+                       [&](int r, int c, float x0, float x1) {
+                         B4[r * LV + c] = x0;
+                         B4[r * LV + c + 1] = x1;
+                       });
+  __syncthreads();
+  copy_out<V, LV>(slot + S::U, B4);
+  split_mn<LV>(B4, [](int, int, float x) { return x; });
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    issue_split_mn(tmem + 128, smem_u32(B3), smem_u32(B4));
+    umma_commit(mbar);  // phase 0: Q and R
+  }
+  // E = Aqk^T do (B4 once R's products have read U), to the slot; do, E and qd split
+  load_rows<IO, V>(B0, static_cast<const IO*>(p.d_out), tok0, rows, static_cast<size_t>(p.HV) * V,
+                   static_cast<size_t>(hv) * V);
+  if (!mbar_wait(mbar, 0, p.wait_ns)) atomicOr(p.status, kStatusTimeout);
+  tc_fence_after();
+  __syncthreads();
+  cta_gemm<C, V, 4, 2>([&](int j, int i, int) { return X2[i * LC + j]; }, [&](int i, int vv, int) { return B0[i * LV + vv]; },
+                       all, [](int m0, int) { return make_int2(m0, C); }, zero, [&](int r, int c, float x0, float x1) {
+                         B4[r * LV + c] = x0;
+                         B4[r * LV + c + 1] = x1;
+                       });
+  __syncthreads();
+  copy_out<V, LV>(slot + S::E, B4);
+  split_mn<LV>(B4, [](int, int, float x) { return x; });
+  split_mn<LV>(B0, [](int, int, float x) { return x; });
+  split_mn<LK>(B1, [&](int i, int d, float x) { return x * F[(i >> 4) * K + d]; });
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    issue_split_mn(tmem + 256, smem_u32(B1), smem_u32(B0));  // qd^T do
+    issue_split_mn(tmem + 384, smem_u32(B2), smem_u32(B4));  // W^T E
+    umma_commit(mbar);  // phase 1
+  }
+  copy_out<C, LC>(slot + S::T, X3);
+  copy_out<C, LC>(slot + S::KK, X1);
+  if (!mbar_wait(mbar, 1, p.wait_ns)) atomicOr(p.status, kStatusTimeout);
+  tc_fence_after();
+  // readout: warp w holds key rows 32 (w % 4) + lane, columns 64 (w / 4) + [0, 64)
+  const int d = 32 * (warp & 3) + lane, h = warp >> 2;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * h;
+  uint8_t* qb = reinterpret_cast<uint8_t*>(slot + S::Q);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float x[32];
+    tmem_ld32(trow + 32 * half, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {  // Q: bf16 high / low parts, K-major 128-B swizzled
+      const int e0 = 64 * h + 32 * half + 8 * c8;
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = e0 + 2 * e;
+        const float y0 = (d == c ? EG[d] : 0.f) - x[8 * c8 + 2 * e], y1 = (d == c + 1 ? EG[d] : 0.f) - x[8 * c8 + 2 * e + 1];
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(y0, y1);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(y0 - __low2float(hb), y1 - __high2float(hb));
+        hi[e] = *reinterpret_cast<const uint32_t*>(&hb);
+        lo[e] = *reinterpret_cast<const uint32_t*>(&lb);
+      }
+      const uint32_t o = sw128_offset(d, e0, K);
+      *reinterpret_cast<uint4*>(qb + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(qb + kQLow + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float r[32], b1[32], b2[32];
+    tmem_ld32(trow + 128 + 32 * half, r);
+    tmem_ld32(trow + 256 + 32 * half, b1);
+    tmem_ld32(trow + 384 + 32 * half, b2);
+    tmem_ld_wait();
+    float* rp = slot + S::RH + kv_off<K>(d, 64 * h + 32 * half);
+    float* bp = slot + S::BD + kv_off<K>(d, 64 * h + 32 * half);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      *reinterpret_cast<float4*>(rp + 4 * j) = make_float4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      *reinterpret_cast<float4*>(bp + 4 * j) = make_float4(b1[4 * j] - b2[4 * j], b1[4 * j + 1] - b2[4 * j + 1],
+                                                           b1[4 * j + 2] - b2[4 * j + 2], b1[4 * j + 3] - b2[4 * j + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <typename IO, int K, int V>
 __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
   using S = Slot<K, V>;
   using L = PrepSmem<K, V>;
   constexpr int LK = L::LK, LV = L::LV;
-  extern __shared__ __align__(16) float sm[];
+  constexpr bool TC = K == 128 && V == 128;  // Q, R and B on tcgen05
+  extern __shared__ __align__(16) uint8_t praw[];
+  float* sm = reinterpret_cast<float*>(praw + ((1024u - (smem_u32(praw) & 1023u)) & 1023u));
   float *B0 = sm + L::B0, *B1 = sm + L::B1, *B2 = sm + L::B2, *B3 = sm + L::B3, *B4 = sm + L::B4;
   float *X1 = sm + L::X1, *X2 = sm + L::X2, *X3 = sm + L::X3;
   float *F = sm + L::F, *G = sm + L::G, *D = sm + L::D, *EG = sm + L::EG, *bs = sm + L::BS;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + L::FLOATS);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::FLOATS) + 2;
   int seq, m, rows;
   long tok0;
   const int f = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
   if (!find_chunk(p, f, seq, m, tok0, rows)) return;
+  if constexpr (TC) {
+    if (tid == 0) {
+      mbar_init(mbar, 1);
+      fence_mbar_init();
+    }
+    if (tid < 32) tmem_alloc(tslot, 512);
+    tc_fence_before();
+  }
   const int hk = hv / (p.HV / p.H);
   float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
   const auto zero = [](int, int) { return 0.f; };
@@ -515,6 +707,10 @@ __global__ void __launch_bounds__(NT, 1) prep_kernel(Params p) {
                       B2[r * LK + c + 1] = x1;
                     });
   __syncthreads();
+  if constexpr (TC) {
+    prep_qrb_tc<IO>(p, sm, slot, tok0, rows, hv, X1, X2, X3, B0, B1, B2, B3, B4, F, G, EG, bs, mbar, tslot);
+    return;
+  }
   // 5. Q = Diag(e^{gl}) - kr^T W (kr = R e^{gl - e_b}); W to the slot
   const auto fa_krT = [&](int d, int i, int) { return B3[i * LK + d] * G[(i >> 4) * K + d]; };
   const auto kr_all = [](int, int) { return make_int2(0, C); };
@@ -1257,7 +1453,7 @@ __global__ void __launch_bounds__(NT, 1) grad_k_kernel(Params p) {
 
 template <typename IO, int K, int V>
 cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
-  const size_t s_prep = PrepSmem<K, V>::FLOATS * 4, s_chain = K == 128 ? tcc::SMEM : ChainSmem<K>::FLOATS * 4,
+  const size_t s_prep = PrepSmem<K, V>::BYTES, s_chain = K == 128 ? tcc::SMEM : ChainSmem<K>::FLOATS * 4,
                s_gv = GvSmem<K, V>::FLOATS * 4,
                s_gc = GcSmem<K>::FLOATS * 4, s_gk = GkSmem::FLOATS * 4;
   cudaError_t e;
