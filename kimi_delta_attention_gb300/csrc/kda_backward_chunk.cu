@@ -51,6 +51,10 @@ constexpr bool kSplit = KDA_CBWD_SPLIT != 0;
 // The decay of one 16-row block that the block factors hold (log2 units, as the forward
 // kernels): beyond it a chunk raises the status range bit.
 constexpr float kMinBlockLog2 = -116.f;
+// Waits for a CTA's own copies and products give up after Params::wait_ns (the status
+// then reports a timeout); draining them before the CTA releases its memory always allows
+// this much.
+constexpr unsigned long long kDrainNs = 2000000000ull;
 
 struct Params {
   const void* q;       // [tokens, H, K]  io type
@@ -548,7 +552,10 @@ __device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* s
   // E = Aqk^T do (B4 once R's products have read U), to the slot; do, E and qd split
   load_rows<IO, V>(B0, static_cast<const IO*>(p.d_out), tok0, rows, static_cast<size_t>(p.HV) * V,
                    static_cast<size_t>(hv) * V);
-  if (!mbar_wait(mbar, 0, p.wait_ns)) atomicOr(p.status, kStatusTimeout);
+  if (!mbar_wait(mbar, 0, p.wait_ns)) {
+    atomicOr(p.status, kStatusTimeout);
+    mbar_wait(mbar, 0, kDrainNs);  // U is rewritten only once the products that read it are done
+  }
   tc_fence_after();
   __syncthreads();
   cta_gemm<C, V, 4, 2>([&](int j, int i, int) { return X2[i * LC + j]; }, [&](int i, int vv, int) { return B0[i * LV + vv]; },
@@ -572,7 +579,10 @@ __device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* s
   }
   copy_out<C, LC>(slot + S::T, X3);
   copy_out<C, LC>(slot + S::KK, X1);
-  if (!mbar_wait(mbar, 1, p.wait_ns)) atomicOr(p.status, kStatusTimeout);
+  if (!mbar_wait(mbar, 1, p.wait_ns)) {
+    atomicOr(p.status, kStatusTimeout);
+    mbar_wait(mbar, 1, kDrainNs);  // the accumulators are read and released only after the products
+  }
   tc_fence_after();
   // readout: warp w holds key rows 32 (w % 4) + lane, columns 64 (w / 4) + [0, 64)
   const int d = 32 * (warp & 3) + lane, h = warp >> 2;
@@ -1028,8 +1038,8 @@ __global__ void __launch_bounds__(NT, 1) chain_tc_kernel(Params p) {
   }
   if (tid == 0 && step < nch) {  // after a failure: the loads issued for later steps, and the products,
                                  // complete (bounded waits) before the CTA releases its memory
-    for (int s2 = step; s2 < issued; ++s2) mbar_wait(&bars[s2 & 1], (s2 >> 1) & 1, p.wait_ns);
-    if (pending) mbar_wait(&bars[2], step & 1, p.wait_ns);
+    for (int s2 = step; s2 < issued; ++s2) mbar_wait(&bars[s2 & 1], (s2 >> 1) & 1, kDrainNs);
+    if (pending) mbar_wait(&bars[2], step & 1, kDrainNs);
   }
   if (dir == 1 && p.ds0 && !*failed) {
     float* dp = p.ds0 + (static_cast<size_t>(seq) * p.HV + hv) * K * V + static_cast<size_t>(row) * V + v0 + c0;

@@ -68,3 +68,44 @@ def test_short_wait_limit_reports_timeout_and_recovers(split):
         assert kda.kda_read_device_status(ws) == 0
     o_ref, S_ref = oracle_full(x)
     assert_close(o.float().cpu().numpy(), S.cpu().numpy(), o_ref, S_ref, "bf16", f"after timeout, split={split}")
+
+
+def test_backward_short_wait_limit_completes_and_recovers():
+    """The chunk-form backward waits only on its own bulk copies and tcgen05 products (the
+    state chains, the preparation's products), with the same limit; they end within
+    microseconds, so a 1 us limit may or may not run out (mbarrier.try_wait suspends for a
+    while before the limit is checked).  Either way the call must complete: status OK with
+    the oracle's gradients, or a reported timeout after its drains; and the next call with
+    the default limit must match the oracle."""
+    import numpy as np
+    import oracle
+    from kda_testutil import np32
+    x = W.make_inputs(1, 300, 2, 2, 128, 128, "bf16", seed=43, init_state=True)   # 5 chunks
+    rng = np.random.default_rng(44)
+    do = torch.from_numpy(rng.standard_normal(tuple(x.v.shape), dtype=np.float32)).to(torch.bfloat16)
+    dfin = torch.from_numpy(rng.standard_normal(tuple(x.initial_state.shape), dtype=np.float32))
+    d = x.to("cuda")
+    shape = kda.make_shape(d.q, d.v)
+    ws = torch.empty(kda.kda_backward_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    ref = oracle.backward(np32(x.q), np32(x.k), np32(x.v), np32(x.g), np32(x.beta), x.scale, np32(do),
+                          d_final_state=np32(dfin), initial_state=np32(x.initial_state))
+
+    def check(got, what):
+        for name, a, r in zip(("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"), got, ref):
+            err = np.abs(a.cpu().numpy() - r).max() / max(np.abs(r).max(), 1e-30)
+            assert err <= 1e-4, f"{what}: {name} error {err:.3e}"
+
+    with _env(KDA_BACKWARD=None, KDA_WAIT_LIMIT_NS="1000"):
+        got = kda.kda_backward(d.q, d.k, d.v, d.g, d.beta, do.cuda(), d.scale, initial_state=d.initial_state,
+                               d_final_state=dfin.cuda(), workspace=ws)
+        torch.cuda.synchronize()
+        st = kda.kda_read_device_status(ws)
+        assert st in (0, KDA_ERR_DEVICE_TIMEOUT)
+        if st == 0:
+            check(got, "1 us limit")
+    with _env(KDA_BACKWARD=None, KDA_WAIT_LIMIT_NS=None):
+        got = kda.kda_backward(d.q, d.k, d.v, d.g, d.beta, do.cuda(), d.scale, initial_state=d.initial_state,
+                               d_final_state=dfin.cuda(), workspace=ws)
+        torch.cuda.synchronize()
+        assert kda.kda_read_device_status(ws) == 0
+    check(got, "default limit after the short one")
