@@ -115,6 +115,10 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 __device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+}
 __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
   const uint2 u = *reinterpret_cast<const uint2*>(p);
   return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
@@ -1223,6 +1227,367 @@ __global__ void __launch_bounds__(NT, 1) grad_v_kernel(Params p) {
                     });
 }
 
+// ------------------------------------------------- value gradients (tcgen05) --
+// K = V = 128: every product of grad_v_kernel as a transposed M = 128 tcgen05 product of
+// bf16 high/low operand splits (three products each), fp32 accumulators in TMEM:
+//   -v_new^T = h^T W^T - U^T   dv_new^T = D^T kr^T + E^T   DH^T = h do^T
+//   -dW^T = h dv_new^T         dkr^T = D v_new^T
+//   [do; dv_new] [v_new; v]^T: rows 0-63 x columns 0-63 are dAqk, rows 64-127 x 64-127 dAv
+//   dv^T = dv_new^T (T Diag(beta))
+// h (the state entering the chunk) and D (the gradient leaving it) stay in shared memory
+// as split K-major tiles, which are also their transposes' MN-major tiles.
+namespace gvt {
+constexpr uint32_t RH = 0, RD = 65536, RW = 131072, RKR = 163840, RDO = 196608, RB = 229376;  // byte offsets
+constexpr uint32_t SMEM = RB + 16 + 4 * (128 + 64) + 1024;
+}  // namespace gvt
+template <class FAH, class FAL, class FBH, class FBL>
+__device__ __forceinline__ void issue_split(uint32_t d, const FAH& ah, const FAL& al, const FBH& bh, const FBL& bl,
+                                            uint32_t idesc, int nks, bool accumulate) {
+  for (int ks = 0; ks < nks; ++ks) {
+    umma_f16(d, ah(ks), bh(ks), idesc, (accumulate || ks > 0) ? 1u : 0u);
+    umma_f16(d, ah(ks), bl(ks), idesc, 1u);
+    umma_f16(d, al(ks), bh(ks), idesc, 1u);
+  }
+}
+// 8 fp32 values -> their bf16 high and low parts, as two 16-byte chunks
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * e] - __low2float(hb), x[2 * e + 1] - __high2float(hb));
+    h[e] = *reinterpret_cast<const uint32_t*>(&hb);
+    l[e] = *reinterpret_cast<const uint32_t*>(&lb);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// byte offset of the 8-element chunk (row r, columns c8 .. c8 + 7) in a 128-byte-swizzled
+// tile of 128-byte rows (one 64-column block; a K-major tile's row, an MN-major tile's K-row)
+__device__ __forceinline__ uint32_t sw_chunk(uint32_t r, uint32_t c8) {
+  return (r >> 3) * 1024u + (r & 7) * 128u + ((((c8 & 63) >> 3) ^ (r & 7)) << 4);
+}
+template <typename IO>
+__global__ void __launch_bounds__(NT, 1) grad_v_tc_kernel(Params p) {
+  constexpr int K = 128, V = 128, LK = K + 4;
+  using S = Slot<K, V>;
+  extern __shared__ __align__(16) uint8_t graw[];
+  uint8_t* sm = graw + ((1024u - (smem_u32(graw) & 1023u)) & 1023u);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + gvt::RB);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + gvt::RB + 8);
+  float* gl2 = reinterpret_cast<float*>(sm + gvt::RB + 16);
+  float* bs = gl2 + K;
+  int seq, m, rows;
+  long tok0;
+  const int f = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (!find_chunk(p, f, seq, m, tok0, rows)) return;
+  const int hk = hv / (p.HV / p.H);
+  float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
+  if (tid == 0) {
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot, sb = smem_u32(sm);
+  const int row = 32 * (warp & 3) + lane, hcol = 32 * (warp >> 2);  // TMEM lane; 32 of a 64-column block
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + hcol;
+  uint32_t phase = 0;
+  auto wait_products = [&]() {
+    if (!mbar_wait(mbar, phase & 1, p.wait_ns)) {
+      atomicOr(p.status, kStatusTimeout);
+      mbar_wait(mbar, phase & 1, kDrainNs);
+    }
+    ++phase;
+    tc_fence_after();
+  };
+  const IO* dop = static_cast<const IO*>(p.d_out);
+  const IO* vp = static_cast<const IO*>(p.v);
+  const size_t vrow = static_cast<size_t>(p.HV) * V, vcol = static_cast<size_t>(hv) * V;
+
+  // 1. kr = k e^{gl - gc} from g and k rows (fp32 scratch over the h, D regions), split
+  //    K-major; beta
+  {
+    float* gs = reinterpret_cast<float*>(sm);
+    float* ks_ = gs + C * LK;
+    load_rows<float, K>(gs, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K);
+    load_rows<IO, K>(ks_, static_cast<const IO*>(p.k), tok0, rows, static_cast<size_t>(p.H) * K, static_cast<size_t>(hk) * K);
+    if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
+    __syncthreads();
+    cumsum_log2<K, LK>(gs);
+    __syncthreads();
+    if (tid < K) gl2[tid] = gs[(C - 1) * LK + tid];
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = tid + NT * u, i = c >> 4, d8 = (c & 15) << 3;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = ks_[i * LK + d8 + e] * ex2(gl2[d8 + e] - gs[i * LK + d8 + e]);
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      const uint32_t o = (d8 >> 6) * 8192u + sw_chunk(i, d8);
+      *reinterpret_cast<uint4*>(sm + gvt::RKR + o) = hi;
+      *reinterpret_cast<uint4*>(sm + gvt::RKR + 16384 + o) = lo;
+    }
+    __syncthreads();  // the scratch is read before h and D overwrite it
+  }
+  // 2. W and do split K-major; h and D split K-major (and dgl = e^{gl} sum_v h D); the
+  //    addends -U^T and E^T into TMEM
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = tid + NT * u, i = c >> 4, c8 = (c & 15) << 3;
+    const uint32_t o = (c8 >> 6) * 8192u + sw_chunk(i, c8);
+    float x[8];
+    const float4 a = *reinterpret_cast<const float4*>(slot + S::W + i * K + c8);
+    const float4 b = *reinterpret_cast<const float4*>(slot + S::W + i * K + c8 + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    uint4 hi, lo;
+    split8(x, hi, lo);
+    *reinterpret_cast<uint4*>(sm + gvt::RW + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RW + 16384 + o) = lo;
+    float4 da = make_float4(0.f, 0.f, 0.f, 0.f), db = da;
+    if (i < rows) {
+      da = load4(dop + static_cast<size_t>(tok0 + i) * vrow + vcol + c8);
+      db = load4(dop + static_cast<size_t>(tok0 + i) * vrow + vcol + c8 + 4);
+    }
+    x[0] = da.x; x[1] = da.y; x[2] = da.z; x[3] = da.w; x[4] = db.x; x[5] = db.y; x[6] = db.z; x[7] = db.w;
+    split8(x, hi, lo);
+    *reinterpret_cast<uint4*>(sm + gvt::RDO + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RDO + 16384 + o) = lo;
+  }
+#pragma unroll 2
+  for (int u = 0; u < 8; ++u) {
+    const int c = tid + NT * u, d = c >> 4, v8 = (c & 15) << 3;
+    const uint32_t o = (v8 >> 6) * 16384u + sw_chunk(d, v8);
+    const float* hs = slot + S::RH + kv_off<K>(d, v8);
+    const float* ds = slot + S::BD + kv_off<K>(d, v8);
+    float xh[8], xd[8];
+    const float4 h0 = *reinterpret_cast<const float4*>(hs), h1 = *reinterpret_cast<const float4*>(hs + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(ds), d1 = *reinterpret_cast<const float4*>(ds + 4);
+    xh[0] = h0.x; xh[1] = h0.y; xh[2] = h0.z; xh[3] = h0.w; xh[4] = h1.x; xh[5] = h1.y; xh[6] = h1.z; xh[7] = h1.w;
+    xd[0] = d0.x; xd[1] = d0.y; xd[2] = d0.z; xd[3] = d0.w; xd[4] = d1.x; xd[5] = d1.y; xd[6] = d1.z; xd[7] = d1.w;
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dot = fmaf(xh[e], xd[e], dot);
+#pragma unroll
+    for (int o2 = 8; o2 >= 1; o2 >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o2);  // the row's 16 threads
+    if ((tid & 15) == 0) slot[S::DGL + d] = ex2(gl2[d]) * dot;
+    uint4 hi, lo;
+    split8(xh, hi, lo);
+    *reinterpret_cast<uint4*>(sm + gvt::RH + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RH + 32768 + o) = lo;
+    split8(xd, hi, lo);
+    *reinterpret_cast<uint4*>(sm + gvt::RD + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RD + 32768 + o) = lo;
+  }
+  {
+    float a[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = -slot[S::U + (hcol + j) * V + row];
+    tmem_st32(tl, a);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = slot[S::E + (hcol + j) * V + row];
+    tmem_st32(tl + 64, a);
+    tmem_st_wait();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t id_ab = idesc_f16kind(128, 64) | IDESC_A_MN_MAJOR;  // A MN-major, B K-major
+    constexpr uint32_t id_kk = idesc_f16kind(128, 64);                      // both K-major
+    // -v_new^T (onto -U^T): A = h^T (MN-major view of h), B = W (K-major)
+    issue_split(tmem, [&](int k) { return sdesc(sb + gvt::RH + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RH + 32768 + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RW + (k >> 2) * 8192 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RW + 16384 + (k >> 2) * 8192 + (k & 3) * 32); }, id_ab, 8, true);
+    // dv_new^T (onto E^T): A = D^T, B = kr
+    issue_split(tmem + 64, [&](int k) { return sdesc(sb + gvt::RD + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RD + 32768 + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RKR + (k >> 2) * 8192 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RKR + 16384 + (k >> 2) * 8192 + (k & 3) * 32); }, id_ab, 8, true);
+    // DH^T: A = h (K-major), B = do (K-major)
+    issue_split(tmem + 128, [&](int k) { return sdesc_sw128(sb + gvt::RH + (k >> 2) * 16384 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RH + 32768 + (k >> 2) * 16384 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RDO + (k >> 2) * 8192 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RDO + 16384 + (k >> 2) * 8192 + (k & 3) * 32); }, id_kk, 8, false);
+    umma_commit(mbar);
+  }
+  wait_products();
+  // 3. v_new^T and dv_new^T split as MN-major B tiles (K-rows = value columns) over W and kr;
+  //    DH to the slot
+  {
+    float x[32];
+    tmem_ld32(tl, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j8 = 0; j8 < 4; ++j8) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = -x[8 * j8 + e];
+      uint4 hi, lo;
+      split8(y, hi, lo);
+      const uint32_t o = sw_chunk(row, hcol + 8 * j8);
+      *reinterpret_cast<uint4*>(sm + gvt::RW + o) = hi;
+      *reinterpret_cast<uint4*>(sm + gvt::RW + 16384 + o) = lo;
+    }
+    tmem_ld32(tl + 64, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j8 = 0; j8 < 4; ++j8) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[8 * j8 + e];
+      uint4 hi, lo;
+      split8(y, hi, lo);
+      const uint32_t o = sw_chunk(row, hcol + 8 * j8);
+      *reinterpret_cast<uint4*>(sm + gvt::RKR + o) = hi;
+      *reinterpret_cast<uint4*>(sm + gvt::RKR + 16384 + o) = lo;
+    }
+    tmem_ld32(tl + 128, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) slot[S::DH + (hcol + j) * K + row] = x[j];
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t id_kb = idesc_f16kind(128, 64) | IDESC_B_MN_MAJOR;  // A K-major, B MN-major
+    // -dW^T: A = h, B = dv_new^T
+    issue_split(tmem + 192, [&](int k) { return sdesc_sw128(sb + gvt::RH + (k >> 2) * 16384 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RH + 32768 + (k >> 2) * 16384 + (k & 3) * 32); },
+                [&](int k) { return sdesc(sb + gvt::RKR + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RKR + 16384 + k * 2048, 16384, 1024, 2); }, id_kb, 8, false);
+    // dkr^T: A = D, B = v_new^T
+    issue_split(tmem + 256, [&](int k) { return sdesc_sw128(sb + gvt::RD + (k >> 2) * 16384 + (k & 3) * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RD + 32768 + (k >> 2) * 16384 + (k & 3) * 32); },
+                [&](int k) { return sdesc(sb + gvt::RW + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RW + 16384 + k * 2048, 16384, 1024, 2); }, id_kb, 8, false);
+    umma_commit(mbar);
+  }
+  wait_products();
+  // 4. dW, dkr to the slot; over h and D: [do^T | dv_new^T] and [v_new^T | v^T] (two 64-wide
+  //    atoms each, 16 KB apart); T Diag(beta) split as an MN-major B over do
+  {
+    float x[32];
+    tmem_ld32(tl + 192, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) slot[S::DW + (hcol + j) * K + row] = -x[j];
+    tmem_ld32(tl + 256, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) slot[S::DKR + (hcol + j) * K + row] = x[j];
+    tmem_ld32(tl + 64, x);  // dv_new^T again
+    tmem_ld_wait();
+#pragma unroll
+    for (int j8 = 0; j8 < 4; ++j8) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[8 * j8 + e];
+      uint4 hi, lo;
+      split8(y, hi, lo);
+      const uint32_t o = sw_chunk(row, hcol + 8 * j8);
+      *reinterpret_cast<uint4*>(sm + gvt::RH + 16384 + o) = hi;
+      *reinterpret_cast<uint4*>(sm + gvt::RH + 49152 + o) = lo;
+    }
+    tmem_ld32(tl, x);  // -v_new^T again
+    tmem_ld_wait();
+#pragma unroll
+    for (int j8 = 0; j8 < 4; ++j8) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = -x[8 * j8 + e];
+      uint4 hi, lo;
+      split8(y, hi, lo);
+      const uint32_t o = sw_chunk(row, hcol + 8 * j8);
+      *reinterpret_cast<uint4*>(sm + gvt::RD + o) = hi;
+      *reinterpret_cast<uint4*>(sm + gvt::RD + 32768 + o) = lo;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {  // do^T and v^T: K-row = value column, 8 chunk rows per chunk
+    const int c = tid + NT * u, vv = c >> 3, i8 = (c & 7) << 3;
+    float xo[8], xv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const bool ok = i8 + e < rows;
+      const size_t at = static_cast<size_t>(tok0 + i8 + e) * vrow + vcol + vv;
+      xo[e] = ok ? load1(dop + at) : 0.f;
+      xv[e] = ok ? load1(vp + at) : 0.f;
+    }
+    const uint32_t o = sw_chunk(vv, i8);
+    uint4 hi, lo;
+    split8(xo, hi, lo);
+    *reinterpret_cast<uint4*>(sm + gvt::RH + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RH + 32768 + o) = lo;
+    split8(xv, hi, lo);
+    *reinterpret_cast<uint4*>(sm + gvt::RD + 16384 + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RD + 49152 + o) = lo;
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {  // T Diag(beta): K-row = chunk row i, columns j
+    const int c = tid + NT * u, i = c >> 3, j8 = (c & 7) << 3;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = slot[S::T + i * C + j8 + e] * bs[j8 + e];
+    uint4 hi, lo;
+    split8(x, hi, lo);
+    const uint32_t o = sw_chunk(i, j8);
+    *reinterpret_cast<uint4*>(sm + gvt::RDO + o) = hi;
+    *reinterpret_cast<uint4*>(sm + gvt::RDO + 8192 + o) = lo;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t id_mm = idesc_f16kind(128, 128) | IDESC_A_MN_MAJOR | IDESC_B_MN_MAJOR;
+    constexpr uint32_t id_kb = idesc_f16kind(128, 64) | IDESC_B_MN_MAJOR;
+    // [do; dv_new] [v_new; v]^T
+    issue_split(tmem + 320, [&](int k) { return sdesc(sb + gvt::RH + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RH + 32768 + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RD + k * 2048, 16384, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RD + 32768 + k * 2048, 16384, 1024, 2); }, id_mm, 8, false);
+    // dv^T: A = dv_new^T (K-major view of its atom), B = T Diag(beta)
+    issue_split(tmem + 448, [&](int k) { return sdesc_sw128(sb + gvt::RH + 16384 + k * 32); },
+                [&](int k) { return sdesc_sw128(sb + gvt::RH + 49152 + k * 32); },
+                [&](int k) { return sdesc(sb + gvt::RDO + k * 2048, 8192, 1024, 2); },
+                [&](int k) { return sdesc(sb + gvt::RDO + 8192 + k * 2048, 8192, 1024, 2); }, id_kb, 4, false);
+    umma_commit(mbar);
+  }
+  wait_products();
+  // 5. dAqk (rows 0-63, columns 0-63) and dAv (rows 64-127, columns 64-127), lower
+  //    triangles; dv
+  {
+    float x[32];
+    const bool first = row < 64;
+    tmem_ld32(tl + 320 + (first ? 0 : 64), x);
+    tmem_ld_wait();
+    const int i = first ? row : row - 64;
+    float* dst = slot + (first ? S::DAQK : S::DAV) + i * C + hcol;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dst[j] = hcol + j <= i ? x[j] : 0.f;
+    tmem_ld32(tl + 448, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (hcol + j < rows) p.dv[(static_cast<size_t>(tok0 + hcol + j) * p.HV + hv) * V + row] = x[j];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ------------------------------------------------------------- C x C stage --
 template <int K>
 struct GcSmem {
@@ -1471,7 +1836,10 @@ cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
       (e = K == 128 ? cudaFuncSetAttribute(chain_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_chain)
                     : cudaFuncSetAttribute(chain_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_chain)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(grad_v_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gv)) != cudaSuccess ||
+      (e = (K == 128 && V == 128)
+               ? cudaFuncSetAttribute(grad_v_tc_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gvt::SMEM)
+               : cudaFuncSetAttribute(grad_v_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gv)) !=
+          cudaSuccess ||
       (e = cudaFuncSetAttribute(grad_cc_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gc)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(grad_k_kernel<IO, K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_gk)) != cudaSuccess)
     return e;
@@ -1483,7 +1851,10 @@ cudaError_t launch_kv(const Params& p, int chunks, cudaStream_t st) {
   else
     chain_kernel<K, V><<<dim3(V < VS ? 1 : V / VS, p.HV, 2 * p.num_seqs), NT, s_chain, st>>>(p);
   if (chunks > 0) {
-    grad_v_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gv, st>>>(p);
+    if (K == 128 && V == 128)
+      grad_v_tc_kernel<IO><<<dim3(chunks, p.HV), NT, gvt::SMEM, st>>>(p);
+    else
+      grad_v_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gv, st>>>(p);
     grad_cc_kernel<IO, K, V><<<dim3(chunks, p.HV), NT, s_gc, st>>>(p);
     grad_k_kernel<IO, K, V><<<dim3(chunks, p.HV, K / DK), NT, s_gk, st>>>(p);
   }
