@@ -611,7 +611,7 @@ BACKWARD_METRIC = ("KDA backward (gradients of q, k, v, g, beta and the initial 
 # is the measured bf16 peak scaled by their ratio
 TF32_PER_BF16 = 1.1 / 2.25
 BACKWARD_LAUNCHES = 5  # prep, chain, value-side, C x C and key-side gradient kernels
-BACKWARD_KERNELS = "prep_kernel, chain_tc_kernel, grad_v_kernel, grad_cc_kernel, grad_k_kernel"
+BACKWARD_KERNELS = "prep_kernel, chain_tc_kernel, grad_v_tc_kernel, grad_cc_kernel, grad_k_kernel"
 
 
 def backward_flops(tokens_heads: int, K: int, V: int, C: int = 64) -> float:
@@ -681,7 +681,8 @@ def run_backward(args):
         "config": {"workload": "backward_bf16_T4096_H32_K128", "B": B, "T": T, "H": H, "HV": HV, "K": K, "V": V,
                    "io": "bf16 q/k/v/d_out, fp32 g/beta/d_final_state; fp32 gradients",
                    "products": ("each operand split into high and low parts, 3 products per product: tcgen05 bf16 "
-                                "for the state chains and prep's K x K / K x V products, warp-level TF32 for the rest"),
+                                "for the state chains, the value-side gradients and prep's K x K / K x V products, "
+                                "warp-level TF32 for the rest"),
                    "l2": "flushed between timed steps"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                      "frac": achieved / tf32_peak, "kernel": f"the whole step ({BACKWARD_KERNELS})",
