@@ -588,10 +588,15 @@ __device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* s
     mbar_wait(mbar, 1, kDrainNs);  // the accumulators are read and released only after the products
   }
   tc_fence_after();
-  // readout: warp w holds key rows 32 (w % 4) + lane, columns 64 (w / 4) + [0, 64)
+  // readout: warp w holds key rows 32 (w % 4) + lane, columns 64 (w / 4) + [0, 64).  Q, R
+  // and B are staged in shared memory (free now: the operands' products are done, T and
+  // kd ki^T are out) in their slot layouts, then written by three bulk copies.
+  __syncthreads();  // every thread's copies of T and kd ki^T have read their tiles
   const int d = 32 * (warp & 3) + lane, h = warp >> 2;
   const uint32_t trow = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * h;
-  uint8_t* qb = reinterpret_cast<uint8_t*>(slot + S::Q);
+  uint8_t* stq = reinterpret_cast<uint8_t*>(sm);  // [0, 64 KB): Q; [64, 128 KB): R; [128, 192 KB): B
+  float* str = sm + 16384;
+  float* stb = sm + 32768;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float x[32];
@@ -611,8 +616,8 @@ __device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* s
         lo[e] = *reinterpret_cast<const uint32_t*>(&lb);
       }
       const uint32_t o = sw128_offset(d, e0, K);
-      *reinterpret_cast<uint4*>(qb + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(qb + kQLow + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(stq + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(stq + kQLow + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   }
 #pragma unroll
@@ -622,8 +627,8 @@ __device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* s
     tmem_ld32(trow + 256 + 32 * half, b1);
     tmem_ld32(trow + 384 + 32 * half, b2);
     tmem_ld_wait();
-    float* rp = slot + S::RH + kv_off<K>(d, 64 * h + 32 * half);
-    float* bp = slot + S::BD + kv_off<K>(d, 64 * h + 32 * half);
+    float* rp = str + kv_off<K>(d, 64 * h + 32 * half);
+    float* bp = stb + kv_off<K>(d, 64 * h + 32 * half);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       *reinterpret_cast<float4*>(rp + 4 * j) = make_float4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
@@ -631,8 +636,16 @@ __device__ __forceinline__ void prep_qrb_tc(const Params& p, float* sm, float* s
                                                            b1[4 * j + 2] - b2[4 * j + 2], b1[4 * j + 3] - b2[4 * j + 3]);
     }
   }
+  fence_proxy_async_smem();  // the staged tiles (generic stores) before the bulk copies read them
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {
+    bulk_store(slot + S::Q, stq, 65536);
+    bulk_store(slot + S::RH, str, 65536);
+    bulk_store(slot + S::BD, stb, 65536);
+    bulk_commit();
+    bulk_wait_read();  // shared memory is read before the CTA releases it
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
