@@ -1704,17 +1704,28 @@ __global__ void __launch_bounds__(NT, 1) grad_k_kernel(Params p) {
   const float* slot = p.ws + (static_cast<size_t>(f) * p.HV + hv) * p.slot_floats;
   const size_t qk_row = static_cast<size_t>(p.H) * K, qk_col = static_cast<size_t>(hk) * K + d0;
 
+  {  // the fp32 tiles by cp.async, all in flight together (g rows past the chunk are zero)
+    const float* gp = p.g + static_cast<size_t>(tok0) * p.HV * K + static_cast<size_t>(hv) * K + d0;
+    for (int idx = tid; idx < C * (DK / 4); idx += NT) {
+      const int r = idx / (DK / 4), c4 = (idx - r * (DK / 4)) * 4;
+      if (r < rows)
+        cp_async16(GC + r * LD + c4, gp + static_cast<size_t>(r) * p.HV * K + c4);
+      else
+        *reinterpret_cast<float4*>(GC + r * LD + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      cp_async16(DWs + r * LD + c4, slot + S::DW + static_cast<size_t>(r) * K + d0 + c4);
+    }
+    for (int idx = tid; idx < C * (C / 4); idx += NT) {
+      const int r = idx / (C / 4), c4 = (idx - r * (C / 4)) * 4;
+      cp_async16(XT + r * LC + c4, slot + S::T + r * C + c4);
+      cp_async16(XQ + r * LC + c4, slot + S::DAQK + r * C + c4);
+      cp_async16(XM + r * LC + c4, slot + S::DMB + r * C + c4);
+    }
+    cp_async_commit();
+  }
   load_rows<IO, DK>(KR, static_cast<const IO*>(p.k), tok0, rows, qk_row, qk_col);
   load_rows<IO, DK>(QR, static_cast<const IO*>(p.q), tok0, rows, qk_row, qk_col);
-  load_rows<float, DK>(GC, p.g, tok0, rows, static_cast<size_t>(p.HV) * K, static_cast<size_t>(hv) * K + d0);
-  for (int idx = tid; idx < C * (DK / 4); idx += NT) {
-    const int r = idx / (DK / 4), c4 = (idx - r * (DK / 4)) * 4;
-    *reinterpret_cast<float4*>(DWs + r * LD + c4) = load4(slot + S::DW + static_cast<size_t>(r) * K + d0 + c4);
-  }
-  copy_in<C, LC>(XT, slot + S::T);
-  copy_in<C, LC>(XQ, slot + S::DAQK);
-  copy_in<C, LC>(XM, slot + S::DMB);
   if (tid < C) bs[tid] = tid < rows ? p.beta[(tok0 + tid) * p.HV + hv] : 0.f;
+  cp_async_wait<0>();
   __syncthreads();
   // tables: Lk, Lq from copies of the raw rows (the raw rows stay for the final pass)
   for (int idx = tid; idx < C * DK; idx += NT) {
@@ -1828,12 +1839,28 @@ __global__ void __launch_bounds__(NT, 1) grad_k_kernel(Params p) {
       }
   }
   __syncthreads();
-  if (tid < DK) {
-    float s = slot[S::DGL + d0 + tid];
-    for (int i = 0; i < C; ++i) s += DKA[i * LD + tid];
-    float* dgp = p.dg + static_cast<size_t>(tok0) * p.HV * K + static_cast<size_t>(hv) * K + d0 + tid;
-    for (int i = C - 1; i >= 0; --i) {
-      s += DGA[i * LD + tid];
+  {  // four threads per key dim, 16 rows each: the column sum of k dk_e^{gl-gc} and the
+     // segment sums of dgc (in refs, free now), then each segment's reverse cumulative sum
+    const int col = tid & (DK - 1), part = tid / DK;
+    float sk = 0.f, sg = 0.f;
+#pragma unroll
+    for (int i = 16 * part; i < 16 * part + 16; ++i) {
+      sk += DKA[i * LD + col];
+      sg += DGA[i * LD + col];
+    }
+    refs[part * DK + col] = sk;
+    refs[4 * DK + part * DK + col] = sg;
+    __syncthreads();
+    float s = slot[S::DGL + d0 + col];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      s += refs[q * DK + col];
+      if (q > part) s += refs[4 * DK + q * DK + col];
+    }
+    float* dgp = p.dg + static_cast<size_t>(tok0) * p.HV * K + static_cast<size_t>(hv) * K + d0 + col;
+#pragma unroll
+    for (int i = 16 * part + 15; i >= 16 * part; --i) {
+      s += DGA[i * LD + col];
       if (i < rows) dgp[static_cast<size_t>(i) * p.HV * K] = s;
     }
   }
