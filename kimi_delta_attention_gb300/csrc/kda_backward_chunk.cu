@@ -1,8 +1,10 @@
 // kda_backward_chunk.cu -- the backward in chunk form: gradients of
 // sum_t <do_t, o_t> + <dS_final, S_final> with respect to q, k, v, g, beta and the
-// initial state, chunk by chunk (C = 64), with every contraction on the tensor cores
-// (warp-level m16n8k8 TF32 products, each operand split into a TF32 high and low part
-// so that three products give fp32 accuracy).
+// initial state, chunk by chunk (C = 64), with every contraction on the tensor cores and
+// each operand split into a high and a low part, so that three products give fp32-level
+// accuracy: tcgen05 products of bf16 parts (accumulators in TMEM) for the state chains,
+// the value-side gradients and the preparation's K x K / K x V products when K = V = 128;
+// warp-level m16n8k8 products of TF32 parts for the rest and for other head sizes.
 //
 // The forward of a chunk (page "手撕KDA", section "1 Naive": the chunked form; gc the
 // cumulative sum of g inside the chunk, gl its last row, S the state entering it):
@@ -27,14 +29,16 @@
 // limit the forward kernels also have; e^{gc}, e^{gl - gc} never exceed 1.
 //
 // Five launches, each parallel over (chunk, value head) except the chains:
-//   prep_kernel     Q, R, B of every chunk, and W, U, Aqk^T do, T and kd ki^T for the
-//                   gradient kernels (workspace slot per (chunk, value head));
-//   chain_kernel    the states entering each chunk (h_{n+1} = Q_n h_n + R_n) and the
-//                   state gradients leaving it (dS_n = Q_n^T dS_{n+1} + B_n), one CTA per
-//                   64 value columns and direction (the columns are independent);
-//   grad_v_kernel   v_new, dv_new and the products with S and dS' (dv final);
-//   grad_cc_kernel  dA, dM and dbeta (C x C);
-//   grad_k_kernel   dq, dk, dg (per 64 key dims).
+//   prep_kernel       Q, R, B of every chunk, and W, U, Aqk^T do, T and kd ki^T for the
+//                     gradient kernels (workspace slot per (chunk, value head));
+//   chain_tc_kernel   the states entering each chunk (h_{n+1} = Q_n h_n + R_n) and the
+//   (chain_kernel)    state gradients leaving it (dS_n = Q_n^T dS_{n+1} + B_n), one CTA per
+//                     64 value columns and direction (the columns are independent);
+//   grad_v_tc_kernel  v_new, dv_new and the products with S and dS' (dv final);
+//   (grad_v_kernel)
+//   grad_cc_kernel    dA, dM and dbeta (C x C);
+//   grad_k_kernel     dq, dk, dg (per 64 key dims).
+// (the kernels in parentheses: K = 64 or V = 64)
 #include "kda_common.cuh"
 #include "sm103.cuh"
 
