@@ -161,3 +161,51 @@ def test_backward_headline_size_sampled_heads():
         mine = [got[0][:, :, sl], got[1][:, :, sl], got[2][:, :, sl], got[3][:, :, sl], got[4][:, :, sl],
                 got[5][:, sl]]
         _assert_grads(mine, ref, f"headline head {h}")
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_backward_large_workloads_sampled(idx, path):
+    """The larger benchmark workloads (B=4 T=16384; 16 packed sequences; GVA B=2 T=32768
+    H=8 HV=32) in one call each of the chunk form: status clean, every gradient finite,
+    and the last sequence's last value head equal to the oracle run on it alone (with
+    G = 1 every gradient; with G = 4, dq and dk sum four value heads, so dv, dg, dbeta
+    and the initial state's gradient).  The oracle's reverse mode takes ~12 s per 16 K
+    tokens on one core, which bounds the sample."""
+    if path == "recurrent":
+        pytest.skip("full-size sampling runs on the default (chunk) path")
+    x = W.workload_inputs(idx)
+    do, dfin = _grads_in(x, 10 + idx)
+    d = x.to("cuda")
+    shape = kda.make_shape(d.q, d.v, d.cu_seqlens)
+    ws = torch.empty(kda.kda_backward_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    got = kda.kda_backward(d.q, d.k, d.v, d.g, d.beta, do.to("cuda"), d.scale, initial_state=d.initial_state,
+                           cu_seqlens=d.cu_seqlens, d_final_state=dfin.to("cuda"), workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.kda_read_device_status(ws) == 0
+    for t in got:
+        assert bool(torch.isfinite(t).all())
+    got = [t.cpu() for t in got]
+    H, HV = x.q.shape[2], x.v.shape[2]
+    G = HV // H
+    s = x.num_seqs - 1
+    if x.cu_seqlens is None:
+        b, t0, L = s, 0, x.q.shape[1]
+    else:
+        cu = x.cu_seqlens.numpy()
+        b, t0, L = 0, int(cu[s]), int(cu[s + 1] - cu[s])
+    ts, bs = slice(t0, t0 + L), slice(b, b + 1)
+    hv = HV - 1
+    hk = hv // G
+    ref = oracle.backward(np32(x.q[bs, ts, hk:hk + 1]), np32(x.k[bs, ts, hk:hk + 1]), np32(x.v[bs, ts, hv:hv + 1]),
+                          np32(x.g[bs, ts, hv:hv + 1]), np32(x.beta[bs, ts, hv:hv + 1]), x.scale,
+                          np32(do[bs, ts, hv:hv + 1]), d_final_state=np32(dfin[s:s + 1, hv:hv + 1]),
+                          initial_state=np32(x.initial_state[s:s + 1, hv:hv + 1]))
+    mine = [got[0][bs, ts, hk:hk + 1].numpy(), got[1][bs, ts, hk:hk + 1].numpy(), got[2][bs, ts, hv:hv + 1].numpy(),
+            got[3][bs, ts, hv:hv + 1].numpy(), got[4][bs, ts, hv:hv + 1].numpy(), got[5][s:s + 1, hv:hv + 1].numpy()]
+    if G > 1:  # dq and dk of the key head sum all of its value heads
+        mine, ref = mine[2:], list(ref[2:])
+        for name, a, r in zip(("dv", "dg", "dbeta", "d_initial_state"), mine, ref):
+            err = np.abs(a - r).max() / max(np.abs(r).max(), 1e-30)
+            assert err <= TOL, f"workload {idx} {name}: error {err:.3e} > {TOL}"
+    else:
+        _assert_grads(mine, ref, f"workload {idx}, sequence {s}, value head {hv}")
