@@ -605,8 +605,8 @@ def run_twopass(args):
 
 
 BACKWARD_METRIC = ("KDA backward (gradients of q, k, v, g, beta and the initial state, chunk form with "
-                   "split-operand tensor-core products) tokens/s on 1 GB300 (T=4096, H=HV=32, K=V=128); "
-                   "% of the TF32 tensor peak")
+                   "split-operand tensor-core products) tokens/s on 1 GB300 (a workload; default T=4096, "
+                   "H=HV=32, K=V=128); % of the TF32 tensor peak")
 # nominal dense TF32 / bf16 tensor rates of the part (1.1 and 2.25 PFLOP/s): the TF32 peak
 # is the measured bf16 peak scaled by their ratio
 TF32_PER_BF16 = 1.1 / 2.25
@@ -629,8 +629,9 @@ def backward_flops(tokens_heads: int, K: int, V: int, C: int = 64) -> float:
 
 
 def run_backward(args):
-    """One step = one kda_backward call on the headline shape (bf16 q, k, v, d_out; fp32 g,
-    beta; a final-state gradient), L2 flushed between steps."""
+    """One step = one kda_backward call on a workload's inputs (default the headline shape;
+    io dtype q, k, v and a seeded output gradient; fp32 g, beta; a final-state gradient; the
+    workload's initial state), L2 flushed between steps."""
     import numpy as np
     import torch
     import kimi_delta_attention_gb300 as kda
@@ -638,21 +639,25 @@ def run_backward(args):
     kda.build()
     kda.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
-    B, T, H, HV, K, V = 1, 4096, 32, 32, 128, 128
-    host = W.make_inputs(B, T, H, HV, K, V, "bf16", seed=21, init_state=False)
+    w = W.WORKLOADS[args.workload]
+    host = W.workload_inputs(args.workload)
+    B, T, H, K = host.q.shape
+    HV, V = host.v.shape[2], host.v.shape[3]
+    NS = host.num_seqs
     rng = np.random.default_rng(22)
-    do_h = torch.from_numpy(rng.standard_normal((B, T, HV, V), dtype=np.float32)).to(torch.bfloat16)
-    dfin_h = torch.from_numpy(rng.standard_normal((B, HV, K, V), dtype=np.float32))
+    io = torch.bfloat16 if w.io_dtype == "bf16" else torch.float32
+    do_h = torch.from_numpy(rng.standard_normal(tuple(host.v.shape), dtype=np.float32)).to(io)
+    dfin_h = torch.from_numpy(rng.standard_normal((NS, HV, K, V), dtype=np.float32))
     x = host.to(dev)
     do, dfin = do_h.to(dev), dfin_h.to(dev)
-    shape = kda.make_shape(x.q, x.v)
+    shape = kda.make_shape(x.q, x.v, x.cu_seqlens)
     ws = torch.empty(kda.kda_backward_workspace_size(shape), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        return kda.kda_backward(x.q, x.k, x.v, x.g, x.beta, do, x.scale, d_final_state=dfin, workspace=ws,
-                                stream=stream.cuda_stream)
+        return kda.kda_backward(x.q, x.k, x.v, x.g, x.beta, do, x.scale, initial_state=x.initial_state,
+                                cu_seqlens=x.cu_seqlens, d_final_state=dfin, workspace=ws, stream=stream.cuda_stream)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -670,6 +675,7 @@ def run_backward(args):
     sampler.stop()
     ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
     tokens = B * T
+    wname = "backward_" + w.name
     flops = backward_flops(tokens * HV, K, V)
     achieved = flops / (ms * 1e-3) / 1e12
     _, bf16_tf, peak_src = load_peaks()
@@ -678,15 +684,15 @@ def run_backward(args):
         "impl": "kda_gb300", "metric": BACKWARD_METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s",
         "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "backward_bf16_T4096_H32_K128", "B": B, "T": T, "H": H, "HV": HV, "K": K, "V": V,
-                   "io": "bf16 q/k/v/d_out, fp32 g/beta/d_final_state; fp32 gradients",
+        "config": {"workload": wname, "B": B, "T": T, "H": H, "HV": HV, "K": K, "V": V, "num_seqs": NS,
+                   "io": f"{w.io_dtype} q/k/v/d_out, fp32 g/beta/d_final_state; fp32 gradients",
                    "products": ("each operand split into high and low parts, 3 products per product: tcgen05 bf16 "
                                 "for the state chains, the value-side gradients and prep's K x K / K x V products, "
                                 "warp-level TF32 for the rest"),
                    "l2": "flushed between timed steps"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                      "frac": achieved / tf32_peak, "kernel": f"the whole step ({BACKWARD_KERNELS})",
-                     "traffic": load_traffic("kda_backward_chunk", "backward_bf16_T4096_H32_K128"),
+                     "traffic": load_traffic("kda_backward_chunk", wname),
                      "flops_per_step": flops, "launches_per_step": BACKWARD_LAUNCHES,
                      "peak_source": (f"{peak_src} bf16 peak x {TF32_PER_BF16:.3f} (nominal dense TF32 / bf16)")},
         "clocks": sampler.summary(), "gpu_launches": args.steps * BACKWARD_LAUNCHES,
