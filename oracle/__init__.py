@@ -5,8 +5,9 @@ may import this package.  The product (the CUDA library and its Python binding)
 never imports, links or executes anything under ``oracle/``; the two share no
 code.
 
-The arithmetic lives in ``kda_oracle.c`` (plain C, double precision); this
-module only compiles it with gcc and marshals numpy arrays into it.
+The arithmetic lives in ``kda_oracle.c`` (plain C, double precision), which this
+module compiles with gcc and marshals numpy arrays into, and in ``backward_chunked.py``
+(plain numpy, double precision).
 
 Forms
 -----
@@ -20,6 +21,10 @@ Forms
 ``backward``: the gradients of sum <do, o> + <dS_final, S_final> with respect to
     q, k, v, g, beta and the initial state, by reverse mode through the token
     recurrence (the forward re-run with every state kept).
+``backward_chunked`` (``backward_chunked.py``, numpy): the same gradients by the chunk
+    form of page "手撕KDA", section "2 baseline" (per-chunk recompute, a reverse sweep
+    over the states, the VJP of the triangular inverse), every exponential of a
+    difference of cumulative decays; a second formulation, pinned against the first.
 ``prestage`` / ``forward_gated``: the activations applied to raw projections
     before the forward (q/k L2 normalisation with eps 1e-6, the bounded gate
     lower_bound * sigmoid(exp(A_log) (g_raw + dt_bias)) or the softplus gate
@@ -247,3 +252,6 @@ def backward(q, k, v, g, beta, scale, do, d_final_state=None, initial_state=None
             ds0[s, h] = ds_u
     r = lambda a: a.reshape((B, T) + a.shape[1:])
     return r(dq), r(dk), r(dv), r(dg), r(db), ds0
+
+
+from .backward_chunked import backward_chunked  # noqa: E402  (the chunk-form backward)

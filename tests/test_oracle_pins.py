@@ -368,3 +368,39 @@ def test_backward_of_an_empty_sequence_passes_the_state_gradient_through():
     dsf = np.arange(4, dtype=np.float32).reshape(1, 1, 2, 2)
     *_, ds0 = oracle.backward(q, k, v, g, b, 1.0, np.zeros(v.shape, np.float32), d_final_state=dsf, initial_state=s0)
     assert np.array_equal(ds0, dsf.astype(np.float64))
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 64])
+def test_chunk_form_backward_equals_reverse_mode(chunk):
+    """The oracle's two backward formulations -- reverse mode through the token
+    recurrence (pinned above by central differences) and the chunk form (per-chunk
+    recompute, a reverse sweep over the states, the triangular inverse's VJP) -- give the
+    same gradients: grouped value heads, an initial state, a final-state gradient, a
+    ragged last chunk, any chunk size."""
+    rng = np.random.default_rng(40 + chunk)
+    q, k, v, g, b, s0 = rand_inputs(rng, 2, 70, 2, 4, 8, 6, s0=True)
+    do = rng.standard_normal(v.shape).astype(np.float32)
+    dsf = rng.standard_normal(s0.shape).astype(np.float32)
+    ref = oracle.backward(q, k, v, g, b, 0.6, do, d_final_state=dsf, initial_state=s0)
+    got = oracle.backward_chunked(q, k, v, g, b, 0.6, do, d_final_state=dsf, initial_state=s0, chunk=chunk)
+    for name, a, r in zip(("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"), got, ref):
+        np.testing.assert_allclose(a, r, rtol=0, atol=1e-9 * np.abs(r).max(), err_msg=name)
+
+
+def test_chunk_form_backward_varlen_and_strong_decay():
+    """Packed sequences (an empty one, one shorter than a chunk, ragged ones) with the
+    bounded gate at its limit (g = -5 per token: the chunk's cumulative decay reaches
+    -320, beyond fp32's exponent range); the chunk form forms every exponent as a
+    difference, so both formulations still agree."""
+    rng = np.random.default_rng(47)
+    lens = [0, 5, 64, 65, 130]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, b, s0 = rand_inputs(rng, 1, int(cu[-1]), 1, 2, 8, 4, s0=True, n_seq=len(lens))
+    g = np.full_like(g, -5.0)
+    do = rng.standard_normal(v.shape).astype(np.float32)
+    dsf = rng.standard_normal(s0.shape).astype(np.float32)
+    ref = oracle.backward(q, k, v, g, b, 0.5, do, d_final_state=dsf, initial_state=s0, cu_seqlens=cu)
+    got = oracle.backward_chunked(q, k, v, g, b, 0.5, do, d_final_state=dsf, initial_state=s0, cu_seqlens=cu)
+    for name, a, r in zip(("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"), got, ref):
+        assert np.all(np.isfinite(a)), name
+        np.testing.assert_allclose(a, r, rtol=0, atol=1e-9 * np.abs(r).max(), err_msg=name)
