@@ -186,10 +186,13 @@ KDA_API kda_status kda_chunk_output(const kda_shape* shape, const void* q, const
  * page's sections 2 and 4: per 64-token chunk the forward's products are recomputed,
  * the states entering the chunks and the state gradients leaving them are carried by
  * two chains (S' = Q S + R forward, dS = Q^T dS' + B backward), and every chunk's
- * gradients follow in parallel.  Products on the tensor cores in TF32 with each operand
- * split into high and low parts (fp32 accuracy); five launches.  Blocks of 16 tokens
- * whose decay passes about -80 (natural log) per key dimension set status bit 4, as
- * the forward's chunk kernels do.
+ * gradients follow in parallel; five launches.  Every product splits each operand into
+ * high and low parts and sums three tensor-core products (fp32-level accuracy): tcgen05
+ * with bf16 parts for the two chains (K = 128), the value-side gradients and the
+ * K x K / K x V products (K = V = 128), warp-level TF32 products elsewhere.  Blocks of
+ * 16 tokens whose decay passes about -80 (natural log) per key dimension set status
+ * bit 4, as the forward's chunk kernels do; a wait on the kernels' own copies or
+ * products that passes the wait limit sets the timeout bit (the call still completes).
  *
  *   d_out          [B, T, HV, V]  io_dtype
  *   d_final_state  [NS, HV, K, V] fp32 or NULL (zeros)
